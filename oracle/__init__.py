@@ -1,0 +1,27 @@
+"""CPU oracle for the MHLA forward pass: test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
+reference legs may import this package.  The library never does.
+"""
+
+from .mhla_oracle import *  # noqa: F401,F403
+from .mhla_oracle import (  # noqa: F401
+    PHI_RELU,
+    PHI_RELU_EPS,
+    TRANSFORMS,
+    apply_transform,
+    block_centres,
+    block_distances,
+    block_of_token,
+    blocks_per_axis,
+    forward,
+    forward_dense,
+    forward_listing_normaliser,
+    linear_attention,
+    mix,
+    mixing_matrix,
+    num_blocks,
+    phi,
+    readout,
+    summaries,
+)
