@@ -1,0 +1,420 @@
+#!/usr/bin/env python3
+"""Throughput of the MHLA forward pass on GB300 (tokens/s and HBM roofline).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one MHLA forward (W to bf16, summaries, mixing GEMM, outputs) over
+one synthetic batch of the workload, inputs resident in HBM.  Rank 0 prints one
+JSON line.  With N > 1 (torchrun) every rank runs an independent batch on its own
+GPU (replicas, weak scaling); ranks meet only for the timing barrier and the
+max-over-ranks reduction.  ``--impl reference`` times the float64 CPU oracle on
+the host cores instead (rank 0 only), on bounded samples of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from token_level_head_block_gb300.workloads import HEADLINE, WORKLOADS  # noqa: E402
+
+METRIC = "MHLA forward tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- distributed harness
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x, device=None):
+    """Maximum of a float over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(units_per_rank, world, steps, max_elapsed_s):
+    """Units processed by all ranks divided by the slowest rank's time."""
+    return units_per_rank * world * steps / max_elapsed_s
+
+
+# ----------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms of the benchmark's GPU."""
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="mhla_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu=timestamp,{CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        return summarize_clocks(rows)
+
+
+def summarize_clocks(rows):
+    def num(x):
+        try:
+            return float(x)
+        except ValueError:
+            return None
+    sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+    smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+            "reasons": reasons, "samples": len(rows),
+            "power_w_max": max((num(r[3]) or 0.0) for r in rows) if rows else None}
+
+
+# ----------------------------------------------------------------- roofline inputs
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "token_level_head_block_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
+    if not m or not d or d.group(1) != kernel_source_digest():
+        return None
+    return int(m.group(1))
+
+
+def kernel_work(wl, name):
+    """(bound, algorithmic bytes or flops per launch) of each kernel of the path."""
+    io = wl.B * wl.N * wl.H * wl.d * wl.elem_bytes
+    BH, M, d = wl.B * wl.H, wl.M, wl.d
+    table = {
+        "tc_summary": ("hbm", 2 * io), "simt_summary": ("hbm", 2 * io),
+        "tc_output": ("hbm", 2 * io), "simt_output": ("hbm", 2 * io),
+        "tc_mix": ("tensor", 2 * M * M * BH * d * (d + 1)), "simt_mix": ("alu", 2 * M * M * BH * d * (d + 1)),
+        "convert_w": ("hbm", M * M * 6),
+    }
+    return table.get(name, ("hbm", 0))
+
+
+# ----------------------------------------------------------------- CPU oracle baseline
+
+def blas_threads():
+    import ctypes
+    try:
+        with open("/proc/self/maps") as f:
+            libs = sorted({line.split()[-1] for line in f if "openblas" in line.lower() and ".so" in line})
+    except OSError:
+        libs = []
+    for lib in libs:
+        try:
+            L = ctypes.CDLL(lib)
+        except OSError:
+            continue
+        for sym in ("openblas_get_num_threads", "openblas_get_num_threads64_",
+                    "scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads"):
+            fn = getattr(L, sym, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn())
+    return os.cpu_count() or 1
+
+
+def oracle_sample_rate(wl, q, k, v, W, budget_s, max_slices=None):
+    """Times the oracle on (b, h) slices until budget_s elapses (at least one slice).
+    Returns (tokens/s, slices, seconds); a slice of one head counts N / H tokens."""
+    import oracle
+    from token_level_head_block_gb300.synth import as_f64
+    phi = oracle.PHI_RELU if wl.phi == "relu" else oracle.PHI_RELU_EPS
+    pairs = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        b, h = pairs[done % len(pairs)]
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1), slice(None))
+        oracle.forward(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, wl.grid, wl.block, phi, wl.eps)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_slices and done >= max_slices):
+            break
+    return done * wl.N / wl.H / el, done, el
+
+
+# ----------------------------------------------------------------- arms
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+    import oracle
+    from token_level_head_block_gb300.synth import draw_workload
+    q, k, v = draw_workload(wl)
+    W = oracle.mixing_matrix(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
+    per_step = max(1, args.ref_slices)
+    for _ in range(args.warmup):
+        oracle_sample_rate(wl, q, k, v, W, 0.0, max_slices=1)
+    times = []
+    for _ in range(args.steps):
+        _, n, el = oracle_sample_rate(wl, q, k, v, W, 1e9, max_slices=per_step)
+        times.append(el)
+    total = sum(times)
+    value = args.steps * per_step * wl.N / wl.H / total
+    cores = blas_threads()
+    sample = (f"each step: {per_step} of the {wl.B * wl.H} (batch, head) slices of {wl.name}, "
+              f"float64 numpy oracle (blocked form); a slice counts N/H tokens")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {**wl.describe(), "parallelism": "host cores (BLAS threads)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_ours(args, wl):
+    import torch
+    import token_level_head_block_gb300 as mhla
+    from token_level_head_block_gb300.synth import draw_workload
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init("nccl")
+    mhla.lib()
+
+    q_h, k_h, v_h = draw_workload(wl, seed=wl.seed + rank)      # each replica its own batch
+    W_h = mhla.init_mixing(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    W = torch.from_numpy(W_h).to(dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(mhla.workspace_size(q, wl.grid, wl.block), dtype=torch.uint8, device=dev)
+    path = mhla.select_path(q, k, v, out, wl.grid, wl.block)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        mhla.forward(q, k, v, W, wl.grid, wl.block, phi=wl.phi, eps=wl.eps, out=out, workspace=ws, stream=stream)
+
+    def timed(n, body):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dev)
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for _ in range(n):
+            body()
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dev)
+        return start.elapsed_time(end) / 1e3
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if mhla.device_status() != 0:
+        raise SystemExit("device wait flag set during warm-up")
+
+    gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gpu_uuid)
+    sampler.start()
+    t_end = time.time() + args.sustain
+    while time.time() < t_end:             # sustained load so the clock samples mean something
+        for _ in range(50):
+            step()
+        torch.cuda.synchronize(dev)
+    el_main = timed(args.steps, step)                       # pass A: the headline number
+    mhla.profile_begin()
+    el_prof = timed(args.steps, step)                       # pass B: per-kernel attribution
+    prof = mhla.profile_end()
+    clocks = sampler.stop()
+    if mhla.device_status() != 0:
+        raise SystemExit("device wait flag set during the timed region")
+
+    max_el = max_over_ranks(el_main, dev)
+    value = whole_job_throughput(wl.tokens, world, args.steps, max_el)
+    ms_per_step = 1e3 * max_el / args.steps
+
+    # e2e: host buffers in pinned memory, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.pin_memory() for t in (q_h, k_h, v_h))
+        ho = torch.empty_like(q_h).pin_memory()
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            step()
+            ho.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        n_e2e = max(3, min(args.steps, 50))
+        el_e2e = max_over_ranks(timed(n_e2e, e2e_step), dev)
+        io = wl.B * wl.N * wl.H * wl.d * wl.elem_bytes
+        e2e = {"value": whole_job_throughput(wl.tokens, world, n_e2e, el_e2e), "unit": UNIT,
+               "h2d_bytes_per_step": 3 * io, "d2h_bytes_per_step": io, "steps": n_e2e,
+               "ms_per_step": 1e3 * el_e2e / n_e2e}
+
+    # roofline of the dominant kernel, from the per-kernel events of pass B
+    peaks, peak_src = load_peaks()
+    kern = {name: {"launches": n, "avg_us": 1e3 * ms / n, "share": 0.0} for name, (n, ms) in prof.items()}
+    total_ms = sum(ms for _, ms in prof.values()) or 1.0
+    for name, (_, ms) in prof.items():
+        kern[name]["share"] = ms / total_ms
+    dominant = max(prof, key=lambda n: prof[n][1])
+    bound, work = kernel_work(wl, dominant)
+    avg_s = prof[dominant][1] / 1e3 / prof[dominant][0]
+    if bound == "hbm":
+        achieved, peak, unit = work / avg_s / 1e9, float(peaks["hbm_gbs"]), "GB/s"
+    else:
+        achieved = work / avg_s / 1e12
+        peak, unit = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])), "TFLOP/s"
+    traffic = profiled_traffic(dominant, wl.name)
+    roofline = {"kernel": dominant, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": traffic, "algorithmic_per_launch": work,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"}
+    fwd_gbs = wl.algorithmic_bytes / (max_el / args.steps) / 1e9
+    forward_roofline = {"bound": "hbm", "achieved": fwd_gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                        "frac": fwd_gbs / float(peaks["hbm_gbs"]), "bytes_per_step": wl.algorithmic_bytes}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, n, el = oracle_sample_rate(wl, q_h, k_h, v_h, W_h, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n} of the {wl.B * wl.H} (batch, head) slices of {wl.name} in {el:.1f} s, "
+                         "float64 numpy oracle (blocked form); a slice counts N/H tokens"}
+
+    launches = sum(n for n, _ in prof.values())
+    if rank == 0:
+        line = {
+            "impl": "ours", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic",
+            "config": {**wl.describe(), "path": path, "global_batch": wl.B * world, "seq_len": wl.N,
+                       "parallelism": f"replicas x{world} (independent batches, no collective)",
+                       "l2": f"inputs {3 * wl.algorithmic_bytes // 4 / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB "
+                             "each step (no flush)",
+                       "clock_window": f"{args.sustain:.1f} s sustained run of the same step, then both timed passes"},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
+            "roofline": roofline, "forward_roofline": forward_roofline,
+            "kernels": kern, "profiled_pass_ms_per_step": 1e3 * el_prof / args.steps,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--sustain", type=float, default=2.0, help="seconds of load before timing (clock samples)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU oracle baseline")
+    ap.add_argument("--ref-slices", type=int, default=1, help="(batch, head) slices per reference step")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)      # at least three untimed warm-up steps
+    wl = WORKLOADS[args.workload]
+    _, world, _ = dist_env()
+    if world != args.gpus and world > 1:
+        print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * mhla.h -- C ABI of the MHLA forward pass (Multi-Head Linear Attention with the
+ * heads taken along the token dimension) for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operation (web pages, cited by title and section):
+ *   [P1] "MHLA：通过令牌级多头机制恢复线性注意力机制的表达能力" module walkthrough,
+ *        171host.com/767426.html, section 5 (principle) and section 7 (the
+ *        plug-and-play BlockDistanceConv / MHLA PyTorch module).
+ *   [P2] "MHLA: Restoring Expressivity of Linear Attention via Token-Level
+ *        Multi-Head", paperlayer.ai summary of arXiv 2601.07832v2, sections 3-4.
+ *
+ * What one forward computes, per batch b and head h (notation of [P2] section 4):
+ *   1. split the N tokens of a 2-D (Y, X) or 3-D (T, Y, X) grid into M
+ *      non-overlapping blocks and form every block's summary
+ *        S_j = sum_{s in j} phi(k_s) v_s^T   (d x d),   z_j = sum_{s in j} phi(k_s);
+ *   2. mix the summaries per query block with the M x M matrix W
+ *        S~_i = sum_j W[i][j] S_j,   z~_i = sum_j W[i][j] z_j;
+ *   3. read out every token t of query block i
+ *        o_t = phi(q_t)^T S~_i / (phi(q_t) . z~_i + eps).
+ *   phi is ReLU ([P1] section 7, MHLA._process_qkv_impl), optionally ReLU + eps.
+ *
+ * Conventions shared by every call:
+ *   - Tensors q, k, v, out are [B, N, H, d] with d contiguous (stride 1) and
+ *     the N tokens in raster order over the grid (last grid axis fastest).
+ *     Strides are in ELEMENTS.  Pointers are borrowed, never freed or kept.
+ *   - Block ids are row-major over the block grid, slowest axis first; W is
+ *     row-major float32, W[i * M + j], i = query (output) block, j = source
+ *     block -- the weight[out][in] of the 1x1 convolution in [P1] section 7.
+ *   - Nothing throws across the ABI; every call returns an mhla_status_t.
+ *     Validation happens before any GPU work is queued.
+ */
+#ifndef MHLA_H
+#define MHLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mhla_status {
+    MHLA_OK = 0,
+    MHLA_ERR_INVALID_ARG = 1,  /* null pointer, bad enum, negative or inconsistent size */
+    MHLA_ERR_SHAPE = 2,        /* grid does not match N, block does not tile grid, ... */
+    MHLA_ERR_UNSUPPORTED = 3,  /* valid request the selected path cannot run */
+    MHLA_ERR_CUDA = 4,         /* a CUDA runtime call or a launch failed */
+    MHLA_ERR_TIMEOUT = 5,      /* a device-side wait gave up (see mhla_device_status) */
+    MHLA_ERR_WORKSPACE = 6     /* workspace missing, too small or misaligned */
+} mhla_status_t;
+
+typedef enum mhla_dtype { MHLA_BF16 = 0, MHLA_F32 = 1 } mhla_dtype_t;
+
+/* Distance -> weight transforms of [P1] section 7, BlockDistanceConv._apply_transform. */
+typedef enum mhla_transform {
+    MHLA_TRANSFORM_LINEAR = 0,    /* 1 - D / max D                         */
+    MHLA_TRANSFORM_COS = 1,       /* cos(D / max D * pi / 4)               */
+    MHLA_TRANSFORM_EXP = 2,       /* exp(-D / exp_sigma)                   */
+    MHLA_TRANSFORM_GAUSSIAN = 3,  /* exp(-D^2 / (2 s^2)), s = max D / 3    */
+    MHLA_TRANSFORM_LOCAL = 4      /* 1 if D <= local_thres else 0          */
+} mhla_transform_t;
+
+typedef enum mhla_phi_kind {
+    MHLA_PHI_RELU = 0,      /* phi(x) = max(x, 0)                               */
+    MHLA_PHI_RELU_EPS = 1   /* phi(x) = max(x, 0) + eps, as the [P1] module does */
+} mhla_phi_kind_t;
+
+/* Which kernels run.  AUTO picks the tensor-core path whenever the request is
+ * eligible for it (bf16, d in {32, 64}, tokens per block a multiple of 128, TMA
+ * friendly strides) and the CUDA-core path otherwise. */
+typedef enum mhla_path { MHLA_PATH_AUTO = 0, MHLA_PATH_SIMT = 1, MHLA_PATH_TC = 2 } mhla_path_t;
+
+/* Token grid or block shape, slowest axis first: (Y, X) when ndim == 2,
+ * (T, Y, X) when ndim == 3.  Unused extents are ignored. */
+typedef struct mhla_shape3 {
+    int32_t ndim;
+    int32_t pad_;
+    int64_t extent[3];
+} mhla_shape3_t;
+
+typedef struct mhla_phi {
+    int32_t kind;   /* mhla_phi_kind_t */
+    float eps;      /* added to the denominator; also to phi under MHLA_PHI_RELU_EPS */
+} mhla_phi_t;
+
+/* A [B, N, H, d] tensor.  data is device memory for mhla_forward. */
+typedef struct mhla_tensor {
+    void* data;
+    int32_t dtype;  /* mhla_dtype_t */
+    int32_t pad_;
+    int64_t B, N, H, d;
+    int64_t stride_b, stride_n, stride_h;   /* elements; d has stride 1 */
+} mhla_tensor_t;
+
+/* Number of token blocks M for a grid and block shape, or -MHLA_ERR_SHAPE /
+ * -MHLA_ERR_INVALID_ARG when the block does not tile the grid. */
+int64_t mhla_num_blocks(const mhla_shape3_t* grid, const mhla_shape3_t* block);
+
+/* Builds the M x M mixing matrix from block-centre distances: centres at
+ * (index + 0.5) per axis in block units, Euclidean distance, the transform,
+ * then every column divided by its sum ([P1] section 7,
+ * BlockDistanceConv._compute_block_distances and _apply_transform; [P2]
+ * section 5 "locality-biased initialization").  Computed in double and rounded
+ * once to float32; a single block gives W = [[1]].
+ *   W_host      host memory the caller owns, room for W_capacity floats;
+ *               receives W[i * M + j].
+ * Returns MHLA_ERR_INVALID_ARG for a null pointer, unknown transform, a
+ * non-positive exp_sigma or W_capacity < M * M; MHLA_ERR_SHAPE when the block
+ * does not tile the grid.  Host only; touches no GPU. */
+mhla_status_t mhla_init_mixing(const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                               int32_t transform, double local_thres, double exp_sigma,
+                               float* W_host, int64_t W_capacity);
+
+/* Device workspace mhla_forward needs for this problem and path (bytes, a
+ * multiple of 256).  q gives B, N, H, d and the dtype.  Host only. */
+mhla_status_t mhla_workspace_size(const mhla_tensor_t* q, const mhla_shape3_t* grid,
+                                  const mhla_shape3_t* block, int32_t path, size_t* bytes);
+
+/* The path AUTO would take for this problem (MHLA_PATH_SIMT or MHLA_PATH_TC),
+ * or a negative status when the problem is invalid.  Host only. */
+int32_t mhla_select_path(const mhla_tensor_t* q, const mhla_tensor_t* k,
+                         const mhla_tensor_t* v, const mhla_tensor_t* out,
+                         const mhla_shape3_t* grid, const mhla_shape3_t* block);
+
+/* The MHLA forward pass ([P2] section 4 "Architecture", "Multi-Head Mixing",
+ * "Token-Level Adaptivity"; [P1] section 7, MHLA.forward with the normaliser
+ * read as phi(q_t) . z~_i + eps).
+ *   q, k, v     device tensors [B, N, H, d], all the same shape and dtype.
+ *   W           device float32, M x M row-major, shared by every batch and head.
+ *   grid, block token grid and block shape; prod(grid) == N, block tiles grid.
+ *   phi         feature map and eps (eps >= 0, finite).
+ *   out         device tensor, same shape and dtype as q; must not overlap
+ *               q, k, v or W.  Written in the input dtype (round to nearest even).
+ *   workspace   device memory of at least mhla_workspace_size() bytes, 256-byte
+ *               aligned, owned by the caller and not used by anything else
+ *               until the work queued on stream has finished.  Passing NULL
+ *               with workspace_bytes == 0 makes the call take it with
+ *               cudaMallocAsync / cudaFreeAsync on the stream.
+ *   stream      cudaStream_t (NULL = legacy default stream).
+ *   path        mhla_path_t; AUTO unless a test wants one path.
+ * Asynchronous: queues kernels on stream and returns; never synchronises.
+ * Returns MHLA_ERR_INVALID_ARG / SHAPE / WORKSPACE before queuing anything
+ * when the request is malformed, MHLA_ERR_UNSUPPORTED when an explicit path
+ * cannot take it, MHLA_ERR_CUDA when a launch fails.  A device-side wait that
+ * gives up is reported later by mhla_device_status.
+ * B == 0 or H == 0 is a valid empty call that queues nothing. */
+mhla_status_t mhla_forward(const mhla_tensor_t* q, const mhla_tensor_t* k,
+                           const mhla_tensor_t* v, const float* W,
+                           const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                           const mhla_phi_t* phi, const mhla_tensor_t* out,
+                           void* workspace, size_t workspace_bytes, void* stream,
+                           int32_t path);
+
+/* Reads and clears the device error word the tensor-core kernels set when one
+ * of their bounded waits gives up (bit 0: pipeline wait timeout).  Synchronises
+ * stream.  *flags receives the word; returns MHLA_ERR_TIMEOUT when it was
+ * non-zero, MHLA_ERR_CUDA when the copy failed. */
+mhla_status_t mhla_device_status(void* stream, uint32_t* flags);
+
+/* Per-kernel timing.  Between mhla_profile_begin and mhla_profile_end every
+ * kernel the library launches is bracketed by a pair of CUDA events recorded on
+ * its launch stream.  mhla_profile_end waits for those events, writes one entry
+ * per kernel name (launch count and summed duration in milliseconds) into out
+ * (room for capacity entries; *count receives the number of names) and stops
+ * collecting.  Host only apart from the event records; thread safe. */
+typedef struct mhla_kernel_time {
+    char name[32];
+    int32_t launches;
+    float total_ms;
+} mhla_kernel_time_t;
+
+mhla_status_t mhla_profile_begin(void);
+mhla_status_t mhla_profile_end(mhla_kernel_time_t* out, int32_t capacity, int32_t* count);
+
+/* Static description of a status code (never NULL). */
+const char* mhla_status_string(int32_t status);
+
+/* Library version, e.g. "mhla-gb300 0.1.0 sm_103a". */
+const char* mhla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHLA_H */

@@ -146,7 +146,7 @@ def apply_transform(D, transform, local_thres=1.5, exp_sigma=3.0):
         mat = _libm(math.exp, -D / float(exp_sigma))
     elif transform == "gaussian":
         sigma = D.max() / 3
-        mat = _libm(math.exp, -(D ** 2) / (2 * sigma ** 2))
+        mat = _libm(math.exp, -(D * D) / (2 * sigma * sigma))
     else:
         mat = (D <= float(local_thres)).astype(np.float64)
     col = np.zeros(M)

@@ -1,0 +1,198 @@
+"""Host-side checks of the C ABI: no GPU needed, no kernel is launched.
+
+The library must load and export every function include/mhla.h declares; the
+host W builder must reproduce the oracle's W bit for bit; every malformed request
+must be rejected with its documented status before any GPU work is queued.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import token_level_head_block_gb300 as mhla
+from tests.golden.write_golden import CASES, case_name, load
+from token_level_head_block_gb300.workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mhla.h")
+
+OK, INVALID, SHAPE, UNSUPPORTED, CUDA, TIMEOUT, WORKSPACE = range(7)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mhla_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    return mhla.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert {"mhla_forward", "mhla_init_mixing", "mhla_workspace_size"} <= set(names)
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(L):
+    assert b"sm_103a" in L.mhla_version()
+    for code in range(7):
+        assert L.mhla_status_string(code).decode() == mhla.STATUS[code]
+    assert L.mhla_status_string(99) == b"unknown status"
+
+
+@pytest.mark.parametrize("case", CASES, ids=[case_name(*c) for c in CASES])
+def test_init_mixing_matches_stored_fixture_bitwise(case):
+    W = mhla.init_mixing(case[0], case[1], case[2], local_thres=case[3], exp_sigma=case[4])
+    assert np.array_equal(W.view(np.uint32), load()[case_name(*case)].view(np.uint32))
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_init_mixing_matches_oracle_bitwise_on_workloads(name):
+    wl = WORKLOADS[name]
+    if wl.M > 300:
+        pytest.skip("python-loop oracle W is slow at this M; covered on the GPU box")
+    W = mhla.init_mixing(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
+    ref = oracle.mixing_matrix(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
+    assert np.array_equal(W.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("transform", list(mhla.TRANSFORMS))
+def test_init_mixing_rectangular_and_single_block(transform):
+    W = mhla.init_mixing((12, 20), (4, 4), transform, 1.5, 2.5)
+    ref = oracle.mixing_matrix((12, 20), (4, 4), transform, 1.5, 2.5)
+    assert np.array_equal(W.view(np.uint32), ref.view(np.uint32))
+    assert mhla.init_mixing((8, 8), (8, 8), transform).tolist() == [[1.0]]
+
+
+def test_num_blocks_and_bad_shapes(L):
+    assert mhla.num_blocks((256, 256), (16, 16)) == 256
+    assert mhla.num_blocks((20, 32, 32), (4, 8, 8)) == 80
+    for g, b in [((14, 14), (4, 4)), ((16, 16), (4, 4, 1)), ((0, 4), (1, 1))]:
+        with pytest.raises(mhla.MhlaError) as e:
+            mhla.num_blocks(g, b)
+        assert e.value.status == SHAPE
+
+
+def test_init_mixing_rejects_bad_arguments(L):
+    g, b = mhla.shape3((8, 8)), mhla.shape3((4, 4))
+    buf = (ctypes.c_float * 16)()      # M = 4 blocks -> 16 entries
+    call = lambda t, lt, s, cap, p=buf: L.mhla_init_mixing(ctypes.byref(g), ctypes.byref(b), t, lt, s, p, cap)
+    assert call(0, 1.5, 3.0, 16) == OK
+    assert call(5, 1.5, 3.0, 16) == INVALID         # unknown transform
+    assert call(2, 1.5, 0.0, 16) == INVALID         # exp with sigma 0
+    assert call(4, -1.0, 3.0, 16) == INVALID        # local with negative threshold
+    assert call(0, 1.5, 3.0, 15) == INVALID         # W too small
+    assert call(0, 1.5, 3.0, 16, None) == INVALID   # null W
+
+
+# ------------------------------------------------------------ forward validation
+
+FAKE = 1 << 40          # a 256-byte aligned address that is never dereferenced here
+
+
+def contig(B, N, H, d, dtype="bf16", base=FAKE):
+    return mhla.tensor_desc(base, dtype, (B, N, H, d), (N * H * d, H * d, d))
+
+
+def call_forward(L, q, k, v, o, grid, block, W=FAKE + (1 << 36), phi=(0, 1e-6), ws=None, ws_bytes=0, path=0):
+    return L.mhla_forward(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.c_void_p(W),
+                          ctypes.byref(mhla.shape3(grid)), ctypes.byref(mhla.shape3(block)),
+                          ctypes.byref(mhla.Phi(*phi)), ctypes.byref(o),
+                          ctypes.c_void_p(ws) if ws else None, ws_bytes, None, path)
+
+
+def four(B, N, H, d, dtype="bf16"):
+    span = B * N * H * d * 4 + 4096
+    return [contig(B, N, H, d, dtype, FAKE + i * span) for i in range(4)]
+
+
+def test_forward_rejects_malformed_requests_before_any_launch(L):
+    q, k, v, o = four(2, 256, 3, 64)
+    grid, block = (16, 16), (4, 4)
+    assert call_forward(L, q, k, v, o, (16, 15), block) == SHAPE           # grid product != N
+    assert call_forward(L, q, k, v, o, grid, (5, 4)) == SHAPE              # block does not tile
+    assert call_forward(L, q, k, v, o, grid, (4, 4, 4)) == SHAPE           # ndim mismatch
+    k2 = contig(2, 256, 3, 32, base=k.data)
+    assert call_forward(L, q, k2, v, o, grid, block) == SHAPE              # d differs
+    v2 = contig(2, 256, 3, 64, "f32", base=v.data)
+    assert call_forward(L, q, k, v2, o, grid, block) == SHAPE              # dtype differs
+    assert call_forward(L, q, k, v, q, grid, block) == INVALID             # out aliases q
+    assert call_forward(L, q, k, v, o, grid, block, W=0) == INVALID        # null W
+    assert call_forward(L, q, k, v, o, grid, block, W=o.data + 64) == INVALID   # W inside out
+    assert call_forward(L, q, k, v, o, grid, block, phi=(7, 1e-6)) == INVALID   # unknown phi
+    assert call_forward(L, q, k, v, o, grid, block, phi=(0, -1.0)) == INVALID   # negative eps
+    assert call_forward(L, q, k, v, o, grid, block, phi=(0, float("inf"))) == INVALID
+    bad = contig(2, 256, 3, 200, base=q.data)
+    assert call_forward(L, bad, bad, bad, contig(2, 256, 3, 200, base=o.data), grid, block) == INVALID
+    o_overlap = mhla.tensor_desc(o.data, "bf16", (2, 256, 3, 64), (256 * 3 * 64, 3 * 64, 32))
+    assert call_forward(L, q, k, v, o_overlap, grid, block) == INVALID    # heads overlap in out
+    assert call_forward(L, q, k, v, o, grid, block, ws=FAKE + 7, ws_bytes=1 << 30) == WORKSPACE  # misaligned
+    assert call_forward(L, q, k, v, o, grid, block, ws=FAKE, ws_bytes=16) == WORKSPACE          # too small
+    assert call_forward(L, q, k, v, o, grid, block, ws=None, ws_bytes=16) == WORKSPACE          # bytes w/o pointer
+    assert call_forward(L, q, k, v, o, grid, block, path=9) == INVALID                          # unknown path
+
+
+def test_forward_explicit_tensor_core_path_refuses_ineligible_problems(L):
+    q, k, v, o = four(1, 196, 3, 64)                                # 2x2 blocks: 4 tokens per block
+    assert call_forward(L, q, k, v, o, (14, 14), (2, 2), path=2) == UNSUPPORTED
+    q, k, v, o = four(1, 256, 1, 32, "f32")                         # fp32 runs on CUDA cores only
+    assert call_forward(L, q, k, v, o, (16, 16), (16, 16), path=2) == UNSUPPORTED
+
+
+def test_empty_batch_is_a_no_op(L):
+    q, k, v, o = four(0, 256, 3, 64)
+    assert call_forward(L, q, k, v, o, (16, 16), (4, 4)) == OK
+    q, k, v, o = four(2, 256, 0, 64)
+    assert call_forward(L, q, k, v, o, (16, 16), (4, 4)) == OK
+
+
+def select(L, q, grid, block, strides=None):
+    ts = four(q[0], q[1], q[2], q[3], q[4] if len(q) > 4 else "bf16")
+    if strides:
+        ts = [mhla.tensor_desc(t.data, t.dtype, (t.B, t.N, t.H, t.d), strides) for t in ts]
+    return L.mhla_select_path(*(ctypes.byref(t) for t in ts), ctypes.byref(mhla.shape3(grid)),
+                              ctypes.byref(mhla.shape3(block)))
+
+
+def test_path_selection(L):
+    TC, SIMT = 2, 1
+    for name in ("dit_s2_4096px", "sana_4096px", "video_20x32x32", "sweep_64x64", "sweep_512x512"):
+        wl = WORKLOADS[name]
+        assert select(L, (wl.B, wl.N, wl.H, wl.d), wl.grid, wl.block) == TC, name
+    wl = WORKLOADS["deit_t_14x14"]
+    assert select(L, (wl.B, wl.N, wl.H, wl.d), wl.grid, wl.block) == SIMT
+    wl = WORKLOADS["tiny_16x16_fp32"]
+    assert select(L, (wl.B, wl.N, wl.H, wl.d, "f32"), wl.grid, wl.block) == SIMT
+    # d = 48 has no tensor-core kernel; 64-token blocks cannot fill a 128-row tile.
+    assert select(L, (1, 256, 2, 48), (16, 16), (16, 16)) == SIMT
+    assert select(L, (1, 256, 2, 64), (16, 16), (8, 8)) == SIMT
+    # strides that break TMA's 16-byte rule fall back to CUDA cores
+    assert select(L, (1, 256, 2, 64), (16, 16), (16, 16), strides=(256 * 2 * 68, 2 * 68, 68)) == SIMT
+    # q, k, v taken as slices of one [B, N, 3, H, d] projection still qualify
+    st = (256 * 3 * 2 * 64, 3 * 2 * 64, 64)
+    q, k, v = (mhla.tensor_desc(FAKE + 2 * i * 2 * 64, "bf16", (2, 256, 2, 64), st) for i in range(3))
+    o = contig(2, 256, 2, 64, base=FAKE + (1 << 30))
+    assert L.mhla_select_path(*(ctypes.byref(t) for t in (q, k, v, o)), ctypes.byref(mhla.shape3((16, 16))),
+                              ctypes.byref(mhla.shape3((16, 16)))) == TC
+
+
+def test_workspace_sizes(L):
+    wl = WORKLOADS["dit_s2_4096px"]
+    q = contig(wl.B, wl.N, wl.H, wl.d)
+    M, BH, d = wl.M, wl.B * wl.H, wl.d
+    n = ctypes.c_size_t()
+    assert L.mhla_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
+                                 ctypes.byref(mhla.shape3(wl.block)), 2, ctypes.byref(n)) == OK
+    expect = M * M * 2 + M * BH * (d + 1) * d * 2 + BH * M * d * d * 2 + BH * M * d * 4
+    assert expect <= n.value < expect + 4 * 256 and n.value % 256 == 0
+    assert L.mhla_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
+                                 ctypes.byref(mhla.shape3(wl.block)), 1, ctypes.byref(n)) == OK
+    assert n.value >= 2 * BH * M * d * (d + 1) * 4

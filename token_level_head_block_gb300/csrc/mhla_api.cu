@@ -1,0 +1,207 @@
+// extern "C" entry points of libmhla: argument validation, problem
+// construction, path selection and workspace handling.  Every check runs on the
+// host before anything is queued on the stream.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+
+#include "mhla_internal.h"
+
+namespace mhla {
+namespace {
+
+int64_t elem_bytes(int dtype) { return dtype == MHLA_BF16 ? 2 : 4; }
+
+bool valid_dtype(int dtype) { return dtype == MHLA_BF16 || dtype == MHLA_F32; }
+
+// Byte span [lo, hi) a [B, N, H, d] tensor can touch.
+void span(const mhla_tensor_t* t, uintptr_t* lo, uintptr_t* hi) {
+  const int64_t e = elem_bytes(t->dtype);
+  const int64_t last = (t->B - 1) * t->stride_b + (t->N - 1) * t->stride_n + (t->H - 1) * t->stride_h + t->d;
+  *lo = reinterpret_cast<uintptr_t>(t->data);
+  *hi = *lo + static_cast<uintptr_t>(last * e);
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+// No two (b, n, h, c) index tuples of an output may share an address: sort the
+// three outer dimensions by stride and require each stride to clear the extent
+// of everything inside it.
+bool non_overlapping(const mhla_tensor_t* t) {
+  struct Dim { int64_t stride, extent; } dims[3] = {
+      {t->stride_b, t->B}, {t->stride_n, t->N}, {t->stride_h, t->H}};
+  std::sort(dims, dims + 3, [](const Dim& a, const Dim& b) { return a.stride < b.stride; });
+  int64_t inner = t->d;   // elements spanned so far
+  for (const Dim& dm : dims) {
+    if (dm.extent <= 1) continue;
+    if (dm.stride < inner) return false;
+    inner = dm.stride * (dm.extent - 1) + inner;
+  }
+  return true;
+}
+
+int check_tensor(const mhla_tensor_t* t) {
+  if (!t) return MHLA_ERR_INVALID_ARG;
+  if (!valid_dtype(t->dtype)) return MHLA_ERR_INVALID_ARG;
+  if (t->B < 0 || t->N < 1 || t->H < 0 || t->d < 1 || t->d > 128) return MHLA_ERR_INVALID_ARG;
+  if (t->stride_b < 0 || t->stride_n < 0 || t->stride_h < 0) return MHLA_ERR_INVALID_ARG;
+  if (t->B > 0 && t->H > 0 && !t->data) return MHLA_ERR_INVALID_ARG;
+  return MHLA_OK;
+}
+
+bool same_shape(const mhla_tensor_t* a, const mhla_tensor_t* b) {
+  return a->B == b->B && a->N == b->N && a->H == b->H && a->d == b->d && a->dtype == b->dtype;
+}
+
+int build_problem(const mhla_tensor_t* q, const mhla_tensor_t* k, const mhla_tensor_t* v,
+                  const mhla_tensor_t* o, const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                  const mhla_phi_t* phi, bool check_alias, Problem* p) {
+  for (const mhla_tensor_t* t : {q, k, v, o}) {
+    const int rc = check_tensor(t);
+    if (rc != MHLA_OK) return rc;
+  }
+  if (!same_shape(q, k) || !same_shape(q, v) || !same_shape(q, o)) return MHLA_ERR_SHAPE;
+  if (!grid || !block) return MHLA_ERR_INVALID_ARG;
+  const int64_t M = mhla_num_blocks(grid, block);
+  if (M < 0) return static_cast<int>(-M);
+  int64_t n_grid = 1;
+  for (int a = 0; a < grid->ndim; ++a) n_grid *= grid->extent[a];
+  if (n_grid != q->N) return MHLA_ERR_SHAPE;
+  if (phi) {
+    if (phi->kind != MHLA_PHI_RELU && phi->kind != MHLA_PHI_RELU_EPS) return MHLA_ERR_INVALID_ARG;
+    if (!(phi->eps >= 0.0f) || !std::isfinite(phi->eps)) return MHLA_ERR_INVALID_ARG;
+  }
+  Problem& P = *p;
+  P.B = q->B; P.N = q->N; P.H = q->H; P.d = q->d; P.dtype = q->dtype;
+  P.ndim = grid->ndim;
+  if (grid->ndim == 2) {
+    P.T = 1; P.Y = grid->extent[0]; P.X = grid->extent[1];
+    P.bt = 1; P.by = block->extent[0]; P.bx = block->extent[1];
+  } else {
+    P.T = grid->extent[0]; P.Y = grid->extent[1]; P.X = grid->extent[2];
+    P.bt = block->extent[0]; P.by = block->extent[1]; P.bx = block->extent[2];
+  }
+  P.nbt = P.T / P.bt; P.nby = P.Y / P.by; P.nbx = P.X / P.bx;
+  P.M = M; P.w = P.N / M;
+  P.phi_kind = phi ? phi->kind : MHLA_PHI_RELU;
+  P.eps = phi ? phi->eps : 1e-6f;
+  P.q = Operand{q->data, q->stride_b, q->stride_n, q->stride_h};
+  P.k = Operand{k->data, k->stride_b, k->stride_n, k->stride_h};
+  P.v = Operand{v->data, v->stride_b, v->stride_n, v->stride_h};
+  P.o = Operand{o->data, o->stride_b, o->stride_n, o->stride_h};
+  if (check_alias && P.B > 0 && P.H > 0) {
+    if (!non_overlapping(o)) return MHLA_ERR_INVALID_ARG;
+    uintptr_t o0, o1;
+    span(o, &o0, &o1);
+    for (const mhla_tensor_t* t : {q, k, v}) {
+      uintptr_t t0, t1;
+      span(t, &t0, &t1);
+      if (overlaps(o0, o1, t0, t1)) return MHLA_ERR_INVALID_ARG;
+    }
+  }
+  return MHLA_OK;
+}
+
+int resolve_path(const Problem& p, int32_t path, int* sel) {
+  if (path == MHLA_PATH_AUTO) {
+    *sel = tc_eligible(p) ? MHLA_PATH_TC : MHLA_PATH_SIMT;
+    return MHLA_OK;
+  }
+  if (path == MHLA_PATH_SIMT) { *sel = MHLA_PATH_SIMT; return MHLA_OK; }
+  if (path == MHLA_PATH_TC) {
+    if (!tc_eligible(p)) return MHLA_ERR_UNSUPPORTED;
+    *sel = MHLA_PATH_TC;
+    return MHLA_OK;
+  }
+  return MHLA_ERR_INVALID_ARG;
+}
+
+size_t workspace_for(const Problem& p, int sel) {
+  return sel == MHLA_PATH_TC ? tc_workspace_bytes(p) : simt_workspace_bytes(p);
+}
+
+}  // namespace
+}  // namespace mhla
+
+using namespace mhla;
+
+extern "C" mhla_status_t mhla_workspace_size(const mhla_tensor_t* q, const mhla_shape3_t* grid,
+                                             const mhla_shape3_t* block, int32_t path, size_t* bytes) {
+  if (!bytes) return MHLA_ERR_INVALID_ARG;
+  Problem p;
+  const int rc = build_problem(q, q, q, q, grid, block, nullptr, /*check_alias=*/false, &p);
+  if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+  if (p.B == 0 || p.H == 0) { *bytes = 0; return MHLA_OK; }
+  int sel = 0;
+  const int rp = resolve_path(p, path, &sel);
+  if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
+  *bytes = workspace_for(p, sel);
+  return MHLA_OK;
+}
+
+extern "C" int32_t mhla_select_path(const mhla_tensor_t* q, const mhla_tensor_t* k, const mhla_tensor_t* v,
+                                    const mhla_tensor_t* out, const mhla_shape3_t* grid,
+                                    const mhla_shape3_t* block) {
+  Problem p;
+  const int rc = build_problem(q, k, v, out, grid, block, nullptr, true, &p);
+  if (rc != MHLA_OK) return -rc;
+  return tc_eligible(p) ? MHLA_PATH_TC : MHLA_PATH_SIMT;
+}
+
+extern "C" mhla_status_t mhla_forward(const mhla_tensor_t* q, const mhla_tensor_t* k, const mhla_tensor_t* v,
+                                      const float* W, const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                                      const mhla_phi_t* phi, const mhla_tensor_t* out, void* workspace,
+                                      size_t workspace_bytes, void* stream, int32_t path) {
+  if (!phi) return MHLA_ERR_INVALID_ARG;
+  Problem p;
+  const int rc = build_problem(q, k, v, out, grid, block, phi, true, &p);
+  if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+  int sel = 0;
+  const int rp = resolve_path(p, path, &sel);
+  if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
+  if (p.B == 0 || p.H == 0) return MHLA_OK;
+  if (!W) return MHLA_ERR_INVALID_ARG;
+  {
+    uintptr_t o0, o1;
+    span(out, &o0, &o1);
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(W);
+    if (overlaps(o0, o1, w0, w0 + static_cast<uintptr_t>(p.M * p.M) * sizeof(float))) return MHLA_ERR_INVALID_ARG;
+  }
+  const size_t need = workspace_for(p, sel);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  bool owned = false;
+  if (!ws) {
+    if (workspace_bytes != 0) return MHLA_ERR_WORKSPACE;
+    if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return MHLA_ERR_CUDA;
+    owned = true;
+  } else {
+    if (workspace_bytes < need) return MHLA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) % kAlign != 0) return MHLA_ERR_WORKSPACE;
+  }
+  const int lr = sel == MHLA_PATH_TC ? launch_tc(p, W, ws, stream) : launch_simt(p, W, ws, stream);
+  if (owned && cudaFreeAsync(ws, s) != cudaSuccess && lr == MHLA_OK) return MHLA_ERR_CUDA;
+  return static_cast<mhla_status_t>(lr);
+}
+
+extern "C" mhla_status_t mhla_device_status(void* stream, uint32_t* flags) {
+  if (!flags) return MHLA_ERR_INVALID_ARG;
+  return static_cast<mhla_status_t>(read_and_clear_device_error(stream, flags));
+}
+
+extern "C" const char* mhla_status_string(int32_t status) {
+  switch (status) {
+    case MHLA_OK: return "ok";
+    case MHLA_ERR_INVALID_ARG: return "invalid argument";
+    case MHLA_ERR_SHAPE: return "shape mismatch";
+    case MHLA_ERR_UNSUPPORTED: return "unsupported by the selected path";
+    case MHLA_ERR_CUDA: return "CUDA error";
+    case MHLA_ERR_TIMEOUT: return "device wait timed out";
+    case MHLA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    default: return "unknown status";
+  }
+}
+
+extern "C" const char* mhla_version(void) { return "mhla-gb300 0.1.0 sm_103a"; }

@@ -1,0 +1,84 @@
+// Internal host/device descriptors shared by the C ABI and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/mhla.h"
+
+namespace mhla {
+
+// One [B, N, H, d] operand: base pointer and element strides.
+struct Operand {
+  void* data;
+  int64_t sb, sn, sh;
+};
+
+// Everything a launch needs about the token geometry, resolved on the host.
+struct Problem {
+  int64_t B, N, H, d;
+  int dtype;            // mhla_dtype_t
+  int ndim;             // 2 or 3
+  int64_t T, Y, X;      // grid (T = 1 for 2-D)
+  int64_t bt, by, bx;   // block (bt = 1 for 2-D)
+  int64_t nbt, nby, nbx;
+  int64_t M, w;         // blocks, tokens per block
+  int phi_kind;
+  float eps;
+  Operand q, k, v, o;
+  int64_t BH() const { return B * H; }
+};
+
+// Block j (row-major over (nbt, nby, nbx)) and in-block slot s (raster over
+// (bt, by, bx)) -> token index n (raster over (T, Y, X)).
+struct TokenGeom {
+  int64_t Y, X, bt, by, bx, nby, nbx, M, w;
+};
+
+inline TokenGeom token_geom(const Problem& p) {
+  return TokenGeom{p.Y, p.X, p.bt, p.by, p.bx, p.nby, p.nbx, p.M, p.w};
+}
+
+// Workspace layout of the CUDA-core path (float32):
+//   Sz  [BH][M][d*(d+1)]  per block: S_j row-major then z_j
+//   Szt [BH][M][d*(d+1)]  mixed:     S~_i row-major then z~_i
+struct SimtWorkspace {
+  float* Sz;
+  float* Szt;
+};
+size_t simt_workspace_bytes(const Problem& p);
+SimtWorkspace simt_carve(const Problem& p, void* base);
+int launch_simt(const Problem& p, const float* W, void* workspace, void* stream);
+
+// Workspace layout of the tensor-core path:
+//   Wb   bf16 [M][Mp]                  W rounded to bf16, Mp = round_up(M, 8)
+//   Sbuf bf16 [M][BH*(d+1)*d]           per source block j: for each (b,h) the
+//                                       d rows of S_j then the row z_j
+//   St   bf16 [BH][M][d][d]             S~_i row-major (r, c)
+//   zt   f32  [BH][M][d]                z~_i
+size_t tc_workspace_bytes(const Problem& p);
+bool tc_eligible(const Problem& p);
+int launch_tc(const Problem& p, const float* W, void* workspace, void* stream);
+
+// Device error word of the tensor-core kernels (bounded waits).
+int read_and_clear_device_error(void* stream, uint32_t* flags);
+
+// Brackets one kernel launch with CUDA events on its stream while
+// mhla_profile_begin/end collection is active; a no-op otherwise.
+class KernelTimer {
+ public:
+  KernelTimer(const char* name, void* stream);
+  ~KernelTimer();
+  KernelTimer(const KernelTimer&) = delete;
+  KernelTimer& operator=(const KernelTimer&) = delete;
+
+ private:
+  const char* name_;
+  void* stream_;
+  void* start_;
+};
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+}  // namespace mhla
