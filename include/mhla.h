@@ -151,6 +151,35 @@ mhla_status_t mhla_forward(const mhla_tensor_t* q, const mhla_tensor_t* k,
                            void* workspace, size_t workspace_bytes, void* stream,
                            int32_t path);
 
+/* mhla_forward for callers that must not allocate device memory -- the paper
+ * has no counterpart to this; it is a property of the library, not the method.
+ * Who needs it: code that runs the forward where device allocation is not
+ * allowed, such as a plugin executing inside an inference engine's enqueue
+ * step (the engine owns all device memory) or a serving loop that plans its
+ * memory once at start-up (cudaFree synchronises the device; an allocation can
+ * fail under fragmentation).  The caller still passes q, k, v, W and out; the
+ * scratch comes from one array of MHLA_NOALLOC_SCRATCH_BYTES (64 MiB) compiled
+ * into the library, which every GPU that loads the library holds until the
+ * process exits.  The call allocates nothing: no cudaMalloc, cudaMallocAsync,
+ * cudaFree or allocating library routine.
+ *   Arguments as for mhla_forward, without workspace and workspace_bytes.
+ *   Returns MHLA_ERR_WORKSPACE, before touching the GPU, when the problem needs
+ *   more scratch than the array holds (mhla_workspace_size says how much it
+ *   needs); other statuses as for mhla_forward.
+ *   The first call on a device looks up the array's device address on that
+ *   device (cudaGetSymbolAddress, with that device current); make that first
+ *   call before any stream capture.
+ *   Every call on a device shares the one array and leaves its contents
+ *   behind; no part of it needs to start at zero, since each call writes every
+ *   scratch byte before reading it.  Calls whose work overlaps on the GPU (two
+ *   streams, or two threads) race on the array: order them on one stream. */
+#define MHLA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+mhla_status_t mhla_forward_noalloc(const mhla_tensor_t* q, const mhla_tensor_t* k,
+                                   const mhla_tensor_t* v, const float* W,
+                                   const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                                   const mhla_phi_t* phi, const mhla_tensor_t* out,
+                                   void* stream, int32_t path);
+
 /* Reads and clears the device error word the tensor-core kernels set when one
  * of their bounded waits gives up (bit 0: pipeline wait timeout).  Synchronises
  * stream.  *flags receives the word; returns MHLA_ERR_TIMEOUT when it was
