@@ -3,7 +3,7 @@
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step = one MHLA forward (W to bf16, summaries, mixing GEMM, outputs) over
+One step = one MHLA forward (summaries, mixing GEMM, outputs) over
 one synthetic batch of the workload, inputs resident in HBM.  Rank 0 prints one
 JSON line.  With N > 1 (torchrun) every rank runs an independent batch on its own
 GPU (replicas, weak scaling); ranks meet only for the timing barrier and the
@@ -178,7 +178,6 @@ def kernel_work(wl, name):
         "tc_summary": ("hbm", 2 * io), "simt_summary": ("hbm", 2 * io),
         "tc_output": ("hbm", 2 * io), "simt_output": ("hbm", 2 * io),
         "tc_mix": ("tensor", 2 * M * M * BH * d * (d + 1)), "simt_mix": ("alu", 2 * M * M * BH * d * (d + 1)),
-        "convert_w": ("hbm", M * M * 6),
     }
     return table.get(name, ("hbm", 0))
 
@@ -373,6 +372,7 @@ def run_ours(args, wl):
                          "float64 numpy oracle (blocked form); a slice counts N/H tokens"}
 
     launches = sum(n for n, _ in prof.values())
+    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", L2_BYTES)
     if rank == 0:
         line = {
             "impl": "ours", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -381,7 +381,7 @@ def run_ours(args, wl):
             "data": "synthetic",
             "config": {**wl.describe(), "path": path, "global_batch": wl.B * world, "seq_len": wl.N,
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
-                       "l2": f"inputs {3 * wl.algorithmic_bytes // 4 / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB "
+                       "l2": f"inputs {3 * wl.algorithmic_bytes // 4 / 1e6:.0f} MB > L2 {l2_bytes / 2**20:.0f} MiB "
                              "each step (no flush)",
                        "clock_window": f"{args.sustain:.1f} s sustained run of the same step, then both timed passes"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches,

@@ -258,5 +258,5 @@ def test_profile_reports_every_kernel():
     run(q, k, v, W, grid, block, path="tc")
     run(q, k, v, W, grid, block, path="simt")
     prof = mhla.profile_end()
-    for name in ("convert_w", "tc_summary", "tc_mix", "tc_output", "simt_summary", "simt_mix", "simt_output"):
+    for name in ("tc_summary", "tc_mix", "tc_output", "simt_summary", "simt_mix", "simt_output"):
         assert prof[name][0] == 1 and prof[name][1] > 0.0, name

@@ -54,7 +54,8 @@ int launch_simt(const Problem& p, const float* W, void* workspace, void* stream)
 //   Wb   bf16 [M][Mp]                  W rounded to bf16, Mp = round_up(M, 8)
 //   Sbuf bf16 [M][BH*(d+1)*d]           per source block j: for each (b,h) the
 //                                       d rows of S_j then the row z_j
-//   St   bf16 [BH][M][d][d]             S~_i row-major (r, c)
+//   St   bf16 [BH][M][d*d]              S~_i in the output MMA's operand layout:
+//                                       element (r, c) at (c/8)*8d + (r/8)*64 + (r%8)*8 + c%8
 //   zt   f32  [BH][M][d]                z~_i
 size_t tc_workspace_bytes(const Problem& p);
 bool tc_eligible(const Problem& p);

@@ -93,6 +93,17 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, uint64_
       : "memory");
 }
 
+// Plain (untiled) bulk copy of `bytes` contiguous bytes, global -> shared; both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_5d(const void* tmap, const void* src, int32_t c0, int32_t c1, int32_t c2,
                                              int32_t c3, int32_t c4) {
   asm volatile(
@@ -109,6 +120,12 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 }
 
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Wait until at most N committed bulk groups are still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -173,11 +190,13 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Shared-memory matrix descriptor of tcgen05.mma.  layout: 2 = 128-byte swizzle,
-// 4 = 64-byte swizzle.  lbo / sbo in bytes: for K-major operands sbo is the
-// distance between 8-row groups; for MN-major operands lbo is the distance
-// between consecutive swizzle-width chunks along M (or N) and sbo the distance
-// between 8-row groups along K.
+// Shared-memory matrix descriptor of tcgen05.mma.  layout: 0 = no swizzle,
+// 2 = 128-byte swizzle, 4 = 64-byte swizzle.  lbo / sbo in bytes.  Swizzled
+// K-major: sbo = distance between 8-row groups.  Swizzled MN-major: lbo =
+// distance between swizzle-width chunks along M (or N), sbo = distance between
+// 8-row groups along K.  Unswizzled MN-major (8 x 16-byte core matrices, 8
+// M/N-elements by 8 K-rows): sbo = distance between core matrices along M (or
+// N), lbo = distance between core matrices along K.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);

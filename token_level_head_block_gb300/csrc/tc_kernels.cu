@@ -7,16 +7,17 @@
 // MHLA.forward):
 //
 //   tc_summary  per (b, head group, block j): [S_j | z_j] = phi(K_j)^T [V_j | 1]
+//               (its prologue also rounds W to bf16 for the mixing GEMM)
 //               K and V chunks of 64 tokens arrive by 5-D TMA (d, H, X, Y, B*T);
 //               phi is applied in shared memory; 128/d heads share one
 //               128 x (128+16) MMA whose diagonal d x d blocks are the S_j and
 //               whose column 128 (a constant "ones" operand) is z_j.
 //   tc_mix      S~ = W . S as one GEMM over the source blocks j:
-//               D[col, i] = sum_j Sbuf[j][col] W[i][j], col = (b, h, row, c).
+//               D[i, col] = sum_j W[i][j] Sbuf[j][col], col = (b, h, row, c).
 //   tc_output   per (b, h, block i), 128 tokens at a time:
-//               o_t = phi(q_t) S~_i / (phi(q_t) . z~_i + eps); the numerator on
-//               the tensor core, the denominator in float32 on CUDA cores while
-//               phi is applied, the result stored by TMA in the input layout.
+//               o_t = phi(q_t) S~_i / (phi(q_t) . z~_i + eps); numerator and
+//               denominator from one MMA (z~_i rides as two extra B columns),
+//               the result scaled, rounded and stored by TMA in the input layout.
 //
 // Every mbarrier wait is bounded (time and poll count); a wait that gives up
 // raises a per-CTA abort flag so the other roles stop waiting too, sets bit 0 of
@@ -99,22 +100,19 @@ __device__ __forceinline__ void chunk_coords(const TcGeom& g, int32_t j, int32_t
   z = b * g.T + jt * g.bt + (c / g.nyc) * g.box_t;
 }
 
-// phi on eight bf16 values in place; returns the float32 values for callers
-// that need them (ReLU is exact in bf16; the + eps variant rounds once).
-__device__ __forceinline__ uint4 phi8(uint4 raw, int phi_kind, float eps, float (&f)[8]) {
-  const float add = phi_kind == MHLA_PHI_RELU_EPS ? eps : 0.0f;
-  __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&raw);
-  uint4 out;
-  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&out);
+// phi on eight bf16 values in place with packed bf16 arithmetic (no float32
+// round trip): max(x, 0), then + eps under MHLA_PHI_RELU_EPS.
+__device__ __forceinline__ uint4 phi8_packed(uint4 raw, bool add_eps, __nv_bfloat162 eps2) {
+  const __nv_bfloat162 zero = __float2bfloat162_rn(0.0f);
+  uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float2 v = __bfloat1622float2(h2[e]);
-    const float a = fmaxf(v.x, 0.0f) + add, b = fmaxf(v.y, 0.0f) + add;
-    f[2 * e] = a;
-    f[2 * e + 1] = b;
-    o2[e] = __floats2bfloat162_rn(a, b);
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w[e]);
+    v = __hmax2(v, zero);
+    if (add_eps) v = __hadd2(v, eps2);
+    w[e] = *reinterpret_cast<uint32_t*>(&v);
   }
-  return out;
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -131,6 +129,8 @@ __device__ __forceinline__ int swz(int row) {
 
 // ============================================================================
 // tc_summary
+// Work item = (b, j, head group) with the head group fastest, so the CTAs that
+// fetch the other heads of the same tokens run side by side.
 // ============================================================================
 template <int D>
 struct SumCfg {
@@ -155,7 +155,8 @@ template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, TcGeom g,
            int32_t G, int64_t n_items, int64_t ncols, int phi_kind, float eps,
-           __nv_bfloat16* __restrict__ Sbuf) {
+           __nv_bfloat16* __restrict__ Sbuf, const float* __restrict__ W, __nv_bfloat16* __restrict__ Wb,
+           int64_t Mp) {
   using Cfg = SumCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
@@ -171,6 +172,16 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   volatile uint32_t* abortf = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // W rounded to bf16 for the mixing GEMM, [M][Mp] with zero padding; every CTA
+  // converts a slice (the GEMM runs after this kernel on the same stream).
+  {
+    const int64_t n = static_cast<int64_t>(g.M) * Mp;
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * kTcThreads + threadIdx.x; e < n;
+         e += static_cast<int64_t>(gridDim.x) * kTcThreads) {
+      const int64_t i = e / Mp, j = e % Mp;
+      Wb[e] = __float2bfloat16_rn(j < g.M ? W[i * g.M + j] : 0.0f);
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::NS; ++s) {
       mbar_init(full + s, 1);
@@ -219,9 +230,9 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       uint64_t fills = 0;
       bool ok = true;
       for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        const int32_t j = static_cast<int32_t>(item % g.M);
-        const int64_t rest = item / g.M;
-        const int32_t grp = static_cast<int32_t>(rest % G), b = static_cast<int32_t>(rest / G);
+        const int32_t grp = static_cast<int32_t>(item % G);
+        const int64_t rest = item / G;
+        const int32_t j = static_cast<int32_t>(rest % g.M), b = static_cast<int32_t>(rest / g.M);
         for (int c = 0; c < g.chunks; ++c) {
           if (!wait_bounded(empty + s, ph ^ 1u, abortf)) { ok = false; break; }
           mbar_arrive_expect_tx(full + s, Cfg::LOADB);
@@ -282,6 +293,8 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     const int hh = rt / D, u = rt % D;
     const int rg = u / (D / 8), p = u % (D / 8);
     uint8_t* head_tile = stages + hh * Cfg::TILE + rg * Cfg::ROWB + p * 16;
+    const bool add_eps = phi_kind == MHLA_PHI_RELU_EPS;
+    const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -292,8 +305,7 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 #pragma unroll
         for (int m = 0; m < Cfg::C / 8; ++m) {
           uint4* ptr = reinterpret_cast<uint4*>(base + m * 8 * Cfg::ROWB);
-          float f[8];
-          *ptr = phi8(*ptr, phi_kind, eps, f);
+          *ptr = phi8_packed(*ptr, add_eps, eps2);
         }
         fence_proxy_async_smem();
         mbar_arrive(phid + s);
@@ -318,9 +330,9 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(tempty + acc);
-      const int32_t j = static_cast<int32_t>(item % g.M);
-      const int64_t rest = item / g.M;
-      const int32_t grp = static_cast<int32_t>(rest % G), b = static_cast<int32_t>(rest / G);
+      const int32_t grp = static_cast<int32_t>(item % G);
+      const int64_t rest = item / G;
+      const int32_t j = static_cast<int32_t>(rest % g.M), b = static_cast<int32_t>(rest / g.M);
       const int32_t h = grp * Cfg::HP + hh;
       if (h < g.H) {
         __nv_bfloat16* dst = Sbuf + static_cast<int64_t>(j) * ncols +
@@ -353,25 +365,33 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 }
 
 // ============================================================================
-// tc_mix:  D[col, i] = sum_j Sbuf[j][col] * W[i][j]
+// tc_mix:  D[i, col] = sum_j W[i][j] * Sbuf[j][col]
+// One tile = 128 query blocks i x 256 columns col = (b, h, row, c) of Sbuf; the
+// tensor-memory row of query block i then holds S~_i (and z~_i) contiguously.
 // ============================================================================
 struct MixCfg {
-  static constexpr int COLS = 128;     // GEMM M: Sbuf columns per tile
-  static constexpr int KC = 64;        // source blocks j per stage
-  static constexpr int A_BYTES = COLS * KC * 2;   // two 64-column MN-major chunks
+  static constexpr int ROWS = 128;               // query blocks per tile (MMA M)
+  static constexpr int COLS = 256;               // Sbuf columns per tile (MMA N)
+  static constexpr int KC = 64;                  // source blocks j per stage
+  static constexpr int A_BYTES = ROWS * KC * 2;  // W chunk, K-major
+  static constexpr int B_BYTES = KC * COLS * 2;  // Sbuf chunk, four 64-column MN-major chunks
+  static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int NS = 4;
+  static constexpr int ACC_STRIDE = 256;
+  static constexpr int TMEM_COLS = 512;
   static constexpr int CTRL = 1024;
+  static constexpr size_t SMEM = static_cast<size_t>(NS) * STAGE + CTRL + 1024;
 };
-constexpr int kMixThreadsTC = 192;   // producer, MMA, 4 epilogue warps
+constexpr int kMixThreadsTC = 320;   // producer, MMA, two epilogue warpgroups taking alternate tiles
 
 __global__ void __launch_bounds__(kMixThreadsTC, 1)
-tc_mix(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_w, int32_t M, int32_t N,
-       int32_t stage_bytes, int32_t tmem_cols, int32_t acc_stride, int64_t ncols, int32_t n_col_tiles,
-       int32_t n_i_tiles, int32_t d, __nv_bfloat16* __restrict__ St, float* __restrict__ zt) {
+tc_mix(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s, int32_t M,
+       int64_t ncols, int32_t n_col_tiles, int32_t n_i_tiles, int32_t d, __nv_bfloat16* __restrict__ St,
+       float* __restrict__ zt) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
   uint8_t* stages = smem;
-  uint8_t* ctrl = smem + MixCfg::NS * stage_bytes;
+  uint8_t* ctrl = smem + MixCfg::NS * MixCfg::STAGE;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + MixCfg::NS;
   uint64_t* tfull = empty + MixCfg::NS;
@@ -397,11 +417,11 @@ tc_mix(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtenso
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_s);
     prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_s);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, static_cast<uint32_t>(tmem_cols));
+    tmem_alloc(tmem_slot, MixCfg::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -409,24 +429,28 @@ tc_mix(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtenso
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Tiles run query-tile fastest, so the query tiles that read the same Sbuf
+  // columns run side by side and share them in L2.
   if (warp == 0) {
     if (lane == 0) {
-      const uint64_t pol_s = policy_evict_first();
       const uint64_t pol_w = policy_evict_last();
+      const uint64_t pol_s = policy_evict_first();
       int s = 0;
       uint32_t ph = 0;
       uint64_t fills = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
-        const int32_t col0 = static_cast<int32_t>(t % n_col_tiles) * MixCfg::COLS;
-        const int32_t i0 = static_cast<int32_t>(t / n_col_tiles) * 256;
+        const int32_t i0 = static_cast<int32_t>(t % n_i_tiles) * MixCfg::ROWS;
+        const int32_t col0 = static_cast<int32_t>(t / n_i_tiles) * MixCfg::COLS;
         for (int kc = 0; kc < nk; ++kc) {
           if (!wait_bounded(empty + s, ph ^ 1u, abortf)) { ok = false; break; }
-          mbar_arrive_expect_tx(full + s, static_cast<uint32_t>(MixCfg::A_BYTES + N * 128));
-          uint8_t* st = stages + s * stage_bytes;
-          tma_load_2d(st, &tm_s, full + s, col0, kc * MixCfg::KC, pol_s);
-          tma_load_2d(st + MixCfg::A_BYTES / 2, &tm_s, full + s, col0 + 64, kc * MixCfg::KC, pol_s);
-          tma_load_2d(st + MixCfg::A_BYTES, &tm_w, full + s, kc * MixCfg::KC, i0, pol_w);
+          mbar_arrive_expect_tx(full + s, MixCfg::STAGE);
+          uint8_t* st = stages + s * MixCfg::STAGE;
+          tma_load_2d(st, &tm_w, full + s, kc * MixCfg::KC, i0, pol_w);
+#pragma unroll
+          for (int a = 0; a < MixCfg::COLS / 64; ++a)
+            tma_load_2d(st + MixCfg::A_BYTES + a * (MixCfg::KC * 128), &tm_s, full + s, col0 + 64 * a,
+                        kc * MixCfg::KC, pol_s);
           ++fills;
           if (++s == MixCfg::NS) { s = 0; ph ^= 1u; }
         }
@@ -438,7 +462,8 @@ tc_mix(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtenso
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, N, /*a MN-major*/ true, /*b K-major*/ false);
+      constexpr uint32_t idesc = idesc_bf16_f32(MixCfg::ROWS, MixCfg::COLS, /*a K-major*/ false,
+                                                /*b MN-major*/ true);
       int s = 0;
       uint32_t ph = 0, local = 0;
       bool ok = true;
@@ -446,15 +471,15 @@ tc_mix(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtenso
         const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
         if (!wait_bounded(tempty + acc, aph ^ 1u, abortf)) break;
         tc_fence_after();
-        const uint32_t dt = tmem + acc * static_cast<uint32_t>(acc_stride);
+        const uint32_t dt = tmem + acc * MixCfg::ACC_STRIDE;
         for (int kc = 0; kc < nk; ++kc) {
           if (!wait_bounded(full + s, ph, abortf)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t base = smem_u32(stages + s * stage_bytes);
+          const uint32_t base = smem_u32(stages + s * MixCfg::STAGE);
 #pragma unroll
           for (int ks = 0; ks < MixCfg::KC / 16; ++ks) {
-            const uint64_t a = smem_desc(base + ks * 2048, MixCfg::A_BYTES / 2, 1024, 2);
-            const uint64_t b = smem_desc(base + MixCfg::A_BYTES + ks * 32, 16, 1024, 2);
+            const uint64_t a = smem_desc(base + ks * 32, 16, 1024, 2);
+            const uint64_t b = smem_desc(base + MixCfg::A_BYTES + ks * 2048, MixCfg::KC * 128, 1024, 2);
             mma_bf16(dt, a, b, idesc, (kc | ks) != 0 ? 1u : 0u);
           }
           mma_commit(empty + s);
@@ -467,44 +492,47 @@ tc_mix(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtenso
       drain_wait(fin, 0);
     }
   } else {
+    // warpgroup wg (warps 2-5 or 6-9) drains accumulator wg: the tiles with local % 2 == wg
+    const int wg = (warp - 2) >> 2;
     const int q4 = warp & 3;
-    const int row = 32 * q4 + lane;
+    const int row = 32 * q4 + lane;                    // query block within the tile
     const int64_t per_bh = static_cast<int64_t>(d + 1) * d;
     uint32_t local = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
+      if (static_cast<int>(local & 1u) != wg) continue;
       const uint32_t acc = local & 1u, aph = (local >> 1) & 1u;
       if (!warp_wait(tfull + acc, aph, abortf)) break;
       tc_fence_after();
-      const int64_t col = static_cast<int64_t>(t % n_col_tiles) * MixCfg::COLS + row;
-      const int32_t i0 = static_cast<int32_t>(t / n_col_tiles) * 256;
-      const bool live = col < ncols;
-      const int64_t bh = col / per_bh, rem = col % per_bh;
-      const int rr = static_cast<int>(rem / d), c = static_cast<int>(rem % d);
-      const uint32_t tb = tmem + acc * static_cast<uint32_t>(acc_stride) + (static_cast<uint32_t>(32 * q4) << 16);
-      for (int cc = 0; cc < N; cc += 32) {
+      const int32_t i = static_cast<int32_t>(t % n_i_tiles) * MixCfg::ROWS + row;
+      const int64_t col0 = (t / n_i_tiles) * MixCfg::COLS;
+      const uint32_t tb = tmem + acc * MixCfg::ACC_STRIDE + (static_cast<uint32_t>(32 * q4) << 16);
+#pragma unroll 1
+      for (int cc = 0; cc < MixCfg::COLS; cc += 32) {
         uint32_t v[32];
-        if (N - cc >= 32) {
-          tmem_ld_x32(tb + cc, v);
-        } else {
-          uint32_t h16[16];
-          tmem_ld_x16(tb + cc, h16);
-#pragma unroll
-          for (int u = 0; u < 16; ++u) v[u] = h16[u];
-#pragma unroll
-          for (int u = 16; u < 32; ++u) v[u] = 0u;
-        }
+        tmem_ld_x32(tb + cc, v);
         tmem_ld_wait();
-        if (live) {
+        const int64_t col = col0 + cc;                 // 32 columns of one row of one (b, h)
+        if (i < M && col < ncols) {
+          const int64_t bh = col / per_bh, rem = col % per_bh;
+          const int64_t rr = rem / d, c0 = rem % d;
+          if (rr < d) {
+            // S~_i tile in the output MMA's unswizzled MN-major layout: 16-byte
+            // core-matrix rows (8 columns c of one row rr), 8 rows rr per core
+            // matrix, core matrices of a column group 128 bytes apart along rr,
+            // column groups d*16 bytes apart.
+            __nv_bfloat16* tile = St + (bh * M + i) * d * d;
+            const int64_t rbase = (rr >> 3) * 64 + (rr & 7) * 8;
 #pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const int32_t i = i0 + cc + u;
-            if (cc + u < N && i < M) {
-              const float val = __uint_as_float(v[u]);
-              if (rr < d)
-                St[((bh * M + i) * d + rr) * d + c] = __float2bfloat16_rn(val);
-              else
-                zt[(bh * M + i) * d + c] = val;
-            }
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(tile + ((c0 >> 3) + q) * (d * 8) + rbase) =
+                  make_uint4(pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                             pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                             pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                             pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(zt + (bh * M + i) * d + c0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) dst[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           }
         }
       }
@@ -516,56 +544,84 @@ tc_mix(const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtenso
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, static_cast<uint32_t>(tmem_cols));
+    tmem_dealloc(tmem, MixCfg::TMEM_COLS);
   }
 }
 
 // ============================================================================
 // tc_output
+// Work item = (b, i, h) with the head fastest, so neighbouring CTAs read the
+// neighbouring 128-byte head rows of the same tokens at about the same time.
+// One MMA per 16 channels gives numerator and denominator together:
+//   D[t][0..d)  = phi(q_t) S~_i                   (B columns 0..d-1: S~_i)
+//   D[t][d]     = phi(q_t) . hi(z~_i)             (B column d:   z~_i rounded to bf16)
+//   D[t][d+1]   = phi(q_t) . (z~_i - hi(z~_i))    (B column d+1: the rounding remainder)
+// so the float32 denominator keeps about 16 bits more than a bf16 z~ would.
+//
+// The kernel streams q at the rate HBM allows only if enough loads are in
+// flight: under full load a q chunk takes several microseconds to arrive, so
+// shared memory goes almost entirely to q stages.  The output of a chunk is
+// written back into its own q stage (the MMA has consumed it by then) and
+// stored from there; the S~_i tiles, one per work item, have their own small
+// ring fed by a second producer warp.
 // ============================================================================
 template <int D>
 struct OutCfg {
   static constexpr int C = 128;                 // tokens per chunk = MMA M
+  static constexpr int N = D + 16;              // S~ columns + the two z~ columns (+ 14 unused)
   static constexpr int ROWB = D * 2;
-  static constexpr int QT = C * ROWB;           // q (then o) tile
-  static constexpr int BT = D * ROWB;           // S~_i tile
-  static constexpr int STAGE = ((QT + BT + 1023) / 1024) * 1024;
-  static constexpr int NS = 6;
-  static constexpr uint32_t SBO = 8 * ROWB;
-  static constexpr uint32_t LAYOUT = D == 64 ? 2u : 4u;
-  static constexpr int TMEM_COLS = 2 * D < 32 ? 32 : 2 * D;
-  static constexpr int CTRL = 1024 + NS * C * 4;  // barriers + denominators
-  static constexpr size_t SMEM = static_cast<size_t>(NS) * STAGE + CTRL + 1024;
+  static constexpr int QT = C * ROWB;           // q tile, then the output tile of the chunk
+  static constexpr int KG = D / 8;              // core matrices along K (= rows of S~)
+  static constexpr int B_SBO = KG * 128;        // bytes between column groups of 8
+  static constexpr int ST_BYTES = D * D * 2;    // S~_i tile as written by tc_mix
+  static constexpr int BT = ((N / 8) * B_SBO + 1023) / 1024 * 1024;  // B slot incl. the z~ column groups
+  static constexpr int NQ = D == 64 ? 9 : 16;   // q stages
+  static constexpr int NB = D == 64 ? 6 : 10;   // B slots (one per work item)
+  static constexpr uint32_t A_SBO = 8 * ROWB;
+  static constexpr uint32_t A_LAYOUT = D == 64 ? 2u : 4u;
+  static constexpr int ACC_STRIDE = D == 64 ? 128 : 64;
+  static constexpr int TMEM_COLS = 2 * ACC_STRIDE;
+  static constexpr int CTRL = 1024;
+  static constexpr size_t SMEM = static_cast<size_t>(NQ) * QT + static_cast<size_t>(NB) * BT + CTRL + 1024;
 };
+// q producer, MMA, 4 phi warps, two epilogue warpgroups taking alternate
+// chunks, B producer
+constexpr int kOutThreadsTC = 480;
 
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
-tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
-          const __grid_constant__ CUtensorMap tm_st, TcGeom g, int64_t n_items, int phi_kind, float eps,
+__global__ void __launch_bounds__(kOutThreadsTC, 1)
+tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o, TcGeom g,
+          int64_t n_items, int phi_kind, float eps, const __nv_bfloat16* __restrict__ St,
           const float* __restrict__ zt) {
   using Cfg = OutCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
-  uint8_t* stages = smem;
-  uint8_t* ctrl = smem + Cfg::NS * Cfg::STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-  uint64_t* phid = full + Cfg::NS;
-  uint64_t* empty = phid + Cfg::NS;
-  uint64_t* ostore = empty + Cfg::NS;
-  uint64_t* tfull = ostore + Cfg::NS;
+  uint8_t* qst = smem;                                   // [NQ] q / output tiles
+  uint8_t* bslot = smem + Cfg::NQ * Cfg::QT;             // [NB] S~ tiles + z~ columns
+  uint8_t* ctrl = bslot + Cfg::NB * Cfg::BT;
+  uint64_t* qfull = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* phid = qfull + Cfg::NQ;
+  uint64_t* ostore = phid + Cfg::NQ;
+  uint64_t* qempty = ostore + Cfg::NQ;
+  uint64_t* bfull = qempty + Cfg::NQ;
+  uint64_t* bempty = bfull + Cfg::NB;
+  uint64_t* tfull = bempty + Cfg::NB;
   uint64_t* tempty = tfull + 2;
   uint64_t* fin = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 512);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 768);
   volatile uint32_t* abortf = tmem_slot + 1;
-  float* den_s = reinterpret_cast<float*>(ctrl + 1024);   // [NS][C]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Cfg::NS; ++s) {
-      mbar_init(full + s, 1);
+    for (int s = 0; s < Cfg::NQ; ++s) {
+      mbar_init(qfull + s, 1);
       mbar_init(phid + s, 128);
-      mbar_init(empty + s, 1);
       mbar_init(ostore + s, 128);
+      mbar_init(qempty + s, 1);
+    }
+    for (int k = 0; k < Cfg::NB; ++k) {
+      mbar_init(bfull + k, 1 + 32);   // the S~ copy (expect_tx) and 32 lanes writing z~
+      mbar_init(bempty + k, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull + a, 1);
@@ -578,7 +634,6 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_o);
-    prefetch_tmap(&tm_st);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -590,148 +645,188 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
+    // ------------------------------------------- q producer
     if (lane == 0) {
       const uint64_t pol_q = policy_evict_first();
-      const uint64_t pol_s = policy_evict_last();
       int s = 0;
       uint32_t ph = 0;
       uint64_t fills = 0;
       bool ok = true;
       for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        const int32_t i = static_cast<int32_t>(item % g.M);
-        const int64_t bh = item / g.M;
-        const int32_t b = static_cast<int32_t>(bh / g.H), h = static_cast<int32_t>(bh % g.H);
+        const int32_t h = static_cast<int32_t>(item % g.H);
+        const int64_t rest = item / g.H;
+        const int32_t i = static_cast<int32_t>(rest % g.M), b = static_cast<int32_t>(rest / g.M);
         for (int c = 0; c < g.chunks; ++c) {
-          if (!wait_bounded(empty + s, ph ^ 1u, abortf)) { ok = false; break; }
-          mbar_arrive_expect_tx(full + s, Cfg::QT + Cfg::BT);
+          if (!wait_bounded(qempty + s, ph ^ 1u, abortf)) { ok = false; break; }
+          mbar_arrive_expect_tx(qfull + s, Cfg::QT);
           int32_t x, y, z;
           chunk_coords(g, i, c, b, x, y, z);
-          uint8_t* st = stages + s * Cfg::STAGE;
-          tma_load_5d(st, &tm_q, full + s, 0, h, x, y, z, pol_q);
-          tma_load_2d(st + Cfg::QT, &tm_st, full + s, 0, static_cast<int32_t>(item * D), pol_s);
+          tma_load_5d(qst + s * Cfg::QT, &tm_q, qfull + s, 0, h, x, y, z, pol_q);
           ++fills;
-          if (++s == Cfg::NS) { s = 0; ph ^= 1u; }
+          if (++s == Cfg::NQ) { s = 0; ph ^= 1u; }
         }
       }
-      for (int st = 0; st < Cfg::NS; ++st) {
-        const uint64_t n = fills / Cfg::NS + (static_cast<uint64_t>(st) < fills % Cfg::NS ? 1 : 0);
-        if (n > 0) drain_wait(full + st, static_cast<uint32_t>((n - 1) & 1));
+      for (int st = 0; st < Cfg::NQ; ++st) {
+        const uint64_t n = fills / Cfg::NQ + (static_cast<uint64_t>(st) < fills % Cfg::NQ ? 1 : 0);
+        if (n > 0) drain_wait(qfull + st, static_cast<uint32_t>((n - 1) & 1));
+      }
+    }
+  } else if (warp == 14) {
+    // ------------------------------------------- B producer: one slot per item
+    // Lane 0 copies S~_i into the slot; all lanes write z~_i as its two bf16
+    // halves into columns D and D+1.  Running up to NB items ahead keeps the
+    // z~ loads off the critical path.
+    const uint64_t pol_s = policy_evict_last();
+    int kb = 0;
+    uint32_t bph = 0;
+    uint64_t fills = 0;
+    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const int64_t h = item % g.H, rest = item / g.H;
+      const int64_t i = rest % g.M, b = rest / g.M;
+      const int64_t tile = (b * g.H + h) * g.M + i;
+      if (!warp_wait(bempty + kb, bph ^ 1u, abortf)) break;
+      uint8_t* slot = bslot + kb * Cfg::BT;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bfull + kb, Cfg::ST_BYTES);
+        bulk_load(slot, St + tile * D * D, Cfg::ST_BYTES, bfull + kb, pol_s);
+      }
+#pragma unroll
+      for (int r = lane; r < D; r += 32) {
+        const float zv = __ldg(zt + tile * D + r);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
+        *reinterpret_cast<uint32_t*>(slot + (D / 8) * Cfg::B_SBO + (r >> 3) * 128 + (r & 7) * 16) =
+            static_cast<uint32_t>(__bfloat16_as_ushort(hi)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bfull + kb);
+      ++fills;
+      if (++kb == Cfg::NB) { kb = 0; bph ^= 1u; }
+    }
+    if (lane == 0) {
+      for (int st = 0; st < Cfg::NB; ++st) {
+        const uint64_t n = fills / Cfg::NB + (static_cast<uint64_t>(st) < fills % Cfg::NB ? 1 : 0);
+        if (n > 0) drain_wait(bfull + st, static_cast<uint32_t>((n - 1) & 1));
       }
     }
   } else if (warp == 1) {
+    // ------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, D, /*a K-major*/ false, /*b MN-major*/ true);
-      int s = 0;
-      uint32_t ph = 0, cnt = 0;
+      constexpr uint32_t idesc = idesc_bf16_f32(128, Cfg::N, /*a K-major*/ false, /*b MN-major*/ true);
+      int s = 0, kb = 0;
+      uint32_t ph = 0, cnt = 0, bph = 0;
       bool ok = true;
       for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        // the slot of this item: S~ copy landed and z~ columns written
+        if (!wait_bounded(bfull + kb, bph, abortf)) break;
+        const uint32_t bbase = smem_u32(bslot + kb * Cfg::BT);
         for (int c = 0; c < g.chunks; ++c, ++cnt) {
           const uint32_t acc = cnt & 1u, aph = (cnt >> 1) & 1u;
           if (!wait_bounded(tempty + acc, aph ^ 1u, abortf)) { ok = false; break; }
           if (!wait_bounded(phid + s, ph, abortf)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t base = smem_u32(stages + s * Cfg::STAGE);
+          const uint32_t base = smem_u32(qst + s * Cfg::QT);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t a = smem_desc(base + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT);
-            const uint64_t b = smem_desc(base + Cfg::QT + ks * 2 * Cfg::SBO, 16, Cfg::SBO, Cfg::LAYOUT);
-            mma_bf16(tmem + acc * D, a, b, idesc, ks != 0 ? 1u : 0u);
+            const uint64_t a = smem_desc(base + ks * 32, 16, Cfg::A_SBO, Cfg::A_LAYOUT);
+            const uint64_t b = smem_desc(bbase + ks * 256, 128, Cfg::B_SBO, 0);
+            mma_bf16(tmem + acc * Cfg::ACC_STRIDE, a, b, idesc, ks != 0 ? 1u : 0u);
           }
           mma_commit(tfull + acc);
-          if (++s == Cfg::NS) { s = 0; ph ^= 1u; }
+          if (++s == Cfg::NQ) { s = 0; ph ^= 1u; }
         }
+        if (!ok) break;
+        mma_commit(bempty + kb);              // slot reusable once this item's MMAs are done
+        if (++kb == Cfg::NB) { kb = 0; bph ^= 1u; }
       }
       mma_commit(fin);
       drain_wait(fin, 0);
     }
   } else if (warp < 6) {
-    // ------------------------------------------- phi on q, denominators
+    // ------------------------------------------- phi on q
     constexpr int CPR = D / 8;            // 16-byte chunks per row
     constexpr int RP = 128 / CPR;         // rows covered per pass
     const int rt = threadIdx.x - 64;
     const int rg = rt / CPR, p = rt % CPR;
-    const int lc = p ^ swz<D>(rg);        // logical chunk: channels lc*8 .. lc*8+7
+    const bool add_eps = phi_kind == MHLA_PHI_RELU_EPS;
+    const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
     for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-      const float4* zp = reinterpret_cast<const float4*>(zt + item * D + lc * 8);
-      const float4 za = __ldg(zp), zb = __ldg(zp + 1);
-      const float zr[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
       for (int c = 0; c < g.chunks; ++c) {
-        if (!warp_wait(full + s, ph, abortf)) { ok = false; break; }
-        uint8_t* tile = stages + s * Cfg::STAGE;
+        if (!warp_wait(qfull + s, ph, abortf)) { ok = false; break; }
+        uint8_t* tile = qst + s * Cfg::QT;
 #pragma unroll
         for (int m = 0; m < Cfg::C / RP; ++m) {
-          const int r = rg + RP * m;
-          uint4* ptr = reinterpret_cast<uint4*>(tile + r * Cfg::ROWB + p * 16);
-          float f[8];
-          *ptr = phi8(*ptr, phi_kind, eps, f);
-          float part = 0.0f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) part = fmaf(f[e], zr[e], part);
-#pragma unroll
-          for (int off = 1; off < CPR; off <<= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-          if (p == 0) den_s[s * Cfg::C + r] = part;
+          uint4* ptr = reinterpret_cast<uint4*>(tile + (rg + RP * m) * Cfg::ROWB + p * 16);
+          *ptr = phi8_packed(*ptr, add_eps, eps2);
         }
         fence_proxy_async_smem();
         mbar_arrive(phid + s);
-        if (++s == Cfg::NS) { s = 0; ph ^= 1u; }
+        if (++s == Cfg::NQ) { s = 0; ph ^= 1u; }
       }
     }
   } else {
-    // ------------------------------------------- epilogue: divide, store by TMA
+    // ------------------------------------------- epilogue: scale, write back, store by TMA
+    // Warpgroup wg (warps 6-9 or 10-13) takes the chunks with cnt % 2 == wg, which
+    // are exactly the chunks accumulated in TMEM accumulator wg.
+    const int wg = (warp - 6) >> 2;
     const int q4 = warp & 3;
     const int row = 32 * q4 + lane;      // token row of the chunk
-    const bool store_thread = (warp == 6 && lane == 0);
+    const bool store_thread = ((warp - 6) & 3) == 0 && lane == 0;
     int s = 0;
     uint32_t ph = 0, cnt = 0;
     bool ok = true;
     for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-      const int32_t i = static_cast<int32_t>(item % g.M);
-      const int64_t bh = item / g.M;
-      const int32_t b = static_cast<int32_t>(bh / g.H), h = static_cast<int32_t>(bh % g.H);
+      const int32_t h = static_cast<int32_t>(item % g.H);
+      const int64_t rest = item / g.H;
+      const int32_t i = static_cast<int32_t>(rest % g.M), b = static_cast<int32_t>(rest / g.M);
       for (int c = 0; c < g.chunks; ++c, ++cnt) {
-        const uint32_t acc = cnt & 1u, aph = (cnt >> 1) & 1u;
+        const int cs = s;
+        const uint32_t cph = ph;
+        if (++s == Cfg::NQ) { s = 0; ph ^= 1u; }
+        if (static_cast<int>(cnt & 1u) != wg) continue;
+        const uint32_t k = cnt >> 1;                 // this warpgroup's chunk number
+        const uint32_t acc = wg, aph = k & 1u;
         if (!warp_wait(tfull + acc, aph, abortf)) { ok = false; break; }
-        // den_s was written by the phi warps before they released this stage.
-        if (!warp_wait(phid + s, ph, abortf)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tb = tmem + acc * D + (static_cast<uint32_t>(32 * q4) << 16);
-        uint32_t v0[32], v1[32];
+        const uint32_t tb = tmem + acc * Cfg::ACC_STRIDE + (static_cast<uint32_t>(32 * q4) << 16);
+        uint32_t v0[32], v1[32], vz[16];
         tmem_ld_x32(tb, v0);
         if (D == 64) tmem_ld_x32(tb + 32, v1);
+        tmem_ld_x16(tb + D, vz);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(tempty + acc);
-        const float den = den_s[s * Cfg::C + row] + eps;
-        uint8_t* orow = stages + s * Cfg::STAGE + row * Cfg::ROWB;
+        const float inv = 1.0f / (__uint_as_float(vz[0]) + __uint_as_float(vz[1]) + eps);
+        // the MMA has finished reading the q tile: the output row goes in its place
+        uint8_t* orow = qst + cs * Cfg::QT + row * Cfg::ROWB;
 #pragma unroll
         for (int q = 0; q < D / 8; ++q) {
           const uint32_t* src = (q < 4) ? (v0 + 8 * q) : (v1 + 8 * (q - 4));
           const uint4 packed = make_uint4(
-              pack_bf16(__uint_as_float(src[0]) / den, __uint_as_float(src[1]) / den),
-              pack_bf16(__uint_as_float(src[2]) / den, __uint_as_float(src[3]) / den),
-              pack_bf16(__uint_as_float(src[4]) / den, __uint_as_float(src[5]) / den),
-              pack_bf16(__uint_as_float(src[6]) / den, __uint_as_float(src[7]) / den));
+              pack_bf16(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv),
+              pack_bf16(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv),
+              pack_bf16(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv),
+              pack_bf16(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv));
           *reinterpret_cast<uint4*>(orow + ((q ^ swz<D>(row)) * 16)) = packed;
         }
         fence_proxy_async_smem();
-        mbar_arrive(ostore + s);
+        mbar_arrive(ostore + cs);
         if (store_thread) {
-          if (wait_bounded(ostore + s, ph, abortf)) {
+          if (wait_bounded(ostore + cs, cph, abortf)) {
             int32_t x, y, z;
             chunk_coords(g, i, c, b, x, y, z);
-            tma_store_5d(&tm_o, stages + s * Cfg::STAGE, 0, h, x, y, z);
+            tma_store_5d(&tm_o, qst + cs * Cfg::QT, 0, h, x, y, z);
             bulk_commit_group();
-            bulk_wait_group_read0();
+            bulk_wait_group_read<0>();       // the stage is free once the store has read it
           } else {
             ok = false;
           }
-          mbar_arrive(empty + s);
+          mbar_arrive(qempty + cs);
         }
         ok = __all_sync(0xffffffffu, ok);
-        if (++s == Cfg::NS) { s = 0; ph ^= 1u; }
       }
     }
     if (store_thread) bulk_wait_group0();
@@ -741,16 +836,6 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::TMEM_COLS);
-  }
-}
-
-// W (float32, M x M) -> bf16 [M][Mp], zero padded columns.
-__global__ void convert_w(const float* __restrict__ W, __nv_bfloat16* __restrict__ Wb, int64_t M, int64_t Mp) {
-  const int64_t n = M * Mp;
-  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < n;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t i = e / Mp, j = e % Mp;
-    Wb[e] = __float2bfloat16_rn(j < M ? W[i * M + j] : 0.0f);
   }
 }
 
@@ -904,15 +989,6 @@ int launch_tc_d(const Problem& p, const float* W, void* workspace, cudaStream_t 
   ChunkPlan c64, c128;
   if (!chunk_plan(p, 64, &c64) || !chunk_plan(p, 128, &c128)) return MHLA_ERR_UNSUPPORTED;
 
-  // ---- step 0: W -> bf16
-  {
-    const int64_t n = p.M * L.Mp;
-    const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 4096));
-    KernelTimer timer("convert_w", stream);
-    convert_w<<<blocks, 256, 0, stream>>>(W, Wb, p.M, L.Mp);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
-
   // ---- step 1: summaries
   {
     using Cfg = SumCfg<D>;
@@ -928,70 +1004,54 @@ int launch_tc_d(const Problem& p, const float* W, void* workspace, cudaStream_t 
     const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
     KernelTimer timer("tc_summary", stream);
     tc_summary<D><<<grid, kTcThreads, Cfg::SMEM, stream>>>(tk, tv, make_geom(p, c64), G, n_items, L.ncols,
-                                                           p.phi_kind, p.eps, Sbuf);
+                                                           p.phi_kind, p.eps, Sbuf, W, Wb, L.Mp);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
 
   // ---- step 2: mixing GEMM
   {
-    const int32_t N = static_cast<int32_t>(std::min<int64_t>(256, (p.M + 15) / 16 * 16));
-    int32_t tcols = 32;
-    while (tcols < N) tcols *= 2;
-    const int32_t acc_stride = tcols;
-    const int32_t tmem_cols = 2 * tcols;
-    const int32_t stage_bytes = MixCfg::A_BYTES + ((N * 128 + 1023) / 1024) * 1024;
-    const size_t smem = static_cast<size_t>(MixCfg::NS) * stage_bytes + MixCfg::CTRL + 1024;
-    CUtensorMap ts, tw;
+    CUtensorMap tw, ts;
+    {
+      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.M)};
+      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.Mp * 2)};
+      const cuuint32_t box[2] = {static_cast<cuuint32_t>(MixCfg::KC), static_cast<cuuint32_t>(MixCfg::ROWS)};
+      if (!encode(&tw, 2, Wb, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
+    }
     {
       const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.ncols), static_cast<cuuint64_t>(p.M)};
       const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.ncols * 2)};
       const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(MixCfg::KC)};
       if (!encode(&ts, 2, Sbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
     }
-    {
-      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.M)};
-      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.Mp * 2)};
-      const cuuint32_t box[2] = {static_cast<cuuint32_t>(MixCfg::KC), static_cast<cuuint32_t>(N)};
-      if (!encode(&tw, 2, Wb, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
-    }
     const int32_t n_col_tiles = static_cast<int32_t>((L.ncols + MixCfg::COLS - 1) / MixCfg::COLS);
-    const int32_t n_i_tiles = static_cast<int32_t>((p.M + 255) / 256);
-    if (cudaFuncSetAttribute(tc_mix, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
+    const int32_t n_i_tiles = static_cast<int32_t>((p.M + MixCfg::ROWS - 1) / MixCfg::ROWS);
+    if (cudaFuncSetAttribute(tc_mix, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(MixCfg::SMEM)) != cudaSuccess)
       return MHLA_ERR_CUDA;
-    const int per_sm = std::max(1, std::min(occupancy(tc_mix, kMixThreadsTC, smem), 512 / tmem_cols));
     const int64_t n_tiles = static_cast<int64_t>(n_col_tiles) * n_i_tiles;
-    const int grid = static_cast<int>(std::min<int64_t>(n_tiles, static_cast<int64_t>(sms) * per_sm));
+    const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
     KernelTimer timer("tc_mix", stream);
-    tc_mix<<<grid, kMixThreadsTC, smem, stream>>>(ts, tw, static_cast<int32_t>(p.M), N, stage_bytes, tmem_cols,
-                                                   acc_stride, L.ncols, n_col_tiles, n_i_tiles,
-                                                   static_cast<int32_t>(p.d), St, zt);
+    tc_mix<<<grid, kMixThreadsTC, MixCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), L.ncols, n_col_tiles,
+                                                           n_i_tiles, static_cast<int32_t>(p.d), St, zt);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
 
   // ---- step 3: outputs
   {
     using Cfg = OutCfg<D>;
-    CUtensorMap tq, to, tst;
+    CUtensorMap tq, to;
     if (!operand_map(p, p.q, c128.box_y, c128.box_t, &tq) || !operand_map(p, p.o, c128.box_y, c128.box_t, &to))
       return MHLA_ERR_CUDA;
-    {
-      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(p.BH() * p.M * p.d)};
-      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.d * 2)};
-      const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.d), static_cast<cuuint32_t>(p.d)};
-      if (!encode(&tst, 2, St, dims, strides, box,
-                  p.d == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
-        return MHLA_ERR_CUDA;
-    }
     const int64_t n_items = p.BH() * p.M;
     if (cudaFuncSetAttribute(tc_output<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Cfg::SMEM)) != cudaSuccess)
       return MHLA_ERR_CUDA;
-    const int per_sm = std::max(1, std::min(occupancy(tc_output<D>, kTcThreads, Cfg::SMEM), 512 / Cfg::TMEM_COLS));
+    const int per_sm =
+        std::max(1, std::min(occupancy(tc_output<D>, kOutThreadsTC, Cfg::SMEM), 512 / Cfg::TMEM_COLS));
     const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
     KernelTimer timer("tc_output", stream);
-    tc_output<D><<<grid, kTcThreads, Cfg::SMEM, stream>>>(tq, to, tst, make_geom(p, c128), n_items, p.phi_kind,
-                                                          p.eps, zt);
+    tc_output<D><<<grid, kOutThreadsTC, Cfg::SMEM, stream>>>(tq, to, make_geom(p, c128), n_items, p.phi_kind, p.eps,
+                                                          St, zt);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
   return MHLA_OK;
