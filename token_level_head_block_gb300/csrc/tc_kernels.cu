@@ -574,7 +574,9 @@ struct OutCfg {
   static constexpr int KG = D / 8;              // core matrices along K (= rows of S~)
   static constexpr int B_SBO = KG * 128;        // bytes between column groups of 8
   static constexpr int ST_BYTES = D * D * 2;    // S~_i tile as written by tc_mix
-  static constexpr int BT = ((N / 8) * B_SBO + 1023) / 1024 * 1024;  // B slot incl. the z~ column groups
+  static constexpr int BOPS = (N / 8) * B_SBO;  // B operand: S~ columns and the z~ column groups
+  static constexpr int ZRAW = D * 4;              // z~_i in float32, copied in after the operand
+  static constexpr int BT = (BOPS + ZRAW + 1023) / 1024 * 1024;
   static constexpr int NQ = D == 64 ? 9 : 16;   // q stages
   static constexpr int NB = D == 64 ? 6 : 10;   // B slots (one per work item)
   static constexpr uint32_t A_SBO = 8 * ROWB;
@@ -585,8 +587,9 @@ struct OutCfg {
   static constexpr size_t SMEM = static_cast<size_t>(NQ) * QT + static_cast<size_t>(NB) * BT + CTRL + 1024;
 };
 // q producer, MMA, 4 phi warps, two epilogue warpgroups taking alternate
-// chunks, B producer
-constexpr int kOutThreadsTC = 480;
+// chunks, B producer, store issuer
+constexpr int kOutThreadsTC = 512;
+constexpr int kOutStoresInFlight = 3;   // TMA stores allowed to be reading shared memory at once
 
 template <int D>
 __global__ void __launch_bounds__(kOutThreadsTC, 1)
@@ -620,7 +623,7 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       mbar_init(qempty + s, 1);
     }
     for (int k = 0; k < Cfg::NB; ++k) {
-      mbar_init(bfull + k, 1 + 32);   // the S~ copy (expect_tx) and 32 lanes writing z~
+      mbar_init(bfull + k, 1);
       mbar_init(bempty + k, 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -673,41 +676,64 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     }
   } else if (warp == 14) {
     // ------------------------------------------- B producer: one slot per item
-    // Lane 0 copies S~_i into the slot; all lanes write z~_i as its two bf16
-    // halves into columns D and D+1.  Running up to NB items ahead keeps the
-    // z~ loads off the critical path.
-    const uint64_t pol_s = policy_evict_last();
-    int kb = 0;
-    uint32_t bph = 0;
-    uint64_t fills = 0;
-    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const int64_t h = item % g.H, rest = item / g.H;
-      const int64_t i = rest % g.M, b = rest / g.M;
-      const int64_t tile = (b * g.H + h) * g.M + i;
-      if (!warp_wait(bempty + kb, bph ^ 1u, abortf)) break;
-      uint8_t* slot = bslot + kb * Cfg::BT;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bfull + kb, Cfg::ST_BYTES);
-        bulk_load(slot, St + tile * D * D, Cfg::ST_BYTES, bfull + kb, pol_s);
-      }
-#pragma unroll
-      for (int r = lane; r < D; r += 32) {
-        const float zv = __ldg(zt + tile * D + r);
-        const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
-        *reinterpret_cast<uint32_t*>(slot + (D / 8) * Cfg::B_SBO + (r >> 3) * 128 + (r & 7) * 16) =
-            static_cast<uint32_t>(__bfloat16_as_ushort(hi)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bfull + kb);
-      ++fills;
-      if (++kb == Cfg::NB) { kb = 0; bph ^= 1u; }
-    }
+    // Two plain bulk copies per item: S~_i into the operand area and z~_i
+    // (float32) behind it.  Nothing here waits on a load, so the producer runs
+    // up to NB items ahead.
     if (lane == 0) {
+      const uint64_t pol_s = policy_evict_last();
+      int kb = 0;
+      uint32_t bph = 0;
+      uint64_t fills = 0;
+      for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int64_t h = item % g.H, rest = item / g.H;
+        const int64_t i = rest % g.M, b = rest / g.M;
+        const int64_t tile = (b * g.H + h) * g.M + i;
+        if (!wait_bounded(bempty + kb, bph ^ 1u, abortf)) break;
+        uint8_t* slot = bslot + kb * Cfg::BT;
+        mbar_arrive_expect_tx(bfull + kb, Cfg::ST_BYTES + Cfg::ZRAW);
+        bulk_load(slot, St + tile * D * D, Cfg::ST_BYTES, bfull + kb, pol_s);
+        bulk_load(slot + Cfg::BOPS, zt + tile * D, Cfg::ZRAW, bfull + kb, pol_s);
+        ++fills;
+        if (++kb == Cfg::NB) { kb = 0; bph ^= 1u; }
+      }
       for (int st = 0; st < Cfg::NB; ++st) {
         const uint64_t n = fills / Cfg::NB + (static_cast<uint64_t>(st) < fills % Cfg::NB ? 1 : 0);
         if (n > 0) drain_wait(bfull + st, static_cast<uint32_t>((n - 1) & 1));
       }
+    }
+  } else if (warp == 15) {
+    // ------------------------------------------- store issuer
+    // Chunks in order: once the epilogue has written a chunk's output tile,
+    // store it by TMA; a stage goes back to the q producer as soon as its
+    // store has read it (up to kOutStoresInFlight stores read at once).
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int pend[kOutStoresInFlight + 1];
+      int npend = 0;
+      bool ok = true;
+      for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const int32_t h = static_cast<int32_t>(item % g.H);
+        const int64_t rest = item / g.H;
+        const int32_t i = static_cast<int32_t>(rest % g.M), b = static_cast<int32_t>(rest / g.M);
+        for (int c = 0; c < g.chunks; ++c) {
+          if (!wait_bounded(ostore + s, ph, abortf)) { ok = false; break; }
+          int32_t x, y, z;
+          chunk_coords(g, i, c, b, x, y, z);
+          tma_store_5d(&tm_o, qst + s * Cfg::QT, 0, h, x, y, z);
+          bulk_commit_group();
+          pend[npend++] = s;
+          if (npend > kOutStoresInFlight) {
+            bulk_wait_group_read<kOutStoresInFlight>();   // the oldest store has read its tile
+            mbar_arrive(qempty + pend[0]);
+#pragma unroll
+            for (int e = 0; e < kOutStoresInFlight; ++e) pend[e] = pend[e + 1];
+            --npend;
+          }
+          if (++s == Cfg::NQ) { s = 0; ph ^= 1u; }
+        }
+      }
+      bulk_wait_group0();
     }
   } else if (warp == 1) {
     // ------------------------------------------- MMA issuer
@@ -743,17 +769,30 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       drain_wait(fin, 0);
     }
   } else if (warp < 6) {
-    // ------------------------------------------- phi on q
+    // ------------------------------------------- phi on q; the z~ columns of B
     constexpr int CPR = D / 8;            // 16-byte chunks per row
     constexpr int RP = 128 / CPR;         // rows covered per pass
     const int rt = threadIdx.x - 64;
     const int rg = rt / CPR, p = rt % CPR;
     const bool add_eps = phi_kind == MHLA_PHI_RELU_EPS;
     const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
-    int s = 0;
-    uint32_t ph = 0;
+    // thread rt < D owns row rt of z~_i: column D of B holds hi, column D+1 lo
+    const int zoff = (D / 8) * Cfg::B_SBO + (rt >> 3) * 128 + (rt & 7) * 16;
+    int s = 0, kb = 0;
+    uint32_t ph = 0, bph = 0;
     bool ok = true;
     for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      // the item's slot: S~_i and the float32 z~_i have landed (the producer runs ahead)
+      if (!warp_wait(bfull + kb, bph, abortf)) break;
+      if (rt < D) {
+        uint8_t* slot = bslot + kb * Cfg::BT;
+        const float zv = *reinterpret_cast<const float*>(slot + Cfg::BOPS + rt * 4);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
+        *reinterpret_cast<uint32_t*>(slot + zoff) =
+            static_cast<uint32_t>(__bfloat16_as_ushort(hi)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
+      }
+      if (++kb == Cfg::NB) { kb = 0; bph ^= 1u; }
       for (int c = 0; c < g.chunks; ++c) {
         if (!warp_wait(qfull + s, ph, abortf)) { ok = false; break; }
         uint8_t* tile = qst + s * Cfg::QT;
@@ -762,33 +801,28 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           uint4* ptr = reinterpret_cast<uint4*>(tile + (rg + RP * m) * Cfg::ROWB + p * 16);
           *ptr = phi8_packed(*ptr, add_eps, eps2);
         }
+        // also publishes this item's z~ columns to the MMA (first chunk)
         fence_proxy_async_smem();
         mbar_arrive(phid + s);
         if (++s == Cfg::NQ) { s = 0; ph ^= 1u; }
       }
     }
   } else {
-    // ------------------------------------------- epilogue: scale, write back, store by TMA
+    // ------------------------------------------- epilogue: scale and write back
     // Warpgroup wg (warps 6-9 or 10-13) takes the chunks with cnt % 2 == wg, which
     // are exactly the chunks accumulated in TMEM accumulator wg.
     const int wg = (warp - 6) >> 2;
     const int q4 = warp & 3;
     const int row = 32 * q4 + lane;      // token row of the chunk
-    const bool store_thread = ((warp - 6) & 3) == 0 && lane == 0;
     int s = 0;
     uint32_t ph = 0, cnt = 0;
     bool ok = true;
     for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-      const int32_t h = static_cast<int32_t>(item % g.H);
-      const int64_t rest = item / g.H;
-      const int32_t i = static_cast<int32_t>(rest % g.M), b = static_cast<int32_t>(rest / g.M);
       for (int c = 0; c < g.chunks; ++c, ++cnt) {
         const int cs = s;
-        const uint32_t cph = ph;
         if (++s == Cfg::NQ) { s = 0; ph ^= 1u; }
         if (static_cast<int>(cnt & 1u) != wg) continue;
-        const uint32_t k = cnt >> 1;                 // this warpgroup's chunk number
-        const uint32_t acc = wg, aph = k & 1u;
+        const uint32_t acc = wg, aph = (cnt >> 1) & 1u;
         if (!warp_wait(tfull + acc, aph, abortf)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tb = tmem + acc * Cfg::ACC_STRIDE + (static_cast<uint32_t>(32 * q4) << 16);
@@ -814,22 +848,8 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         }
         fence_proxy_async_smem();
         mbar_arrive(ostore + cs);
-        if (store_thread) {
-          if (wait_bounded(ostore + cs, cph, abortf)) {
-            int32_t x, y, z;
-            chunk_coords(g, i, c, b, x, y, z);
-            tma_store_5d(&tm_o, qst + cs * Cfg::QT, 0, h, x, y, z);
-            bulk_commit_group();
-            bulk_wait_group_read<0>();       // the stage is free once the store has read it
-          } else {
-            ok = false;
-          }
-          mbar_arrive(qempty + cs);
-        }
-        ok = __all_sync(0xffffffffu, ok);
       }
     }
-    if (store_thread) bulk_wait_group0();
   }
   tc_fence_before();
   __syncthreads();
