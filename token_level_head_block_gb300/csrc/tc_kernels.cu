@@ -384,9 +384,10 @@ struct MixCfg {
 };
 constexpr int kMixThreadsTC = 320;   // producer, MMA, two epilogue warpgroups taking alternate tiles
 
+template <int D>
 __global__ void __launch_bounds__(kMixThreadsTC, 1)
 tc_mix(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s, int32_t M,
-       int64_t ncols, int32_t n_col_tiles, int32_t n_i_tiles, int32_t d, __nv_bfloat16* __restrict__ St,
+       int64_t ncols, int32_t n_col_tiles, int32_t n_i_tiles, __nv_bfloat16* __restrict__ St,
        float* __restrict__ zt) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
@@ -493,10 +494,10 @@ tc_mix(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtenso
     }
   } else {
     // warpgroup wg (warps 2-5 or 6-9) drains accumulator wg: the tiles with local % 2 == wg
+    constexpr int32_t PER_BH = (D + 1) * D;            // Sbuf columns of one (b, h): d rows of S, then z
     const int wg = (warp - 2) >> 2;
     const int q4 = warp & 3;
     const int row = 32 * q4 + lane;                    // query block within the tile
-    const int64_t per_bh = static_cast<int64_t>(d + 1) * d;
     uint32_t local = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
       if (static_cast<int>(local & 1u) != wg) continue;
@@ -504,37 +505,39 @@ tc_mix(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtenso
       if (!warp_wait(tfull + acc, aph, abortf)) break;
       tc_fence_after();
       const int32_t i = static_cast<int32_t>(t % n_i_tiles) * MixCfg::ROWS + row;
-      const int64_t col0 = (t / n_i_tiles) * MixCfg::COLS;
+      const int32_t col0 = static_cast<int32_t>(t / n_i_tiles) * MixCfg::COLS;
+      // column col0 + cc is (bh, rem) with rem = rr * D + c: one division per tile
+      int32_t bh = col0 / PER_BH, rem = col0 - bh * PER_BH;
       const uint32_t tb = tmem + acc * MixCfg::ACC_STRIDE + (static_cast<uint32_t>(32 * q4) << 16);
 #pragma unroll 1
       for (int cc = 0; cc < MixCfg::COLS; cc += 32) {
         uint32_t v[32];
         tmem_ld_x32(tb + cc, v);
         tmem_ld_wait();
-        const int64_t col = col0 + cc;                 // 32 columns of one row of one (b, h)
-        if (i < M && col < ncols) {
-          const int64_t bh = col / per_bh, rem = col % per_bh;
-          const int64_t rr = rem / d, c0 = rem % d;
-          if (rr < d) {
+        if (i < M && col0 + cc < ncols) {
+          const int32_t rr = rem / D, c0 = rem % D;    // 32 columns of one row rr of one (b, h)
+          const int64_t tile_id = static_cast<int64_t>(bh) * M + i;
+          if (rr < D) {
             // S~_i tile in the output MMA's unswizzled MN-major layout: 16-byte
             // core-matrix rows (8 columns c of one row rr), 8 rows rr per core
             // matrix, core matrices of a column group 128 bytes apart along rr,
-            // column groups d*16 bytes apart.
-            __nv_bfloat16* tile = St + (bh * M + i) * d * d;
-            const int64_t rbase = (rr >> 3) * 64 + (rr & 7) * 8;
+            // column groups D*16 bytes apart.
+            __nv_bfloat16* tile = St + tile_id * D * D + (rr >> 3) * 64 + (rr & 7) * 8;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              *reinterpret_cast<uint4*>(tile + ((c0 >> 3) + q) * (d * 8) + rbase) =
+              *reinterpret_cast<uint4*>(tile + ((c0 >> 3) + q) * (D * 8)) =
                   make_uint4(pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
                              pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
                              pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
                              pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(zt + (bh * M + i) * d + c0);
+            uint4* dst = reinterpret_cast<uint4*>(zt + tile_id * D + c0);
 #pragma unroll
             for (int q = 0; q < 8; ++q) dst[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           }
         }
+        rem += 32;
+        if (rem >= PER_BH) { rem -= PER_BH; ++bh; }
       }
       tc_fence_before();
       mbar_arrive(tempty + acc);
@@ -1045,14 +1048,14 @@ int launch_tc_d(const Problem& p, const float* W, void* workspace, cudaStream_t 
     }
     const int32_t n_col_tiles = static_cast<int32_t>((L.ncols + MixCfg::COLS - 1) / MixCfg::COLS);
     const int32_t n_i_tiles = static_cast<int32_t>((p.M + MixCfg::ROWS - 1) / MixCfg::ROWS);
-    if (cudaFuncSetAttribute(tc_mix, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_mix<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(MixCfg::SMEM)) != cudaSuccess)
       return MHLA_ERR_CUDA;
     const int64_t n_tiles = static_cast<int64_t>(n_col_tiles) * n_i_tiles;
     const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
     KernelTimer timer("tc_mix", stream);
-    tc_mix<<<grid, kMixThreadsTC, MixCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), L.ncols, n_col_tiles,
-                                                           n_i_tiles, static_cast<int32_t>(p.d), St, zt);
+    tc_mix<D><<<grid, kMixThreadsTC, MixCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), L.ncols,
+                                                              n_col_tiles, n_i_tiles, St, zt);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
 
