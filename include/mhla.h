@@ -170,9 +170,11 @@ mhla_status_t mhla_forward(const mhla_tensor_t* q, const mhla_tensor_t* k,
  *   device (cudaGetSymbolAddress, with that device current); make that first
  *   call before any stream capture.
  *   Every call on a device shares the one array and leaves its contents
- *   behind; no part of it needs to start at zero, since each call writes every
- *   scratch byte before reading it.  Calls whose work overlaps on the GPU (two
- *   streams, or two threads) race on the array: order them on one stream. */
+ *   behind; no part of it needs to start at zero: a call writes every scratch
+ *   byte whose value reaches its results before reading it (padding it reads
+ *   unwritten only feeds outputs it discards).  Calls whose work overlaps on
+ *   the GPU (two streams, or two threads) race on the array: order them on one
+ *   stream. */
 #define MHLA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 mhla_status_t mhla_forward_noalloc(const mhla_tensor_t* q, const mhla_tensor_t* k,
                                    const mhla_tensor_t* v, const float* W,

@@ -52,10 +52,10 @@ int launch_simt(const Problem& p, const float* W, void* workspace, void* stream)
 
 // Workspace layout of the tensor-core path:
 //   Wb   bf16 [M][Mp]                  W rounded to bf16, Mp = round_up(M, 8)
-//   Sbuf bf16 [M][BH*(d+1)*d]           per source block j: for each (b,h) the
-//                                       d rows of S_j then the row z_j
-//   St   bf16 [BH][M][d*d]              S~_i in the output MMA's operand layout:
-//                                       element (r, c) at (c/8)*8d + (r/8)*64 + (r%8)*8 + c%8
+//   Sbuf bf16 [G][M][128]               columns col = (b,h) then the d rows of S_j
+//                                       then the row z_j, blocked by G groups of
+//                                       128 columns: (col/128, j, col%128)
+//   St   bf16 [BH][M][d][d]             S~_i row-major (r, c)
 //   zt   f32  [BH][M][d]                z~_i
 size_t tc_workspace_bytes(const Problem& p);
 bool tc_eligible(const Problem& p);

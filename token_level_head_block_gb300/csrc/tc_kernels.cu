@@ -154,7 +154,7 @@ constexpr int kTcThreads = 320;  // producer, MMA, 4 phi warps, 4 epilogue warps
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, TcGeom g,
-           int32_t G, int64_t n_items, int64_t ncols, int phi_kind, float eps,
+           int32_t G, int64_t n_items, int phi_kind, float eps,
            __nv_bfloat16* __restrict__ Sbuf, const float* __restrict__ W, __nv_bfloat16* __restrict__ Wb,
            int64_t Mp) {
   using Cfg = SumCfg<D>;
@@ -335,9 +335,12 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       const int32_t j = static_cast<int32_t>(rest % g.M), b = static_cast<int32_t>(rest / g.M);
       const int32_t h = grp * Cfg::HP + hh;
       if (h < g.H) {
-        __nv_bfloat16* dst = Sbuf + static_cast<int64_t>(j) * ncols +
-                             (static_cast<int64_t>(b) * g.H + h) * (D + 1) * D;
-        uint4* drow = reinterpret_cast<uint4*>(dst + r * D);
+        // Sbuf is blocked by groups of 128 columns: column col of source block j
+        // lives at ((col / 128) * M + j) * 128 + col % 128.  A row of D columns
+        // starting at a multiple of D stays inside one group.
+        const int64_t col = (static_cast<int64_t>(b) * g.H + h) * (D + 1) * D + r * D;
+        const int64_t grow = (col >> 7) * g.M + j;
+        uint4* drow = reinterpret_cast<uint4*>(Sbuf + grow * 128 + (col & 127));
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           drow[q] = make_uint4(pack_bf16(__uint_as_float(v0[8 * q]), __uint_as_float(v0[8 * q + 1])),
@@ -352,7 +355,8 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
                                      pack_bf16(__uint_as_float(v1[8 * q + 4]), __uint_as_float(v1[8 * q + 5])),
                                      pack_bf16(__uint_as_float(v1[8 * q + 6]), __uint_as_float(v1[8 * q + 7])));
         }
-        dst[D * D + r] = __float2bfloat16_rn(__uint_as_float(vz[0]));
+        const int64_t zcol = (static_cast<int64_t>(b) * g.H + h) * (D + 1) * D + D * D + r;
+        Sbuf[((zcol >> 7) * g.M + j) * 128 + (zcol & 127)] = __float2bfloat16_rn(__uint_as_float(vz[0]));
       }
     }
   }
@@ -449,9 +453,11 @@ tc_mix(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtenso
           uint8_t* st = stages + s * MixCfg::STAGE;
           tma_load_2d(st, &tm_w, full + s, kc * MixCfg::KC, i0, pol_w);
 #pragma unroll
-          for (int a = 0; a < MixCfg::COLS / 64; ++a)
-            tma_load_2d(st + MixCfg::A_BYTES + a * (MixCfg::KC * 128), &tm_s, full + s, col0 + 64 * a,
-                        kc * MixCfg::KC, pol_s);
+          for (int a = 0; a < MixCfg::COLS / 64; ++a) {
+            const int32_t col = col0 + 64 * a;                    // 64 columns inside one 128-column group
+            tma_load_3d(st + MixCfg::A_BYTES + a * (MixCfg::KC * 128), &tm_s, full + s, col & 127,
+                        kc * MixCfg::KC, col >> 7, pol_s);
+          }
           ++fills;
           if (++s == MixCfg::NS) { s = 0; ph ^= 1u; }
         }
@@ -518,14 +524,10 @@ tc_mix(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtenso
           const int32_t rr = rem / D, c0 = rem % D;    // 32 columns of one row rr of one (b, h)
           const int64_t tile_id = static_cast<int64_t>(bh) * M + i;
           if (rr < D) {
-            // S~_i tile in the output MMA's unswizzled MN-major layout: 16-byte
-            // core-matrix rows (8 columns c of one row rr), 8 rows rr per core
-            // matrix, core matrices of a column group 128 bytes apart along rr,
-            // column groups D*16 bytes apart.
-            __nv_bfloat16* tile = St + tile_id * D * D + (rr >> 3) * 64 + (rr & 7) * 8;
+            __nv_bfloat16* tile = St + tile_id * D * D + rr * D + c0;     // S~_i row-major
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              *reinterpret_cast<uint4*>(tile + ((c0 >> 3) + q) * (D * 8)) =
+              *reinterpret_cast<uint4*>(tile + q * 8) =
                   make_uint4(pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
                              pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
                              pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
@@ -548,6 +550,194 @@ tc_mix(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtenso
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, MixCfg::TMEM_COLS);
+  }
+}
+
+// ============================================================================
+// tc_mix_resident: the same GEMM for M <= 256 with all of W (bf16, <= 128 KB)
+// resident in shared memory.  One tile = 128 Sbuf columns x all query blocks:
+// every Sbuf panel is read exactly once, and per 16 source blocks one MMA per
+// 128-row query tile writes its own TMEM accumulator.  Epilogue warpgroup w
+// drains query tile w; accumulator sets alternate between tiles.
+// ============================================================================
+struct MixResCfg {
+  static constexpr int ROWS = 128;                // query blocks per MMA (M)
+  static constexpr int COLS = 128;                // Sbuf columns per tile (N)
+  static constexpr int KC = 64;                   // source blocks per stage
+  static constexpr int W_CHUNK = ROWS * KC * 2;   // one (query tile, 64 source blocks) W chunk
+  static constexpr int W_BYTES = 2 * 4 * W_CHUNK; // up to 256 x 256
+  static constexpr int STAGE = KC * COLS * 2;     // Sbuf chunk: two 64-column MN-major chunks
+  static constexpr int NS = 6;
+  static constexpr int SET = 2 * COLS;            // TMEM columns of one accumulator set (2 query tiles)
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int CTRL = 1024;
+  static constexpr size_t SMEM = static_cast<size_t>(W_BYTES) + static_cast<size_t>(NS) * STAGE + CTRL + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kMixThreadsTC, 1)
+tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s, int32_t M,
+                int64_t ncols, int32_t n_tiles, __nv_bfloat16* __restrict__ St, float* __restrict__ zt) {
+  using Cfg = MixResCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
+  uint8_t* wres = smem;                                  // [query tile][k chunk] W, K-major
+  uint8_t* stages = smem + Cfg::W_BYTES;
+  uint8_t* ctrl = stages + Cfg::NS * Cfg::STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + Cfg::NS;
+  uint64_t* tfull = empty + Cfg::NS;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* wfull = tempty + 2;
+  uint64_t* fin = wfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 512);
+  volatile uint32_t* abortf = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_it = (M + Cfg::ROWS - 1) / Cfg::ROWS;     // 1 or 2 query tiles
+  const int nk = (M + Cfg::KC - 1) / Cfg::KC;           // 1..4 source chunks
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::NS; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull + a, 1);
+      mbar_init(tempty + a, 256);
+    }
+    mbar_init(wfull, 1);
+    mbar_init(fin, 1);
+    *abortf = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_s);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_last();
+      const uint64_t pol_s = policy_evict_first();
+      // all of W once
+      mbar_arrive_expect_tx(wfull, static_cast<uint32_t>(n_it * nk * Cfg::W_CHUNK));
+      for (int it = 0; it < n_it; ++it)
+        for (int kc = 0; kc < nk; ++kc)
+          tma_load_2d(wres + (it * 4 + kc) * Cfg::W_CHUNK, &tm_w, wfull, kc * Cfg::KC, it * Cfg::ROWS, pol_w);
+      int s = 0;
+      uint32_t ph = 0;
+      uint64_t fills = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!wait_bounded(empty + s, ph ^ 1u, abortf)) { ok = false; break; }
+          mbar_arrive_expect_tx(full + s, Cfg::STAGE);
+          uint8_t* st = stages + s * Cfg::STAGE;
+          // one 128-column group of Sbuf, rows j contiguous; rows j >= M read as zeros
+          tma_load_3d(st, &tm_s, full + s, 0, kc * Cfg::KC, static_cast<int32_t>(t), pol_s);
+          tma_load_3d(st + Cfg::STAGE / 2, &tm_s, full + s, 64, kc * Cfg::KC, static_cast<int32_t>(t), pol_s);
+          ++fills;
+          if (++s == Cfg::NS) { s = 0; ph ^= 1u; }
+        }
+      }
+      drain_wait(wfull, 0);
+      for (int st = 0; st < Cfg::NS; ++st) {
+        const uint64_t n = fills / Cfg::NS + (static_cast<uint64_t>(st) < fills % Cfg::NS ? 1 : 0);
+        if (n > 0) drain_wait(full + st, static_cast<uint32_t>((n - 1) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(Cfg::ROWS, Cfg::COLS, /*a K-major*/ false, /*b MN-major*/ true);
+      int s = 0;
+      uint32_t ph = 0, local = 0;
+      bool ok = wait_bounded(wfull, 0, abortf);
+      tc_fence_after();
+      const uint32_t wbase = smem_u32(wres);
+      for (int64_t t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++local) {
+        const uint32_t set = local & 1u, sph = (local >> 1) & 1u;
+        if (!wait_bounded(tempty + set, sph ^ 1u, abortf)) break;
+        tc_fence_after();
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!wait_bounded(full + s, ph, abortf)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t base = smem_u32(stages + s * Cfg::STAGE);
+#pragma unroll
+          for (int ks = 0; ks < Cfg::KC / 16; ++ks) {
+            const uint64_t b = smem_desc(base + ks * 2048, Cfg::STAGE / 2, 1024, 2);
+            for (int it = 0; it < n_it; ++it) {
+              const uint64_t a = smem_desc(wbase + (it * 4 + kc) * Cfg::W_CHUNK + ks * 32, 16, 1024, 2);
+              mma_bf16(tmem + set * Cfg::SET + it * Cfg::COLS, a, b, idesc, (kc | ks) != 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(empty + s);
+          if (++s == Cfg::NS) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(tfull + set);
+      }
+      mma_commit(fin);
+      drain_wait(fin, 0);
+    }
+  } else {
+    // warpgroup wg (warps 2-5 or 6-9) drains query tile wg of every accumulator set
+    constexpr int32_t PER_BH = (D + 1) * D;            // Sbuf columns of one (b, h): d rows of S, then z
+    const int wg = (warp - 2) >> 2;
+    const int q4 = warp & 3;
+    const int32_t i = wg * Cfg::ROWS + 32 * q4 + lane;  // this thread's query block
+    uint32_t local = 0;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
+      const uint32_t set = local & 1u, sph = (local >> 1) & 1u;
+      if (!warp_wait(tfull + set, sph, abortf)) break;
+      tc_fence_after();
+      if (wg < n_it) {
+        const int32_t col0 = static_cast<int32_t>(t) * Cfg::COLS;
+        int32_t bh = col0 / PER_BH, rem = col0 - bh * PER_BH;
+        const uint32_t tb = tmem + set * Cfg::SET + wg * Cfg::COLS + (static_cast<uint32_t>(32 * q4) << 16);
+#pragma unroll 1
+        for (int cc = 0; cc < Cfg::COLS; cc += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(tb + cc, v);
+          tmem_ld_wait();
+          if (i < M && col0 + cc < ncols) {
+            const int32_t rr = rem / D, c0 = rem % D;
+            const int64_t tile_id = static_cast<int64_t>(bh) * M + i;
+            if (rr < D) {
+              __nv_bfloat16* tile = St + tile_id * D * D + rr * D + c0;   // S~_i row-major
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(tile + q * 8) =
+                    make_uint4(pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                               pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                               pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                               pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(zt + tile_id * D + c0);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) dst[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+          }
+          rem += 32;
+          if (rem >= PER_BH) { rem -= PER_BH; ++bh; }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty + set);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::TMEM_COLS);
   }
 }
 
@@ -596,8 +786,8 @@ constexpr int kOutStoresInFlight = 3;   // TMA stores allowed to be reading shar
 
 template <int D>
 __global__ void __launch_bounds__(kOutThreadsTC, 1)
-tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o, TcGeom g,
-          int64_t n_items, int phi_kind, float eps, const __nv_bfloat16* __restrict__ St,
+tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+          const __grid_constant__ CUtensorMap tm_st, TcGeom g, int64_t n_items, int phi_kind, float eps,
           const float* __restrict__ zt) {
   using Cfg = OutCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -640,6 +830,7 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_o);
+    prefetch_tmap(&tm_st);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -679,8 +870,10 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     }
   } else if (warp == 14) {
     // ------------------------------------------- B producer: one slot per item
-    // Two plain bulk copies per item: S~_i into the operand area and z~_i
-    // (float32) behind it.  Nothing here waits on a load, so the producer runs
+    // Per item: S~_i (row-major in global memory) through a 4-D tensor view
+    // (c % 8, r, c / 8, tile) whose box lands exactly in the unswizzled
+    // MN-major core-matrix layout the MMA reads, and z~_i (float32) by a plain
+    // bulk copy behind it.  Nothing here waits on a load, so the producer runs
     // up to NB items ahead.
     if (lane == 0) {
       const uint64_t pol_s = policy_evict_last();
@@ -694,7 +887,7 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         if (!wait_bounded(bempty + kb, bph ^ 1u, abortf)) break;
         uint8_t* slot = bslot + kb * Cfg::BT;
         mbar_arrive_expect_tx(bfull + kb, Cfg::ST_BYTES + Cfg::ZRAW);
-        bulk_load(slot, St + tile * D * D, Cfg::ST_BYTES, bfull + kb, pol_s);
+        tma_load_4d(slot, &tm_st, bfull + kb, 0, 0, 0, static_cast<int32_t>(tile), pol_s);
         bulk_load(slot + Cfg::BOPS, zt + tile * D, Cfg::ZRAW, bfull + kb, pol_s);
         ++fills;
         if (++kb == Cfg::NB) { kb = 0; bph ^= 1u; }
@@ -946,18 +1139,19 @@ bool operand_map(const Problem& p, const Operand& o, int64_t box_y, int64_t box_
 
 struct TcLayout {
   size_t wb_off, sbuf_off, st_off, zt_off, total;
-  int64_t Mp, ncols;
+  int64_t Mp, ncols, ngroups;
 };
 
 TcLayout tc_layout(const Problem& p) {
   TcLayout L;
   L.Mp = (p.M + 7) / 8 * 8;
   L.ncols = p.BH() * (p.d + 1) * p.d;
+  L.ngroups = (L.ncols + 127) / 128;                    // Sbuf column groups of 128
   size_t off = 0;
   L.wb_off = off;
   off += align_up(static_cast<size_t>(p.M) * L.Mp * 2);
   L.sbuf_off = off;
-  off += align_up(static_cast<size_t>(p.M) * L.ncols * 2);
+  off += align_up(static_cast<size_t>(p.M) * L.ngroups * 128 * 2);
   L.st_off = off;
   off += align_up(static_cast<size_t>(p.BH()) * p.M * p.d * p.d * 2);
   L.zt_off = off;
@@ -1026,13 +1220,37 @@ int launch_tc_d(const Problem& p, const float* W, void* workspace, cudaStream_t 
     const int per_sm = std::max(1, occupancy(tc_summary<D>, kTcThreads, Cfg::SMEM));
     const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
     KernelTimer timer("tc_summary", stream);
-    tc_summary<D><<<grid, kTcThreads, Cfg::SMEM, stream>>>(tk, tv, make_geom(p, c64), G, n_items, L.ncols,
+    tc_summary<D><<<grid, kTcThreads, Cfg::SMEM, stream>>>(tk, tv, make_geom(p, c64), G, n_items,
                                                            p.phi_kind, p.eps, Sbuf, W, Wb, L.Mp);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
 
-  // ---- step 2: mixing GEMM
-  {
+  // ---- step 2: mixing GEMM (all of W in shared memory when M <= 256)
+  if (p.M <= 256) {
+    CUtensorMap tw, ts;
+    {
+      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.M)};
+      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.Mp * 2)};
+      const cuuint32_t box[2] = {static_cast<cuuint32_t>(MixResCfg::KC), static_cast<cuuint32_t>(MixResCfg::ROWS)};
+      if (!encode(&tw, 2, Wb, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
+    }
+    {
+      // Sbuf as (128 columns, M source blocks, G groups)
+      const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(L.ngroups)};
+      const cuuint64_t strides[2] = {256u, static_cast<cuuint64_t>(p.M * 256)};
+      const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(MixResCfg::KC), 1u};
+      if (!encode(&ts, 3, Sbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
+    }
+    const int32_t n_tiles = static_cast<int32_t>((L.ncols + MixResCfg::COLS - 1) / MixResCfg::COLS);
+    if (cudaFuncSetAttribute(tc_mix_resident<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(MixResCfg::SMEM)) != cudaSuccess)
+      return MHLA_ERR_CUDA;
+    const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
+    KernelTimer timer("tc_mix", stream);
+    tc_mix_resident<D><<<grid, kMixThreadsTC, MixResCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), L.ncols,
+                                                                          n_tiles, St, zt);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  } else {
     CUtensorMap tw, ts;
     {
       const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.M)};
@@ -1041,10 +1259,11 @@ int launch_tc_d(const Problem& p, const float* W, void* workspace, cudaStream_t 
       if (!encode(&tw, 2, Wb, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
     }
     {
-      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.ncols), static_cast<cuuint64_t>(p.M)};
-      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.ncols * 2)};
-      const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(MixCfg::KC)};
-      if (!encode(&ts, 2, Sbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
+      // Sbuf as (128 columns, M source blocks, G groups)
+      const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(L.ngroups)};
+      const cuuint64_t strides[2] = {256u, static_cast<cuuint64_t>(p.M * 256)};
+      const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(MixCfg::KC), 1u};
+      if (!encode(&ts, 3, Sbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
     }
     const int32_t n_col_tiles = static_cast<int32_t>((L.ncols + MixCfg::COLS - 1) / MixCfg::COLS);
     const int32_t n_i_tiles = static_cast<int32_t>((p.M + MixCfg::ROWS - 1) / MixCfg::ROWS);
@@ -1065,6 +1284,17 @@ int launch_tc_d(const Problem& p, const float* W, void* workspace, cudaStream_t 
     CUtensorMap tq, to;
     if (!operand_map(p, p.q, c128.box_y, c128.box_t, &tq) || !operand_map(p, p.o, c128.box_y, c128.box_t, &to))
       return MHLA_ERR_CUDA;
+    // S~ tiles (row-major [BH*M][d][d]) seen as (c % 8, r, c / 8, tile): a
+    // (8, d, d/8, 1) box lands as 16-byte rows of 8 columns, d rows per column
+    // group: the unswizzled MN-major operand layout.
+    CUtensorMap tst;
+    {
+      const cuuint64_t dims[4] = {8u, static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(p.d / 8),
+                                  static_cast<cuuint64_t>(p.BH() * p.M)};
+      const cuuint64_t strides[3] = {static_cast<cuuint64_t>(p.d * 2), 16u, static_cast<cuuint64_t>(p.d * p.d * 2)};
+      const cuuint32_t box[4] = {8u, static_cast<cuuint32_t>(p.d), static_cast<cuuint32_t>(p.d / 8), 1u};
+      if (!encode(&tst, 4, St, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return MHLA_ERR_CUDA;
+    }
     const int64_t n_items = p.BH() * p.M;
     if (cudaFuncSetAttribute(tc_output<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Cfg::SMEM)) != cudaSuccess)
@@ -1073,8 +1303,8 @@ int launch_tc_d(const Problem& p, const float* W, void* workspace, cudaStream_t 
         std::max(1, std::min(occupancy(tc_output<D>, kOutThreadsTC, Cfg::SMEM), 512 / Cfg::TMEM_COLS));
     const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
     KernelTimer timer("tc_output", stream);
-    tc_output<D><<<grid, kOutThreadsTC, Cfg::SMEM, stream>>>(tq, to, make_geom(p, c128), n_items, p.phi_kind, p.eps,
-                                                          St, zt);
+    tc_output<D><<<grid, kOutThreadsTC, Cfg::SMEM, stream>>>(tq, to, tst, make_geom(p, c128), n_items, p.phi_kind,
+                                                              p.eps, zt);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
   return MHLA_OK;
