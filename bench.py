@@ -178,6 +178,7 @@ def kernel_work(wl, name):
         "tc_summary": ("hbm", 2 * io), "simt_summary": ("hbm", 2 * io),
         "tc_output": ("hbm", 2 * io), "simt_output": ("hbm", 2 * io),
         "tc_mix": ("tensor", 2 * M * M * BH * d * (d + 1)), "simt_mix": ("alu", 2 * M * M * BH * d * (d + 1)),
+        "tc_small": ("hbm", 4 * io),
     }
     return table.get(name, ("hbm", 0))
 

@@ -65,10 +65,25 @@ typedef enum mhla_phi_kind {
     MHLA_PHI_RELU_EPS = 1   /* phi(x) = max(x, 0) + eps, as the [P1] module does */
 } mhla_phi_kind_t;
 
-/* Which kernels run.  AUTO picks the tensor-core path whenever the request is
- * eligible for it (bf16, d in {32, 64}, tokens per block a multiple of 128, TMA
- * friendly strides) and the CUDA-core path otherwise. */
-typedef enum mhla_path { MHLA_PATH_AUTO = 0, MHLA_PATH_SIMT = 1, MHLA_PATH_TC = 2 } mhla_path_t;
+/* Which kernels run.  AUTO takes, in this order, the first path the request is
+ * eligible for:
+ *   FUSED  one tensor-core launch for short sequences: bf16, d in {32, 64},
+ *          N <= 256 tokens, M <= 96 blocks, strides multiples of 8 elements,
+ *          16-byte aligned bases.  It forms the same result through the
+ *          two-stage form o_t = sum_s P[t][s] v_s / (sum_s P[t][s] + eps),
+ *          P[t][s] = W[b(t)][b(s)] phi(q_t) . phi(k_s) ([P2] section 4
+ *          "Multi-Head Mixing"; [P1] section 5(4)), needs no workspace and
+ *          suits grids with many small blocks (M^2 comparable to N).
+ *   TC     three tensor-core launches (summaries, mixing GEMM, readout): bf16,
+ *          d in {32, 64}, tokens per block a multiple of 128 in whole block
+ *          rows, TMA friendly strides.
+ *   SIMT   CUDA cores, any supported request (float32 included). */
+typedef enum mhla_path {
+    MHLA_PATH_AUTO = 0,
+    MHLA_PATH_SIMT = 1,
+    MHLA_PATH_TC = 2,
+    MHLA_PATH_FUSED = 3
+} mhla_path_t;
 
 /* Token grid or block shape, slowest axis first: (Y, X) when ndim == 2,
  * (T, Y, X) when ndim == 3.  Unused extents are ignored. */
@@ -116,8 +131,9 @@ mhla_status_t mhla_init_mixing(const mhla_shape3_t* grid, const mhla_shape3_t* b
 mhla_status_t mhla_workspace_size(const mhla_tensor_t* q, const mhla_shape3_t* grid,
                                   const mhla_shape3_t* block, int32_t path, size_t* bytes);
 
-/* The path AUTO would take for this problem (MHLA_PATH_SIMT or MHLA_PATH_TC),
- * or a negative status when the problem is invalid.  Host only. */
+/* The path AUTO would take for this problem (MHLA_PATH_SIMT, MHLA_PATH_TC or
+ * MHLA_PATH_FUSED), or a negative status when the problem is invalid.  Host
+ * only. */
 int32_t mhla_select_path(const mhla_tensor_t* q, const mhla_tensor_t* k,
                          const mhla_tensor_t* v, const mhla_tensor_t* out,
                          const mhla_shape3_t* grid, const mhla_shape3_t* block);
@@ -182,9 +198,10 @@ mhla_status_t mhla_forward_noalloc(const mhla_tensor_t* q, const mhla_tensor_t* 
                                    const mhla_phi_t* phi, const mhla_tensor_t* out,
                                    void* stream, int32_t path);
 
-/* Reads and clears the device error word the tensor-core kernels set when one
- * of their bounded waits gives up (bit 0: pipeline wait timeout).  Synchronises
- * stream.  *flags receives the word; returns MHLA_ERR_TIMEOUT when it was
+/* Reads and clears the device error words the tensor-core and fused kernels
+ * set when one of their bounded waits gives up (bit 0: pipeline wait timeout;
+ * bit 1: a copy or MMA still in flight when the kernel gave up did not finish
+ * within its drain limit).  Synchronises stream.  *flags receives the word; returns MHLA_ERR_TIMEOUT when it was
  * non-zero, MHLA_ERR_CUDA when the copy failed. */
 mhla_status_t mhla_device_status(void* stream, uint32_t* flags);
 

@@ -134,9 +134,10 @@ def test_forward_rejects_malformed_requests_before_any_launch(L):
     assert call_forward(L, bad, bad, bad, contig(2, 256, 3, 200, base=o.data), grid, block) == INVALID
     o_overlap = mhla.tensor_desc(o.data, "bf16", (2, 256, 3, 64), (256 * 3 * 64, 3 * 64, 32))
     assert call_forward(L, q, k, v, o_overlap, grid, block) == INVALID    # heads overlap in out
-    assert call_forward(L, q, k, v, o, grid, block, ws=FAKE + 7, ws_bytes=1 << 30) == WORKSPACE  # misaligned
-    assert call_forward(L, q, k, v, o, grid, block, ws=FAKE, ws_bytes=16) == WORKSPACE          # too small
-    assert call_forward(L, q, k, v, o, grid, block, ws=None, ws_bytes=16) == WORKSPACE          # bytes w/o pointer
+    for path in (0, 1, 3):   # auto (the fused path here, which needs no workspace), CUDA cores, fused
+        assert call_forward(L, q, k, v, o, grid, block, ws=FAKE + 7, ws_bytes=1 << 30, path=path) == WORKSPACE
+        assert call_forward(L, q, k, v, o, grid, block, ws=None, ws_bytes=16, path=path) == WORKSPACE
+    assert call_forward(L, q, k, v, o, grid, block, ws=FAKE, ws_bytes=16, path=1) == WORKSPACE  # too small
     assert call_forward(L, q, k, v, o, grid, block, path=9) == INVALID                          # unknown path
 
 
@@ -145,6 +146,19 @@ def test_forward_explicit_tensor_core_path_refuses_ineligible_problems(L):
     assert call_forward(L, q, k, v, o, (14, 14), (2, 2), path=2) == UNSUPPORTED
     q, k, v, o = four(1, 256, 1, 32, "f32")                         # fp32 runs on CUDA cores only
     assert call_forward(L, q, k, v, o, (16, 16), (16, 16), path=2) == UNSUPPORTED
+
+
+def test_forward_explicit_fused_path_refuses_ineligible_problems(L):
+    q, k, v, o = four(1, 1024, 2, 64)                               # more than 256 tokens
+    assert call_forward(L, q, k, v, o, (32, 32), (16, 8), path=3) == UNSUPPORTED
+    q, k, v, o = four(1, 256, 2, 64)                                # M = 128 > 96 blocks
+    assert call_forward(L, q, k, v, o, (16, 16), (1, 2), path=3) == UNSUPPORTED
+    q, k, v, o = four(1, 196, 3, 48)                                # d = 48
+    assert call_forward(L, q, k, v, o, (14, 14), (2, 2), path=3) == UNSUPPORTED
+    q, k, v, o = four(1, 196, 3, 64, "f32")                         # float32
+    assert call_forward(L, q, k, v, o, (14, 14), (2, 2), path=3) == UNSUPPORTED
+    ts = [mhla.tensor_desc(t.data, "bf16", (1, 196, 3, 64), (196 * 3 * 68, 3 * 68, 68)) for t in four(1, 196, 3, 64)]
+    assert call_forward(L, *ts, (14, 14), (2, 2), path=3) == UNSUPPORTED   # strides break the 16-byte rule
 
 
 def test_empty_batch_is_a_no_op(L):
@@ -163,25 +177,35 @@ def select(L, q, grid, block, strides=None):
 
 
 def test_path_selection(L):
-    TC, SIMT = 2, 1
+    SIMT, TC, FUSED = 1, 2, 3
     for name in ("dit_s2_4096px", "sana_4096px", "video_20x32x32", "sweep_64x64", "sweep_512x512"):
         wl = WORKLOADS[name]
         assert select(L, (wl.B, wl.N, wl.H, wl.d), wl.grid, wl.block) == TC, name
-    wl = WORKLOADS["deit_t_14x14"]
-    assert select(L, (wl.B, wl.N, wl.H, wl.d), wl.grid, wl.block) == SIMT
+    wl = WORKLOADS["deit_t_14x14"]                   # 196 tokens, 49 blocks: one fused launch
+    assert select(L, (wl.B, wl.N, wl.H, wl.d), wl.grid, wl.block) == FUSED
     wl = WORKLOADS["tiny_16x16_fp32"]
     assert select(L, (wl.B, wl.N, wl.H, wl.d, "f32"), wl.grid, wl.block) == SIMT
-    # d = 48 has no tensor-core kernel; 64-token blocks cannot fill a 128-row tile.
+    # short sequences take the fused kernel even where the three-launch path applies
+    assert select(L, (1, 256, 2, 64), (16, 16), (16, 16)) == FUSED
+    assert select(L, (2, 37, 1, 32), (1, 37), (1, 1)) == FUSED
+    # d = 48 has no tensor-core kernel; 64-token blocks cannot fill a 128-row tile;
+    # 128 blocks of 2 tokens exceed the fused kernel's 96 blocks.
     assert select(L, (1, 256, 2, 48), (16, 16), (16, 16)) == SIMT
-    assert select(L, (1, 256, 2, 64), (16, 16), (8, 8)) == SIMT
+    assert select(L, (1, 1024, 2, 64), (32, 32), (8, 8)) == SIMT
+    assert select(L, (1, 256, 2, 64), (16, 16), (1, 2)) == SIMT
     # strides that break TMA's 16-byte rule fall back to CUDA cores
     assert select(L, (1, 256, 2, 64), (16, 16), (16, 16), strides=(256 * 2 * 68, 2 * 68, 68)) == SIMT
     # q, k, v taken as slices of one [B, N, 3, H, d] projection still qualify
-    st = (256 * 3 * 2 * 64, 3 * 2 * 64, 64)
-    q, k, v = (mhla.tensor_desc(FAKE + 2 * i * 2 * 64, "bf16", (2, 256, 2, 64), st) for i in range(3))
-    o = contig(2, 256, 2, 64, base=FAKE + (1 << 30))
-    assert L.mhla_select_path(*(ctypes.byref(t) for t in (q, k, v, o)), ctypes.byref(mhla.shape3((16, 16))),
-                              ctypes.byref(mhla.shape3((16, 16)))) == TC
+    st = (512 * 3 * 2 * 64, 3 * 2 * 64, 64)
+    q, k, v = (mhla.tensor_desc(FAKE + 2 * i * 2 * 64, "bf16", (2, 512, 2, 64), st) for i in range(3))
+    o = contig(2, 512, 2, 64, base=FAKE + (1 << 30))
+    assert L.mhla_select_path(*(ctypes.byref(t) for t in (q, k, v, o)), ctypes.byref(mhla.shape3((16, 32))),
+                              ctypes.byref(mhla.shape3((16, 8)))) == TC
+    st = (196 * 3 * 3 * 64, 3 * 3 * 64, 64)
+    q, k, v = (mhla.tensor_desc(FAKE + 2 * i * 3 * 64, "bf16", (2, 196, 3, 64), st) for i in range(3))
+    o = contig(2, 196, 3, 64, base=FAKE + (1 << 30))
+    assert L.mhla_select_path(*(ctypes.byref(t) for t in (q, k, v, o)), ctypes.byref(mhla.shape3((14, 14))),
+                              ctypes.byref(mhla.shape3((2, 2)))) == FUSED
 
 
 def test_workspace_sizes(L):
@@ -196,3 +220,9 @@ def test_workspace_sizes(L):
     assert L.mhla_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
                                  ctypes.byref(mhla.shape3(wl.block)), 1, ctypes.byref(n)) == OK
     assert n.value >= 2 * BH * M * d * (d + 1) * 4
+    wl = WORKLOADS["deit_t_14x14"]                     # the fused path needs no workspace
+    q = contig(wl.B, wl.N, wl.H, wl.d)
+    for path in (0, 3):
+        assert L.mhla_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
+                                     ctypes.byref(mhla.shape3(wl.block)), path, ctypes.byref(n)) == OK
+        assert n.value == 0

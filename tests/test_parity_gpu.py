@@ -114,6 +114,57 @@ def test_simt_path_fp32_small(name, phi):
     check_full(f"simt_f32/{name}/{phi}", q, k, v, W, grid, block, "f32", phi, 1e-6, "simt")
 
 
+# Fused short-sequence path: N <= 256 tokens, M <= 96 blocks.  Cases cover one
+# and two query tiles, a ragged last key chunk (N not a multiple of 32), a single
+# token, one block, one block per token, the 96-block limit, 3-D grids and both d.
+FUSED_CASES = {
+    "deit_like_d64": (3, 3, 64, (14, 14), (2, 2)),
+    "n1_d64": (2, 1, 64, (1, 1), (1, 1)),
+    "n37_d64_w1": (2, 2, 64, (1, 37), (1, 1)),
+    "n100_d32": (2, 3, 32, (10, 10), (2, 5)),
+    "n128_d32": (2, 2, 32, (8, 16), (4, 4)),
+    "n129_d64": (1, 2, 64, (3, 43), (3, 1)),
+    "n250_d32": (1, 2, 32, (10, 25), (5, 5)),
+    "n256_d64_m1": (1, 2, 64, (16, 16), (16, 16)),
+    "m96_d64": (1, 1, 64, (12, 16), (2, 1)),
+    "3d_d64": (2, 2, 64, (4, 6, 8), (2, 3, 2)),
+    "3d_d32": (1, 3, 32, (3, 8, 8), (1, 4, 4)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FUSED_CASES))
+@pytest.mark.parametrize("phi", ["relu", "relu_eps"])
+def test_fused_path_small(name, phi):
+    B, H, d, grid, block = FUSED_CASES[name]
+    N = int(np.prod(grid))
+    q, k, v = draw_qkv(B, N, H, d, seed=31, dtype="bf16")
+    M = oracle.num_blocks(grid, block)
+    W = draw_matrix(M, seed=32)                  # asymmetric: a transposed W would show
+    check_full(f"fused/{name}/{phi}", q, k, v, W, grid, block, "bf16", phi, 1e-6, "fused")
+
+
+def test_fused_path_takes_slices_of_one_projection_and_is_deterministic():
+    B, N, H, d, grid, block = 2, 196, 3, 64, (14, 14), (2, 2)
+    qkv = draw_qkv(B, N, 3 * H, d, seed=33)[0].view(B, N, 3, H, d)
+    W = mhla.init_mixing(grid, block, "linear")
+    qd, Wd = qkv.to(DEV), torch.from_numpy(W).to(DEV)
+    outs = [mhla.forward(qd[:, :, 0], qd[:, :, 1], qd[:, :, 2], Wd, grid, block, path="fused") for _ in range(2)]
+    torch.cuda.synchronize()
+    assert mhla.device_status() == 0
+    assert torch.equal(outs[0], outs[1])
+    ref = oracle.forward(as_f64(qkv[:, :, 0]), as_f64(qkv[:, :, 1]), as_f64(qkv[:, :, 2]), W, grid, block)
+    assert normwise(as_f64(outs[0].cpu()), ref) <= TOL["bf16"]
+
+
+def test_fused_path_agrees_with_the_three_launch_path():
+    B, H, d, grid, block = 2, 3, 64, (16, 16), (16, 8)
+    q, k, v = draw_qkv(B, 256, H, d, seed=34)
+    W = mhla.init_mixing(grid, block, "cos")
+    a = run(q, k, v, W, grid, block, path="fused").cpu()
+    b = run(q, k, v, W, grid, block, path="tc").cpu()
+    assert normwise(as_f64(a), as_f64(b)) <= TOL["bf16"]
+
+
 def test_tiny_fp32_workload():
     wl = WORKLOADS["tiny_16x16_fp32"]
     q, k, v = draw_workload(wl)
@@ -181,7 +232,7 @@ def test_workload_w_matches_oracle_bitwise_at_large_m():
 
 # ------------------------------------------------------------------ edge cases
 
-@pytest.mark.parametrize("path", ["tc", "simt"])
+@pytest.mark.parametrize("path", ["tc", "simt", "fused"])
 def test_zero_query_rows_give_zero(path):
     B, H, d, grid, block = 1, 2, 64, (16, 16), (16, 8)
     q, k, v = draw_qkv(B, 256, H, d, seed=21)
@@ -192,7 +243,7 @@ def test_zero_query_rows_give_zero(path):
     assert torch.all(out[0, 5, 1] == 0) and torch.all(out[0, 200, 0] == 0)
 
 
-@pytest.mark.parametrize("path", ["tc", "simt"])
+@pytest.mark.parametrize("path", ["tc", "simt", "fused"])
 def test_constant_values_give_weighted_mean(path):
     B, H, d, grid, block = 1, 2, 64, (16, 16), (16, 8)
     q, k, _ = draw_qkv(B, 256, H, d, seed=22)
@@ -257,6 +308,7 @@ def test_profile_reports_every_kernel():
     mhla.profile_begin()
     run(q, k, v, W, grid, block, path="tc")
     run(q, k, v, W, grid, block, path="simt")
+    run(q, k, v, W, grid, block, path="fused")
     prof = mhla.profile_end()
-    for name in ("tc_summary", "tc_mix", "tc_output", "simt_summary", "simt_mix", "simt_output"):
+    for name in ("tc_summary", "tc_mix", "tc_output", "simt_summary", "simt_mix", "simt_output", "tc_small"):
         assert prof[name][0] == 1 and prof[name][1] > 0.0, name

@@ -76,14 +76,14 @@ def test_noalloc_matches_regular_entry_point_twice_in_a_row(case):
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
-    # 64 x 3 heads of a 14 x 14 grid with 2 x 2 blocks runs on CUDA cores with
-    # float32 summaries: about 313 MB of scratch, far above the 64 MiB array.
+    # 64 x 3 heads of a 14 x 14 grid with 2 x 2 blocks on the CUDA-core path
+    # keep float32 summaries: about 313 MB of scratch, far above the 64 MiB array.
     B, H, d, grid, block = 64, 3, 64, (14, 14), (2, 2)
     q = torch.randn(B, 196, H, d, device=DEV).to(torch.bfloat16)
-    need = mhla.workspace_size(q, grid, block)
+    need = mhla.workspace_size(q, grid, block, "simt")
     assert need > (64 << 20)
     out = torch.full_like(q, 7.0)
     W = torch.ones(49, 49, device=DEV)
-    assert call_noalloc(q, q, q, W, grid, block, out) == 6           # MHLA_ERR_WORKSPACE
+    assert call_noalloc(q, q, q, W, grid, block, out, path="simt") == 6   # MHLA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.all(out == 7.0)                                      # nothing ran

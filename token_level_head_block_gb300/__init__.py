@@ -22,7 +22,7 @@ __all__ = [
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libmhla.so")
 
-PATHS = {"auto": 0, "simt": 1, "tc": 2}
+PATHS = {"auto": 0, "simt": 1, "tc": 2, "fused": 3}
 TRANSFORMS = {"linear": 0, "cos": 1, "exp": 2, "gaussian": 3, "local": 4}
 PHIS = {"relu": 0, "relu_eps": 1}
 DTYPES = {"bf16": 0, "f32": 1}
@@ -172,7 +172,7 @@ def select_path(q, k, v, out, grid, block):
                                ctypes.byref(_desc(out)), ctypes.byref(shape3(grid)), ctypes.byref(shape3(block)))
     if r < 0:
         raise MhlaError(-r, "mhla_select_path")
-    return {1: "simt", 2: "tc"}[r]
+    return {1: "simt", 2: "tc", 3: "fused"}[r]
 
 
 def forward(q, k, v, W, grid, block, phi="relu", eps=1e-6, out=None, workspace=None, stream=None,

@@ -104,9 +104,17 @@ int build_problem(const mhla_tensor_t* q, const mhla_tensor_t* k, const mhla_ten
   return MHLA_OK;
 }
 
+// AUTO: the fused short-sequence kernel, else the three tensor-core launches,
+// else the CUDA cores.
+int auto_path(const Problem& p) {
+  if (small_eligible(p)) return MHLA_PATH_FUSED;
+  if (tc_eligible(p)) return MHLA_PATH_TC;
+  return MHLA_PATH_SIMT;
+}
+
 int resolve_path(const Problem& p, int32_t path, int* sel) {
   if (path == MHLA_PATH_AUTO) {
-    *sel = tc_eligible(p) ? MHLA_PATH_TC : MHLA_PATH_SIMT;
+    *sel = auto_path(p);
     return MHLA_OK;
   }
   if (path == MHLA_PATH_SIMT) { *sel = MHLA_PATH_SIMT; return MHLA_OK; }
@@ -115,10 +123,16 @@ int resolve_path(const Problem& p, int32_t path, int* sel) {
     *sel = MHLA_PATH_TC;
     return MHLA_OK;
   }
+  if (path == MHLA_PATH_FUSED) {
+    if (!small_eligible(p)) return MHLA_ERR_UNSUPPORTED;
+    *sel = MHLA_PATH_FUSED;
+    return MHLA_OK;
+  }
   return MHLA_ERR_INVALID_ARG;
 }
 
 size_t workspace_for(const Problem& p, int sel) {
+  if (sel == MHLA_PATH_FUSED) return 0;
   return sel == MHLA_PATH_TC ? tc_workspace_bytes(p) : simt_workspace_bytes(p);
 }
 
@@ -147,7 +161,7 @@ extern "C" int32_t mhla_select_path(const mhla_tensor_t* q, const mhla_tensor_t*
   Problem p;
   const int rc = build_problem(q, k, v, out, grid, block, nullptr, true, &p);
   if (rc != MHLA_OK) return -rc;
-  return tc_eligible(p) ? MHLA_PATH_TC : MHLA_PATH_SIMT;
+  return auto_path(p);
 }
 
 extern "C" mhla_status_t mhla_forward(const mhla_tensor_t* q, const mhla_tensor_t* k, const mhla_tensor_t* v,
@@ -170,16 +184,15 @@ extern "C" mhla_status_t mhla_forward(const mhla_tensor_t* q, const mhla_tensor_
     if (overlaps(o0, o1, w0, w0 + static_cast<uintptr_t>(p.M * p.M) * sizeof(float))) return MHLA_ERR_INVALID_ARG;
   }
   const size_t need = workspace_for(p, sel);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = workspace;
+  if (!ws && workspace_bytes != 0) return MHLA_ERR_WORKSPACE;
+  if (ws && (workspace_bytes < need || reinterpret_cast<uintptr_t>(ws) % kAlign != 0)) return MHLA_ERR_WORKSPACE;
+  if (sel == MHLA_PATH_FUSED) return static_cast<mhla_status_t>(launch_small(p, W, stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   bool owned = false;
   if (!ws) {
-    if (workspace_bytes != 0) return MHLA_ERR_WORKSPACE;
     if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return MHLA_ERR_CUDA;
     owned = true;
-  } else {
-    if (workspace_bytes < need) return MHLA_ERR_WORKSPACE;
-    if (reinterpret_cast<uintptr_t>(ws) % kAlign != 0) return MHLA_ERR_WORKSPACE;
   }
   const int lr = sel == MHLA_PATH_TC ? launch_tc(p, W, ws, stream) : launch_simt(p, W, ws, stream);
   if (owned && cudaFreeAsync(ws, s) != cudaSuccess && lr == MHLA_OK) return MHLA_ERR_CUDA;
@@ -188,7 +201,12 @@ extern "C" mhla_status_t mhla_forward(const mhla_tensor_t* q, const mhla_tensor_
 
 extern "C" mhla_status_t mhla_device_status(void* stream, uint32_t* flags) {
   if (!flags) return MHLA_ERR_INVALID_ARG;
-  return static_cast<mhla_status_t>(read_and_clear_device_error(stream, flags));
+  uint32_t tc = 0, small = 0;
+  const int a = read_and_clear_device_error(stream, &tc);
+  const int b = read_and_clear_small_error(stream, &small);
+  if (a == MHLA_ERR_CUDA || b == MHLA_ERR_CUDA) return MHLA_ERR_CUDA;
+  *flags = tc | small;
+  return *flags ? MHLA_ERR_TIMEOUT : MHLA_OK;
 }
 
 extern "C" const char* mhla_status_string(int32_t status) {

@@ -61,8 +61,14 @@ size_t tc_workspace_bytes(const Problem& p);
 bool tc_eligible(const Problem& p);
 int launch_tc(const Problem& p, const float* W, void* workspace, void* stream);
 
-// Device error word of the tensor-core kernels (bounded waits).
+// Fused short-sequence path (N <= 256 tokens, M <= 96 blocks, bf16, d in
+// {32, 64}): one launch that forms the two-stage N x N product; no workspace.
+bool small_eligible(const Problem& p);
+int launch_small(const Problem& p, const float* W, void* stream);
+
+// Device error words of the tensor-core and fused kernels (bounded waits).
 int read_and_clear_device_error(void* stream, uint32_t* flags);
+int read_and_clear_small_error(void* stream, uint32_t* flags);
 
 // Brackets one kernel launch with CUDA events on its stream while
 // mhla_profile_begin/end collection is active; a no-op otherwise.

@@ -32,6 +32,7 @@
 
 #include "mhla_internal.h"
 #include "ptx.cuh"
+#include "tma_host.h"
 
 namespace mhla {
 
@@ -1311,6 +1312,13 @@ int launch_tc_d(const Problem& p, const float* W, void* workspace, cudaStream_t 
 }
 
 }  // namespace
+
+bool encode_tensor_map(CUtensorMap* m, int rank, void* base, const cuuint64_t* dims,
+                       const cuuint64_t* strides_bytes, const cuuint32_t* box, CUtensorMapSwizzle swz) {
+  return encode(m, rank, base, dims, strides_bytes, box, swz);
+}
+
+int device_sm_count() { return device_sms(); }
 
 bool tc_eligible(const Problem& p) {
   if (p.dtype != MHLA_BF16) return false;
