@@ -25,3 +25,4 @@ from .mhla_oracle import (  # noqa: F401
     readout,
     summaries,
 )
+from .mhla_backward import backward, phi_derivative  # noqa: F401,E402
