@@ -14,7 +14,6 @@ the host cores instead (rank 0 only), on bounded samples of the same workload.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -148,11 +147,22 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_digest():
+# Source files a kernel's code lives in (with the shared inline-PTX header).
+KERNEL_SOURCES = {"tc_summary": "tc_kernels.cu", "tc_mix": "tc_kernels.cu", "tc_output": "tc_kernels.cu",
+                  "tc_small": "small_kernels.cu", "simt_summary": "simt_kernels.cu",
+                  "simt_mix": "simt_kernels.cu", "simt_output": "simt_kernels.cu"}
+
+
+def kernel_source_digest(kernel):
+    """Hash of the source files of one kernel: a profile summary taken on other
+    code than the current one does not count."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "token_level_head_block_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(f.read())
+    csrc = os.path.join(ROOT, "token_level_head_block_gb300", "csrc")
+    for name in (KERNEL_SOURCES.get(kernel, ""), "ptx.cuh"):
+        p = os.path.join(csrc, name)
+        if name and os.path.exists(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -165,7 +175,7 @@ def profiled_traffic(kernel, workload):
     text = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
-    if not m or not d or d.group(1) != kernel_source_digest():
+    if not m or not d or d.group(1) != kernel_source_digest(kernel):
         return None
     return int(m.group(1))
 

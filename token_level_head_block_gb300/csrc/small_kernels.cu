@@ -16,23 +16,29 @@
 // block count this is cheaper than the three-launch path whenever M^2 is not
 // small next to N (DeiT-T: N = 196, M = 49).
 //
-// One work unit = (b, h, 128 query tokens).  Persistent CTAs of four warps:
-//   TMA      q tile (128 x d) and all keys and values (KR x d, KR = N rounded
-//            up to 32, rows past N zero-filled) through 4-D maps (d, H, N, B);
-//   phi      in place on the q and k tiles in shared memory;
-//   MMA 1    scores phi(Q) phi(K)^T, 128 x KR, float32 in tensor memory;
-//   weights  every thread owns one query row: P = score * W[b(t)][b(s)],
-//            rounded to bf16 and written K-major (128-byte swizzle) as the next
-//            MMA's A operand; the denominator sums the rounded P in float32;
-//   MMA 2    P V, 128 x d, from the value tile as it landed (MN-major B);
-//   output   scale by 1 / (den + eps), round to bf16, 16-byte stores.
-// The next unit's q and k tiles load while the weights and the output of the
-// current one are formed; its value tile once MMA 2 has read the current one.
+// One work unit = (b, h, 128 query tokens).  Persistent CTAs of nine warps:
+//   warp 8   (control) TMA of the q tile (128 x d) and of all keys and values
+//            (KR x d, KR = N rounded up to 32, rows past N zero-filled) through
+//            4-D maps (d, H, N, B); issues both MMAs;
+//   warps 0-7 (workers, two warpgroups):
+//            phi in place on the q and k tiles in shared memory;
+//            after MMA 1 (scores phi(Q) phi(K)^T, 128 x KR, float32 in tensor
+//            memory) each thread owns one query row and half of the key
+//            columns: P = score * W[b(t)][b(s)] rounded to bf16, written
+//            K-major (128-byte swizzle) as the A operand of MMA 2, 64 keys at
+//            a time; the control warp starts MMA 2 on each 64-key chunk as
+//            soon as both warpgroups have written it;
+//            MMA 2 = P [V | 1]: the value tile as it landed (MN-major B) plus a
+//            constant ones column, so the tensor core also sums the rounded P
+//            into the denominator; each warpgroup scales half of the output
+//            columns by 1 / (den + eps), rounds to bf16 and stores them.
+// The next unit's q and k tiles load once MMA 1 has read the current ones, its
+// values once MMA 2 has; the first unit's loads overlap the set-up of W.
 //
 // Every wait is bounded (2 s of %globaltimer, 2^28 polls); a wait that gives
-// up sets bit 0 of this file's device error word, all threads of the CTA agree
-// to stop, copies and MMAs in flight are drained (bit 1 if that drain gives up)
-// and tensor memory is released.
+// up sets bit 0 of this file's device error word and a per-CTA abort flag so
+// the other roles stop waiting too; copies and MMAs in flight are drained
+// (bit 1 if that drain gives up) and tensor memory is released.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -54,11 +60,12 @@ using namespace ptx;
 constexpr uint64_t kSmallWaitNs = 2000000000ull;   // 2 s
 constexpr uint32_t kSmallWaitPolls = 1u << 28;
 constexpr uint64_t kSmallDrainNs = 50000000ull;    // 50 ms for work already in flight
-constexpr int kSmallThreads = 128;
+constexpr int kWorkers = 256;                      // warps 0-7
+constexpr int kSmallThreads = kWorkers + 32;       // + the control warp
 constexpr int kQRows = 128;      // query tokens per unit: MMA M, one TMEM lane each
 constexpr int kMaxKeys = 256;    // keys per image: MMA N of the score product
 constexpr int kMaxBlocks = 96;   // W is held in shared memory as float32
-constexpr int kTmemCols = 512;   // scores in [0, 256), P V in [256, 256 + d)
+constexpr int kTmemCols = 512;   // scores in [0, 256), P [V | 1] in [256, 256 + d + 16)
 
 template <int D>
 struct SmallCfg {
@@ -67,17 +74,19 @@ struct SmallCfg {
   static constexpr int KV_BYTES = kMaxKeys * ROWB;
   static constexpr int P_CHUNK = kQRows * 128;       // 64 keys of P: 128 rows of 128 bytes
   static constexpr int P_BYTES = (kMaxKeys / 64) * P_CHUNK;
-  static constexpr int W_BYTES = kMaxBlocks * kMaxBlocks * 4;
+  static constexpr int W_BYTES = kMaxBlocks * (kMaxBlocks + 1) * 4;   // rows of M + 1 (zero sentinel)
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + Q_BYTES;      // k directly after q: phi runs over both
   static constexpr int V_OFF = K_OFF + KV_BYTES;
-  static constexpr int P_OFF = V_OFF + KV_BYTES;
+  static constexpr int ONES_OFF = V_OFF + KV_BYTES;  // second N atom of MMA 2's B operand
+  static constexpr int P_OFF = ONES_OFF + KV_BYTES;
   static constexpr int W_OFF = P_OFF + P_BYTES;
-  static constexpr int BLK_OFF = W_OFF + W_BYTES;    // block id of every token, one byte each
-  static constexpr int CTRL_OFF = BLK_OFF + kMaxKeys;
-  static constexpr size_t SMEM = CTRL_OFF + 64 + 1024;
+  static constexpr int BLK_OFF = W_OFF + (W_BYTES + 15) / 16 * 16;   // byte offset of W[.][b(s)] per key
+  static constexpr int CTRL_OFF = BLK_OFF + kMaxKeys * 2;
+  static constexpr size_t SMEM = CTRL_OFF + 128 + 1024;
   static constexpr uint32_t SBO = 8 * ROWB;          // 8-row groups of a token tile
   static constexpr uint32_t LAYOUT = D == 64 ? 2u : 4u;   // 128- or 64-byte swizzle
+  static constexpr int NO = D + 16;                  // MMA 2 columns: d values, the ones block
 };
 
 struct SmallGeom {
@@ -86,15 +95,25 @@ struct SmallGeom {
   int64_t osb, osn, osh;             // output strides, elements
 };
 
-__device__ __noinline__ bool small_wait(uint64_t* bar, uint32_t parity) {
+__device__ __noinline__ bool small_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1; it < kSmallWaitPolls; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer() - t0 > kSmallWaitNs) break;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kSmallWaitNs) break;
+    }
   }
+  *abort_flag = 1u;
   atomicOr(&g_small_error, 1u);
   return false;
+}
+
+// Every lane waits, then the warp agrees, so warp-collective tcgen05.ld that
+// follows runs on all lanes or on none.
+__device__ __forceinline__ bool small_warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
+  return __all_sync(0xffffffffu, small_wait(bar, parity, abort_flag));
 }
 
 __device__ __noinline__ void small_drain(uint64_t* bar, uint32_t parity) {
@@ -137,48 +156,38 @@ tc_small(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
   uint8_t* sq = smem + Cfg::Q_OFF;
   uint8_t* sk = smem + Cfg::K_OFF;
   uint8_t* sv = smem + Cfg::V_OFF;
+  uint8_t* sones = smem + Cfg::ONES_OFF;
   uint8_t* sp = smem + Cfg::P_OFF;
   float* sw = reinterpret_cast<float*>(smem + Cfg::W_OFF);
-  uint8_t* sblk = smem + Cfg::BLK_OFF;
+  uint16_t* soff = reinterpret_cast<uint16_t*>(smem + Cfg::BLK_OFF);
   uint64_t* full_qk = reinterpret_cast<uint64_t*>(smem + Cfg::CTRL_OFF);
   uint64_t* full_v = full_qk + 1;
-  uint64_t* done1 = full_qk + 2;
-  uint64_t* done2 = full_qk + 3;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full_qk + 4);
+  uint64_t* phid = full_qk + 2;     // workers: phi applied
+  uint64_t* done1 = full_qk + 3;    // MMA 1 complete
+  uint64_t* done2 = full_qk + 4;    // MMA 2 complete
+  uint64_t* odone = full_qk + 5;    // workers: MMA 2 result read from tensor memory
+  uint64_t* chunk = full_qk + 6;    // [4] workers: 64 keys of P written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full_qk + 10);
+  volatile uint32_t* abortf = tmem_slot + 1;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const uint32_t qk_bytes = static_cast<uint32_t>((kQRows + g.KR) * Cfg::ROWB);
-  const uint32_t v_bytes = static_cast<uint32_t>(g.KR * Cfg::ROWB);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_chunks = (g.KR + 63) / 64;
 
-  if (tid == 0) {
+  if (tid == kWorkers) {
     mbar_init(full_qk, 1);
     mbar_init(full_v, 1);
+    mbar_init(phid, kWorkers / 32);
     mbar_init(done1, 1);
     mbar_init(done2, 1);
+    mbar_init(odone, kWorkers / 32);
+    for (int c = 0; c < 4; ++c) mbar_init(chunk + c, kWorkers / 32);
+    *abortf = 0u;
     fence_mbar_init();
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
   }
-  if (warp == 0) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
-  for (int e = tid; e < g.M * g.M; e += kSmallThreads) sw[e] = W[e];
-  // Block id of token n: blocks row-major over (nbt, nby, nbx), tokens raster
-  // over (T, Y, X).
-  for (int n = tid; n < kMaxKeys; n += kSmallThreads) {
-    int id = 0;
-    if (n < g.N) {
-      const int x = n % g.X, r = n / g.X, y = r % g.Y, t = r / g.Y;
-      id = ((t / g.bt) * g.nby + y / g.by) * g.nbx + x / g.bx;
-    }
-    sblk[n] = static_cast<uint8_t>(id);
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   const uint64_t pol_q = policy_evict_first();
   const uint64_t pol_kv = policy_evict_last();   // every query tile of (b, h) reads them
@@ -186,162 +195,204 @@ tc_small(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     const int32_t qt = static_cast<int32_t>(u % g.nqt);
     const int64_t bh = u / g.nqt;
     const int32_t h = static_cast<int32_t>(bh % g.H), b = static_cast<int32_t>(bh / g.H);
-    mbar_arrive_expect_tx(full_qk, qk_bytes);
+    mbar_arrive_expect_tx(full_qk, static_cast<uint32_t>((kQRows + g.KR) * Cfg::ROWB));
     tma_load_4d(sq, &tm_q, full_qk, 0, h, qt * kQRows, b, pol_q);
     tma_load_4d(sk, &tm_k, full_qk, 0, h, 0, b, pol_kv);
   };
   auto issue_v = [&](int64_t u) {
     const int64_t bh = u / g.nqt;
     const int32_t h = static_cast<int32_t>(bh % g.H), b = static_cast<int32_t>(bh / g.H);
-    mbar_arrive_expect_tx(full_v, v_bytes);
+    mbar_arrive_expect_tx(full_v, static_cast<uint32_t>(g.KR * Cfg::ROWB));
     tma_load_4d(sv, &tm_v, full_v, 0, h, 0, b, pol_kv);
   };
-
-  // Issued (thread 0) and consumed (all threads) counts of each barrier's phases.
-  uint32_t n_qk = 0, n_v = 0, n_m1 = 0, n_m2 = 0;
-  uint32_t c_qk = 0, c_v = 0, c_m1 = 0, c_m2 = 0;
-  if (tid == 0 && static_cast<int64_t>(blockIdx.x) < n_units) {
+  uint32_t n_qk = 0, n_v = 0, n_m1 = 0, n_m2 = 0;   // phases issued (control lane)
+  if (tid == kWorkers && static_cast<int64_t>(blockIdx.x) < n_units) {
     issue_qk(blockIdx.x);
     issue_v(blockIdx.x);
     n_qk = n_v = 1;
   }
-  const bool add_eps = phi_kind == MHLA_PHI_RELU_EPS;
-  const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  const int swr = tid & 7;   // 128-byte swizzle phase of this thread's P row
-
-  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const int32_t qt = static_cast<int32_t>(u % g.nqt);
-    const int64_t bh = u / g.nqt;
-    const int32_t h = static_cast<int32_t>(bh % g.H), b = static_cast<int32_t>(bh / g.H);
-    const int64_t next = u + gridDim.x;
-
-    // ---- q and k tiles landed: phi in place over both (contiguous)
-    if (!__syncthreads_and(small_wait(full_qk, c_qk & 1u))) break;
-    ++c_qk;
-    {
-      uint4* base = reinterpret_cast<uint4*>(sq);
-      const int n16 = (kQRows + g.KR) * Cfg::ROWB / 16;
-      for (int e = tid; e < n16; e += kSmallThreads) base[e] = phi8(base[e], add_eps, eps2);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- MMA 1: scores = phi(Q) phi(K)^T, 128 x KR, TMEM columns [0, KR)
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16_f32(128, g.KR, /*a K-major*/ false, /*b K-major*/ false);
-      const uint32_t qa = smem_u32(sq), ka = smem_u32(sk);
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
-        mma_bf16(tmem, smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
-                 smem_desc(ka + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT), idesc, ks > 0 ? 1u : 0u);
-      mma_commit(done1);
-      ++n_m1;
-    }
-    if (!__syncthreads_and(small_wait(done1, c_m1 & 1u))) break;
-    ++c_m1;
-    tc_fence_after();
-    // q and k of this unit are consumed: the next unit's may land meanwhile.
-    if (tid == 0 && next < n_units) {
-      fence_proxy_async_smem();
-      issue_qk(next);
-      ++n_qk;
-    }
-
-    // ---- weights: P[t][s] = score * W[b(t)][b(s)], bf16, K-major SW128
-    const int32_t nq = qt * kQRows + tid;
-    const float* wrow = sw + (nq < g.N ? sblk[nq] : 0) * g.M;
-    float den = 0.0f;
-    for (int m = 0; m < g.KR / 32; ++m) {
-      uint32_t r[32];
-      tmem_ld_x32(lane_base + m * 32, r);
-      const uint4 id0 = *reinterpret_cast<const uint4*>(sblk + m * 32);
-      const uint4 id1 = *reinterpret_cast<const uint4*>(sblk + m * 32 + 16);
-      tmem_ld_wait();
-      const uint32_t ids[8] = {id0.x, id0.y, id0.z, id0.w, id1.x, id1.y, id1.z, id1.w};
-      uint32_t packed[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const int s = m * 32 + e;
-        const uint32_t j0 = (ids[e >> 2] >> (8 * (e & 3))) & 0xFFu;
-        const uint32_t j1 = (ids[e >> 2] >> (8 * ((e + 1) & 3))) & 0xFFu;
-        const float p0 = s < g.N ? __uint_as_float(r[e]) * wrow[j0] : 0.0f;
-        const float p1 = s + 1 < g.N ? __uint_as_float(r[e + 1]) * wrow[j1] : 0.0f;
-        packed[e >> 1] = pack2(p0, p1);
-        const float2 pr = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&packed[e >> 1]));
-        den += pr.x + pr.y;
-      }
-      uint8_t* prow = sp + (m >> 1) * Cfg::P_CHUNK + tid * 128;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int unit = (m & 1) * 4 + q;
-        *reinterpret_cast<uint4*>(prow + ((unit ^ swr) * 16)) =
-            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-
-    // ---- MMA 2: P V, 128 x d, TMEM columns [256, 256 + d)
-    bool vok = true;
-    if (tid == 0) vok = small_wait(full_v, c_v & 1u);
-    if (!__syncthreads_and(vok)) break;
-    ++c_v;
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16_f32(128, D, /*a K-major*/ false, /*b MN-major*/ true);
-      const uint32_t pa = smem_u32(sp), va = smem_u32(sv);
-      for (int ks = 0; ks < g.KR / 16; ++ks)
-        mma_bf16(tmem + 256, smem_desc(pa + (ks >> 2) * Cfg::P_CHUNK + (ks & 3) * 32, 16, 1024, 2),
-                 smem_desc(va + ks * 2 * Cfg::SBO, Cfg::KV_BYTES, Cfg::SBO, Cfg::LAYOUT), idesc,
-                 ks > 0 ? 1u : 0u);
-      mma_commit(done2);
-      ++n_m2;
-    }
-    if (!__syncthreads_and(small_wait(done2, c_m2 & 1u))) break;
-    ++c_m2;
-    tc_fence_after();
-    if (tid == 0 && next < n_units) {
-      issue_v(next);
-      ++n_v;
-    }
-
-    // ---- output: o_t = (P V)_t / (den_t + eps)
-    uint32_t o0[32], o1[32];
-    tmem_ld_x32(lane_base + 256, o0);
-    if (D == 64) tmem_ld_x32(lane_base + 288, o1);
-    tmem_ld_wait();
-    tc_fence_before();
-    if (nq < g.N) {
-      const float inv = 1.0f / (den + eps);
-      uint4* dst = reinterpret_cast<uint4*>(out + b * g.osb + static_cast<int64_t>(nq) * g.osn + h * g.osh);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        dst[q] = make_uint4(pack2(__uint_as_float(o0[8 * q]) * inv, __uint_as_float(o0[8 * q + 1]) * inv),
-                            pack2(__uint_as_float(o0[8 * q + 2]) * inv, __uint_as_float(o0[8 * q + 3]) * inv),
-                            pack2(__uint_as_float(o0[8 * q + 4]) * inv, __uint_as_float(o0[8 * q + 5]) * inv),
-                            pack2(__uint_as_float(o0[8 * q + 6]) * inv, __uint_as_float(o0[8 * q + 7]) * inv));
-      if (D == 64) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          dst[4 + q] =
-              make_uint4(pack2(__uint_as_float(o1[8 * q]) * inv, __uint_as_float(o1[8 * q + 1]) * inv),
-                         pack2(__uint_as_float(o1[8 * q + 2]) * inv, __uint_as_float(o1[8 * q + 3]) * inv),
-                         pack2(__uint_as_float(o1[8 * q + 4]) * inv, __uint_as_float(o1[8 * q + 5]) * inv),
-                         pack2(__uint_as_float(o1[8 * q + 6]) * inv, __uint_as_float(o1[8 * q + 7]) * inv));
-      }
-    }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
   }
+  if (tid < kWorkers) {
+    // W with a zero column M appended to every row (the block of padded keys),
+    // every element copied asynchronously so all of them are in flight at once.
+    const int M = g.M, nW = M * M;
+    for (int e = tid; e < nW; e += kWorkers) cp_async_4(sw + (e / M) * (M + 1) + e % M, W + e);
+    for (int i = tid; i < M; i += kWorkers) sw[i * (M + 1) + M] = 0.0f;
+    // Byte offset of W[.][b(s)] for key s: blocks row-major over (nbt, nby,
+    // nbx), tokens raster over (T, Y, X); keys past N point at the zero column.
+    for (int n = tid; n < kMaxKeys; n += kWorkers) {
+      int id = M;
+      if (n < g.N) {
+        const int x = n % g.X, r = n / g.X, y = r % g.Y, t = r / g.Y;
+        id = ((t / g.bt) * g.nby + y / g.by) * g.nbx + x / g.bx;
+      }
+      soff[n] = static_cast<uint16_t>(id * 4);
+    }
+    // Constant ones block of MMA 2's B operand: row s holds (1, 0, ..., 0) in
+    // the swizzled layout, so output column d sums P over the keys.
+    for (int idx = tid; idx < kMaxKeys * (D / 8); idx += kWorkers) {
+      const int row = idx / (D / 8), phys = idx % (D / 8);
+      const int logical = phys ^ (D == 64 ? (row & 7) : ((row >> 1) & 3));
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (logical == 0) v.x = 0x3F80u;   // bf16 1.0 in the low half
+      *reinterpret_cast<uint4*>(sones + row * Cfg::ROWB + phys * 16) = v;
+    }
+    fence_proxy_async_smem();
+    cp_async_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-  // Copies and MMAs issued but never waited for (a wait gave up) must finish
-  // before shared and tensor memory go away.
-  if (tid == 0) {
-    if (n_qk > c_qk) small_drain(full_qk, (n_qk - 1) & 1u);
-    if (n_v > c_v) small_drain(full_v, (n_v - 1) & 1u);
-    if (n_m1 > c_m1) small_drain(done1, (n_m1 - 1) & 1u);
-    if (n_m2 > c_m2) small_drain(done2, (n_m2 - 1) & 1u);
+  if (warp == kWorkers / 32) {
+    // ------------------------------------------------------------ control
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++it) {
+        const uint32_t par = it & 1u;
+        const int64_t next = u + gridDim.x;
+        if (!small_wait(phid, par, abortf)) break;
+        tc_fence_after();
+        {
+          const uint32_t idesc = idesc_bf16_f32(128, g.KR, /*a K-major*/ false, /*b K-major*/ false);
+          const uint32_t qa = smem_u32(sq), ka = smem_u32(sk);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem, smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
+                     smem_desc(ka + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT), idesc, ks > 0 ? 1u : 0u);
+          mma_commit(done1);
+          ++n_m1;
+        }
+        if (!small_wait(done1, par, abortf)) break;
+        if (next < n_units) {   // q and k consumed: the next unit's may land
+          issue_qk(next);
+          ++n_qk;
+        }
+        // The previous unit's result must be out of tensor memory before
+        // MMA 2 overwrites it, and this unit's values must have landed.
+        if (it > 0 && !small_wait(odone, par ^ 1u, abortf)) break;
+        if (!small_wait(full_v, par, abortf)) break;
+        const uint32_t idesc2 = idesc_bf16_f32(128, Cfg::NO, /*a K-major*/ false, /*b MN-major*/ true);
+        const uint32_t pa = smem_u32(sp), va = smem_u32(sv);
+        for (int c = 0; c < n_chunks; ++c) {
+          if (!small_wait(chunk + c, par, abortf)) { ok = false; break; }
+          tc_fence_after();
+          const int ks_end = min(4 * c + 4, g.KR / 16);
+          for (int ks = 4 * c; ks < ks_end; ++ks)
+            mma_bf16(tmem + 256, smem_desc(pa + c * Cfg::P_CHUNK + (ks & 3) * 32, 16, 1024, 2),
+                     smem_desc(va + ks * 2 * Cfg::SBO, Cfg::ONES_OFF - Cfg::V_OFF, Cfg::SBO, Cfg::LAYOUT), idesc2,
+                     ks > 0 ? 1u : 0u);
+        }
+        if (!ok) break;
+        mma_commit(done2);
+        ++n_m2;
+        if (!small_wait(done2, par, abortf)) break;
+        if (next < n_units) {   // values consumed
+          issue_v(next);
+          ++n_v;
+        }
+      }
+      // Copies and MMAs issued must finish before shared and tensor memory go
+      // away (a phase already complete returns at once).
+      if (n_qk) small_drain(full_qk, (n_qk - 1) & 1u);
+      if (n_v) small_drain(full_v, (n_v - 1) & 1u);
+      if (n_m1) small_drain(done1, (n_m1 - 1) & 1u);
+      if (n_m2) small_drain(done2, (n_m2 - 1) & 1u);
+    }
+  } else {
+    // ------------------------------------------------------------ workers
+    const int row = tid & 127;              // query row = TMEM lane
+    const int half = tid >> 7;              // key columns and output columns of this warpgroup
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const bool add_eps = phi_kind == MHLA_PHI_RELU_EPS;
+    const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
+    const int swr = row & 7;                // 128-byte swizzle phase of this thread's P row
+    const int n16 = (kQRows + g.KR) * Cfg::ROWB / 16;
+    uint32_t it = 0;
+    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+      const uint32_t par = it & 1u;
+      const int32_t qt = static_cast<int32_t>(u % g.nqt);
+      const int64_t bh = u / g.nqt;
+      const int32_t h = static_cast<int32_t>(bh % g.H), b = static_cast<int32_t>(bh / g.H);
+
+      // ---- phi in place over the q and k tiles (contiguous)
+      if (!small_warp_wait(full_qk, par, abortf)) break;
+      {
+        uint4* base = reinterpret_cast<uint4*>(sq);
+        for (int e = tid; e < n16; e += kWorkers) base[e] = phi8(base[e], add_eps, eps2);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(phid);
+
+      // ---- P[t][s] = score * W[b(t)][b(s)], bf16, K-major SW128, 64 keys per chunk
+      if (!small_warp_wait(done1, par, abortf)) break;
+      tc_fence_after();
+      const int32_t nq = qt * kQRows + row;
+      const uint8_t* wrow =
+          reinterpret_cast<const uint8_t*>(sw) + (nq < g.N ? soff[nq] / 4 : 0) * (g.M + 1) * 4;
+      for (int c = 0; c < n_chunks; ++c) {
+        const int m = 2 * c + half;         // 32 keys of this warpgroup in chunk c
+        if (m < g.KR / 32) {
+          uint32_t r[32];
+          tmem_ld_x32(lane_base + m * 32, r);
+          uint4 offs[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) offs[i] = reinterpret_cast<const uint4*>(soff + m * 32)[i];
+          tmem_ld_wait();
+          const uint32_t* ow = reinterpret_cast<const uint32_t*>(offs);
+          uint32_t packed[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const uint32_t o2 = ow[e >> 1];
+            const float w0 = *reinterpret_cast<const float*>(wrow + (o2 & 0xFFFFu));
+            const float w1 = *reinterpret_cast<const float*>(wrow + (o2 >> 16));
+            packed[e >> 1] = pack2(__uint_as_float(r[e]) * w0, __uint_as_float(r[e + 1]) * w1);
+          }
+          uint8_t* prow = sp + c * Cfg::P_CHUNK + row * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(prow + (((half * 4 + q) ^ swr) * 16)) =
+                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(chunk + c);
+      }
+
+      // ---- output: o_t = (P V)_t / (P 1)_t + eps), this warpgroup's half of the columns
+      if (!small_warp_wait(done2, par, abortf)) break;
+      tc_fence_after();
+      constexpr int HC = D / 2;
+      uint32_t o[HC], dn;
+      if constexpr (HC == 32) {
+        tmem_ld_x32(lane_base + 256 + half * HC, o);
+      } else {
+        tmem_ld_x16(lane_base + 256 + half * HC, o);
+      }
+      tmem_ld_x1(lane_base + 256 + D, dn);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(odone);
+      if (nq < g.N) {
+        const float inv = 1.0f / (__uint_as_float(dn) + eps);
+        uint4* dst = reinterpret_cast<uint4*>(out + b * g.osb + static_cast<int64_t>(nq) * g.osn + h * g.osh +
+                                              half * HC);
+#pragma unroll
+        for (int q = 0; q < HC / 8; ++q)
+          dst[q] = make_uint4(pack2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv),
+                              pack2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
+                              pack2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
+                              pack2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
