@@ -167,6 +167,48 @@ mhla_status_t mhla_forward(const mhla_tensor_t* q, const mhla_tensor_t* k,
                            void* workspace, size_t workspace_bytes, void* stream,
                            int32_t path);
 
+/* Device workspace mhla_backward needs for this problem and path (bytes, a
+ * multiple of 256).  q gives B, N, H, d and the dtype.  Host only. */
+mhla_status_t mhla_backward_workspace_size(const mhla_tensor_t* q, const mhla_shape3_t* grid,
+                                           const mhla_shape3_t* block, int32_t path, size_t* bytes);
+
+/* Gradients of the MHLA forward for training: given dout = dL/d(out) of a
+ * forward with the same q, k, v, W, grid, block and phi, writes dq, dk, dv and
+ * dW = dL/dW.  The pages print no backward pass; they make the mixing
+ * coefficients learnable ([P2] section 4 "Multi-Head Mixing": learned,
+ * initialised from block distances; [P1] section 7: W is a 1x1 convolution's
+ * weight), so these are the chain-rule derivatives of the three forward steps
+ * taken in reverse:
+ *   dnum_t = dout_t / den_t,   dden_t = -(dout_t . o_t) / den_t
+ *   dq_t   = (S~_i dnum_t + dden_t z~_i) * [q_t > 0]
+ *   dS~_i  = sum_{t in i} phi(q_t) dnum_t^T,  dz~_i = sum_{t in i} dden_t phi(q_t)
+ *   dS_j   = sum_i W[i][j] dS~_i,             dz_j  = sum_i W[i][j] dz~_i
+ *   dW[i][j] = sum_{b,h} <dS~_i, S_j> + dz~_i . z_j
+ *   dv_s   = dS_j^T phi(k_s),  dk_s = (dS_j v_s + dz_j) * [k_s > 0]
+ * phi'(x) is 1 for x > 0 and 0 otherwise in both phi modes.  The summaries and
+ * the mixing are recomputed from k, v and W (nothing is kept from the forward).
+ *   q, k, v, dout  device tensors [B, N, H, d], same shape and dtype.
+ *   dq, dk, dv     device tensors, same shape and dtype, written in that dtype;
+ *                  none may overlap another tensor argument, W or dW.
+ *   W              device float32 M x M, as for mhla_forward.
+ *   dW             device float32 M x M, overwritten with the sum over every
+ *                  batch and head (one W is shared by all); must not overlap W.
+ *   workspace      at least mhla_backward_workspace_size() bytes, 256-byte
+ *                  aligned, or NULL with workspace_bytes == 0 (stream-ordered
+ *                  cudaMallocAsync / cudaFreeAsync).
+ *   path           AUTO or SIMT (CUDA cores, float32 arithmetic, any d <= 128
+ *                  and block shape); TC and FUSED return MHLA_ERR_UNSUPPORTED.
+ * Asynchronous on stream; statuses as for mhla_forward.  B == 0 or H == 0
+ * writes dW = 0 and nothing else. */
+mhla_status_t mhla_backward(const mhla_tensor_t* q, const mhla_tensor_t* k,
+                            const mhla_tensor_t* v, const float* W,
+                            const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                            const mhla_phi_t* phi, const mhla_tensor_t* dout,
+                            const mhla_tensor_t* dq, const mhla_tensor_t* dk,
+                            const mhla_tensor_t* dv, float* dW,
+                            void* workspace, size_t workspace_bytes, void* stream,
+                            int32_t path);
+
 /* mhla_forward for callers that must not allocate device memory -- the paper
  * has no counterpart to this; it is a property of the library, not the method.
  * Who needs it: code that runs the forward where device allocation is not

@@ -226,3 +226,61 @@ def test_workspace_sizes(L):
         assert L.mhla_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
                                      ctypes.byref(mhla.shape3(wl.block)), path, ctypes.byref(n)) == OK
         assert n.value == 0
+
+
+# ------------------------------------------------------------ backward validation
+
+def call_backward(L, q, k, v, g, dq, dk, dv, grid, block, W=FAKE + (1 << 36), dW=FAKE + (1 << 37),
+                  phi=(0, 1e-6), ws=None, ws_bytes=0, path=0):
+    return L.mhla_backward(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.c_void_p(W),
+                           ctypes.byref(mhla.shape3(grid)), ctypes.byref(mhla.shape3(block)),
+                           ctypes.byref(mhla.Phi(*phi)), ctypes.byref(g), ctypes.byref(dq), ctypes.byref(dk),
+                           ctypes.byref(dv), ctypes.c_void_p(dW) if dW else None,
+                           ctypes.c_void_p(ws) if ws else None, ws_bytes, None, path)
+
+
+def seven(B, N, H, d, dtype="bf16"):
+    span = B * N * H * d * 4 + 4096
+    return [contig(B, N, H, d, dtype, FAKE + i * span) for i in range(7)]
+
+
+def test_backward_rejects_malformed_requests_before_any_launch(L):
+    q, k, v, g, dq, dk, dv = seven(2, 1024, 3, 64)
+    grid, block = (32, 32), (16, 8)
+    assert call_backward(L, q, k, v, g, dq, dk, dv, (32, 31), block) == SHAPE
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, (5, 8)) == SHAPE
+    dk2 = contig(2, 1024, 3, 32, base=dk.data)
+    assert call_backward(L, q, k, v, g, dq, dk2, dv, grid, block) == SHAPE          # d differs
+    g2 = contig(2, 1024, 3, 64, "f32", base=g.data)
+    assert call_backward(L, q, k, v, g2, dq, dk, dv, grid, block) == SHAPE          # dtype differs
+    assert call_backward(L, q, k, v, g, dq, dq, dv, grid, block) == INVALID         # dq and dk alias
+    assert call_backward(L, q, k, v, g, q, dk, dv, grid, block) == INVALID          # dq aliases q
+    assert call_backward(L, q, k, v, g, dq, dk, g, grid, block) == INVALID          # dv aliases dout
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, W=0) == INVALID    # null W
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, dW=0) == INVALID   # null dW
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, dW=FAKE + (1 << 36) + 64) == INVALID  # dW in W
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, dW=dq.data + 128) == INVALID          # dW in dq
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, W=dk.data) == INVALID                 # W in dk
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, phi=(3, 1e-6)) == INVALID
+    over = mhla.tensor_desc(dv.data, "bf16", (2, 1024, 3, 64), (1024 * 3 * 64, 3 * 64, 32))
+    assert call_backward(L, q, k, v, g, dq, dk, over, grid, block) == INVALID       # heads overlap in dv
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, ws=FAKE + 7, ws_bytes=1 << 40) == WORKSPACE
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, ws=FAKE, ws_bytes=16) == WORKSPACE
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, ws=None, ws_bytes=16) == WORKSPACE
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, path=2) == UNSUPPORTED
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, path=3) == UNSUPPORTED
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, path=9) == INVALID
+
+
+def test_backward_workspace_size(L):
+    wl = WORKLOADS["dit_s2_4096px"]
+    q = contig(wl.B, wl.N, wl.H, wl.d)
+    n = ctypes.c_size_t()
+    for path in (0, 1):
+        assert L.mhla_backward_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
+                                              ctypes.byref(mhla.shape3(wl.block)), path, ctypes.byref(n)) == OK
+        per = wl.B * wl.H * wl.M * wl.d * (wl.d + 1) * 4
+        expect = 3 * per + wl.B * wl.H * wl.M * wl.M * 4
+        assert expect <= n.value < expect + 4 * 256 and n.value % 256 == 0
+    assert L.mhla_backward_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
+                                          ctypes.byref(mhla.shape3(wl.block)), 2, ctypes.byref(n)) == UNSUPPORTED

@@ -15,7 +15,8 @@ import numpy as np
 
 __all__ = [
     "MhlaError", "lib", "library_path", "num_blocks", "init_mixing", "workspace_size",
-    "select_path", "forward", "device_status", "profile_begin", "profile_end", "tensor_desc", "shape3",
+    "select_path", "forward", "backward", "backward_workspace_size", "device_status", "profile_begin",
+    "profile_end", "tensor_desc", "shape3",
     "PATHS", "TRANSFORMS",
 ]
 
@@ -88,6 +89,13 @@ def lib():
     L.mhla_forward.argtypes = [P(Tensor), P(Tensor), P(Tensor), ctypes.c_void_p, P(Shape3), P(Shape3), P(Phi),
                                P(Tensor), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int32]
     L.mhla_forward.restype = ctypes.c_int
+    L.mhla_backward_workspace_size.argtypes = [P(Tensor), P(Shape3), P(Shape3), ctypes.c_int32,
+                                               P(ctypes.c_size_t)]
+    L.mhla_backward_workspace_size.restype = ctypes.c_int
+    L.mhla_backward.argtypes = [P(Tensor), P(Tensor), P(Tensor), ctypes.c_void_p, P(Shape3), P(Shape3), P(Phi),
+                                P(Tensor), P(Tensor), P(Tensor), P(Tensor), ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int32]
+    L.mhla_backward.restype = ctypes.c_int
     L.mhla_device_status.argtypes = [ctypes.c_void_p, P(ctypes.c_uint32)]
     L.mhla_device_status.restype = ctypes.c_int
     L.mhla_status_string.argtypes = [ctypes.c_int32]
@@ -201,6 +209,47 @@ def forward(q, k, v, W, grid, block, phi="relu", eps=1e-6, out=None, workspace=N
                             ws_bytes, ctypes.c_void_p(sptr) if sptr else None, PATHS[path])
     _check(st, "mhla_forward")
     return out
+
+
+def backward_workspace_size(q, grid, block, path="auto"):
+    n = ctypes.c_size_t(0)
+    _check(lib().mhla_backward_workspace_size(ctypes.byref(_desc(q) if not isinstance(q, Tensor) else q),
+                                              ctypes.byref(shape3(grid)), ctypes.byref(shape3(block)),
+                                              PATHS[path], ctypes.byref(n)), "mhla_backward_workspace_size")
+    return int(n.value)
+
+
+def backward(q, k, v, W, dout, grid, block, phi="relu", eps=1e-6, dq=None, dk=None, dv=None, dW=None,
+             workspace=None, stream=None, path="auto"):
+    """Gradients (dq, dk, dv, dW) of the MHLA forward given dout = dL/d(out).
+
+    Device tensors [B, N, H, d] like ``forward``; dW is a float32 M x M CUDA
+    tensor (allocated when not given) holding the sum over batches and heads.
+    Asynchronous on ``stream`` (default: torch's current stream).
+    """
+    import torch
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dW is None:
+        dW = torch.empty_like(W)
+    for name, x in (("W", W), ("dW", dW)):
+        if not x.is_contiguous() or x.dtype != torch.float32:
+            raise ValueError(f"{name} must be a contiguous float32 tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() *
+                                                            workspace.element_size())
+    st = lib().mhla_backward(ctypes.byref(_desc(q)), ctypes.byref(_desc(k)), ctypes.byref(_desc(v)),
+                             ctypes.c_void_p(W.data_ptr()), ctypes.byref(shape3(grid)),
+                             ctypes.byref(shape3(block)), ctypes.byref(Phi(PHIS[phi], float(eps))),
+                             ctypes.byref(_desc(dout)), ctypes.byref(_desc(dq)), ctypes.byref(_desc(dk)),
+                             ctypes.byref(_desc(dv)), ctypes.c_void_p(dW.data_ptr()),
+                             ctypes.c_void_p(ws_ptr) if ws_ptr else None, ws_bytes,
+                             ctypes.c_void_p(sptr) if sptr else None, PATHS[path])
+    _check(st, "mhla_backward")
+    return dq, dk, dv, dW
 
 
 def profile_begin():

@@ -50,6 +50,22 @@ size_t simt_workspace_bytes(const Problem& p);
 SimtWorkspace simt_carve(const Problem& p, void* base);
 int launch_simt(const Problem& p, const float* W, void* workspace, void* stream);
 
+// Backward pass operands (dout read; dq, dk, dv, dW written) and the CUDA-core
+// backward's workspace (float32):
+//   Sz   [BH][M][d*(d+1)]  S_j, z_j (recomputed)
+//   Szt  [BH][M][d*(d+1)]  S~_i, z~_i; later overwritten with dS_j, dz_j
+//   dSzt [BH][M][d*(d+1)]  dS~_i, dz~_i
+//   part [BH][M][M]        per-(b, h) partial sums of dW
+struct BwdOperands {
+  Operand dout, dq, dk, dv;
+  float* dW;
+};
+struct SimtBwdWorkspace {
+  float *Sz, *Szt, *dSzt, *part;
+};
+size_t simt_bwd_workspace_bytes(const Problem& p);
+int launch_simt_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream);
+
 // Workspace layout of the tensor-core path:
 //   Wb   bf16 [M][Mp]                  W rounded to bf16, Mp = round_up(M, 8)
 //   Sbuf bf16 [G][M][128]               columns col = (b,h) then the d rows of S_j

@@ -8,6 +8,7 @@
 //   simt_mix      S~_i = sum_j W[i][j] S_j and z~_i likewise, per (b, h)
 //   simt_output   o_t = phi(q_t) S~_i / (phi(q_t) . z~_i + eps)
 // Workspace: two float32 buffers [BH][M][d*(d+1)] (S_j row-major, then z_j).
+// The backward pass (below) reuses the summary and mixing kernels.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -97,7 +98,9 @@ simt_summary(const T* __restrict__ k, const T* __restrict__ v, Operand ko, Opera
 constexpr int kMixThreads = 128;
 constexpr int kMixRows = 8;     // query blocks i per thread
 
-// S~ = W . S per (b, h), treating the d*(d+1) entries of every block as columns.
+// S~ = W . S per (b, h), treating the d*(d+1) entries of every block as columns
+// (TRANS: W^T . S, the mixing step of the backward pass).
+template <bool TRANS>
 __global__ void __launch_bounds__(kMixThreads)
 simt_mix(const float* __restrict__ W, const float* __restrict__ Sz, float* __restrict__ Szt,
          int64_t M, int64_t E, int64_t BH) {
@@ -113,7 +116,7 @@ simt_mix(const float* __restrict__ W, const float* __restrict__ Sz, float* __res
       const float s = src[j * E];
 #pragma unroll
       for (int u = 0; u < kMixRows; ++u)
-        if (i0 + u < M) acc[u] = fmaf(__ldg(W + (i0 + u) * M + j), s, acc[u]);
+        if (i0 + u < M) acc[u] = fmaf(__ldg(TRANS ? W + j * M + i0 + u : W + (i0 + u) * M + j), s, acc[u]);
     }
 #pragma unroll
     for (int u = 0; u < kMixRows; ++u)
@@ -165,6 +168,222 @@ simt_output(const T* __restrict__ q, Operand qo, T* __restrict__ o, Operand oo, 
   }
 }
 
+// ============================================================================
+// Backward pass.  The pages print none; these kernels follow the chain rule
+// through the three forward steps in reverse (the derivation is in the
+// header, next to mhla_backward):
+//   simt_bwd_query  per (b, h, query block i): dq, dS~_i = sum_t phi(q_t) dnum_t^T,
+//                   dz~_i = sum_t dden_t phi(q_t), with dnum_t = g_t / den_t and
+//                   dden_t = -(g_t . o_t) / den_t recomputed from S~_i, z~_i
+//   simt_mix<true>  dS_j = sum_i W[i][j] dS~_i, dz_j likewise
+//   simt_dw_*       dW[i][j] = sum_{b,h} <dS~_i, S_j> + dz~_i . z_j
+//   simt_bwd_key    per (b, h, source block j): dv_s = dS_j^T phi(k_s),
+//                   dk_s = (dS_j v_s + dz_j) * [k_s > 0]
+// ============================================================================
+constexpr int kBwdThreads = 256;
+constexpr int kBwdWarps = kBwdThreads / 32;
+constexpr int kBwdChunk = 32;   // tokens staged per accumulation step
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// One CTA per (b, h, i).  S~_i in shared memory with rows padded to d + 1 so
+// that lanes walking a column and lanes walking a row both avoid bank conflicts.
+template <typename T, int ENT>
+__global__ void __launch_bounds__(kBwdThreads)
+simt_bwd_query(const T* __restrict__ q, Operand qo, const T* __restrict__ g_out, Operand go, T* __restrict__ dq,
+               Operand dqo, TokenGeom g, int64_t H, int d, int phi_kind, float eps, const float* __restrict__ Szt,
+               float* __restrict__ dSzt) {
+  extern __shared__ float sm[];
+  const int E = d * d, P = d + 1;
+  float* st = sm;                          // [d][d + 1] S~_i
+  float* zt = st + d * P;                  // [d]        z~_i
+  float* sq = zt + d;                      // [kBwdChunk][d] phi(q_t)
+  float* sdn = sq + kBwdChunk * d;         // [kBwdChunk][d] dnum_t
+  float* sdd = sdn + kBwdChunk * d;        // [kBwdChunk]    dden_t
+  const int64_t item = blockIdx.x;
+  const int64_t i = item % g.M, bh = item / g.M;
+  const int64_t b = bh / H, h = bh % H;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const float* src = Szt + (bh * g.M + i) * static_cast<int64_t>(E + d);
+  for (int e = tid; e < E; e += kBwdThreads) st[(e / d) * P + e % d] = src[e];
+  for (int r = tid; r < d; r += kBwdThreads) zt[r] = src[E + r];
+  const T* qb = q + b * qo.sb + h * qo.sh;
+  const T* gb = g_out + b * go.sb + h * go.sh;
+  T* dqb = dq + b * dqo.sb + h * dqo.sh;
+
+  float acc[ENT];
+#pragma unroll
+  for (int m = 0; m < ENT; ++m) acc[m] = 0.0f;
+  float zacc = 0.0f;
+  __syncthreads();
+
+  for (int64_t s0 = 0; s0 < g.w; s0 += kBwdChunk) {
+    const int cnt = static_cast<int>(g.w - s0 < kBwdChunk ? g.w - s0 : kBwdChunk);
+    for (int sl = warp; sl < cnt; sl += kBwdWarps) {
+      const int64_t n = token_of(g, i, s0 + sl);
+      float* myq = sq + sl * d;
+      float* mydn = sdn + sl * d;
+      float den = 0.0f;
+      for (int r = lane; r < d; r += 32) {
+        const float x = phi_f(load_f(qb + n * qo.sn + r), phi_kind, eps);
+        myq[r] = x;
+        den = fmaf(x, zt[r], den);
+      }
+      den = warp_sum(den) + eps;
+      __syncwarp();
+      // num_c = sum_r phi(q)_r S~[r][c];  g . o = sum_c g_c num_c / den
+      float go_dot = 0.0f;
+      for (int c = lane; c < d; c += 32) {
+        float num = 0.0f;
+        for (int r = 0; r < d; ++r) num = fmaf(myq[r], st[r * P + c], num);
+        const float gc = load_f(gb + n * go.sn + c);
+        go_dot = fmaf(gc, num, go_dot);
+        mydn[c] = gc / den;
+      }
+      go_dot = warp_sum(go_dot) / den;
+      const float dden = -go_dot / den;
+      if (lane == 0) sdd[sl] = dden;
+      __syncwarp();
+      // dphi(q)_r = sum_c S~[r][c] dnum_c + dden z~_r, masked by phi'
+      for (int r = lane; r < d; r += 32) {
+        float x = dden * zt[r];
+        for (int c = 0; c < d; ++c) x = fmaf(st[r * P + c], mydn[c], x);
+        const float qr = load_f(qb + n * qo.sn + r);
+        store_f(dqb + n * dqo.sn + r, qr > 0.0f ? x : 0.0f);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < ENT; ++m) {
+      const int e = tid + m * kBwdThreads;
+      if (e < E) {
+        const int r = e / d, c = e % d;
+        float a = acc[m];
+        for (int sl = 0; sl < cnt; ++sl) a = fmaf(sq[sl * d + r], sdn[sl * d + c], a);
+        acc[m] = a;
+      }
+    }
+    if (tid < d)
+      for (int sl = 0; sl < cnt; ++sl) zacc = fmaf(sq[sl * d + tid], sdd[sl], zacc);
+    __syncthreads();
+  }
+  float* out = dSzt + (bh * g.M + i) * static_cast<int64_t>(E + d);
+#pragma unroll
+  for (int m = 0; m < ENT; ++m) {
+    const int e = tid + m * kBwdThreads;
+    if (e < E) out[e] = acc[m];
+  }
+  if (tid < d) out[E + tid] = zacc;
+}
+
+// One CTA per (b, h, j): dS_j (rows padded to d + 1) and dz_j in shared
+// memory, one warp per token.
+template <typename T>
+__global__ void __launch_bounds__(kBwdThreads)
+simt_bwd_key(const T* __restrict__ k, Operand ko, const T* __restrict__ v, Operand vo, T* __restrict__ dk,
+             Operand dko, T* __restrict__ dv, Operand dvo, TokenGeom g, int64_t H, int d, int phi_kind, float eps,
+             const float* __restrict__ dSz) {
+  extern __shared__ float sm[];
+  const int E = d * d, P = d + 1;
+  float* ds = sm;                          // [d][d + 1] dS_j
+  float* dz = ds + d * P;                  // [d]        dz_j
+  float* rows = dz + d;                    // [kBwdWarps][2 d] phi(k_s), v_s
+  const int64_t item = blockIdx.x;
+  const int64_t j = item % g.M, bh = item / g.M;
+  const int64_t b = bh / H, h = bh % H;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const float* src = dSz + (bh * g.M + j) * static_cast<int64_t>(E + d);
+  for (int e = tid; e < E; e += kBwdThreads) ds[(e / d) * P + e % d] = src[e];
+  for (int r = tid; r < d; r += kBwdThreads) dz[r] = src[E + r];
+  __syncthreads();
+  const T* kb = k + b * ko.sb + h * ko.sh;
+  const T* vb = v + b * vo.sb + h * vo.sh;
+  T* dkb = dk + b * dko.sb + h * dko.sh;
+  T* dvb = dv + b * dvo.sb + h * dvo.sh;
+  float* myk = rows + warp * 2 * d;
+  float* myv = myk + d;
+  for (int64_t s = warp; s < g.w; s += kBwdWarps) {
+    const int64_t n = token_of(g, j, s);
+    for (int r = lane; r < d; r += 32) {
+      myk[r] = phi_f(load_f(kb + n * ko.sn + r), phi_kind, eps);
+      myv[r] = load_f(vb + n * vo.sn + r);
+    }
+    __syncwarp();
+    for (int c = lane; c < d; c += 32) {     // dv_c = sum_r phi(k)_r dS[r][c]
+      float x = 0.0f;
+      for (int r = 0; r < d; ++r) x = fmaf(myk[r], ds[r * P + c], x);
+      store_f(dvb + n * dvo.sn + c, x);
+    }
+    for (int r = lane; r < d; r += 32) {     // dphi(k)_r = sum_c dS[r][c] v_c + dz_r
+      float x = dz[r];
+      for (int c = 0; c < d; ++c) x = fmaf(ds[r * P + c], myv[c], x);
+      const float kr = load_f(kb + n * ko.sn + r);
+      store_f(dkb + n * dko.sn + r, kr > 0.0f ? x : 0.0f);
+    }
+    __syncwarp();
+  }
+}
+
+constexpr int kDwTile = 64;     // 64 x 64 outputs per CTA, 4 x 4 per thread
+constexpr int kDwK = 32;        // entries of the contraction staged per step
+
+// part[bh][i][j] = sum_e dSzt[bh][i][e] * Sz[bh][j][e]   (one (b, h) per z index)
+__global__ void __launch_bounds__(256)
+simt_dw_partial(const float* __restrict__ dSzt, const float* __restrict__ Sz, float* __restrict__ part, int64_t M,
+                int64_t E) {
+  __shared__ float sa[kDwK][kDwTile + 4];
+  __shared__ float sb[kDwK][kDwTile + 4];
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kDwTile, j0 = static_cast<int64_t>(blockIdx.y) * kDwTile;
+  const int64_t bh = blockIdx.z;
+  const float* A = dSzt + bh * M * E;
+  const float* Bm = Sz + bh * M * E;
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  float acc[4][4] = {};
+  for (int64_t e0 = 0; e0 < E; e0 += kDwK) {
+    for (int x = threadIdx.x; x < kDwK * kDwTile; x += 256) {
+      const int row = x / kDwK, kk = x % kDwK;
+      const int64_t e = e0 + kk;
+      sa[kk][row] = (i0 + row < M && e < E) ? A[(i0 + row) * E + e] : 0.0f;
+      sb[kk][row] = (j0 + row < M && e < E) ? Bm[(j0 + row) * E + e] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < kDwK; ++kk) {
+      float a[4], bb[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        a[u] = sa[kk][ty * 4 + u];
+        bb[u] = sb[kk][tx * 4 + u];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(a[u], bb[w], acc[u][w]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int64_t ii = i0 + ty * 4 + u, jj = j0 + tx * 4 + w;
+      if (ii < M && jj < M) part[(bh * M + ii) * M + jj] = acc[u][w];
+    }
+}
+
+// dW = sum over (b, h) of the partials, in a fixed order (deterministic).
+__global__ void simt_dw_reduce(const float* __restrict__ part, float* __restrict__ dW, int64_t MM, int64_t BH) {
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (x >= MM) return;
+  float s = 0.0f;
+  for (int64_t bh = 0; bh < BH; ++bh) s += part[bh * MM + x];
+  dW[x] = s;
+}
+
 template <typename T>
 int launch_simt_typed(const Problem& p, const float* W, const SimtWorkspace& ws, cudaStream_t stream) {
   const TokenGeom g = token_geom(p);
@@ -201,7 +420,7 @@ int launch_simt_typed(const Problem& p, const float* W, const SimtWorkspace& ws,
   if (mix_grid.y > 65535) return MHLA_ERR_UNSUPPORTED;
   {
     KernelTimer timer("simt_mix", stream);
-    simt_mix<<<mix_grid, kMixThreads, 0, stream>>>(W, ws.Sz, ws.Szt, p.M, E, BH);
+    simt_mix<false><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.Sz, ws.Szt, p.M, E, BH);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
 
@@ -215,6 +434,100 @@ int launch_simt_typed(const Problem& p, const float* W, const SimtWorkspace& ws,
     KernelTimer timer("simt_output", stream);
     simt_output<T><<<static_cast<unsigned>(items), kOutThreads, out_smem, stream>>>(
         qp, p.q, op, p.o, g, p.H, d, p.phi_kind, p.eps, ws.Szt);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  return MHLA_OK;
+}
+
+template <typename T>
+int launch_simt_bwd_typed(const Problem& p, const float* W, const BwdOperands& bo, const SimtBwdWorkspace& ws,
+                          cudaStream_t stream) {
+  const TokenGeom g = token_geom(p);
+  const int d = static_cast<int>(p.d);
+  const int64_t BH = p.BH();
+  const int64_t items = BH * p.M;
+  if (items > 0x7fffffffLL || BH > 65535) return MHLA_ERR_UNSUPPORTED;
+  const T* qp = static_cast<const T*>(p.q.data);
+  const T* kp = static_cast<const T*>(p.k.data);
+  const T* vp = static_cast<const T*>(p.v.data);
+  const T* gp = static_cast<const T*>(bo.dout.data);
+  T* dqp = static_cast<T*>(bo.dq.data);
+  T* dkp = static_cast<T*>(bo.dk.data);
+  T* dvp = static_cast<T*>(bo.dv.data);
+  const int64_t E = p.d * (p.d + 1);
+
+  // forward summaries and mixing, recomputed
+  {
+    const size_t sum_smem = 2 * kSumChunk * d * sizeof(float);
+    KernelTimer timer("simt_summary", stream);
+    if (d <= 16)
+      simt_summary<T, 1><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    else if (d <= 32)
+      simt_summary<T, 4><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    else if (d <= 64)
+      simt_summary<T, 16><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    else
+      simt_summary<T, 64><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  const dim3 mix_grid(static_cast<unsigned>((E + kMixThreads - 1) / kMixThreads),
+                      static_cast<unsigned>((p.M + kMixRows - 1) / kMixRows),
+                      static_cast<unsigned>(std::min<int64_t>(BH, 65535)));
+  if (mix_grid.y > 65535) return MHLA_ERR_UNSUPPORTED;
+  {
+    KernelTimer timer("simt_mix", stream);
+    simt_mix<false><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.Sz, ws.Szt, p.M, E, BH);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  // query blocks: dq, dS~, dz~
+  {
+    const size_t smem = (d * (d + 1) + d + 2 * kBwdChunk * d + kBwdChunk) * sizeof(float);
+    auto launch = [&](auto kern) -> int {
+      if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem)) != cudaSuccess)
+        return MHLA_ERR_CUDA;
+      KernelTimer timer("simt_bwd_query", stream);
+      kern<<<static_cast<unsigned>(items), kBwdThreads, smem, stream>>>(qp, p.q, gp, bo.dout, dqp, bo.dq, g, p.H, d,
+                                                                          p.phi_kind, p.eps, ws.Szt, ws.dSzt);
+      return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+    };
+    const int rc = d <= 16   ? launch(simt_bwd_query<T, 1>)
+                   : d <= 32 ? launch(simt_bwd_query<T, 4>)
+                   : d <= 64 ? launch(simt_bwd_query<T, 16>)
+                             : launch(simt_bwd_query<T, 64>);
+    if (rc != MHLA_OK) return rc;
+  }
+  // dW (before the transposed mixing overwrites S~ with dS)
+  {
+    const dim3 grid(static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile),
+                    static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile), static_cast<unsigned>(BH));
+    if (grid.x > 65535) return MHLA_ERR_UNSUPPORTED;
+    KernelTimer timer("simt_dw", stream);
+    simt_dw_partial<<<grid, 256, 0, stream>>>(ws.dSzt, ws.Sz, ws.part, p.M, E);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+    const int64_t MM = p.M * p.M;
+    simt_dw_reduce<<<static_cast<unsigned>((MM + 255) / 256), 256, 0, stream>>>(ws.part, bo.dW, MM, BH);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  // dS = W^T dS~ into the S~ buffer
+  {
+    KernelTimer timer("simt_mix", stream);
+    simt_mix<true><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.dSzt, ws.Szt, p.M, E, BH);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  // source blocks: dk, dv
+  {
+    const size_t smem = (d * (d + 1) + d + 2 * kBwdWarps * d) * sizeof(float);
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(simt_bwd_key<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem)) != cudaSuccess)
+      return MHLA_ERR_CUDA;
+    KernelTimer timer("simt_bwd_key", stream);
+    simt_bwd_key<T><<<static_cast<unsigned>(items), kBwdThreads, smem, stream>>>(
+        kp, p.k, vp, p.v, dkp, bo.dk, dvp, bo.dv, g, p.H, d, p.phi_kind, p.eps, ws.Szt);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
   return MHLA_OK;
@@ -238,6 +551,25 @@ int launch_simt(const Problem& p, const float* W, void* workspace, void* stream)
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.dtype == MHLA_BF16) return launch_simt_typed<__nv_bfloat16>(p, W, ws, s);
   return launch_simt_typed<float>(p, W, ws, s);
+}
+
+size_t simt_bwd_workspace_bytes(const Problem& p) {
+  const size_t per = static_cast<size_t>(p.BH()) * p.M * p.d * (p.d + 1) * sizeof(float);
+  const size_t part = static_cast<size_t>(p.BH()) * p.M * p.M * sizeof(float);
+  return 3 * align_up(per) + align_up(part);
+}
+
+int launch_simt_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream) {
+  const size_t per = static_cast<size_t>(p.BH()) * p.M * p.d * (p.d + 1) * sizeof(float);
+  char* c = static_cast<char*>(workspace);
+  SimtBwdWorkspace ws;
+  ws.Sz = reinterpret_cast<float*>(c);
+  ws.Szt = reinterpret_cast<float*>(c + align_up(per));
+  ws.dSzt = reinterpret_cast<float*>(c + 2 * align_up(per));
+  ws.part = reinterpret_cast<float*>(c + 3 * align_up(per));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.dtype == MHLA_BF16) return launch_simt_bwd_typed<__nv_bfloat16>(p, W, bo, ws, s);
+  return launch_simt_bwd_typed<float>(p, W, bo, ws, s);
 }
 
 }  // namespace mhla
