@@ -267,7 +267,10 @@ def test_backward_rejects_malformed_requests_before_any_launch(L):
     assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, ws=FAKE + 7, ws_bytes=1 << 40) == WORKSPACE
     assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, ws=FAKE, ws_bytes=16) == WORKSPACE
     assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, ws=None, ws_bytes=16) == WORKSPACE
-    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, path=2) == UNSUPPORTED
+    assert call_backward(L, q, k, v, g, dq, dk, dv, grid, (4, 4), path=2) == UNSUPPORTED   # 16-token blocks
+    st68 = (1024 * 3 * 68, 3 * 68, 68)
+    dv68 = mhla.tensor_desc(dv.data, "bf16", (2, 1024, 3, 64), st68)
+    assert call_backward(L, q, k, v, g, dq, dk, dv68, grid, block, path=2) == UNSUPPORTED   # TMA-unfit dv
     assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, path=3) == UNSUPPORTED
     assert call_backward(L, q, k, v, g, dq, dk, dv, grid, block, path=9) == INVALID
 
@@ -275,12 +278,19 @@ def test_backward_rejects_malformed_requests_before_any_launch(L):
 def test_backward_workspace_size(L):
     wl = WORKLOADS["dit_s2_4096px"]
     q = contig(wl.B, wl.N, wl.H, wl.d)
-    n = ctypes.c_size_t()
-    for path in (0, 1):
+    M, BH, d = wl.M, wl.B * wl.H, wl.d
+    sizes = {}
+    for path in (0, 1, 2):
+        n = ctypes.c_size_t()
         assert L.mhla_backward_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
                                               ctypes.byref(mhla.shape3(wl.block)), path, ctypes.byref(n)) == OK
-        per = wl.B * wl.H * wl.M * wl.d * (wl.d + 1) * 4
-        expect = 3 * per + wl.B * wl.H * wl.M * wl.M * 4
-        assert expect <= n.value < expect + 4 * 256 and n.value % 256 == 0
+        assert n.value % 256 == 0
+        sizes[path] = n.value
+    simt = 3 * BH * M * d * (d + 1) * 4 + BH * M * M * 4
+    assert simt <= sizes[1] < simt + 4 * 256
+    groups = (BH * (d + 1) * d + 127) // 128
+    tc = 2 * M * M * 2 + 2 * M * groups * 128 * 2 + BH * M * d * d * 2 + BH * M * d * 4
+    assert tc < sizes[2] <= tc + 76 * M * M * 4 + 8 * 256          # + the split dW partial products
+    assert sizes[0] == max(sizes[1], sizes[2])                         # AUTO: enough for either path
     assert L.mhla_backward_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
-                                          ctypes.byref(mhla.shape3(wl.block)), 2, ctypes.byref(n)) == UNSUPPORTED
+                                          ctypes.byref(mhla.shape3(wl.block)), 3, ctypes.byref(n)) == UNSUPPORTED

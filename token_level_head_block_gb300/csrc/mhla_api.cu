@@ -202,13 +202,25 @@ extern "C" mhla_status_t mhla_forward(const mhla_tensor_t* q, const mhla_tensor_
 namespace mhla {
 namespace {
 
-int resolve_bwd_path(int32_t path, int* sel) {
-  if (path == MHLA_PATH_AUTO || path == MHLA_PATH_SIMT) { *sel = MHLA_PATH_SIMT; return MHLA_OK; }
-  if (path == MHLA_PATH_TC || path == MHLA_PATH_FUSED) return MHLA_ERR_UNSUPPORTED;
+// AUTO takes the tensor-core backward whenever every operand qualifies.
+int resolve_bwd_path(const Problem& p, const BwdOperands& bo, int32_t path, int* sel) {
+  if (path == MHLA_PATH_AUTO) {
+    *sel = tc_bwd_eligible(p, bo) ? MHLA_PATH_TC : MHLA_PATH_SIMT;
+    return MHLA_OK;
+  }
+  if (path == MHLA_PATH_SIMT) { *sel = MHLA_PATH_SIMT; return MHLA_OK; }
+  if (path == MHLA_PATH_TC) {
+    if (!tc_bwd_eligible(p, bo)) return MHLA_ERR_UNSUPPORTED;
+    *sel = MHLA_PATH_TC;
+    return MHLA_OK;
+  }
+  if (path == MHLA_PATH_FUSED) return MHLA_ERR_UNSUPPORTED;
   return MHLA_ERR_INVALID_ARG;
 }
 
-size_t bwd_workspace_for(const Problem& p, int /*sel*/) { return simt_bwd_workspace_bytes(p); }
+size_t bwd_workspace_for(const Problem& p, int sel) {
+  return sel == MHLA_PATH_TC ? tc_bwd_workspace_bytes(p) : simt_bwd_workspace_bytes(p);
+}
 
 }  // namespace
 }  // namespace mhla
@@ -219,10 +231,21 @@ extern "C" mhla_status_t mhla_backward_workspace_size(const mhla_tensor_t* q, co
   Problem p;
   const int rc = build_problem(q, q, q, q, grid, block, nullptr, /*check_alias=*/false, &p);
   if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+  // Only q is known here: the operands of the later call take q's strides.
+  BwdOperands bo;
+  bo.dout = bo.dq = bo.dk = bo.dv = p.q;
+  bo.dW = nullptr;
   int sel = 0;
-  const int rp = resolve_bwd_path(path, &sel);
+  const int rp = resolve_bwd_path(p, bo, path, &sel);
   if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
-  *bytes = (p.B == 0 || p.H == 0) ? 0 : bwd_workspace_for(p, sel);
+  if (p.B == 0 || p.H == 0) {
+    *bytes = 0;
+  } else if (path == MHLA_PATH_AUTO && sel == MHLA_PATH_TC) {
+    // enough for either path, whichever AUTO takes for the actual operands
+    *bytes = std::max(tc_bwd_workspace_bytes(p), simt_bwd_workspace_bytes(p));
+  } else {
+    *bytes = bwd_workspace_for(p, sel);
+  }
   return MHLA_OK;
 }
 
@@ -240,8 +263,14 @@ extern "C" mhla_status_t mhla_backward(const mhla_tensor_t* q, const mhla_tensor
     if (rt != MHLA_OK) return static_cast<mhla_status_t>(rt);
     if (!same_shape(q, t)) return MHLA_ERR_SHAPE;
   }
+  BwdOperands bo;
+  bo.dout = Operand{dout->data, dout->stride_b, dout->stride_n, dout->stride_h};
+  bo.dq = Operand{dq->data, dq->stride_b, dq->stride_n, dq->stride_h};
+  bo.dk = Operand{dk->data, dk->stride_b, dk->stride_n, dk->stride_h};
+  bo.dv = Operand{dv->data, dv->stride_b, dv->stride_n, dv->stride_h};
+  bo.dW = dW;
   int sel = 0;
-  const int rp = resolve_bwd_path(path, &sel);
+  const int rp = resolve_bwd_path(p, bo, path, &sel);
   if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
   if (!W || !dW) return MHLA_ERR_INVALID_ARG;
   const uintptr_t w_bytes = static_cast<uintptr_t>(p.M * p.M) * sizeof(float);
@@ -269,29 +298,24 @@ extern "C" mhla_status_t mhla_backward(const mhla_tensor_t* q, const mhla_tensor
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.B == 0 || p.H == 0)   // no (b, h) contributes: dW is zero
     return cudaMemsetAsync(dW, 0, w_bytes, s) == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
-  BwdOperands bo;
-  bo.dout = Operand{dout->data, dout->stride_b, dout->stride_n, dout->stride_h};
-  bo.dq = Operand{dq->data, dq->stride_b, dq->stride_n, dq->stride_h};
-  bo.dk = Operand{dk->data, dk->stride_b, dk->stride_n, dk->stride_h};
-  bo.dv = Operand{dv->data, dv->stride_b, dv->stride_n, dv->stride_h};
-  bo.dW = dW;
   bool owned = false;
   if (!ws) {
     if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return MHLA_ERR_CUDA;
     owned = true;
   }
-  const int lr = launch_simt_bwd(p, W, bo, ws, stream);
+  const int lr = sel == MHLA_PATH_TC ? launch_tc_bwd(p, W, bo, ws, stream) : launch_simt_bwd(p, W, bo, ws, stream);
   if (owned && cudaFreeAsync(ws, s) != cudaSuccess && lr == MHLA_OK) return MHLA_ERR_CUDA;
   return static_cast<mhla_status_t>(lr);
 }
 
 extern "C" mhla_status_t mhla_device_status(void* stream, uint32_t* flags) {
   if (!flags) return MHLA_ERR_INVALID_ARG;
-  uint32_t tc = 0, small = 0;
+  uint32_t tc = 0, small = 0, bwd = 0;
   const int a = read_and_clear_device_error(stream, &tc);
   const int b = read_and_clear_small_error(stream, &small);
-  if (a == MHLA_ERR_CUDA || b == MHLA_ERR_CUDA) return MHLA_ERR_CUDA;
-  *flags = tc | small;
+  const int c = read_and_clear_bwd_error(stream, &bwd);
+  if (a == MHLA_ERR_CUDA || b == MHLA_ERR_CUDA || c == MHLA_ERR_CUDA) return MHLA_ERR_CUDA;
+  *flags = tc | small | bwd;
   return *flags ? MHLA_ERR_TIMEOUT : MHLA_OK;
 }
 

@@ -66,6 +66,15 @@ struct SimtBwdWorkspace {
 size_t simt_bwd_workspace_bytes(const Problem& p);
 int launch_simt_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream);
 
+// Tensor-core backward (bf16, d in {32, 64}, the forward tensor-core path's
+// token geometry, TMA-friendly strides on every operand).  Workspace: Wb and
+// W^T in bf16 [M][Mp]; Sbuf and dSbuf as the forward's Sbuf; St, zt as the
+// forward's (S~, z~, later overwritten with dS, dz); float32 dW partials.
+bool tc_bwd_eligible(const Problem& p, const BwdOperands& bo);
+size_t tc_bwd_workspace_bytes(const Problem& p);
+int launch_tc_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream);
+int read_and_clear_bwd_error(void* stream, uint32_t* flags);
+
 // Workspace layout of the tensor-core path:
 //   Wb   bf16 [M][Mp]                  W rounded to bf16, Mp = round_up(M, 8)
 //   Sbuf bf16 [G][M][128]               columns col = (b,h) then the d rows of S_j
@@ -81,6 +90,12 @@ int launch_tc(const Problem& p, const float* W, void* workspace, void* stream);
 // {32, 64}): one launch that forms the two-stage N x N product; no workspace.
 bool small_eligible(const Problem& p);
 int launch_small(const Problem& p, const float* W, void* stream);
+
+// Steps of the tensor-core path on caller-given buffers (layouts as above):
+// tc_run_summary writes Wb (and W^T into WbT when WbT is not null) and Sbuf;
+// tc_run_mix computes St, zt = Wm . Sbuf for the bf16 [M][Mp] matrix Wm.
+int tc_run_summary(const Problem& p, const float* W, void* Wb, void* WbT, int64_t Mp, void* Sbuf, void* stream);
+int tc_run_mix(const Problem& p, const void* Wm, int64_t Mp, const void* Sbuf, void* St, float* zt, void* stream);
 
 // Device error words of the tensor-core and fused kernels (bounded waits).
 int read_and_clear_device_error(void* stream, uint32_t* flags);

@@ -32,6 +32,7 @@
 
 #include "mhla_internal.h"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 #include "tma_host.h"
 
 namespace mhla {
@@ -42,91 +43,15 @@ namespace {
 
 using namespace ptx;
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr uint32_t kWaitLimitPolls = 1u << 28;
-constexpr uint64_t kDrainLimitNs = 50000000ull;   // 50 ms for copies already in flight
+using namespace tc;
 
-__device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1; it < kWaitLimitPolls; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) break;
-    }
-  }
-  *abort_flag = 1u;
-  atomicOr(&g_tc_error, 1u);
-  return false;
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
+  return wait_bounded_on(bar, parity, abort_flag, &g_tc_error);
 }
-
-// Every lane waits, then the warp agrees: warp-collective instructions that
-// follow (shuffles, tcgen05.ld) run either on all lanes or on none.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
-  const bool ok = wait_bounded(bar, parity, abort_flag);
-  return __all_sync(0xffffffffu, ok);
+  return warp_wait_on(bar, parity, abort_flag, &g_tc_error);
 }
-
-// Wait for a phase that must already be under way (copies or MMAs in flight),
-// without consulting the abort flag.
-__device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 0; it < kWaitLimitPolls; ++it) {
-    if (mbar_try_wait(bar, parity)) return;
-    if ((it & 63u) == 63u && globaltimer() - t0 > kDrainLimitNs) {
-      atomicOr(&g_tc_error, 2u);
-      return;
-    }
-  }
-}
-
-// Token-grid geometry of one launch (all int32: checked on the host).
-struct TcGeom {
-  int32_t M, nbx, nby;     // block grid, x fastest
-  int32_t bx, by, bt, T;   // block extents; frames per batch image (1 for 2-D)
-  int32_t box_y, box_t;    // TMA box of one chunk along y and t (x: whole block rows)
-  int32_t nyc;             // chunks stacked along y inside one frame of a block
-  int32_t chunks;          // chunks per block
-  int32_t H, B;
-};
-
-// Coordinates (x, y, z = b*T + t) of chunk c of block j of batch b.
-__device__ __forceinline__ void chunk_coords(const TcGeom& g, int32_t j, int32_t c, int32_t b, int32_t& x,
-                                             int32_t& y, int32_t& z) {
-  const int32_t jx = j % g.nbx, jr = j / g.nbx;
-  const int32_t jy = jr % g.nby, jt = jr / g.nby;
-  x = jx * g.bx;
-  y = jy * g.by + (c % g.nyc) * g.box_y;
-  z = b * g.T + jt * g.bt + (c / g.nyc) * g.box_t;
-}
-
-// phi on eight bf16 values in place with packed bf16 arithmetic (no float32
-// round trip): max(x, 0), then + eps under MHLA_PHI_RELU_EPS.
-__device__ __forceinline__ uint4 phi8_packed(uint4 raw, bool add_eps, __nv_bfloat162 eps2) {
-  const __nv_bfloat162 zero = __float2bfloat162_rn(0.0f);
-  uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w[e]);
-    v = __hmax2(v, zero);
-    if (add_eps) v = __hadd2(v, eps2);
-    w[e] = *reinterpret_cast<uint32_t*>(&v);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// 16-byte chunk position inside a swizzled row: 128-byte swizzle for d = 64
-// (row r XORs chunk bits with r mod 8), 64-byte swizzle for d = 32.
-template <int D>
-__device__ __forceinline__ int swz(int row) {
-  return D == 64 ? (row & 7) : ((row >> 1) & 3);
-}
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) { drain_wait_on(bar, parity, &g_tc_error); }
 
 // ============================================================================
 // tc_summary
@@ -157,7 +82,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, TcGeom g,
            int32_t G, int64_t n_items, int phi_kind, float eps,
            __nv_bfloat16* __restrict__ Sbuf, const float* __restrict__ W, __nv_bfloat16* __restrict__ Wb,
-           int64_t Mp) {
+           __nv_bfloat16* __restrict__ WbT, int64_t Mp) {
   using Cfg = SumCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
@@ -173,14 +98,16 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   volatile uint32_t* abortf = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // W rounded to bf16 for the mixing GEMM, [M][Mp] with zero padding; every CTA
-  // converts a slice (the GEMM runs after this kernel on the same stream).
+  // W rounded to bf16 for the mixing GEMM, [M][Mp] with zero padding (and, when
+  // WbT is given, W^T likewise); every CTA converts a slice (the GEMM runs after
+  // this kernel on the same stream).
   {
     const int64_t n = static_cast<int64_t>(g.M) * Mp;
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * kTcThreads + threadIdx.x; e < n;
          e += static_cast<int64_t>(gridDim.x) * kTcThreads) {
       const int64_t i = e / Mp, j = e % Mp;
       Wb[e] = __float2bfloat16_rn(j < g.M ? W[i * g.M + j] : 0.0f);
+      if (WbT) WbT[e] = __float2bfloat16_rn(j < g.M ? W[j * g.M + i] : 0.0f);   // W^T for the backward
     }
   }
   if (threadIdx.x == 0) {
@@ -1085,59 +1012,6 @@ bool encode(CUtensorMap* m, int rank, void* base, const cuuint64_t* dims, const 
             swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct ChunkPlan {
-  int64_t box_y, box_t, nyc, chunks;
-};
-
-// Split every block into chunks of C tokens made of whole block rows (and,
-// where a frame holds fewer than C tokens, whole frames).
-bool chunk_plan(const Problem& p, int64_t C, ChunkPlan* cp) {
-  if (p.w % C != 0 || C % p.bx != 0 || p.bx > 256) return false;
-  const int64_t rows = C / p.bx;
-  if (rows <= p.by) {
-    if (p.by % rows != 0) return false;
-    cp->box_y = rows;
-    cp->box_t = 1;
-    cp->nyc = p.by / rows;
-  } else {
-    if (rows % p.by != 0) return false;
-    const int64_t frames = rows / p.by;
-    if (p.bt % frames != 0) return false;
-    cp->box_y = p.by;
-    cp->box_t = frames;
-    cp->nyc = 1;
-  }
-  if (cp->box_y > 256 || cp->box_t > 256) return false;
-  cp->chunks = p.w / C;
-  return true;
-}
-
-bool operand_tma_ok(const Problem& p, const Operand& o) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(o.data);
-  if (a % 16 != 0) return false;
-  if (o.sh % 8 != 0 || o.sn % 8 != 0 || o.sb % 8 != 0) return false;
-  if ((p.H > 1 && o.sh <= 0) || o.sn <= 0) return false;
-  if (p.T > 1 && o.sb != p.T * p.Y * p.X * o.sn) return false;   // (b, t) fold into one dimension
-  const int64_t zstride = p.T > 1 ? p.Y * p.X * o.sn : o.sb;
-  if (p.B > 1 && zstride <= 0) return false;
-  const int64_t lim = int64_t{1} << 39;   // strides in bytes below 2^40
-  return o.sh < lim && o.sn * p.X < lim && zstride < lim;
-}
-
-bool operand_map(const Problem& p, const Operand& o, int64_t box_y, int64_t box_t, CUtensorMap* m) {
-  const int64_t zstride = p.T > 1 ? p.Y * p.X * o.sn : (p.B > 1 ? o.sb : p.Y * p.X * o.sn);
-  const int64_t sh = p.H > 1 ? o.sh : p.d;
-  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(p.H),
-                              static_cast<cuuint64_t>(p.X), static_cast<cuuint64_t>(p.Y),
-                              static_cast<cuuint64_t>(p.B * p.T)};
-  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(sh * 2), static_cast<cuuint64_t>(o.sn * 2),
-                                 static_cast<cuuint64_t>(p.X * o.sn * 2), static_cast<cuuint64_t>(zstride * 2)};
-  const cuuint32_t box[5] = {static_cast<cuuint32_t>(p.d), 1u, static_cast<cuuint32_t>(p.bx),
-                             static_cast<cuuint32_t>(box_y), static_cast<cuuint32_t>(box_t)};
-  return encode(m, 5, o.data, dims, strides, box,
-                p.d == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-}
-
 struct TcLayout {
   size_t wb_off, sbuf_off, st_off, zt_off, total;
   int64_t Mp, ncols, ngroups;
@@ -1175,22 +1049,114 @@ int occupancy(K kernel, int threads, size_t smem) {
   return n;
 }
 
-TcGeom make_geom(const Problem& p, const ChunkPlan& cp) {
-  TcGeom g;
-  g.M = static_cast<int32_t>(p.M);
-  g.nbx = static_cast<int32_t>(p.nbx);
-  g.nby = static_cast<int32_t>(p.nby);
-  g.bx = static_cast<int32_t>(p.bx);
-  g.by = static_cast<int32_t>(p.by);
-  g.bt = static_cast<int32_t>(p.bt);
-  g.T = static_cast<int32_t>(p.T);
-  g.box_y = static_cast<int32_t>(cp.box_y);
-  g.box_t = static_cast<int32_t>(cp.box_t);
-  g.nyc = static_cast<int32_t>(cp.nyc);
-  g.chunks = static_cast<int32_t>(cp.chunks);
-  g.H = static_cast<int32_t>(p.H);
-  g.B = static_cast<int32_t>(p.B);
-  return g;
+template <int D>
+int run_summary(const Problem& p, const float* W, __nv_bfloat16* Wb, __nv_bfloat16* WbT, int64_t Mp,
+                __nv_bfloat16* Sbuf, cudaStream_t stream) {
+  using Cfg = SumCfg<D>;
+  const int sms = device_sms();
+  if (sms <= 0) return MHLA_ERR_CUDA;
+  ChunkPlan c64;
+  if (!chunk_plan(p, 64, &c64)) return MHLA_ERR_UNSUPPORTED;
+  CUtensorMap tk, tv;
+  if (!operand_map(p, p.k, c64.box_y, c64.box_t, &tk) || !operand_map(p, p.v, c64.box_y, c64.box_t, &tv))
+    return MHLA_ERR_CUDA;
+  const int32_t G = static_cast<int32_t>((p.H + Cfg::HP - 1) / Cfg::HP);
+  const int64_t n_items = p.B * G * p.M;
+  if (cudaFuncSetAttribute(tc_summary<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(Cfg::SMEM)) != cudaSuccess)
+    return MHLA_ERR_CUDA;
+  const int per_sm = std::max(1, occupancy(tc_summary<D>, kTcThreads, Cfg::SMEM));
+  const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
+  KernelTimer timer("tc_summary", stream);
+  tc_summary<D><<<grid, kTcThreads, Cfg::SMEM, stream>>>(tk, tv, make_geom(p, c64), G, n_items, p.phi_kind, p.eps,
+                                                         Sbuf, W, Wb, WbT, Mp);
+  return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+}
+
+// D[i, col] = sum_j Wm[i][j] Sbuf[j][col] for the ncols = BH (d + 1) d columns:
+// S~ (row-major [BH][M][d][d]) and z~ (float32 [BH][M][d]).
+template <int D>
+int run_mix(const Problem& p, const __nv_bfloat16* Wm, int64_t Mp, const __nv_bfloat16* Sbuf, __nv_bfloat16* St,
+            float* zt, cudaStream_t stream) {
+  const int sms = device_sms();
+  if (sms <= 0) return MHLA_ERR_CUDA;
+  const int64_t ncols = p.BH() * (p.d + 1) * p.d;
+  const int64_t ngroups = (ncols + 127) / 128;
+  // Sbuf as (128 columns, M source blocks, G groups)
+  const cuuint64_t sdims[3] = {128u, static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(ngroups)};
+  const cuuint64_t sstrides[2] = {256u, static_cast<cuuint64_t>(p.M * 256)};
+  const cuuint64_t wdims[2] = {static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.M)};
+  const cuuint64_t wstrides[1] = {static_cast<cuuint64_t>(Mp * 2)};
+  void* wptr = const_cast<__nv_bfloat16*>(Wm);
+  void* sptr = const_cast<__nv_bfloat16*>(Sbuf);
+  if (p.M <= 256) {   // all of W in shared memory
+    CUtensorMap tw, ts;
+    const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(MixResCfg::KC), static_cast<cuuint32_t>(MixResCfg::ROWS)};
+    const cuuint32_t sbox[3] = {64u, static_cast<cuuint32_t>(MixResCfg::KC), 1u};
+    if (!encode(&tw, 2, wptr, wdims, wstrides, wbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&ts, 3, sptr, sdims, sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MHLA_ERR_CUDA;
+    const int32_t n_tiles = static_cast<int32_t>((ncols + MixResCfg::COLS - 1) / MixResCfg::COLS);
+    if (cudaFuncSetAttribute(tc_mix_resident<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(MixResCfg::SMEM)) != cudaSuccess)
+      return MHLA_ERR_CUDA;
+    const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
+    KernelTimer timer("tc_mix", stream);
+    tc_mix_resident<D><<<grid, kMixThreadsTC, MixResCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), ncols,
+                                                                          n_tiles, St, zt);
+    return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+  }
+  CUtensorMap tw, ts;
+  const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(MixCfg::KC), static_cast<cuuint32_t>(MixCfg::ROWS)};
+  const cuuint32_t sbox[3] = {64u, static_cast<cuuint32_t>(MixCfg::KC), 1u};
+  if (!encode(&tw, 2, wptr, wdims, wstrides, wbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode(&ts, 3, sptr, sdims, sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MHLA_ERR_CUDA;
+  const int32_t n_col_tiles = static_cast<int32_t>((ncols + MixCfg::COLS - 1) / MixCfg::COLS);
+  const int32_t n_i_tiles = static_cast<int32_t>((p.M + MixCfg::ROWS - 1) / MixCfg::ROWS);
+  if (cudaFuncSetAttribute(tc_mix<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(MixCfg::SMEM)) !=
+      cudaSuccess)
+    return MHLA_ERR_CUDA;
+  const int64_t n_tiles = static_cast<int64_t>(n_col_tiles) * n_i_tiles;
+  const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
+  KernelTimer timer("tc_mix", stream);
+  tc_mix<D><<<grid, kMixThreadsTC, MixCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), ncols, n_col_tiles,
+                                                            n_i_tiles, St, zt);
+  return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+}
+
+template <int D>
+int run_output(const Problem& p, const __nv_bfloat16* St, const float* zt, cudaStream_t stream) {
+  using Cfg = OutCfg<D>;
+  const int sms = device_sms();
+  if (sms <= 0) return MHLA_ERR_CUDA;
+  ChunkPlan c128;
+  if (!chunk_plan(p, 128, &c128)) return MHLA_ERR_UNSUPPORTED;
+  CUtensorMap tq, to;
+  if (!operand_map(p, p.q, c128.box_y, c128.box_t, &tq) || !operand_map(p, p.o, c128.box_y, c128.box_t, &to))
+    return MHLA_ERR_CUDA;
+  // S~ tiles (row-major [BH*M][d][d]) seen as (c % 8, r, c / 8, tile): a
+  // (8, d, d/8, 1) box lands as 16-byte rows of 8 columns, d rows per column
+  // group: the unswizzled MN-major operand layout.
+  CUtensorMap tst;
+  {
+    const cuuint64_t dims[4] = {8u, static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(p.d / 8),
+                                static_cast<cuuint64_t>(p.BH() * p.M)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(p.d * 2), 16u, static_cast<cuuint64_t>(p.d * p.d * 2)};
+    const cuuint32_t box[4] = {8u, static_cast<cuuint32_t>(p.d), static_cast<cuuint32_t>(p.d / 8), 1u};
+    if (!encode(&tst, 4, const_cast<__nv_bfloat16*>(St), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MHLA_ERR_CUDA;
+  }
+  const int64_t n_items = p.BH() * p.M;
+  if (cudaFuncSetAttribute(tc_output<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::SMEM)) !=
+      cudaSuccess)
+    return MHLA_ERR_CUDA;
+  const int per_sm = std::max(1, std::min(occupancy(tc_output<D>, kOutThreadsTC, Cfg::SMEM), 512 / Cfg::TMEM_COLS));
+  const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
+  KernelTimer timer("tc_output", stream);
+  tc_output<D><<<grid, kOutThreadsTC, Cfg::SMEM, stream>>>(tq, to, tst, make_geom(p, c128), n_items, p.phi_kind, p.eps,
+                                                            zt);
+  return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
 }
 
 template <int D>
@@ -1201,114 +1167,10 @@ int launch_tc_d(const Problem& p, const float* W, void* workspace, cudaStream_t 
   __nv_bfloat16* Sbuf = reinterpret_cast<__nv_bfloat16*>(ws + L.sbuf_off);
   __nv_bfloat16* St = reinterpret_cast<__nv_bfloat16*>(ws + L.st_off);
   float* zt = reinterpret_cast<float*>(ws + L.zt_off);
-  const int sms = device_sms();
-  if (sms <= 0) return MHLA_ERR_CUDA;
-
-  ChunkPlan c64, c128;
-  if (!chunk_plan(p, 64, &c64) || !chunk_plan(p, 128, &c128)) return MHLA_ERR_UNSUPPORTED;
-
-  // ---- step 1: summaries
-  {
-    using Cfg = SumCfg<D>;
-    CUtensorMap tk, tv;
-    if (!operand_map(p, p.k, c64.box_y, c64.box_t, &tk) || !operand_map(p, p.v, c64.box_y, c64.box_t, &tv))
-      return MHLA_ERR_CUDA;
-    const int32_t G = static_cast<int32_t>((p.H + Cfg::HP - 1) / Cfg::HP);
-    const int64_t n_items = p.B * G * p.M;
-    if (cudaFuncSetAttribute(tc_summary<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Cfg::SMEM)) != cudaSuccess)
-      return MHLA_ERR_CUDA;
-    const int per_sm = std::max(1, occupancy(tc_summary<D>, kTcThreads, Cfg::SMEM));
-    const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
-    KernelTimer timer("tc_summary", stream);
-    tc_summary<D><<<grid, kTcThreads, Cfg::SMEM, stream>>>(tk, tv, make_geom(p, c64), G, n_items,
-                                                           p.phi_kind, p.eps, Sbuf, W, Wb, L.Mp);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
-
-  // ---- step 2: mixing GEMM (all of W in shared memory when M <= 256)
-  if (p.M <= 256) {
-    CUtensorMap tw, ts;
-    {
-      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.M)};
-      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.Mp * 2)};
-      const cuuint32_t box[2] = {static_cast<cuuint32_t>(MixResCfg::KC), static_cast<cuuint32_t>(MixResCfg::ROWS)};
-      if (!encode(&tw, 2, Wb, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
-    }
-    {
-      // Sbuf as (128 columns, M source blocks, G groups)
-      const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(L.ngroups)};
-      const cuuint64_t strides[2] = {256u, static_cast<cuuint64_t>(p.M * 256)};
-      const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(MixResCfg::KC), 1u};
-      if (!encode(&ts, 3, Sbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
-    }
-    const int32_t n_tiles = static_cast<int32_t>((L.ncols + MixResCfg::COLS - 1) / MixResCfg::COLS);
-    if (cudaFuncSetAttribute(tc_mix_resident<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(MixResCfg::SMEM)) != cudaSuccess)
-      return MHLA_ERR_CUDA;
-    const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
-    KernelTimer timer("tc_mix", stream);
-    tc_mix_resident<D><<<grid, kMixThreadsTC, MixResCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), L.ncols,
-                                                                          n_tiles, St, zt);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  } else {
-    CUtensorMap tw, ts;
-    {
-      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.M)};
-      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.Mp * 2)};
-      const cuuint32_t box[2] = {static_cast<cuuint32_t>(MixCfg::KC), static_cast<cuuint32_t>(MixCfg::ROWS)};
-      if (!encode(&tw, 2, Wb, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
-    }
-    {
-      // Sbuf as (128 columns, M source blocks, G groups)
-      const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(L.ngroups)};
-      const cuuint64_t strides[2] = {256u, static_cast<cuuint64_t>(p.M * 256)};
-      const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(MixCfg::KC), 1u};
-      if (!encode(&ts, 3, Sbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MHLA_ERR_CUDA;
-    }
-    const int32_t n_col_tiles = static_cast<int32_t>((L.ncols + MixCfg::COLS - 1) / MixCfg::COLS);
-    const int32_t n_i_tiles = static_cast<int32_t>((p.M + MixCfg::ROWS - 1) / MixCfg::ROWS);
-    if (cudaFuncSetAttribute(tc_mix<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(MixCfg::SMEM)) != cudaSuccess)
-      return MHLA_ERR_CUDA;
-    const int64_t n_tiles = static_cast<int64_t>(n_col_tiles) * n_i_tiles;
-    const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
-    KernelTimer timer("tc_mix", stream);
-    tc_mix<D><<<grid, kMixThreadsTC, MixCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), L.ncols,
-                                                              n_col_tiles, n_i_tiles, St, zt);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
-
-  // ---- step 3: outputs
-  {
-    using Cfg = OutCfg<D>;
-    CUtensorMap tq, to;
-    if (!operand_map(p, p.q, c128.box_y, c128.box_t, &tq) || !operand_map(p, p.o, c128.box_y, c128.box_t, &to))
-      return MHLA_ERR_CUDA;
-    // S~ tiles (row-major [BH*M][d][d]) seen as (c % 8, r, c / 8, tile): a
-    // (8, d, d/8, 1) box lands as 16-byte rows of 8 columns, d rows per column
-    // group: the unswizzled MN-major operand layout.
-    CUtensorMap tst;
-    {
-      const cuuint64_t dims[4] = {8u, static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(p.d / 8),
-                                  static_cast<cuuint64_t>(p.BH() * p.M)};
-      const cuuint64_t strides[3] = {static_cast<cuuint64_t>(p.d * 2), 16u, static_cast<cuuint64_t>(p.d * p.d * 2)};
-      const cuuint32_t box[4] = {8u, static_cast<cuuint32_t>(p.d), static_cast<cuuint32_t>(p.d / 8), 1u};
-      if (!encode(&tst, 4, St, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return MHLA_ERR_CUDA;
-    }
-    const int64_t n_items = p.BH() * p.M;
-    if (cudaFuncSetAttribute(tc_output<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Cfg::SMEM)) != cudaSuccess)
-      return MHLA_ERR_CUDA;
-    const int per_sm =
-        std::max(1, std::min(occupancy(tc_output<D>, kOutThreadsTC, Cfg::SMEM), 512 / Cfg::TMEM_COLS));
-    const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
-    KernelTimer timer("tc_output", stream);
-    tc_output<D><<<grid, kOutThreadsTC, Cfg::SMEM, stream>>>(tq, to, tst, make_geom(p, c128), n_items, p.phi_kind,
-                                                              p.eps, zt);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
-  return MHLA_OK;
+  int rc = run_summary<D>(p, W, Wb, nullptr, L.Mp, Sbuf, stream);
+  if (rc == MHLA_OK) rc = run_mix<D>(p, Wb, L.Mp, Sbuf, St, zt, stream);
+  if (rc == MHLA_OK) rc = run_output<D>(p, St, zt, stream);
+  return rc;
 }
 
 }  // namespace
@@ -1319,6 +1181,22 @@ bool encode_tensor_map(CUtensorMap* m, int rank, void* base, const cuuint64_t* d
 }
 
 int device_sm_count() { return device_sms(); }
+
+int tc_run_summary(const Problem& p, const float* W, void* Wb, void* WbT, int64_t Mp, void* Sbuf, void* stream) {
+  auto* wb = static_cast<__nv_bfloat16*>(Wb);
+  auto* wbt = static_cast<__nv_bfloat16*>(WbT);
+  auto* sb = static_cast<__nv_bfloat16*>(Sbuf);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return p.d == 64 ? run_summary<64>(p, W, wb, wbt, Mp, sb, s) : run_summary<32>(p, W, wb, wbt, Mp, sb, s);
+}
+
+int tc_run_mix(const Problem& p, const void* Wm, int64_t Mp, const void* Sbuf, void* St, float* zt, void* stream) {
+  auto* wm = static_cast<const __nv_bfloat16*>(Wm);
+  auto* sb = static_cast<const __nv_bfloat16*>(Sbuf);
+  auto* st = static_cast<__nv_bfloat16*>(St);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return p.d == 64 ? run_mix<64>(p, wm, Mp, sb, st, zt, s) : run_mix<32>(p, wm, Mp, sb, st, zt, s);
+}
 
 bool tc_eligible(const Problem& p) {
   if (p.dtype != MHLA_BF16) return false;
