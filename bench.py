@@ -2,9 +2,12 @@
 """Throughput of the MHLA forward pass on GB300 (tokens/s and HBM roofline).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                  [--pass forward|backward]
 
 One step = one MHLA forward (summaries, mixing GEMM, outputs) over
-one synthetic batch of the workload, inputs resident in HBM.  Rank 0 prints one
+one synthetic batch of the workload, inputs resident in HBM; with
+``--pass backward`` one step is one backward pass (dq, dk, dv, dW for a seeded
+dout).  Rank 0 prints one
 JSON line.  With N > 1 (torchrun) every rank runs an independent batch on its own
 GPU (replicas, weak scaling); ranks meet only for the timing barrier and the
 max-over-ranks reduction.  ``--impl reference`` times the float64 CPU oracle on
@@ -31,6 +34,7 @@ if ROOT not in sys.path:
 from token_level_head_block_gb300.workloads import HEADLINE, WORKLOADS  # noqa: E402
 
 METRIC = "MHLA forward tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
+METRIC_BWD = "MHLA backward (dq, dk, dv, dW) tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
 UNIT = "tokens/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -150,7 +154,10 @@ def load_peaks():
 # Source files a kernel's code lives in (with the shared inline-PTX header).
 KERNEL_SOURCES = {"tc_summary": "tc_kernels.cu", "tc_mix": "tc_kernels.cu", "tc_output": "tc_kernels.cu",
                   "tc_small": "small_kernels.cu", "simt_summary": "simt_kernels.cu",
-                  "simt_mix": "simt_kernels.cu", "simt_output": "simt_kernels.cu"}
+                  "simt_mix": "simt_kernels.cu", "simt_output": "simt_kernels.cu",
+                  "tc_bwd_query": "bwd_tc_kernels.cu", "tc_bwd_key": "bwd_tc_kernels.cu",
+                  "tc_dw": "bwd_tc_kernels.cu", "simt_bwd_query": "simt_kernels.cu",
+                  "simt_bwd_key": "simt_kernels.cu", "simt_dw": "simt_kernels.cu"}
 
 
 def kernel_source_digest(kernel):
@@ -189,6 +196,10 @@ def kernel_work(wl, name):
         "tc_output": ("hbm", 2 * io), "simt_output": ("hbm", 2 * io),
         "tc_mix": ("tensor", 2 * M * M * BH * d * (d + 1)), "simt_mix": ("alu", 2 * M * M * BH * d * (d + 1)),
         "tc_small": ("hbm", 4 * io),
+        # backward: read q, dout, write dq; read k, v, write dk, dv; dW = dS~ . S^T
+        "tc_bwd_query": ("hbm", 3 * io), "simt_bwd_query": ("hbm", 3 * io),
+        "tc_bwd_key": ("hbm", 4 * io), "simt_bwd_key": ("hbm", 4 * io),
+        "tc_dw": ("tensor", 2 * M * M * BH * d * (d + 1)), "simt_dw": ("alu", 2 * M * M * BH * d * (d + 1)),
     }
     return table.get(name, ("hbm", 0))
 
@@ -216,9 +227,10 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def oracle_sample_rate(wl, q, k, v, W, budget_s, max_slices=None):
-    """Times the oracle on (b, h) slices until budget_s elapses (at least one slice).
-    Returns (tokens/s, slices, seconds); a slice of one head counts N / H tokens."""
+def oracle_sample_rate(wl, q, k, v, W, budget_s, max_slices=None, g=None):
+    """Times the oracle (the backward oracle when dout g is given) on (b, h)
+    slices until budget_s elapses (at least one slice).  Returns (tokens/s,
+    slices, seconds); a slice of one head counts N / H tokens."""
     import oracle
     from token_level_head_block_gb300.synth import as_f64
     phi = oracle.PHI_RELU if wl.phi == "relu" else oracle.PHI_RELU_EPS
@@ -227,12 +239,22 @@ def oracle_sample_rate(wl, q, k, v, W, budget_s, max_slices=None):
     while True:
         b, h = pairs[done % len(pairs)]
         sl = (slice(b, b + 1), slice(None), slice(h, h + 1), slice(None))
-        oracle.forward(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, wl.grid, wl.block, phi, wl.eps)
+        if g is None:
+            oracle.forward(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, wl.grid, wl.block, phi, wl.eps)
+        else:
+            oracle.backward(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, as_f64(g[sl]), wl.grid, wl.block, phi,
+                            wl.eps)
         done += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (max_slices and done >= max_slices):
             break
     return done * wl.N / wl.H / el, done, el
+
+
+def draw_dout(wl, seed=None):
+    """Seeded dL/d(out) for the backward pass, N(0, 1) in the workload's dtype."""
+    from token_level_head_block_gb300.synth import draw_qkv
+    return draw_qkv(wl.B, wl.N, wl.H, wl.d, wl.seed + 100 if seed is None else seed, wl.dtype)[0]
 
 
 # ----------------------------------------------------------------- arms
@@ -245,21 +267,23 @@ def run_reference(args, wl):
     import oracle
     from token_level_head_block_gb300.synth import draw_workload
     q, k, v = draw_workload(wl)
+    g = draw_dout(wl) if args.pass_ == "backward" else None
     W = oracle.mixing_matrix(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
     per_step = max(1, args.ref_slices)
     for _ in range(args.warmup):
-        oracle_sample_rate(wl, q, k, v, W, 0.0, max_slices=1)
+        oracle_sample_rate(wl, q, k, v, W, 0.0, max_slices=1, g=g)
     times = []
     for _ in range(args.steps):
-        _, n, el = oracle_sample_rate(wl, q, k, v, W, 1e9, max_slices=per_step)
+        _, n, el = oracle_sample_rate(wl, q, k, v, W, 1e9, max_slices=per_step, g=g)
         times.append(el)
     total = sum(times)
     value = args.steps * per_step * wl.N / wl.H / total
     cores = blas_threads()
+    what = "backward oracle" if g is not None else "oracle (blocked form)"
     sample = (f"each step: {per_step} of the {wl.B * wl.H} (batch, head) slices of {wl.name}, "
-              f"float64 numpy oracle (blocked form); a slice counts N/H tokens")
+              f"float64 numpy {what}; a slice counts N/H tokens")
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": METRIC_BWD if g is not None else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {**wl.describe(), "parallelism": "host cores (BLAS threads)"},
@@ -281,17 +305,29 @@ def run_ours(args, wl):
     dist_init("nccl")
     mhla.lib()
 
+    bwd = args.pass_ == "backward"
     q_h, k_h, v_h = draw_workload(wl, seed=wl.seed + rank)      # each replica its own batch
+    g_h = draw_dout(wl, seed=wl.seed + 100 + rank) if bwd else None
     W_h = mhla.init_mixing(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
     W = torch.from_numpy(W_h).to(dev)
     out = torch.empty_like(q)
-    ws = torch.empty(mhla.workspace_size(q, wl.grid, wl.block), dtype=torch.uint8, device=dev)
-    path = mhla.select_path(q, k, v, out, wl.grid, wl.block)
     stream = torch.cuda.current_stream(dev)
+    if bwd:
+        g = g_h.to(dev)
+        dq, dk, dv, dW = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(W)
+        ws = torch.empty(mhla.backward_workspace_size(q, wl.grid, wl.block), dtype=torch.uint8, device=dev)
 
-    def step():
-        mhla.forward(q, k, v, W, wl.grid, wl.block, phi=wl.phi, eps=wl.eps, out=out, workspace=ws, stream=stream)
+        def step():
+            mhla.backward(q, k, v, W, g, wl.grid, wl.block, phi=wl.phi, eps=wl.eps, dq=dq, dk=dk, dv=dv, dW=dW,
+                          workspace=ws, stream=stream)
+    else:
+        ws = torch.empty(mhla.workspace_size(q, wl.grid, wl.block), dtype=torch.uint8, device=dev)
+
+        def step():
+            mhla.forward(q, k, v, W, wl.grid, wl.block, phi=wl.phi, eps=wl.eps, out=out, workspace=ws,
+                         stream=stream)
+    path = mhla.select_path(q, k, v, out, wl.grid, wl.block)
 
     def timed(n, body):
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -335,14 +371,26 @@ def run_ours(args, wl):
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (t.pin_memory() for t in (q_h, k_h, v_h))
-        ho = torch.empty_like(q_h).pin_memory()
+        if bwd:
+            hg = g_h.pin_memory()
+            hdq, hdk, hdv = (torch.empty_like(q_h).pin_memory() for _ in range(3))
+            hdW = torch.empty(dW.shape, dtype=dW.dtype).pin_memory()
 
-        def e2e_step():
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            step()
-            ho.copy_(out, non_blocking=True)
+            def e2e_step():
+                for dst, src in ((q, hq), (k, hk), (v, hv), (g, hg)):
+                    dst.copy_(src, non_blocking=True)
+                step()
+                for dst, src in ((hdq, dq), (hdk, dk), (hdv, dv), (hdW, dW)):
+                    dst.copy_(src, non_blocking=True)
+        else:
+            ho = torch.empty_like(q_h).pin_memory()
+
+            def e2e_step():
+                q.copy_(hq, non_blocking=True)
+                k.copy_(hk, non_blocking=True)
+                v.copy_(hv, non_blocking=True)
+                step()
+                ho.copy_(out, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -350,7 +398,8 @@ def run_ours(args, wl):
         el_e2e = max_over_ranks(timed(n_e2e, e2e_step), dev)
         io = wl.B * wl.N * wl.H * wl.d * wl.elem_bytes
         e2e = {"value": whole_job_throughput(wl.tokens, world, n_e2e, el_e2e), "unit": UNIT,
-               "h2d_bytes_per_step": 3 * io, "d2h_bytes_per_step": io, "steps": n_e2e,
+               "h2d_bytes_per_step": (4 if bwd else 3) * io,
+               "d2h_bytes_per_step": 3 * io + wl.M * wl.M * 4 if bwd else io, "steps": n_e2e,
                "ms_per_step": 1e3 * el_e2e / n_e2e}
 
     # roofline of the dominant kernel, from the per-kernel events of pass B
@@ -371,32 +420,37 @@ def run_ours(args, wl):
     roofline = {"kernel": dominant, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "traffic": traffic, "algorithmic_per_launch": work,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"}
-    fwd_gbs = wl.algorithmic_bytes / (max_el / args.steps) / 1e9
+    # read q, k, v (+ dout) and write o (dq, dk, dv)
+    pass_bytes = wl.algorithmic_bytes * 7 // 4 if bwd else wl.algorithmic_bytes
+    fwd_gbs = pass_bytes / (max_el / args.steps) / 1e9
     forward_roofline = {"bound": "hbm", "achieved": fwd_gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
-                        "frac": fwd_gbs / float(peaks["hbm_gbs"]), "bytes_per_step": wl.algorithmic_bytes}
+                        "frac": fwd_gbs / float(peaks["hbm_gbs"]), "bytes_per_step": pass_bytes}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, n, el = oracle_sample_rate(wl, q_h, k_h, v_h, W_h, args.cpu_seconds)
+        rate, n, el = oracle_sample_rate(wl, q_h, k_h, v_h, W_h, args.cpu_seconds, g=g_h)
+        what = "backward oracle" if bwd else "oracle (blocked form)"
         cpu = {"value": rate, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                "sample": f"{n} of the {wl.B * wl.H} (batch, head) slices of {wl.name} in {el:.1f} s, "
-                         "float64 numpy oracle (blocked form); a slice counts N/H tokens"}
+                         f"float64 numpy {what}; a slice counts N/H tokens"}
 
     launches = sum(n for n, _ in prof.values())
     l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", L2_BYTES)
     if rank == 0:
         line = {
-            "impl": "ours", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "impl": "ours", "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic",
-            "config": {**wl.describe(), "path": path, "global_batch": wl.B * world, "seq_len": wl.N,
+            "config": {**wl.describe(), "pass": args.pass_,
+                       "path": ("tc" if "tc_bwd_query" in prof else "simt") if bwd else path,
+                       "global_batch": wl.B * world, "seq_len": wl.N,
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
                        "l2": f"inputs {3 * wl.algorithmic_bytes // 4 / 1e6:.0f} MB > L2 {l2_bytes / 2**20:.0f} MiB "
                              "each step (no flush)",
                        "clock_window": f"{args.sustain:.1f} s sustained run of the same step, then both timed passes"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
-            "roofline": roofline, "forward_roofline": forward_roofline,
+            "roofline": roofline, ("backward_roofline" if bwd else "forward_roofline"): forward_roofline,
             "kernels": kern, "profiled_pass_ms_per_step": 1e3 * el_prof / args.steps,
             "cpu_baseline": cpu,
         }
@@ -413,6 +467,7 @@ def main():
     ap.add_argument("--sustain", type=float, default=2.0, help="seconds of load before timing (clock samples)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU oracle baseline")
     ap.add_argument("--ref-slices", type=int, default=1, help="(batch, head) slices per reference step")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

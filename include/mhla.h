@@ -196,8 +196,13 @@ mhla_status_t mhla_backward_workspace_size(const mhla_tensor_t* q, const mhla_sh
  *   workspace      at least mhla_backward_workspace_size() bytes, 256-byte
  *                  aligned, or NULL with workspace_bytes == 0 (stream-ordered
  *                  cudaMallocAsync / cudaFreeAsync).
- *   path           AUTO or SIMT (CUDA cores, float32 arithmetic, any d <= 128
- *                  and block shape); TC and FUSED return MHLA_ERR_UNSUPPORTED.
+ *   path           AUTO takes TC whenever every operand qualifies, else SIMT.
+ *                  TC: tensor cores, bf16 with float32 accumulation, d in
+ *                  {32, 64}, the forward TC path's token geometry and TMA
+ *                  friendly strides on q, k, v, dout, dq, dk, dv; SIMT: CUDA
+ *                  cores, float32 arithmetic, any d <= 128 and block shape.
+ *                  FUSED returns MHLA_ERR_UNSUPPORTED.
+ * With AUTO, mhla_backward_workspace_size returns enough for either path.
  * Asynchronous on stream; statuses as for mhla_forward.  B == 0 or H == 0
  * writes dW = 0 and nothing else. */
 mhla_status_t mhla_backward(const mhla_tensor_t* q, const mhla_tensor_t* k,

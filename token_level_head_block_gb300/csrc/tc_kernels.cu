@@ -483,20 +483,24 @@ tc_mix(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtenso
 
 // ============================================================================
 // tc_mix_resident: the same GEMM for M <= 256 with all of W (bf16, <= 128 KB)
-// resident in shared memory.  One tile = 128 Sbuf columns x all query blocks:
-// every Sbuf panel is read exactly once, and per 16 source blocks one MMA per
-// 128-row query tile writes its own TMEM accumulator.  Epilogue warpgroup w
-// drains query tile w; accumulator sets alternate between tiles.
+// resident in shared memory, computed transposed: D[col][i] = sum_j
+// Sbuf[j][col] W[i][j].  One tile = 128 Sbuf columns (MMA M, the TMEM lanes) x
+// all query blocks (MMA N <= 256): per 16 source blocks a single 128 x N x 16
+// MMA, A = the Sbuf chunk as it landed (MN-major), B = W (K-major).  With the
+// columns on TMEM lanes, the 32 lanes of an epilogue warp hold 32 consecutive
+// columns of one query block, so each store writes 64 contiguous bytes of S~
+// (or 128 of z~).  Two accumulator sets alternate between tiles; both
+// epilogue warpgroups drain every tile, each half of the query blocks.
 // ============================================================================
 struct MixResCfg {
-  static constexpr int ROWS = 128;                // query blocks per MMA (M)
-  static constexpr int COLS = 128;                // Sbuf columns per tile (N)
+  static constexpr int COLS = 128;                // Sbuf columns per tile (MMA M)
+  static constexpr int NMAX = 256;                // query blocks (MMA N, at most)
   static constexpr int KC = 64;                   // source blocks per stage
-  static constexpr int W_CHUNK = ROWS * KC * 2;   // one (query tile, 64 source blocks) W chunk
-  static constexpr int W_BYTES = 2 * 4 * W_CHUNK; // up to 256 x 256
-  static constexpr int STAGE = KC * COLS * 2;     // Sbuf chunk: two 64-column MN-major chunks
+  static constexpr int W_CHUNK = NMAX * KC * 2;   // W rows i for 64 source blocks, K-major
+  static constexpr int W_BYTES = 4 * W_CHUNK;     // up to 256 x 256
+  static constexpr int STAGE = KC * COLS * 2;     // Sbuf chunk: two 64-column MN-major halves
   static constexpr int NS = 6;
-  static constexpr int SET = 2 * COLS;            // TMEM columns of one accumulator set (2 query tiles)
+  static constexpr int SET = NMAX;                // TMEM columns of one accumulator set
   static constexpr int TMEM_COLS = 512;
   static constexpr int CTRL = 1024;
   static constexpr size_t SMEM = static_cast<size_t>(W_BYTES) + static_cast<size_t>(NS) * STAGE + CTRL + 1024;
@@ -505,11 +509,11 @@ struct MixResCfg {
 template <int D>
 __global__ void __launch_bounds__(kMixThreadsTC, 1)
 tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s, int32_t M,
-                int64_t ncols, int32_t n_tiles, __nv_bfloat16* __restrict__ St, float* __restrict__ zt) {
+                int32_t NP, int64_t ncols, int32_t n_tiles, __nv_bfloat16* __restrict__ St, float* __restrict__ zt) {
   using Cfg = MixResCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
-  uint8_t* wres = smem;                                  // [query tile][k chunk] W, K-major
+  uint8_t* wres = smem;                                  // [k chunk] W rows i, K-major
   uint8_t* stages = smem + Cfg::W_BYTES;
   uint8_t* ctrl = stages + Cfg::NS * Cfg::STAGE;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
@@ -522,8 +526,8 @@ tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
   volatile uint32_t* abortf = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_it = (M + Cfg::ROWS - 1) / Cfg::ROWS;     // 1 or 2 query tiles
   const int nk = (M + Cfg::KC - 1) / Cfg::KC;           // 1..4 source chunks
+  const uint32_t wchunk = static_cast<uint32_t>(NP) * Cfg::KC * 2;
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::NS; ++s) {
       mbar_init(full + s, 1);
@@ -555,11 +559,9 @@ tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_last();
       const uint64_t pol_s = policy_evict_first();
-      // all of W once
-      mbar_arrive_expect_tx(wfull, static_cast<uint32_t>(n_it * nk * Cfg::W_CHUNK));
-      for (int it = 0; it < n_it; ++it)
-        for (int kc = 0; kc < nk; ++kc)
-          tma_load_2d(wres + (it * 4 + kc) * Cfg::W_CHUNK, &tm_w, wfull, kc * Cfg::KC, it * Cfg::ROWS, pol_w);
+      // all of W once: chunk kc holds rows i < NP (rows >= M read as zeros) of source blocks kc*64 ..
+      mbar_arrive_expect_tx(wfull, static_cast<uint32_t>(nk) * wchunk);
+      for (int kc = 0; kc < nk; ++kc) tma_load_2d(wres + kc * wchunk, &tm_w, wfull, kc * Cfg::KC, 0, pol_w);
       int s = 0;
       uint32_t ph = 0;
       uint64_t fills = 0;
@@ -584,7 +586,7 @@ tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(Cfg::ROWS, Cfg::COLS, /*a K-major*/ false, /*b MN-major*/ true);
+      const uint32_t idesc = idesc_bf16_f32(Cfg::COLS, NP, /*a MN-major*/ true, /*b K-major*/ false);
       int s = 0;
       uint32_t ph = 0, local = 0;
       bool ok = wait_bounded(wfull, 0, abortf);
@@ -600,11 +602,9 @@ tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
           const uint32_t base = smem_u32(stages + s * Cfg::STAGE);
 #pragma unroll
           for (int ks = 0; ks < Cfg::KC / 16; ++ks) {
-            const uint64_t b = smem_desc(base + ks * 2048, Cfg::STAGE / 2, 1024, 2);
-            for (int it = 0; it < n_it; ++it) {
-              const uint64_t a = smem_desc(wbase + (it * 4 + kc) * Cfg::W_CHUNK + ks * 32, 16, 1024, 2);
-              mma_bf16(tmem + set * Cfg::SET + it * Cfg::COLS, a, b, idesc, (kc | ks) != 0 ? 1u : 0u);
-            }
+            const uint64_t a = smem_desc(base + ks * 2048, Cfg::STAGE / 2, 1024, 2);
+            const uint64_t b = smem_desc(wbase + kc * wchunk + ks * 32, 16, 1024, 2);
+            mma_bf16(tmem + set * Cfg::SET, a, b, idesc, (kc | ks) != 0 ? 1u : 0u);
           }
           mma_commit(empty + s);
           if (++s == Cfg::NS) { s = 0; ph ^= 1u; }
@@ -616,45 +616,40 @@ tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
       drain_wait(fin, 0);
     }
   } else {
-    // warpgroup wg (warps 2-5 or 6-9) drains query tile wg of every accumulator set
+    // warpgroup wg (warps 2-5 or 6-9) drains query blocks [128 wg, 128 wg + 128) of every tile
     constexpr int32_t PER_BH = (D + 1) * D;            // Sbuf columns of one (b, h): d rows of S, then z
     const int wg = (warp - 2) >> 2;
     const int q4 = warp & 3;
-    const int32_t i = wg * Cfg::ROWS + 32 * q4 + lane;  // this thread's query block
+    const int i_lo = wg * 128, i_hi = min(M, i_lo + 128);
     uint32_t local = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
       const uint32_t set = local & 1u, sph = (local >> 1) & 1u;
       if (!warp_wait(tfull + set, sph, abortf)) break;
       tc_fence_after();
-      if (wg < n_it) {
-        const int32_t col0 = static_cast<int32_t>(t) * Cfg::COLS;
-        int32_t bh = col0 / PER_BH, rem = col0 - bh * PER_BH;
-        const uint32_t tb = tmem + set * Cfg::SET + wg * Cfg::COLS + (static_cast<uint32_t>(32 * q4) << 16);
+      // this lane's column; 32-column runs never cross a row of S (d is a multiple of 32)
+      const int64_t col = t * Cfg::COLS + 32 * q4 + lane;
+      const bool live = col < ncols;
+      const int64_t bh = col / PER_BH;
+      const int32_t rem = static_cast<int32_t>(col - bh * PER_BH);
+      const int32_t rr = rem / D, c = rem % D;
+      const uint32_t tb = tmem + set * Cfg::SET + (static_cast<uint32_t>(32 * q4) << 16);
 #pragma unroll 1
-        for (int cc = 0; cc < Cfg::COLS; cc += 32) {
-          uint32_t v[32];
-          tmem_ld_x32(tb + cc, v);
-          tmem_ld_wait();
-          if (i < M && col0 + cc < ncols) {
-            const int32_t rr = rem / D, c0 = rem % D;
-            const int64_t tile_id = static_cast<int64_t>(bh) * M + i;
-            if (rr < D) {
-              __nv_bfloat16* tile = St + tile_id * D * D + rr * D + c0;   // S~_i row-major
+      for (int i0 = i_lo; i0 < i_hi; i0 += 32) {
+        uint32_t v[32];
+        tmem_ld_x32(tb + i0, v);
+        tmem_ld_wait();
+        if (live) {
+          if (rr < D) {
+            __nv_bfloat16* dst = St + (bh * M + i0) * (D * D) + rr * D + c;   // S~_i row-major
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(tile + q * 8) =
-                    make_uint4(pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                               pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                               pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                               pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
-            } else {
-              uint4* dst = reinterpret_cast<uint4*>(zt + tile_id * D + c0);
+            for (int e = 0; e < 32; ++e)
+              if (i0 + e < i_hi) dst[static_cast<int64_t>(e) * D * D] = __float2bfloat16_rn(__uint_as_float(v[e]));
+          } else {
+            float* dst = zt + (bh * M + i0) * D + c;
 #pragma unroll
-              for (int q = 0; q < 8; ++q) dst[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
+            for (int e = 0; e < 32; ++e)
+              if (i0 + e < i_hi) dst[static_cast<int64_t>(e) * D] = __uint_as_float(v[e]);
           }
-          rem += 32;
-          if (rem >= PER_BH) { rem -= PER_BH; ++bh; }
         }
       }
       tc_fence_before();
@@ -1091,7 +1086,8 @@ int run_mix(const Problem& p, const __nv_bfloat16* Wm, int64_t Mp, const __nv_bf
   void* sptr = const_cast<__nv_bfloat16*>(Sbuf);
   if (p.M <= 256) {   // all of W in shared memory
     CUtensorMap tw, ts;
-    const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(MixResCfg::KC), static_cast<cuuint32_t>(MixResCfg::ROWS)};
+    const int32_t NP = static_cast<int32_t>((p.M + 15) / 16 * 16);   // MMA N: query blocks rounded up to 16
+    const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(MixResCfg::KC), static_cast<cuuint32_t>(NP)};
     const cuuint32_t sbox[3] = {64u, static_cast<cuuint32_t>(MixResCfg::KC), 1u};
     if (!encode(&tw, 2, wptr, wdims, wstrides, wbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode(&ts, 3, sptr, sdims, sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -1102,8 +1098,8 @@ int run_mix(const Problem& p, const __nv_bfloat16* Wm, int64_t Mp, const __nv_bf
       return MHLA_ERR_CUDA;
     const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
     KernelTimer timer("tc_mix", stream);
-    tc_mix_resident<D><<<grid, kMixThreadsTC, MixResCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), ncols,
-                                                                          n_tiles, St, zt);
+    tc_mix_resident<D><<<grid, kMixThreadsTC, MixResCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), NP,
+                                                                          ncols, n_tiles, St, zt);
     return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
   }
   CUtensorMap tw, ts;
