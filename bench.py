@@ -2,12 +2,12 @@
 """Throughput of the MHLA forward pass on GB300 (tokens/s and HBM roofline).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-                  [--pass forward|backward]
+                  [--pass forward|backward|causal]
 
 One step = one MHLA forward (summaries, mixing GEMM, outputs) over
 one synthetic batch of the workload, inputs resident in HBM; with
 ``--pass backward`` one step is one backward pass (dq, dk, dv, dW for a seeded
-dout).  Rank 0 prints one
+dout); with ``--pass causal`` one causal (chunkwise) MHLA forward.  Rank 0 prints one
 JSON line.  With N > 1 (torchrun) every rank runs an independent batch on its own
 GPU (replicas, weak scaling); ranks meet only for the timing barrier and the
 max-over-ranks reduction.  ``--impl reference`` times the float64 CPU oracle on
@@ -35,6 +35,8 @@ from token_level_head_block_gb300.workloads import HEADLINE, WORKLOADS  # noqa: 
 
 METRIC = "MHLA forward tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
 METRIC_BWD = "MHLA backward (dq, dk, dv, dW) tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
+METRIC_CAUSAL = "causal MHLA forward tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
+METRICS = {"forward": METRIC, "backward": METRIC_BWD, "causal": METRIC_CAUSAL}
 UNIT = "tokens/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -152,12 +154,13 @@ def load_peaks():
 
 
 # Source files a kernel's code lives in (with the shared inline-PTX header).
-KERNEL_SOURCES = {"tc_summary": "tc_kernels.cu", "tc_mix": "tc_kernels.cu", "tc_output": "tc_kernels.cu",
+KERNEL_SOURCES = {"tc_summary": "tc_summary.cu", "tc_mix": "tc_mix.cu", "tc_output": "tc_output.cu",
                   "tc_small": "small_kernels.cu", "simt_summary": "simt_kernels.cu",
                   "simt_mix": "simt_kernels.cu", "simt_output": "simt_kernels.cu",
                   "tc_bwd_query": "bwd_tc_kernels.cu", "tc_bwd_key": "bwd_tc_kernels.cu",
                   "tc_dw": "bwd_tc_kernels.cu", "simt_bwd_query": "simt_kernels.cu",
-                  "simt_bwd_key": "simt_kernels.cu", "simt_dw": "simt_kernels.cu"}
+                  "simt_bwd_key": "simt_kernels.cu", "simt_dw": "simt_kernels.cu",
+                  "simt_causal_output": "simt_kernels.cu"}
 
 
 def kernel_source_digest(kernel):
@@ -165,7 +168,7 @@ def kernel_source_digest(kernel):
     code than the current one does not count."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "token_level_head_block_gb300", "csrc")
-    for name in (KERNEL_SOURCES.get(kernel, ""), "ptx.cuh"):
+    for name in (KERNEL_SOURCES.get(kernel, ""), "ptx.cuh", "tc_common.cuh"):
         p = os.path.join(csrc, name)
         if name and os.path.exists(p):
             with open(p, "rb") as f:
@@ -200,6 +203,8 @@ def kernel_work(wl, name):
         "tc_bwd_query": ("hbm", 3 * io), "simt_bwd_query": ("hbm", 3 * io),
         "tc_bwd_key": ("hbm", 4 * io), "simt_bwd_key": ("hbm", 4 * io),
         "tc_dw": ("tensor", 2 * M * M * BH * d * (d + 1)), "simt_dw": ("alu", 2 * M * M * BH * d * (d + 1)),
+        # causal: read q, k, v (k, v again for the blocks' prefixes), write o
+        "simt_causal_output": ("hbm", 4 * io),
     }
     return table.get(name, ("hbm", 0))
 
@@ -227,7 +232,7 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def oracle_sample_rate(wl, q, k, v, W, budget_s, max_slices=None, g=None):
+def oracle_sample_rate(wl, q, k, v, W, budget_s, max_slices=None, g=None, causal=False):
     """Times the oracle (the backward oracle when dout g is given) on (b, h)
     slices until budget_s elapses (at least one slice).  Returns (tokens/s,
     slices, seconds); a slice of one head counts N / H tokens."""
@@ -239,7 +244,9 @@ def oracle_sample_rate(wl, q, k, v, W, budget_s, max_slices=None, g=None):
     while True:
         b, h = pairs[done % len(pairs)]
         sl = (slice(b, b + 1), slice(None), slice(h, h + 1), slice(None))
-        if g is None:
+        if causal:
+            oracle.forward_causal(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, wl.grid, wl.block, phi, wl.eps)
+        elif g is None:
             oracle.forward(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, wl.grid, wl.block, phi, wl.eps)
         else:
             oracle.backward(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, as_f64(g[sl]), wl.grid, wl.block, phi,
@@ -268,22 +275,23 @@ def run_reference(args, wl):
     from token_level_head_block_gb300.synth import draw_workload
     q, k, v = draw_workload(wl)
     g = draw_dout(wl) if args.pass_ == "backward" else None
+    causal = args.pass_ == "causal"
     W = oracle.mixing_matrix(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
     per_step = max(1, args.ref_slices)
     for _ in range(args.warmup):
-        oracle_sample_rate(wl, q, k, v, W, 0.0, max_slices=1, g=g)
+        oracle_sample_rate(wl, q, k, v, W, 0.0, max_slices=1, g=g, causal=causal)
     times = []
     for _ in range(args.steps):
-        _, n, el = oracle_sample_rate(wl, q, k, v, W, 1e9, max_slices=per_step, g=g)
+        _, n, el = oracle_sample_rate(wl, q, k, v, W, 1e9, max_slices=per_step, g=g, causal=causal)
         times.append(el)
     total = sum(times)
     value = args.steps * per_step * wl.N / wl.H / total
     cores = blas_threads()
-    what = "backward oracle" if g is not None else "oracle (blocked form)"
+    what = {"forward": "oracle (blocked form)", "backward": "backward oracle", "causal": "causal oracle"}[args.pass_]
     sample = (f"each step: {per_step} of the {wl.B * wl.H} (batch, head) slices of {wl.name}, "
               f"float64 numpy {what}; a slice counts N/H tokens")
     print(json.dumps({
-        "impl": "reference", "metric": METRIC_BWD if g is not None else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": METRICS[args.pass_], "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {**wl.describe(), "parallelism": "host cores (BLAS threads)"},
@@ -313,7 +321,13 @@ def run_ours(args, wl):
     W = torch.from_numpy(W_h).to(dev)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
-    if bwd:
+    if args.pass_ == "causal":
+        ws = torch.empty(mhla.causal_workspace_size(q, wl.grid, wl.block), dtype=torch.uint8, device=dev)
+
+        def step():
+            mhla.forward_causal(q, k, v, W, wl.grid, wl.block, phi=wl.phi, eps=wl.eps, out=out, workspace=ws,
+                                stream=stream)
+    elif bwd:
         g = g_h.to(dev)
         dq, dk, dv, dW = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(W)
         ws = torch.empty(mhla.backward_workspace_size(q, wl.grid, wl.block), dtype=torch.uint8, device=dev)
@@ -428,8 +442,10 @@ def run_ours(args, wl):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, n, el = oracle_sample_rate(wl, q_h, k_h, v_h, W_h, args.cpu_seconds, g=g_h)
-        what = "backward oracle" if bwd else "oracle (blocked form)"
+        rate, n, el = oracle_sample_rate(wl, q_h, k_h, v_h, W_h, args.cpu_seconds, g=g_h,
+                                         causal=args.pass_ == "causal")
+        what = {"forward": "oracle (blocked form)", "backward": "backward oracle",
+                "causal": "causal oracle"}[args.pass_]
         cpu = {"value": rate, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                "sample": f"{n} of the {wl.B * wl.H} (batch, head) slices of {wl.name} in {el:.1f} s, "
                          f"float64 numpy {what}; a slice counts N/H tokens"}
@@ -438,7 +454,7 @@ def run_ours(args, wl):
     l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", L2_BYTES)
     if rank == 0:
         line = {
-            "impl": "ours", "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "impl": "ours", "metric": METRICS[args.pass_], "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic",
@@ -450,7 +466,7 @@ def run_ours(args, wl):
                              "each step (no flush)",
                        "clock_window": f"{args.sustain:.1f} s sustained run of the same step, then both timed passes"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
-            "roofline": roofline, ("backward_roofline" if bwd else "forward_roofline"): forward_roofline,
+            "roofline": roofline, f"{args.pass_}_roofline": forward_roofline,
             "kernels": kern, "profiled_pass_ms_per_step": 1e3 * el_prof / args.steps,
             "cpu_baseline": cpu,
         }
@@ -467,7 +483,7 @@ def main():
     ap.add_argument("--sustain", type=float, default=2.0, help="seconds of load before timing (clock samples)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU oracle baseline")
     ap.add_argument("--ref-slices", type=int, default=1, help="(batch, head) slices per reference step")
-    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "causal"], default="forward")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

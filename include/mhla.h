@@ -214,6 +214,32 @@ mhla_status_t mhla_backward(const mhla_tensor_t* q, const mhla_tensor_t* k,
                             void* workspace, size_t workspace_bytes, void* stream,
                             int32_t path);
 
+/* Device workspace mhla_forward_causal needs (bytes, a multiple of 256).  Host
+ * only; MHLA_ERR_SHAPE when the blocks are not contiguous token ranges. */
+mhla_status_t mhla_causal_workspace_size(const mhla_tensor_t* q, const mhla_shape3_t* grid,
+                                         const mhla_shape3_t* block, int32_t path, size_t* bytes);
+
+/* Causal (chunkwise) MHLA for autoregressive models ([P2] App. B "Causal MHLA":
+ * block-specific mixed summaries, reusing each block's mixture, causal at the
+ * cost of chunkwise linear attention).  The page gives no formula; this is the
+ * causal restriction of the two-stage form: token t of query block i sees
+ * every past block j < i through W[i][j] and the tokens s <= t of its own
+ * block through W[i][i]:
+ *   o_t = phi(q_t)^T (S<_i + W[i][i] P_t) / (phi(q_t) . (z<_i + W[i][i] y_t) + eps)
+ *   S<_i = sum_{j<i} W[i][j] S_j,  P_t = sum_{s in i, s <= t} phi(k_s) v_s^T,
+ * z<_i and y_t likewise.  Entries W[i][j] with j > i are never read.
+ *   Arguments as for mhla_forward.  The blocks must be contiguous ranges of
+ *   raster-order tokens (a 1-D sequence grid (1, N) in blocks (1, w), or whole
+ *   rows or frames), else MHLA_ERR_SHAPE.
+ *   path: AUTO or SIMT (CUDA cores, float32 arithmetic, any d <= 128, bf16 or
+ *   float32); TC and FUSED return MHLA_ERR_UNSUPPORTED. */
+mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_tensor_t* k,
+                                  const mhla_tensor_t* v, const float* W,
+                                  const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                                  const mhla_phi_t* phi, const mhla_tensor_t* out,
+                                  void* workspace, size_t workspace_bytes, void* stream,
+                                  int32_t path);
+
 /* mhla_forward for callers that must not allocate device memory -- the paper
  * has no counterpart to this; it is a property of the library, not the method.
  * Who needs it: code that runs the forward where device allocation is not

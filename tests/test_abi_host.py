@@ -294,3 +294,34 @@ def test_backward_workspace_size(L):
     assert sizes[0] == max(sizes[1], sizes[2])                         # AUTO: enough for either path
     assert L.mhla_backward_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
                                           ctypes.byref(mhla.shape3(wl.block)), 3, ctypes.byref(n)) == UNSUPPORTED
+
+
+# ------------------------------------------------------------ causal validation
+
+def call_causal(L, q, k, v, o, grid, block, W=FAKE + (1 << 36), phi=(0, 1e-6), ws=None, ws_bytes=0, path=0):
+    return L.mhla_forward_causal(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.c_void_p(W),
+                                 ctypes.byref(mhla.shape3(grid)), ctypes.byref(mhla.shape3(block)),
+                                 ctypes.byref(mhla.Phi(*phi)), ctypes.byref(o),
+                                 ctypes.c_void_p(ws) if ws else None, ws_bytes, None, path)
+
+
+def test_causal_rejects_malformed_requests_before_any_launch(L):
+    q, k, v, o = four(2, 1024, 3, 64)
+    assert call_causal(L, q, k, v, o, (32, 32), (4, 4)) == SHAPE               # blocks not contiguous
+    assert call_causal(L, q, k, v, o, (32, 32), (2, 2)) == SHAPE
+    assert call_causal(L, q, k, v, o, (1, 1000), (1, 8)) == SHAPE              # grid product != N
+    assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), W=0) == INVALID
+    assert call_causal(L, q, k, v, q, (1, 1024), (1, 64)) == INVALID           # out aliases q
+    assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), path=2) == UNSUPPORTED
+    assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), path=3) == UNSUPPORTED
+    assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), ws=FAKE + 8, ws_bytes=1 << 30) == WORKSPACE
+    assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), ws=FAKE, ws_bytes=16) == WORKSPACE
+    assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), ws=None, ws_bytes=16) == WORKSPACE
+    n = ctypes.c_size_t()
+    assert L.mhla_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3((32, 32))),
+                                        ctypes.byref(mhla.shape3((8, 32))), 0, ctypes.byref(n)) == OK
+    assert n.value == 2 * ((2 * 3 * 4 * 64 * 65 * 4 + 255) // 256 * 256)     # two float32 summary buffers
+    assert L.mhla_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3((32, 32))),
+                                        ctypes.byref(mhla.shape3((8, 8))), 0, ctypes.byref(n)) == SHAPE
+    e = four(0, 1024, 3, 64)
+    assert call_causal(L, *e, (32, 32), (8, 32)) == OK                         # empty batch: nothing queued

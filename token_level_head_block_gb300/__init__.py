@@ -15,7 +15,8 @@ import numpy as np
 
 __all__ = [
     "MhlaError", "lib", "library_path", "num_blocks", "init_mixing", "workspace_size",
-    "select_path", "forward", "backward", "backward_workspace_size", "device_status", "profile_begin",
+    "select_path", "forward", "forward_causal", "causal_workspace_size", "backward", "backward_workspace_size",
+    "device_status", "profile_begin",
     "profile_end", "tensor_desc", "shape3",
     "PATHS", "TRANSFORMS",
 ]
@@ -89,6 +90,12 @@ def lib():
     L.mhla_forward.argtypes = [P(Tensor), P(Tensor), P(Tensor), ctypes.c_void_p, P(Shape3), P(Shape3), P(Phi),
                                P(Tensor), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int32]
     L.mhla_forward.restype = ctypes.c_int
+    L.mhla_causal_workspace_size.argtypes = [P(Tensor), P(Shape3), P(Shape3), ctypes.c_int32, P(ctypes.c_size_t)]
+    L.mhla_causal_workspace_size.restype = ctypes.c_int
+    L.mhla_forward_causal.argtypes = [P(Tensor), P(Tensor), P(Tensor), ctypes.c_void_p, P(Shape3), P(Shape3),
+                                      P(Phi), P(Tensor), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                      ctypes.c_int32]
+    L.mhla_forward_causal.restype = ctypes.c_int
     L.mhla_backward_workspace_size.argtypes = [P(Tensor), P(Shape3), P(Shape3), ctypes.c_int32,
                                                P(ctypes.c_size_t)]
     L.mhla_backward_workspace_size.restype = ctypes.c_int
@@ -208,6 +215,37 @@ def forward(q, k, v, W, grid, block, phi="relu", eps=1e-6, out=None, workspace=N
                             ctypes.byref(_desc(out)), ctypes.c_void_p(ws_ptr) if ws_ptr else None,
                             ws_bytes, ctypes.c_void_p(sptr) if sptr else None, PATHS[path])
     _check(st, "mhla_forward")
+    return out
+
+
+def causal_workspace_size(q, grid, block, path="auto"):
+    n = ctypes.c_size_t(0)
+    _check(lib().mhla_causal_workspace_size(ctypes.byref(_desc(q) if not isinstance(q, Tensor) else q),
+                                            ctypes.byref(shape3(grid)), ctypes.byref(shape3(block)), PATHS[path],
+                                            ctypes.byref(n)), "mhla_causal_workspace_size")
+    return int(n.value)
+
+
+def forward_causal(q, k, v, W, grid, block, phi="relu", eps=1e-6, out=None, workspace=None, stream=None,
+                   path="auto"):
+    """Causal (chunkwise) MHLA of device tensors [B, N, H, d]; blocks must be
+    contiguous token ranges (e.g. grid (1, N), block (1, w)).  Returns ``out``."""
+    import torch
+    if out is None:
+        out = torch.empty_like(q)
+    if not W.is_contiguous() or W.dtype != torch.float32:
+        raise ValueError("W must be a contiguous float32 tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() *
+                                                            workspace.element_size())
+    st = lib().mhla_forward_causal(ctypes.byref(_desc(q)), ctypes.byref(_desc(k)), ctypes.byref(_desc(v)),
+                                   ctypes.c_void_p(W.data_ptr()), ctypes.byref(shape3(grid)),
+                                   ctypes.byref(shape3(block)), ctypes.byref(Phi(PHIS[phi], float(eps))),
+                                   ctypes.byref(_desc(out)), ctypes.c_void_p(ws_ptr) if ws_ptr else None,
+                                   ws_bytes, ctypes.c_void_p(sptr) if sptr else None, PATHS[path])
+    _check(st, "mhla_forward_causal")
     return out
 
 

@@ -308,6 +308,80 @@ extern "C" mhla_status_t mhla_backward(const mhla_tensor_t* q, const mhla_tensor
   return static_cast<mhla_status_t>(lr);
 }
 
+namespace mhla {
+namespace {
+
+// Every block a contiguous range of raster-order tokens: for some axis a, the
+// block is one unit on every slower axis and the whole grid on every faster one.
+bool blocks_contiguous(const Problem& p) {
+  const int64_t g[3] = {p.T, p.Y, p.X}, b[3] = {p.bt, p.by, p.bx};
+  for (int a = 0; a < 3; ++a) {
+    bool ok = true;
+    for (int s = 0; s < a; ++s) ok = ok && b[s] == 1;
+    for (int f = a + 1; f < 3; ++f) ok = ok && b[f] == g[f];
+    if (ok) return true;
+  }
+  return false;
+}
+
+int resolve_causal_path(int32_t path, int* sel) {
+  if (path == MHLA_PATH_AUTO || path == MHLA_PATH_SIMT) { *sel = MHLA_PATH_SIMT; return MHLA_OK; }
+  if (path == MHLA_PATH_TC || path == MHLA_PATH_FUSED) return MHLA_ERR_UNSUPPORTED;
+  return MHLA_ERR_INVALID_ARG;
+}
+
+}  // namespace
+}  // namespace mhla
+
+extern "C" mhla_status_t mhla_causal_workspace_size(const mhla_tensor_t* q, const mhla_shape3_t* grid,
+                                                    const mhla_shape3_t* block, int32_t path, size_t* bytes) {
+  if (!bytes) return MHLA_ERR_INVALID_ARG;
+  Problem p;
+  const int rc = build_problem(q, q, q, q, grid, block, nullptr, /*check_alias=*/false, &p);
+  if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+  if (!blocks_contiguous(p)) return MHLA_ERR_SHAPE;
+  int sel = 0;
+  const int rp = resolve_causal_path(path, &sel);
+  if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
+  *bytes = (p.B == 0 || p.H == 0) ? 0 : simt_workspace_bytes(p);
+  return MHLA_OK;
+}
+
+extern "C" mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_tensor_t* k, const mhla_tensor_t* v,
+                                             const float* W, const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                                             const mhla_phi_t* phi, const mhla_tensor_t* out, void* workspace,
+                                             size_t workspace_bytes, void* stream, int32_t path) {
+  if (!phi) return MHLA_ERR_INVALID_ARG;
+  Problem p;
+  const int rc = build_problem(q, k, v, out, grid, block, phi, true, &p);
+  if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+  if (!blocks_contiguous(p)) return MHLA_ERR_SHAPE;
+  int sel = 0;
+  const int rp = resolve_causal_path(path, &sel);
+  if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
+  if (p.B == 0 || p.H == 0) return MHLA_OK;
+  if (!W) return MHLA_ERR_INVALID_ARG;
+  {
+    uintptr_t o0, o1;
+    span(out, &o0, &o1);
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(W);
+    if (overlaps(o0, o1, w0, w0 + static_cast<uintptr_t>(p.M * p.M) * sizeof(float))) return MHLA_ERR_INVALID_ARG;
+  }
+  const size_t need = simt_workspace_bytes(p);
+  void* ws = workspace;
+  if (!ws && workspace_bytes != 0) return MHLA_ERR_WORKSPACE;
+  if (ws && (workspace_bytes < need || reinterpret_cast<uintptr_t>(ws) % kAlign != 0)) return MHLA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool owned = false;
+  if (!ws) {
+    if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return MHLA_ERR_CUDA;
+    owned = true;
+  }
+  const int lr = launch_simt_causal(p, W, ws, stream);
+  if (owned && cudaFreeAsync(ws, s) != cudaSuccess && lr == MHLA_OK) return MHLA_ERR_CUDA;
+  return static_cast<mhla_status_t>(lr);
+}
+
 extern "C" mhla_status_t mhla_device_status(void* stream, uint32_t* flags) {
   if (!flags) return MHLA_ERR_INVALID_ARG;
   uint32_t tc = 0, small = 0, bwd = 0;

@@ -49,6 +49,9 @@ struct SimtWorkspace {
 size_t simt_workspace_bytes(const Problem& p);
 SimtWorkspace simt_carve(const Problem& p, void* base);
 int launch_simt(const Problem& p, const float* W, void* workspace, void* stream);
+// Causal MHLA on CUDA cores (contiguous blocks); same workspace as the forward,
+// Szt holding the mixed past summaries.
+int launch_simt_causal(const Problem& p, const float* W, void* workspace, void* stream);
 
 // Backward pass operands (dout read; dq, dk, dv, dW written) and the CUDA-core
 // backward's workspace (float32):
@@ -96,6 +99,10 @@ int launch_small(const Problem& p, const float* W, void* stream);
 // tc_run_mix computes St, zt = Wm . Sbuf for the bf16 [M][Mp] matrix Wm.
 int tc_run_summary(const Problem& p, const float* W, void* Wb, void* WbT, int64_t Mp, void* Sbuf, void* stream);
 int tc_run_mix(const Problem& p, const void* Wm, int64_t Mp, const void* Sbuf, void* St, float* zt, void* stream);
+int tc_run_output(const Problem& p, const void* St, const float* zt, void* stream);
+int read_and_clear_summary_error(void* stream, uint32_t* flags);
+int read_and_clear_mix_error(void* stream, uint32_t* flags);
+int read_and_clear_output_error(void* stream, uint32_t* flags);
 
 // Device error words of the tensor-core and fused kernels (bounded waits).
 int read_and_clear_device_error(void* stream, uint32_t* flags);

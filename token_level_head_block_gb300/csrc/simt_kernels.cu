@@ -100,7 +100,8 @@ constexpr int kMixRows = 8;     // query blocks i per thread
 
 // S~ = W . S per (b, h), treating the d*(d+1) entries of every block as columns
 // (TRANS: W^T . S, the mixing step of the backward pass).
-template <bool TRANS>
+// (PAST: only source blocks j < i, the mixed past summaries of causal MHLA.)
+template <bool TRANS, bool PAST = false>
 __global__ void __launch_bounds__(kMixThreads)
 simt_mix(const float* __restrict__ W, const float* __restrict__ Sz, float* __restrict__ Szt,
          int64_t M, int64_t E, int64_t BH) {
@@ -116,7 +117,8 @@ simt_mix(const float* __restrict__ W, const float* __restrict__ Sz, float* __res
       const float s = src[j * E];
 #pragma unroll
       for (int u = 0; u < kMixRows; ++u)
-        if (i0 + u < M) acc[u] = fmaf(__ldg(TRANS ? W + j * M + i0 + u : W + (i0 + u) * M + j), s, acc[u]);
+        if (i0 + u < M && (!PAST || j < i0 + u))
+          acc[u] = fmaf(__ldg(TRANS ? W + j * M + i0 + u : W + (i0 + u) * M + j), s, acc[u]);
     }
 #pragma unroll
     for (int u = 0; u < kMixRows; ++u)
@@ -169,6 +171,107 @@ simt_output(const T* __restrict__ q, Operand qo, T* __restrict__ o, Operand oo, 
 }
 
 // ============================================================================
+// Causal MHLA ([P2] "MHLA: Restoring Expressivity of Linear Attention via
+// Token-Level Multi-Head", App. B "Causal MHLA": block-specific mixed summaries,
+// causal, at the cost of chunkwise linear attention).  Blocks are contiguous
+// token ranges; for token t of query block i
+//   o_t = phi(q_t) (S<_i + W[i][i] P_t) / (phi(q_t) . (z<_i + W[i][i] y_t) + eps)
+// with S<_i = sum_{j < i} W[i][j] S_j (simt_mix<false, true>) and P_t, y_t the
+// running sums of phi(k_s) v_s^T, phi(k_s) over the block's tokens s <= t.
+// simt_causal_output walks the block in chunks of kCausalChunk tokens: the
+// running state starts at S<_i, z<_i; inside a chunk each token adds the
+// W[i][i]-weighted causal scores against the chunk's earlier tokens, then the
+// state absorbs W[i][i] times the chunk's summary.
+// ============================================================================
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+constexpr int kCausalThreads = 256;
+constexpr int kCausalWarps = kCausalThreads / 32;
+constexpr int kCausalChunk = 32;   // one key per lane in the score step
+
+template <typename T, int ENT>
+__global__ void __launch_bounds__(kCausalThreads)
+simt_causal_output(const T* __restrict__ q, Operand qo, const T* __restrict__ k, Operand ko,
+                   const T* __restrict__ v, Operand vo, T* __restrict__ o, Operand oo, TokenGeom g, int64_t H, int d,
+                   int phi_kind, float eps, const float* __restrict__ W, const float* __restrict__ Szt) {
+  extern __shared__ float sm[];
+  const int E = d * d, P = d + 1;
+  float* st = sm;                          // [d][d] running state S<_i + W_ii P
+  float* zs = st + E;                      // [d]    running z<_i + W_ii y
+  float* sq = zs + d;                      // [chunk][d]     phi(q)
+  float* sk = sq + kCausalChunk * d;       // [chunk][d + 1] phi(k), rows padded (lanes walk keys)
+  float* sv = sk + kCausalChunk * P;       // [chunk][d]     v
+  float* sa = sv + kCausalChunk * d;       // [warps][chunk] causal scores of the warp's token
+  const int64_t item = blockIdx.x;
+  const int64_t i = item % g.M, bh = item / g.M;
+  const int64_t b = bh / H, h = bh % H;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const float wii = __ldg(W + i * g.M + i);
+  const float* src = Szt + (bh * g.M + i) * static_cast<int64_t>(E + d);
+  for (int e = tid; e < E + d; e += kCausalThreads) sm[e] = src[e];
+  const T* qb = q + b * qo.sb + h * qo.sh;
+  const T* kb = k + b * ko.sb + h * ko.sh;
+  const T* vb = v + b * vo.sb + h * vo.sh;
+  T* ob = o + b * oo.sb + h * oo.sh;
+  for (int64_t s0 = 0; s0 < g.w; s0 += kCausalChunk) {
+    const int cnt = static_cast<int>(g.w - s0 < kCausalChunk ? g.w - s0 : kCausalChunk);
+    __syncthreads();   // the state is complete (and the previous chunk's rows are free)
+    for (int e = tid; e < cnt * d; e += kCausalThreads) {
+      const int sl = e / d, c = e % d;
+      const int64_t n = token_of(g, i, s0 + sl);   // contiguous blocks: n increases with s
+      sq[sl * d + c] = phi_f(load_f(qb + n * qo.sn + c), phi_kind, eps);
+      sk[sl * P + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
+      sv[sl * d + c] = load_f(vb + n * vo.sn + c);
+    }
+    __syncthreads();
+    for (int sl = warp; sl < cnt; sl += kCausalWarps) {
+      const float* myq = sq + sl * d;
+      // lane = key s of the chunk: a_s = W_ii phi(q_t) . phi(k_s) for s <= t
+      float a = 0.0f;
+      if (lane <= sl) {
+        for (int r = 0; r < d; ++r) a = fmaf(myq[r], sk[lane * P + r], a);
+        a *= wii;
+      }
+      float* mya = sa + warp * kCausalChunk;
+      mya[lane] = a;
+      float den = 0.0f;
+      for (int r = lane; r < d; r += 32) den = fmaf(myq[r], zs[r], den);
+      den = warp_sum(den + a) + eps;
+      __syncwarp();
+      const int64_t n = token_of(g, i, s0 + sl);
+      for (int c = lane; c < d; c += 32) {
+        float num = 0.0f;
+        for (int r = 0; r < d; ++r) num = fmaf(myq[r], st[r * d + c], num);
+        for (int s2 = 0; s2 <= sl; ++s2) num = fmaf(mya[s2], sv[s2 * d + c], num);
+        store_f(ob + n * oo.sn + c, num / den);
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+    // state += W_ii * (the chunk's summary)
+#pragma unroll
+    for (int m = 0; m < ENT; ++m) {
+      const int e = tid + m * kCausalThreads;
+      if (e < E) {
+        const int r = e / d, c = e % d;
+        float acc = 0.0f;
+        for (int sl = 0; sl < cnt; ++sl) acc = fmaf(sk[sl * P + r], sv[sl * d + c], acc);
+        st[e] = fmaf(wii, acc, st[e]);
+      }
+    }
+    if (tid < d) {
+      float acc = 0.0f;
+      for (int sl = 0; sl < cnt; ++sl) acc += sk[sl * P + tid];
+      zs[tid] = fmaf(wii, acc, zs[tid]);
+    }
+  }
+}
+
+// ============================================================================
 // Backward pass.  The pages print none; these kernels follow the chain rule
 // through the three forward steps in reverse (the derivation is in the
 // header, next to mhla_backward):
@@ -183,12 +286,6 @@ simt_output(const T* __restrict__ q, Operand qo, T* __restrict__ o, Operand oo, 
 constexpr int kBwdThreads = 256;
 constexpr int kBwdWarps = kBwdThreads / 32;
 constexpr int kBwdChunk = 32;   // tokens staged per accumulation step
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-  return x;
-}
 
 // One CTA per (b, h, i).  S~_i in shared memory with rows padded to d + 1 so
 // that lanes walking a column and lanes walking a row both avoid bank conflicts.
@@ -533,7 +630,70 @@ int launch_simt_bwd_typed(const Problem& p, const float* W, const BwdOperands& b
   return MHLA_OK;
 }
 
+template <typename T>
+int launch_simt_causal_typed(const Problem& p, const float* W, const SimtWorkspace& ws, cudaStream_t stream) {
+  const TokenGeom g = token_geom(p);
+  const int d = static_cast<int>(p.d);
+  const int64_t BH = p.BH();
+  const int64_t items = BH * p.M;
+  if (items > 0x7fffffffLL) return MHLA_ERR_UNSUPPORTED;
+  const T* qp = static_cast<const T*>(p.q.data);
+  const T* kp = static_cast<const T*>(p.k.data);
+  const T* vp = static_cast<const T*>(p.v.data);
+  T* op = static_cast<T*>(p.o.data);
+  {
+    const size_t sum_smem = 2 * kSumChunk * d * sizeof(float);
+    KernelTimer timer("simt_summary", stream);
+    if (d <= 16)
+      simt_summary<T, 1><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    else if (d <= 32)
+      simt_summary<T, 4><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    else if (d <= 64)
+      simt_summary<T, 16><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    else
+      simt_summary<T, 64><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  const int64_t E = p.d * (p.d + 1);
+  const dim3 mix_grid(static_cast<unsigned>((E + kMixThreads - 1) / kMixThreads),
+                      static_cast<unsigned>((p.M + kMixRows - 1) / kMixRows),
+                      static_cast<unsigned>(std::min<int64_t>(BH, 65535)));
+  if (mix_grid.y > 65535) return MHLA_ERR_UNSUPPORTED;
+  {
+    KernelTimer timer("simt_mix", stream);
+    simt_mix<false, true><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.Sz, ws.Szt, p.M, E, BH);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  {
+    const size_t smem = (d * d + d + kCausalChunk * (3 * d + 1) + kCausalWarps * kCausalChunk) * sizeof(float);
+    auto launch = [&](auto kern) -> int {
+      if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem)) != cudaSuccess)
+        return MHLA_ERR_CUDA;
+      KernelTimer timer("simt_causal_output", stream);
+      kern<<<static_cast<unsigned>(items), kCausalThreads, smem, stream>>>(qp, p.q, kp, p.k, vp, p.v, op, p.o, g, p.H,
+                                                                             d, p.phi_kind, p.eps, W, ws.Szt);
+      return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+    };
+    return d <= 16   ? launch(simt_causal_output<T, 1>)
+           : d <= 32 ? launch(simt_causal_output<T, 4>)
+           : d <= 64 ? launch(simt_causal_output<T, 16>)
+                     : launch(simt_causal_output<T, 64>);
+  }
+}
+
 }  // namespace
+
+int launch_simt_causal(const Problem& p, const float* W, void* workspace, void* stream) {
+  const SimtWorkspace ws = simt_carve(p, workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.dtype == MHLA_BF16) return launch_simt_causal_typed<__nv_bfloat16>(p, W, ws, s);
+  return launch_simt_causal_typed<float>(p, W, ws, s);
+}
 
 size_t simt_workspace_bytes(const Problem& p) {
   const size_t per = static_cast<size_t>(p.BH()) * p.M * p.d * (p.d + 1) * sizeof(float);

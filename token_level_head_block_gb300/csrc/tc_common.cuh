@@ -108,6 +108,29 @@ static __device__ __forceinline__ int swz(int row) {
 
 // ----------------------------------------------------------------- host side
 
+template <typename K>
+int occupancy(K kernel, int threads, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) return 0;
+  return n;
+}
+
+// Copies a translation unit's device error word to *flags and clears it
+// (synchronises stream); MHLA_ERR_TIMEOUT when it was set.
+template <typename Word>
+int read_and_clear_word(Word& word, void* stream, uint32_t* flags) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int host = 0;
+  if (cudaMemcpyFromSymbolAsync(&host, word, sizeof(host), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MHLA_ERR_CUDA;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbolAsync(word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MHLA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MHLA_ERR_CUDA;
+  *flags = host;
+  return host ? MHLA_ERR_TIMEOUT : MHLA_OK;
+}
+
 struct ChunkPlan {
   int64_t box_y, box_t, nyc, chunks;
 };

@@ -79,6 +79,11 @@ WORKLOADS = {
                  note="video latent 20x32x32 (N=20480), 4x8x8 blocks (M=80)"),
     ]
     + [
+        # causal language-model shape: a 1-D sequence of 4096 tokens in chunks of 64
+        Workload("lm_causal_4096", 4, 12, 64, (1, 4096), (1, 64), "bf16", "linear", 1009,
+                 note="causal sequence of 4096 tokens, 64-token blocks (M=64), 12 heads"),
+    ]
+    + [
         Workload(f"sweep_{s}x{s}", 4, 6, 64, (s, s), (16, 16), "bf16", "exp", 1005,
                  note=f"N sweep point {s}x{s} at 16x16 blocks")
         for s in (64, 128, 256, 512)
