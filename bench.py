@@ -160,7 +160,7 @@ KERNEL_SOURCES = {"tc_summary": "tc_summary.cu", "tc_mix": "tc_mix.cu", "tc_outp
                   "tc_bwd_query": "bwd_tc_kernels.cu", "tc_bwd_key": "bwd_tc_kernels.cu",
                   "tc_dw": "bwd_tc_kernels.cu", "simt_bwd_query": "simt_kernels.cu",
                   "simt_bwd_key": "simt_kernels.cu", "simt_dw": "simt_kernels.cu",
-                  "simt_causal_output": "simt_kernels.cu"}
+                  "simt_causal_output": "simt_kernels.cu", "tc_causal_tile": "causal_tc_kernels.cu"}
 
 
 def kernel_source_digest(kernel):
@@ -203,8 +203,8 @@ def kernel_work(wl, name):
         "tc_bwd_query": ("hbm", 3 * io), "simt_bwd_query": ("hbm", 3 * io),
         "tc_bwd_key": ("hbm", 4 * io), "simt_bwd_key": ("hbm", 4 * io),
         "tc_dw": ("tensor", 2 * M * M * BH * d * (d + 1)), "simt_dw": ("alu", 2 * M * M * BH * d * (d + 1)),
-        # causal: read q, k, v (k, v again for the blocks' prefixes), write o
-        "simt_causal_output": ("hbm", 4 * io),
+        # causal: read q, k, v, write o
+        "simt_causal_output": ("hbm", 4 * io), "tc_causal_tile": ("hbm", 4 * io),
     }
     return table.get(name, ("hbm", 0))
 
@@ -459,7 +459,8 @@ def run_ours(args, wl):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic",
             "config": {**wl.describe(), "pass": args.pass_,
-                       "path": ("tc" if "tc_bwd_query" in prof else "simt") if bwd else path,
+                       "path": ("tc" if "tc_bwd_query" in prof else "simt") if bwd else
+                               (("tc" if "tc_causal_tile" in prof else "simt") if args.pass_ == "causal" else path),
                        "global_batch": wl.B * world, "seq_len": wl.N,
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
                        "l2": f"inputs {3 * wl.algorithmic_bytes // 4 / 1e6:.0f} MB > L2 {l2_bytes / 2**20:.0f} MiB "

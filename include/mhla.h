@@ -231,8 +231,17 @@ mhla_status_t mhla_causal_workspace_size(const mhla_tensor_t* q, const mhla_shap
  *   Arguments as for mhla_forward.  The blocks must be contiguous ranges of
  *   raster-order tokens (a 1-D sequence grid (1, N) in blocks (1, w), or whole
  *   rows or frames), else MHLA_ERR_SHAPE.
- *   path: AUTO or SIMT (CUDA cores, float32 arithmetic, any d <= 128, bf16 or
- *   float32); TC and FUSED return MHLA_ERR_UNSUPPORTED. */
+ *   path: AUTO takes TC whenever the request qualifies, else SIMT.
+ *     TC: tensor cores, bf16 with float32 accumulation, d in {32, 64},
+ *     N a multiple of 128, blocks of 64 tokens or a multiple of 128, strides
+ *     multiples of 8 elements; the sequence is cut into units of min(w, 128)
+ *     tokens whose causal states come from one mixing GEMM with the unit-level
+ *     matrix W'[u][u'] (W[b(u)][b(u')] for a past block, W[b(u)][b(u)] for an
+ *     earlier unit of the same block, 0 otherwise), then every 128-token tile
+ *     forms its causal scores and its state term in one accumulator.
+ *     SIMT: CUDA cores, float32 arithmetic, any d <= 128, bf16 or float32.
+ *     FUSED returns MHLA_ERR_UNSUPPORTED.
+ *   With AUTO, mhla_causal_workspace_size returns enough for either path. */
 mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_tensor_t* k,
                                   const mhla_tensor_t* v, const float* W,
                                   const mhla_shape3_t* grid, const mhla_shape3_t* block,

@@ -312,15 +312,26 @@ def test_causal_rejects_malformed_requests_before_any_launch(L):
     assert call_causal(L, q, k, v, o, (1, 1000), (1, 8)) == SHAPE              # grid product != N
     assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), W=0) == INVALID
     assert call_causal(L, q, k, v, q, (1, 1024), (1, 64)) == INVALID           # out aliases q
-    assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), path=2) == UNSUPPORTED
+    assert call_causal(L, q, k, v, o, (1, 1024), (1, 32), path=2) == UNSUPPORTED   # 32-token blocks
+    q2, k2, v2, o2 = four(2, 1000, 3, 64)
+    assert call_causal(L, q2, k2, v2, o2, (1, 1000), (1, 125), path=2) == UNSUPPORTED   # N not a multiple of 128
     assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), path=3) == UNSUPPORTED
     assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), ws=FAKE + 8, ws_bytes=1 << 30) == WORKSPACE
     assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), ws=FAKE, ws_bytes=16) == WORKSPACE
     assert call_causal(L, q, k, v, o, (1, 1024), (1, 64), ws=None, ws_bytes=16) == WORKSPACE
     n = ctypes.c_size_t()
     assert L.mhla_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3((32, 32))),
+                                        ctypes.byref(mhla.shape3((8, 32))), 1, ctypes.byref(n)) == OK
+    simt = n.value
+    assert simt == 2 * ((2 * 3 * 4 * 64 * 65 * 4 + 255) // 256 * 256)       # two float32 summary buffers
+    assert L.mhla_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3((32, 32))),
+                                        ctypes.byref(mhla.shape3((8, 32))), 2, ctypes.byref(n)) == OK
+    tc = n.value                                                             # 8 units of 128 tokens
+    units, groups = 8, (2 * 3 * 65 * 64 + 127) // 128
+    assert tc >= units * 8 * 2 + units * groups * 128 * 2 + 2 * 3 * units * 64 * 64 * 2 + 2 * 3 * units * 64 * 4
+    assert L.mhla_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3((32, 32))),
                                         ctypes.byref(mhla.shape3((8, 32))), 0, ctypes.byref(n)) == OK
-    assert n.value == 2 * ((2 * 3 * 4 * 64 * 65 * 4 + 255) // 256 * 256)     # two float32 summary buffers
+    assert n.value == max(tc, simt)
     assert L.mhla_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3((32, 32))),
                                         ctypes.byref(mhla.shape3((8, 8))), 0, ctypes.byref(n)) == SHAPE
     e = four(0, 1024, 3, 64)

@@ -59,6 +59,52 @@ def test_causal_matches_oracle(name, phi):
     assert err <= TOL[dtype], f"{name}/{phi}: normwise error {err:.3e}"
 
 
+# Tensor-core causal path: bf16, d in {32, 64}, N a multiple of 128, blocks of
+# 64 tokens (two units per tile) or a multiple of 128 (one unit per tile, one
+# or more units per block); M_u = 512 takes the streaming mixing GEMM.
+TC_CASES = {
+    "w64_d64": (2, 3, 64, (1, 512), (1, 64)),
+    "w64_d32": (1, 2, 32, (1, 1024), (1, 64)),
+    "w128_d64": (2, 2, 64, (1, 768), (1, 128)),
+    "w256_d64": (1, 3, 64, (1, 1024), (1, 256)),
+    "w384_d32": (1, 2, 32, (1, 768), (1, 384)),
+    "rows_w128_d64": (1, 2, 64, (8, 128), (1, 128)),
+    "frames_w256_d32": (1, 2, 32, (4, 8, 16), (2, 8, 16)),
+    "mu512_d64": (1, 1, 64, (1, 32768), (1, 64)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TC_CASES))
+@pytest.mark.parametrize("phi", ["relu", "relu_eps"])
+def test_causal_tensor_core_path(name, phi):
+    B, H, d, grid, block = TC_CASES[name]
+    N = int(np.prod(grid))
+    q, k, v = draw_qkv(B, N, H, d, seed=76, dtype="bf16")
+    W = draw_matrix(oracle.num_blocks(grid, block), seed=77)
+    got = run(q, k, v, W, grid, block, phi, path="tc")
+    if N <= 4096:
+        ref = oracle.forward_causal(as_f64(q), as_f64(k), as_f64(v), W, grid, block, PHI[phi], 1e-6)
+        err = normwise(got, ref)
+    else:   # the python-loop oracle on a sample of tokens: the first, a middle and the last block
+        M = oracle.num_blocks(grid, block)
+        w = N // M
+        cut = [slice(0, 2 * w), slice(N // 2 - w, N // 2 + w), slice(N - 2 * w, N)]
+        ref_all = oracle.forward_causal(as_f64(q), as_f64(k), as_f64(v), W, grid, block, PHI[phi], 1e-6)
+        err = max(normwise(got[:, c], ref_all[:, c]) for c in cut)
+    assert err <= TOL["bf16"], f"tc/{name}/{phi}: normwise error {err:.3e}"
+
+
+def test_causal_paths_agree():
+    B, H, d, grid, block = 2, 3, 64, (1, 1024), (1, 64)
+    q, k, v = draw_qkv(B, 1024, H, d, seed=78)
+    W = mhla.init_mixing(grid, block, "linear")
+    a = run(q, k, v, W, grid, block, path="tc")
+    b = run(q, k, v, W, grid, block, path="simt")
+    c = run(q, k, v, W, grid, block, path="tc")
+    assert np.array_equal(a, c)
+    assert normwise(a, b) <= TOL["bf16"]
+
+
 def test_causal_ignores_w_above_the_diagonal_and_is_deterministic():
     B, H, d, grid, block = 2, 2, 64, (1, 256), (1, 32)
     q, k, v = draw_qkv(B, 256, H, d, seed=73)
@@ -71,8 +117,10 @@ def test_causal_ignores_w_above_the_diagonal_and_is_deterministic():
     assert np.array_equal(a, b) and np.array_equal(a, c)
 
 
-def test_causal_strided_slices_of_one_projection():
-    B, N, H, d, grid, block = 2, 384, 3, 64, (1, 384), (1, 48)
+@pytest.mark.parametrize("grid,block", [((1, 384), (1, 48)), ((1, 512), (1, 64))], ids=["simt", "tc"])
+def test_causal_strided_slices_of_one_projection(grid, block):
+    B, H, d = 2, 3, 64
+    N = int(np.prod(grid))
     qkv = draw_qkv(B, N, 3 * H, d, seed=75)[0].view(B, N, 3, H, d)
     W = mhla.init_mixing(grid, block, "linear")
     qd = qkv.to(DEV)

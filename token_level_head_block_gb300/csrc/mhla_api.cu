@@ -324,10 +324,23 @@ bool blocks_contiguous(const Problem& p) {
   return false;
 }
 
-int resolve_causal_path(int32_t path, int* sel) {
-  if (path == MHLA_PATH_AUTO || path == MHLA_PATH_SIMT) { *sel = MHLA_PATH_SIMT; return MHLA_OK; }
-  if (path == MHLA_PATH_TC || path == MHLA_PATH_FUSED) return MHLA_ERR_UNSUPPORTED;
+int resolve_causal_path(const Problem& p, int32_t path, int* sel) {
+  if (path == MHLA_PATH_AUTO) {
+    *sel = tc_causal_eligible(p) ? MHLA_PATH_TC : MHLA_PATH_SIMT;
+    return MHLA_OK;
+  }
+  if (path == MHLA_PATH_SIMT) { *sel = MHLA_PATH_SIMT; return MHLA_OK; }
+  if (path == MHLA_PATH_TC) {
+    if (!tc_causal_eligible(p)) return MHLA_ERR_UNSUPPORTED;
+    *sel = MHLA_PATH_TC;
+    return MHLA_OK;
+  }
+  if (path == MHLA_PATH_FUSED) return MHLA_ERR_UNSUPPORTED;
   return MHLA_ERR_INVALID_ARG;
+}
+
+size_t causal_workspace_for(const Problem& p, int sel) {
+  return sel == MHLA_PATH_TC ? tc_causal_workspace_bytes(p) : simt_workspace_bytes(p);
 }
 
 }  // namespace
@@ -341,9 +354,16 @@ extern "C" mhla_status_t mhla_causal_workspace_size(const mhla_tensor_t* q, cons
   if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
   if (!blocks_contiguous(p)) return MHLA_ERR_SHAPE;
   int sel = 0;
-  const int rp = resolve_causal_path(path, &sel);
+  const int rp = resolve_causal_path(p, path, &sel);
   if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
-  *bytes = (p.B == 0 || p.H == 0) ? 0 : simt_workspace_bytes(p);
+  if (p.B == 0 || p.H == 0) {
+    *bytes = 0;
+  } else if (path == MHLA_PATH_AUTO && sel == MHLA_PATH_TC) {
+    // only q is known here: enough for either path, whichever AUTO takes
+    *bytes = std::max(tc_causal_workspace_bytes(p), simt_workspace_bytes(p));
+  } else {
+    *bytes = causal_workspace_for(p, sel);
+  }
   return MHLA_OK;
 }
 
@@ -357,7 +377,7 @@ extern "C" mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_
   if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
   if (!blocks_contiguous(p)) return MHLA_ERR_SHAPE;
   int sel = 0;
-  const int rp = resolve_causal_path(path, &sel);
+  const int rp = resolve_causal_path(p, path, &sel);
   if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
   if (p.B == 0 || p.H == 0) return MHLA_OK;
   if (!W) return MHLA_ERR_INVALID_ARG;
@@ -367,7 +387,7 @@ extern "C" mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_
     const uintptr_t w0 = reinterpret_cast<uintptr_t>(W);
     if (overlaps(o0, o1, w0, w0 + static_cast<uintptr_t>(p.M * p.M) * sizeof(float))) return MHLA_ERR_INVALID_ARG;
   }
-  const size_t need = simt_workspace_bytes(p);
+  const size_t need = causal_workspace_for(p, sel);
   void* ws = workspace;
   if (!ws && workspace_bytes != 0) return MHLA_ERR_WORKSPACE;
   if (ws && (workspace_bytes < need || reinterpret_cast<uintptr_t>(ws) % kAlign != 0)) return MHLA_ERR_WORKSPACE;
@@ -377,19 +397,20 @@ extern "C" mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_
     if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return MHLA_ERR_CUDA;
     owned = true;
   }
-  const int lr = launch_simt_causal(p, W, ws, stream);
+  const int lr = sel == MHLA_PATH_TC ? launch_tc_causal(p, W, ws, stream) : launch_simt_causal(p, W, ws, stream);
   if (owned && cudaFreeAsync(ws, s) != cudaSuccess && lr == MHLA_OK) return MHLA_ERR_CUDA;
   return static_cast<mhla_status_t>(lr);
 }
 
 extern "C" mhla_status_t mhla_device_status(void* stream, uint32_t* flags) {
   if (!flags) return MHLA_ERR_INVALID_ARG;
-  uint32_t tc = 0, small = 0, bwd = 0;
+  uint32_t tc = 0, small = 0, bwd = 0, causal = 0;
   const int a = read_and_clear_device_error(stream, &tc);
   const int b = read_and_clear_small_error(stream, &small);
   const int c = read_and_clear_bwd_error(stream, &bwd);
-  if (a == MHLA_ERR_CUDA || b == MHLA_ERR_CUDA || c == MHLA_ERR_CUDA) return MHLA_ERR_CUDA;
-  *flags = tc | small | bwd;
+  const int e = read_and_clear_causal_error(stream, &causal);
+  if (a == MHLA_ERR_CUDA || b == MHLA_ERR_CUDA || c == MHLA_ERR_CUDA || e == MHLA_ERR_CUDA) return MHLA_ERR_CUDA;
+  *flags = tc | small | bwd | causal;
   return *flags ? MHLA_ERR_TIMEOUT : MHLA_OK;
 }
 

@@ -52,6 +52,13 @@ int launch_simt(const Problem& p, const float* W, void* workspace, void* stream)
 // Causal MHLA on CUDA cores (contiguous blocks); same workspace as the forward,
 // Szt holding the mixed past summaries.
 int launch_simt_causal(const Problem& p, const float* W, void* workspace, void* stream);
+// Causal MHLA on tensor cores (bf16, d in {32, 64}, contiguous blocks of 64
+// tokens or a multiple of 128, N a multiple of 128).  Workspace: the unit-level
+// W' (bf16), unit summaries (Sbuf layout), unit states (St, zt layouts).
+bool tc_causal_eligible(const Problem& p);
+size_t tc_causal_workspace_bytes(const Problem& p);
+int launch_tc_causal(const Problem& p, const float* W, void* workspace, void* stream);
+int read_and_clear_causal_error(void* stream, uint32_t* flags);
 
 // Backward pass operands (dout read; dq, dk, dv, dW written) and the CUDA-core
 // backward's workspace (float32):

@@ -83,8 +83,8 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // W rounded to bf16 for the mixing GEMM, [M][Mp] with zero padding (and, when
   // WbT is given, W^T likewise); every CTA converts a slice (the GEMM runs after
-  // this kernel on the same stream).
-  {
+  // this kernel on the same stream).  Wb null: summaries only.
+  if (Wb) {
     const int64_t n = static_cast<int64_t>(g.M) * Mp;
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * kTcThreads + threadIdx.x; e < n;
          e += static_cast<int64_t>(gridDim.x) * kTcThreads) {
