@@ -181,6 +181,8 @@ def test_path_selection(L):
     for name in ("dit_s2_4096px", "sana_4096px", "video_20x32x32", "sweep_64x64", "sweep_512x512"):
         wl = WORKLOADS[name]
         assert select(L, (wl.B, wl.N, wl.H, wl.d), wl.grid, wl.block) == TC, name
+    wl = WORKLOADS["lm_causal_4096"]                 # contiguous 64-token blocks: the tile readout
+    assert select(L, (wl.B, wl.N, wl.H, wl.d), wl.grid, wl.block) == TC
     wl = WORKLOADS["deit_t_14x14"]                   # 196 tokens, 49 blocks: one fused launch
     assert select(L, (wl.B, wl.N, wl.H, wl.d), wl.grid, wl.block) == FUSED
     wl = WORKLOADS["tiny_16x16_fp32"]

@@ -165,6 +165,26 @@ def test_fused_path_agrees_with_the_three_launch_path():
     assert normwise(as_f64(a), as_f64(b)) <= TOL["bf16"]
 
 
+# The tensor-core forward on contiguous 64-token blocks (1-D sequences, rows of
+# 64): summaries and mixing as usual, the readout per 128-token tile of two blocks.
+TILE_CASES = {
+    "seq_d64": (2, 3, 64, (1, 1024), (1, 64)),
+    "seq_d32": (1, 2, 32, (1, 512), (1, 64)),
+    "rows_d64": (2, 2, 64, (16, 64), (1, 64)),
+    "m512_d64": (1, 1, 64, (1, 32768), (1, 64)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TILE_CASES))
+@pytest.mark.parametrize("phi", ["relu", "relu_eps"])
+def test_tensor_core_tile_readout(name, phi):
+    B, H, d, grid, block = TILE_CASES[name]
+    N = int(np.prod(grid))
+    q, k, v = draw_qkv(B, N, H, d, seed=35, dtype="bf16")
+    W = draw_matrix(oracle.num_blocks(grid, block), seed=36)
+    check_full(f"tile/{name}/{phi}", q, k, v, W, grid, block, "bf16", phi, 1e-6, "tc")
+
+
 def test_tiny_fp32_workload():
     wl = WORKLOADS["tiny_16x16_fp32"]
     q, k, v = draw_workload(wl)
@@ -204,6 +224,7 @@ def workload_inputs(name):
 @pytest.mark.parametrize("name,samples", [
     ("deit_t_14x14", None), ("dit_s2_4096px", 3), ("sana_4096px", 3), ("video_20x32x32", 3),
     ("sweep_64x64", None), ("sweep_128x128", 4), ("sweep_256x256", 2), ("sweep_512x512", 2),
+    ("lm_causal_4096", 3),
 ])
 def test_workload_parity(name, samples):
     wl, q, k, v = workload_inputs(name)

@@ -84,7 +84,10 @@ struct CtGeom {
   int32_t N, H, M, w, U, Mu, nt;   // tokens, heads, blocks, block and unit length, units, tiles per (b, h)
 };
 
-template <int D, int NU>
+// INTRA = false (the non-causal forward on 64-token contiguous blocks): units
+// are the blocks, the states are the ordinary mixed summaries S~, z~, and only
+// the state part of MMA 2 runs (no k, v tiles, no scores).
+template <int D, int NU, bool INTRA>
 __global__ void __launch_bounds__(kCtThreads, 1)
 tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_st, CtGeom g,
@@ -166,10 +169,12 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       auto issue_qkv = [&](int st, int64_t u) {
         int32_t b, h, tile;
         coords(u, b, h, tile);
-        mbar_arrive_expect_tx(full + st, 3 * Cfg::TILE);
+        mbar_arrive_expect_tx(full + st, (INTRA ? 3 : 1) * Cfg::TILE);
         tma_load_4d(qt + st * Cfg::TILE, &tm_q, full + st, 0, h, tile * kTile, b, pol);
-        tma_load_4d(kt + st * Cfg::TILE, &tm_k, full + st, 0, h, tile * kTile, b, pol);
-        tma_load_4d(vt + st * Cfg::TILE, &tm_v, full + st, 0, h, tile * kTile, b, pol);
+        if (INTRA) {
+          tma_load_4d(kt + st * Cfg::TILE, &tm_k, full + st, 0, h, tile * kTile, b, pol);
+          tma_load_4d(vt + st * Cfg::TILE, &tm_v, full + st, 0, h, tile * kTile, b, pol);
+        }
       };
       auto issue_st = [&](int64_t u) {
         int32_t b, h, tile;
@@ -199,7 +204,7 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // MMA 1: scores = phi(Q) phi(K)^T, 128 x 128
         if (!cwait(phid, par, abortf)) break;
         tc_fence_after();
-        {
+        if (INTRA) {
           constexpr uint32_t idesc = idesc_bf16_f32(128, kTile, /*a K-major*/ false, /*b K-major*/ false);
           const uint32_t qa = smem_u32(qt + st * Cfg::TILE), ka = smem_u32(kt + st * Cfg::TILE);
 #pragma unroll
@@ -219,10 +224,12 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           constexpr uint32_t idesc = idesc_bf16_f32(128, Cfg::NO, /*a K-major*/ false, /*b MN-major*/ true);
           const uint32_t pa = smem_u32(sp), va = smem_u32(vt + st * Cfg::TILE);
           const uint32_t lbo_v = static_cast<uint32_t>(Cfg::ONES_OFF - (Cfg::VT_OFF + st * Cfg::TILE));
+          if (INTRA) {
 #pragma unroll
-          for (int ks = 0; ks < kTile / 16; ++ks)
-            mma_bf16(tmem + 128, smem_desc(pa + (ks >> 2) * Cfg::P_CHUNK + (ks & 3) * 32, 16, 1024, 2),
-                     smem_desc(va + ks * 2 * Cfg::SBO, lbo_v, Cfg::SBO, Cfg::LAYOUT), idesc, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < kTile / 16; ++ks)
+              mma_bf16(tmem + 128, smem_desc(pa + (ks >> 2) * Cfg::P_CHUNK + (ks & 3) * 32, 16, 1024, 2),
+                       smem_desc(va + ks * 2 * Cfg::SBO, lbo_v, Cfg::SBO, Cfg::LAYOUT), idesc, ks > 0 ? 1u : 0u);
+          }
 #pragma unroll
           for (int k = 0; k < NU; ++k) {
             const uint32_t aq = NU > 1 ? smem_u32(qm + k * Cfg::TILE) : smem_u32(qt + st * Cfg::TILE);
@@ -230,7 +237,8 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
               mma_bf16(tmem + 128, smem_desc(aq + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
-                       smem_desc(sb + ks * 2 * Cfg::SBO, Cfg::ST, Cfg::SBO, Cfg::LAYOUT), idesc, 1u);
+                       smem_desc(sb + ks * 2 * Cfg::SBO, Cfg::ST, Cfg::SBO, Cfg::LAYOUT), idesc,
+                       (INTRA || k > 0 || ks > 0) ? 1u : 0u);
           }
           mma_commit(done2);
           ++n_m2;
@@ -270,7 +278,7 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       coords(u, b, h, tile);
       // ---- phi on the q and k tiles of this stage
       if (!cwarp_wait(full + st, (it >> 1) & 1u, abortf)) break;
-      for (int e = tid; e < 2 * Cfg::TILE / 16; e += kCtWorkers) {
+      for (int e = tid; e < (INTRA ? 2 : 1) * Cfg::TILE / 16; e += kCtWorkers) {
         uint4* p = reinterpret_cast<uint4*>(e < Cfg::TILE / 16 ? qt + st * Cfg::TILE : kt + st * Cfg::TILE) +
                    (e % (Cfg::TILE / 16));
         *p = phi8_packed(*p, add_eps, eps2);
@@ -293,9 +301,9 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int32_t blk = (n0 + row) / g.w;
       const int32_t first = blk * g.w - n0;          // first key of this row's block inside the tile (may be < 0)
       const float wii = __ldg(W + static_cast<int64_t>(blk) * g.M + blk);
-      if (!cwarp_wait(done1, par, abortf)) break;
+      if (INTRA && !cwarp_wait(done1, par, abortf)) break;
       tc_fence_after();
-      for (int m = half; m < kTile / 32; m += 2) {   // 32 keys per step
+      for (int m = half; INTRA && m < kTile / 32; m += 2) {   // 32 keys per step
         uint32_t r[32];
         tmem_ld_x32(lane_base + m * 32, r);
         tmem_ld_wait();
@@ -314,6 +322,8 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
               make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
       }
       if constexpr (NU > 1) {
+        // every warp's phi on the q tile is in (other warps wrote parts of this row)
+        if (!cwarp_wait(phid, par, abortf)) break;
         // warpgroup `half` writes unit `half`'s copy of this row: phi(q_t) there, zeros elsewhere
         const uint8_t* src = qt + st * Cfg::TILE + row * Cfg::ROWB;
         uint8_t* dst = qm + half * Cfg::TILE + row * Cfg::ROWB;
@@ -436,14 +446,14 @@ bool ct_map(const Problem& p, const Operand& o, CUtensorMap* m) {
                            p.d == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int D, int NU>
-int launch_ct_tile(const Problem& p, const float* W, const CtLayout& L, const __nv_bfloat16* St, const float* zt,
+template <int D, int NU, bool INTRA>
+int launch_ct_tile(const Problem& p, const float* W, int64_t Mu, const __nv_bfloat16* St, const float* zt,
                    cudaStream_t stream) {
   using Cfg = CtCfg<D, NU>;
   CUtensorMap tq, tk, tv, tst;
   if (!ct_map(p, p.q, &tq) || !ct_map(p, p.k, &tk) || !ct_map(p, p.v, &tv)) return MHLA_ERR_CUDA;
   {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(p.BH() * L.Mu * D)};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(p.BH() * Mu * D)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D * 2)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(D)};
     if (!encode_tensor_map(&tst, 2, const_cast<__nv_bfloat16*>(St), dims, strides, box,
@@ -455,26 +465,27 @@ int launch_ct_tile(const Problem& p, const float* W, const CtLayout& L, const __
   g.H = static_cast<int32_t>(p.H);
   g.M = static_cast<int32_t>(p.M);
   g.w = static_cast<int32_t>(p.w);
-  g.U = L.U;
-  g.Mu = static_cast<int32_t>(L.Mu);
+  g.U = static_cast<int32_t>(p.N / Mu);
+  g.Mu = static_cast<int32_t>(Mu);
   g.nt = static_cast<int32_t>(p.N / kTile);
   const int64_t n_units = p.BH() * g.nt;
   const int sms = device_sm_count();
   if (sms <= 0) return MHLA_ERR_CUDA;
-  if (cudaFuncSetAttribute(tc_causal_tile<D, NU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tc_causal_tile<D, NU, INTRA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(Cfg::SMEM)) != cudaSuccess)
     return MHLA_ERR_CUDA;
   const int grid = static_cast<int>(std::min<int64_t>(n_units, sms));
-  KernelTimer timer("tc_causal_tile", stream);
-  tc_causal_tile<D, NU><<<grid, kCtThreads, Cfg::SMEM, stream>>>(tq, tk, tv, tst, g, n_units, p.phi_kind, p.eps, W,
-                                                                  zt, static_cast<__nv_bfloat16*>(p.o.data), p.o.sb,
-                                                                  p.o.sn, p.o.sh);
+  KernelTimer timer(INTRA ? "tc_causal_tile" : "tc_tile_output", stream);
+  tc_causal_tile<D, NU, INTRA><<<grid, kCtThreads, Cfg::SMEM, stream>>>(
+      tq, tk, tv, tst, g, n_units, p.phi_kind, p.eps, W, zt, static_cast<__nv_bfloat16*>(p.o.data), p.o.sb, p.o.sn,
+      p.o.sh);
   return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
 }
 
 }  // namespace
 
 bool tc_causal_eligible(const Problem& p) {
+  if (!blocks_contiguous(p)) return false;
   if (p.dtype != MHLA_BF16 || (p.d != 32 && p.d != 64)) return false;
   if (p.B < 1 || p.H < 1 || p.N % kTile != 0) return false;
   if (p.w != 64 && p.w % 128 != 0) return false;
@@ -514,8 +525,24 @@ int launch_tc_causal(const Problem& p, const float* W, void* workspace, void* st
   if (rc == MHLA_OK) rc = tc_run_mix(pu, Wu, L.Mp, ws + L.sbuf_off, St, zt, stream);
   if (rc != MHLA_OK) return rc;
   const int NU = L.U == 64 ? 2 : 1;
-  if (p.d == 64) return NU == 2 ? launch_ct_tile<64, 2>(p, W, L, St, zt, s) : launch_ct_tile<64, 1>(p, W, L, St, zt, s);
-  return NU == 2 ? launch_ct_tile<32, 2>(p, W, L, St, zt, s) : launch_ct_tile<32, 1>(p, W, L, St, zt, s);
+  if (p.d == 64)
+    return NU == 2 ? launch_ct_tile<64, 2, true>(p, W, L.Mu, St, zt, s) : launch_ct_tile<64, 1, true>(p, W, L.Mu, St, zt, s);
+  return NU == 2 ? launch_ct_tile<32, 2, true>(p, W, L.Mu, St, zt, s) : launch_ct_tile<32, 1, true>(p, W, L.Mu, St, zt, s);
+}
+
+bool tc_tile_eligible(const Problem& p) {
+  return p.w == 64 && blocks_contiguous(p) && tc_causal_eligible(p);
+}
+
+int launch_tc_tile_forward(const Problem& p, const float* W, void* Wb, int64_t Mp, void* Sbuf, void* St, float* zt,
+                           void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Problem pu = unit_problem(p, 64);   // units are the blocks
+  int rc = tc_run_summary(pu, W, Wb, nullptr, Mp, Sbuf, stream);
+  if (rc == MHLA_OK) rc = tc_run_mix(pu, Wb, Mp, Sbuf, St, zt, stream);
+  if (rc != MHLA_OK) return rc;
+  const auto* st = static_cast<const __nv_bfloat16*>(St);
+  return p.d == 64 ? launch_ct_tile<64, 2, false>(p, W, p.M, st, zt, s) : launch_ct_tile<32, 2, false>(p, W, p.M, st, zt, s);
 }
 
 int read_and_clear_causal_error(void* stream, uint32_t* flags) {

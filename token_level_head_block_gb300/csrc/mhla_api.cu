@@ -311,19 +311,6 @@ extern "C" mhla_status_t mhla_backward(const mhla_tensor_t* q, const mhla_tensor
 namespace mhla {
 namespace {
 
-// Every block a contiguous range of raster-order tokens: for some axis a, the
-// block is one unit on every slower axis and the whole grid on every faster one.
-bool blocks_contiguous(const Problem& p) {
-  const int64_t g[3] = {p.T, p.Y, p.X}, b[3] = {p.bt, p.by, p.bx};
-  for (int a = 0; a < 3; ++a) {
-    bool ok = true;
-    for (int s = 0; s < a; ++s) ok = ok && b[s] == 1;
-    for (int f = a + 1; f < 3; ++f) ok = ok && b[f] == g[f];
-    if (ok) return true;
-  }
-  return false;
-}
-
 int resolve_causal_path(const Problem& p, int32_t path, int* sel) {
   if (path == MHLA_PATH_AUTO) {
     *sel = tc_causal_eligible(p) ? MHLA_PATH_TC : MHLA_PATH_SIMT;

@@ -59,6 +59,12 @@ bool tc_causal_eligible(const Problem& p);
 size_t tc_causal_workspace_bytes(const Problem& p);
 int launch_tc_causal(const Problem& p, const float* W, void* workspace, void* stream);
 int read_and_clear_causal_error(void* stream, uint32_t* flags);
+// The forward's tensor-core path for contiguous 64-token blocks (N a multiple
+// of 128): summaries and mixing as usual, then per 128-token tile one MMA per
+// block of the tile against that block's rows.  Workspace as tc_layout.
+bool tc_tile_eligible(const Problem& p);
+int launch_tc_tile_forward(const Problem& p, const float* W, void* Wb, int64_t Mp, void* Sbuf, void* St, float* zt,
+                           void* stream);
 
 // Backward pass operands (dout read; dq, dk, dv, dW written) and the CUDA-core
 // backward's workspace (float32):
@@ -129,6 +135,19 @@ class KernelTimer {
   void* stream_;
   void* start_;
 };
+
+// Every block a contiguous range of raster-order tokens: for some axis a, the
+// block is one unit on every slower axis and the whole grid on every faster one.
+inline bool blocks_contiguous(const Problem& p) {
+  const int64_t g[3] = {p.T, p.Y, p.X}, b[3] = {p.bt, p.by, p.bx};
+  for (int a = 0; a < 3; ++a) {
+    bool ok = true;
+    for (int s = 0; s < a; ++s) ok = ok && b[s] == 1;
+    for (int f = a + 1; f < 3; ++f) ok = ok && b[f] == g[f];
+    if (ok) return true;
+  }
+  return false;
+}
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }

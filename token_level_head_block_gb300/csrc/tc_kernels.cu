@@ -104,7 +104,9 @@ bool encode_tensor_map(CUtensorMap* m, int rank, void* base, const cuuint64_t* d
 
 int device_sm_count() { return device_sms(); }
 
-bool tc_eligible(const Problem& p) {
+// The three-launch tensor-core forward: tokens per block a multiple of 128 in
+// whole block rows, or contiguous 64-token blocks (the tile readout).
+bool tc_rows_eligible(const Problem& p) {
   if (p.dtype != MHLA_BF16) return false;
   if (p.d != 32 && p.d != 64) return false;
   if (p.B < 1 || p.H < 1) return false;
@@ -120,11 +122,16 @@ bool tc_eligible(const Problem& p) {
   return true;
 }
 
+bool tc_eligible(const Problem& p) { return tc_rows_eligible(p) || tc_tile_eligible(p); }
+
 size_t tc_workspace_bytes(const Problem& p) { return tc_layout(p).total; }
 
 int launch_tc(const Problem& p, const float* W, void* workspace, void* stream) {
   const TcLayout L = tc_layout(p);
   char* ws = static_cast<char*>(workspace);
+  if (!tc_rows_eligible(p))
+    return launch_tc_tile_forward(p, W, ws + L.wb_off, L.Mp, ws + L.sbuf_off, ws + L.st_off,
+                                  reinterpret_cast<float*>(ws + L.zt_off), stream);
   int rc = tc_run_summary(p, W, ws + L.wb_off, nullptr, L.Mp, ws + L.sbuf_off, stream);
   if (rc == MHLA_OK)
     rc = tc_run_mix(p, ws + L.wb_off, L.Mp, ws + L.sbuf_off, ws + L.st_off, reinterpret_cast<float*>(ws + L.zt_off),
