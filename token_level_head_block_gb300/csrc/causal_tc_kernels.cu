@@ -15,18 +15,21 @@
 //                                               0 otherwise,
 // (z'_u likewise): one GEMM with the forward's mixing kernel on the expanded
 // unit-level W'.  Then per 128-token tile (1 or 2 units), with phi(Q)_u the
-// tile's rows of unit u (zero elsewhere) and P[t][s] = W[b(t)][b(t)] phi(q_t) .
-// phi(k_s) for s <= t in the same block (0 otherwise):
-//   [num | den] = [P | phi(Q)_0 | phi(Q)_1] [[V | 1]; [S'_0 | z'_0]; [S'_1 | z'_1]]
-// one accumulator for the causal part inside the tile and the state part, so
-// numerator and denominator come out of the same MMA.
+// tile's rows of unit u and P[t][s] = W[b(t)][b(t)] phi(q_t) . phi(k_s) for
+// s <= t in the same block (0 otherwise):
+//   [num | den]_t = P_t [V | 1] + phi(q_t) [S'_u(t) | z'_u(t)]
+// numerator and denominator from the same MMAs.
+//
+// With two units per tile the state term of each unit gets its own
+// accumulator (A = the whole phi(Q) tile, each row reads its own unit's), so
+// the state MMAs run while the workers form P.
 //
 // tc_causal_tile: persistent CTAs, warp 8 issues TMA and MMAs, warps 0-7
-// (two warpgroups) apply phi, form P and the masked phi(Q) copies, and write
-// the output.  q, k, v tiles are double-buffered (the next tile's loads run
-// while the current one computes).  Every wait is bounded; a wait that gives up
-// sets bit 0 of this file's device error word and an abort flag, the CTA
-// drains what it issued and releases tensor memory.
+// (two warpgroups) apply phi, form P and write the output.  q, k, v tiles and
+// the state tiles are double-buffered (the next tile's loads run while the
+// current one computes).  Every wait is bounded; a wait that gives up sets
+// bit 0 of this file's device error word and an abort flag, the CTA drains
+// what it issued and releases tensor memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -71,13 +74,16 @@ struct CtCfg {
   static constexpr int VT_OFF = KT_OFF + 2 * TILE;    // [2] v tiles, then the ones atom
   static constexpr int ONES_OFF = VT_OFF + 2 * TILE;
   static constexpr int P_OFF = ONES_OFF + TILE;
-  static constexpr int QM_OFF = P_OFF + 2 * P_CHUNK;  // NU > 1: phi(q) rows of each unit
-  static constexpr int SZ_OFF = QM_OFF + (NU > 1 ? NU * TILE : 0);   // per unit: state tile, z' atom
-  static constexpr int ZRAW_OFF = SZ_OFF + NU * 2 * ST;
-  static constexpr int CTRL_OFF = ZRAW_OFF + NU * D * 4;
+  static constexpr int SLOT = NU * 2 * ST;            // per unit: state tile, z' atom
+  static constexpr int SZ_OFF = P_OFF + 2 * P_CHUNK;  // [2] slots
+  static constexpr int ZRAW_OFF = SZ_OFF + 2 * SLOT;  // [2][NU][D] float32
+  static constexpr int CTRL_OFF = ZRAW_OFF + 2 * NU * D * 4;
   static constexpr size_t SMEM = CTRL_OFF + 128 + 1024;
   static constexpr int NO = D + 16;                   // MMA 2 columns: d values, the denominator block
-  static constexpr int TMEM_COLS = 256;               // scores [0, 128), the accumulator [128, 128 + NO)
+  // scores [0, 128); P [V | 1] (and, with one unit, its state term) at 128;
+  // with two units, their state terms at 256 and 384
+  static constexpr int TMEM_COLS = NU > 1 ? 512 : 256;
+  static __host__ __device__ constexpr int state_col(int k) { return NU > 1 ? 256 + 128 * k : 128; }
 };
 
 struct CtGeom {
@@ -86,7 +92,7 @@ struct CtGeom {
 
 // INTRA = false (the non-causal forward on 64-token contiguous blocks): units
 // are the blocks, the states are the ordinary mixed summaries S~, z~, and only
-// the state part of MMA 2 runs (no k, v tiles, no scores).
+// the state MMAs run (no k, v tiles, no scores).
 template <int D, int NU, bool INTRA>
 __global__ void __launch_bounds__(kCtThreads, 1)
 tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -102,26 +108,28 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   uint8_t* vt = smem + Cfg::VT_OFF;
   uint8_t* ones = smem + Cfg::ONES_OFF;
   uint8_t* sp = smem + Cfg::P_OFF;
-  uint8_t* qm = smem + Cfg::QM_OFF;
   uint8_t* sz = smem + Cfg::SZ_OFF;
   float* zraw = reinterpret_cast<float*>(smem + Cfg::ZRAW_OFF);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::CTRL_OFF);   // [2] q, k, v of a stage landed
-  uint64_t* full_st = full + 2;       // the tile's state tiles and z' landed
-  uint64_t* phid = full + 3;          // workers: phi applied
-  uint64_t* done1 = full + 4;         // MMA 1 (scores) complete
-  uint64_t* ready = full + 5;         // workers: P, the masked phi(q) copies and the z' atoms written
-  uint64_t* done2 = full + 6;         // MMA 2 complete
-  uint64_t* odone = full + 7;         // workers: the accumulator read
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 8);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::CTRL_OFF);   // [2] q (k, v) of a stage landed
+  uint64_t* full_st = full + 2;       // [2] state tiles and z' of a slot landed
+  uint64_t* phid = full + 4;          // workers: phi applied
+  uint64_t* done1 = full + 5;         // MMA 1 (scores) complete
+  uint64_t* zready = full + 6;        // workers: the z' atoms of the slot written
+  uint64_t* ready = full + 7;         // workers: P written
+  uint64_t* done2 = full + 8;         // every MMA of the tile complete
+  uint64_t* odone = full + 9;         // workers: the accumulators read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 10);
   volatile uint32_t* abortf = tmem_slot + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == kCtWorkers) {
-    mbar_init(full, 1);
-    mbar_init(full + 1, 1);
-    mbar_init(full_st, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(full_st + i, 1);
+    }
     mbar_init(phid, kCtWorkers / 32);
     mbar_init(done1, 1);
+    mbar_init(zready, kCtWorkers / 32);
     mbar_init(ready, kCtWorkers / 32);
     mbar_init(done2, 1);
     mbar_init(odone, kCtWorkers / 32);
@@ -137,14 +145,14 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tmem_relinquish();
   }
   if (tid < kCtWorkers) {
-    // ones atom of [V | 1]: row s holds (1, 0, ..., 0); z' atoms start at zero
+    // ones atom of [V | 1]: row s holds (1, 0, ..., 0); the z' atoms start at zero
     for (int idx = tid; idx < kTile * (D / 8); idx += kCtWorkers) {
       const int row = idx / (D / 8), phys = idx % (D / 8);
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if ((phys ^ swz<D>(row)) == 0) v.x = 0x3F80u;
       *reinterpret_cast<uint4*>(ones + row * Cfg::ROWB + phys * 16) = v;
     }
-    for (int e = tid; e < NU * 2 * Cfg::ST / 16; e += kCtWorkers)
+    for (int e = tid; e < 2 * Cfg::SLOT / 16; e += kCtWorkers)
       reinterpret_cast<uint4*>(sz)[e] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
@@ -166,7 +174,7 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       const uint64_t pol_st = policy_evict_last();
-      auto issue_qkv = [&](int st, int64_t u) {
+      auto issue = [&](int st, int64_t u) {   // stage st: q (k, v) tiles and the state slot
         int32_t b, h, tile;
         coords(u, b, h, tile);
         mbar_arrive_expect_tx(full + st, (INTRA ? 3 : 1) * Cfg::TILE);
@@ -175,38 +183,32 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           tma_load_4d(kt + st * Cfg::TILE, &tm_k, full + st, 0, h, tile * kTile, b, pol);
           tma_load_4d(vt + st * Cfg::TILE, &tm_v, full + st, 0, h, tile * kTile, b, pol);
         }
-      };
-      auto issue_st = [&](int64_t u) {
-        int32_t b, h, tile;
-        coords(u, b, h, tile);
-        mbar_arrive_expect_tx(full_st, NU * (Cfg::ST + D * 4));
+        mbar_arrive_expect_tx(full_st + st, NU * (Cfg::ST + D * 4));
         for (int k = 0; k < NU; ++k) {
           const int64_t su = (static_cast<int64_t>(b) * g.H + h) * g.Mu + static_cast<int64_t>(tile) * NU + k;
-          tma_load_2d(sz + k * 2 * Cfg::ST, &tm_st, full_st, 0, static_cast<int32_t>(su * D), pol_st);
-          bulk_load(zraw + k * D, zt + su * D, D * 4, full_st, pol_st);
+          tma_load_2d(sz + st * Cfg::SLOT + k * 2 * Cfg::ST, &tm_st, full_st + st, 0, static_cast<int32_t>(su * D),
+                      pol_st);
+          bulk_load(zraw + (st * NU + k) * D, zt + su * D, D * 4, full_st + st, pol_st);
         }
       };
-      uint32_t n_full[2] = {0, 0}, n_st = 0, n_m1 = 0, n_m2 = 0;
+      uint32_t n_stage[2] = {0, 0}, n_m1 = 0, n_m2 = 0;
       const int64_t u0 = blockIdx.x, stride = gridDim.x;
-      if (u0 < n_units) {
-        issue_qkv(0, u0);
-        issue_st(u0);
-        n_full[0] = n_st = 1;
-        if (u0 + stride < n_units) {
-          issue_qkv(1, u0 + stride);
-          n_full[1] = 1;
+      for (int st = 0; st < 2; ++st)
+        if (u0 + st * stride < n_units) {
+          issue(st, u0 + st * stride);
+          n_stage[st] = 1;
         }
-      }
       uint32_t it = 0;
       for (int64_t u = u0; u < n_units; u += stride, ++it) {
-        const uint32_t par = it & 1u;
+        const uint32_t par = it & 1u, par2 = (it >> 1) & 1u;
         const int st = static_cast<int>(it & 1u);
+        const uint32_t qa = smem_u32(qt + st * Cfg::TILE);
         // MMA 1: scores = phi(Q) phi(K)^T, 128 x 128
-        if (!cwait(phid, par, abortf)) break;
+        if (!cwait(full + st, par2, abortf) || !cwait(phid, par, abortf)) break;
         tc_fence_after();
         if (INTRA) {
           constexpr uint32_t idesc = idesc_bf16_f32(128, kTile, /*a K-major*/ false, /*b K-major*/ false);
-          const uint32_t qa = smem_u32(qt + st * Cfg::TILE), ka = smem_u32(kt + st * Cfg::TILE);
+          const uint32_t ka = smem_u32(kt + st * Cfg::TILE);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks)
             mma_bf16(tmem, smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
@@ -214,70 +216,66 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           mma_commit(done1);
           ++n_m1;
         }
-        // MMA 2: [P | phi(Q)_u] [[V | 1]; [S'_u | z'_u]] into columns [128, 128 + d + 16);
-        // the v tile and the state tiles landed (TMA), P, the copies and z' written
-        if (!cwait(full + st, (it >> 1) & 1u, abortf) || !cwait(full_st, par, abortf)) break;
-        if (!cwait(ready, par, abortf)) break;
+        // state MMAs: phi(Q) [S'_u | z'_u hi lo], one accumulator per unit (with one
+        // unit, the accumulator P [V | 1] joins next)
+        if (!cwait(full_st + st, par2, abortf) || !cwait(zready, par, abortf)) break;
         if (it > 0 && !cwait(odone, par ^ 1u, abortf)) break;
         tc_fence_after();
-        {
-          constexpr uint32_t idesc = idesc_bf16_f32(128, Cfg::NO, /*a K-major*/ false, /*b MN-major*/ true);
+        constexpr uint32_t idesc2 = idesc_bf16_f32(128, Cfg::NO, /*a K-major*/ false, /*b MN-major*/ true);
+#pragma unroll
+        for (int k = 0; k < NU; ++k) {
+          const uint32_t sb = smem_u32(sz + st * Cfg::SLOT + k * 2 * Cfg::ST);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem + Cfg::state_col(k), smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
+                     smem_desc(sb + ks * 2 * Cfg::SBO, Cfg::ST, Cfg::SBO, Cfg::LAYOUT), idesc2, ks > 0 ? 1u : 0u);
+        }
+        if (INTRA) {   // P [V | 1] into column 128
+          if (!cwait(ready, par, abortf)) break;
+          tc_fence_after();
           const uint32_t pa = smem_u32(sp), va = smem_u32(vt + st * Cfg::TILE);
           const uint32_t lbo_v = static_cast<uint32_t>(Cfg::ONES_OFF - (Cfg::VT_OFF + st * Cfg::TILE));
-          if (INTRA) {
 #pragma unroll
-            for (int ks = 0; ks < kTile / 16; ++ks)
-              mma_bf16(tmem + 128, smem_desc(pa + (ks >> 2) * Cfg::P_CHUNK + (ks & 3) * 32, 16, 1024, 2),
-                       smem_desc(va + ks * 2 * Cfg::SBO, lbo_v, Cfg::SBO, Cfg::LAYOUT), idesc, ks > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int k = 0; k < NU; ++k) {
-            const uint32_t aq = NU > 1 ? smem_u32(qm + k * Cfg::TILE) : smem_u32(qt + st * Cfg::TILE);
-            const uint32_t sb = smem_u32(sz + k * 2 * Cfg::ST);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-              mma_bf16(tmem + 128, smem_desc(aq + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
-                       smem_desc(sb + ks * 2 * Cfg::SBO, Cfg::ST, Cfg::SBO, Cfg::LAYOUT), idesc,
-                       (INTRA || k > 0 || ks > 0) ? 1u : 0u);
-          }
-          mma_commit(done2);
-          ++n_m2;
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            mma_bf16(tmem + 128, smem_desc(pa + (ks >> 2) * Cfg::P_CHUNK + (ks & 3) * 32, 16, 1024, 2),
+                     smem_desc(va + ks * 2 * Cfg::SBO, lbo_v, Cfg::SBO, Cfg::LAYOUT), idesc2,
+                     (NU == 1 || ks > 0) ? 1u : 0u);
         }
+        mma_commit(done2);
+        ++n_m2;
         if (!cwait(done2, par, abortf)) break;
-        // this tile's q, k, v stage and state tiles are consumed
-        const int64_t nu1 = u + stride, nu2 = u + 2 * stride;
-        if (nu1 < n_units) {
-          issue_st(nu1);
-          ++n_st;
-        }
-        if (nu2 < n_units) {
-          issue_qkv(st, nu2);
-          ++n_full[st];
+        // this stage's tiles and state slot are consumed: the tile after next goes there
+        if (u + 2 * stride < n_units) {
+          issue(st, u + 2 * stride);
+          ++n_stage[st];
         }
       }
       for (int st = 0; st < 2; ++st)
-        if (n_full[st]) cdrain(full + st, (n_full[st] - 1) & 1u);
-      if (n_st) cdrain(full_st, (n_st - 1) & 1u);
+        if (n_stage[st]) {
+          cdrain(full + st, (n_stage[st] - 1) & 1u);
+          cdrain(full_st + st, (n_stage[st] - 1) & 1u);
+        }
       if (n_m1) cdrain(done1, (n_m1 - 1) & 1u);
       if (n_m2) cdrain(done2, (n_m2 - 1) & 1u);
     }
   } else {
     // ------------------------------------------------------------ workers
     const int row = tid & 127;                    // query row = TMEM lane
-    const int half = tid >> 7;                    // key chunk and output columns of this warpgroup
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const int half = tid >> 7;                    // key chunks and output columns of this warpgroup
+    const int q4 = warp & 3;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    const int my_unit = NU > 1 ? q4 >> 1 : 0;     // rows 0-63 unit 0, 64-127 unit 1: uniform per warp
     const bool add_eps = phi_kind == MHLA_PHI_RELU_EPS;
     const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
     const int swr = row & 7;
-    const int my_unit = row / (kTile / NU);       // unit of this row inside the tile
     uint32_t it = 0;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-      const uint32_t par = it & 1u;
+      const uint32_t par = it & 1u, par2 = (it >> 1) & 1u;
       const int st = static_cast<int>(it & 1u);
       int32_t b, h, tile;
       coords(u, b, h, tile);
-      // ---- phi on the q and k tiles of this stage
-      if (!cwarp_wait(full + st, (it >> 1) & 1u, abortf)) break;
+      // ---- phi on the q (and k) tiles of this stage
+      if (!cwarp_wait(full + st, par2, abortf)) break;
       for (int e = tid; e < (INTRA ? 2 : 1) * Cfg::TILE / 16; e += kCtWorkers) {
         uint4* p = reinterpret_cast<uint4*>(e < Cfg::TILE / 16 ? qt + st * Cfg::TILE : kt + st * Cfg::TILE) +
                    (e % (Cfg::TILE / 16));
@@ -286,74 +284,83 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(phid);
-      // ---- z' atoms of the state part (row r: columns 0, 1 = hi, lo)
-      if (!cwarp_wait(full_st, par, abortf)) break;
+      // ---- z' atoms of this slot (row r: columns 0, 1 = hi, lo)
+      if (!cwarp_wait(full_st + st, par2, abortf)) break;
       if (tid < NU * D) {
         const int k = tid / D, r = tid % D;
-        const float zv = zraw[k * D + r];
+        const float zv = zraw[(st * NU + k) * D + r];
         const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
         const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
-        *reinterpret_cast<uint32_t*>(sz + k * 2 * Cfg::ST + Cfg::ST + r * Cfg::ROWB + swz<D>(r) * 16) =
+        *reinterpret_cast<uint32_t*>(sz + st * Cfg::SLOT + k * 2 * Cfg::ST + Cfg::ST + r * Cfg::ROWB + swz<D>(r) * 16) =
             static_cast<uint32_t>(__bfloat16_as_ushort(hi)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
       }
-      // ---- P = W_ii * score for keys s <= t of the same block; masked phi(q) copies
-      const int32_t n0 = tile * kTile;
-      const int32_t blk = (n0 + row) / g.w;
-      const int32_t first = blk * g.w - n0;          // first key of this row's block inside the tile (may be < 0)
-      const float wii = __ldg(W + static_cast<int64_t>(blk) * g.M + blk);
-      if (INTRA && !cwarp_wait(done1, par, abortf)) break;
-      tc_fence_after();
-      for (int m = half; INTRA && m < kTile / 32; m += 2) {   // 32 keys per step
-        uint32_t r[32];
-        tmem_ld_x32(lane_base + m * 32, r);
-        tmem_ld_wait();
-        uint32_t packed[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int s0 = m * 32 + e;
-          const bool k0 = s0 <= row && s0 >= first;
-          const bool k1 = s0 + 1 <= row && s0 + 1 >= first;
-          packed[e >> 1] = pack_bf16(k0 ? __uint_as_float(r[e]) * wii : 0.0f, k1 ? __uint_as_float(r[e + 1]) * wii : 0.0f);
-        }
-        uint8_t* prow = sp + (m >> 1) * Cfg::P_CHUNK + row * 128;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(prow + ((((m & 1) * 4 + q) ^ swr) * 16)) =
-              make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-      }
-      if constexpr (NU > 1) {
-        // every warp's phi on the q tile is in (other warps wrote parts of this row)
-        if (!cwarp_wait(phid, par, abortf)) break;
-        // warpgroup `half` writes unit `half`'s copy of this row: phi(q_t) there, zeros elsewhere
-        const uint8_t* src = qt + st * Cfg::TILE + row * Cfg::ROWB;
-        uint8_t* dst = qm + half * Cfg::TILE + row * Cfg::ROWB;
-#pragma unroll
-        for (int q = 0; q < D / 8; ++q) {
-          const uint4 v = my_unit == half ? *reinterpret_cast<const uint4*>(src + q * 16) : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(dst + q * 16) = v;
-        }
-      }
       fence_proxy_async_smem();
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ready);
+      if (lane == 0) mbar_arrive(zready);
+      const int32_t n0 = tile * kTile;
+      if (INTRA) {
+        // ---- P = W_ii * score for keys s <= t of the same block
+        const int32_t blk = (n0 + row) / g.w;
+        const int32_t first = blk * g.w - n0;      // first key of this row's block inside the tile (may be < 0)
+        const float wii = __ldg(W + static_cast<int64_t>(blk) * g.M + blk);
+        if (!cwarp_wait(done1, par, abortf)) break;
+        tc_fence_after();
+        for (int m = half; m < kTile / 32; m += 2) {   // 32 keys per step
+          uint32_t r[32];
+          tmem_ld_x32(lane_base + m * 32, r);
+          tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int s0 = m * 32 + e;
+            const bool k0 = s0 <= row && s0 >= first;
+            const bool k1 = s0 + 1 <= row && s0 + 1 >= first;
+            packed[e >> 1] =
+                pack_bf16(k0 ? __uint_as_float(r[e]) * wii : 0.0f, k1 ? __uint_as_float(r[e + 1]) * wii : 0.0f);
+          }
+          uint8_t* prow = sp + (m >> 1) * Cfg::P_CHUNK + row * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(prow + ((((m & 1) * 4 + q) ^ swr) * 16)) =
+                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ready);
+      }
       // ---- output: o_t = num_t / (den_t + eps), this warpgroup's half of the columns
       if (!cwarp_wait(done2, par, abortf)) break;
       tc_fence_after();
       constexpr int HC = D / 2;
       uint32_t o[HC], dn[2];
+      const uint32_t sc = lane_base + Cfg::state_col(my_unit);
       if constexpr (HC == 32) {
-        tmem_ld_x32(lane_base + 128 + half * HC, o);
+        tmem_ld_x32(sc + half * HC, o);
       } else {
-        tmem_ld_x16(lane_base + 128 + half * HC, o);
+        tmem_ld_x16(sc + half * HC, o);
       }
-      tmem_ld_x1(lane_base + 128 + D, dn[0]);
-      tmem_ld_x1(lane_base + 128 + D + 1, dn[1]);
+      tmem_ld_x1(sc + D, dn[0]);
+      tmem_ld_x1(sc + D + 1, dn[1]);
       tmem_ld_wait();
+      float den = __uint_as_float(dn[0]) + __uint_as_float(dn[1]);
+      if (INTRA && NU > 1) {   // add P [V | 1] from column 128
+        uint32_t o2[HC], d2;
+        if constexpr (HC == 32) {
+          tmem_ld_x32(lane_base + 128 + half * HC, o2);
+        } else {
+          tmem_ld_x16(lane_base + 128 + half * HC, o2);
+        }
+        tmem_ld_x1(lane_base + 128 + D, d2);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < HC; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) + __uint_as_float(o2[e]));
+        den += __uint_as_float(d2);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(odone);
-      const float inv = 1.0f / (__uint_as_float(dn[0]) + __uint_as_float(dn[1]) + eps);
+      const float inv = 1.0f / (den + eps);
       uint4* dstp = reinterpret_cast<uint4*>(out + b * osb + static_cast<int64_t>(n0 + row) * osn + h * osh +
                                              half * HC);
 #pragma unroll
