@@ -9,11 +9,13 @@
 //
 //   (forward summaries and mixing, recomputed by the forward's kernels)
 //   tc_bwd_query  per (b, query block i, head group), 128 tokens at a time:
-//                 MMA A   [num | den] = phi(Q) [S~ | z~hi z~lo]
-//                 epilogue dnum = g / den, dden = -(g . o) / den (CUDA cores)
-//                 MMA B   dphi(Q) = [dnum | dden] [S~^T ; z~hi z~lo]
+//                 MMA A   num = phi(Q) S~
+//                 epilogue den = phi(q) . z~ + eps, dnum = g / den,
+//                          dden = -(g . o) / den (CUDA cores)
+//                 MMA B   dnum S~^T
 //                 MMA C   [dS~ | dz~] += phi(Q)^T [dnum | dden], over the block
-//                 dq = dphi(Q) * [q > 0]; dS~, dz~ go to a buffer laid out like
+//                 dq = (dnum S~^T + dden z~) * [q > 0]; the next chunk's MMA A
+//                 runs under MMAs B and C; dS~, dz~ go to a buffer laid out like
 //                 the forward's summaries, so the forward's mixing GEMM with W^T
 //                 turns them into dS, dz
 //   tc_dw         dW[i][j] = sum over summary columns of dS~[i][col] S[j][col]:
@@ -50,6 +52,9 @@ using namespace tc;
 __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile uint32_t* abortf) {
   return wait_bounded_on(bar, parity, abortf, &g_bwd_error);
 }
+__device__ __forceinline__ bool bwarp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abortf) {
+  return warp_wait_on(bar, parity, abortf, &g_bwd_error);
+}
 __device__ __forceinline__ void bdrain(uint64_t* bar, uint32_t parity) { drain_wait_on(bar, parity, &g_bwd_error); }
 
 // 16-byte unit of a row in a 128-byte-swizzled tile (rows of 128 bytes).
@@ -57,36 +62,64 @@ __device__ __forceinline__ int swz128(int row) { return row & 7; }
 
 // ============================================================================
 // tc_bwd_query
+// Work item = (b, query block i, head group of 128 / d heads), head group
+// fastest; 128-token chunks.  Per chunk n:
+//   MMA A   num = phi(Q) S~                               (accumulator n % 2)
+//   epi 1   den = phi(q) . z~ + eps (CUDA cores), dnum = g / den written over
+//           g, dden = -(g . num) / den^2
+//   MMA B   dnum S~^T                                      (accumulator n % 2)
+//   MMA C   [dS~ | dz~] += phi(Q)^T [dnum | dden]          (one accumulator per item)
+//   epi 2   dq = (dnum S~^T + dden z~) * [q > 0] written over dnum, stored by TMA
+//   epi 3   after the item's last chunk: dS~, dz~ to a buffer laid out like the
+//           forward's summaries, so the forward's mixing GEMM with W^T turns
+//           them into dS, dz
+// Roles (24 warps): q and S~ producer, MMA issuer, dq store issuer, dout
+// producer, a phi warpgroup, two epilogue-1 and two epilogue-2 warpgroups
+// (each pair splits the heads of the item).  Every hand-off is an mbarrier, so the phases of neighbouring
+// chunks overlap: MMA A of chunk n + 1 runs under epilogue 1 of chunk n, and
+// epilogue 2 of chunk n under epilogue 1 of chunk n + 1.
 // ============================================================================
 template <int D>
 struct BqCfg {
-  static constexpr int HP = 128 / D;             // heads per work item
-  static constexpr int C = 128;                  // tokens per chunk (MMA M)
+  static constexpr int HP = 128 / D;              // heads per work item
+  static constexpr int C = 128;                   // tokens per chunk (MMA M)
   static constexpr int ROWB = D * 2;
-  static constexpr int TILE = C * ROWB;          // one head's [128][D] token tile
-  static constexpr int HT = HP * TILE;           // all heads of a chunk
+  static constexpr int TILE = C * ROWB;           // one head's [128][D] token tile
+  static constexpr int HT = HP * TILE;            // all heads of a chunk (32 KB)
   static constexpr uint32_t SBO = 8 * ROWB;
   static constexpr uint32_t LAYOUT = D == 64 ? 2u : 4u;
-  static constexpr int ST = D * D * 2;           // one S~ tile (row-major, swizzled like a token tile)
-  static constexpr int EXT = C * 128;            // [128][64] 128-byte-swizzled K-extension tile
-  static constexpr int ZB = D * 128;             // [D][64] K-extension of S~^T for MMA B
-  // shared memory
-  static constexpr int QT_OFF = 0;                       // phi(q), HP tiles
-  static constexpr int GT_OFF = QT_OFF + HT;             // dout, HP tiles
-  static constexpr int DN_OFF = GT_OFF + HT;             // dnum, HP tiles, then DDC; later dq
-  static constexpr int DDC_OFF = DN_OFF + HT;            // dden as N columns (MN-major, layout of D)
-  static constexpr int DDA_OFF = DDC_OFF + TILE;         // dden as K columns (K-major, 128-byte swizzle)
-  static constexpr int SZ_OFF = DDA_OFF + EXT;           // per head: S~ tile, then the z~ N atom
-  static constexpr int ZB_OFF = SZ_OFF + HP * 2 * ST;    // per head: z~ K-extension
-  static constexpr int ZRAW_OFF = ZB_OFF + HP * ZB;      // z~ float32, HP x D
-  static constexpr int MASK_OFF = ZRAW_OFF + HP * D * 4; // [HP][128][D/8] bits of q > 0
-  static constexpr int CTRL_OFF = MASK_OFF + HP * C * (D / 8);
-  static constexpr size_t SMEM = CTRL_OFF + 128 + 1024;
-  static constexpr int ASTR = D == 64 ? 128 : 64;        // TMEM columns per head of MMA A
-  static constexpr int CCOL = 256;                       // MMA C accumulator (128 + 16 columns)
-  static constexpr int TMEM_COLS = 512;
+  static constexpr int ST = D * D * 2;            // one S~ tile (row-major, swizzled like a token tile)
+  static constexpr int NQ = 2;                    // q stages
+  static constexpr int NG = 3;                    // dout stages: dout, then dnum, then dq
+  static constexpr int MASKB = HP * C * (D / 8);  // q > 0 bits of a chunk
+  static constexpr int DDB = 2 * C * 16;          // dden operand: 2 groups of 8 columns, unswizzled MN-major
+  static constexpr int Q_OFF = 0;
+  static constexpr int G_OFF = Q_OFF + NQ * HT;
+  static constexpr int SZ_OFF = G_OFF + NG * HT;             // [2] slots of HP S~ tiles
+  static constexpr int ZRAW_OFF = SZ_OFF + 2 * HP * ST;      // [2][HP][D] z~ float32
+  static constexpr int DDB_OFF = ZRAW_OFF + 2 * HP * D * 4;  // [NG] dden operands
+  static constexpr int DDS_OFF = DDB_OFF + NG * DDB;         // [NG][HP][C] dden float32
+  static constexpr int MASK_OFF = DDS_OFF + NG * HP * C * 4; // [NG] q > 0 bits
+  static constexpr int CTRL_OFF = MASK_OFF + NG * MASKB;
+  static constexpr size_t SMEM = CTRL_OFF + 512 + 1024;
+  static constexpr int CCOL = 256;                // [dS~ | dz~]: 128 + 16 columns
+  static constexpr int TMEM_COLS = 512;           // accumulators 0 and 1 at 0 and 128
 };
-constexpr int kBqThreads = 256;
+constexpr int kBqThreads = 768;
+
+// q > 0 bits of the eight bf16 values of a 16-byte unit (bit e for element e).
+// Per 16-bit half: adding 0x7FFF to the magnitude sets the half's top bit
+// exactly when the magnitude is non-zero (no carry reaches the next half); the
+// sign bit then clears it for negative values.
+__device__ __forceinline__ uint32_t positive_bits(uint4 q) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t p[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) p[k] = ((w[k] & 0x7FFF7FFFu) + 0x7FFF7FFFu) & ~w[k] & 0x80008000u;
+  // word k: low half to bit 2k, high half to bit 2k + 16, then folded to 2k + 1
+  const uint32_t c = (p[0] >> 15) | (p[1] >> 13) | (p[2] >> 11) | (p[3] >> 9);
+  return (c | (c >> 15)) & 0xFFu;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kBqThreads, 1)
@@ -95,33 +128,59 @@ tc_bwd_query(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
              int32_t G, int64_t n_items, int phi_kind, float eps, const float* __restrict__ zt,
              __nv_bfloat16* __restrict__ dSbuf) {
   using Cfg = BqCfg<D>;
-  constexpr int HP = Cfg::HP;
+  constexpr int HP = Cfg::HP, NQ = Cfg::NQ, NG = Cfg::NG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
-  uint8_t* qt = smem + Cfg::QT_OFF;
-  uint8_t* gt = smem + Cfg::GT_OFF;
-  uint8_t* dn = smem + Cfg::DN_OFF;
-  uint8_t* ddc = smem + Cfg::DDC_OFF;
-  uint8_t* dda = smem + Cfg::DDA_OFF;
+  uint8_t* qst = smem + Cfg::Q_OFF;
+  uint8_t* gst = smem + Cfg::G_OFF;
   uint8_t* sz = smem + Cfg::SZ_OFF;
-  uint8_t* zb = smem + Cfg::ZB_OFF;
   float* zraw = reinterpret_cast<float*>(smem + Cfg::ZRAW_OFF);
-  uint8_t* mask = smem + Cfg::MASK_OFF;
-  uint64_t* bq = reinterpret_cast<uint64_t*>(smem + Cfg::CTRL_OFF);   // q tiles landed
-  uint64_t* bg = bq + 1;                                               // dout tiles landed
-  uint64_t* bs = bq + 2;                                               // S~, z~ of an item landed
-  uint64_t* bm1 = bq + 3;                                              // MMA A complete
-  uint64_t* bm2 = bq + 4;                                              // MMA B and C complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bq + 5);
+  uint8_t* ddb = smem + Cfg::DDB_OFF;
+  float* dds = reinterpret_cast<float*>(smem + Cfg::DDS_OFF);
+  uint8_t* masks = smem + Cfg::MASK_OFF;
+  uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + Cfg::CTRL_OFF);
+  uint64_t* qempty = qfull + NQ;     // MMA C of the chunk done
+  uint64_t* phid = qempty + NQ;      // phi applied (128 arrivals)
+  uint64_t* gfull = phid + NQ;
+  uint64_t* gempty = gfull + NG;     // the dq store has read the stage
+  uint64_t* mfull = gempty + NG;     // q > 0 bits written (128)
+  uint64_t* mempty = mfull + NG;     // q > 0 bits read by epilogue 2 (256)
+  uint64_t* dqready = mempty + NG;   // dq written over the stage (256)
+  uint64_t* sfull = dqready + NG;    // [2] S~ tiles and z~ of an item landed
+  uint64_t* sempty = sfull + 2;      // [2] the item's last chunk is through epilogue 2 (256)
+  uint64_t* tfullA = sempty + 2;     // [2] MMA A done
+  uint64_t* e1done = tfullA + 2;     // [2] epilogue 1 done (256)
+  uint64_t* mmadone = e1done + 2;    // [2] MMAs B and C done
+  uint64_t* accfree = mmadone + 2;   // [2] epilogue 2 has read the accumulator (256)
+  uint64_t* cfree = accfree + 2;     // epilogue 3 has read [dS~ | dz~] (256)
+  uint64_t* fin = cfree + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
   volatile uint32_t* abortf = tmem_slot + 1;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    mbar_init(bq, 1);
-    mbar_init(bg, 1);
-    mbar_init(bs, 1);
-    mbar_init(bm1, 1);
-    mbar_init(bm2, 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NQ; ++s) {
+      mbar_init(qfull + s, 1);
+      mbar_init(qempty + s, 1);
+      mbar_init(phid + s, 128);
+    }
+    for (int s = 0; s < NG; ++s) {
+      mbar_init(gfull + s, 1);
+      mbar_init(gempty + s, 1);
+      mbar_init(mfull + s, 128);
+      mbar_init(mempty + s, 256);
+      mbar_init(dqready + s, 256);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sfull + s, 1);
+      mbar_init(sempty + s, 256);
+      mbar_init(tfullA + s, 1);
+      mbar_init(e1done + s, 256);
+      mbar_init(mmadone + s, 1);
+      mbar_init(accfree + s, 256);
+    }
+    mbar_init(cfree, 256);
+    mbar_init(fin, 1);
     *abortf = 0u;
     fence_mbar_init();
     prefetch_tmap(&tm_q);
@@ -129,25 +188,19 @@ tc_bwd_query(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     prefetch_tmap(&tm_dq);
     prefetch_tmap(&tm_st);
   }
-  if (warp == 0) {
+  if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
     tmem_relinquish();
   }
-  // The dden and z~ extension tiles: only their first columns are ever written.
-  for (int e = tid; e < (Cfg::TILE + Cfg::EXT) / 16; e += kBqThreads)
-    reinterpret_cast<uint4*>(ddc)[e] = make_uint4(0u, 0u, 0u, 0u);
-  for (int e = tid; e < HP * 2 * Cfg::ST / 16; e += kBqThreads)
-    reinterpret_cast<uint4*>(sz)[e] = make_uint4(0u, 0u, 0u, 0u);
-  for (int e = tid; e < HP * Cfg::ZB / 16; e += kBqThreads)
-    reinterpret_cast<uint4*>(zb)[e] = make_uint4(0u, 0u, 0u, 0u);
+  // the dden operands: only their first HP columns are ever written
+  for (int e = threadIdx.x; e < NG * Cfg::DDB / 16; e += kBqThreads)
+    reinterpret_cast<uint4*>(ddb)[e] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const uint64_t pol_stream = policy_evict_first();
-  const uint64_t pol_keep = policy_evict_last();
   // item -> (grp, i, b), head group fastest
   auto item_coords = [&](int64_t item, int32_t& grp, int32_t& i, int32_t& b) {
     grp = static_cast<int32_t>(item % G);
@@ -155,300 +208,391 @@ tc_bwd_query(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     i = static_cast<int32_t>(rest % g.M);
     b = static_cast<int32_t>(rest / g.M);
   };
-  auto issue_tiles = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int64_t item, int c) {
-    int32_t grp, i, b;
-    item_coords(item, grp, i, b);
-    int32_t x, y, z;
-    chunk_coords(g, i, c, b, x, y, z);
-    mbar_arrive_expect_tx(bar, Cfg::HT);
-#pragma unroll
-    for (int hh = 0; hh < HP; ++hh)   // heads >= H read zeros
-      tma_load_5d(dst + hh * Cfg::TILE, map, bar, 0, grp * HP + hh, x, y, z, pol_stream);
-  };
-  auto issue_sz = [&](int64_t item) {
-    int32_t grp, i, b;
-    item_coords(item, grp, i, b);
-    uint32_t bytes = 0;
-    for (int hh = 0; hh < HP; ++hh)
-      if (grp * HP + hh < g.H) bytes += Cfg::ST + D * 4;
-    mbar_arrive_expect_tx(bs, bytes);
-    for (int hh = 0; hh < HP; ++hh) {
-      const int32_t h = grp * HP + hh;
-      if (h >= g.H) continue;
-      const int64_t tile = (static_cast<int64_t>(b) * g.H + h) * g.M + i;
-      tma_load_2d(sz + hh * 2 * Cfg::ST, &tm_st, bs, 0, static_cast<int32_t>(tile * D), pol_keep);
-      bulk_load(zraw + hh * D, zt + tile * D, D * 4, bs, pol_keep);
-    }
-  };
 
-  // Issued (thread 0) and consumed (every thread) phase counts.
-  uint32_t n_q = 0, n_g = 0, n_s = 0, n_m1 = 0, n_m2 = 0;
-  uint32_t c_q = 0, c_g = 0, c_s = 0, c_m1 = 0, c_m2 = 0;
-  if (tid == 0 && static_cast<int64_t>(blockIdx.x) < n_items) {
-    issue_sz(blockIdx.x);
-    issue_tiles(&tm_q, qt, bq, blockIdx.x, 0);
-    issue_tiles(&tm_g, gt, bg, blockIdx.x, 0);
-    n_s = n_q = n_g = 1;
-  }
-  const bool add_eps = phi_kind == MHLA_PHI_RELU_EPS;
-  const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
-  const int row = 32 * (warp & 3) + lane;      // token row of the chunk = TMEM lane
-  const int wg = warp >> 2;
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-  bool ok = true;
-
-  for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-    int32_t grp, i, b;
-    item_coords(item, grp, i, b);
-    // ---- the item's S~ and z~: build the z~ operand pieces
-    if (!__syncthreads_and(bwait(bs, c_s & 1u, abortf))) break;
-    ++c_s;
-    if (tid < HP * D) {
-      const int hh = tid / D, r = tid % D;
-      const float zv = grp * HP + hh < g.H ? zraw[hh * D + r] : 0.0f;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
-      const uint32_t hilo = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
-                            (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
-      // MMA A, N atom after S~: row r (K), columns 0, 1 = hi, lo (unit 0 of the row)
-      *reinterpret_cast<uint32_t*>(sz + hh * 2 * Cfg::ST + Cfg::ST + r * Cfg::ROWB + swz<D>(r) * 16) = hilo;
-      // MMA B, K extension: row r (N), K columns hh = hi, HP + hh = lo
-      uint8_t* zrow = zb + hh * Cfg::ZB + r * 128 + swz128(r) * 16;
-      *reinterpret_cast<__nv_bfloat16*>(zrow + hh * 2) = hi;
-      *reinterpret_cast<__nv_bfloat16*>(zrow + (HP + hh) * 2) = lo;
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    for (int c = 0; c < g.chunks; ++c) {
-      const bool last = c + 1 == g.chunks;
-      const int64_t nitem = last ? item + gridDim.x : item;
-      const int nc = last ? 0 : c + 1;
-      const bool has_next = nitem < n_items;
-      // ---- phi in place on the q tiles, and the q > 0 bits
-      if (!__syncthreads_and(bwait(bq, c_q & 1u, abortf))) { ok = false; break; }
-      ++c_q;
-      for (int e = tid; e < Cfg::HT / 16; e += kBqThreads) {
-        const int hh = e / (Cfg::TILE / 16), rem = e % (Cfg::TILE / 16);
-        const int t = rem / (D / 8), p = rem % (D / 8);
-        uint4* ptr = reinterpret_cast<uint4*>(qt) + e;
-        const uint4 raw = *ptr;
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t bits = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
-          bits |= (__low2float(v2) > 0.0f ? 1u : 0u) << (2 * k);
-          bits |= (__high2float(v2) > 0.0f ? 1u : 0u) << (2 * k + 1);
-        }
-        mask[(hh * Cfg::C + t) * (D / 8) + (p ^ swz<D>(t))] = static_cast<uint8_t>(bits);
-        *ptr = phi8_packed(raw, add_eps, eps2);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-
-      // ---- MMA A: [num | den] = phi(q) [S~ | z~]
-      if (tid == 0) {
-        bulk_wait_group_read<0>();   // the previous chunk's dq stores have read the dn tiles
-        tc_fence_after();
-        constexpr uint32_t idesc = idesc_bf16_f32(128, D + 16, /*a K-major*/ false, /*b MN-major*/ true);
-#pragma unroll
-        for (int hh = 0; hh < HP; ++hh) {
-          const uint32_t qa = smem_u32(qt + hh * Cfg::TILE), sb = smem_u32(sz + hh * 2 * Cfg::ST);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + hh * Cfg::ASTR, smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
-                     smem_desc(sb + ks * 2 * Cfg::SBO, Cfg::ST, Cfg::SBO, Cfg::LAYOUT), idesc, ks > 0 ? 1u : 0u);
-        }
-        mma_commit(bm1);
-        ++n_m1;
-      }
-      if (!__syncthreads_and(bwait(bm1, c_m1 & 1u, abortf))) { ok = false; break; }
-      ++c_m1;
-      if (!__syncthreads_and(bwait(bg, c_g & 1u, abortf))) { ok = false; break; }
-      ++c_g;
-      tc_fence_after();
-
-      // ---- epilogue 1: dnum = g / den, dden = -(g . o) / den
-      for (int hh = wg; hh < HP; hh += 2) {
-        const uint32_t tb = lane_base + hh * Cfg::ASTR;
-        uint32_t nv[D];
-        uint32_t dv2[2];
-        if constexpr (D == 64) {
-          tmem_ld_x32(tb, *reinterpret_cast<uint32_t(*)[32]>(nv));
-          tmem_ld_x32(tb + 32, *reinterpret_cast<uint32_t(*)[32]>(nv + 32));
-        } else {
-          tmem_ld_x32(tb, *reinterpret_cast<uint32_t(*)[32]>(nv));
-        }
-        tmem_ld_x1(tb + D, dv2[0]);
-        tmem_ld_x1(tb + D + 1, dv2[1]);
-        tmem_ld_wait();
-        const float den = __uint_as_float(dv2[0]) + __uint_as_float(dv2[1]) + eps;
-        // heads past H (zero inputs) contribute exact zeros, whatever eps is
-        const float inv = grp * HP + hh < g.H ? 1.0f / den : 0.0f;
-        const uint8_t* grow = gt + hh * Cfg::TILE + row * Cfg::ROWB;
-        float go = 0.0f;
-#pragma unroll
-        for (int u = 0; u < D / 8; ++u) {
-          const uint4 gr = *reinterpret_cast<const uint4*>(grow + ((u ^ swz<D>(row)) * 16));
-          const uint32_t gw[4] = {gr.x, gr.y, gr.z, gr.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(&gw[k]);
-            go = fmaf(__low2float(g2), __uint_as_float(nv[8 * u + 2 * k]), go);
-            go = fmaf(__high2float(g2), __uint_as_float(nv[8 * u + 2 * k + 1]), go);
-          }
-        }
-        const float dden = -go * inv * inv;   // -(g . num / den) / den
-        uint8_t* drow = dn + hh * Cfg::TILE + row * Cfg::ROWB;
-#pragma unroll
-        for (int u = 0; u < D / 8; ++u) {
-          const uint4 gr = *reinterpret_cast<const uint4*>(grow + ((u ^ swz<D>(row)) * 16));
-          const uint32_t gw[4] = {gr.x, gr.y, gr.z, gr.w};
-          uint32_t ow[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(&gw[k]);
-            ow[k] = pack_bf16(__low2float(g2) * inv, __high2float(g2) * inv);
-          }
-          *reinterpret_cast<uint4*>(drow + ((u ^ swz<D>(row)) * 16)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-        }
-        const __nv_bfloat16 ddb = __float2bfloat16_rn(dden);
-        // MMA C's B: N column hh of the dden atom (row = token, unit 0 of the row)
-        *reinterpret_cast<__nv_bfloat16*>(ddc + row * Cfg::ROWB + swz<D>(row) * 16 + hh * 2) = ddb;
-        // MMA B's A: K columns hh and HP + hh (they meet z~ hi and lo)
-        uint8_t* arow = dda + row * 128 + swz128(row) * 16;
-        *reinterpret_cast<__nv_bfloat16*>(arow + hh * 2) = ddb;
-        *reinterpret_cast<__nv_bfloat16*>(arow + (HP + hh) * 2) = ddb;
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-
-      // ---- MMA B (dphi(q)) and MMA C (dS~, dz~); the dout tiles are free
-      if (tid == 0) {
-        if (has_next) {
-          issue_tiles(&tm_g, gt, bg, nitem, nc);
-          ++n_g;
-        }
-        tc_fence_after();
-        constexpr uint32_t idb = idesc_bf16_f32(128, D, /*a K-major*/ false, /*b K-major*/ false);
-#pragma unroll
-        for (int hh = 0; hh < HP; ++hh) {
-          const uint32_t da = smem_u32(dn + hh * Cfg::TILE), sb = smem_u32(sz + hh * 2 * Cfg::ST);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + hh * D, smem_desc(da + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
-                     smem_desc(sb + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT), idb, ks > 0 ? 1u : 0u);
-          mma_bf16(tmem + hh * D, smem_desc(smem_u32(dda), 16, 1024, 2),
-                   smem_desc(smem_u32(zb + hh * Cfg::ZB), 16, 1024, 2), idb, 1u);
-        }
-        constexpr uint32_t idc = idesc_bf16_f32(128, 128 + 16, /*a MN-major*/ true, /*b MN-major*/ true);
-        const uint32_t qa = smem_u32(qt), da = smem_u32(dn);
-#pragma unroll
-        for (int ks = 0; ks < Cfg::C / 16; ++ks)
-          mma_bf16(tmem + Cfg::CCOL, smem_desc(qa + ks * 2 * Cfg::SBO, Cfg::TILE, Cfg::SBO, Cfg::LAYOUT),
-                   smem_desc(da + ks * 2 * Cfg::SBO, Cfg::TILE, Cfg::SBO, Cfg::LAYOUT), idc,
-                   (c > 0 || ks > 0) ? 1u : 0u);
-        mma_commit(bm2);
-        ++n_m2;
-      }
-      if (!__syncthreads_and(bwait(bm2, c_m2 & 1u, abortf))) { ok = false; break; }
-      ++c_m2;
-      tc_fence_after();
-      if (tid == 0 && has_next) {   // phi(q), S~ and z~ are consumed
-        if (last) {
-          issue_sz(nitem);
-          ++n_s;
-        }
-        issue_tiles(&tm_q, qt, bq, nitem, nc);
-        ++n_q;
-      }
-
-      // ---- epilogue 2: dq = dphi(q) * [q > 0] into the dn tiles, then stored
-      for (int hh = wg; hh < HP; hh += 2) {
-        uint32_t v[D];
-        if constexpr (D == 64) {
-          tmem_ld_x32(lane_base + hh * D, *reinterpret_cast<uint32_t(*)[32]>(v));
-          tmem_ld_x32(lane_base + hh * D + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        } else {
-          tmem_ld_x32(lane_base + hh * D, *reinterpret_cast<uint32_t(*)[32]>(v));
-        }
-        tmem_ld_wait();
-        const uint8_t* mrow = mask + (hh * Cfg::C + row) * (D / 8);
-        uint8_t* orow = dn + hh * Cfg::TILE + row * Cfg::ROWB;
-#pragma unroll
-        for (int u = 0; u < D / 8; ++u) {
-          const uint32_t bits = mrow[u];
-          uint32_t ow[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float a0 = (bits >> (2 * k)) & 1u ? __uint_as_float(v[8 * u + 2 * k]) : 0.0f;
-            const float a1 = (bits >> (2 * k + 1)) & 1u ? __uint_as_float(v[8 * u + 2 * k + 1]) : 0.0f;
-            ow[k] = pack_bf16(a0, a1);
-          }
-          *reinterpret_cast<uint4*>(orow + ((u ^ swz<D>(row)) * 16)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) {
-        int32_t x, y, z;
-        chunk_coords(g, i, c, b, x, y, z);
+  if (warp == 0) {
+    // ------------------------------------------- q and S~ producer
+    if (lane == 0) {
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_s = policy_evict_last();
+      uint32_t qfills[NQ] = {}, sfills[2] = {};
+      int qs = 0;
+      uint32_t qph = 0, k = 0;
+      bool ok = true;
+      for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
+        int32_t grp, i, b;
+        item_coords(item, grp, i, b);
+        const int sl = static_cast<int>(k & 1u);
+        if (!bwait(sempty + sl, ((k >> 1) & 1u) ^ 1u, abortf)) break;
+        uint32_t bytes = 0;
         for (int hh = 0; hh < HP; ++hh)
-          if (grp * HP + hh < g.H) tma_store_5d(&tm_dq, dn + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z);
-        bulk_commit_group();
-      }
-
-      // ---- epilogue 3 (after the block's last chunk): dS~ and dz~ to dSbuf
-      if (last) {
-        // thread: TMEM lane row = (hh, r); warpgroup wg takes half of the d columns
-        const int hh = row / D, r = row % D;
-        const uint32_t tb = lane_base + Cfg::CCOL + hh * D + wg * (D / 2);
-        uint32_t v[D / 2];
-        if constexpr (D == 64) {
-          tmem_ld_x32(tb, *reinterpret_cast<uint32_t(*)[32]>(v));
-        } else {
-          tmem_ld_x16(tb, *reinterpret_cast<uint32_t(*)[16]>(v));
+          if (grp * HP + hh < g.H) bytes += Cfg::ST + D * 4;
+        mbar_arrive_expect_tx(sfull + sl, bytes);
+        for (int hh = 0; hh < HP; ++hh) {
+          const int32_t h = grp * HP + hh;
+          if (h >= g.H) continue;
+          const int64_t tile = (static_cast<int64_t>(b) * g.H + h) * g.M + i;
+          tma_load_2d(sz + (sl * HP + hh) * Cfg::ST, &tm_st, sfull + sl, 0, static_cast<int32_t>(tile * D), pol_s);
+          bulk_load(zraw + (sl * HP + hh) * D, zt + tile * D, D * 4, sfull + sl, pol_s);
         }
-        uint32_t vz = 0;
-        tmem_ld_x1(lane_base + Cfg::CCOL + 128 + hh, vz);
-        tmem_ld_wait();
-        const int32_t h = grp * HP + hh;
-        if (h < g.H) {
-          constexpr int32_t PER_BH = (D + 1) * D;
-          const int64_t col = (static_cast<int64_t>(b) * g.H + h) * PER_BH + r * D + wg * (D / 2);
-          uint4* drow = reinterpret_cast<uint4*>(dSbuf + ((col >> 7) * g.M + i) * 128 + (col & 127));
+        ++sfills[sl];
+        for (int c = 0; c < g.chunks; ++c) {
+          if (!bwait(qempty + qs, qph ^ 1u, abortf)) { ok = false; break; }
+          int32_t x, y, z;
+          chunk_coords(g, i, c, b, x, y, z);
+          mbar_arrive_expect_tx(qfull + qs, Cfg::HT);
 #pragma unroll
-          for (int q = 0; q < D / 16; ++q)
-            drow[q] = make_uint4(pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                                 pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                                 pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                                 pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
-          if (wg == 0) {
-            const int64_t zcol = (static_cast<int64_t>(b) * g.H + h) * PER_BH + D * D + r;
-            dSbuf[((zcol >> 7) * g.M + i) * 128 + (zcol & 127)] = __float2bfloat16_rn(__uint_as_float(vz));
+          for (int hh = 0; hh < HP; ++hh)   // heads >= H read zeros
+            tma_load_5d(qst + qs * Cfg::HT + hh * Cfg::TILE, &tm_q, qfull + qs, 0, grp * HP + hh, x, y, z, pol_q);
+          ++qfills[qs];
+          if (++qs == NQ) { qs = 0; qph ^= 1u; }
+        }
+      }
+      for (int s = 0; s < NQ; ++s)
+        if (qfills[s]) bdrain(qfull + s, (qfills[s] - 1) & 1u);
+      for (int s = 0; s < 2; ++s)
+        if (sfills[s]) bdrain(sfull + s, (sfills[s] - 1) & 1u);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------- dout producer
+    if (lane == 0) {
+      const uint64_t pol_g = policy_evict_first();
+      uint32_t gfills[NG] = {};
+      int gs = 0;
+      uint32_t gph = 0;
+      bool ok = true;
+      for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        int32_t grp, i, b;
+        item_coords(item, grp, i, b);
+        for (int c = 0; c < g.chunks; ++c) {
+          if (!bwait(gempty + gs, gph ^ 1u, abortf)) { ok = false; break; }
+          int32_t x, y, z;
+          chunk_coords(g, i, c, b, x, y, z);
+          mbar_arrive_expect_tx(gfull + gs, Cfg::HT);
+#pragma unroll
+          for (int hh = 0; hh < HP; ++hh)
+            tma_load_5d(gst + gs * Cfg::HT + hh * Cfg::TILE, &tm_g, gfull + gs, 0, grp * HP + hh, x, y, z, pol_g);
+          ++gfills[gs];
+          if (++gs == NG) { gs = 0; gph ^= 1u; }
+        }
+      }
+      for (int s = 0; s < NG; ++s)
+        if (gfills[s]) bdrain(gfull + s, (gfills[s] - 1) & 1u);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------- dq store issuer
+    if (lane == 0) {
+      int gs = 0;
+      uint32_t gph = 0;
+      bool ok = true;
+      for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        int32_t grp, i, b;
+        item_coords(item, grp, i, b);
+        for (int c = 0; c < g.chunks; ++c) {
+          if (!bwait(dqready + gs, gph, abortf)) { ok = false; break; }
+          int32_t x, y, z;
+          chunk_coords(g, i, c, b, x, y, z);
+          for (int hh = 0; hh < HP; ++hh)
+            if (grp * HP + hh < g.H)
+              tma_store_5d(&tm_dq, gst + gs * Cfg::HT + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z);
+          bulk_commit_group();
+          bulk_wait_group_read<0>();      // the stage has been read: back to the dout producer
+          mbar_arrive(gempty + gs);
+          if (++gs == NG) { gs = 0; gph ^= 1u; }
+        }
+      }
+      bulk_wait_group0();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------- MMA issuer
+    // Two streams in chunk order, issued as their inputs become ready: MMA A
+    // of chunk nA (q stage phi'd, S~ landed, accumulator nA % 2 read out by
+    // epilogue 2 of chunk nA - 2) and MMAs B, C of chunk nB < nA (epilogue 1
+    // done; for an item's first chunk also [dS~ | dz~] read out).
+    if (lane == 0) {
+      constexpr uint32_t idA = idesc_bf16_f32(128, D, /*a K-major*/ false, /*b MN-major*/ true);
+      constexpr uint32_t idB = idesc_bf16_f32(128, D, /*a K-major*/ false, /*b K-major*/ false);
+      constexpr uint32_t idC = idesc_bf16_f32(128, 128, /*a MN-major*/ true, /*b MN-major*/ true);
+      constexpr uint32_t idZ = idesc_bf16_f32(128, 16, /*a MN-major*/ true, /*b MN-major*/ true);
+      int64_t itemA = blockIdx.x, itemB = blockIdx.x;
+      int cA = 0, cB = 0;
+      uint32_t nA = 0, nB = 0, kA = 0, kB = 0;
+      uint64_t t0 = globaltimer();
+      uint32_t idle = 0;
+      while (itemB < n_items) {
+        bool prog = false;
+        if (itemA < n_items && nA < nB + 2) {
+          const uint32_t s = nA % NQ, acc = nA & 1u, sl = kA & 1u;
+          if ((cA != 0 || mbar_test_wait(sfull + sl, (kA >> 1) & 1u)) &&
+              mbar_test_wait(phid + s, (nA / NQ) & 1u) && mbar_test_wait(accfree + acc, ((nA >> 1) & 1u) ^ 1u)) {
+            tc_fence_after();
+#pragma unroll
+            for (int hh = 0; hh < HP; ++hh) {
+              const uint32_t qa = smem_u32(qst + s * Cfg::HT + hh * Cfg::TILE);
+              const uint32_t sb = smem_u32(sz + (sl * HP + hh) * Cfg::ST);
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + acc * 128 + hh * D, smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
+                         smem_desc(sb + ks * 2 * Cfg::SBO, Cfg::ST, Cfg::SBO, Cfg::LAYOUT), idA, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(tfullA + acc);
+            ++nA;
+            if (++cA == g.chunks) { cA = 0; itemA += gridDim.x; ++kA; }
+            prog = true;
           }
         }
-        tc_fence_before();
-        __syncthreads();
+        if (nB < nA) {
+          const uint32_t acc = nB & 1u, sl = kB & 1u, s = nB % NQ, gs = nB % NG;
+          if (mbar_test_wait(e1done + acc, (nB >> 1) & 1u) && (cB != 0 || mbar_test_wait(cfree, (kB & 1u) ^ 1u))) {
+            tc_fence_after();
+#pragma unroll
+            for (int hh = 0; hh < HP; ++hh) {
+              const uint32_t da = smem_u32(gst + gs * Cfg::HT + hh * Cfg::TILE);
+              const uint32_t sb = smem_u32(sz + (sl * HP + hh) * Cfg::ST);
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + acc * 128 + hh * D, smem_desc(da + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
+                         smem_desc(sb + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT), idB, ks > 0 ? 1u : 0u);
+            }
+            const uint32_t qa = smem_u32(qst + s * Cfg::HT), da = smem_u32(gst + gs * Cfg::HT);
+            const uint32_t zb = smem_u32(ddb + gs * Cfg::DDB);
+#pragma unroll
+            for (int ks = 0; ks < Cfg::C / 16; ++ks) {
+              const uint64_t adesc = smem_desc(qa + ks * 2 * Cfg::SBO, Cfg::TILE, Cfg::SBO, Cfg::LAYOUT);
+              const uint32_t accum = (cB > 0 || ks > 0) ? 1u : 0u;
+              mma_bf16(tmem + Cfg::CCOL, adesc, smem_desc(da + ks * 2 * Cfg::SBO, Cfg::TILE, Cfg::SBO, Cfg::LAYOUT),
+                       idC, accum);
+              mma_bf16(tmem + Cfg::CCOL + 128, adesc, smem_desc(zb + ks * 256, 128, Cfg::C * 16, 0), idZ, accum);
+            }
+            mma_commit(mmadone + acc);
+            mma_commit(qempty + s);
+            ++nB;
+            if (++cB == g.chunks) { cB = 0; itemB += gridDim.x; ++kB; }
+            prog = true;
+          }
+        }
+        if (prog) {
+          idle = 0;
+          t0 = globaltimer();
+        } else if ((++idle & 63u) == 0) {
+          if (*abortf) break;
+          if (globaltimer() - t0 > kWaitLimitNs || idle >= kWaitLimitPolls) {
+            *abortf = 1u;
+            atomicOr(&g_bwd_error, 1u);
+            break;
+          }
+        }
+      }
+      mma_commit(fin);
+      bdrain(fin, 0);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------- phi on q, and the q > 0 bits
+    const int t4 = threadIdx.x - 128;
+    const bool add_eps = phi_kind == MHLA_PHI_RELU_EPS;
+    const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
+    int qs = 0, gs = 0;
+    uint32_t qph = 0, gph = 0;
+    bool ok = true;
+    for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      for (int c = 0; c < g.chunks; ++c) {
+        if (!bwarp_wait(qfull + qs, qph, abortf) || !bwarp_wait(mempty + gs, gph ^ 1u, abortf)) { ok = false; break; }
+        uint8_t* qs_base = qst + qs * Cfg::HT;
+        uint8_t* mk = masks + gs * Cfg::MASKB;
+#pragma unroll 4
+        for (int e = t4; e < Cfg::HT / 16; e += 128) {
+          const int hh = e / (Cfg::TILE / 16), rem = e % (Cfg::TILE / 16);
+          const int t = rem / (D / 8), p = rem % (D / 8);
+          uint4* ptr = reinterpret_cast<uint4*>(qs_base) + e;
+          const uint4 raw = *ptr;
+          mk[(hh * Cfg::C + t) * (D / 8) + (p ^ swz<D>(t))] = static_cast<uint8_t>(positive_bits(raw));
+          *ptr = phi8_packed(raw, add_eps, eps2);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(phid + qs);
+        mbar_arrive(mfull + gs);
+        if (++qs == NQ) { qs = 0; qph ^= 1u; }
+        if (++gs == NG) { gs = 0; gph ^= 1u; }
       }
     }
-  }
-
-  if (tid == 0) {
-    bulk_wait_group0();
-    if (n_q > c_q) bdrain(bq, (n_q - 1) & 1u);
-    if (n_g > c_g) bdrain(bg, (n_g - 1) & 1u);
-    if (n_s > c_s) bdrain(bs, (n_s - 1) & 1u);
-    if (n_m1 > c_m1) bdrain(bm1, (n_m1 - 1) & 1u);
-    if (n_m2 > c_m2) bdrain(bm2, (n_m2 - 1) & 1u);
+  } else {
+    const int q4 = warp & 3;
+    const int ew = (warp >> 2) & 1;                 // warpgroup of the pair: heads ew, ew + 2, ...
+    const int row = 32 * q4 + lane;                 // token row of the chunk = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+    int qs = 0, gs = 0;
+    uint32_t qph = 0, gph = 0, n = 0, k = 0;
+    bool ok = true;
+    if (warp < 16) {
+      // ----------------------------------------- epilogue 1: den, dnum, dden
+      for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
+        const int32_t grp = static_cast<int32_t>(item % G);
+        const int sl = static_cast<int>(k & 1u);
+        for (int c = 0; c < g.chunks; ++c, ++n) {
+          const uint32_t acc = n & 1u;
+          if (!bwarp_wait(tfullA + acc, (n >> 1) & 1u, abortf) || !bwarp_wait(gfull + gs, gph, abortf) ||
+              !bwarp_wait(phid + qs, qph, abortf) || !bwarp_wait(sfull + sl, (k >> 1) & 1u, abortf)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int hh = ew; hh < HP; hh += 2) {
+            uint32_t nv[32];
+            tmem_ld_x32(lane_base + acc * 128 + hh * D, nv);
+            // den = phi(q_t) . z~ + eps on the CUDA cores, from this row of the q tile
+            const uint8_t* qrow = qst + qs * Cfg::HT + hh * Cfg::TILE + row * Cfg::ROWB;
+            const float* zr = zraw + (sl * HP + hh) * D;
+            float dpart[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int u = 0; u < D / 8; ++u) {
+              const uint4 qv = *reinterpret_cast<const uint4*>(qrow + ((u ^ swz<D>(row)) * 16));
+              const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+              const float4 za = *reinterpret_cast<const float4*>(zr + 8 * u);
+              const float4 zb = *reinterpret_cast<const float4*>(zr + 8 * u + 4);
+              const float zz[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 q2 = *reinterpret_cast<const __nv_bfloat162*>(&qw[e]);
+                dpart[e] = fmaf(__low2float(q2), zz[2 * e], dpart[e]);
+                dpart[e] = fmaf(__high2float(q2), zz[2 * e + 1], dpart[e]);
+              }
+            }
+            const bool valid = grp * HP + hh < g.H;
+            // heads past H (zero inputs, no S~ loaded) give exact zeros
+            const float inv = valid ? 1.0f / ((dpart[0] + dpart[1]) + (dpart[2] + dpart[3]) + eps) : 0.0f;
+            uint8_t* grow = gst + gs * Cfg::HT + hh * Cfg::TILE + row * Cfg::ROWB;
+            float gpart[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int h2 = 0; h2 < D / 32; ++h2) {
+              if (h2 > 0) tmem_ld_x32(lane_base + acc * 128 + hh * D + 32 * h2, nv);
+              tmem_ld_wait();
+#pragma unroll
+              for (int u4 = 0; u4 < 4; ++u4) {
+                const int u = 4 * h2 + u4;
+                uint4* gp = reinterpret_cast<uint4*>(grow + ((u ^ swz<D>(row)) * 16));
+                const uint4 gr = *gp;
+                const uint32_t gw[4] = {gr.x, gr.y, gr.z, gr.w};
+                uint32_t ow[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(&gw[e]);
+                  const float g0 = __low2float(g2), g1 = __high2float(g2);
+                  gpart[e] = fmaf(g0, __uint_as_float(nv[8 * u4 + 2 * e]), gpart[e]);
+                  gpart[e] = fmaf(g1, __uint_as_float(nv[8 * u4 + 2 * e + 1]), gpart[e]);
+                  ow[e] = pack_bf16(g0 * inv, g1 * inv);
+                }
+                *gp = make_uint4(ow[0], ow[1], ow[2], ow[3]);   // dnum over g (this row is this thread's)
+              }
+            }
+            const float go = (gpart[0] + gpart[1]) + (gpart[2] + gpart[3]);
+            const float dden = valid ? -go * inv * inv : 0.0f;   // -(g . num / den) / den
+            dds[(gs * HP + hh) * Cfg::C + row] = dden;
+            // column hh of the dden operand (token row, unswizzled MN-major)
+            *reinterpret_cast<__nv_bfloat16*>(ddb + gs * Cfg::DDB + row * 16 + hh * 2) = __float2bfloat16_rn(dden);
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(e1done + acc);
+          if (++qs == NQ) { qs = 0; qph ^= 1u; }
+          if (++gs == NG) { gs = 0; gph ^= 1u; }
+        }
+      }
+    } else {
+      // ----------------------------------------- epilogue 2: dq; epilogue 3: dS~, dz~
+      for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
+        int32_t grp, i, b;
+        item_coords(item, grp, i, b);
+        const int sl = static_cast<int>(k & 1u);
+        for (int c = 0; c < g.chunks; ++c, ++n) {
+          const uint32_t acc = n & 1u, aph = (n >> 1) & 1u;
+          if (!bwarp_wait(mmadone + acc, aph, abortf) || !bwarp_wait(e1done + acc, aph, abortf) ||
+              !bwarp_wait(mfull + gs, gph, abortf) || !bwarp_wait(sfull + sl, (k >> 1) & 1u, abortf)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int hh = ew; hh < HP; hh += 2) {
+            uint32_t v[32];
+            tmem_ld_x32(lane_base + acc * 128 + hh * D, v);
+            const float* zr = zraw + (sl * HP + hh) * D;
+            const float ddv = dds[(gs * HP + hh) * Cfg::C + row];
+            const uint8_t* mrow = masks + gs * Cfg::MASKB + (hh * Cfg::C + row) * (D / 8);
+            uint64_t mbits;
+            if constexpr (D == 64) {
+              mbits = *reinterpret_cast<const uint64_t*>(mrow);
+            } else {
+              mbits = *reinterpret_cast<const uint32_t*>(mrow);
+            }
+            uint8_t* orow = gst + gs * Cfg::HT + hh * Cfg::TILE + row * Cfg::ROWB;
+#pragma unroll
+            for (int h2 = 0; h2 < D / 32; ++h2) {
+              if (h2 > 0) tmem_ld_x32(lane_base + acc * 128 + hh * D + 32 * h2, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int u4 = 0; u4 < 4; ++u4) {
+                const int u = 4 * h2 + u4;
+                const uint32_t bits = static_cast<uint32_t>(mbits >> (8 * u)) & 0xFFu;
+                const float4 za = *reinterpret_cast<const float4*>(zr + 8 * u);
+                const float4 zb = *reinterpret_cast<const float4*>(zr + 8 * u + 4);
+                const float zz[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
+                uint32_t ow[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int c0 = 8 * u4 + 2 * e;
+                  const float a0 = (bits >> (2 * e)) & 1u ? fmaf(ddv, zz[2 * e], __uint_as_float(v[c0])) : 0.0f;
+                  const float a1 = (bits >> (2 * e + 1)) & 1u ? fmaf(ddv, zz[2 * e + 1], __uint_as_float(v[c0 + 1])) : 0.0f;
+                  ow[e] = pack_bf16(a0, a1);
+                }
+                *reinterpret_cast<uint4*>(orow + ((u ^ swz<D>(row)) * 16)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(accfree + acc);
+          fence_proxy_async_smem();
+          mbar_arrive(dqready + gs);
+          mbar_arrive(mempty + gs);
+          if (c + 1 == g.chunks) {
+            // ---- epilogue 3: row = (head hh, channel r) of phi(Q)^T
+            const int hh = row / D, r = row % D;
+            const int32_t h = grp * HP + hh;
+            constexpr int32_t PER_BH = (D + 1) * D;
+            const int64_t col = (static_cast<int64_t>(b) * g.H + h) * PER_BH + r * D + ew * (D / 2);
+            uint4* drow = reinterpret_cast<uint4*>(dSbuf + ((col >> 7) * g.M + i) * 128 + (col & 127));
+            uint32_t vz = 0;
+            tmem_ld_x1(lane_base + Cfg::CCOL + 128 + hh, vz);
+            uint32_t v[D / 2];
+            if constexpr (D == 64) {
+              tmem_ld_x32(lane_base + Cfg::CCOL + hh * D + ew * 32, v);
+            } else {
+              tmem_ld_x16(lane_base + Cfg::CCOL + hh * D + ew * 16, v);
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(cfree);
+            if (h < g.H) {
+#pragma unroll
+              for (int q = 0; q < D / 16; ++q)
+                drow[q] = make_uint4(pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                                     pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                     pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                     pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+            }
+            if (h < g.H && ew == 0) {
+              const int64_t zcol = (static_cast<int64_t>(b) * g.H + h) * PER_BH + D * D + r;
+              dSbuf[((zcol >> 7) * g.M + i) * 128 + (zcol & 127)] = __float2bfloat16_rn(__uint_as_float(vz));
+            }
+            mbar_arrive(sempty + sl);
+          }
+          if (++gs == NG) { gs = 0; gph ^= 1u; }
+        }
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::TMEM_COLS);
   }
