@@ -2,12 +2,14 @@
 """Throughput of the MHLA forward pass on GB300 (tokens/s and HBM roofline).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-                  [--pass forward|backward|causal]
+                  [--pass forward|backward|causal|module]
 
 One step = one MHLA forward (summaries, mixing GEMM, outputs) over
 one synthetic batch of the workload, inputs resident in HBM; with
 ``--pass backward`` one step is one backward pass (dq, dk, dv, dW for a seeded
-dout); with ``--pass causal`` one causal (chunkwise) MHLA forward.  Rank 0 prints one
+dout); with ``--pass causal`` one causal (chunkwise) MHLA forward; with ``--pass
+module`` one forward of the whole module around the core (LayerNorm, qkv
+projection, MHLA, 5 x 5 positional term, output projection) on x [B, N, H * d].  Rank 0 prints one
 JSON line.  With N > 1 (torchrun) every rank runs an independent batch on its own
 GPU (replicas, weak scaling); ranks meet only for the timing barrier and the
 max-over-ranks reduction.  ``--impl reference`` times the float64 CPU oracle on
@@ -36,7 +38,9 @@ from token_level_head_block_gb300.workloads import HEADLINE, WORKLOADS  # noqa: 
 METRIC = "MHLA forward tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
 METRIC_BWD = "MHLA backward (dq, dk, dv, dW) tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
 METRIC_CAUSAL = "causal MHLA forward tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
-METRICS = {"forward": METRIC, "backward": METRIC_BWD, "causal": METRIC_CAUSAL}
+METRIC_MODULE = ("MHLA module forward (LayerNorm, qkv projection, MHLA, 5x5 positional term, output projection) "
+                 "tokens/sec at 1 GB300")
+METRICS = {"forward": METRIC, "backward": METRIC_BWD, "causal": METRIC_CAUSAL, "module": METRIC_MODULE}
 UNIT = "tokens/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -205,6 +209,10 @@ def kernel_work(wl, name):
         "tc_dw": ("tensor", 2 * M * M * BH * d * (d + 1)), "simt_dw": ("alu", 2 * M * M * BH * d * (d + 1)),
         # causal: read q, k, v, write o
         "simt_causal_output": ("hbm", 4 * io), "tc_causal_tile": ("hbm", 4 * io),
+        # module: x -> LayerNorm; qkv = xn W^T; o += lepe(v) (read v, o; write o); y = o W^T
+        "mhla_ln_rows": ("hbm", 2 * io), "mhla_lepe_add": ("hbm", 3 * io),
+        "cublaslt_qkv": ("tensor", 2 * wl.tokens * (wl.H * d) * 3 * (wl.H * d)),
+        "cublaslt_out": ("tensor", 2 * wl.tokens * (wl.H * d) * (wl.H * d)),
     }
     return table.get(name, ("hbm", 0))
 
@@ -258,6 +266,32 @@ def oracle_sample_rate(wl, q, k, v, W, budget_s, max_slices=None, g=None, causal
     return done * wl.N / wl.H / el, done, el
 
 
+def module_inputs(wl, seed):
+    """Seeded x [B, N, H * d] and module parameters for the module pass."""
+    from token_level_head_block_gb300.synth import draw_module_params, draw_tokens
+    C = wl.H * wl.d
+    return draw_tokens(wl.B, wl.N, C, seed), draw_module_params(C, seed + 1)
+
+
+def oracle_module_rate(wl, x, params, W, budget_s, max_items=None):
+    """Times the module oracle on whole batch elements (the projections mix the
+    heads, so a batch element is the smallest unit) until budget_s elapses.
+    Returns (tokens/s, batch elements, seconds)."""
+    import oracle
+    from token_level_head_block_gb300.synth import as_f64
+    phi = oracle.PHI_RELU if wl.phi == "relu" else oracle.PHI_RELU_EPS
+    p64 = {k: as_f64(t) for k, t in params.items()}
+    done, t0 = 0, time.perf_counter()
+    while True:
+        b = done % wl.B
+        oracle.module_forward(as_f64(x[b:b + 1]), p64, W, wl.grid, wl.block, wl.H, phi, wl.eps)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_items and done >= max_items):
+            break
+    return done * wl.N / el, done, el
+
+
 def draw_dout(wl, seed=None):
     """Seeded dL/d(out) for the backward pass, N(0, 1) in the workload's dtype."""
     from token_level_head_block_gb300.synth import draw_qkv
@@ -273,10 +307,31 @@ def run_reference(args, wl):
     import numpy as np  # noqa: F401
     import oracle
     from token_level_head_block_gb300.synth import draw_workload
+    W = oracle.mixing_matrix(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
+    if args.pass_ == "module":
+        x, params = module_inputs(wl, wl.seed + 300)
+        for _ in range(args.warmup):
+            oracle_module_rate(wl, x, params, W, 0.0, max_items=1)
+        times = []
+        for _ in range(args.steps):
+            times.append(oracle_module_rate(wl, x, params, W, 1e9, max_items=1)[2])
+        total = sum(times)
+        value = args.steps * wl.N / total
+        sample = f"each step: one of the {wl.B} batch elements of {wl.name}, float64 numpy module oracle"
+        print(json.dumps({
+            "impl": "reference", "metric": METRICS[args.pass_], "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {**wl.describe(), "pass": "module",
+                                            "parallelism": "host cores (BLAS threads)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
     q, k, v = draw_workload(wl)
     g = draw_dout(wl) if args.pass_ == "backward" else None
     causal = args.pass_ == "causal"
-    W = oracle.mixing_matrix(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
     per_step = max(1, args.ref_slices)
     for _ in range(args.warmup):
         oracle_sample_rate(wl, q, k, v, W, 0.0, max_slices=1, g=g, causal=causal)
@@ -314,6 +369,7 @@ def run_ours(args, wl):
     mhla.lib()
 
     bwd = args.pass_ == "backward"
+    module = args.pass_ == "module"
     q_h, k_h, v_h = draw_workload(wl, seed=wl.seed + rank)      # each replica its own batch
     g_h = draw_dout(wl, seed=wl.seed + 100 + rank) if bwd else None
     W_h = mhla.init_mixing(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
@@ -321,7 +377,18 @@ def run_ours(args, wl):
     W = torch.from_numpy(W_h).to(dev)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
-    if args.pass_ == "causal":
+    if module:
+        x_h, params_h = module_inputs(wl, wl.seed + 300 + rank)
+        x = x_h.to(dev)
+        params = {name: t.to(dev) for name, t in params_h.items()}
+        y = torch.empty_like(x)
+        ws = torch.empty(mhla.module_workspace_size(wl.B, wl.N, wl.H * wl.d, wl.H, wl.grid, wl.block),
+                         dtype=torch.uint8, device=dev)
+
+        def step():
+            mhla.module_forward(x, params, W, wl.grid, wl.block, wl.H, phi=wl.phi, eps=wl.eps, out=y, workspace=ws,
+                                stream=stream)
+    elif args.pass_ == "causal":
         ws = torch.empty(mhla.causal_workspace_size(q, wl.grid, wl.block), dtype=torch.uint8, device=dev)
 
         def step():
@@ -385,7 +452,14 @@ def run_ours(args, wl):
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (t.pin_memory() for t in (q_h, k_h, v_h))
-        if bwd:
+        if module:
+            hx, hy = x_h.pin_memory(), torch.empty_like(x_h).pin_memory()
+
+            def e2e_step():
+                x.copy_(hx, non_blocking=True)
+                step()
+                hy.copy_(y, non_blocking=True)
+        elif bwd:
             hg = g_h.pin_memory()
             hdq, hdk, hdv = (torch.empty_like(q_h).pin_memory() for _ in range(3))
             hdW = torch.empty(dW.shape, dtype=dW.dtype).pin_memory()
@@ -412,7 +486,7 @@ def run_ours(args, wl):
         el_e2e = max_over_ranks(timed(n_e2e, e2e_step), dev)
         io = wl.B * wl.N * wl.H * wl.d * wl.elem_bytes
         e2e = {"value": whole_job_throughput(wl.tokens, world, n_e2e, el_e2e), "unit": UNIT,
-               "h2d_bytes_per_step": (4 if bwd else 3) * io,
+               "h2d_bytes_per_step": io if module else (4 if bwd else 3) * io,
                "d2h_bytes_per_step": 3 * io + wl.M * wl.M * 4 if bwd else io, "steps": n_e2e,
                "ms_per_step": 1e3 * el_e2e / n_e2e}
 
@@ -439,9 +513,22 @@ def run_ours(args, wl):
     fwd_gbs = pass_bytes / (max_el / args.steps) / 1e9
     forward_roofline = {"bound": "hbm", "achieved": fwd_gbs, "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
                         "frac": fwd_gbs / float(peaks["hbm_gbs"]), "bytes_per_step": pass_bytes}
+    if module:
+        # the two projections carry the step's flops: 8 tokens C^2
+        C = wl.H * wl.d
+        flops = 8 * wl.tokens * C * C
+        tf = flops / (max_el / args.steps) / 1e12
+        tpeak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        forward_roofline = {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s", "frac": tf / tpeak,
+                            "flops_per_step": flops, "note": "projection flops over the whole step"}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and module:
+        rate, n, el = oracle_module_rate(wl, x_h, params_h, W_h.astype("float64"), args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{n} of the {wl.B} batch elements of {wl.name} in {el:.1f} s, float64 numpy module "
+                         "oracle"}
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, n, el = oracle_sample_rate(wl, q_h, k_h, v_h, W_h, args.cpu_seconds, g=g_h,
                                          causal=args.pass_ == "causal")
         what = {"forward": "oracle (blocked form)", "backward": "backward oracle",
@@ -460,6 +547,7 @@ def run_ours(args, wl):
             "data": "synthetic",
             "config": {**wl.describe(), "pass": args.pass_,
                        "path": ("tc" if "tc_bwd_query" in prof else "simt") if bwd else
+                               ("module (core: " + path + ")") if module else
                                (("tc" if "tc_causal_tile" in prof else "simt") if args.pass_ == "causal" else path),
                        "global_batch": wl.B * world, "seq_len": wl.N,
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
@@ -484,7 +572,7 @@ def main():
     ap.add_argument("--sustain", type=float, default=2.0, help="seconds of load before timing (clock samples)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU oracle baseline")
     ap.add_argument("--ref-slices", type=int, default=1, help="(batch, head) slices per reference step")
-    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "causal"], default="forward")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "causal", "module"], default="forward")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

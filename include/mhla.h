@@ -280,6 +280,80 @@ mhla_status_t mhla_forward_noalloc(const mhla_tensor_t* q, const mhla_tensor_t* 
                                    const mhla_phi_t* phi, const mhla_tensor_t* out,
                                    void* stream, int32_t path);
 
+/* ---------------------------------------------------------------------------
+ * The module around the core ([P1] section 7, class MHLA: norm, to_qkv, lepe,
+ * to_out and forward), for a [B, N, C] bf16 token array x with C = heads * d:
+ *
+ *   xn      = LayerNorm(x)                        (mhla_layer_norm)
+ *   q, k, v = split(xn W_qkv^T + b_qkv, 3)        (a GEMM; q, k, v are read in
+ *             place as [B, N, heads, d] views of its [B, N, 3C] result)
+ *   o       = MHLA(q, k, v)                       (mhla_forward, path AUTO)
+ *   o      += lepe(v)                             (mhla_lepe_add)
+ *   y       = o W_out^T + b_out                   (a GEMM)
+ *
+ * The two projections go to cuBLASLt (loaded at run time); without it the
+ * module call returns MHLA_ERR_UNSUPPORTED.  Dropout is the identity
+ * (inference); q_norm / k_norm are identities (the listing's default).
+ * ------------------------------------------------------------------------ */
+
+/* LayerNorm over the last axis of a row-major [rows, C] bf16 device array:
+ * y = (x - mean) / sqrt(var + eps) * weight + bias with the biased variance and
+ * float32 statistics, rounded to bf16 ([P1] section 7, MHLA.norm, an
+ * nn.LayerNorm(dim)).  C % 8 == 0 and C <= 2048; x, y, weight and bias (float32
+ * [C]) 16-byte aligned device memory; y may equal x, other overlaps are
+ * invalid.  Asynchronous on stream. */
+mhla_status_t mhla_layer_norm(const void* x, void* y, int64_t rows, int64_t C, const float* weight,
+                              const float* bias, float eps, void* stream);
+
+/* out += lepe(v): the locally-enhanced positional term of [P1] section 7
+ * (MHLA.lepe, a depthwise nn.Conv2d with 5 x 5 kernels and padding 2, and
+ * "out = out + lepe" in MHLA.forward):
+ *   out[b, (y, x), c] += bias[c] + sum_{i, j < 5} weight[c][i][j] * v[b, (y + i - 2, x + j - 2), c]
+ * with zero outside the frame, over the (Y, X) axes of the grid (each frame of
+ * a 3-D grid on its own).  Channel c is h * d + j of a [B, N, H, d] view.
+ *   v, out   bf16 device views of the same shape; d % 8 == 0, every stride a
+ *            multiple of 8 elements, 16-byte aligned bases; out must not
+ *            overlap v.
+ *   weight   device float32 [H * d][5][5];  bias  device float32 [H * d].
+ * Rounds o + (bias + conv) once to bf16.  Asynchronous on stream. */
+mhla_status_t mhla_lepe_add(const mhla_tensor_t* v, const mhla_tensor_t* out, const mhla_shape3_t* grid,
+                            const float* weight, const float* bias, void* stream);
+
+/* Parameters of the module; every pointer is device memory the caller owns. */
+typedef struct mhla_module_params {
+    const float* ln_weight;    /* [C] float32 */
+    const float* ln_bias;      /* [C] float32 */
+    const void* qkv_weight;    /* [3C][C] bf16, nn.Linear layout [out][in]; rows q, then k, then v,
+                                  each (head, d) with the head slower */
+    const void* qkv_bias;      /* [3C] bf16 or NULL */
+    const float* lepe_weight;  /* [C][5][5] float32, or NULL for no positional term */
+    const float* lepe_bias;    /* [C] float32; required with lepe_weight */
+    const void* out_weight;    /* [C][C] bf16, [out][in] */
+    const void* out_bias;      /* [C] bf16 or NULL */
+    float ln_eps;              /* LayerNorm eps (1e-5 in the listing) */
+    int32_t heads;             /* C = heads * d */
+} mhla_module_params_t;
+
+/* Device workspace mhla_module_forward needs (bytes): the normalised input and
+ * the core's output (one buffer), the [B, N, 3C] projection, the core's own
+ * workspace and 32 MiB for cuBLASLt.  Host only. */
+mhla_status_t mhla_module_workspace_size(int64_t B, int64_t N, int64_t C, int32_t heads,
+                                         const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                                         size_t* bytes);
+
+/* The module forward on x [B, N, C] (bf16, row-major, 16-byte aligned; tokens in
+ * raster order over grid) into y of the same layout (y may equal x).  W, grid,
+ * block and phi are those of mhla_forward (the listing uses
+ * MHLA_PHI_RELU_EPS).  C % 8 == 0, C <= 2048, d = C / heads with d % 8 == 0.
+ * workspace as for mhla_forward (NULL with workspace_bytes == 0: stream-ordered
+ * allocation).  Asynchronous on stream; returns MHLA_ERR_UNSUPPORTED when
+ * cuBLASLt cannot be loaded or has no algorithm for the shapes. */
+mhla_status_t mhla_module_forward(const void* x, void* y, int64_t B, int64_t N, int64_t C,
+                                  const mhla_module_params_t* params, const float* W,
+                                  const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                                  const mhla_phi_t* phi, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
 /* Reads and clears the device error words the tensor-core and fused kernels
  * set when one of their bounded waits gives up (bit 0: pipeline wait timeout;
  * bit 1: a copy or MMA still in flight when the kernel gave up did not finish

@@ -1,0 +1,135 @@
+"""GPU parity of the module around the core (LayerNorm, 5 x 5 positional term,
+the whole module with its projections) against the float64 module oracle.
+
+bf16 storage between the steps bounds the agreement: every stored value is
+rounded once to bf16 (relative 2^-9), so element checks take 2^-7 of the value
+plus a small absolute floor, and the module output is held to the 2e-2
+normwise bound of bf16 inputs with float32 accumulation.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import token_level_head_block_gb300 as mhla
+from token_level_head_block_gb300.synth import as_f64, draw_module_params, draw_tokens
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+def _bf16_close(got, ref, rel=2.0 ** -7, abs_=1e-3):
+    err = np.abs(got - ref)
+    bad = err > rel * np.abs(ref) + abs_
+    assert not bad.any(), f"{bad.sum()} of {bad.size} elements off, worst {err.max():.3g}"
+
+
+def _normwise(got, ref):
+    return float(np.linalg.norm((got - ref).ravel()) / np.linalg.norm(ref.ravel()))
+
+
+@pytest.mark.parametrize("rows,C", [(1, 64), (37, 384), (1000, 256), (129, 1024), (64, 2048), (5, 520)])
+def test_layer_norm(rows, C):
+    x = draw_tokens(1, rows, C, seed=11 + C)[0]
+    rng = np.random.default_rng(C)
+    w = torch.from_numpy((1 + 0.1 * rng.standard_normal(C)).astype(np.float32))
+    b = torch.from_numpy((0.1 * rng.standard_normal(C)).astype(np.float32))
+    y = mhla.layer_norm(x.to(DEV), w.to(DEV), b.to(DEV), eps=1e-5)
+    torch.cuda.synchronize()
+    ref = oracle.layer_norm(as_f64(x), as_f64(w), as_f64(b), 1e-5)
+    _bf16_close(as_f64(y.cpu()), ref, abs_=2e-3)
+
+
+def test_layer_norm_in_place_and_constant_rows():
+    C = 128
+    x = draw_tokens(1, 16, C, seed=3)[0]
+    x[3] = 2.5                              # a constant row normalises to the bias
+    w, b = torch.ones(C), torch.full((C,), 0.25)
+    xd = x.to(DEV)
+    mhla.layer_norm(xd, w.to(DEV), b.to(DEV), out=xd)
+    torch.cuda.synchronize()
+    ref = oracle.layer_norm(as_f64(x), as_f64(w), as_f64(b))
+    got = as_f64(xd.cpu())
+    _bf16_close(got, ref, abs_=2e-3)
+    assert np.all(got[3] == 0.25)
+
+
+LEPE_CASES = [
+    # (B, grid, H, d)
+    (2, (13, 21), 2, 32),         # ragged tiles on both axes, C = 64
+    (1, (64, 64), 6, 64),         # DiT-like channels, C = 384
+    (1, (8, 40), 3, 32),          # C = 96: a partial 64-channel chunk
+    (2, (3, 9, 17), 2, 64),       # 3-D grid: every frame on its own
+    (1, (1, 5), 1, 8),            # a single row narrower than the kernel
+]
+
+
+@pytest.mark.parametrize("B,grid,H,d", LEPE_CASES)
+def test_lepe_add_strided_v(B, grid, H, d):
+    N = int(np.prod(grid))
+    C = H * d
+    rng = np.random.default_rng(N + C)
+    # v as the third C-slice of a [B, N, 3C] projection (the module's layout)
+    qkv = draw_tokens(B, N, 3 * C, seed=17)
+    v_full = qkv.to(DEV)
+    v = v_full[:, :, 2 * C:].view(B, N, H, d)
+    o = draw_tokens(B, N, C, seed=19)
+    o_dev = o.to(DEV).view(B, N, H, d).contiguous()
+    w = torch.from_numpy((0.2 * rng.standard_normal((C, 5, 5))).astype(np.float32))
+    bias = torch.from_numpy((0.1 * rng.standard_normal(C)).astype(np.float32))
+    mhla.lepe_add(v, o_dev, grid, w.to(DEV), bias.to(DEV))
+    torch.cuda.synchronize()
+    v_ref = as_f64(qkv)[:, :, 2 * C:]
+    ref = as_f64(o) + oracle.lepe(v_ref, grid, as_f64(w), as_f64(bias))
+    _bf16_close(as_f64(o_dev.cpu()).reshape(B, N, C), ref, abs_=2e-3)
+
+
+MODULE_CASES = [
+    # (name, B, grid, block, heads, d, lepe, biases, transform)
+    ("tiny_simt_core", 2, (16, 16), (4, 4), 2, 32, True, True, "linear"),
+    ("dit_like_tc_core", 1, (64, 64), (16, 16), 6, 64, True, True, "exp"),
+    ("video_like_3d", 1, (4, 16, 16), (2, 8, 8), 2, 64, True, False, "linear"),
+    ("no_lepe_no_bias", 2, (32, 32), (8, 8), 4, 32, False, False, "cos"),
+]
+
+
+@pytest.mark.parametrize("name,B,grid,block,heads,d,lepe,biases,transform", MODULE_CASES,
+                         ids=[c[0] for c in MODULE_CASES])
+def test_module_forward(name, B, grid, block, heads, d, lepe, biases, transform):
+    N, C = int(np.prod(grid)), heads * d
+    x = draw_tokens(B, N, C, seed=101)
+    p = draw_module_params(C, seed=202, lepe=lepe, biases=biases)
+    W = mhla.init_mixing(grid, block, transform)
+    pd = {k: t.to(DEV) for k, t in p.items()}
+    y = mhla.module_forward(x.to(DEV), pd, torch.from_numpy(W).to(DEV), grid, block, heads, phi="relu_eps",
+                            eps=1e-6)
+    torch.cuda.synchronize()
+    assert mhla.device_status() == 0
+    ref = oracle.module_forward(as_f64(x), {k: as_f64(t) for k, t in p.items()}, W.astype(np.float64), grid,
+                                block, heads, oracle.PHI_RELU_EPS, 1e-6)
+    err = _normwise(as_f64(y.cpu()), ref)
+    assert err < 2e-2, err
+
+
+def test_module_with_workspace_and_in_place():
+    B, grid, block, heads, d = 1, (32, 32), (16, 16), 2, 64
+    N, C = 1024, 128
+    x = draw_tokens(B, N, C, seed=5)
+    p = {k: t.to(DEV) for k, t in draw_module_params(C, seed=6).items()}
+    W = torch.from_numpy(mhla.init_mixing(grid, block)).to(DEV)
+    ws = torch.empty(mhla.module_workspace_size(B, N, C, heads, grid, block), dtype=torch.uint8, device=DEV)
+    a = mhla.module_forward(x.to(DEV), p, W, grid, block, heads, workspace=ws)
+    xd = x.to(DEV)
+    mhla.module_forward(xd, p, W, grid, block, heads, out=xd, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a, xd)
+
+
+def test_module_rejects_bad_shapes():
+    x = torch.zeros(1, 64, 60, dtype=torch.bfloat16, device=DEV)     # C % 8 != 0
+    p = {k: t.to(DEV) for k, t in draw_module_params(64, seed=1).items()}
+    W = torch.ones(1, 1, device=DEV)
+    with pytest.raises(mhla.MhlaError):
+        mhla.module_forward(x, p, W, (8, 8), (8, 8), 2)

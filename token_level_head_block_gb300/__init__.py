@@ -16,7 +16,8 @@ import numpy as np
 __all__ = [
     "MhlaError", "lib", "library_path", "num_blocks", "init_mixing", "workspace_size",
     "select_path", "forward", "forward_causal", "causal_workspace_size", "backward", "backward_workspace_size",
-    "device_status", "profile_begin",
+    "device_status", "profile_begin", "layer_norm", "lepe_add", "module_forward",
+    "module_workspace_size",
     "profile_end", "tensor_desc", "shape3",
     "PATHS", "TRANSFORMS",
 ]
@@ -58,6 +59,17 @@ class Tensor(ctypes.Structure):
         ("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("pad_", ctypes.c_int32),
         ("B", ctypes.c_int64), ("N", ctypes.c_int64), ("H", ctypes.c_int64), ("d", ctypes.c_int64),
         ("stride_b", ctypes.c_int64), ("stride_n", ctypes.c_int64), ("stride_h", ctypes.c_int64),
+    ]
+
+
+class ModuleParams(ctypes.Structure):
+    """mhla_module_params_t: device pointers of the module's parameters."""
+    _fields_ = [
+        ("ln_weight", ctypes.c_void_p), ("ln_bias", ctypes.c_void_p),
+        ("qkv_weight", ctypes.c_void_p), ("qkv_bias", ctypes.c_void_p),
+        ("lepe_weight", ctypes.c_void_p), ("lepe_bias", ctypes.c_void_p),
+        ("out_weight", ctypes.c_void_p), ("out_bias", ctypes.c_void_p),
+        ("ln_eps", ctypes.c_float), ("heads", ctypes.c_int32),
     ]
 
 
@@ -103,6 +115,18 @@ def lib():
                                 P(Tensor), P(Tensor), P(Tensor), P(Tensor), ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int32]
     L.mhla_backward.restype = ctypes.c_int
+    L.mhla_layer_norm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                  ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p]
+    L.mhla_layer_norm.restype = ctypes.c_int
+    L.mhla_lepe_add.argtypes = [P(Tensor), P(Tensor), P(Shape3), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    L.mhla_lepe_add.restype = ctypes.c_int
+    L.mhla_module_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                             P(Shape3), P(Shape3), P(ctypes.c_size_t)]
+    L.mhla_module_workspace_size.restype = ctypes.c_int
+    L.mhla_module_forward.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                      ctypes.c_int64, P(ModuleParams), ctypes.c_void_p, P(Shape3), P(Shape3),
+                                      P(Phi), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    L.mhla_module_forward.restype = ctypes.c_int
     L.mhla_device_status.argtypes = [ctypes.c_void_p, P(ctypes.c_uint32)]
     L.mhla_device_status.restype = ctypes.c_int
     L.mhla_status_string.argtypes = [ctypes.c_int32]
@@ -288,6 +312,73 @@ def backward(q, k, v, W, dout, grid, block, phi="relu", eps=1e-6, dq=None, dk=No
                              ctypes.c_void_p(sptr) if sptr else None, PATHS[path])
     _check(st, "mhla_backward")
     return dq, dk, dv, dW
+
+
+def _stream_ptr(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    sptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return ctypes.c_void_p(sptr) if sptr else None
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def layer_norm(x, weight, bias, eps=1e-5, out=None, stream=None):
+    """LayerNorm over the last axis of a contiguous bf16 CUDA tensor (float32
+    weight and bias of that size); returns ``out`` (may be ``x``)."""
+    import torch
+    out = torch.empty_like(x) if out is None else out
+    C = x.shape[-1]
+    st = lib().mhla_layer_norm(_ptr(x), _ptr(out), x.numel() // C, C, _ptr(weight), _ptr(bias), float(eps),
+                               _stream_ptr(stream, x.device))
+    _check(st, "mhla_layer_norm")
+    return out
+
+
+def lepe_add(v, out, grid, weight, bias, stream=None):
+    """out += 5 x 5 depthwise convolution of v (+ bias) over the token image, for
+    bf16 [B, N, H, d] CUDA views; weight float32 [H * d, 5, 5], bias [H * d]."""
+    st = lib().mhla_lepe_add(ctypes.byref(_desc(v)), ctypes.byref(_desc(out)), ctypes.byref(shape3(grid)),
+                             _ptr(weight), _ptr(bias), _stream_ptr(stream, v.device))
+    _check(st, "mhla_lepe_add")
+    return out
+
+
+def module_workspace_size(B, N, C, heads, grid, block):
+    n = ctypes.c_size_t(0)
+    _check(lib().mhla_module_workspace_size(B, N, C, heads, ctypes.byref(shape3(grid)), ctypes.byref(shape3(block)),
+                                            ctypes.byref(n)), "mhla_module_workspace_size")
+    return int(n.value)
+
+
+def module_forward(x, params, W, grid, block, heads, phi="relu_eps", eps=1e-6, ln_eps=1e-5, out=None,
+                   workspace=None, stream=None):
+    """The MHLA module (LayerNorm, qkv projection, MHLA, 5 x 5 positional term,
+    output projection) on a contiguous bf16 CUDA tensor x [B, N, C].
+
+    ``params``: CUDA tensors ln_weight, ln_bias (float32 [C]); qkv_weight (bf16
+    [3C, C]) and optional qkv_bias (bf16 [3C]); optional lepe_weight (float32
+    [C, 5, 5]) with lepe_bias (float32 [C]); out_weight (bf16 [C, C]) and
+    optional out_bias (bf16 [C]).  Returns ``out`` ([B, N, C], bf16).
+    """
+    import torch
+    B, N, C = x.shape
+    out = torch.empty_like(x) if out is None else out
+    p = ModuleParams(_ptr(params["ln_weight"]), _ptr(params["ln_bias"]), _ptr(params["qkv_weight"]),
+                     _ptr(params.get("qkv_bias")), _ptr(params.get("lepe_weight")), _ptr(params.get("lepe_bias")),
+                     _ptr(params["out_weight"]), _ptr(params.get("out_bias")), float(ln_eps), int(heads))
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() *
+                                                            workspace.element_size())
+    st = lib().mhla_module_forward(_ptr(x), _ptr(out), B, N, C, ctypes.byref(p), _ptr(W),
+                                   ctypes.byref(shape3(grid)), ctypes.byref(shape3(block)),
+                                   ctypes.byref(Phi(PHIS[phi], float(eps))),
+                                   ctypes.c_void_p(ws_ptr) if ws_ptr else None, ws_bytes,
+                                   _stream_ptr(stream, x.device))
+    _check(st, "mhla_module_forward")
+    return out
 
 
 def profile_begin():

@@ -415,3 +415,221 @@ extern "C" const char* mhla_status_string(int32_t status) {
 }
 
 extern "C" const char* mhla_version(void) { return "mhla-gb300 0.1.0 sm_103a"; }
+
+// ----------------------------------------------------------------- module
+
+namespace mhla {
+namespace {
+
+bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+int check_grid_tokens(const mhla_shape3_t* grid, int64_t N, int64_t* T, int64_t* Y, int64_t* X) {
+  if (!grid || (grid->ndim != 2 && grid->ndim != 3)) return MHLA_ERR_INVALID_ARG;
+  int64_t n = 1;
+  for (int a = 0; a < grid->ndim; ++a) {
+    if (grid->extent[a] < 1) return MHLA_ERR_SHAPE;
+    n *= grid->extent[a];
+  }
+  if (n != N) return MHLA_ERR_SHAPE;
+  *T = grid->ndim == 3 ? grid->extent[0] : 1;
+  *Y = grid->extent[grid->ndim - 2];
+  *X = grid->extent[grid->ndim - 1];
+  return MHLA_OK;
+}
+
+bool lepe_view_ok(const mhla_tensor_t* t) {
+  return t->dtype == MHLA_BF16 && t->d % 8 == 0 && t->stride_b % 8 == 0 && t->stride_n % 8 == 0 &&
+         t->stride_h % 8 == 0 && aligned16(t->data);
+}
+
+int lepe_args(const mhla_tensor_t* v, const mhla_tensor_t* out, const mhla_shape3_t* grid, const float* weight,
+              const float* bias, LepeArgs* a) {
+  for (const mhla_tensor_t* t : {v, out}) {
+    const int rc = check_tensor(t);
+    if (rc != MHLA_OK) return rc;
+  }
+  if (!same_shape(v, out)) return MHLA_ERR_SHAPE;
+  int64_t T, Y, X;
+  const int rg = check_grid_tokens(grid, v->N, &T, &Y, &X);
+  if (rg != MHLA_OK) return rg;
+  if (!lepe_view_ok(v) || !lepe_view_ok(out)) return MHLA_ERR_UNSUPPORTED;
+  if (v->B > 0 && v->H > 0) {
+    if (!weight || !bias) return MHLA_ERR_INVALID_ARG;
+    if (!non_overlapping(out)) return MHLA_ERR_INVALID_ARG;
+    uintptr_t o0, o1, v0, v1;
+    span(out, &o0, &o1);
+    span(v, &v0, &v1);
+    if (overlaps(o0, o1, v0, v1)) return MHLA_ERR_INVALID_ARG;
+  }
+  if (v->H * v->d > (int64_t{1} << 30) || T * Y * X > (int64_t{1} << 40) || v->B * T * ((v->H * v->d + 63) / 64) >= 65536 ||
+      (X + 15) / 16 >= (int64_t{1} << 31) || (Y + 7) / 8 >= 65536)
+    return MHLA_ERR_UNSUPPORTED;
+  a->v = v->data;
+  a->o = out->data;
+  a->vsb = v->stride_b; a->vsn = v->stride_n; a->vsh = v->stride_h;
+  a->osb = out->stride_b; a->osn = out->stride_n; a->osh = out->stride_h;
+  a->B = v->B;
+  a->d = static_cast<int32_t>(v->d);
+  a->C = static_cast<int32_t>(v->H * v->d);
+  a->T = static_cast<int32_t>(T); a->Y = static_cast<int32_t>(Y); a->X = static_cast<int32_t>(X);
+  a->weight = weight;
+  a->bias = bias;
+  return MHLA_OK;
+}
+
+// Buffers of the module inside its workspace.
+struct ModuleLayout {
+  size_t a_off, qkv_off, core_off, lt_off, total;
+};
+
+// The core's [B, N, heads, d] views of the projection and of the output buffer.
+void module_views(void* qkv, void* obuf, int64_t B, int64_t N, int64_t C, int32_t heads, mhla_tensor_t* q,
+                  mhla_tensor_t* k, mhla_tensor_t* v, mhla_tensor_t* o) {
+  const int64_t d = C / heads;
+  auto* base = static_cast<uint16_t*>(qkv);
+  mhla_tensor_t* views[3] = {q, k, v};
+  for (int s = 0; s < 3; ++s) {
+    mhla_tensor_t& t = *views[s];
+    t.data = qkv ? base + s * C : nullptr;
+    t.dtype = MHLA_BF16;
+    t.pad_ = 0;
+    t.B = B; t.N = N; t.H = heads; t.d = d;
+    t.stride_b = N * 3 * C; t.stride_n = 3 * C; t.stride_h = d;
+  }
+  o->data = obuf;
+  o->dtype = MHLA_BF16;
+  o->pad_ = 0;
+  o->B = B; o->N = N; o->H = heads; o->d = d;
+  o->stride_b = N * C; o->stride_n = C; o->stride_h = d;
+}
+
+int module_check(int64_t B, int64_t N, int64_t C, int32_t heads, const mhla_shape3_t* grid,
+                 const mhla_shape3_t* block) {
+  if (B < 0 || N < 1 || C < 8 || heads < 1 || C % heads != 0) return MHLA_ERR_INVALID_ARG;
+  if (C % 8 != 0 || C > 2048 || (C / heads) % 8 != 0 || C / heads > 128) return MHLA_ERR_UNSUPPORTED;
+  if (!grid || !block) return MHLA_ERR_INVALID_ARG;
+  int64_t T, Y, X;
+  const int rg = check_grid_tokens(grid, N, &T, &Y, &X);
+  if (rg != MHLA_OK) return rg;
+  const int64_t M = mhla_num_blocks(grid, block);
+  if (M < 0) return static_cast<int>(-M);
+  if (B * N >= (int64_t{1} << 40)) return MHLA_ERR_UNSUPPORTED;
+  return MHLA_OK;
+}
+
+int module_layout(int64_t B, int64_t N, int64_t C, int32_t heads, const mhla_shape3_t* grid,
+                  const mhla_shape3_t* block, ModuleLayout* L) {
+  const int64_t R = B * N;
+  mhla_tensor_t q, k, v, o;
+  // a 256-byte aligned stand-in address: the core's path choice depends on alignment, not on the value
+  module_views(reinterpret_cast<void*>(uintptr_t{1} << 20), reinterpret_cast<void*>(uintptr_t{1} << 21), B, N, C,
+               heads, &q, &k, &v, &o);
+  size_t core = 0;
+  const mhla_status_t rc = mhla_workspace_size(&q, grid, block, MHLA_PATH_AUTO, &core);
+  if (rc != MHLA_OK) return rc;
+  size_t off = 0;
+  L->a_off = off;
+  off += align_up(static_cast<size_t>(R) * C * 2);
+  L->qkv_off = off;
+  off += align_up(static_cast<size_t>(R) * 3 * C * 2);
+  L->core_off = off;
+  off += align_up(core);
+  L->lt_off = off;
+  off += align_up(linear_workspace_bytes());
+  L->total = off;
+  return MHLA_OK;
+}
+
+}  // namespace
+}  // namespace mhla
+
+extern "C" mhla_status_t mhla_layer_norm(const void* x, void* y, int64_t rows, int64_t C, const float* weight,
+                                         const float* bias, float eps, void* stream) {
+  if (rows < 0 || C < 8) return MHLA_ERR_INVALID_ARG;
+  if (C % 8 != 0 || C > 2048) return MHLA_ERR_UNSUPPORTED;
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return MHLA_ERR_INVALID_ARG;
+  if (rows == 0) return MHLA_OK;
+  if (!x || !y || !weight || !bias) return MHLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(weight) || !aligned16(bias)) return MHLA_ERR_INVALID_ARG;
+  const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), y0 = reinterpret_cast<uintptr_t>(y);
+  const uintptr_t n = static_cast<uintptr_t>(rows * C * 2);
+  if (x0 != y0 && overlaps(x0, x0 + n, y0, y0 + n)) return MHLA_ERR_INVALID_ARG;
+  if ((rows + 7) / 8 >= (int64_t{1} << 31)) return MHLA_ERR_UNSUPPORTED;
+  return static_cast<mhla_status_t>(
+      launch_layer_norm(x, y, rows, static_cast<int32_t>(C), weight, bias, eps, stream));
+}
+
+extern "C" mhla_status_t mhla_lepe_add(const mhla_tensor_t* v, const mhla_tensor_t* out, const mhla_shape3_t* grid,
+                                       const float* weight, const float* bias, void* stream) {
+  LepeArgs a;
+  const int rc = lepe_args(v, out, grid, weight, bias, &a);
+  if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+  if (v->B == 0 || v->H == 0) return MHLA_OK;
+  return static_cast<mhla_status_t>(launch_lepe_add(a, stream));
+}
+
+extern "C" mhla_status_t mhla_module_workspace_size(int64_t B, int64_t N, int64_t C, int32_t heads,
+                                                    const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                                                    size_t* bytes) {
+  if (!bytes) return MHLA_ERR_INVALID_ARG;
+  const int rc = module_check(B, N, C, heads, grid, block);
+  if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+  if (B == 0) { *bytes = 0; return MHLA_OK; }
+  ModuleLayout L;
+  const int rl = module_layout(B, N, C, heads, grid, block, &L);
+  if (rl != MHLA_OK) return static_cast<mhla_status_t>(rl);
+  *bytes = L.total;
+  return MHLA_OK;
+}
+
+extern "C" mhla_status_t mhla_module_forward(const void* x, void* y, int64_t B, int64_t N, int64_t C,
+                                             const mhla_module_params_t* params, const float* W,
+                                             const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                                             const mhla_phi_t* phi, void* workspace, size_t workspace_bytes,
+                                             void* stream) {
+  if (!params || !phi) return MHLA_ERR_INVALID_ARG;
+  const int rc = module_check(B, N, C, params->heads, grid, block);
+  if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+  if (B == 0) return MHLA_OK;
+  if (!x || !y || !W || !params->ln_weight || !params->ln_bias || !params->qkv_weight || !params->out_weight)
+    return MHLA_ERR_INVALID_ARG;
+  if (params->lepe_weight && !params->lepe_bias) return MHLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(params->ln_weight) || !aligned16(params->ln_bias) ||
+      !aligned16(params->qkv_weight) || !aligned16(params->out_weight))
+    return MHLA_ERR_INVALID_ARG;
+  if (!(params->ln_eps >= 0.0f) || !std::isfinite(params->ln_eps)) return MHLA_ERR_INVALID_ARG;
+  if (!linear_available()) return MHLA_ERR_UNSUPPORTED;
+  ModuleLayout L;
+  const int rl = module_layout(B, N, C, params->heads, grid, block, &L);
+  if (rl != MHLA_OK) return static_cast<mhla_status_t>(rl);
+  void* ws = workspace;
+  if (!ws && workspace_bytes != 0) return MHLA_ERR_WORKSPACE;
+  if (ws && (workspace_bytes < L.total || reinterpret_cast<uintptr_t>(ws) % kAlign != 0)) return MHLA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool owned = false;
+  if (!ws) {
+    if (cudaMallocAsync(&ws, L.total, s) != cudaSuccess) return MHLA_ERR_CUDA;
+    owned = true;
+  }
+  char* base = static_cast<char*>(ws);
+  void* abuf = base + L.a_off;
+  void* qkv = base + L.qkv_off;
+  const int64_t R = B * N;
+  mhla_tensor_t q, k, v, o;
+  module_views(qkv, abuf, B, N, C, params->heads, &q, &k, &v, &o);
+  int r = launch_layer_norm(x, abuf, R, static_cast<int32_t>(C), params->ln_weight, params->ln_bias, params->ln_eps,
+                            stream);
+  if (r == MHLA_OK)
+    r = launch_linear("cublaslt_qkv", abuf, params->qkv_weight, params->qkv_bias, qkv, R, C, 3 * C, base + L.lt_off, stream);
+  if (r == MHLA_OK)
+    r = mhla_forward(&q, &k, &v, W, grid, block, phi, &o, base + L.core_off, L.lt_off - L.core_off, stream,
+                     MHLA_PATH_AUTO);
+  if (r == MHLA_OK && params->lepe_weight) {
+    LepeArgs a;
+    r = lepe_args(&v, &o, grid, params->lepe_weight, params->lepe_bias, &a);
+    if (r == MHLA_OK) r = launch_lepe_add(a, stream);
+  }
+  if (r == MHLA_OK) r = launch_linear("cublaslt_out", abuf, params->out_weight, params->out_bias, y, R, C, C, base + L.lt_off, stream);
+  if (owned && cudaFreeAsync(ws, s) != cudaSuccess && r == MHLA_OK) return MHLA_ERR_CUDA;
+  return static_cast<mhla_status_t>(r);
+}

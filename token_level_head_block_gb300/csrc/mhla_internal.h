@@ -149,6 +149,25 @@ inline bool blocks_contiguous(const Problem& p) {
   return false;
 }
 
+// Module around the core: LayerNorm rows, the 5 x 5 depthwise positional term
+// added into the core's output, and bf16 linear layers through cuBLASLt.
+struct LepeArgs {
+  const void* v;
+  void* o;
+  int64_t vsb, vsn, vsh, osb, osn, osh;   // elements
+  int64_t B;
+  int32_t d, C, T, Y, X;
+  const float* weight;   // [C][5][5]
+  const float* bias;     // [C]
+};
+int launch_layer_norm(const void* x, void* y, int64_t rows, int32_t C, const float* weight, const float* bias,
+                      float eps, void* stream);
+int launch_lepe_add(const LepeArgs& a, void* stream);
+int launch_linear(const char* name, const void* x, const void* W, const void* bias, void* y, int64_t rows, int64_t k,
+                  int64_t n_out, void* lt_ws, void* stream);
+bool linear_available();
+size_t linear_workspace_bytes();
+
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
