@@ -312,8 +312,9 @@ mhla_status_t mhla_layer_norm(const void* x, void* y, int64_t rows, int64_t C, c
  * with zero outside the frame, over the (Y, X) axes of the grid (each frame of
  * a 3-D grid on its own).  Channel c is h * d + j of a [B, N, H, d] view.
  *   v, out   bf16 device views of the same shape; d % 8 == 0, every stride a
- *            multiple of 8 elements, 16-byte aligned bases; out must not
- *            overlap v.
+ *            multiple of 8 elements, 16-byte aligned bases; heads adjacent
+ *            (stride_h == d), as in a projection's [B, N, 3C] rows or a
+ *            contiguous [B, N, H, d] tensor; out must not overlap v.
  *   weight   device float32 [H * d][5][5];  bias  device float32 [H * d].
  * Rounds o + (bias + conv) once to bf16.  Asynchronous on stream. */
 mhla_status_t mhla_lepe_add(const mhla_tensor_t* v, const mhla_tensor_t* out, const mhla_shape3_t* grid,

@@ -391,13 +391,15 @@ extern "C" mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_
 
 extern "C" mhla_status_t mhla_device_status(void* stream, uint32_t* flags) {
   if (!flags) return MHLA_ERR_INVALID_ARG;
-  uint32_t tc = 0, small = 0, bwd = 0, causal = 0;
+  uint32_t tc = 0, small = 0, bwd = 0, causal = 0, module = 0;
   const int a = read_and_clear_device_error(stream, &tc);
   const int b = read_and_clear_small_error(stream, &small);
   const int c = read_and_clear_bwd_error(stream, &bwd);
   const int e = read_and_clear_causal_error(stream, &causal);
-  if (a == MHLA_ERR_CUDA || b == MHLA_ERR_CUDA || c == MHLA_ERR_CUDA || e == MHLA_ERR_CUDA) return MHLA_ERR_CUDA;
-  *flags = tc | small | bwd | causal;
+  const int f = read_and_clear_module_error(stream, &module);
+  if (a == MHLA_ERR_CUDA || b == MHLA_ERR_CUDA || c == MHLA_ERR_CUDA || e == MHLA_ERR_CUDA || f == MHLA_ERR_CUDA)
+    return MHLA_ERR_CUDA;
+  *flags = tc | small | bwd | causal | module;
   return *flags ? MHLA_ERR_TIMEOUT : MHLA_OK;
 }
 
@@ -442,6 +444,14 @@ bool lepe_view_ok(const mhla_tensor_t* t) {
          t->stride_h % 8 == 0 && aligned16(t->data);
 }
 
+// v and out move by TMA as (channel, x, y, frame, batch): heads adjacent.
+bool lepe_tma_ok(const mhla_tensor_t* v, int64_t T, int64_t Y, int64_t X) {
+  if (v->H > 1 && v->stride_h != v->d) return false;
+  if (v->stride_n < v->H * v->d) return false;
+  const int64_t lim = int64_t{1} << 39;   // bytes / 2
+  return v->stride_n * X * Y * T < lim && v->stride_b < lim && v->H * v->d < (int64_t{1} << 31);
+}
+
 int lepe_args(const mhla_tensor_t* v, const mhla_tensor_t* out, const mhla_shape3_t* grid, const float* weight,
               const float* bias, LepeArgs* a) {
   for (const mhla_tensor_t* t : {v, out}) {
@@ -452,7 +462,8 @@ int lepe_args(const mhla_tensor_t* v, const mhla_tensor_t* out, const mhla_shape
   int64_t T, Y, X;
   const int rg = check_grid_tokens(grid, v->N, &T, &Y, &X);
   if (rg != MHLA_OK) return rg;
-  if (!lepe_view_ok(v) || !lepe_view_ok(out)) return MHLA_ERR_UNSUPPORTED;
+  if (!lepe_view_ok(v) || !lepe_view_ok(out) || !lepe_tma_ok(v, T, Y, X) || !lepe_tma_ok(out, T, Y, X))
+    return MHLA_ERR_UNSUPPORTED;
   if (v->B > 0 && v->H > 0) {
     if (!weight || !bias) return MHLA_ERR_INVALID_ARG;
     if (!non_overlapping(out)) return MHLA_ERR_INVALID_ARG;
@@ -561,7 +572,7 @@ extern "C" mhla_status_t mhla_layer_norm(const void* x, void* y, int64_t rows, i
 
 extern "C" mhla_status_t mhla_lepe_add(const mhla_tensor_t* v, const mhla_tensor_t* out, const mhla_shape3_t* grid,
                                        const float* weight, const float* bias, void* stream) {
-  LepeArgs a;
+  LepeArgs a = {};
   const int rc = lepe_args(v, out, grid, weight, bias, &a);
   if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
   if (v->B == 0 || v->H == 0) return MHLA_OK;
@@ -625,7 +636,7 @@ extern "C" mhla_status_t mhla_module_forward(const void* x, void* y, int64_t B, 
     r = mhla_forward(&q, &k, &v, W, grid, block, phi, &o, base + L.core_off, L.lt_off - L.core_off, stream,
                      MHLA_PATH_AUTO);
   if (r == MHLA_OK && params->lepe_weight) {
-    LepeArgs a;
+    LepeArgs a = {};
     r = lepe_args(&v, &o, grid, params->lepe_weight, params->lepe_bias, &a);
     if (r == MHLA_OK) r = launch_lepe_add(a, stream);
   }

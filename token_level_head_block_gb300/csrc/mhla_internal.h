@@ -166,6 +166,7 @@ int launch_lepe_add(const LepeArgs& a, void* stream);
 int launch_linear(const char* name, const void* x, const void* W, const void* bias, void* y, int64_t rows, int64_t k,
                   int64_t n_out, void* lt_ws, void* stream);
 bool linear_available();
+int read_and_clear_module_error(void* stream, uint32_t* flags);
 size_t linear_workspace_bytes();
 
 constexpr size_t kAlign = 256;

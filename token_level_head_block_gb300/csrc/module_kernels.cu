@@ -23,9 +23,17 @@
 #include <mutex>
 
 #include "mhla_internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+#include "tma_host.h"
 
 namespace mhla {
+
+__device__ unsigned int g_module_error = 0;
+
 namespace {
+
+using namespace tc;
 
 // ------------------------------------------------------------------ LayerNorm
 
@@ -98,28 +106,27 @@ __global__ void __launch_bounds__(256) mhla_ln_rows(const __nv_bfloat16* __restr
 
 // ------------------------------------------------------- LePE (5 x 5 depthwise)
 
-// One CTA: a 16 x 16 token patch of one frame and 64 channels (8 units of 8).
-// The v patch with its 2-token halo is staged in shared memory, one plane per
-// channel unit (plane stride padded by 16 bytes, so the 8 units of a token land
-// in different banks).  Thread (unit u, row y, strip s) owns 8 tokens of row y
-// and the 8 channels of unit u: it reads their o units, convolves two channels
-// at a time with packed float32 FMAs, and writes the units back, so the 8
-// threads of a token move its 128 contiguous bytes.
-constexpr int kLpTY = 16, kLpTX = 16, kLpHY = kLpTY + 4, kLpHX = kLpTX + 4, kLpUnits = 8;
-constexpr int kLpPlane = kLpHY * kLpHX * 16 + 16;   // bytes per channel-unit plane
-constexpr int kLpThreads = kLpUnits * kLpTY * (kLpTX / 8);   // 256
-constexpr size_t kLpSmem = static_cast<size_t>(kLpUnits) * kLpPlane + 25 * 64 * 4 + 64 * 4;
+// Persistent CTAs walk 8 x 16 token patches of one frame and 64 channels (32
+// pairs), channel chunk slowest.  Per patch two TMA loads land in one of two
+// stage buffers: v with its 2-token halo, [12][20][64] bf16, whose out-of-frame
+// elements read as zero (the convolution's padding), and the o tile,
+// [8][16][64] bf16.  Thread (pair q = lane, row y, strip s) convolves 8 tokens
+// of its row for its two channels with packed float32 FMAs and adds them into
+// the o tile in place (the 32 lanes of a warp touch 128 contiguous bytes, no
+// bank conflicts); one TMA store then writes the tile back, clipped at the
+// frame and channel edges.  The next patch's loads run while this one is
+// convolved; the 5 x 5 weights are reloaded only when the chunk changes.
+constexpr int kLpTY = 8, kLpTX = 16, kLpHY = kLpTY + 4, kLpHX = kLpTX + 4;
+constexpr int kLpV = kLpHY * kLpHX * 128;                     // v patch bytes
+constexpr int kLpO = kLpTY * kLpTX * 128;                     // o tile bytes
+constexpr int kLpStage = kLpV + kLpO;
+constexpr int kLpThreads = 32 * kLpTY * (kLpTX / 8);          // 512: warp = (row, strip)
+constexpr size_t kLpSmem = 2 * kLpStage + 25 * 64 * 4 + 64 * 4 + 64 + 128;
 
-struct LpView {
-  const __nv_bfloat16* v;
-  __nv_bfloat16* o;
-  int64_t vsb, vsn, vsh, osb, osn, osh;   // elements
-  int32_t d, C, T, Y, X;
+struct LpGeom {
+  int64_t ntiles;
+  int32_t C, B, T, Y, X, ntx, nty;
 };
-
-__device__ __forceinline__ int64_t unit_offset(int32_t c, int32_t d, int64_t sh) {
-  return static_cast<int64_t>(c / d) * sh + (c % d);
-}
 
 // acc += w * v on two float32 lanes (each lane rounds like fmaf)
 __device__ __forceinline__ uint64_t fma2(uint64_t w, uint64_t v, uint64_t acc) {
@@ -128,98 +135,125 @@ __device__ __forceinline__ uint64_t fma2(uint64_t w, uint64_t v, uint64_t acc) {
   return d;
 }
 
-__device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
-  return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
-}
+__global__ void __launch_bounds__(kLpThreads, 2) mhla_lepe_add(const __grid_constant__ CUtensorMap tm_v,
+                                                               const __grid_constant__ CUtensorMap tm_o, LpGeom g,
+                                                               const float* __restrict__ weight,
+                                                               const float* __restrict__ bias) {
+  extern __shared__ uint8_t lp_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(lp_raw) + 127) & ~uintptr_t{127});
+  uint8_t* stage = smem;                                              // [2] (v patch, o tile)
+  float* wsm = reinterpret_cast<float*>(smem + 2 * kLpStage);         // [25 taps][64 channels]
+  float* bsm = wsm + 25 * 64;                                         // [64]
+  uint64_t* full = reinterpret_cast<uint64_t*>(bsm + 64);             // [2]
+  volatile uint32_t* abortf = reinterpret_cast<volatile uint32_t*>(full + 2);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t frames = static_cast<int64_t>(g.B) * g.T;
 
-// the two bf16 values of a 32-bit word as a float32 pair (exact)
-__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
-  return static_cast<uint64_t>(w << 16) | (static_cast<uint64_t>(w & 0xFFFF0000u) << 32);
-}
-
-__global__ void __launch_bounds__(kLpThreads, 3) mhla_lepe_add(LpView L, const float* __restrict__ weight,
-                                                            const float* __restrict__ bias) {
-  extern __shared__ __align__(16) uint8_t lp_smem[];
-  uint8_t* planes = lp_smem;
-  float* wsm = reinterpret_cast<float*>(lp_smem + kLpUnits * kLpPlane);   // [25 taps][64 channels]
-  float* bsm = wsm + 25 * 64;                                              // [64]
-  const int tid = threadIdx.x;
-  const int nchunks = (L.C + 63) / 64;
-  const int chunk = static_cast<int>(blockIdx.z % nchunks);
-  const int64_t frame = blockIdx.z / nchunks;                               // b * T + t
-  const int64_t b = frame / L.T, t = frame % L.T;
-  const int y0 = blockIdx.y * kLpTY, x0 = blockIdx.x * kLpTX;
-  const int c0 = chunk * 64;
-  const int units = min(kLpUnits, (L.C - c0) / 8);
-  const int64_t tok0 = t * static_cast<int64_t>(L.Y) * L.X;                 // first token of the frame
-
-  for (int e = tid; e < units * 8 * 25; e += kLpThreads) {
-    const int c = e / 25, tap = e % 25;
-    wsm[tap * 64 + c] = weight[static_cast<int64_t>(c0 + c) * 25 + tap];
-  }
-  for (int e = tid; e < units * 8; e += kLpThreads) bsm[e] = bias[c0 + e];
-  // v patch with halo, zero outside the frame
-  for (int e = tid; e < kLpHY * kLpHX * kLpUnits; e += kLpThreads) {
-    const int u = e % kLpUnits, pos = e / kLpUnits;
-    const int hy = pos / kLpHX, hx = pos % kLpHX;
-    const int gy = y0 + hy - 2, gx = x0 + hx - 2;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (u < units && gy >= 0 && gy < L.Y && gx >= 0 && gx < L.X) {
-      const int64_t n = tok0 + static_cast<int64_t>(gy) * L.X + gx;
-      val = *reinterpret_cast<const uint4*>(L.v + b * L.vsb + n * L.vsn + unit_offset(c0 + 8 * u, L.d, L.vsh));
-    }
-    *reinterpret_cast<uint4*>(planes + u * kLpPlane + pos * 16) = val;
+  // tile -> (chunk, frame, ty, tx), tx fastest
+  auto decode = [&](int64_t t, int& chunk, int64_t& frame, int& ty, int& tx) {
+    tx = static_cast<int>(t % g.ntx);
+    int64_t r = t / g.ntx;
+    ty = static_cast<int>(r % g.nty);
+    r /= g.nty;
+    frame = r % frames;
+    chunk = static_cast<int>(r / frames);
+  };
+  uint32_t issued[2] = {0u, 0u};
+  auto issue = [&](int st, int64_t t) {
+    int chunk, ty, tx;
+    int64_t frame;
+    decode(t, chunk, frame, ty, tx);
+    const int32_t tf = static_cast<int32_t>(frame % g.T), b = static_cast<int32_t>(frame / g.T);
+    const uint64_t pol = policy_evict_first();
+    mbar_arrive_expect_tx(full + st, kLpStage);
+    tma_load_5d(stage + st * kLpStage, &tm_v, full + st, chunk * 64, tx * kLpTX - 2, ty * kLpTY - 2, tf, b, pol);
+    tma_load_5d(stage + st * kLpStage + kLpV, &tm_o, full + st, chunk * 64, tx * kLpTX, ty * kLpTY, tf, b, pol);
+    ++issued[st];
+  };
+  if (tid == 0) {
+    mbar_init(full, 1);
+    mbar_init(full + 1, 1);
+    *abortf = 0u;
+    fence_mbar_init();
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_o);
+    for (int st = 0; st < 2; ++st)
+      if (static_cast<int64_t>(blockIdx.x) + st * gridDim.x < g.ntiles) issue(st, blockIdx.x + st * gridDim.x);
   }
   __syncthreads();
 
-  const int u = tid % kLpUnits, rest = tid / kLpUnits;
-  const int y = rest % kLpTY, s = rest / kLpTY;   // output row, 8-token strip
-  const int gy = y0 + y;
-  if (u >= units || gy >= L.Y) return;
-  const int xs = x0 + s * 8;
-  const int nx = min(8, L.X - xs);                // tokens of the strip inside the frame
-  if (nx <= 0) return;
-  __nv_bfloat16* obase = L.o + b * L.osb + unit_offset(c0 + 8 * u, L.d, L.osh);
-  const int64_t nrow = tok0 + static_cast<int64_t>(gy) * L.X + xs;
-  uint4 ov[8];
+  const int y = warp % kLpTY, s = warp / kLpTY;   // output row, 8-token strip
+  const int ch = 2 * lane;
+  int cur_chunk = -1;
+  uint32_t k = 0;
+  for (int64_t t = blockIdx.x; t < g.ntiles; t += gridDim.x, ++k) {
+    int chunk, ty, tx;
+    int64_t frame;
+    decode(t, chunk, frame, ty, tx);
+    const int c0 = chunk * 64;
+    const int pairs = min(32, (g.C - c0) / 2);   // a multiple of 4
+    if (chunk != cur_chunk) {                    // the previous patch is done (barrier below)
+      for (int e = tid; e < pairs * 2 * 25; e += kLpThreads) {
+        const int c = e / 25, tap = e % 25;
+        wsm[tap * 64 + c] = weight[static_cast<int64_t>(c0 + c) * 25 + tap];
+      }
+      for (int e = tid; e < pairs * 2; e += kLpThreads) bsm[e] = bias[c0 + e];
+      cur_chunk = chunk;
+    }
+    const int st = static_cast<int>(k & 1u);
+    const bool ok = warp_wait_on(full + st, (k >> 1) & 1u, abortf, &g_module_error);
+    if (!__syncthreads_and(ok)) break;
+
+    if (lane < pairs) {
+      const uint8_t* pl = stage + st * kLpStage + (y * kLpHX + s * 8) * 128 + lane * 4;
+      uint32_t* ot = reinterpret_cast<uint32_t*>(stage + st * kLpStage + kLpV + (y * kLpTX + s * 8) * 128) + lane;
+      uint64_t acc[8];
+      const uint64_t bias2 = *reinterpret_cast<const uint64_t*>(bsm + ch);
 #pragma unroll
-  for (int x = 0; x < 8; ++x)
-    ov[x] = x < nx ? *reinterpret_cast<const uint4*>(obase + (nrow + x) * L.osn) : make_uint4(0u, 0u, 0u, 0u);
-  const uint8_t* pl = planes + u * kLpPlane;
+      for (int x = 0; x < 8; ++x) acc[x] = bias2;
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {                   // channels 8u + 2p, 8u + 2p + 1
-    const int ch = 8 * u + 2 * p;
-    uint64_t acc[8];
-    const uint64_t bias2 = pack_f2(bsm[ch], bsm[ch + 1]);
+      for (int i = 0; i < 5; ++i) {
+        uint64_t vv[12];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) acc[x] = bias2;
-#pragma unroll 1
-    for (int i = 0; i < 5; ++i) {
-      uint64_t vv[12];
+        for (int c = 0; c < 12; ++c) {   // bf16 pair -> float32 pair (exact)
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(pl + (i * kLpHX + c) * 128);
+          vv[c] = static_cast<uint64_t>(w << 16) | (static_cast<uint64_t>(w & 0xFFFF0000u) << 32);
+        }
 #pragma unroll
-      for (int c = 0; c < 12; ++c)
-        vv[c] = bf2_to_f2(*reinterpret_cast<const uint32_t*>(pl + ((y + i) * kLpHX + s * 8 + c) * 16 + p * 4));
+        for (int j = 0; j < 5; ++j) {
+          const uint64_t w2 = *reinterpret_cast<const uint64_t*>(wsm + (i * 5 + j) * 64 + ch);
 #pragma unroll
-      for (int j = 0; j < 5; ++j) {
-        const uint64_t w2 = *reinterpret_cast<const uint64_t*>(wsm + (i * 5 + j) * 64 + ch);
+          for (int x = 0; x < 8; ++x) acc[x] = fma2(w2, vv[x + j], acc[x]);
+        }
+      }
+      // o + (bias + conv), rounded once, in place in the o tile
 #pragma unroll
-        for (int x = 0; x < 8; ++x) acc[x] = fma2(w2, vv[x + j], acc[x]);
+      for (int x = 0; x < 8; ++x) {
+        const uint32_t ow = ot[x * 32];
+        const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(&ow);
+        const __nv_bfloat162 r =
+            __floats2bfloat162_rn(__low2float(o2) + __uint_as_float(static_cast<uint32_t>(acc[x])),
+                                  __high2float(o2) + __uint_as_float(static_cast<uint32_t>(acc[x] >> 32)));
+        ot[x * 32] = *reinterpret_cast<const uint32_t*>(&r);
       }
     }
-    // o + (bias + conv), rounded once
-#pragma unroll
-    for (int x = 0; x < 8; ++x) {
-      uint32_t* wd = reinterpret_cast<uint32_t*>(&ov[x]) + p;
-      const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(wd);
-      const float lo = __low2float(o2) + __uint_as_float(static_cast<uint32_t>(acc[x]));
-      const float hi = __high2float(o2) + __uint_as_float(static_cast<uint32_t>(acc[x] >> 32));
-      const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
-      *wd = *reinterpret_cast<const uint32_t*>(&r);
+    fence_proxy_async_smem();
+    __syncthreads();                             // the o tile is complete; the weights are free
+    if (tid == 0) {
+      const int32_t tf = static_cast<int32_t>(frame % g.T), b = static_cast<int32_t>(frame / g.T);
+      tma_store_5d(&tm_o, stage + st * kLpStage + kLpV, c0, tx * kLpTX, ty * kLpTY, tf, b);
+      bulk_commit_group();
+      if (t + 2 * static_cast<int64_t>(gridDim.x) < g.ntiles) {
+        bulk_wait_group_read<0>();               // the store has read the stage: reload it
+        issue(st, t + 2 * gridDim.x);
+      }
     }
   }
-#pragma unroll
-  for (int x = 0; x < 8; ++x)
-    if (x < nx) *reinterpret_cast<uint4*>(obase + (nrow + x) * L.osn) = ov[x];
+  if (tid == 0) {
+    bulk_wait_group0();
+    for (int st = 0; st < 2; ++st)
+      if (issued[st]) drain_wait_on(full + st, (issued[st] - 1) & 1u, &g_module_error);
+  }
 }
 
 // ------------------------------------------------------------ cuBLASLt loader
@@ -344,12 +378,25 @@ int launch_layer_norm(const void* x, void* y, int64_t rows, int32_t C, const flo
 }
 
 int launch_lepe_add(const LepeArgs& a, void* stream) {
-  LpView L;
-  L.v = static_cast<const __nv_bfloat16*>(a.v);
-  L.o = static_cast<__nv_bfloat16*>(a.o);
-  L.vsb = a.vsb; L.vsn = a.vsn; L.vsh = a.vsh;
-  L.osb = a.osb; L.osn = a.osn; L.osh = a.osh;
-  L.d = a.d; L.C = a.C; L.T = a.T; L.Y = a.Y; L.X = a.X;
+  // v and o as 5-D tensors (channel, x, y, frame, batch); their heads are adjacent
+  auto map = [&](const void* base, int64_t sn, int64_t sb, uint32_t bx, uint32_t by, CUtensorMap* m) {
+    const int64_t frame_stride = static_cast<int64_t>(a.Y) * a.X * sn;
+    const int64_t bstride = a.B > 1 ? sb : frame_stride * a.T;
+    const cuuint64_t dims[5] = {static_cast<cuuint64_t>(a.C), static_cast<cuuint64_t>(a.X),
+                                static_cast<cuuint64_t>(a.Y), static_cast<cuuint64_t>(a.T),
+                                static_cast<cuuint64_t>(a.B)};
+    const cuuint64_t strides[4] = {static_cast<cuuint64_t>(sn * 2), static_cast<cuuint64_t>(a.X * sn * 2),
+                                   static_cast<cuuint64_t>(frame_stride * 2), static_cast<cuuint64_t>(bstride * 2)};
+    const cuuint32_t box[5] = {64u, bx, by, 1u, 1u};
+    return encode_tensor_map(m, 5, const_cast<void*>(base), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  };
+  CUtensorMap tv, to;
+  if (!map(a.v, a.vsn, a.vsb, kLpHX, kLpHY, &tv) || !map(a.o, a.osn, a.osb, kLpTX, kLpTY, &to)) return MHLA_ERR_CUDA;
+  LpGeom g;
+  g.C = a.C; g.B = static_cast<int32_t>(a.B); g.T = a.T; g.Y = a.Y; g.X = a.X;
+  g.ntx = (a.X + kLpTX - 1) / kLpTX;
+  g.nty = (a.Y + kLpTY - 1) / kLpTY;
+  g.ntiles = static_cast<int64_t>((a.C + 63) / 64) * a.B * a.T * g.nty * g.ntx;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(mhla_lepe_add, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kLpSmem)) !=
@@ -357,12 +404,16 @@ int launch_lepe_add(const LepeArgs& a, void* stream) {
       return MHLA_ERR_CUDA;
     attr = true;
   }
-  const int64_t nchunks = (a.C + 63) / 64;
-  const dim3 grid(static_cast<unsigned>((a.X + kLpTX - 1) / kLpTX), static_cast<unsigned>((a.Y + kLpTY - 1) / kLpTY),
-                  static_cast<unsigned>(a.B * a.T * nchunks));
+  const int sms = device_sm_count();
+  if (sms <= 0) return MHLA_ERR_CUDA;
+  const int grid = static_cast<int>(std::min<int64_t>(g.ntiles, 2 * static_cast<int64_t>(sms)));
   KernelTimer timer("mhla_lepe_add", stream);
-  mhla_lepe_add<<<grid, kLpThreads, kLpSmem, static_cast<cudaStream_t>(stream)>>>(L, a.weight, a.bias);
+  mhla_lepe_add<<<grid, kLpThreads, kLpSmem, static_cast<cudaStream_t>(stream)>>>(tv, to, g, a.weight, a.bias);
   return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+}
+
+int read_and_clear_module_error(void* stream, uint32_t* flags) {
+  return read_and_clear_word(g_module_error, stream, flags);
 }
 
 int launch_linear(const char* name, const void* x, const void* W, const void* bias, void* y, int64_t rows, int64_t k,
