@@ -164,7 +164,9 @@ KERNEL_SOURCES = {"tc_summary": "tc_summary.cu", "tc_mix": "tc_mix.cu", "tc_outp
                   "tc_bwd_query": "bwd_tc_kernels.cu", "tc_bwd_key": "bwd_tc_kernels.cu",
                   "tc_dw": "bwd_tc_kernels.cu", "simt_bwd_query": "simt_kernels.cu",
                   "simt_bwd_key": "simt_kernels.cu", "simt_dw": "simt_kernels.cu",
-                  "simt_causal_output": "simt_kernels.cu", "tc_causal_tile": "causal_tc_kernels.cu"}
+                  "simt_causal_output": "simt_kernels.cu", "tc_causal_tile": "causal_tc_kernels.cu",
+                  "tc_tile_output": "causal_tc_kernels.cu", "mhla_lepe_add": "module_kernels.cu",
+                  "mhla_ln_rows": "module_kernels.cu"}
 
 
 def kernel_source_digest(kernel):
@@ -209,6 +211,8 @@ def kernel_work(wl, name):
         "tc_dw": ("tensor", 2 * M * M * BH * d * (d + 1)), "simt_dw": ("alu", 2 * M * M * BH * d * (d + 1)),
         # causal: read q, k, v, write o
         "simt_causal_output": ("hbm", 4 * io), "tc_causal_tile": ("hbm", 4 * io),
+        # readout of contiguous 64-token blocks: read q, write o
+        "tc_tile_output": ("hbm", 2 * io),
         # module: x -> LayerNorm; qkv = xn W^T; o += lepe(v) (read v, o; write o); y = o W^T
         "mhla_ln_rows": ("hbm", 2 * io), "mhla_lepe_add": ("hbm", 3 * io),
         "cublaslt_qkv": ("tensor", 2 * wl.tokens * (wl.H * d) * 3 * (wl.H * d)),
