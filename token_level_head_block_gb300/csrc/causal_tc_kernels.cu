@@ -58,7 +58,7 @@ __device__ __forceinline__ bool cwarp_wait(uint64_t* bar, uint32_t parity, volat
 __device__ __forceinline__ void cdrain(uint64_t* bar, uint32_t parity) { drain_wait_on(bar, parity, &g_causal_error); }
 
 constexpr int kCtWorkers = 256;
-constexpr int kCtThreads = kCtWorkers + 32;
+constexpr int kCtThreads = kCtWorkers + 64;   // workers, MMA issuer, load producer
 constexpr int kTile = 128;
 
 template <int D, int NU>
@@ -169,67 +169,82 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     b = static_cast<int32_t>(bh / g.H);
   };
 
-  if (warp == kCtWorkers / 32) {
-    // ------------------------------------------------------------ control
+  // stage st: q (k, v) tiles and the state slot of unit u
+  auto issue = [&](int st, int64_t u, uint64_t pol, uint64_t pol_st) {
+    int32_t b, h, tile;
+    coords(u, b, h, tile);
+    mbar_arrive_expect_tx(full + st, (INTRA ? 3 : 1) * Cfg::TILE);
+    tma_load_4d(qt + st * Cfg::TILE, &tm_q, full + st, 0, h, tile * kTile, b, pol);
+    if (INTRA) {
+      tma_load_4d(kt + st * Cfg::TILE, &tm_k, full + st, 0, h, tile * kTile, b, pol);
+      tma_load_4d(vt + st * Cfg::TILE, &tm_v, full + st, 0, h, tile * kTile, b, pol);
+    }
+    mbar_arrive_expect_tx(full_st + st, NU * (Cfg::ST + D * 4));
+    for (int k = 0; k < NU; ++k) {
+      const int64_t su = (static_cast<int64_t>(b) * g.H + h) * g.Mu + static_cast<int64_t>(tile) * NU + k;
+      tma_load_2d(sz + st * Cfg::SLOT + k * 2 * Cfg::ST, &tm_st, full_st + st, 0, static_cast<int32_t>(su * D),
+                  pol_st);
+      bulk_load(zraw + (st * NU + k) * D, zt + su * D, D * 4, full_st + st, pol_st);
+    }
+  };
+
+  if (warp == kCtWorkers / 32 + 1) {
+    // ------------------------------------------------------------ load producer
+    // Tiles n and n + 1 up front; tile n + 2 into stage n % 2 as soon as every MMA
+    // of tile n is complete.
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       const uint64_t pol_st = policy_evict_last();
-      auto issue = [&](int st, int64_t u) {   // stage st: q (k, v) tiles and the state slot
-        int32_t b, h, tile;
-        coords(u, b, h, tile);
-        mbar_arrive_expect_tx(full + st, (INTRA ? 3 : 1) * Cfg::TILE);
-        tma_load_4d(qt + st * Cfg::TILE, &tm_q, full + st, 0, h, tile * kTile, b, pol);
-        if (INTRA) {
-          tma_load_4d(kt + st * Cfg::TILE, &tm_k, full + st, 0, h, tile * kTile, b, pol);
-          tma_load_4d(vt + st * Cfg::TILE, &tm_v, full + st, 0, h, tile * kTile, b, pol);
-        }
-        mbar_arrive_expect_tx(full_st + st, NU * (Cfg::ST + D * 4));
-        for (int k = 0; k < NU; ++k) {
-          const int64_t su = (static_cast<int64_t>(b) * g.H + h) * g.Mu + static_cast<int64_t>(tile) * NU + k;
-          tma_load_2d(sz + st * Cfg::SLOT + k * 2 * Cfg::ST, &tm_st, full_st + st, 0, static_cast<int32_t>(su * D),
-                      pol_st);
-          bulk_load(zraw + (st * NU + k) * D, zt + su * D, D * 4, full_st + st, pol_st);
-        }
-      };
-      uint32_t n_stage[2] = {0, 0}, n_m1 = 0, n_m2 = 0;
+      uint32_t n_stage[2] = {0, 0};
       const int64_t u0 = blockIdx.x, stride = gridDim.x;
       for (int st = 0; st < 2; ++st)
         if (u0 + st * stride < n_units) {
-          issue(st, u0 + st * stride);
+          issue(st, u0 + st * stride, pol, pol_st);
           n_stage[st] = 1;
         }
       uint32_t it = 0;
-      for (int64_t u = u0; u < n_units; u += stride, ++it) {
+      for (int64_t u = u0; u + 2 * stride < n_units; u += stride, ++it) {
+        if (!cwait(done2, it & 1u, abortf)) break;
+        const int st = static_cast<int>(it & 1u);
+        issue(st, u + 2 * stride, pol, pol_st);
+        ++n_stage[st];
+      }
+      for (int st = 0; st < 2; ++st)
+        if (n_stage[st]) {
+          cdrain(full + st, (n_stage[st] - 1) & 1u);
+          cdrain(full_st + st, (n_stage[st] - 1) & 1u);
+        }
+    }
+  } else if (warp == kCtWorkers / 32) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t n_m1 = 0, n_m2 = 0;
+      const int64_t u0 = blockIdx.x, stride = gridDim.x;
+      // MMA 1 of a tile: scores = phi(Q) phi(K)^T, 128 x 128 (TMEM columns 0..127)
+      auto mma1 = [&](int st) {
+        constexpr uint32_t idesc = idesc_bf16_f32(128, kTile, /*a K-major*/ false, /*b K-major*/ false);
+        const uint32_t qa = smem_u32(qt + st * Cfg::TILE), ka = smem_u32(kt + st * Cfg::TILE);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_bf16(tmem, smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
+                   smem_desc(ka + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT), idesc, ks > 0 ? 1u : 0u);
+        mma_commit(done1);
+        ++n_m1;
+      };
+      bool ok = u0 < n_units && cwait(full, 0, abortf) && cwait(phid, 0, abortf);
+      if (ok) {
+        tc_fence_after();
+        if (INTRA) mma1(0);
+      }
+      uint32_t it = 0;
+      for (int64_t u = u0; ok && u < n_units; u += stride, ++it) {
         const uint32_t par = it & 1u, par2 = (it >> 1) & 1u;
         const int st = static_cast<int>(it & 1u);
+        const bool has_next = u + stride < n_units;
         const uint32_t qa = smem_u32(qt + st * Cfg::TILE);
-        // MMA 1: scores = phi(Q) phi(K)^T, 128 x 128
-        if (!cwait(full + st, par2, abortf) || !cwait(phid, par, abortf)) break;
-        tc_fence_after();
-        if (INTRA) {
-          constexpr uint32_t idesc = idesc_bf16_f32(128, kTile, /*a K-major*/ false, /*b K-major*/ false);
-          const uint32_t ka = smem_u32(kt + st * Cfg::TILE);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem, smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
-                     smem_desc(ka + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT), idesc, ks > 0 ? 1u : 0u);
-          mma_commit(done1);
-          ++n_m1;
-        }
-        // state MMAs: phi(Q) [S'_u | z'_u hi lo], one accumulator per unit (with one
-        // unit, the accumulator P [V | 1] joins next)
-        if (!cwait(full_st + st, par2, abortf) || !cwait(zready, par, abortf)) break;
+        // the previous tile's output has read the accumulators
         if (it > 0 && !cwait(odone, par ^ 1u, abortf)) break;
-        tc_fence_after();
         constexpr uint32_t idesc2 = idesc_bf16_f32(128, Cfg::NO, /*a K-major*/ false, /*b MN-major*/ true);
-#pragma unroll
-        for (int k = 0; k < NU; ++k) {
-          const uint32_t sb = smem_u32(sz + st * Cfg::SLOT + k * 2 * Cfg::ST);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + Cfg::state_col(k), smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
-                     smem_desc(sb + ks * 2 * Cfg::SBO, Cfg::ST, Cfg::SBO, Cfg::LAYOUT), idesc2, ks > 0 ? 1u : 0u);
-        }
         if (INTRA) {   // P [V | 1] into column 128
           if (!cwait(ready, par, abortf)) break;
           tc_fence_after();
@@ -238,28 +253,40 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
           for (int ks = 0; ks < kTile / 16; ++ks)
             mma_bf16(tmem + 128, smem_desc(pa + (ks >> 2) * Cfg::P_CHUNK + (ks & 3) * 32, 16, 1024, 2),
-                     smem_desc(va + ks * 2 * Cfg::SBO, lbo_v, Cfg::SBO, Cfg::LAYOUT), idesc2,
-                     (NU == 1 || ks > 0) ? 1u : 0u);
+                     smem_desc(va + ks * 2 * Cfg::SBO, lbo_v, Cfg::SBO, Cfg::LAYOUT), idesc2, ks > 0 ? 1u : 0u);
+        }
+        // state MMAs: phi(Q) [S'_u | z'_u hi lo], one accumulator per unit; with one
+        // unit (NU == 1) it is the accumulator of P [V | 1] (column 128) and adds to it
+        if (!cwait(full_st + st, par2, abortf) || !cwait(zready, par, abortf)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < NU; ++k) {
+          const uint32_t sb = smem_u32(sz + st * Cfg::SLOT + k * 2 * Cfg::ST);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem + Cfg::state_col(k), smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
+                     smem_desc(sb + ks * 2 * Cfg::SBO, Cfg::ST, Cfg::SBO, Cfg::LAYOUT), idesc2,
+                     (ks > 0 || (INTRA && NU == 1)) ? 1u : 0u);
+        }
+        // the next tile's phi is done before this tile's MMAs are reported (so its
+        // phid arrival cannot run a phase ahead of this wait); then its scores
+        // (columns 0..127, read out into P before this tile's P [V | 1] was issued)
+        if (has_next) {
+          const int sn = st ^ 1;
+          if (!cwait(full + sn, ((it + 1) >> 1) & 1u, abortf) || !cwait(phid, par ^ 1u, abortf)) break;
+          tc_fence_after();
         }
         mma_commit(done2);
         ++n_m2;
-        if (!cwait(done2, par, abortf)) break;
-        // this stage's tiles and state slot are consumed: the tile after next goes there
-        if (u + 2 * stride < n_units) {
-          issue(st, u + 2 * stride);
-          ++n_stage[st];
-        }
+        if (INTRA && has_next) mma1(st ^ 1);
       }
-      for (int st = 0; st < 2; ++st)
-        if (n_stage[st]) {
-          cdrain(full + st, (n_stage[st] - 1) & 1u);
-          cdrain(full_st + st, (n_stage[st] - 1) & 1u);
-        }
       if (n_m1) cdrain(done1, (n_m1 - 1) & 1u);
       if (n_m2) cdrain(done2, (n_m2 - 1) & 1u);
     }
   } else {
     // ------------------------------------------------------------ workers
+    // One tile ahead: phi of tile n + 1 runs under this tile's MMAs, and the
+    // scores of tile n + 1 under this tile's output.
     const int row = tid & 127;                    // query row = TMEM lane
     const int half = tid >> 7;                    // key chunks and output columns of this warpgroup
     const int q4 = warp & 3;
@@ -268,14 +295,8 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const bool add_eps = phi_kind == MHLA_PHI_RELU_EPS;
     const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
     const int swr = row & 7;
-    uint32_t it = 0;
-    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-      const uint32_t par = it & 1u, par2 = (it >> 1) & 1u;
-      const int st = static_cast<int>(it & 1u);
-      int32_t b, h, tile;
-      coords(u, b, h, tile);
-      // ---- phi on the q (and k) tiles of this stage
-      if (!cwarp_wait(full + st, par2, abortf)) break;
+    // phi on the q (and k) tiles of a stage
+    auto apply_phi = [&](int st) {
       for (int e = tid; e < (INTRA ? 2 : 1) * Cfg::TILE / 16; e += kCtWorkers) {
         uint4* p = reinterpret_cast<uint4*>(e < Cfg::TILE / 16 ? qt + st * Cfg::TILE : kt + st * Cfg::TILE) +
                    (e % (Cfg::TILE / 16));
@@ -284,8 +305,9 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(phid);
-      // ---- z' atoms of this slot (row r: columns 0, 1 = hi, lo)
-      if (!cwarp_wait(full_st + st, par2, abortf)) break;
+    };
+    // z' atoms of a slot (row r: columns 0, 1 = hi, lo)
+    auto write_z = [&](int st) {
       if (tid < NU * D) {
         const int k = tid / D, r = tid % D;
         const float zv = zraw[(st * NU + k) * D + r];
@@ -297,41 +319,78 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(zready);
+    };
+    // W_ii of this row's block in tile u (read ahead of the scores)
+    auto row_weight = [&](int64_t u) {
+      const int32_t tile = static_cast<int32_t>(u % g.nt);
+      const int32_t blk = (tile * kTile + row) / g.w;
+      return INTRA ? __ldg(W + static_cast<int64_t>(blk) * g.M + blk) : 0.0f;
+    };
+    // P = W_ii * score for keys s <= t of the same block, from the scores of tile u
+    auto form_p = [&](int64_t u, float wii) {
+      int32_t b, h, tile;
+      coords(u, b, h, tile);
       const int32_t n0 = tile * kTile;
-      if (INTRA) {
-        // ---- P = W_ii * score for keys s <= t of the same block
-        const int32_t blk = (n0 + row) / g.w;
-        const int32_t first = blk * g.w - n0;      // first key of this row's block inside the tile (may be < 0)
-        const float wii = __ldg(W + static_cast<int64_t>(blk) * g.M + blk);
-        if (!cwarp_wait(done1, par, abortf)) break;
-        tc_fence_after();
-        for (int m = half; m < kTile / 32; m += 2) {   // 32 keys per step
-          uint32_t r[32];
-          tmem_ld_x32(lane_base + m * 32, r);
-          tmem_ld_wait();
-          uint32_t packed[16];
+      const int32_t blk = (n0 + row) / g.w;
+      const int32_t first = blk * g.w - n0;      // first key of this row's block inside the tile (may be < 0)
+      for (int m = half; m < kTile / 32; m += 2) {   // 32 keys per step
+        uint32_t r[32];
+        tmem_ld_x32(lane_base + m * 32, r);
+        tmem_ld_wait();
+        uint32_t packed[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int s0 = m * 32 + e;
-            const bool k0 = s0 <= row && s0 >= first;
-            const bool k1 = s0 + 1 <= row && s0 + 1 >= first;
-            packed[e >> 1] =
-                pack_bf16(k0 ? __uint_as_float(r[e]) * wii : 0.0f, k1 ? __uint_as_float(r[e + 1]) * wii : 0.0f);
-          }
-          uint8_t* prow = sp + (m >> 1) * Cfg::P_CHUNK + row * 128;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(prow + ((((m & 1) * 4 + q) ^ swr) * 16)) =
-                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+        for (int e = 0; e < 32; e += 2) {
+          const int s0 = m * 32 + e;
+          const bool k0 = s0 <= row && s0 >= first;
+          const bool k1 = s0 + 1 <= row && s0 + 1 >= first;
+          packed[e >> 1] =
+              pack_bf16(k0 ? __uint_as_float(r[e]) * wii : 0.0f, k1 ? __uint_as_float(r[e + 1]) * wii : 0.0f);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(ready);
+        uint8_t* prow = sp + (m >> 1) * Cfg::P_CHUNK + row * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(prow + ((((m & 1) * 4 + q) ^ swr) * 16)) =
+              make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ready);
+    };
+
+    bool ok = static_cast<int64_t>(blockIdx.x) < n_units;
+    if (ok) {
+      ok = cwarp_wait(full, 0, abortf);
+      if (ok) apply_phi(0);
+      if (ok && INTRA) {
+        const float wii0 = row_weight(blockIdx.x);
+        ok = cwarp_wait(done1, 0, abortf);
+        if (ok) {
+          tc_fence_after();
+          form_p(blockIdx.x, wii0);
+        }
+      }
+      ok = ok && cwarp_wait(full_st, 0, abortf);
+      if (ok) write_z(0);
+    }
+    uint32_t it = 0;
+    for (int64_t u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++it) {
+      const uint32_t par = it & 1u;
+      const int st = static_cast<int>(it & 1u), sn = st ^ 1;
+      const uint32_t parn2 = ((it + 1) >> 1) & 1u;
+      const bool has_next = u + gridDim.x < n_units;
+      int32_t b, h, tile;
+      coords(u, b, h, tile);
+      const float wii_next = has_next ? row_weight(u + gridDim.x) : 0.0f;
+      // ---- phi of the next tile
+      if (has_next) {
+        if (!cwarp_wait(full + sn, parn2, abortf)) break;
+        apply_phi(sn);
       }
       // ---- output: o_t = num_t / (den_t + eps), this warpgroup's half of the columns
       if (!cwarp_wait(done2, par, abortf)) break;
       tc_fence_after();
+      const int32_t n0 = tile * kTile;
       constexpr int HC = D / 2;
       uint32_t o[HC], dn[2];
       const uint32_t sc = lane_base + Cfg::state_col(my_unit);
@@ -369,6 +428,17 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                              pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv),
                              pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv),
                              pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv));
+      // ---- the next tile's P (after this tile's P [V | 1] has read P), then its z'
+      // atoms (after this tile's state MMAs, so zready stays one phase ahead at most)
+      if (has_next) {
+        if (INTRA) {
+          if (!cwarp_wait(done1, par ^ 1u, abortf)) break;
+          tc_fence_after();
+          form_p(u + gridDim.x, wii_next);
+        }
+        if (!cwarp_wait(full_st + sn, parn2, abortf)) break;
+        write_z(sn);
+      }
     }
   }
   tc_fence_before();
@@ -377,21 +447,6 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::TMEM_COLS);
   }
-}
-
-// W' of the units, bf16 [Mu][Mp]: W[b(u)][b(u')] for a past block, W[b(u)][b(u)]
-// for an earlier unit of the same block, 0 otherwise.
-__global__ void causal_unit_mixing(const float* __restrict__ W, int32_t M, int32_t upb, int32_t Mu, int64_t Mp,
-                                   __nv_bfloat16* __restrict__ Wu) {
-  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (e >= static_cast<int64_t>(Mu) * Mp) return;
-  const int32_t u = static_cast<int32_t>(e / Mp), v = static_cast<int32_t>(e % Mp);
-  float x = 0.0f;
-  if (v < Mu) {
-    const int32_t bu = u / upb, bv = v / upb;
-    if (bv < bu || (bv == bu && v < u)) x = W[static_cast<int64_t>(bu) * M + bv];
-  }
-  Wu[e] = __float2bfloat16_rn(x);
 }
 
 // ----------------------------------------------------------------- host side
@@ -520,15 +575,9 @@ int launch_tc_causal(const Problem& p, const float* W, void* workspace, void* st
   auto* St = reinterpret_cast<__nv_bfloat16*>(ws + L.st_off);
   auto* zt = reinterpret_cast<float*>(ws + L.zt_off);
   const Problem pu = unit_problem(p, L.U);
-  {
-    const int64_t n = L.Mu * L.Mp;
-    KernelTimer timer("causal_unit_mixing", stream);
-    causal_unit_mixing<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
-        W, static_cast<int32_t>(p.M), static_cast<int32_t>(p.w / L.U < 1 ? 1 : p.w / L.U),
-        static_cast<int32_t>(L.Mu), L.Mp, Wu);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
-  int rc = tc_run_summary(pu, W, nullptr, nullptr, 0, ws + L.sbuf_off, stream);
+  // unit summaries, and the unit-level causal W' in the summary kernel's prologue
+  int rc = tc_run_summary(pu, W, Wu, nullptr, L.Mp, ws + L.sbuf_off, stream, static_cast<int32_t>(p.M),
+                          static_cast<int32_t>(p.w / L.U < 1 ? 1 : p.w / L.U));
   if (rc == MHLA_OK) rc = tc_run_mix(pu, Wu, L.Mp, ws + L.sbuf_off, St, zt, stream);
   if (rc != MHLA_OK) return rc;
   const int NU = L.U == 64 ? 2 : 1;

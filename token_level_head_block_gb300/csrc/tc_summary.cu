@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, TcGeom g,
            int32_t G, int64_t n_items, int phi_kind, float eps,
            __nv_bfloat16* __restrict__ Sbuf, const float* __restrict__ W, __nv_bfloat16* __restrict__ Wb,
-           __nv_bfloat16* __restrict__ WbT, int64_t Mp) {
+           __nv_bfloat16* __restrict__ WbT, int64_t Mp, int32_t Mw, int32_t upb) {
   using Cfg = SumCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
@@ -83,13 +83,25 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // W rounded to bf16 for the mixing GEMM, [M][Mp] with zero padding (and, when
   // WbT is given, W^T likewise); every CTA converts a slice (the GEMM runs after
-  // this kernel on the same stream).  Wb null: summaries only.
+  // this kernel on the same stream).  Wb null: summaries only.  upb > 0: the
+  // summaries are of causal units (upb per block of the Mw x Mw matrix W), and
+  // Wb is the unit-level W': W[b(i)][b(j)] for a past block, W[b(i)][b(i)] for
+  // an earlier unit of the same block, 0 otherwise.
   if (Wb) {
     const int64_t n = static_cast<int64_t>(g.M) * Mp;
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * kTcThreads + threadIdx.x; e < n;
          e += static_cast<int64_t>(gridDim.x) * kTcThreads) {
       const int64_t i = e / Mp, j = e % Mp;
-      Wb[e] = __float2bfloat16_rn(j < g.M ? W[i * g.M + j] : 0.0f);
+      float x = 0.0f;
+      if (j < g.M) {
+        if (upb > 0) {
+          const int64_t bi = i / upb, bj = j / upb;
+          if (bj < bi || (bj == bi && j < i)) x = W[bi * Mw + bj];
+        } else {
+          x = W[i * g.M + j];
+        }
+      }
+      Wb[e] = __float2bfloat16_rn(x);
       if (WbT) WbT[e] = __float2bfloat16_rn(j < g.M ? W[j * g.M + i] : 0.0f);   // W^T for the backward
     }
   }
@@ -281,7 +293,7 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 
 template <int D>
 int run_summary(const Problem& p, const float* W, __nv_bfloat16* Wb, __nv_bfloat16* WbT, int64_t Mp,
-                __nv_bfloat16* Sbuf, cudaStream_t stream) {
+                __nv_bfloat16* Sbuf, int32_t Mw, int32_t upb, cudaStream_t stream) {
   using Cfg = SumCfg<D>;
   const int sms = device_sm_count();
   if (sms <= 0) return MHLA_ERR_CUDA;
@@ -299,18 +311,20 @@ int run_summary(const Problem& p, const float* W, __nv_bfloat16* Wb, __nv_bfloat
   const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
   KernelTimer timer("tc_summary", stream);
   tc_summary<D><<<grid, kTcThreads, Cfg::SMEM, stream>>>(tk, tv, make_geom(p, c64), G, n_items, p.phi_kind, p.eps,
-                                                         Sbuf, W, Wb, WbT, Mp);
+                                                         Sbuf, W, Wb, WbT, Mp, Mw, upb);
   return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
 }
 
 }  // namespace
 
-int tc_run_summary(const Problem& p, const float* W, void* Wb, void* WbT, int64_t Mp, void* Sbuf, void* stream) {
+int tc_run_summary(const Problem& p, const float* W, void* Wb, void* WbT, int64_t Mp, void* Sbuf, void* stream,
+                   int32_t Mw, int32_t upb) {
   auto* wb = static_cast<__nv_bfloat16*>(Wb);
   auto* wbt = static_cast<__nv_bfloat16*>(WbT);
   auto* sb = static_cast<__nv_bfloat16*>(Sbuf);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return p.d == 64 ? run_summary<64>(p, W, wb, wbt, Mp, sb, s) : run_summary<32>(p, W, wb, wbt, Mp, sb, s);
+  return p.d == 64 ? run_summary<64>(p, W, wb, wbt, Mp, sb, Mw, upb, s)
+                   : run_summary<32>(p, W, wb, wbt, Mp, sb, Mw, upb, s);
 }
 
 int read_and_clear_summary_error(void* stream, uint32_t* flags) { return read_and_clear_word(g_sum_error, stream, flags); }
