@@ -293,7 +293,8 @@ tc_bwd_query(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           chunk_coords(g, i, c, b, x, y, z);
           for (int hh = 0; hh < HP; ++hh)
             if (grp * HP + hh < g.H)
-              tma_store_5d(&tm_dq, gst + gs * Cfg::HT + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z);
+              tma_store_5d_hint(&tm_dq, gst + gs * Cfg::HT + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z,
+                                policy_evict_first());
           bulk_commit_group();
           bulk_wait_group_read<0>();      // the stage has been read: back to the dout producer
           mbar_arrive(gempty + gs);
@@ -867,8 +868,8 @@ tc_bwd_key(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         chunk_coords(g, j, c, b, x, y, z);
         for (int hh = 0; hh < HP; ++hh) {
           if (grp * HP + hh >= g.H) continue;
-          tma_store_5d(&tm_dk, kt + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z);
-          tma_store_5d(&tm_dv, vt + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z);
+          tma_store_5d_hint(&tm_dk, kt + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z, policy_evict_first());
+          tma_store_5d_hint(&tm_dv, vt + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z, policy_evict_first());
         }
         bulk_commit_group();
       }

@@ -171,7 +171,7 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     // bulk copy behind it.  Nothing here waits on a load, so the producer runs
     // up to NB items ahead.
     if (lane == 0) {
-      const uint64_t pol_s = policy_evict_last();
+      const uint64_t pol_s = policy_evict_first();
       int kb = 0;
       uint32_t bph = 0;
       uint64_t fills = 0;
@@ -211,7 +211,7 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           if (!wait_bounded(ostore + s, ph, abortf)) { ok = false; break; }
           int32_t x, y, z;
           chunk_coords(g, i, c, b, x, y, z);
-          tma_store_5d(&tm_o, qst + s * Cfg::QT, 0, h, x, y, z);
+          tma_store_5d_hint(&tm_o, qst + s * Cfg::QT, 0, h, x, y, z, policy_evict_first());
           bulk_commit_group();
           pend[npend++] = s;
           if (npend > kOutStoresInFlight) {

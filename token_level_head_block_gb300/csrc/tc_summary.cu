@@ -264,19 +264,20 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
         const int64_t col = (static_cast<int64_t>(b) * g.H + h) * (D + 1) * D + r * D;
         const int64_t grow = (col >> 7) * g.M + j;
         uint4* drow = reinterpret_cast<uint4*>(Sbuf + grow * 128 + (col & 127));
+        const uint64_t keep = policy_evict_last();
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          drow[q] = make_uint4(pack_bf16(__uint_as_float(v0[8 * q]), __uint_as_float(v0[8 * q + 1])),
+          st_global_v4_hint(drow + q, make_uint4(pack_bf16(__uint_as_float(v0[8 * q]), __uint_as_float(v0[8 * q + 1])),
                                pack_bf16(__uint_as_float(v0[8 * q + 2]), __uint_as_float(v0[8 * q + 3])),
                                pack_bf16(__uint_as_float(v0[8 * q + 4]), __uint_as_float(v0[8 * q + 5])),
-                               pack_bf16(__uint_as_float(v0[8 * q + 6]), __uint_as_float(v0[8 * q + 7])));
+                               pack_bf16(__uint_as_float(v0[8 * q + 6]), __uint_as_float(v0[8 * q + 7]))), keep);
         if (D == 64) {
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            drow[4 + q] = make_uint4(pack_bf16(__uint_as_float(v1[8 * q]), __uint_as_float(v1[8 * q + 1])),
+            st_global_v4_hint(drow + 4 + q, make_uint4(pack_bf16(__uint_as_float(v1[8 * q]), __uint_as_float(v1[8 * q + 1])),
                                      pack_bf16(__uint_as_float(v1[8 * q + 2]), __uint_as_float(v1[8 * q + 3])),
                                      pack_bf16(__uint_as_float(v1[8 * q + 4]), __uint_as_float(v1[8 * q + 5])),
-                                     pack_bf16(__uint_as_float(v1[8 * q + 6]), __uint_as_float(v1[8 * q + 7])));
+                                     pack_bf16(__uint_as_float(v1[8 * q + 6]), __uint_as_float(v1[8 * q + 7]))), keep);
         }
         const int64_t zcol = (static_cast<int64_t>(b) * g.H + h) * (D + 1) * D + D * D + r;
         Sbuf[((zcol >> 7) * g.M + j) * 128 + (zcol & 127)] = __float2bfloat16_rn(__uint_as_float(vz[0]));
