@@ -89,8 +89,8 @@ struct BqCfg {
   static constexpr uint32_t SBO = 8 * ROWB;
   static constexpr uint32_t LAYOUT = D == 64 ? 2u : 4u;
   static constexpr int ST = D * D * 2;            // one S~ tile (row-major, swizzled like a token tile)
-  static constexpr int NQ = 2;                    // q stages
-  static constexpr int NG = 3;                    // dout stages: dout, then dnum, then dq
+  static constexpr int NQ = 3;                    // q stages
+  static constexpr int NG = 2;                    // dout stages: dout, then dnum, then dq
   static constexpr int MASKB = HP * C * (D / 8);  // q > 0 bits of a chunk
   static constexpr int DDB = 2 * C * 16;          // dden operand: 2 groups of 8 columns, unswizzled MN-major
   static constexpr int Q_OFF = 0;
