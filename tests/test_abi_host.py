@@ -292,7 +292,10 @@ def test_backward_workspace_size(L):
     assert simt <= sizes[1] < simt + 4 * 256
     groups = (BH * (d + 1) * d + 127) // 128
     tc = 2 * M * M * 2 + 2 * M * groups * 128 * 2 + BH * M * d * d * 2 + BH * M * d * 4
-    assert tc < sizes[2] <= tc + 76 * M * M * 4 + 8 * 256          # + the split dW partial products
+    # + the dW partial products: one 256 x 256 tile of dW (M = 256) split over up to 152 CTAs
+    tiles = ((M + 255) // 256) ** 2
+    nsplit = min(groups, -(-152 // tiles))
+    assert tc < sizes[2] <= tc + nsplit * M * M * 4 + 8 * 256
     assert sizes[0] == max(sizes[1], sizes[2])                         # AUTO: enough for either path
     assert L.mhla_backward_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
                                           ctypes.byref(mhla.shape3(wl.block)), 3, ctypes.byref(n)) == UNSUPPORTED

@@ -898,15 +898,17 @@ tc_bwd_key(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 // 64-column halves of a group into a 4-stage ring, warp 1 issues the MMAs,
 // warps 4-7 write the float32 tile.
 // ============================================================================
+// One CTA: 256 rows i (two 128-row MMA halves, so each j row of S is read once
+// for both), up to 256 rows j, and a slice of the summary columns.
 struct DwCfg {
-  static constexpr int IT = 128;                  // rows i per tile (MMA M)
+  static constexpr int IT = 256;                  // rows i per tile (two MMA M halves)
   static constexpr int JT = 256;                  // rows j per tile (MMA N, at most)
-  static constexpr int A_BYTES = IT * 128;        // [128][64] K-major, 128-byte swizzle
+  static constexpr int A_BYTES = IT * 128;        // [256][64] K-major, 128-byte swizzle
   static constexpr int B_BYTES = JT * 128;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int NS = 4;
+  static constexpr int NS = 3;
   static constexpr size_t SMEM = static_cast<size_t>(NS) * STAGE + 256 + 1024;
-  static constexpr int TMEM_COLS = 256;
+  static constexpr int TMEM_COLS = 512;           // the two halves' accumulators at 0 and 256
 };
 constexpr int kDwThreads = 256;
 
@@ -961,7 +963,7 @@ tc_dw(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensor
         const int32_t grp = static_cast<int32_t>(g0 + st / 2), half = st & 1;
         mbar_arrive_expect_tx(full + s, Cfg::A_BYTES + bbytes);
         uint8_t* base = stages + s * Cfg::STAGE;
-        tma_load_3d(base, &tm_a, full + s, half * 64, i0, grp, pol);            // rows i >= M read zeros
+        tma_load_3d(base, &tm_a, full + s, half * 64, i0, grp, pol);            // 256 rows; i >= M read zeros
         tma_load_3d(base + Cfg::A_BYTES, &tm_b, full + s, half * 64, j0, grp, pol);
         ++fills;
         if (++s == Cfg::NS) { s = 0; ph ^= 1u; }
@@ -981,9 +983,11 @@ tc_dw(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensor
         tc_fence_after();
         const uint32_t base = smem_u32(stages + s * Cfg::STAGE);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem, smem_desc(base + ks * 32, 16, 1024, 2), smem_desc(base + Cfg::A_BYTES + ks * 32, 16, 1024, 2),
-                   idesc, (st > 0 || ks > 0) ? 1u : 0u);
+        for (int mh = 0; mh < 2; ++mh)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + mh * 256, smem_desc(base + mh * 128 * 128 + ks * 32, 16, 1024, 2),
+                     smem_desc(base + Cfg::A_BYTES + ks * 32, 16, 1024, 2), idesc, (st > 0 || ks > 0) ? 1u : 0u);
         mma_commit(empty + s);
         if (++s == Cfg::NS) { s = 0; ph ^= 1u; }
       }
@@ -991,25 +995,36 @@ tc_dw(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensor
       bdrain(done, 0);
     }
   } else if (warp >= 4) {
+    // warp 4 + q4 reads TMEM lanes 32 q4 .. 32 q4 + 31 of both halves
     const int q4 = warp & 3;
-    const int32_t i = i0 + 32 * q4 + lane;
     const bool ok = __all_sync(0xffffffffu, bwait(done, 0, abortf));
     if (ok) {
       tc_fence_after();
-      const uint32_t tb = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-      float* prow = part + (static_cast<int64_t>(split) * M + i) * M;
-      for (int cc = 0; cc < JN; cc += 32) {
-        uint32_t v[32];
-        tmem_ld_x32(tb + cc, v);
-        tmem_ld_wait();
-        if (i < M) {
-          if (nsteps == 0) {
+      for (int mh = 0; mh < 2; ++mh) {
+        const int32_t i = i0 + mh * 128 + 32 * q4 + lane;
+        const uint32_t tb = tmem + mh * 256 + (static_cast<uint32_t>(32 * q4) << 16);
+        float* prow = part + (static_cast<int64_t>(split) * M + i) * M;
+        for (int cc = 0; cc < JN; cc += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(tb + cc, v);
+          tmem_ld_wait();
+          if (i < M) {
+            if (nsteps == 0) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = 0u;
+              for (int e = 0; e < 32; ++e) v[e] = 0u;
+            }
+            if (j0 + cc + 32 <= M && M % 4 == 0) {   // 16-byte stores: each lane writes 128 contiguous bytes
+              float4* dst = reinterpret_cast<float4*>(prow + j0 + cc);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                     __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (j0 + cc + e < M) prow[j0 + cc + e] = __uint_as_float(v[e]);
+            }
           }
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (j0 + cc + e < M) prow[j0 + cc + e] = __uint_as_float(v[e]);
         }
       }
     }
