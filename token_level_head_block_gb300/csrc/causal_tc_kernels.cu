@@ -578,7 +578,7 @@ int launch_tc_causal(const Problem& p, const float* W, void* workspace, void* st
   // unit summaries, and the unit-level causal W' in the summary kernel's prologue
   int rc = tc_run_summary(pu, W, Wu, nullptr, L.Mp, ws + L.sbuf_off, stream, static_cast<int32_t>(p.M),
                           static_cast<int32_t>(p.w / L.U < 1 ? 1 : p.w / L.U));
-  if (rc == MHLA_OK) rc = tc_run_mix(pu, Wu, L.Mp, ws + L.sbuf_off, St, zt, stream);
+  if (rc == MHLA_OK) rc = tc_run_mix(pu, Wu, L.Mp, ws + L.sbuf_off, St, zt, stream, /*discard_input=*/true);
   if (rc != MHLA_OK) return rc;
   const int NU = L.U == 64 ? 2 : 1;
   if (p.d == 64)
@@ -595,7 +595,7 @@ int launch_tc_tile_forward(const Problem& p, const float* W, void* Wb, int64_t M
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Problem pu = unit_problem(p, 64);   // units are the blocks
   int rc = tc_run_summary(pu, W, Wb, nullptr, Mp, Sbuf, stream);
-  if (rc == MHLA_OK) rc = tc_run_mix(pu, Wb, Mp, Sbuf, St, zt, stream);
+  if (rc == MHLA_OK) rc = tc_run_mix(pu, Wb, Mp, Sbuf, St, zt, stream, /*discard_input=*/true);
   if (rc != MHLA_OK) return rc;
   const auto* st = static_cast<const __nv_bfloat16*>(St);
   return p.d == 64 ? launch_ct_tile<64, 2, false>(p, W, p.M, st, zt, s) : launch_ct_tile<32, 2, false>(p, W, p.M, st, zt, s);

@@ -111,10 +111,13 @@ int launch_small(const Problem& p, const float* W, void* stream);
 // tc_run_summary writes Wb (and W^T into WbT when WbT is not null) and Sbuf;
 // with upb > 0 the problem's blocks are causal units, upb per block of the
 // Mw x Mw matrix W, and Wb receives the unit-level causal matrix instead;
-// tc_run_mix computes St, zt = Wm . Sbuf for the bf16 [M][Mp] matrix Wm.
+// tc_run_mix computes St, zt = Wm . Sbuf for the bf16 [M][Mp] matrix Wm; with
+// discard_input its M <= 256 kernel drops Sbuf's L2 lines once read (no
+// write-back): only for callers that do not read Sbuf afterwards.
 int tc_run_summary(const Problem& p, const float* W, void* Wb, void* WbT, int64_t Mp, void* Sbuf, void* stream,
                    int32_t Mw = 0, int32_t upb = 0);
-int tc_run_mix(const Problem& p, const void* Wm, int64_t Mp, const void* Sbuf, void* St, float* zt, void* stream);
+int tc_run_mix(const Problem& p, const void* Wm, int64_t Mp, const void* Sbuf, void* St, float* zt, void* stream,
+               bool discard_input = false);
 int tc_run_output(const Problem& p, const void* St, const float* zt, void* stream);
 int read_and_clear_summary_error(void* stream, uint32_t* flags);
 int read_and_clear_mix_error(void* stream, uint32_t* flags);

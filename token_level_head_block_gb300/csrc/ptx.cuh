@@ -145,6 +145,12 @@ __device__ __forceinline__ void tma_store_5d(const void* tmap, const void* src, 
       : "memory");
 }
 
+// Drops a 128-byte L2 line without writing it back (its contents become
+// undefined): for a scratch buffer whose last reader is done with it.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // Global stores with an L2 cache policy (createpolicy value), e.g. evict-last
 // for an intermediate the next kernel reads.
 __device__ __forceinline__ void st_global_v4_hint(void* p, uint4 v, uint64_t policy) {

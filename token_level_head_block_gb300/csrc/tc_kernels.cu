@@ -135,7 +135,7 @@ int launch_tc(const Problem& p, const float* W, void* workspace, void* stream) {
   int rc = tc_run_summary(p, W, ws + L.wb_off, nullptr, L.Mp, ws + L.sbuf_off, stream);
   if (rc == MHLA_OK)
     rc = tc_run_mix(p, ws + L.wb_off, L.Mp, ws + L.sbuf_off, ws + L.st_off, reinterpret_cast<float*>(ws + L.zt_off),
-                    stream);
+                    stream, /*discard_input=*/true);
   if (rc == MHLA_OK) rc = tc_run_output(p, ws + L.st_off, reinterpret_cast<float*>(ws + L.zt_off), stream);
   return rc;
 }

@@ -249,7 +249,8 @@ struct MixResCfg {
 template <int D>
 __global__ void __launch_bounds__(kMixThreadsTC, 1)
 tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s, int32_t M,
-                int32_t NP, int64_t ncols, int32_t n_tiles, __nv_bfloat16* __restrict__ St, float* __restrict__ zt) {
+                int32_t NP, int64_t ncols, int32_t n_tiles, __nv_bfloat16* __restrict__ St, float* __restrict__ zt,
+                const __nv_bfloat16* discard_s) {
   using Cfg = MixResCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
@@ -394,6 +395,12 @@ tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
       }
       tc_fence_before();
       mbar_arrive(tempty + set);
+      // every MMA of tile t is done: its 128-column group of Sbuf (read exactly
+      // once, by this CTA) leaves L2 without a write-back when the caller allows
+      if (discard_s) {
+        const uint8_t* grp = reinterpret_cast<const uint8_t*>(discard_s + t * static_cast<int64_t>(M) * 128);
+        for (int e = (warp - 2) * 32 + lane; e < 2 * M; e += 256) discard_l2_line(grp + e * 128);
+      }
     }
   }
   tc_fence_before();
@@ -408,7 +415,7 @@ tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
 // S~ (row-major [BH][M][d][d]) and z~ (float32 [BH][M][d]).
 template <int D>
 int run_mix(const Problem& p, const __nv_bfloat16* Wm, int64_t Mp, const __nv_bfloat16* Sbuf, __nv_bfloat16* St,
-            float* zt, cudaStream_t stream) {
+            float* zt, bool discard_input, cudaStream_t stream) {
   const int sms = device_sm_count();
   if (sms <= 0) return MHLA_ERR_CUDA;
   const int64_t ncols = p.BH() * (p.d + 1) * p.d;
@@ -435,7 +442,8 @@ int run_mix(const Problem& p, const __nv_bfloat16* Wm, int64_t Mp, const __nv_bf
     const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
     KernelTimer timer("tc_mix", stream);
     tc_mix_resident<D><<<grid, kMixThreadsTC, MixResCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), NP,
-                                                                          ncols, n_tiles, St, zt);
+                                                                          ncols, n_tiles, St, zt,
+                                                                          discard_input ? Sbuf : nullptr);
     return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
   }
   CUtensorMap tw, ts;
@@ -459,12 +467,14 @@ int run_mix(const Problem& p, const __nv_bfloat16* Wm, int64_t Mp, const __nv_bf
 
 }  // namespace
 
-int tc_run_mix(const Problem& p, const void* Wm, int64_t Mp, const void* Sbuf, void* St, float* zt, void* stream) {
+int tc_run_mix(const Problem& p, const void* Wm, int64_t Mp, const void* Sbuf, void* St, float* zt, void* stream,
+               bool discard_input) {
   auto* wm = static_cast<const __nv_bfloat16*>(Wm);
   auto* sb = static_cast<const __nv_bfloat16*>(Sbuf);
   auto* st = static_cast<__nv_bfloat16*>(St);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return p.d == 64 ? run_mix<64>(p, wm, Mp, sb, st, zt, s) : run_mix<32>(p, wm, Mp, sb, st, zt, s);
+  return p.d == 64 ? run_mix<64>(p, wm, Mp, sb, st, zt, discard_input, s)
+                   : run_mix<32>(p, wm, Mp, sb, st, zt, discard_input, s);
 }
 
 int read_and_clear_mix_error(void* stream, uint32_t* flags) { return read_and_clear_word(g_mix_error, stream, flags); }

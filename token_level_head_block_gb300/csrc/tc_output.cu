@@ -83,7 +83,7 @@ template <int D>
 __global__ void __launch_bounds__(kOutThreadsTC, 1)
 tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
           const __grid_constant__ CUtensorMap tm_st, TcGeom g, int64_t n_items, int phi_kind, float eps,
-          const float* __restrict__ zt) {
+          const float* __restrict__ zt, const __nv_bfloat16* St) {
   using Cfg = OutCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
@@ -339,6 +339,15 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         }
         fence_proxy_async_smem();
         mbar_arrive(ostore + cs);
+        if (c + 1 == g.chunks) {
+          // the item's last MMA has read its S~ tile and z~ (each read once, by this
+          // CTA): their lines leave L2 without a write-back
+          const int64_t tile = ((item / g.H) / g.M * g.H + item % g.H) * g.M + (item / g.H) % g.M;
+          const int e = 32 * q4 + lane;
+          if (e < D * D * 2 / 128) discard_l2_line(reinterpret_cast<const uint8_t*>(St + tile * D * D) + e * 128);
+          else if (e < D * D * 2 / 128 + D * 4 / 128)
+            discard_l2_line(reinterpret_cast<const uint8_t*>(zt + tile * D) + (e - D * D * 2 / 128) * 128);
+        }
       }
     }
   }
@@ -382,7 +391,7 @@ int run_output(const Problem& p, const __nv_bfloat16* St, const float* zt, cudaS
   const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
   KernelTimer timer("tc_output", stream);
   tc_output<D><<<grid, kOutThreadsTC, Cfg::SMEM, stream>>>(tq, to, tst, make_geom(p, c128), n_items, p.phi_kind, p.eps,
-                                                            zt);
+                                                            zt, St);
   return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
 }
 
