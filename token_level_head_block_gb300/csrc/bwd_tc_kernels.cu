@@ -1161,7 +1161,7 @@ int launch_tc_bwd_d(const Problem& p, const float* W, const BwdOperands& bo, voi
       tc_dw_reduce<<<static_cast<unsigned>((MM + 255) / 256), 256, 0, stream>>>(part, bo.dW, MM, L.nsplit);
       if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
     }
-    rc = tc_run_mix(p, WbT, L.Mp, dSbuf, St, zt, stream);
+    rc = tc_run_mix(p, WbT, L.Mp, dSbuf, St, zt, stream, /*discard_input=*/true);   // dS~ is not read again
     if (rc != MHLA_OK) return rc;
   }
   // b4: source blocks
