@@ -171,7 +171,7 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     // bulk copy behind it.  Nothing here waits on a load, so the producer runs
     // up to NB items ahead.
     if (lane == 0) {
-      const uint64_t pol_s = policy_evict_first();
+      const uint64_t pol_s = policy_evict_last();
       int kb = 0;
       uint32_t bph = 0;
       uint64_t fills = 0;
@@ -211,7 +211,12 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           if (!wait_bounded(ostore + s, ph, abortf)) { ok = false; break; }
           int32_t x, y, z;
           chunk_coords(g, i, c, b, x, y, z);
-          tma_store_5d_hint(&tm_o, qst + s * Cfg::QT, 0, h, x, y, z, policy_evict_first());
+          // d = 64: the output leaves L2 early (evict-first); measured slower at d = 32
+          if constexpr (D == 64) {
+            tma_store_5d_hint(&tm_o, qst + s * Cfg::QT, 0, h, x, y, z, policy_evict_first());
+          } else {
+            tma_store_5d(&tm_o, qst + s * Cfg::QT, 0, h, x, y, z);
+          }
           bulk_commit_group();
           pend[npend++] = s;
           if (npend > kOutStoresInFlight) {
@@ -339,9 +344,9 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         }
         fence_proxy_async_smem();
         mbar_arrive(ostore + cs);
-        if (c + 1 == g.chunks) {
+        if (D == 64 && c + 1 == g.chunks) {
           // the item's last MMA has read its S~ tile and z~ (each read once, by this
-          // CTA): their lines leave L2 without a write-back
+          // CTA): their lines leave L2 without a write-back (measured slower at d = 32)
           const int64_t tile = ((item / g.H) / g.M * g.H + item % g.H) * g.M + (item / g.H) % g.M;
           const int e = 32 * q4 + lane;
           if (e < D * D * 2 / 128) discard_l2_line(reinterpret_cast<const uint8_t*>(St + tile * D * D) + e * 128);
