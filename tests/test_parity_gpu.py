@@ -62,10 +62,14 @@ def check_full(case, q, k, v, W, grid, block, dtype, phi="relu", eps=1e-6, path=
 # (B, H, d, grid, block): tokens per block a multiple of 128 so both paths apply;
 # odd head counts leave part of the last head group of the summary kernel empty,
 # M > 256 needs two query-block tiles in the mixing GEMM, M not a multiple of 64
-# leaves a ragged source-block chunk.
+# leaves a ragged source-block chunk; d = 32 with an even head count reads out
+# head pairs as 64-channel rows (block-diagonal operand), odd counts one head at
+# a time.
 TC_CASES = {
     "2d_h3_d64": (2, 3, 64, (32, 48), (16, 8)),
     "2d_h5_d32": (2, 5, 32, (32, 32), (8, 16)),
+    "2d_h4_d32_pairs": (2, 4, 32, (32, 32), (8, 16)),
+    "3d_h6_d32_pairs": (1, 6, 32, (8, 8, 16), (4, 4, 8)),
     "3d_h2_d64": (2, 2, 64, (4, 16, 16), (2, 8, 8)),
     "3d_frames_d32": (1, 3, 32, (8, 8, 16), (4, 4, 8)),
     "w256_d64": (2, 2, 64, (32, 32), (16, 16)),

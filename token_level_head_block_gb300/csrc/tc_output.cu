@@ -79,11 +79,17 @@ struct OutCfg {
 constexpr int kOutThreadsTC = 512;
 constexpr int kOutStoresInFlight = 3;   // TMA stores allowed to be reading shared memory at once
 
-template <int D>
+// PAIR (D = 64 only): each 64-channel row is two adjacent heads of 32 channels
+// (heads 2h', 2h' + 1 as one "head" h' of the TMA view), so q and o move in
+// 128-byte rows; the B operand is block-diagonal, [S~_a 0; 0 S~_b], with z~_a
+// hi, lo in columns 64, 65 for the rows of head a and z~_b in 66, 67 for the rows
+// of head b, and each half of the output row takes its own denominator.
+template <int D, bool PAIR>
 __global__ void __launch_bounds__(kOutThreadsTC, 1)
 tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
           const __grid_constant__ CUtensorMap tm_st, TcGeom g, int64_t n_items, int phi_kind, float eps,
           const float* __restrict__ zt, const __nv_bfloat16* St) {
+  static_assert(!PAIR || D == 64, "head pairs form 64-channel rows");
   using Cfg = OutCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
@@ -130,6 +136,14 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
     tmem_relinquish();
+  }
+  if (PAIR) {   // the off-diagonal 32 x 32 blocks of every slot's S~ operand stay zero
+    for (int e = threadIdx.x; e < Cfg::NB * 8 * 32; e += kOutThreadsTC) {
+      const int kb = e / 256, grp = (e / 32) % 8, r = e % 32;
+      const int row = grp < 4 ? 32 + r : r;
+      *reinterpret_cast<uint4*>(bslot + kb * Cfg::BT + grp * Cfg::B_SBO + row * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -181,9 +195,21 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         const int64_t tile = (b * g.H + h) * g.M + i;
         if (!wait_bounded(bempty + kb, bph ^ 1u, abortf)) break;
         uint8_t* slot = bslot + kb * Cfg::BT;
-        mbar_arrive_expect_tx(bfull + kb, Cfg::ST_BYTES + Cfg::ZRAW);
-        tma_load_4d(slot, &tm_st, bfull + kb, 0, 0, 0, static_cast<int32_t>(tile), pol_s);
-        bulk_load(slot + Cfg::BOPS, zt + tile * D, Cfg::ZRAW, bfull + kb, pol_s);
+        if constexpr (PAIR) {
+          // heads 2h and 2h + 1 (32 x 32 tiles): one (8, 32) box per column group onto the diagonal
+          mbar_arrive_expect_tx(bfull + kb, 8 * 512 + Cfg::ZRAW);
+          for (int e = 0; e < 2; ++e) {
+            const int64_t t2 = (b * 2 * g.H + 2 * h + e) * g.M + i;
+            for (int gq = 0; gq < 4; ++gq)
+              tma_load_4d(slot + (4 * e + gq) * Cfg::B_SBO + 32 * e * 16, &tm_st, bfull + kb, 0, 0, gq,
+                          static_cast<int32_t>(t2), pol_s);
+            bulk_load(slot + Cfg::BOPS + e * 128, zt + t2 * 32, 128, bfull + kb, pol_s);
+          }
+        } else {
+          mbar_arrive_expect_tx(bfull + kb, Cfg::ST_BYTES + Cfg::ZRAW);
+          tma_load_4d(slot, &tm_st, bfull + kb, 0, 0, 0, static_cast<int32_t>(tile), pol_s);
+          bulk_load(slot + Cfg::BOPS, zt + tile * D, Cfg::ZRAW, bfull + kb, pol_s);
+        }
         ++fills;
         if (++kb == Cfg::NB) { kb = 0; bph ^= 1u; }
       }
@@ -285,8 +311,13 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         const float zv = *reinterpret_cast<const float*>(slot + Cfg::BOPS + rt * 4);
         const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
         const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
-        *reinterpret_cast<uint32_t*>(slot + zoff) =
+        const uint32_t hl =
             static_cast<uint32_t>(__bfloat16_as_ushort(hi)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
+        if constexpr (PAIR) {   // row rt belongs to head rt / 32: columns 64, 65 or 66, 67
+          *reinterpret_cast<uint2*>(slot + zoff) = rt < 32 ? make_uint2(hl, 0u) : make_uint2(0u, hl);
+        } else {
+          *reinterpret_cast<uint32_t*>(slot + zoff) = hl;
+        }
       }
       if (++kb == Cfg::NB) { kb = 0; bph ^= 1u; }
       for (int c = 0; c < g.chunks; ++c) {
@@ -329,12 +360,14 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(tempty + acc);
-        const float inv = 1.0f / (__uint_as_float(vz[0]) + __uint_as_float(vz[1]) + eps);
+        const float inv0 = 1.0f / (__uint_as_float(vz[0]) + __uint_as_float(vz[1]) + eps);
+        const float inv1 = PAIR ? 1.0f / (__uint_as_float(vz[2]) + __uint_as_float(vz[3]) + eps) : inv0;
         // the MMA has finished reading the q tile: the output row goes in its place
         uint8_t* orow = qst + cs * Cfg::QT + row * Cfg::ROWB;
 #pragma unroll
         for (int q = 0; q < D / 8; ++q) {
           const uint32_t* src = (q < 4) ? (v0 + 8 * q) : (v1 + 8 * (q - 4));
+          const float inv = q < 4 ? inv0 : inv1;
           const uint4 packed = make_uint4(
               pack_bf16(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv),
               pack_bf16(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv),
@@ -344,7 +377,7 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         }
         fence_proxy_async_smem();
         mbar_arrive(ostore + cs);
-        if (D == 64 && c + 1 == g.chunks) {
+        if (D == 64 && !PAIR && c + 1 == g.chunks) {
           // the item's last MMA has read its S~ tile and z~ (each read once, by this
           // CTA): their lines leave L2 without a write-back (measured slower at d = 32)
           const int64_t tile = ((item / g.H) / g.M * g.H + item % g.H) * g.M + (item / g.H) % g.M;
@@ -366,46 +399,62 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 
 // ----------------------------------------------------------------- host side
 
-template <int D>
+template <int D, bool PAIR>
 int run_output(const Problem& p, const __nv_bfloat16* St, const float* zt, cudaStream_t stream) {
   using Cfg = OutCfg<D>;
   const int sms = device_sm_count();
   if (sms <= 0) return MHLA_ERR_CUDA;
+  // PAIR: the problem seen with heads of 64 channels, two real heads each
+  Problem v = p;
+  if (PAIR) {
+    v.d = 64;
+    v.H = p.H / 2;
+    v.q.sh = 2 * p.q.sh;
+    v.o.sh = 2 * p.o.sh;
+  }
   ChunkPlan c128;
-  if (!chunk_plan(p, 128, &c128)) return MHLA_ERR_UNSUPPORTED;
+  if (!chunk_plan(v, 128, &c128)) return MHLA_ERR_UNSUPPORTED;
   CUtensorMap tq, to;
-  if (!operand_map(p, p.q, c128.box_y, c128.box_t, &tq) || !operand_map(p, p.o, c128.box_y, c128.box_t, &to))
+  if (!operand_map(v, v.q, c128.box_y, c128.box_t, &tq) || !operand_map(v, v.o, c128.box_y, c128.box_t, &to))
     return MHLA_ERR_CUDA;
   // S~ tiles (row-major [BH*M][d][d]) seen as (c % 8, r, c / 8, tile): a
   // (8, d, d/8, 1) box lands as 16-byte rows of 8 columns, d rows per column
-  // group: the unswizzled MN-major operand layout.
+  // group: the unswizzled MN-major operand layout (PAIR: one column group per box).
   CUtensorMap tst;
   {
     const cuuint64_t dims[4] = {8u, static_cast<cuuint64_t>(p.d), static_cast<cuuint64_t>(p.d / 8),
                                 static_cast<cuuint64_t>(p.BH() * p.M)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(p.d * 2), 16u, static_cast<cuuint64_t>(p.d * p.d * 2)};
-    const cuuint32_t box[4] = {8u, static_cast<cuuint32_t>(p.d), static_cast<cuuint32_t>(p.d / 8), 1u};
+    const cuuint32_t box[4] = {8u, static_cast<cuuint32_t>(p.d), PAIR ? 1u : static_cast<cuuint32_t>(p.d / 8), 1u};
     if (!encode_tensor_map(&tst, 4, const_cast<__nv_bfloat16*>(St), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
       return MHLA_ERR_CUDA;
   }
-  const int64_t n_items = p.BH() * p.M;
-  if (cudaFuncSetAttribute(tc_output<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::SMEM)) !=
-      cudaSuccess)
+  const int64_t n_items = v.BH() * v.M;
+  if (cudaFuncSetAttribute(tc_output<D, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(Cfg::SMEM)) != cudaSuccess)
     return MHLA_ERR_CUDA;
-  const int per_sm = std::max(1, std::min(occupancy(tc_output<D>, kOutThreadsTC, Cfg::SMEM), 512 / Cfg::TMEM_COLS));
+  const int per_sm =
+      std::max(1, std::min(occupancy(tc_output<D, PAIR>, kOutThreadsTC, Cfg::SMEM), 512 / Cfg::TMEM_COLS));
   const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
   KernelTimer timer("tc_output", stream);
-  tc_output<D><<<grid, kOutThreadsTC, Cfg::SMEM, stream>>>(tq, to, tst, make_geom(p, c128), n_items, p.phi_kind, p.eps,
-                                                            zt, St);
+  tc_output<D, PAIR><<<grid, kOutThreadsTC, Cfg::SMEM, stream>>>(tq, to, tst, make_geom(v, c128), n_items,
+                                                                  p.phi_kind, p.eps, zt, St);
   return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
 }
 
 }  // namespace
 
+// d = 32 with an even number of adjacent heads reads out head pairs as 64-channel rows.
+bool output_pairs_heads(const Problem& p) {
+  return p.d == 32 && p.H % 2 == 0 && p.q.sh == 32 && p.o.sh == 32 && operand_tma_ok(p, p.q) &&
+         operand_tma_ok(p, p.o);
+}
+
 int tc_run_output(const Problem& p, const void* St, const float* zt, void* stream) {
   auto* st = static_cast<const __nv_bfloat16*>(St);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return p.d == 64 ? run_output<64>(p, st, zt, s) : run_output<32>(p, st, zt, s);
+  if (p.d == 64) return run_output<64, false>(p, st, zt, s);
+  return output_pairs_heads(p) ? run_output<64, true>(p, st, zt, s) : run_output<32, false>(p, st, zt, s);
 }
 
 int read_and_clear_output_error(void* stream, uint32_t* flags) { return read_and_clear_word(g_out_error, stream, flags); }
