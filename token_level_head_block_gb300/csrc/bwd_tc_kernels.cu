@@ -894,12 +894,11 @@ tc_bwd_key(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
 // ============================================================================
 // tc_dw: part[s][i][j] = sum over the column groups of split s of
 //        dSbuf[i][col] Sbuf[j][col]   (both [G][M][128] bf16, K-major tiles)
-// One CTA per (i tile of 128, j tile of up to 256, split).  Warp 0 loads
-// 64-column halves of a group into a 4-stage ring, warp 1 issues the MMAs,
-// warps 4-7 write the float32 tile.
+// One CTA per (i tile of 256 as two 128-row MMA halves, so each j row of S is
+// read once for both; j tile of up to 256; split of the column groups).  Warp 0
+// loads 64-column halves of a group into a 3-stage ring, warp 1 issues the MMAs,
+// warps 4-7 write the float32 tile with 16-byte stores.
 // ============================================================================
-// One CTA: 256 rows i (two 128-row MMA halves, so each j row of S is read once
-// for both), up to 256 rows j, and a slice of the summary columns.
 struct DwCfg {
   static constexpr int IT = 256;                  // rows i per tile (two MMA M halves)
   static constexpr int JT = 256;                  // rows j per tile (MMA N, at most)

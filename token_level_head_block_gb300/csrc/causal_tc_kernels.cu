@@ -24,10 +24,10 @@
 // accumulator (A = the whole phi(Q) tile, each row reads its own unit's), so
 // the state MMAs run while the workers form P.
 //
-// tc_causal_tile: persistent CTAs, warp 8 issues TMA and MMAs, warps 0-7
-// (two warpgroups) apply phi, form P and write the output.  q, k, v tiles and
-// the state tiles are double-buffered (the next tile's loads run while the
-// current one computes).  Every wait is bounded; a wait that gives up sets
+// tc_causal_tile: persistent CTAs; warp 9 issues the TMA loads, warp 8 the
+// MMAs, warps 0-7 (two warpgroups) apply phi, form P and write the output, one
+// tile ahead (phi and the scores of the next tile run under this tile's MMAs and
+// output).  q, k, v tiles and the state tiles are double-buffered.  Every wait is bounded; a wait that gives up sets
 // bit 0 of this file's device error word and an abort flag, the CTA drains
 // what it issued and releases tensor memory.
 #include <cuda.h>
