@@ -145,6 +145,10 @@ __device__ __forceinline__ void tma_store_5d(const void* tmap, const void* src, 
       : "memory");
 }
 
+// Waits until the grids this one depends on (launched before it on the stream,
+// with programmatic serialization) have completed and their writes are visible.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Drops a 128-byte L2 line without writing it back (its contents become
 // undefined): for a scratch buffer whose last reader is done with it.
 __device__ __forceinline__ void discard_l2_line(const void* p) {

@@ -9,6 +9,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "mhla_internal.h"
 #include "ptx.cuh"
 #include "tma_host.h"
@@ -107,6 +109,25 @@ static __device__ __forceinline__ int swz(int row) {
 }
 
 // ----------------------------------------------------------------- host side
+
+// Launch with programmatic stream serialization: the grid may start while the
+// previous kernel on the stream drains (its CTAs take SMs as they free up); the
+// threads that read the previous kernel's results call grid_dep_wait() first.
+template <typename... Params, typename... Args>
+static cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 template <typename K>
 int occupancy(K kernel, int threads, size_t smem) {

@@ -106,6 +106,7 @@ tc_mix(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtenso
   // columns run side by side and share them in L2.
   if (warp == 0) {
     if (lane == 0) {
+      grid_dep_wait();   // W in bf16 and Sbuf come from the summary launch
       const uint64_t pol_w = policy_evict_last();
       const uint64_t pol_s = policy_evict_first();
       int s = 0;
@@ -298,6 +299,7 @@ tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
 
   if (warp == 0) {
     if (lane == 0) {
+      grid_dep_wait();   // W in bf16 and Sbuf come from the summary launch
       const uint64_t pol_w = policy_evict_last();
       const uint64_t pol_s = policy_evict_first();
       // all of W once: chunk kc holds rows i < NP (rows >= M read as zeros) of source blocks kc*64 ..
@@ -441,10 +443,10 @@ int run_mix(const Problem& p, const __nv_bfloat16* Wm, int64_t Mp, const __nv_bf
       return MHLA_ERR_CUDA;
     const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
     KernelTimer timer("tc_mix", stream);
-    tc_mix_resident<D><<<grid, kMixThreadsTC, MixResCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), NP,
-                                                                          ncols, n_tiles, St, zt,
-                                                                          discard_input ? Sbuf : nullptr);
-    return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+    const cudaError_t e = launch_dependent(tc_mix_resident<D>, dim3(grid), dim3(kMixThreadsTC), MixResCfg::SMEM,
+                                           stream, tw, ts, static_cast<int32_t>(p.M), NP, ncols, n_tiles, St, zt,
+                                           discard_input ? Sbuf : static_cast<const __nv_bfloat16*>(nullptr));
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
   }
   CUtensorMap tw, ts;
   const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(MixCfg::KC), static_cast<cuuint32_t>(MixCfg::ROWS)};
@@ -460,8 +462,9 @@ int run_mix(const Problem& p, const __nv_bfloat16* Wm, int64_t Mp, const __nv_bf
   const int64_t n_tiles = static_cast<int64_t>(n_col_tiles) * n_i_tiles;
   const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
   KernelTimer timer("tc_mix", stream);
-  tc_mix<D><<<grid, kMixThreadsTC, MixCfg::SMEM, stream>>>(tw, ts, static_cast<int32_t>(p.M), ncols, n_col_tiles,
-                                                            n_i_tiles, St, zt);
+  const cudaError_t e = launch_dependent(tc_mix<D>, dim3(grid), dim3(kMixThreadsTC), MixCfg::SMEM, stream, tw, ts,
+                                         static_cast<int32_t>(p.M), ncols, n_col_tiles, n_i_tiles, St, zt);
+  if (e != cudaSuccess) return MHLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
 }
 

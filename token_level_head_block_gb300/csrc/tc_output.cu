@@ -185,6 +185,7 @@ tc_output(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     // bulk copy behind it.  Nothing here waits on a load, so the producer runs
     // up to NB items ahead.
     if (lane == 0) {
+      grid_dep_wait();   // S~ and z~ come from the mixing launch
       const uint64_t pol_s = policy_evict_last();
       int kb = 0;
       uint32_t bph = 0;
@@ -437,8 +438,9 @@ int run_output(const Problem& p, const __nv_bfloat16* St, const float* zt, cudaS
       std::max(1, std::min(occupancy(tc_output<D, PAIR>, kOutThreadsTC, Cfg::SMEM), 512 / Cfg::TMEM_COLS));
   const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
   KernelTimer timer("tc_output", stream);
-  tc_output<D, PAIR><<<grid, kOutThreadsTC, Cfg::SMEM, stream>>>(tq, to, tst, make_geom(v, c128), n_items,
-                                                                  p.phi_kind, p.eps, zt, St);
+  const cudaError_t e = launch_dependent(tc_output<D, PAIR>, dim3(grid), dim3(kOutThreadsTC), Cfg::SMEM, stream, tq,
+                                         to, tst, make_geom(v, c128), n_items, p.phi_kind, p.eps, zt, St);
+  if (e != cudaSuccess) return MHLA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
 }
 
