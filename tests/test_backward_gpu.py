@@ -39,7 +39,7 @@ def log(case, **kw):
 def dw_term_scale(q, k, v, W, g, grid, block, phi_kind, eps):
     """max over (i, j) of sum_{b,h} sum |dS~_i| |S_j| + |dz~_i| |z_j|: the size of
     the terms dW[i][j] adds up.  With one block dW is O(eps) times this (o does
-    not depend on a lone W except through eps), so bf16 operands are judged
+    not depend on a lone W except through eps), so bf16 operands are measured
     against the terms, not against dW's own near-zero value."""
     S, z = oracle.summaries(k, v, grid, block, phi_kind, eps)
     St, zt = oracle.mix(W, S, z)
