@@ -341,3 +341,23 @@ def test_causal_rejects_malformed_requests_before_any_launch(L):
                                         ctypes.byref(mhla.shape3((8, 8))), 0, ctypes.byref(n)) == SHAPE
     e = four(0, 1024, 3, 64)
     assert call_causal(L, *e, (32, 32), (8, 32)) == OK                         # empty batch: nothing queued
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    """With the library absent the binding raises on first use; it has no other
+    path to fall back on (the package never imports the oracle)."""
+    monkeypatch.setattr(mhla, "_lib", None)
+    monkeypatch.setattr(mhla, "_LIB_PATH", str(tmp_path / "libmhla.so"))
+    with pytest.raises(mhla.MhlaError, match="missing"):
+        mhla.lib()
+    with pytest.raises(mhla.MhlaError):
+        mhla.init_mixing((16, 16), (4, 4))
+
+
+def test_package_sources_never_import_the_oracle():
+    pkg = os.path.join(ROOT, "token_level_head_block_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith(".py"):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), fn
