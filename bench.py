@@ -244,6 +244,14 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
+def runs_of(n, total, what):
+    """How many oracle runs a timed sample made over `total` units named `what`
+    (the sampler cycles through them, so n may exceed total)."""
+    if n <= total:
+        return f"{n} of the {total} {what}"
+    return f"{n} runs cycling over the {total} {what}"
+
+
 def oracle_sample_rate(wl, q, k, v, W, budget_s, max_slices=None, g=None, causal=False):
     """Times the oracle (the backward oracle when dout g is given) on (b, h)
     slices until budget_s elapses (at least one slice).  Returns (tokens/s,
@@ -530,15 +538,15 @@ def run_ours(args, wl):
     if rank == 0 and world == 1 and not args.no_cpu_baseline and module:
         rate, n, el = oracle_module_rate(wl, x_h, params_h, W_h.astype("float64"), args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{n} of the {wl.B} batch elements of {wl.name} in {el:.1f} s, float64 numpy module "
-                         "oracle"}
+               "sample": f"{runs_of(n, wl.B, 'batch elements')} of {wl.name} in {el:.1f} s, float64 numpy "
+                         "module oracle"}
     elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, n, el = oracle_sample_rate(wl, q_h, k_h, v_h, W_h, args.cpu_seconds, g=g_h,
                                          causal=args.pass_ == "causal")
         what = {"forward": "oracle (blocked form)", "backward": "backward oracle",
                 "causal": "causal oracle"}[args.pass_]
         cpu = {"value": rate, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{n} of the {wl.B * wl.H} (batch, head) slices of {wl.name} in {el:.1f} s, "
+               "sample": f"{runs_of(n, wl.B * wl.H, '(batch, head) slices')} of {wl.name} in {el:.1f} s, "
                          f"float64 numpy {what}; a slice counts N/H tokens"}
 
     launches = sum(n for n, _ in prof.values())
