@@ -133,3 +133,40 @@ def test_module_rejects_bad_shapes():
     W = torch.ones(1, 1, device=DEV)
     with pytest.raises(mhla.MhlaError):
         mhla.module_forward(x, p, W, (8, 8), (8, 8), 2)
+
+
+def test_module_refuses_before_any_launch():
+    """A request the core refuses (here W inside the buffer the core writes)
+    is turned down before the LayerNorm or the projection runs: the workspace
+    comes back untouched."""
+    B, grid, block, heads, d = 1, (16, 16), (4, 4), 2, 32
+    N, C = 256, 64
+    x = draw_tokens(B, N, C, seed=8).to(DEV)
+    p = {k: t.to(DEV) for k, t in draw_module_params(C, seed=9).items()}
+    ws = torch.full((mhla.module_workspace_size(B, N, C, heads, grid, block),), 0x5A, dtype=torch.uint8, device=DEV)
+    M = mhla.num_blocks(grid, block)
+    W_inside = ws[:M * M * 4].view(torch.float32)       # overlaps the normalised input / core output buffer
+    with pytest.raises(mhla.MhlaError) as e:
+        mhla.module_forward(x, p, W_inside, grid, block, heads, workspace=ws)
+    assert e.value.status == 1
+    torch.cuda.synchronize()
+    assert bool((ws == 0x5A).all())
+
+
+def test_lepe_add_many_frames():
+    """More (frame, channel chunk) tiles than a 16-bit grid axis holds: the
+    persistent kernel walks them with a 64-bit tile index."""
+    B, grid, H, d = 22000, (2, 3), 3, 64          # 22000 frames x 3 channel chunks = 66000 tiles
+    N, C = 6, 192
+    rng = np.random.default_rng(23)
+    v = draw_tokens(B, N, C, seed=24)
+    o = draw_tokens(B, N, C, seed=25)
+    o_dev = o.to(DEV).view(B, N, H, d)
+    w = torch.from_numpy((0.2 * rng.standard_normal((C, 5, 5))).astype(np.float32))
+    bias = torch.from_numpy((0.1 * rng.standard_normal(C)).astype(np.float32))
+    mhla.lepe_add(v.to(DEV).view(B, N, H, d), o_dev, grid, w.to(DEV), bias.to(DEV))
+    torch.cuda.synchronize()
+    got = as_f64(o_dev.cpu()).reshape(B, N, C)
+    for b in (0, 1, 4097, 12345, B - 1):          # frames are independent: a sample against the oracle
+        ref = as_f64(o[b:b + 1]) + oracle.lepe(as_f64(v[b:b + 1]), grid, as_f64(w), as_f64(bias))
+        _bf16_close(got[b:b + 1], ref, abs_=2e-3)

@@ -104,6 +104,14 @@ int build_problem(const mhla_tensor_t* q, const mhla_tensor_t* k, const mhla_ten
   return MHLA_OK;
 }
 
+// W (M x M float32) must not overlap the output the call writes.
+bool w_overlaps_out(const mhla_tensor_t* out, const float* W, int64_t M) {
+  uintptr_t o0, o1;
+  span(out, &o0, &o1);
+  const uintptr_t w0 = reinterpret_cast<uintptr_t>(W);
+  return overlaps(o0, o1, w0, w0 + static_cast<uintptr_t>(M * M) * sizeof(float));
+}
+
 // AUTO: the fused short-sequence kernel, else the three tensor-core launches,
 // else the CUDA cores.
 int auto_path(const Problem& p) {
@@ -177,12 +185,7 @@ extern "C" mhla_status_t mhla_forward(const mhla_tensor_t* q, const mhla_tensor_
   if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
   if (p.B == 0 || p.H == 0) return MHLA_OK;
   if (!W) return MHLA_ERR_INVALID_ARG;
-  {
-    uintptr_t o0, o1;
-    span(out, &o0, &o1);
-    const uintptr_t w0 = reinterpret_cast<uintptr_t>(W);
-    if (overlaps(o0, o1, w0, w0 + static_cast<uintptr_t>(p.M * p.M) * sizeof(float))) return MHLA_ERR_INVALID_ARG;
-  }
+  if (w_overlaps_out(out, W, p.M)) return MHLA_ERR_INVALID_ARG;
   const size_t need = workspace_for(p, sel);
   void* ws = workspace;
   if (!ws && workspace_bytes != 0) return MHLA_ERR_WORKSPACE;
@@ -368,12 +371,7 @@ extern "C" mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_
   if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
   if (p.B == 0 || p.H == 0) return MHLA_OK;
   if (!W) return MHLA_ERR_INVALID_ARG;
-  {
-    uintptr_t o0, o1;
-    span(out, &o0, &o1);
-    const uintptr_t w0 = reinterpret_cast<uintptr_t>(W);
-    if (overlaps(o0, o1, w0, w0 + static_cast<uintptr_t>(p.M * p.M) * sizeof(float))) return MHLA_ERR_INVALID_ARG;
-  }
+  if (w_overlaps_out(out, W, p.M)) return MHLA_ERR_INVALID_ARG;
   const size_t need = causal_workspace_for(p, sel);
   void* ws = workspace;
   if (!ws && workspace_bytes != 0) return MHLA_ERR_WORKSPACE;
@@ -472,9 +470,10 @@ int lepe_args(const mhla_tensor_t* v, const mhla_tensor_t* out, const mhla_shape
     span(v, &v0, &v1);
     if (overlaps(o0, o1, v0, v1)) return MHLA_ERR_INVALID_ARG;
   }
-  if (v->H * v->d > (int64_t{1} << 30) || T * Y * X > (int64_t{1} << 40) || v->B * T * ((v->H * v->d + 63) / 64) >= 65536 ||
-      (X + 15) / 16 >= (int64_t{1} << 31) || (Y + 7) / 8 >= 65536)
-    return MHLA_ERR_UNSUPPORTED;
+  // The kernel keeps channels, frames, rows and columns in 32 bits (TMA
+  // coordinates) and the tile index in 64.
+  const int64_t lim32 = int64_t{1} << 30;
+  if (v->H * v->d > lim32 || v->B >= lim32 || T >= lim32 || Y >= lim32 || X >= lim32) return MHLA_ERR_UNSUPPORTED;
   a->v = v->data;
   a->o = out->data;
   a->vsb = v->stride_b; a->vsn = v->stride_n; a->vsh = v->stride_h;
@@ -524,7 +523,7 @@ int module_check(int64_t B, int64_t N, int64_t C, int32_t heads, const mhla_shap
   if (rg != MHLA_OK) return rg;
   const int64_t M = mhla_num_blocks(grid, block);
   if (M < 0) return static_cast<int>(-M);
-  if (B * N >= (int64_t{1} << 40)) return MHLA_ERR_UNSUPPORTED;
+  if (B * N >= (int64_t{1} << 40) || (B * N + 7) / 8 >= (int64_t{1} << 31)) return MHLA_ERR_UNSUPPORTED;
   return MHLA_OK;
 }
 
@@ -628,18 +627,23 @@ extern "C" mhla_status_t mhla_module_forward(const void* x, void* y, int64_t B, 
   const int64_t R = B * N;
   mhla_tensor_t q, k, v, o;
   module_views(qkv, abuf, B, N, C, params->heads, &q, &k, &v, &o);
-  int r = launch_layer_norm(x, abuf, R, static_cast<int32_t>(C), params->ln_weight, params->ln_bias, params->ln_eps,
-                            stream);
+  // The core's and the positional term's checks run on these views before the
+  // first launch, so a request either of them refuses queues nothing.
+  Problem core;
+  int r = build_problem(&q, &k, &v, &o, grid, block, phi, /*check_alias=*/true, &core);
+  if (r == MHLA_OK && w_overlaps_out(&o, W, core.M)) r = MHLA_ERR_INVALID_ARG;
+  LepeArgs lepe = {};
+  if (r == MHLA_OK && params->lepe_weight)
+    r = lepe_args(&v, &o, grid, params->lepe_weight, params->lepe_bias, &lepe);
+  if (r == MHLA_OK)
+    r = launch_layer_norm(x, abuf, R, static_cast<int32_t>(C), params->ln_weight, params->ln_bias, params->ln_eps,
+                          stream);
   if (r == MHLA_OK)
     r = launch_linear("cublaslt_qkv", abuf, params->qkv_weight, params->qkv_bias, qkv, R, C, 3 * C, base + L.lt_off, stream);
   if (r == MHLA_OK)
     r = mhla_forward(&q, &k, &v, W, grid, block, phi, &o, base + L.core_off, L.lt_off - L.core_off, stream,
                      MHLA_PATH_AUTO);
-  if (r == MHLA_OK && params->lepe_weight) {
-    LepeArgs a = {};
-    r = lepe_args(&v, &o, grid, params->lepe_weight, params->lepe_bias, &a);
-    if (r == MHLA_OK) r = launch_lepe_add(a, stream);
-  }
+  if (r == MHLA_OK && params->lepe_weight) r = launch_lepe_add(lepe, stream);
   if (r == MHLA_OK) r = launch_linear("cublaslt_out", abuf, params->out_weight, params->out_bias, y, R, C, C, base + L.lt_off, stream);
   if (owned && cudaFreeAsync(ws, s) != cudaSuccess && r == MHLA_OK) return MHLA_ERR_CUDA;
   return static_cast<mhla_status_t>(r);
