@@ -55,3 +55,29 @@ def test_clock_summary_flags_throttling():
     s = bench.summarize_clocks(rows)
     assert s["sm_mhz"] == 1900 and s["sm_max_mhz"] == 2070 and s["samples"] == 3
     assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+
+
+@pytest.mark.parametrize("pass_", ["forward", "backward", "causal", "module"])
+def test_reference_arm_prints_one_contract_line(pass_):
+    """`--impl reference` times the oracle on the host alone and prints one JSON
+    line with the keys the benchmark contract names."""
+    import json
+    import subprocess
+    import sys
+    wl = "lm_causal_4096" if pass_ == "causal" else "tiny_16x16_fp32"
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--pass", pass_,
+                        "--workload", wl, "--steps", "2", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3
+    assert line["value"] > 0 and line["unit"] == "tokens/s" and line["config"]["workload"] == wl
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
