@@ -270,8 +270,7 @@ struct LtApi {
   decltype(&cublasLtMatmulPreferenceDestroy) pref_destroy = nullptr;
   decltype(&cublasLtMatmulAlgoGetHeuristic) heuristic = nullptr;
   decltype(&cublasLtMatmul) matmul = nullptr;
-  cublasLtHandle_t handle = nullptr;
-  bool ok = false;
+  bool ok = false;   // every entry point found
 };
 
 const LtApi& lt_api() {
@@ -298,10 +297,23 @@ const LtApi& lt_api() {
                sym(api.pref_set, "cublasLtMatmulPreferenceSetAttribute") &&
                sym(api.pref_destroy, "cublasLtMatmulPreferenceDestroy") &&
                sym(api.heuristic, "cublasLtMatmulAlgoGetHeuristic") && sym(api.matmul, "cublasLtMatmul");
-    if (!all) return;
-    api.ok = api.create(&api.handle) == CUBLAS_STATUS_SUCCESS;
+    api.ok = all;
   });
   return api;
+}
+
+// One cuBLASLt handle per device, created on first use with that device
+// current; null when the device cannot be used.
+cublasLtHandle_t lt_handle() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static cublasLtHandle_t handles[kMaxDevices] = {};
+  const LtApi& lt = lt_api();
+  int dev = -1;
+  if (!lt.ok || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!handles[dev] && lt.create(&handles[dev]) != CUBLAS_STATUS_SUCCESS) handles[dev] = nullptr;
+  return handles[dev];
 }
 
 constexpr size_t kLtWorkspace = size_t{32} << 20;
@@ -312,7 +324,8 @@ constexpr size_t kLtWorkspace = size_t{32} << 20;
 int linear_bf16(const char* name, const void* x, const void* W, const void* bias, void* y, int64_t rows, int64_t k,
                 int64_t n_out, void* lt_ws, cudaStream_t stream) {
   const LtApi& lt = lt_api();
-  if (!lt.ok) return MHLA_ERR_UNSUPPORTED;
+  const cublasLtHandle_t handle = lt_handle();
+  if (!handle) return MHLA_ERR_UNSUPPORTED;
   cublasLtMatmulDesc_t op = nullptr;
   cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
   cublasLtMatmulPreference_t pref = nullptr;
@@ -339,13 +352,13 @@ int linear_bf16(const char* name, const void* x, const void* W, const void* bias
     if (lt.pref_set(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb, sizeof(wsb)) != CUBLAS_STATUS_SUCCESS) break;
     cublasLtMatmulHeuristicResult_t res{};
     int found = 0;
-    if (lt.heuristic(lt.handle, op, la, lb, lc, lc, pref, 1, &res, &found) != CUBLAS_STATUS_SUCCESS || found < 1) {
+    if (lt.heuristic(handle, op, la, lb, lc, lc, pref, 1, &res, &found) != CUBLAS_STATUS_SUCCESS || found < 1) {
       rc = MHLA_ERR_UNSUPPORTED;
       break;
     }
     const float alpha = 1.0f, beta = 0.0f;
     KernelTimer timer(name, stream);
-    if (lt.matmul(lt.handle, op, &alpha, W, la, x, lb, &beta, y, lc, y, lc, &res.algo, lt_ws, kLtWorkspace, stream) !=
+    if (lt.matmul(handle, op, &alpha, W, la, x, lb, &beta, y, lc, y, lc, &res.algo, lt_ws, kLtWorkspace, stream) !=
         CUBLAS_STATUS_SUCCESS)
       break;
     rc = MHLA_OK;
@@ -397,13 +410,10 @@ int launch_lepe_add(const LepeArgs& a, void* stream) {
   g.ntx = (a.X + kLpTX - 1) / kLpTX;
   g.nty = (a.Y + kLpTY - 1) / kLpTY;
   g.ntiles = static_cast<int64_t>((a.C + 63) / 64) * a.B * a.T * g.nty * g.ntx;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(mhla_lepe_add, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kLpSmem)) !=
-        cudaSuccess)
-      return MHLA_ERR_CUDA;
-    attr = true;
-  }
+  // a per-device setting: made on every call, for whichever device is current
+  if (cudaFuncSetAttribute(mhla_lepe_add, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kLpSmem)) !=
+      cudaSuccess)
+    return MHLA_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return MHLA_ERR_CUDA;
   const int grid = static_cast<int>(std::min<int64_t>(g.ntiles, 2 * static_cast<int64_t>(sms)));
@@ -421,7 +431,7 @@ int launch_linear(const char* name, const void* x, const void* W, const void* bi
   return linear_bf16(name, x, W, bias, y, rows, k, n_out, lt_ws, static_cast<cudaStream_t>(stream));
 }
 
-bool linear_available() { return lt_api().ok; }
+bool linear_available() { return lt_handle() != nullptr; }
 
 size_t linear_workspace_bytes() { return kLtWorkspace; }
 
