@@ -27,4 +27,5 @@ from .mhla_oracle import (  # noqa: F401
 )
 from .mhla_backward import backward, phi_derivative  # noqa: F401,E402
 from .mhla_causal import blocks_are_contiguous, forward_causal, forward_causal_dense  # noqa: F401,E402
+from .mhla_causal_backward import backward_causal, backward_causal_dense  # noqa: F401,E402
 from .mhla_module import LEPE_K, LN_EPS, layer_norm, lepe, linear, module_forward  # noqa: F401,E402
