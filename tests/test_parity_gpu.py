@@ -33,6 +33,17 @@ def normwise(got, ref):
     return float(np.abs(got - ref).max() / np.abs(ref).max())
 
 
+def error_report(got, ref):
+    """The bar (normwise) with two views of the whole error distribution: the
+    relative Frobenius error and the elementwise 99.9th percentile of
+    |got - ref|, both against the same scale max |ref|."""
+    diff = np.abs(got - ref)
+    scale = np.abs(ref).max()
+    return {"normwise": float(diff.max() / scale),
+            "frobenius": float(np.linalg.norm(diff.ravel()) / np.linalg.norm(ref.ravel())),
+            "p999": float(np.percentile(diff, 99.9) / scale)}
+
+
 def log(case, **kw):
     path = os.environ.get("MHLA_PARITY_LOG")
     if path:
@@ -52,8 +63,9 @@ def check_full(case, q, k, v, W, grid, block, dtype, phi="relu", eps=1e-6, path=
     out = run(q, k, v, W, grid, block, phi, eps, path)
     assert out.dtype == q.dtype
     ref = oracle.forward(as_f64(q), as_f64(k), as_f64(v), W, grid, block, PHI[phi], eps)
-    err = normwise(as_f64(out), ref)
-    log(case, err=err, path=path, dtype=dtype)
+    rep = error_report(as_f64(out), ref)
+    err = rep["normwise"]
+    log(case, err=err, path=path, dtype=dtype, **rep)
     assert err <= TOL[dtype], f"{case}: normwise error {err:.3e}"
     return err
 
@@ -235,15 +247,16 @@ def test_workload_parity(name, samples):
     W = mhla.init_mixing(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
     out = as_f64(run(q, k, v, W, wl.grid, wl.block, wl.phi, wl.eps).cpu())
     pairs = [(b, h) for b in range(wl.B) for h in range(wl.H)] if samples is None else sample_bh(wl.B, wl.H, samples)
-    worst = 0.0
+    worst = {"normwise": 0.0, "frobenius": 0.0, "p999": 0.0}
     for b, h in pairs:
         sl = (slice(b, b + 1), slice(None), slice(h, h + 1), slice(None))
         ref = oracle.forward(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, wl.grid, wl.block,
                              PHI[wl.phi], wl.eps)
-        err = normwise(out[sl], ref)
-        worst = max(worst, err)
+        rep = error_report(out[sl], ref)
+        worst = {key: max(worst[key], rep[key]) for key in worst}
+        err = rep["normwise"]
         assert err <= TOL[wl.dtype], f"{name} (b={b}, h={h}): normwise error {err:.3e}"
-    log(f"workload/{name}", err=worst, pairs=len(pairs))
+    log(f"workload/{name}", err=worst["normwise"], pairs=len(pairs), **worst)
     assert np.isfinite(out).all()
 
 
