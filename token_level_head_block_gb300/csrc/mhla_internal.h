@@ -128,7 +128,8 @@ int read_and_clear_device_error(void* stream, uint32_t* flags);
 int read_and_clear_small_error(void* stream, uint32_t* flags);
 
 // Brackets one kernel launch with CUDA events on its stream while
-// mhla_profile_begin/end collection is active; a no-op otherwise.
+// mhla_profile_begin/end collection is active, and always with an NVTX range
+// named after the kernel (free when no profiler is attached).
 class KernelTimer {
  public:
   KernelTimer(const char* name, void* stream);

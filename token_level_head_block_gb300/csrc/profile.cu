@@ -1,5 +1,9 @@
-// Per-kernel CUDA-event timing behind mhla_profile_begin / mhla_profile_end.
+// Per-kernel CUDA-event timing behind mhla_profile_begin / mhla_profile_end,
+// and an NVTX range named after the kernel around every launch (a no-op unless
+// a profiler such as Nsight Systems or Nsight Compute is attached; ncu can then
+// select launches with --nvtx-include).
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 #include <cstring>
@@ -24,6 +28,7 @@ std::vector<Record> g_records;
 }  // namespace
 
 KernelTimer::KernelTimer(const char* name, void* stream) : name_(name), stream_(stream), start_(nullptr) {
+  nvtxRangePushA(name);
   if (!g_active.load(std::memory_order_acquire)) return;
   cudaEvent_t e;
   if (cudaEventCreate(&e) != cudaSuccess) return;
@@ -35,6 +40,7 @@ KernelTimer::KernelTimer(const char* name, void* stream) : name_(name), stream_(
 }
 
 KernelTimer::~KernelTimer() {
+  nvtxRangePop();
   if (!start_) return;
   cudaEvent_t stop;
   if (cudaEventCreate(&stop) != cudaSuccess || cudaEventRecord(stop, static_cast<cudaStream_t>(stream_)) != cudaSuccess) {
