@@ -35,6 +35,7 @@ def test_workspace_holds_the_buffers_of_the_dit_shape():
     (1, 64, 64, 2, (8, 9), (8, 8), SHAPE),            # grid does not hold N tokens
     (1, 64, 64, 2, (8, 8), (3, 8), SHAPE),            # block does not tile the grid
     (-1, 64, 64, 2, (8, 8), (8, 8), INVALID),
+    (1, 1 << 34, 64, 2, (1 << 17, 1 << 17), (1 << 9, 1 << 9), UNSUPPORTED),   # LayerNorm grid past 2^31 CTAs
 ])
 def test_workspace_size_rejects(B, N, C, heads, grid, block, status):
     assert _ws(B, N, C, heads, grid, block)[0] == status
