@@ -348,7 +348,10 @@ mhla_status_t mhla_module_workspace_size(int64_t B, int64_t N, int64_t C, int32_
  * MHLA_PHI_RELU_EPS).  C % 8 == 0, C <= 2048, d = C / heads with d % 8 == 0.
  * workspace as for mhla_forward (NULL with workspace_bytes == 0: stream-ordered
  * allocation).  Asynchronous on stream; returns MHLA_ERR_UNSUPPORTED when
- * cuBLASLt cannot be loaded or has no algorithm for the shapes. */
+ * cuBLASLt cannot be loaded or has no algorithm for the shapes.  The argument
+ * checks of every step (the core's and the positional term's included) run
+ * before the first launch; only cuBLASLt finding no algorithm or a failed
+ * launch can return after earlier steps were queued. */
 mhla_status_t mhla_module_forward(const void* x, void* y, int64_t B, int64_t N, int64_t C,
                                   const mhla_module_params_t* params, const float* W,
                                   const mhla_shape3_t* grid, const mhla_shape3_t* block,
