@@ -361,3 +361,25 @@ def test_package_sources_never_import_the_oracle():
             if fn.endswith(".py"):
                 text = open(os.path.join(dirpath, fn)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), fn
+
+
+def test_noalloc_refuses_oversized_problems_before_touching_the_device(L):
+    """A problem whose scratch exceeds the library's fixed array comes back as
+    MHLA_ERR_WORKSPACE from the host checks alone (were the device consulted
+    first, a machine without one would answer MHLA_ERR_CUDA instead)."""
+    fn = L.mhla_forward_noalloc
+    P = ctypes.POINTER
+    fn.argtypes = [P(mhla.Tensor), P(mhla.Tensor), P(mhla.Tensor), ctypes.c_void_p, P(mhla.Shape3),
+                   P(mhla.Shape3), P(mhla.Phi), P(mhla.Tensor), ctypes.c_void_p, ctypes.c_int32]
+    fn.restype = ctypes.c_int
+    q, k, v, o = four(64, 196, 3, 64)                 # float32 summaries on the CUDA cores: ~313 MB
+    grid, block = mhla.shape3((14, 14)), mhla.shape3((2, 2))
+    need = ctypes.c_size_t(0)
+    assert L.mhla_workspace_size(ctypes.byref(q), ctypes.byref(grid), ctypes.byref(block), 1,
+                                 ctypes.byref(need)) == OK
+    m = re.search(r"#define MHLA_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", open(HEADER).read())
+    assert need.value > int(m.group(1)) << int(m.group(2))
+    st = fn(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.c_void_p(FAKE + (1 << 36)), ctypes.byref(grid),
+            ctypes.byref(block), ctypes.byref(mhla.Phi(0, 1e-6)), ctypes.byref(o), None, 1)
+    assert st == WORKSPACE
+
