@@ -4,8 +4,13 @@ the whole module with its projections) against the float64 module oracle.
 bf16 storage between the steps bounds the agreement: every stored value is
 rounded once to bf16 (relative 2^-9), so element checks take 2^-7 of the value
 plus a small absolute floor, and the module output is held to the 2e-2
-normwise bound of bf16 inputs with float32 accumulation.
+normwise bound of bf16 inputs with float32 accumulation,
+max |y - y_ref| / max |y_ref|, the bar every parity test here uses (the
+relative Frobenius error is logged beside it with MHLA_PARITY_LOG set).
 """
+
+import json
+import os
 
 import numpy as np
 import pytest
@@ -27,7 +32,19 @@ def _bf16_close(got, ref, rel=2.0 ** -7, abs_=1e-3):
 
 
 def _normwise(got, ref):
+    """The parity bar: the largest elementwise error against the largest |ref|."""
+    return float(np.abs(got - ref).max() / np.abs(ref).max())
+
+
+def _frobenius(got, ref):
     return float(np.linalg.norm((got - ref).ravel()) / np.linalg.norm(ref.ravel()))
+
+
+def _log(case, **kw):
+    path = os.environ.get("MHLA_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": case, **kw}) + "\n")
 
 
 @pytest.mark.parametrize("rows,C", [(1, 64), (37, 384), (1000, 256), (129, 1024), (64, 2048), (5, 520)])
@@ -109,8 +126,10 @@ def test_module_forward(name, B, grid, block, heads, d, lepe, biases, transform)
     assert mhla.device_status() == 0
     ref = oracle.module_forward(as_f64(x), {k: as_f64(t) for k, t in p.items()}, W.astype(np.float64), grid,
                                 block, heads, oracle.PHI_RELU_EPS, 1e-6)
-    err = _normwise(as_f64(y.cpu()), ref)
-    assert err < 2e-2, err
+    got = as_f64(y.cpu())
+    err = _normwise(got, ref)
+    _log(f"module_{name}", err=err, frobenius=_frobenius(got, ref))
+    assert err <= 2e-2, f"{name}: normwise error {err:.3e}"
 
 
 def test_module_with_workspace_and_in_place():
