@@ -158,7 +158,8 @@ def load_peaks():
 
 
 # Source files a kernel's code lives in (with the shared inline-PTX header).
-KERNEL_SOURCES = {"tc_summary": "tc_summary.cu", "tc_mix": "tc_mix.cu", "tc_output": "tc_output.cu",
+KERNEL_SOURCES = {"tc_summary": ("tc_summary.cu", "tc_fwd_bodies.cuh"), "tc_mix": ("tc_mix.cu", "tc_fwd_bodies.cuh"),
+                  "tc_output": ("tc_output.cu", "tc_fwd_bodies.cuh"), "tc_fused": ("tc_fused.cu", "tc_fwd_bodies.cuh"),
                   "tc_small": "small_kernels.cu", "simt_summary": "simt_kernels.cu",
                   "simt_mix": "simt_kernels.cu", "simt_output": "simt_kernels.cu",
                   "tc_bwd_query": "bwd_tc_kernels.cu", "tc_bwd_key": "bwd_tc_kernels.cu",
@@ -174,7 +175,8 @@ def kernel_source_digest(kernel):
     code than the current one does not count."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "token_level_head_block_gb300", "csrc")
-    for name in (KERNEL_SOURCES.get(kernel, ""), "ptx.cuh", "tc_common.cuh"):
+    own = KERNEL_SOURCES.get(kernel, ())
+    for name in ((own,) if isinstance(own, str) else tuple(own)) + ("ptx.cuh", "tc_common.cuh"):
         p = os.path.join(csrc, name)
         if name and os.path.exists(p):
             with open(p, "rb") as f:
@@ -205,6 +207,8 @@ def kernel_work(wl, name):
         "tc_output": ("hbm", 2 * io), "simt_output": ("hbm", 2 * io),
         "tc_mix": ("tensor", 2 * M * M * BH * d * (d + 1)), "simt_mix": ("alu", 2 * M * M * BH * d * (d + 1)),
         "tc_small": ("hbm", 4 * io),
+        # the whole forward in one persistent launch: read q, k, v, write o
+        "tc_fused": ("hbm", 4 * io),
         # backward: read q, dout, write dq; read k, v, write dk, dv; dW = dS~ . S^T
         "tc_bwd_query": ("hbm", 3 * io), "simt_bwd_query": ("hbm", 3 * io),
         "tc_bwd_key": ("hbm", 4 * io), "simt_bwd_key": ("hbm", 4 * io),
@@ -415,12 +419,12 @@ def run_ours(args, wl):
             mhla.backward(q, k, v, W, g, wl.grid, wl.block, phi=wl.phi, eps=wl.eps, dq=dq, dk=dk, dv=dv, dW=dW,
                           workspace=ws, stream=stream)
     else:
-        ws = torch.empty(mhla.workspace_size(q, wl.grid, wl.block), dtype=torch.uint8, device=dev)
+        ws = torch.empty(mhla.workspace_size(q, wl.grid, wl.block, args.path), dtype=torch.uint8, device=dev)
 
         def step():
             mhla.forward(q, k, v, W, wl.grid, wl.block, phi=wl.phi, eps=wl.eps, out=out, workspace=ws,
-                         stream=stream)
-    path = mhla.select_path(q, k, v, out, wl.grid, wl.block)
+                         stream=stream, path=args.path)
+    path = mhla.select_path(q, k, v, out, wl.grid, wl.block) if args.path == "auto" else args.path
 
     def timed(n, body):
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -585,6 +589,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU oracle baseline")
     ap.add_argument("--ref-slices", type=int, default=1, help="(batch, head) slices per reference step")
     ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "causal", "module"], default="forward")
+    ap.add_argument("--path", default="auto", choices=["auto", "tc", "tc_fused", "simt", "fused"],
+                    help="forward kernels (auto: what the library picks; tc_fused: the single persistent launch)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

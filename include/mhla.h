@@ -76,13 +76,20 @@ typedef enum mhla_phi_kind {
  *          suits grids with many small blocks (M^2 comparable to N).
  *   TC     three tensor-core launches (summaries, mixing GEMM, readout): bf16,
  *          d in {32, 64}, tokens per block a multiple of 128 in whole block
- *          rows, TMA friendly strides.
- *   SIMT   CUDA cores, any supported request (float32 included). */
+ *          rows (or contiguous 64-token blocks), TMA friendly strides.
+ *   SIMT   CUDA cores, any supported request (float32 included).
+ * TC_FUSED, never taken by AUTO, runs TC's three pipelines in one persistent
+ * launch (M <= 256, tokens per block a multiple of 128 in whole block rows):
+ * some CTAs form the block summaries while the others run the mixing GEMM
+ * batch by batch as the summaries arrive, then every CTA reads out.  It gives
+ * TC's results bit for bit; on GB300 it is slower than TC (the summaries need
+ * every SM to draw full HBM bandwidth), so it is kept for measurement. */
 typedef enum mhla_path {
     MHLA_PATH_AUTO = 0,
     MHLA_PATH_SIMT = 1,
     MHLA_PATH_TC = 2,
-    MHLA_PATH_FUSED = 3
+    MHLA_PATH_FUSED = 3,
+    MHLA_PATH_TC_FUSED = 4
 } mhla_path_t;
 
 /* Token grid or block shape, slowest axis first: (Y, X) when ndim == 2,
@@ -201,7 +208,7 @@ mhla_status_t mhla_backward_workspace_size(const mhla_tensor_t* q, const mhla_sh
  *                  {32, 64}, the forward TC path's token geometry and TMA
  *                  friendly strides on q, k, v, dout, dq, dk, dv; SIMT: CUDA
  *                  cores, float32 arithmetic, any d <= 128 and block shape.
- *                  FUSED returns MHLA_ERR_UNSUPPORTED.
+ *                  FUSED and TC_FUSED return MHLA_ERR_UNSUPPORTED.
  * With AUTO, mhla_backward_workspace_size returns enough for either path.
  * Asynchronous on stream; statuses as for mhla_forward.  B == 0 or H == 0
  * writes dW = 0 and nothing else. */
@@ -240,7 +247,7 @@ mhla_status_t mhla_causal_workspace_size(const mhla_tensor_t* q, const mhla_shap
  *     earlier unit of the same block, 0 otherwise), then every 128-token tile
  *     forms its causal scores and its state term in one accumulator.
  *     SIMT: CUDA cores, float32 arithmetic, any d <= 128, bf16 or float32.
- *     FUSED returns MHLA_ERR_UNSUPPORTED.
+ *     FUSED and TC_FUSED return MHLA_ERR_UNSUPPORTED.
  *   With AUTO, mhla_causal_workspace_size returns enough for either path. */
 mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_tensor_t* k,
                                   const mhla_tensor_t* v, const float* W,
@@ -258,15 +265,21 @@ mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_tensor_t* k
  * fail under fragmentation).  The caller still passes q, k, v, W and out; the
  * scratch comes from one array of MHLA_NOALLOC_SCRATCH_BYTES (64 MiB) compiled
  * into the library, which every GPU that loads the library holds until the
- * process exits.  The call allocates nothing: no cudaMalloc, cudaMallocAsync,
- * cudaFree or allocating library routine.
+ * process exits.  After its set-up call (below) the call allocates nothing:
+ * no cudaMalloc, cudaMallocAsync, cudaFree or allocating library routine.
  *   Arguments as for mhla_forward, without workspace and workspace_bytes.
  *   Returns MHLA_ERR_WORKSPACE, before touching the GPU, when the problem needs
  *   more scratch than the array holds (mhla_workspace_size says how much it
  *   needs); other statuses as for mhla_forward.
- *   The first call on a device looks up the array's device address on that
- *   device (cudaGetSymbolAddress, with that device current); make that first
- *   call before any stream capture.
+ *   Set-up: the first call in a CUDA context (per device, and again after a
+ *   device reset, which creates a new context) looks up the array's device
+ *   address there (cudaGetSymbolAddress, with the caller's device current).
+ *   That first lookup loads the library's device code into the context, and
+ *   the driver allocates the array's 64 MiB at that moment -- so the first
+ *   call can fail with MHLA_ERR_CUDA under memory pressure, and it is the one
+ *   call that does allocate, implicitly.  Make it at start-up, before any
+ *   stream capture: a call with B == 0 does the set-up, queues nothing and
+ *   returns MHLA_OK.  Every later call in that context allocates nothing.
  *   Every call on a device shares the one array and leaves its contents
  *   behind; no part of it needs to start at zero: a call writes every scratch
  *   byte whose value reaches its results before reading it (padding it reads

@@ -102,6 +102,46 @@ def test_tensor_core_path_small(name, phi):
 
 
 @pytest.mark.parametrize("name", sorted(TC_CASES))
+def test_tensor_core_single_launch_small(name):
+    """The same cases in one persistent launch (where M <= 256)."""
+    B, H, d, grid, block = TC_CASES[name]
+    N = int(np.prod(grid))
+    q, k, v = draw_qkv(B, N, H, d, seed=11, dtype="bf16")
+    M = oracle.num_blocks(grid, block)
+    W = draw_matrix(M, seed=12)
+    path = "tc_fused" if M <= 256 else "tc"
+    check_full(f"tc_fused/{name}", q, k, v, W, grid, block, "bf16", "relu", 1e-6, path)
+
+
+@pytest.mark.parametrize("name", sorted(TC_CASES))
+def test_single_launch_equals_split_launches_bitwise(name):
+    """The persistent single launch runs the same arithmetic as the three
+    launches (same operands, same MMA order per item and tile), whatever CTA
+    takes which item: the outputs are identical bit for bit, run after run."""
+    B, H, d, grid, block = TC_CASES[name]
+    N = int(np.prod(grid))
+    q, k, v = draw_qkv(B, N, H, d, seed=37, dtype="bf16")
+    W = draw_matrix(oracle.num_blocks(grid, block), seed=38)
+    single = "tc_fused" if oracle.num_blocks(grid, block) <= 256 else "tc"
+    a = run(q, k, v, W, grid, block, path=single).cpu()
+    b = run(q, k, v, W, grid, block, path=single).cpu()
+    c = run(q, k, v, W, grid, block, path="tc").cpu()
+    assert torch.equal(a, b)
+    assert torch.equal(a, c)
+
+
+@pytest.mark.parametrize("B", [1, 7])
+def test_single_launch_batches_straddling_mixing_tiles(B):
+    """Mixing tiles of 128 summary columns that straddle two batches (H (d + 1) d
+    is not a multiple of 128) wait for both batches' summaries and count for
+    both batches' readout."""
+    H, d, grid, block = 5, 32, (16, 32), (8, 16)
+    q, k, v = draw_qkv(B, 512, H, d, seed=39, dtype="bf16")
+    W = draw_matrix(oracle.num_blocks(grid, block), seed=40)
+    check_full(f"tc_straddle/B{B}", q, k, v, W, grid, block, "bf16", "relu", 1e-6, "tc_fused")
+
+
+@pytest.mark.parametrize("name", sorted(TC_CASES))
 def test_simt_path_bf16_small(name):
     B, H, d, grid, block = TC_CASES[name]
     N = int(np.prod(grid))
@@ -260,6 +300,17 @@ def test_workload_parity(name, samples):
     assert np.isfinite(out).all()
 
 
+@pytest.mark.parametrize("name", ["dit_s2_4096px", "sana_4096px", "video_20x32x32"])
+def test_workload_single_launch_equals_split_launches(name):
+    """At full size, in the launch configuration the benchmark times: the single
+    persistent launch and the three launches agree bit for bit."""
+    wl, q, k, v = workload_inputs(name)
+    W = mhla.init_mixing(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
+    a = run(q, k, v, W, wl.grid, wl.block, wl.phi, wl.eps, path="tc_fused")
+    b = run(q, k, v, W, wl.grid, wl.block, wl.phi, wl.eps, path="tc")
+    assert torch.equal(a, b)
+
+
 def test_workload_w_matches_oracle_bitwise_at_large_m():
     for name in ("dit_s2_4096px", "sweep_512x512"):
         wl = WORKLOADS[name]
@@ -345,8 +396,10 @@ def test_profile_reports_every_kernel():
     W = mhla.init_mixing(grid, block, "linear")
     mhla.profile_begin()
     run(q, k, v, W, grid, block, path="tc")
+    run(q, k, v, W, grid, block, path="tc_fused")
     run(q, k, v, W, grid, block, path="simt")
     run(q, k, v, W, grid, block, path="fused")
     prof = mhla.profile_end()
-    for name in ("tc_summary", "tc_mix", "tc_output", "simt_summary", "simt_mix", "simt_output", "tc_small"):
+    for name in ("tc_fused", "tc_summary", "tc_mix", "tc_output", "simt_summary", "simt_mix", "simt_output",
+                 "tc_small"):
         assert prof[name][0] == 1 and prof[name][1] > 0.0, name

@@ -4,11 +4,16 @@ It exists for callers that may not allocate device memory where they run the
 forward (an inference engine's plugin inside the engine's enqueue step, a serving
 loop that fixes its memory at start-up): it takes its scratch from a 64 MiB array
 compiled into the library instead of a caller workspace or cudaMallocAsync.
-Its output must match the regular entry point's within the parity tolerance, on
-two calls in a row with different inputs (the shared scratch carries nothing from
-one call to the next), and a problem needing more scratch than the array holds
-must be refused before any GPU work.  This file is collected last and needs
-nothing from the other tests.
+
+The first call in a context is its set-up (it loads the array there); a call
+with an empty batch does exactly that and nothing else, and is made first, as a
+caller would at start-up.  The output must then match the float64 oracle at the
+parity bar and the regular entry point within the same bar, on two calls in a
+row with different inputs (the shared scratch carries nothing from one call to
+the next).  The CUDA-core cases run before the tensor-core case, so the
+tensor-core call reads over scratch bytes another layout left behind.  A problem
+needing more scratch than the array holds must be refused before any GPU work.
+This file is collected last and needs nothing from the other tests.
 """
 
 import ctypes
@@ -17,6 +22,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import token_level_head_block_gb300 as mhla
 from token_level_head_block_gb300.synth import as_f64, draw_matrix, draw_qkv
 
@@ -49,30 +55,47 @@ def call_noalloc(q, k, v, W, grid, block, out, path="auto"):
                         mhla.PATHS[path])
 
 
-def normwise(a, b):
-    a, b = as_f64(a.cpu()), as_f64(b.cpu())
-    return float(np.abs(a - b).max() / np.abs(b).max())
+def normwise(got, ref):
+    return float(np.abs(got - ref).max() / np.abs(ref).max())
+
+
+def test_noalloc_set_up_call_with_an_empty_batch():
+    """The start-up call a caller makes: B = 0 sets the array up and queues nothing."""
+    grid, block, H, d = (16, 16), (4, 4), 2, 32
+    q = torch.empty(0, 256, H, d, dtype=torch.float32, device=DEV)
+    W = torch.ones(16, 16, device=DEV)
+    assert call_noalloc(q, q, q, W, grid, block, torch.empty_like(q)) == 0
+    torch.cuda.synchronize()
+    assert mhla.device_status() == 0
 
 
 @pytest.mark.parametrize("case", [
-    # (B, H, d, grid, block, dtype): tensor-core path, then the CUDA-core path
-    (2, 3, 64, (32, 48), (16, 8), "bf16"),
-    (1, 2, 32, (16, 16), (4, 4), "f32"),
-])
-def test_noalloc_matches_regular_entry_point_twice_in_a_row(case):
-    B, H, d, grid, block, dtype = case
+    # (B, H, d, grid, block, dtype, path): the CUDA cores first, so the
+    # tensor-core call runs over scratch left behind by another layout
+    (1, 2, 32, (16, 16), (4, 4), "f32", "simt"),
+    (2, 4, 64, (32, 64), (8, 16), "bf16", "simt"),
+    (2, 3, 64, (32, 48), (16, 8), "bf16", "tc"),
+], ids=["simt_f32", "simt_bf16_larger_scratch", "tc_bf16"])
+def test_noalloc_matches_oracle_and_regular_entry_point_twice_in_a_row(case):
+    B, H, d, grid, block, dtype, path = case
     N = int(np.prod(grid))
     M = mhla.num_blocks(grid, block)
-    W = torch.from_numpy(draw_matrix(M, seed=31)).to(DEV)
+    W_host = draw_matrix(M, seed=31)
+    W = torch.from_numpy(W_host).to(DEV)
     for seed in (41, 42):                               # two calls in a row, different inputs
-        q, k, v = (t.to(DEV) for t in draw_qkv(B, N, H, d, seed=seed, dtype=dtype))
+        qh, kh, vh = draw_qkv(B, N, H, d, seed=seed, dtype=dtype)
+        q, k, v = qh.to(DEV), kh.to(DEV), vh.to(DEV)
         out = torch.full_like(q, float("nan"))
-        assert call_noalloc(q, k, v, W, grid, block, out) == 0
-        ref = mhla.forward(q, k, v, W, grid, block)
+        assert call_noalloc(q, k, v, W, grid, block, out, path=path) == 0
+        regular = mhla.forward(q, k, v, W, grid, block, path=path)
         torch.cuda.synchronize()
         assert mhla.device_status() == 0
-        err = normwise(out, ref)
-        assert err <= TOL[q.dtype], f"seed {seed}: normwise difference {err:.3e}"
+        got = as_f64(out.cpu())
+        ref = oracle.forward(as_f64(qh), as_f64(kh), as_f64(vh), W_host.astype(np.float64), grid, block)
+        err = normwise(got, ref)
+        assert err <= TOL[q.dtype], f"seed {seed}: normwise error against the oracle {err:.3e}"
+        diff = normwise(got, as_f64(regular.cpu()))
+        assert diff <= TOL[q.dtype], f"seed {seed}: normwise difference from mhla_forward {diff:.3e}"
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():

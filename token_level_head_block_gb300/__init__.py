@@ -25,7 +25,7 @@ __all__ = [
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libmhla.so")
 
-PATHS = {"auto": 0, "simt": 1, "tc": 2, "fused": 3}
+PATHS = {"auto": 0, "simt": 1, "tc": 2, "fused": 3, "tc_fused": 4}
 TRANSFORMS = {"linear": 0, "cos": 1, "exp": 2, "gaussian": 3, "local": 4}
 PHIS = {"relu": 0, "relu_eps": 1}
 DTYPES = {"bf16": 0, "f32": 1}

@@ -22,11 +22,11 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-ffp-contra
               "--expt-relaxed-constexpr", f"-I{INCLUDE}"]
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", f"-I{INCLUDE}"]
 
-CUDA_SOURCES = ["mhla_api.cu", "simt_kernels.cu", "tc_kernels.cu", "tc_summary.cu", "tc_mix.cu", "tc_output.cu",
+CUDA_SOURCES = ["mhla_api.cu", "simt_kernels.cu", "tc_kernels.cu", "tc_summary.cu", "tc_mix.cu", "tc_output.cu", "tc_fused.cu",
                 "small_kernels.cu", "bwd_tc_kernels.cu", "causal_tc_kernels.cu", "profile.cu", "noalloc.cu",
                 "module_kernels.cu"]
 CXX_SOURCES = ["mhla_init.cpp"]
-HEADERS = ["mhla_internal.h", "ptx.cuh", "tma_host.h", "tc_common.cuh"]
+HEADERS = ["mhla_internal.h", "ptx.cuh", "tma_host.h", "tc_common.cuh", "tc_fwd_bodies.cuh"]
 
 
 def _nvcc():

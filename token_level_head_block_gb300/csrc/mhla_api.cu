@@ -131,6 +131,11 @@ int resolve_path(const Problem& p, int32_t path, int* sel) {
     *sel = MHLA_PATH_TC;
     return MHLA_OK;
   }
+  if (path == MHLA_PATH_TC_FUSED) {
+    if (!tc_fused_eligible(p)) return MHLA_ERR_UNSUPPORTED;
+    *sel = MHLA_PATH_TC_FUSED;
+    return MHLA_OK;
+  }
   if (path == MHLA_PATH_FUSED) {
     if (!small_eligible(p)) return MHLA_ERR_UNSUPPORTED;
     *sel = MHLA_PATH_FUSED;
@@ -141,7 +146,7 @@ int resolve_path(const Problem& p, int32_t path, int* sel) {
 
 size_t workspace_for(const Problem& p, int sel) {
   if (sel == MHLA_PATH_FUSED) return 0;
-  return sel == MHLA_PATH_TC ? tc_workspace_bytes(p) : simt_workspace_bytes(p);
+  return (sel == MHLA_PATH_TC || sel == MHLA_PATH_TC_FUSED) ? tc_workspace_bytes(p) : simt_workspace_bytes(p);
 }
 
 }  // namespace
@@ -197,7 +202,8 @@ extern "C" mhla_status_t mhla_forward(const mhla_tensor_t* q, const mhla_tensor_
     if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return MHLA_ERR_CUDA;
     owned = true;
   }
-  const int lr = sel == MHLA_PATH_TC ? launch_tc(p, W, ws, stream) : launch_simt(p, W, ws, stream);
+  const int lr = sel == MHLA_PATH_SIMT ? launch_simt(p, W, ws, stream)
+                                      : launch_tc(p, W, ws, stream, /*fused=*/sel == MHLA_PATH_TC_FUSED);
   if (owned && cudaFreeAsync(ws, s) != cudaSuccess && lr == MHLA_OK) return MHLA_ERR_CUDA;
   return static_cast<mhla_status_t>(lr);
 }
@@ -217,7 +223,7 @@ int resolve_bwd_path(const Problem& p, const BwdOperands& bo, int32_t path, int*
     *sel = MHLA_PATH_TC;
     return MHLA_OK;
   }
-  if (path == MHLA_PATH_FUSED) return MHLA_ERR_UNSUPPORTED;
+  if (path == MHLA_PATH_FUSED || path == MHLA_PATH_TC_FUSED) return MHLA_ERR_UNSUPPORTED;
   return MHLA_ERR_INVALID_ARG;
 }
 
@@ -325,7 +331,7 @@ int resolve_causal_path(const Problem& p, int32_t path, int* sel) {
     *sel = MHLA_PATH_TC;
     return MHLA_OK;
   }
-  if (path == MHLA_PATH_FUSED) return MHLA_ERR_UNSUPPORTED;
+  if (path == MHLA_PATH_FUSED || path == MHLA_PATH_TC_FUSED) return MHLA_ERR_UNSUPPORTED;
   return MHLA_ERR_INVALID_ARG;
 }
 

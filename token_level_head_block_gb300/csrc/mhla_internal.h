@@ -98,9 +98,26 @@ int read_and_clear_bwd_error(void* stream, uint32_t* flags);
 //                                       128 columns: (col/128, j, col%128)
 //   St   bf16 [BH][M][d][d]             S~_i row-major (r, c)
 //   zt   f32  [BH][M][d]                z~_i
+//   ctr  u32  [2B + 1]                  counters of the fused launch (zeroed per call)
 size_t tc_workspace_bytes(const Problem& p);
 bool tc_eligible(const Problem& p);
-int launch_tc(const Problem& p, const float* W, void* workspace, void* stream);
+// The three-launch path's own condition (tokens per block a multiple of 128 in
+// whole block rows); tc_eligible also admits the tile readout's contiguous
+// 64-token blocks.
+bool tc_rows_eligible(const Problem& p);
+// fused: the single persistent launch (tc_fused.cu; the caller checked
+// tc_fused_eligible); otherwise the summary, mixing and readout launches.
+int launch_tc(const Problem& p, const float* W, void* workspace, void* stream, bool fused = false);
+
+// The fused launch: tc_rows_eligible and M <= 256.  Sbuf, St, zt as above; ctr
+// holds 2B + 1 counters the launch zeroes on the stream first.
+bool tc_fused_eligible(const Problem& p);
+size_t tc_fused_counter_bytes(const Problem& p);
+int launch_tc_fused(const Problem& p, const float* W, void* Sbuf, void* St, float* zt, void* ctr, void* stream);
+int read_and_clear_fused_error(void* stream, uint32_t* flags);
+// d = 32 with an even number of adjacent heads: the readout pairs heads into
+// 64-channel rows.
+bool output_pairs_heads(const Problem& p);
 
 // Fused short-sequence path (N <= 256 tokens, M <= 96 blocks, bf16, d in
 // {32, 64}): one launch that forms the two-stage N x N product; no workspace.

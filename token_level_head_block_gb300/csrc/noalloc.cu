@@ -11,6 +11,7 @@
 // (summaries, mixed summaries, the bf16 copy of W) comes from a fixed-size array
 // that lives in this library's device image, so the call itself allocates
 // nothing.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -25,23 +26,59 @@ constexpr size_t kScratchBytes = MHLA_NOALLOC_SCRATCH_BYTES;
 // One copy per GPU that loads this library, held until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 
-// Device address of the scratch array on the current device.  The name
-// g_noalloc_scratch in host code is only a host-side stand-in for the symbol,
-// so the address is looked up once per device, with that device current.
-void* scratch_on_current_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
-    g_scratch_addr[dev] = ptr;
+// cuCtxGetCurrent through the runtime's driver entry point (no link-time
+// dependency on libcuda).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of the array in each context it was looked up in.  The key is
+// the CUDA context, not the device index: a context created after a reset of
+// the device holds its own copy of the array at its own address.
+constexpr int kMaxContexts = 64;
+std::mutex g_mu;
+CUcontext g_ctx[kMaxContexts] = {};
+void* g_addr[kMaxContexts] = {};
+int g_used = 0;
+
+// The name g_noalloc_scratch in host code is only a host-side stand-in for the
+// symbol, so its device address is looked up once per context, with the
+// caller's device current.  The first lookup in a context loads this file's
+// device code there, and the driver allocates the array's memory at that
+// moment: the reason callers make their first call at start-up.
+void* scratch_in_current_context() {
+  CtxGetCurrentFn get = ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (!get || get(&ctx) != CUDA_SUCCESS) return nullptr;
+  if (!ctx) {
+    // No context is current on this thread yet: make the current device's
+    // primary context current (cudaSetDevice initialises it; no memory is
+    // allocated for this library).
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || cudaSetDevice(dev) != cudaSuccess) return nullptr;
+    if (get(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
   }
-  return g_scratch_addr[dev];
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int e = 0; e < g_used; ++e)
+    if (g_ctx[e] == ctx) return g_addr[e];
+  if (g_used == kMaxContexts) return nullptr;
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
+  g_ctx[g_used] = ctx;
+  g_addr[g_used] = ptr;
+  ++g_used;
+  return ptr;
 }
 
 }  // namespace
@@ -57,7 +94,7 @@ extern "C" mhla_status_t mhla_forward_noalloc(const mhla_tensor_t* q, const mhla
   const mhla_status_t sz = mhla_workspace_size(q, grid, block, path, &need);
   if (sz != MHLA_OK) return sz;
   if (need > mhla::kScratchBytes) return MHLA_ERR_WORKSPACE;
-  void* scratch = mhla::scratch_on_current_device();
+  void* scratch = mhla::scratch_in_current_context();
   if (!scratch) return MHLA_ERR_CUDA;
   // mhla_forward re-checks the need for the path it actually takes against the
   // array's capacity and returns MHLA_ERR_WORKSPACE when it does not fit.

@@ -61,6 +61,32 @@ static __device__ __noinline__ void drain_wait_on(uint64_t* bar, uint32_t parity
   }
 }
 
+// Waits until a global counter another CTA of the same grid raises reaches
+// target (acquire), bounded like the mbarrier waits; on success the data it
+// publishes may be read by this thread's TMA and bulk copies too.
+static __device__ __noinline__ bool wait_counter_on(const uint32_t* ctr, uint32_t target,
+                                                    volatile uint32_t* abort_flag, unsigned int* err) {
+  if (ld_acquire_gpu(ctr) >= target) {
+    fence_proxy_async_global();
+    return true;
+  }
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1; it < kWaitLimitPolls; ++it) {
+    __nanosleep(128);
+    if (ld_acquire_gpu(ctr) >= target) {
+      fence_proxy_async_global();
+      return true;
+    }
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) break;
+    }
+  }
+  *abort_flag = 1u;
+  atomicOr(err, 1u);
+  return false;
+}
+
 // Token-grid geometry of one launch (all int32: checked on the host).
 struct TcGeom {
   int32_t M, nbx, nby;     // block grid, x fastest

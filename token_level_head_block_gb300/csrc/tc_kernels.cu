@@ -66,7 +66,7 @@ bool encode(CUtensorMap* m, int rank, void* base, const cuuint64_t* dims, const 
 }
 
 struct TcLayout {
-  size_t wb_off, sbuf_off, st_off, zt_off, total;
+  size_t wb_off, sbuf_off, st_off, zt_off, ctr_off, total;
   int64_t Mp, ncols, ngroups;
 };
 
@@ -84,6 +84,8 @@ TcLayout tc_layout(const Problem& p) {
   off += align_up(static_cast<size_t>(p.BH()) * p.M * p.d * p.d * 2);
   L.zt_off = off;
   off += align_up(static_cast<size_t>(p.BH()) * p.M * p.d * 4);
+  L.ctr_off = off;
+  off += align_up(tc_fused_counter_bytes(p));
   L.total = off;
   return L;
 }
@@ -126,12 +128,15 @@ bool tc_eligible(const Problem& p) { return tc_rows_eligible(p) || tc_tile_eligi
 
 size_t tc_workspace_bytes(const Problem& p) { return tc_layout(p).total; }
 
-int launch_tc(const Problem& p, const float* W, void* workspace, void* stream) {
+int launch_tc(const Problem& p, const float* W, void* workspace, void* stream, bool fused) {
   const TcLayout L = tc_layout(p);
   char* ws = static_cast<char*>(workspace);
   if (!tc_rows_eligible(p))
     return launch_tc_tile_forward(p, W, ws + L.wb_off, L.Mp, ws + L.sbuf_off, ws + L.st_off,
                                   reinterpret_cast<float*>(ws + L.zt_off), stream);
+  if (fused)
+    return launch_tc_fused(p, W, ws + L.sbuf_off, ws + L.st_off, reinterpret_cast<float*>(ws + L.zt_off),
+                           ws + L.ctr_off, stream);
   int rc = tc_run_summary(p, W, ws + L.wb_off, nullptr, L.Mp, ws + L.sbuf_off, stream);
   if (rc == MHLA_OK)
     rc = tc_run_mix(p, ws + L.wb_off, L.Mp, ws + L.sbuf_off, ws + L.st_off, reinterpret_cast<float*>(ws + L.zt_off),
@@ -141,12 +146,13 @@ int launch_tc(const Problem& p, const float* W, void* workspace, void* stream) {
 }
 
 int read_and_clear_device_error(void* stream, uint32_t* flags) {
-  uint32_t a = 0, b = 0, c = 0;
+  uint32_t a = 0, b = 0, c = 0, f = 0;
   const int ra = read_and_clear_summary_error(stream, &a);
   const int rb = read_and_clear_mix_error(stream, &b);
   const int rc = read_and_clear_output_error(stream, &c);
-  if (ra == MHLA_ERR_CUDA || rb == MHLA_ERR_CUDA || rc == MHLA_ERR_CUDA) return MHLA_ERR_CUDA;
-  *flags = a | b | c;
+  const int rf = read_and_clear_fused_error(stream, &f);
+  if (ra == MHLA_ERR_CUDA || rb == MHLA_ERR_CUDA || rc == MHLA_ERR_CUDA || rf == MHLA_ERR_CUDA) return MHLA_ERR_CUDA;
+  *flags = a | b | c | f;
   return *flags ? MHLA_ERR_TIMEOUT : MHLA_OK;
 }
 

@@ -17,6 +17,7 @@
 #include "mhla_internal.h"
 #include "ptx.cuh"
 #include "tc_common.cuh"
+#include "tc_fwd_bodies.cuh"
 #include "tma_host.h"
 
 namespace mhla {
@@ -223,64 +224,28 @@ tc_mix(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtenso
 }
 
 // ============================================================================
-// tc_mix_resident: the same GEMM for M <= 256 with all of W (bf16, <= 128 KB)
-// resident in shared memory, computed transposed: D[col][i] = sum_j
-// Sbuf[j][col] W[i][j].  One tile = 128 Sbuf columns (MMA M, the TMEM lanes) x
-// all query blocks (MMA N <= 256): per 16 source blocks a single 128 x N x 16
-// MMA, A = the Sbuf chunk as it landed (MN-major), B = W (K-major).  With the
-// columns on TMEM lanes, the 32 lanes of an epilogue warp hold 32 consecutive
-// columns of one query block, so each store writes 64 contiguous bytes of S~
-// (or 128 of z~).  Two accumulator sets alternate between tiles; both
-// epilogue warpgroups drain every tile, each half of the query blocks.
+// tc_mix_resident: the M <= 256 mixing pipeline (tc_fwd_bodies.cuh: W resident
+// in shared memory, transposed GEMM with the Sbuf columns on the TMEM lanes) in
+// a launch of its own, W loaded by TMA from its bf16 copy.
 // ============================================================================
-struct MixResCfg {
-  static constexpr int COLS = 128;                // Sbuf columns per tile (MMA M)
-  static constexpr int NMAX = 256;                // query blocks (MMA N, at most)
-  static constexpr int KC = 64;                   // source blocks per stage
-  static constexpr int W_CHUNK = NMAX * KC * 2;   // W rows i for 64 source blocks, K-major
-  static constexpr int W_BYTES = 4 * W_CHUNK;     // up to 256 x 256
-  static constexpr int STAGE = KC * COLS * 2;     // Sbuf chunk: two 64-column MN-major halves
-  static constexpr int NS = 6;
-  static constexpr int SET = NMAX;                // TMEM columns of one accumulator set
-  static constexpr int TMEM_COLS = 512;
-  static constexpr int CTRL = 1024;
-  static constexpr size_t SMEM = static_cast<size_t>(W_BYTES) + static_cast<size_t>(NS) * STAGE + CTRL + 1024;
-};
+constexpr int kMixResStages = 6;
+using MixRes = MixResCfg<kMixResStages>;
+constexpr size_t kMixResSmem = MixRes::DATA + 1024 + 1024;
 
 template <int D>
 __global__ void __launch_bounds__(kMixThreadsTC, 1)
 tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s, int32_t M,
                 int32_t NP, int64_t ncols, int32_t n_tiles, __nv_bfloat16* __restrict__ St, float* __restrict__ zt,
                 const __nv_bfloat16* discard_s) {
-  using Cfg = MixResCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
-  uint8_t* wres = smem;                                  // [k chunk] W rows i, K-major
-  uint8_t* stages = smem + Cfg::W_BYTES;
-  uint8_t* ctrl = stages + Cfg::NS * Cfg::STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-  uint64_t* empty = full + Cfg::NS;
-  uint64_t* tfull = empty + Cfg::NS;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* wfull = tempty + 2;
-  uint64_t* fin = wfull + 1;
+  uint8_t* ctrl = smem + MixRes::DATA;
+  const MixBars bars = mix_bars<kMixResStages>(ctrl);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 512);
   volatile uint32_t* abortf = tmem_slot + 1;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nk = (M + Cfg::KC - 1) / Cfg::KC;           // 1..4 source chunks
-  const uint32_t wchunk = static_cast<uint32_t>(NP) * Cfg::KC * 2;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Cfg::NS; ++s) {
-      mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull + a, 1);
-      mbar_init(tempty + a, 256);
-    }
-    mbar_init(wfull, 1);
-    mbar_init(fin, 1);
+    mix_init<kMixResStages>(bars);
     *abortf = 0u;
     fence_mbar_init();
   }
@@ -289,127 +254,21 @@ tc_mix_resident(const __grid_constant__ CUtensorMap tm_w, const __grid_constant_
     prefetch_tmap(&tm_s);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_alloc(tmem_slot, MixRes::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      grid_dep_wait();   // W in bf16 and Sbuf come from the summary launch
-      const uint64_t pol_w = policy_evict_last();
-      const uint64_t pol_s = policy_evict_first();
-      // all of W once: chunk kc holds rows i < NP (rows >= M read as zeros) of source blocks kc*64 ..
-      mbar_arrive_expect_tx(wfull, static_cast<uint32_t>(nk) * wchunk);
-      for (int kc = 0; kc < nk; ++kc) tma_load_2d(wres + kc * wchunk, &tm_w, wfull, kc * Cfg::KC, 0, pol_w);
-      int s = 0;
-      uint32_t ph = 0;
-      uint64_t fills = 0;
-      bool ok = true;
-      for (int64_t t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
-        for (int kc = 0; kc < nk; ++kc) {
-          if (!wait_bounded(empty + s, ph ^ 1u, abortf)) { ok = false; break; }
-          mbar_arrive_expect_tx(full + s, Cfg::STAGE);
-          uint8_t* st = stages + s * Cfg::STAGE;
-          // one 128-column group of Sbuf, rows j contiguous; rows j >= M read as zeros
-          tma_load_3d(st, &tm_s, full + s, 0, kc * Cfg::KC, static_cast<int32_t>(t), pol_s);
-          tma_load_3d(st + Cfg::STAGE / 2, &tm_s, full + s, 64, kc * Cfg::KC, static_cast<int32_t>(t), pol_s);
-          ++fills;
-          if (++s == Cfg::NS) { s = 0; ph ^= 1u; }
-        }
-      }
-      drain_wait(wfull, 0);
-      for (int st = 0; st < Cfg::NS; ++st) {
-        const uint64_t n = fills / Cfg::NS + (static_cast<uint64_t>(st) < fills % Cfg::NS ? 1 : 0);
-        if (n > 0) drain_wait(full + st, static_cast<uint32_t>((n - 1) & 1));
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(Cfg::COLS, NP, /*a MN-major*/ true, /*b K-major*/ false);
-      int s = 0;
-      uint32_t ph = 0, local = 0;
-      bool ok = wait_bounded(wfull, 0, abortf);
-      tc_fence_after();
-      const uint32_t wbase = smem_u32(wres);
-      for (int64_t t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++local) {
-        const uint32_t set = local & 1u, sph = (local >> 1) & 1u;
-        if (!wait_bounded(tempty + set, sph ^ 1u, abortf)) break;
-        tc_fence_after();
-        for (int kc = 0; kc < nk; ++kc) {
-          if (!wait_bounded(full + s, ph, abortf)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t base = smem_u32(stages + s * Cfg::STAGE);
-#pragma unroll
-          for (int ks = 0; ks < Cfg::KC / 16; ++ks) {
-            const uint64_t a = smem_desc(base + ks * 2048, Cfg::STAGE / 2, 1024, 2);
-            const uint64_t b = smem_desc(wbase + kc * wchunk + ks * 32, 16, 1024, 2);
-            mma_bf16(tmem + set * Cfg::SET, a, b, idesc, (kc | ks) != 0 ? 1u : 0u);
-          }
-          mma_commit(empty + s);
-          if (++s == Cfg::NS) { s = 0; ph ^= 1u; }
-        }
-        if (!ok) break;
-        mma_commit(tfull + set);
-      }
-      mma_commit(fin);
-      drain_wait(fin, 0);
-    }
-  } else {
-    // warpgroup wg (warps 2-5 or 6-9) drains query blocks [128 wg, 128 wg + 128) of every tile
-    constexpr int32_t PER_BH = (D + 1) * D;            // Sbuf columns of one (b, h): d rows of S, then z
-    const int wg = (warp - 2) >> 2;
-    const int q4 = warp & 3;
-    const int i_lo = wg * 128, i_hi = min(M, i_lo + 128);
-    uint32_t local = 0;
-    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
-      const uint32_t set = local & 1u, sph = (local >> 1) & 1u;
-      if (!warp_wait(tfull + set, sph, abortf)) break;
-      tc_fence_after();
-      // this lane's column; 32-column runs never cross a row of S (d is a multiple of 32)
-      const int64_t col = t * Cfg::COLS + 32 * q4 + lane;
-      const bool live = col < ncols;
-      const int64_t bh = col / PER_BH;
-      const int32_t rem = static_cast<int32_t>(col - bh * PER_BH);
-      const int32_t rr = rem / D, c = rem % D;
-      const uint32_t tb = tmem + set * Cfg::SET + (static_cast<uint32_t>(32 * q4) << 16);
-#pragma unroll 1
-      for (int i0 = i_lo; i0 < i_hi; i0 += 32) {
-        uint32_t v[32];
-        tmem_ld_x32(tb + i0, v);
-        tmem_ld_wait();
-        if (live) {
-          if (rr < D) {
-            __nv_bfloat16* dst = St + (bh * M + i0) * (D * D) + rr * D + c;   // S~_i row-major
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (i0 + e < i_hi) dst[static_cast<int64_t>(e) * D * D] = __float2bfloat16_rn(__uint_as_float(v[e]));
-          } else {
-            float* dst = zt + (bh * M + i0) * D + c;
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (i0 + e < i_hi) dst[static_cast<int64_t>(e) * D] = __uint_as_float(v[e]);
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(tempty + set);
-      // every MMA of tile t is done: its 128-column group of Sbuf (read exactly
-      // once, by this CTA) leaves L2 without a write-back when the caller allows
-      if (discard_s) {
-        const uint8_t* grp = reinterpret_cast<const uint8_t*>(discard_s + t * static_cast<int64_t>(M) * 128);
-        for (int e = (warp - 2) * 32 + lane; e < 2 * M; e += 256) discard_l2_line(grp + e * 128);
-      }
-    }
-  }
+  const MixDeps none{nullptr, 0u, nullptr, 1};
+  mix_roles<kMixResStages, D>(&tm_w, &tm_s, M, NP, ncols, blockIdx.x, gridDim.x, n_tiles, St, zt, discard_s, smem,
+                              bars, tmem, abortf, &g_mix_error, none);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    tmem_dealloc(tmem, MixRes::TMEM_COLS);
   }
 }
 
@@ -432,18 +291,18 @@ int run_mix(const Problem& p, const __nv_bfloat16* Wm, int64_t Mp, const __nv_bf
   if (p.M <= 256) {   // all of W in shared memory
     CUtensorMap tw, ts;
     const int32_t NP = static_cast<int32_t>((p.M + 15) / 16 * 16);   // MMA N: query blocks rounded up to 16
-    const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(MixResCfg::KC), static_cast<cuuint32_t>(NP)};
-    const cuuint32_t sbox[3] = {64u, static_cast<cuuint32_t>(MixResCfg::KC), 1u};
+    const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(MixRes::KC), static_cast<cuuint32_t>(NP)};
+    const cuuint32_t sbox[3] = {64u, static_cast<cuuint32_t>(MixRes::KC), 1u};
     if (!encode_tensor_map(&tw, 2, wptr, wdims, wstrides, wbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tensor_map(&ts, 3, sptr, sdims, sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_128B))
       return MHLA_ERR_CUDA;
-    const int32_t n_tiles = static_cast<int32_t>((ncols + MixResCfg::COLS - 1) / MixResCfg::COLS);
+    const int32_t n_tiles = static_cast<int32_t>((ncols + MixRes::COLS - 1) / MixRes::COLS);
     if (cudaFuncSetAttribute(tc_mix_resident<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(MixResCfg::SMEM)) != cudaSuccess)
+                             static_cast<int>(kMixResSmem)) != cudaSuccess)
       return MHLA_ERR_CUDA;
     const int grid = static_cast<int>(std::min<int64_t>(n_tiles, sms));
     KernelTimer timer("tc_mix", stream);
-    const cudaError_t e = launch_dependent(tc_mix_resident<D>, dim3(grid), dim3(kMixThreadsTC), MixResCfg::SMEM,
+    const cudaError_t e = launch_dependent(tc_mix_resident<D>, dim3(grid), dim3(kMixThreadsTC), kMixResSmem,
                                            stream, tw, ts, static_cast<int32_t>(p.M), NP, ncols, n_tiles, St, zt,
                                            discard_input ? Sbuf : static_cast<const __nv_bfloat16*>(nullptr));
     return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
