@@ -167,7 +167,8 @@ KERNEL_SOURCES = {"tc_summary": ("tc_summary.cu", "tc_fwd_bodies.cuh"), "tc_mix"
                   "simt_bwd_key": "simt_kernels.cu", "simt_dw": "simt_kernels.cu",
                   "simt_causal_output": "simt_kernels.cu", "tc_causal_tile": "causal_tc_kernels.cu",
                   "tc_tile_output": "causal_tc_kernels.cu", "mhla_lepe_add": "module_kernels.cu",
-                  "mhla_ln_rows": "module_kernels.cu"}
+                  "mhla_ln_rows": "module_kernels.cu", "mhla_gemm_qkv": "gemm_kernels.cu",
+                  "mhla_gemm_out": "gemm_kernels.cu"}
 
 
 def kernel_source_digest(kernel):
@@ -219,8 +220,8 @@ def kernel_work(wl, name):
         "tc_tile_output": ("hbm", 2 * io),
         # module: x -> LayerNorm; qkv = xn W^T; o += lepe(v) (read v, o; write o); y = o W^T
         "mhla_ln_rows": ("hbm", 2 * io), "mhla_lepe_add": ("hbm", 3 * io),
-        "cublaslt_qkv": ("tensor", 2 * wl.tokens * (wl.H * d) * 3 * (wl.H * d)),
-        "cublaslt_out": ("tensor", 2 * wl.tokens * (wl.H * d) * (wl.H * d)),
+        "mhla_gemm_qkv": ("tensor", 2 * wl.tokens * (wl.H * d) * 3 * (wl.H * d)),
+        "mhla_gemm_out": ("tensor", 2 * wl.tokens * (wl.H * d) * (wl.H * d)),
     }
     return table.get(name, ("hbm", 0))
 

@@ -298,16 +298,27 @@ mhla_status_t mhla_forward_noalloc(const mhla_tensor_t* q, const mhla_tensor_t* 
  * to_out and forward), for a [B, N, C] bf16 token array x with C = heads * d:
  *
  *   xn      = LayerNorm(x)                        (mhla_layer_norm)
- *   q, k, v = split(xn W_qkv^T + b_qkv, 3)        (a GEMM; q, k, v are read in
- *             place as [B, N, heads, d] views of its [B, N, 3C] result)
+ *   q, k, v = split(xn W_qkv^T + b_qkv, 3)        (mhla_linear; q, k, v are read
+ *             in place as [B, N, heads, d] views of its [B, N, 3C] result)
  *   o       = MHLA(q, k, v)                       (mhla_forward, path AUTO)
  *   o      += lepe(v)                             (mhla_lepe_add)
- *   y       = o W_out^T + b_out                   (a GEMM)
+ *   y       = o W_out^T + b_out                   (mhla_linear)
  *
- * The two projections go to cuBLASLt (loaded at run time); without it the
- * module call returns MHLA_ERR_UNSUPPORTED.  Dropout is the identity
- * (inference); q_norm / k_norm are identities (the listing's default).
+ * Every step runs in this library's own kernels (the projections on the
+ * tensor cores, tcgen05).  Dropout is the identity (inference); q_norm /
+ * k_norm are identities (the listing's default).
  * ------------------------------------------------------------------------ */
+
+/* A linear layer y = x w^T + bias in bf16 with float32 accumulation, rounded
+ * once to bf16: the module's to_qkv and to_out ([P1] section 7, nn.Linear).
+ *   x      device [rows][k] bf16, row-major;  w  device [n_out][k] bf16
+ *          (nn.Linear's [out][in] layout);  bias  device [n_out] bf16 or NULL;
+ *   y      device [rows][n_out] bf16; must not overlap x, w or bias.
+ * k and n_out multiples of 8, every pointer 16-byte aligned, rows < 2^31
+ * (MHLA_ERR_UNSUPPORTED otherwise); rows == 0 queues nothing.  Asynchronous on
+ * stream; tensor-core GEMM in 128 x 256 output tiles. */
+mhla_status_t mhla_linear(const void* x, const void* w, const void* bias, void* y, int64_t rows, int64_t k,
+                          int64_t n_out, void* stream);
 
 /* LayerNorm over the last axis of a row-major [rows, C] bf16 device array:
  * y = (x - mean) / sqrt(var + eps) * weight + bias with the biased variance and
@@ -349,8 +360,8 @@ typedef struct mhla_module_params {
 } mhla_module_params_t;
 
 /* Device workspace mhla_module_forward needs (bytes): the normalised input and
- * the core's output (one buffer), the [B, N, 3C] projection, the core's own
- * workspace and 32 MiB for cuBLASLt.  Host only. */
+ * the core's output (one buffer), the [B, N, 3C] projection and the core's own
+ * workspace.  Host only. */
 mhla_status_t mhla_module_workspace_size(int64_t B, int64_t N, int64_t C, int32_t heads,
                                          const mhla_shape3_t* grid, const mhla_shape3_t* block,
                                          size_t* bytes);
@@ -358,13 +369,12 @@ mhla_status_t mhla_module_workspace_size(int64_t B, int64_t N, int64_t C, int32_
 /* The module forward on x [B, N, C] (bf16, row-major, 16-byte aligned; tokens in
  * raster order over grid) into y of the same layout (y may equal x).  W, grid,
  * block and phi are those of mhla_forward (the listing uses
- * MHLA_PHI_RELU_EPS).  C % 8 == 0, C <= 2048, d = C / heads with d % 8 == 0.
+ * MHLA_PHI_RELU_EPS).  C % 8 == 0, C <= 2048, d = C / heads with d % 8 == 0,
+ * B * N < 2^31; the projection biases, when given, 16-byte aligned.
  * workspace as for mhla_forward (NULL with workspace_bytes == 0: stream-ordered
- * allocation).  Asynchronous on stream; returns MHLA_ERR_UNSUPPORTED when
- * cuBLASLt cannot be loaded or has no algorithm for the shapes.  The argument
- * checks of every step (the core's and the positional term's included) run
- * before the first launch; only cuBLASLt finding no algorithm or a failed
- * launch can return after earlier steps were queued. */
+ * allocation).  Asynchronous on stream.  The argument checks of every step (the
+ * core's and the positional term's included) run before the first launch; only
+ * a failed launch can return after earlier steps were queued. */
 mhla_status_t mhla_module_forward(const void* x, void* y, int64_t B, int64_t N, int64_t C,
                                   const mhla_module_params_t* params, const float* W,
                                   const mhla_shape3_t* grid, const mhla_shape3_t* block,

@@ -73,6 +73,49 @@ def test_layer_norm_in_place_and_constant_rows():
     assert np.all(got[3] == 0.25)
 
 
+LINEAR_CASES = [
+    # (rows, k, n_out, bias): one tile and a ragged one on every axis (rows past
+    # a 128-row tile, n_out past a column tile and not a multiple of 64, k past a
+    # 64-wide chunk), the module's DiT-S/2 shapes, the largest C; k <= 384 keeps
+    # a slice of w resident per CTA, larger k streams both operands
+    (1, 8, 8, True),
+    (300, 72, 136, True),
+    (512, 384, 1152, True),
+    (1000, 384, 384, False),
+    (257, 2048, 264, True),
+    (700, 512, 200, True),
+    (4096, 64, 256, False),
+]
+
+
+@pytest.mark.parametrize("rows,k,n_out,bias", LINEAR_CASES)
+def test_linear_layer(rows, k, n_out, bias):
+    """The projections' tensor-core GEMM against the float64 nn.Linear of the
+    module oracle: float32 accumulation leaves only the final bf16 rounding."""
+    x = draw_tokens(1, rows, k, seed=31 + k)[0]
+    rng = np.random.default_rng(n_out)
+    w = torch.from_numpy((rng.standard_normal((n_out, k)) / np.sqrt(k)).astype(np.float32)).to(torch.bfloat16)
+    b = torch.from_numpy((0.1 * rng.standard_normal(n_out)).astype(np.float32)).to(torch.bfloat16) if bias else None
+    y = mhla.linear(x.to(DEV), w.to(DEV), None if b is None else b.to(DEV))
+    torch.cuda.synchronize()
+    assert mhla.device_status() == 0
+    ref = oracle.linear(as_f64(x), as_f64(w), None if b is None else as_f64(b))
+    got = as_f64(y.cpu())
+    _bf16_close(got, ref, abs_=2e-3)
+    assert _normwise(got, ref) <= 2e-2
+
+
+def test_linear_refuses_bad_shapes_and_empty_rows():
+    x = torch.zeros(4, 12, dtype=torch.bfloat16, device=DEV)            # k % 8 != 0
+    w = torch.zeros(16, 12, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(mhla.MhlaError) as e:
+        mhla.linear(x, w)
+    assert e.value.status == 3
+    x0 = torch.zeros(0, 16, dtype=torch.bfloat16, device=DEV)
+    w0 = torch.zeros(8, 16, dtype=torch.bfloat16, device=DEV)
+    assert mhla.linear(x0, w0).shape == (0, 8)
+
+
 LEPE_CASES = [
     # (B, grid, H, d)
     (2, (13, 21), 2, 32),         # ragged tiles on both axes, C = 64

@@ -120,6 +120,9 @@ def lib():
     L.mhla_layer_norm.restype = ctypes.c_int
     L.mhla_lepe_add.argtypes = [P(Tensor), P(Tensor), P(Shape3), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     L.mhla_lepe_add.restype = ctypes.c_int
+    L.mhla_linear.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                              ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+    L.mhla_linear.restype = ctypes.c_int
     L.mhla_module_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                              P(Shape3), P(Shape3), P(ctypes.c_size_t)]
     L.mhla_module_workspace_size.restype = ctypes.c_int
@@ -335,6 +338,20 @@ def layer_norm(x, weight, bias, eps=1e-5, out=None, stream=None):
     st = lib().mhla_layer_norm(_ptr(x), _ptr(out), x.numel() // C, C, _ptr(weight), _ptr(bias), float(eps),
                                _stream_ptr(stream, x.device))
     _check(st, "mhla_layer_norm")
+    return out
+
+
+def linear(x, w, bias=None, out=None, stream=None):
+    """y = x w^T (+ bias) for a contiguous bf16 CUDA tensor x [..., k] and an
+    nn.Linear-layout weight w [n_out, k] (bias [n_out] or None); returns ``out``."""
+    import torch
+    k = x.shape[-1]
+    n_out = w.shape[0]
+    rows = x.numel() // k if k else 0
+    if out is None:
+        out = torch.empty(*x.shape[:-1], n_out, dtype=x.dtype, device=x.device)
+    st = lib().mhla_linear(_ptr(x), _ptr(w), _ptr(bias), _ptr(out), rows, k, n_out, _stream_ptr(stream, x.device))
+    _check(st, "mhla_linear")
     return out
 
 

@@ -24,7 +24,7 @@ CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-ffp-contract=off", f"-I{INCLUDE}"]
 
 CUDA_SOURCES = ["mhla_api.cu", "simt_kernels.cu", "tc_kernels.cu", "tc_summary.cu", "tc_mix.cu", "tc_output.cu", "tc_fused.cu",
                 "small_kernels.cu", "bwd_tc_kernels.cu", "causal_tc_kernels.cu", "profile.cu", "noalloc.cu",
-                "module_kernels.cu"]
+                "module_kernels.cu", "gemm_kernels.cu"]
 CXX_SOURCES = ["mhla_init.cpp"]
 HEADERS = ["mhla_internal.h", "ptx.cuh", "tma_host.h", "tc_common.cuh", "tc_fwd_bodies.cuh"]
 

@@ -395,15 +395,17 @@ extern "C" mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_
 
 extern "C" mhla_status_t mhla_device_status(void* stream, uint32_t* flags) {
   if (!flags) return MHLA_ERR_INVALID_ARG;
-  uint32_t tc = 0, small = 0, bwd = 0, causal = 0, module = 0;
+  uint32_t tc = 0, small = 0, bwd = 0, causal = 0, module = 0, gemm = 0;
   const int a = read_and_clear_device_error(stream, &tc);
   const int b = read_and_clear_small_error(stream, &small);
   const int c = read_and_clear_bwd_error(stream, &bwd);
   const int e = read_and_clear_causal_error(stream, &causal);
   const int f = read_and_clear_module_error(stream, &module);
-  if (a == MHLA_ERR_CUDA || b == MHLA_ERR_CUDA || c == MHLA_ERR_CUDA || e == MHLA_ERR_CUDA || f == MHLA_ERR_CUDA)
+  const int g = read_and_clear_gemm_error(stream, &gemm);
+  if (a == MHLA_ERR_CUDA || b == MHLA_ERR_CUDA || c == MHLA_ERR_CUDA || e == MHLA_ERR_CUDA || f == MHLA_ERR_CUDA ||
+      g == MHLA_ERR_CUDA)
     return MHLA_ERR_CUDA;
-  *flags = tc | small | bwd | causal | module;
+  *flags = tc | small | bwd | causal | module | gemm;
   return *flags ? MHLA_ERR_TIMEOUT : MHLA_OK;
 }
 
@@ -495,7 +497,7 @@ int lepe_args(const mhla_tensor_t* v, const mhla_tensor_t* out, const mhla_shape
 
 // Buffers of the module inside its workspace.
 struct ModuleLayout {
-  size_t a_off, qkv_off, core_off, lt_off, total;
+  size_t a_off, qkv_off, core_off, total;
 };
 
 // The core's [B, N, heads, d] views of the projection and of the output buffer.
@@ -529,7 +531,7 @@ int module_check(int64_t B, int64_t N, int64_t C, int32_t heads, const mhla_shap
   if (rg != MHLA_OK) return rg;
   const int64_t M = mhla_num_blocks(grid, block);
   if (M < 0) return static_cast<int>(-M);
-  if (B * N >= (int64_t{1} << 40) || (B * N + 7) / 8 >= (int64_t{1} << 31)) return MHLA_ERR_UNSUPPORTED;
+  if (B * N >= (int64_t{1} << 31)) return MHLA_ERR_UNSUPPORTED;   // the projections' row coordinate
   return MHLA_OK;
 }
 
@@ -550,8 +552,6 @@ int module_layout(int64_t B, int64_t N, int64_t C, int32_t heads, const mhla_sha
   off += align_up(static_cast<size_t>(R) * 3 * C * 2);
   L->core_off = off;
   off += align_up(core);
-  L->lt_off = off;
-  off += align_up(linear_workspace_bytes());
   L->total = off;
   return MHLA_OK;
 }
@@ -573,6 +573,25 @@ extern "C" mhla_status_t mhla_layer_norm(const void* x, void* y, int64_t rows, i
   if ((rows + 7) / 8 >= (int64_t{1} << 31)) return MHLA_ERR_UNSUPPORTED;
   return static_cast<mhla_status_t>(
       launch_layer_norm(x, y, rows, static_cast<int32_t>(C), weight, bias, eps, stream));
+}
+
+extern "C" mhla_status_t mhla_linear(const void* x, const void* w, const void* bias, void* y, int64_t rows, int64_t k,
+                                     int64_t n_out, void* stream) {
+  if (rows < 0 || k < 1 || n_out < 1) return MHLA_ERR_INVALID_ARG;
+  if (!gemm_supported(rows == 0 ? 1 : rows, k, n_out)) return MHLA_ERR_UNSUPPORTED;
+  if (rows == 0) return MHLA_OK;
+  if (!x || !w || !y) return MHLA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias))) return MHLA_ERR_INVALID_ARG;
+  const uintptr_t y0 = reinterpret_cast<uintptr_t>(y), y1 = y0 + static_cast<uintptr_t>(rows * n_out * 2);
+  const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), w0 = reinterpret_cast<uintptr_t>(w);
+  if (overlaps(y0, y1, x0, x0 + static_cast<uintptr_t>(rows * k * 2)) ||
+      overlaps(y0, y1, w0, w0 + static_cast<uintptr_t>(n_out * k * 2)))
+    return MHLA_ERR_INVALID_ARG;
+  if (bias) {
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(bias);
+    if (overlaps(y0, y1, b0, b0 + static_cast<uintptr_t>(n_out * 2))) return MHLA_ERR_INVALID_ARG;
+  }
+  return static_cast<mhla_status_t>(launch_gemm("mhla_gemm", x, w, bias, y, rows, k, n_out, stream));
 }
 
 extern "C" mhla_status_t mhla_lepe_add(const mhla_tensor_t* v, const mhla_tensor_t* out, const mhla_shape3_t* grid,
@@ -614,7 +633,8 @@ extern "C" mhla_status_t mhla_module_forward(const void* x, void* y, int64_t B, 
       !aligned16(params->qkv_weight) || !aligned16(params->out_weight))
     return MHLA_ERR_INVALID_ARG;
   if (!(params->ln_eps >= 0.0f) || !std::isfinite(params->ln_eps)) return MHLA_ERR_INVALID_ARG;
-  if (!linear_available()) return MHLA_ERR_UNSUPPORTED;
+  if ((params->qkv_bias && !aligned16(params->qkv_bias)) || (params->out_bias && !aligned16(params->out_bias)))
+    return MHLA_ERR_INVALID_ARG;
   ModuleLayout L;
   const int rl = module_layout(B, N, C, params->heads, grid, block, &L);
   if (rl != MHLA_OK) return static_cast<mhla_status_t>(rl);
@@ -645,12 +665,12 @@ extern "C" mhla_status_t mhla_module_forward(const void* x, void* y, int64_t B, 
     r = launch_layer_norm(x, abuf, R, static_cast<int32_t>(C), params->ln_weight, params->ln_bias, params->ln_eps,
                           stream);
   if (r == MHLA_OK)
-    r = launch_linear("cublaslt_qkv", abuf, params->qkv_weight, params->qkv_bias, qkv, R, C, 3 * C, base + L.lt_off, stream);
+    r = launch_gemm("mhla_gemm_qkv", abuf, params->qkv_weight, params->qkv_bias, qkv, R, C, 3 * C, stream);
   if (r == MHLA_OK)
-    r = mhla_forward(&q, &k, &v, W, grid, block, phi, &o, base + L.core_off, L.lt_off - L.core_off, stream,
+    r = mhla_forward(&q, &k, &v, W, grid, block, phi, &o, base + L.core_off, L.total - L.core_off, stream,
                      MHLA_PATH_AUTO);
   if (r == MHLA_OK && params->lepe_weight) r = launch_lepe_add(lepe, stream);
-  if (r == MHLA_OK) r = launch_linear("cublaslt_out", abuf, params->out_weight, params->out_bias, y, R, C, C, base + L.lt_off, stream);
+  if (r == MHLA_OK) r = launch_gemm("mhla_gemm_out", abuf, params->out_weight, params->out_bias, y, R, C, C, stream);
   if (owned && cudaFreeAsync(ws, s) != cudaSuccess && r == MHLA_OK) return MHLA_ERR_CUDA;
   return static_cast<mhla_status_t>(r);
 }

@@ -174,7 +174,7 @@ inline bool blocks_contiguous(const Problem& p) {
 }
 
 // Module around the core: LayerNorm rows, the 5 x 5 depthwise positional term
-// added into the core's output, and bf16 linear layers through cuBLASLt.
+// added into the core's output, and the bf16 linear layers (launch_gemm).
 struct LepeArgs {
   const void* v;
   void* o;
@@ -187,11 +187,14 @@ struct LepeArgs {
 int launch_layer_norm(const void* x, void* y, int64_t rows, int32_t C, const float* weight, const float* bias,
                       float eps, void* stream);
 int launch_lepe_add(const LepeArgs& a, void* stream);
-int launch_linear(const char* name, const void* x, const void* W, const void* bias, void* y, int64_t rows, int64_t k,
-                  int64_t n_out, void* lt_ws, void* stream);
-bool linear_available();
 int read_and_clear_module_error(void* stream, uint32_t* flags);
-size_t linear_workspace_bytes();
+// y[rows][n_out] = x[rows][k] w^T (+ bias), bf16, w [n_out][k] (nn.Linear's
+// layout); tcgen05 GEMM (gemm_kernels.cu).  k % 8 == 0, n_out % 8 == 0, x, w,
+// bias and y 16-byte aligned; name labels the launch for the kernel timer.
+bool gemm_supported(int64_t rows, int64_t k, int64_t n_out);
+int launch_gemm(const char* name, const void* x, const void* w, const void* bias, void* y, int64_t rows, int64_t k,
+                int64_t n_out, void* stream);
+int read_and_clear_gemm_error(void* stream, uint32_t* flags);
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }

@@ -3,19 +3,13 @@
 // to_qkv, lepe, to_out and forward):
 //
 //   xn = LayerNorm(x)                       mhla_ln_rows (one warp per token)
-//   qkv = xn W_qkv^T (+ b_qkv)              cuBLASLt GEMM, bias in its epilogue
+//   qkv = xn W_qkv^T (+ b_qkv)              mhla_gemm (gemm_kernels.cu), bias in its epilogue
 //   o = MHLA(q, k, v)                       the core, reading q, k, v in place
 //                                           from the qkv rows (strided views)
 //   o += lepe(v) = dwconv5x5(v) + b_lepe    mhla_lepe_add (one pass over v and o)
-//   y = o W_out^T (+ b_out)                 cuBLASLt GEMM, bias in its epilogue
-//
-// The projections are plain GEMMs and go to cuBLASLt, which is loaded at run
-// time (dlopen), so the library loads on machines without it and only the
-// module call reports MHLA_ERR_UNSUPPORTED there.
-#include <cublasLt.h>
+//   y = o W_out^T (+ b_out)                 mhla_gemm, bias in its epilogue
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <dlfcn.h>
 
 #include <algorithm>
 #include <cmath>
@@ -50,11 +44,49 @@ __global__ void __launch_bounds__(256) mhla_ln_rows(const __nv_bfloat16* __restr
   const int nu = C / 8;   // 16-byte units per row
   const uint4* src = reinterpret_cast<const uint4*>(x + row * C);
   uint4 v[NV];
-  float s = 0.0f;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
     const int u = lane + 32 * k;
     v[k] = u < nu ? src[u] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  const float2 st = ln_row_stats<NV>(v, C, eps, lane);
+  uint4* dst = reinterpret_cast<uint4*>(y + row * C);
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int u = lane + 32 * k;
+    if (u >= nu) continue;
+    const float4 ga = reinterpret_cast<const float4*>(weight)[2 * u], gb = reinterpret_cast<const float4*>(weight)[2 * u + 1];
+    const float4 ba = reinterpret_cast<const float4*>(bias)[2 * u], bb = reinterpret_cast<const float4*>(bias)[2 * u + 1];
+    const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+    const float bt[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+    dst[u] = ln_apply8(v[k], st.x, st.y, g, bt);
+  }
+}
+
+// Rows of C <= 512: one row per half warp (16 lanes, NU 16-byte units each), so
+// an SM keeps twice as many rows in flight as with a warp per row; the same
+// statistics (mean, then the biased variance from the deviations) reduced
+// within the half warp.
+template <int NU>
+__global__ void __launch_bounds__(256) mhla_ln_rows_half(const __nv_bfloat16* __restrict__ x,
+                                                         __nv_bfloat16* __restrict__ y, int64_t rows, int32_t C,
+                                                         const float* __restrict__ weight,
+                                                         const float* __restrict__ bias, float eps) {
+  const int lane = threadIdx.x & 15;
+  const unsigned mask = 0xFFFFu << (threadIdx.x & 16);   // this half warp's lanes
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4);
+  if (row >= rows) return;
+  const int nu = C / 8;
+  const uint4* src = reinterpret_cast<const uint4*>(x + row * C);
+  uint4 v[NU];
+#pragma unroll
+  for (int k = 0; k < NU; ++k) {
+    const int u = lane + 16 * k;
+    v[k] = u < nu ? src[u] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int k = 0; k < NU; ++k) {
     const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -63,12 +95,12 @@ __global__ void __launch_bounds__(256) mhla_ln_rows(const __nv_bfloat16* __restr
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(mask, s, o, 16);
   const float mean = s / static_cast<float>(C);
   float q = 0.0f;
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    if (lane + 32 * k >= nu) continue;
+  for (int k = 0; k < NU; ++k) {
+    if (lane + 16 * k >= nu) continue;
     const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -79,28 +111,18 @@ __global__ void __launch_bounds__(256) mhla_ln_rows(const __nv_bfloat16* __restr
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+  for (int o = 8; o > 0; o >>= 1) q += __shfl_xor_sync(mask, q, o, 16);
   const float rstd = rsqrtf(q / static_cast<float>(C) + eps);
   uint4* dst = reinterpret_cast<uint4*>(y + row * C);
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int u = lane + 32 * k;
+  for (int k = 0; k < NU; ++k) {
+    const int u = lane + 16 * k;
     if (u >= nu) continue;
-    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
     const float4 ga = reinterpret_cast<const float4*>(weight)[2 * u], gb = reinterpret_cast<const float4*>(weight)[2 * u + 1];
     const float4 ba = reinterpret_cast<const float4*>(bias)[2 * u], bb = reinterpret_cast<const float4*>(bias)[2 * u + 1];
     const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
     const float bt[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
-    uint32_t out[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
-      const float a = (__low2float(b2) - mean) * rstd * g[2 * e] + bt[2 * e];
-      const float b = (__high2float(b2) - mean) * rstd * g[2 * e + 1] + bt[2 * e + 1];
-      const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
-      out[e] = *reinterpret_cast<const uint32_t*>(&r);
-    }
-    dst[u] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[u] = ln_apply8(v[k], mean, rstd, g, bt);
   }
 }
 
@@ -110,7 +132,7 @@ __global__ void __launch_bounds__(256) mhla_ln_rows(const __nv_bfloat16* __restr
 // pairs), channel chunk slowest.  Per patch two TMA loads land in one of two
 // stage buffers: v with its 2-token halo, [12][20][64] bf16, whose out-of-frame
 // elements read as zero (the convolution's padding), and the o tile,
-// [8][16][64] bf16.  Thread (pair q = lane, row y, strip s) convolves 8 tokens
+// [8][16][64] bf16.  Thread (pair q = lane, row y, strip s) convolves kLpSX tokens
 // of its row for its two channels with packed float32 FMAs and adds them into
 // the o tile in place (the 32 lanes of a warp touch 128 contiguous bytes, no
 // bank conflicts); one TMA store then writes the tile back, clipped at the
@@ -120,7 +142,8 @@ constexpr int kLpTY = 8, kLpTX = 16, kLpHY = kLpTY + 4, kLpHX = kLpTX + 4;
 constexpr int kLpV = kLpHY * kLpHX * 128;                     // v patch bytes
 constexpr int kLpO = kLpTY * kLpTX * 128;                     // o tile bytes
 constexpr int kLpStage = kLpV + kLpO;
-constexpr int kLpThreads = 32 * kLpTY * (kLpTX / 8);          // 512: warp = (row, strip)
+constexpr int kLpSX = 16;                                     // tokens of a row one thread convolves
+constexpr int kLpThreads = 32 * kLpTY * (kLpTX / kLpSX);      // 256: warp = (row, strip)
 constexpr size_t kLpSmem = 2 * kLpStage + 25 * 64 * 4 + 64 * 4 + 64 + 128;
 
 struct LpGeom {
@@ -182,7 +205,7 @@ __global__ void __launch_bounds__(kLpThreads, 2) mhla_lepe_add(const __grid_cons
   }
   __syncthreads();
 
-  const int y = warp % kLpTY, s = warp / kLpTY;   // output row, 8-token strip
+  const int y = warp % kLpTY, s = warp / kLpTY;   // output row, strip of kLpSX tokens
   const int ch = 2 * lane;
   int cur_chunk = -1;
   uint32_t k = 0;
@@ -205,17 +228,17 @@ __global__ void __launch_bounds__(kLpThreads, 2) mhla_lepe_add(const __grid_cons
     if (!__syncthreads_and(ok)) break;
 
     if (lane < pairs) {
-      const uint8_t* pl = stage + st * kLpStage + (y * kLpHX + s * 8) * 128 + lane * 4;
-      uint32_t* ot = reinterpret_cast<uint32_t*>(stage + st * kLpStage + kLpV + (y * kLpTX + s * 8) * 128) + lane;
-      uint64_t acc[8];
+      const uint8_t* pl = stage + st * kLpStage + (y * kLpHX + s * kLpSX) * 128 + lane * 4;
+      uint32_t* ot = reinterpret_cast<uint32_t*>(stage + st * kLpStage + kLpV + (y * kLpTX + s * kLpSX) * 128) + lane;
+      uint64_t acc[kLpSX];
       const uint64_t bias2 = *reinterpret_cast<const uint64_t*>(bsm + ch);
 #pragma unroll
-      for (int x = 0; x < 8; ++x) acc[x] = bias2;
+      for (int x = 0; x < kLpSX; ++x) acc[x] = bias2;
 #pragma unroll
       for (int i = 0; i < 5; ++i) {
-        uint64_t vv[12];
+        uint64_t vv[kLpSX + 4];
 #pragma unroll
-        for (int c = 0; c < 12; ++c) {   // bf16 pair -> float32 pair (exact)
+        for (int c = 0; c < kLpSX + 4; ++c) {   // bf16 pair -> float32 pair (exact)
           const uint32_t w = *reinterpret_cast<const uint32_t*>(pl + (i * kLpHX + c) * 128);
           vv[c] = static_cast<uint64_t>(w << 16) | (static_cast<uint64_t>(w & 0xFFFF0000u) << 32);
         }
@@ -223,12 +246,12 @@ __global__ void __launch_bounds__(kLpThreads, 2) mhla_lepe_add(const __grid_cons
         for (int j = 0; j < 5; ++j) {
           const uint64_t w2 = *reinterpret_cast<const uint64_t*>(wsm + (i * 5 + j) * 64 + ch);
 #pragma unroll
-          for (int x = 0; x < 8; ++x) acc[x] = fma2(w2, vv[x + j], acc[x]);
+          for (int x = 0; x < kLpSX; ++x) acc[x] = fma2(w2, vv[x + j], acc[x]);
         }
       }
       // o + (bias + conv), rounded once, in place in the o tile
 #pragma unroll
-      for (int x = 0; x < 8; ++x) {
+      for (int x = 0; x < kLpSX; ++x) {
         const uint32_t ow = ot[x * 32];
         const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(&ow);
         const __nv_bfloat162 r =
@@ -256,121 +279,6 @@ __global__ void __launch_bounds__(kLpThreads, 2) mhla_lepe_add(const __grid_cons
   }
 }
 
-// ------------------------------------------------------------ cuBLASLt loader
-
-struct LtApi {
-  decltype(&cublasLtCreate) create = nullptr;
-  decltype(&cublasLtMatmulDescCreate) desc_create = nullptr;
-  decltype(&cublasLtMatmulDescSetAttribute) desc_set = nullptr;
-  decltype(&cublasLtMatmulDescDestroy) desc_destroy = nullptr;
-  decltype(&cublasLtMatrixLayoutCreate) layout_create = nullptr;
-  decltype(&cublasLtMatrixLayoutDestroy) layout_destroy = nullptr;
-  decltype(&cublasLtMatmulPreferenceCreate) pref_create = nullptr;
-  decltype(&cublasLtMatmulPreferenceSetAttribute) pref_set = nullptr;
-  decltype(&cublasLtMatmulPreferenceDestroy) pref_destroy = nullptr;
-  decltype(&cublasLtMatmulAlgoGetHeuristic) heuristic = nullptr;
-  decltype(&cublasLtMatmul) matmul = nullptr;
-  bool ok = false;   // every entry point found
-};
-
-const LtApi& lt_api() {
-  static LtApi api;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    const char* names[] = {"libcublasLt.so.13", "libcublasLt.so", "/usr/local/cuda/lib64/libcublasLt.so.13",
-                           "/usr/local/cuda/targets/sbsa-linux/lib/libcublasLt.so.13",
-                           "/usr/local/cuda/targets/x86_64-linux/lib/libcublasLt.so.13"};
-    void* h = nullptr;
-    for (const char* n : names)
-      if ((h = dlopen(n, RTLD_NOW | RTLD_LOCAL)) != nullptr) break;
-    if (!h) return;
-    auto sym = [&](auto& fn, const char* name) {
-      fn = reinterpret_cast<std::remove_reference_t<decltype(fn)>>(dlsym(h, name));
-      return fn != nullptr;
-    };
-    bool all = sym(api.create, "cublasLtCreate") && sym(api.desc_create, "cublasLtMatmulDescCreate") &&
-               sym(api.desc_set, "cublasLtMatmulDescSetAttribute") &&
-               sym(api.desc_destroy, "cublasLtMatmulDescDestroy") &&
-               sym(api.layout_create, "cublasLtMatrixLayoutCreate") &&
-               sym(api.layout_destroy, "cublasLtMatrixLayoutDestroy") &&
-               sym(api.pref_create, "cublasLtMatmulPreferenceCreate") &&
-               sym(api.pref_set, "cublasLtMatmulPreferenceSetAttribute") &&
-               sym(api.pref_destroy, "cublasLtMatmulPreferenceDestroy") &&
-               sym(api.heuristic, "cublasLtMatmulAlgoGetHeuristic") && sym(api.matmul, "cublasLtMatmul");
-    api.ok = all;
-  });
-  return api;
-}
-
-// One cuBLASLt handle per device, created on first use with that device
-// current; null when the device cannot be used.
-cublasLtHandle_t lt_handle() {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static cublasLtHandle_t handles[kMaxDevices] = {};
-  const LtApi& lt = lt_api();
-  int dev = -1;
-  if (!lt.ok || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(mu);
-  if (!handles[dev] && lt.create(&handles[dev]) != CUBLAS_STATUS_SUCCESS) handles[dev] = nullptr;
-  return handles[dev];
-}
-
-constexpr size_t kLtWorkspace = size_t{32} << 20;
-
-// y[rows][n_out] = x[rows][k] W^T (+ bias[n_out]), W [n_out][k], all bf16 and
-// row-major, float32 accumulation.  In cuBLASLt's column-major terms:
-// y^T (n_out x rows) = op_T(W stored k x n_out) * x^T (k x rows).
-int linear_bf16(const char* name, const void* x, const void* W, const void* bias, void* y, int64_t rows, int64_t k,
-                int64_t n_out, void* lt_ws, cudaStream_t stream) {
-  const LtApi& lt = lt_api();
-  const cublasLtHandle_t handle = lt_handle();
-  if (!handle) return MHLA_ERR_UNSUPPORTED;
-  cublasLtMatmulDesc_t op = nullptr;
-  cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
-  cublasLtMatmulPreference_t pref = nullptr;
-  int rc = MHLA_ERR_CUDA;
-  do {
-    if (lt.desc_create(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS) break;
-    const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
-    if (lt.desc_set(op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta)) != CUBLAS_STATUS_SUCCESS) break;
-    if (lt.desc_set(op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)) != CUBLAS_STATUS_SUCCESS) break;
-    if (bias) {
-      const cublasLtEpilogue_t epi = CUBLASLT_EPILOGUE_BIAS;
-      if (lt.desc_set(op, CUBLASLT_MATMUL_DESC_EPILOGUE, &epi, sizeof(epi)) != CUBLAS_STATUS_SUCCESS) break;
-      if (lt.desc_set(op, CUBLASLT_MATMUL_DESC_BIAS_POINTER, &bias, sizeof(bias)) != CUBLAS_STATUS_SUCCESS) break;
-    }
-    if (lt.layout_create(&la, CUDA_R_16BF, static_cast<uint64_t>(k), static_cast<uint64_t>(n_out), k) !=
-            CUBLAS_STATUS_SUCCESS ||
-        lt.layout_create(&lb, CUDA_R_16BF, static_cast<uint64_t>(k), static_cast<uint64_t>(rows), k) !=
-            CUBLAS_STATUS_SUCCESS ||
-        lt.layout_create(&lc, CUDA_R_16BF, static_cast<uint64_t>(n_out), static_cast<uint64_t>(rows), n_out) !=
-            CUBLAS_STATUS_SUCCESS)
-      break;
-    if (lt.pref_create(&pref) != CUBLAS_STATUS_SUCCESS) break;
-    const uint64_t wsb = kLtWorkspace;
-    if (lt.pref_set(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb, sizeof(wsb)) != CUBLAS_STATUS_SUCCESS) break;
-    cublasLtMatmulHeuristicResult_t res{};
-    int found = 0;
-    if (lt.heuristic(handle, op, la, lb, lc, lc, pref, 1, &res, &found) != CUBLAS_STATUS_SUCCESS || found < 1) {
-      rc = MHLA_ERR_UNSUPPORTED;
-      break;
-    }
-    const float alpha = 1.0f, beta = 0.0f;
-    KernelTimer timer(name, stream);
-    if (lt.matmul(handle, op, &alpha, W, la, x, lb, &beta, y, lc, y, lc, &res.algo, lt_ws, kLtWorkspace, stream) !=
-        CUBLAS_STATUS_SUCCESS)
-      break;
-    rc = MHLA_OK;
-  } while (false);
-  if (pref) lt.pref_destroy(pref);
-  if (lc) lt.layout_destroy(lc);
-  if (lb) lt.layout_destroy(lb);
-  if (la) lt.layout_destroy(la);
-  if (op) lt.desc_destroy(op);
-  return rc;
-}
-
 }  // namespace
 
 // ------------------------------------------------------------- host entries
@@ -383,8 +291,12 @@ int launch_layer_norm(const void* x, void* y, int64_t rows, int32_t C, const flo
   auto* yo = static_cast<__nv_bfloat16*>(y);
   KernelTimer timer("mhla_ln_rows", stream);
   const int nv = (C / 8 + 31) / 32;
-  if (nv <= 1) mhla_ln_rows<1><<<grid, 256, 0, s>>>(xi, yo, rows, C, weight, bias, eps);
-  else if (nv <= 2) mhla_ln_rows<2><<<grid, 256, 0, s>>>(xi, yo, rows, C, weight, bias, eps);
+  const unsigned grid_half = static_cast<unsigned>((rows + 15) / 16);
+  const int nu16 = (C / 8 + 15) / 16;   // units per lane of a half warp
+  if (nu16 <= 1) mhla_ln_rows_half<1><<<grid_half, 256, 0, s>>>(xi, yo, rows, C, weight, bias, eps);
+  else if (nu16 <= 2) mhla_ln_rows_half<2><<<grid_half, 256, 0, s>>>(xi, yo, rows, C, weight, bias, eps);
+  else if (nu16 <= 3) mhla_ln_rows_half<3><<<grid_half, 256, 0, s>>>(xi, yo, rows, C, weight, bias, eps);
+  else if (nu16 <= 4) mhla_ln_rows_half<4><<<grid_half, 256, 0, s>>>(xi, yo, rows, C, weight, bias, eps);
   else if (nv <= 4) mhla_ln_rows<4><<<grid, 256, 0, s>>>(xi, yo, rows, C, weight, bias, eps);
   else mhla_ln_rows<8><<<grid, 256, 0, s>>>(xi, yo, rows, C, weight, bias, eps);
   return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
@@ -425,14 +337,5 @@ int launch_lepe_add(const LepeArgs& a, void* stream) {
 int read_and_clear_module_error(void* stream, uint32_t* flags) {
   return read_and_clear_word(g_module_error, stream, flags);
 }
-
-int launch_linear(const char* name, const void* x, const void* W, const void* bias, void* y, int64_t rows, int64_t k,
-                  int64_t n_out, void* lt_ws, void* stream) {
-  return linear_bf16(name, x, W, bias, y, rows, k, n_out, lt_ws, static_cast<cudaStream_t>(stream));
-}
-
-bool linear_available() { return lt_handle() != nullptr; }
-
-size_t linear_workspace_bytes() { return kLtWorkspace; }
 
 }  // namespace mhla

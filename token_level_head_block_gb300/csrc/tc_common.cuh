@@ -127,6 +127,62 @@ static __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// LayerNorm of a row of C bf16 values held by one warp, lane holding the
+// 16-byte units lane, lane + 32, ... (zeros past C): the mean, then the biased
+// variance from the deviations, both reduced in the same order by every
+// kernel that normalises, so they agree bit for bit.  Returns (mean, rstd).
+template <int NV>
+static __device__ __forceinline__ float2 ln_row_stats(const uint4 (&v)[NV], int32_t C, float eps, int lane) {
+  const int nu = C / 8;
+  float s = 0.0f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+      s += __low2float(b2) + __high2float(b2);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float mean = s / static_cast<float>(C);
+  float q = 0.0f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    if (lane + 32 * k >= nu) continue;
+    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+      const float a = __low2float(b2) - mean, b = __high2float(b2) - mean;
+      q = fmaf(a, a, q);
+      q = fmaf(b, b, q);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+  return make_float2(mean, rsqrtf(q / static_cast<float>(C) + eps));
+}
+
+// Eight bf16 values of a row normalised, scaled and shifted, rounded once to
+// bf16: y = (x - mean) rstd g + b.  Every LayerNorm in the library applies it
+// through this function, so a fused normalisation equals the stand-alone one.
+static __device__ __forceinline__ uint4 ln_apply8(uint4 raw, float mean, float rstd, const float (&g)[8],
+                                                  const float (&bt)[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[e]);
+    const float a = (__low2float(b2) - mean) * rstd * g[2 * e] + bt[2 * e];
+    const float b = (__high2float(b2) - mean) * rstd * g[2 * e + 1] + bt[2 * e + 1];
+    const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+    out[e] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 // 16-byte chunk position inside a swizzled row: 128-byte swizzle for d = 64
 // (row r XORs chunk bits with r mod 8), 64-byte swizzle for d = 32.
 template <int D>
