@@ -388,6 +388,20 @@ mhla_status_t mhla_module_forward(const void* x, void* y, int64_t B, int64_t N, 
  * non-zero, MHLA_ERR_CUDA when the copy failed. */
 mhla_status_t mhla_device_status(void* stream, uint32_t* flags);
 
+/* Diagnostic hook for testing the timeout path of the device-side waits (no
+ * counterpart in the method).  With warp >= 0, every bounded mbarrier wait made
+ * by warp index `warp` of any kernel of this library that does not find its
+ * phase complete at the first poll behaves as if the completion it waits for
+ * never came: it gives up after limit_ns nanoseconds
+ * (1 us .. 1 s), the kernel's other roles stop, copies already in flight are
+ * drained, tensor memory is released, and the next mhla_device_status reports
+ * MHLA_ERR_TIMEOUT (bit 0).  The outputs of calls made meanwhile are undefined.
+ * warp == -1 turns it off (the default).  Synchronous; call it only while no
+ * work of this library is queued or running.  Returns MHLA_ERR_INVALID_ARG for
+ * a warp outside -1 .. 31 or a limit outside the range, MHLA_ERR_CUDA when a
+ * copy to the device failed. */
+mhla_status_t mhla_debug_stall_waits(int32_t warp, uint64_t limit_ns);
+
 /* Per-kernel timing.  Between mhla_profile_begin and mhla_profile_end every
  * kernel the library launches is bracketed by a pair of CUDA events recorded on
  * its launch stream.  mhla_profile_end waits for those events, writes one entry

@@ -383,3 +383,13 @@ def test_noalloc_refuses_oversized_problems_before_touching_the_device(L):
             ctypes.byref(block), ctypes.byref(mhla.Phi(0, 1e-6)), ctypes.byref(o), None, 1)
     assert st == WORKSPACE
 
+
+
+def test_stall_hook_refuses_bad_arguments_on_the_host(L):
+    """The timeout-path diagnostic hook validates before touching the device."""
+    L.mhla_debug_stall_waits.argtypes = [ctypes.c_int32, ctypes.c_uint64]
+    L.mhla_debug_stall_waits.restype = ctypes.c_int
+    assert L.mhla_debug_stall_waits(-2, 0) == 1          # warp outside -1 .. 31
+    assert L.mhla_debug_stall_waits(32, 1000000) == 1
+    assert L.mhla_debug_stall_waits(1, 999) == 1         # limit below 1 us
+    assert L.mhla_debug_stall_waits(1, 2000000000) == 1  # limit above 1 s

@@ -130,6 +130,8 @@ def lib():
                                       ctypes.c_int64, P(ModuleParams), ctypes.c_void_p, P(Shape3), P(Shape3),
                                       P(Phi), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     L.mhla_module_forward.restype = ctypes.c_int
+    L.mhla_debug_stall_waits.argtypes = [ctypes.c_int32, ctypes.c_uint64]
+    L.mhla_debug_stall_waits.restype = ctypes.c_int
     L.mhla_device_status.argtypes = [ctypes.c_void_p, P(ctypes.c_uint32)]
     L.mhla_device_status.restype = ctypes.c_int
     L.mhla_status_string.argtypes = [ctypes.c_int32]
@@ -409,6 +411,13 @@ def profile_end():
     n = ctypes.c_int32(0)
     _check(lib().mhla_profile_end(buf, 32, ctypes.byref(n)), "mhla_profile_end")
     return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(min(n.value, 32))}
+
+
+def debug_stall_waits(warp, limit_ns=1_000_000):
+    """Diagnostic hook of the timeout path: warp >= 0 makes every bounded wait
+    of that warp index give up after limit_ns (the kernels then stop and report
+    MHLA_ERR_TIMEOUT through device_status); warp = -1 turns it off."""
+    _check(lib().mhla_debug_stall_waits(int(warp), int(limit_ns)), "mhla_debug_stall_waits")
 
 
 def device_status(stream=None):

@@ -26,7 +26,7 @@ CUDA_SOURCES = ["mhla_api.cu", "simt_kernels.cu", "tc_kernels.cu", "tc_summary.c
                 "small_kernels.cu", "bwd_tc_kernels.cu", "causal_tc_kernels.cu", "profile.cu", "noalloc.cu",
                 "module_kernels.cu", "gemm_kernels.cu"]
 CXX_SOURCES = ["mhla_init.cpp"]
-HEADERS = ["mhla_internal.h", "ptx.cuh", "tma_host.h", "tc_common.cuh", "tc_fwd_bodies.cuh"]
+HEADERS = ["mhla_internal.h", "ptx.cuh", "tma_host.h", "tc_common.cuh", "tc_fwd_bodies.cuh", "stall_hook.cuh"]
 
 
 def _nvcc():

@@ -319,9 +319,12 @@ tc_bwd_query(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
       uint32_t nA = 0, nB = 0, kA = 0, kB = 0;
       uint64_t t0 = globaltimer();
       uint32_t idle = 0;
+      // diagnostic hook (stall_hook.cuh): this issuer sees no completion at all
+      const bool stalled = stall_this_warp();
+      const uint64_t limit_ns = stalled ? c_stall_ns : kWaitLimitNs;
       while (itemB < n_items) {
         bool prog = false;
-        if (itemA < n_items && nA < nB + 2) {
+        if (!stalled && itemA < n_items && nA < nB + 2) {
           const uint32_t s = nA % NQ, acc = nA & 1u, sl = kA & 1u;
           if ((cA != 0 || mbar_test_wait(sfull + sl, (kA >> 1) & 1u)) &&
               mbar_test_wait(phid + s, (nA / NQ) & 1u) && mbar_test_wait(accfree + acc, ((nA >> 1) & 1u) ^ 1u)) {
@@ -376,7 +379,7 @@ tc_bwd_query(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
           t0 = globaltimer();
         } else if ((++idle & 63u) == 0) {
           if (*abortf) break;
-          if (globaltimer() - t0 > kWaitLimitNs || idle >= kWaitLimitPolls) {
+          if (globaltimer() - t0 > limit_ns || idle >= kWaitLimitPolls) {
             *abortf = 1u;
             atomicOr(&g_bwd_error, 1u);
             break;
@@ -1212,5 +1215,7 @@ int read_and_clear_bwd_error(void* stream, uint32_t* flags) {
   *flags = host;
   return host ? MHLA_ERR_TIMEOUT : MHLA_OK;
 }
+
+MHLA_DEFINE_STALL_SETTER(set_stall_bwd)
 
 }  // namespace mhla

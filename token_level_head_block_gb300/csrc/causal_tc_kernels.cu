@@ -605,4 +605,6 @@ int read_and_clear_causal_error(void* stream, uint32_t* flags) {
   return read_and_clear_word(g_causal_error, stream, flags);
 }
 
+MHLA_DEFINE_STALL_SETTER(set_stall_causal)
+
 }  // namespace mhla

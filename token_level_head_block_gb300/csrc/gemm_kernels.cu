@@ -385,4 +385,6 @@ int launch_gemm(const char* name, const void* x, const void* w, const void* bias
 
 int read_and_clear_gemm_error(void* stream, uint32_t* flags) { return read_and_clear_word(g_gemm_error, stream, flags); }
 
+MHLA_DEFINE_STALL_SETTER(set_stall_gemm)
+
 }  // namespace mhla

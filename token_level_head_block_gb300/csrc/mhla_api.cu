@@ -409,6 +409,19 @@ extern "C" mhla_status_t mhla_device_status(void* stream, uint32_t* flags) {
   return *flags ? MHLA_ERR_TIMEOUT : MHLA_OK;
 }
 
+extern "C" mhla_status_t mhla_debug_stall_waits(int32_t warp, uint64_t limit_ns) {
+  if (warp < -1 || warp >= 32) return MHLA_ERR_INVALID_ARG;
+  if (warp >= 0 && (limit_ns < 1000 || limit_ns > 1000000000ull)) return MHLA_ERR_INVALID_ARG;
+  const uint32_t w = warp < 0 ? 0u : static_cast<uint32_t>(warp) + 1u;
+  const uint64_t ns = warp < 0 ? 0 : limit_ns;
+  int (*const setters[])(uint32_t, uint64_t) = {set_stall_summary, set_stall_mix, set_stall_output,
+                                                set_stall_fused,   set_stall_small, set_stall_bwd,
+                                                set_stall_causal,  set_stall_module, set_stall_gemm};
+  for (auto set : setters)
+    if (set(w, ns) != MHLA_OK) return MHLA_ERR_CUDA;
+  return MHLA_OK;
+}
+
 extern "C" const char* mhla_status_string(int32_t status) {
   switch (status) {
     case MHLA_OK: return "ok";

@@ -144,6 +144,18 @@ int read_and_clear_output_error(void* stream, uint32_t* flags);
 int read_and_clear_device_error(void* stream, uint32_t* flags);
 int read_and_clear_small_error(void* stream, uint32_t* flags);
 
+// Each file's copy of the diagnostic stall hook (stall_hook.cuh): the warp
+// index + 1 whose bounded waits stall (0: off) and how long they last.
+int set_stall_summary(uint32_t warp_plus_1, uint64_t ns);
+int set_stall_mix(uint32_t warp_plus_1, uint64_t ns);
+int set_stall_output(uint32_t warp_plus_1, uint64_t ns);
+int set_stall_fused(uint32_t warp_plus_1, uint64_t ns);
+int set_stall_small(uint32_t warp_plus_1, uint64_t ns);
+int set_stall_bwd(uint32_t warp_plus_1, uint64_t ns);
+int set_stall_causal(uint32_t warp_plus_1, uint64_t ns);
+int set_stall_module(uint32_t warp_plus_1, uint64_t ns);
+int set_stall_gemm(uint32_t warp_plus_1, uint64_t ns);
+
 // Brackets one kernel launch with CUDA events on its stream while
 // mhla_profile_begin/end collection is active, and always with an NVTX range
 // named after the kernel (free when no profiler is attached).

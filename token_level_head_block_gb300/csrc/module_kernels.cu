@@ -338,4 +338,6 @@ int read_and_clear_module_error(void* stream, uint32_t* flags) {
   return read_and_clear_word(g_module_error, stream, flags);
 }
 
+MHLA_DEFINE_STALL_SETTER(set_stall_module)
+
 }  // namespace mhla

@@ -47,6 +47,7 @@
 
 #include "mhla_internal.h"
 #include "ptx.cuh"
+#include "stall_hook.cuh"
 #include "tma_host.h"
 
 namespace mhla {
@@ -97,6 +98,13 @@ struct SmallGeom {
 
 __device__ __noinline__ bool small_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
+  // diagnostic hook (stall_hook.cuh), looked at only once a wait has to poll
+  if (stall_this_warp()) {
+    stalled_wait(abort_flag);
+    *abort_flag = 1u;
+    atomicOr(&g_small_error, 1u);
+    return false;
+  }
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1; it < kSmallWaitPolls; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -491,5 +499,7 @@ int read_and_clear_small_error(void* stream, uint32_t* flags) {
   *flags = host;
   return host ? MHLA_ERR_TIMEOUT : MHLA_OK;
 }
+
+MHLA_DEFINE_STALL_SETTER(set_stall_small)
 
 }  // namespace mhla

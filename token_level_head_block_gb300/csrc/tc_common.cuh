@@ -13,6 +13,7 @@
 
 #include "mhla_internal.h"
 #include "ptx.cuh"
+#include "stall_hook.cuh"
 #include "tma_host.h"
 
 namespace mhla {
@@ -27,6 +28,14 @@ constexpr uint64_t kDrainLimitNs = 50000000ull;   // 50 ms for copies already in
 static __device__ __noinline__ bool wait_bounded_on(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                                     unsigned int* err) {
   if (mbar_try_wait(bar, parity)) return true;
+  // diagnostic hook (stall_hook.cuh), looked at only once a wait has to poll:
+  // for the chosen warp the completion never comes
+  if (stall_this_warp()) {
+    stalled_wait(abort_flag);
+    *abort_flag = 1u;
+    atomicOr(err, 1u);
+    return false;
+  }
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1; it < kWaitLimitPolls; ++it) {
     if (mbar_try_wait(bar, parity)) return true;

@@ -285,4 +285,6 @@ int read_and_clear_fused_error(void* stream, uint32_t* flags) {
   return read_and_clear_word(g_fused_error, stream, flags);
 }
 
+MHLA_DEFINE_STALL_SETTER(set_stall_fused)
+
 }  // namespace mhla

@@ -341,4 +341,6 @@ int tc_run_mix(const Problem& p, const void* Wm, int64_t Mp, const void* Sbuf, v
 
 int read_and_clear_mix_error(void* stream, uint32_t* flags) { return read_and_clear_word(g_mix_error, stream, flags); }
 
+MHLA_DEFINE_STALL_SETTER(set_stall_mix)
+
 }  // namespace mhla

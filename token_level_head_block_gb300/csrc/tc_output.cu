@@ -151,4 +151,6 @@ int tc_run_output(const Problem& p, const void* St, const float* zt, void* strea
 
 int read_and_clear_output_error(void* stream, uint32_t* flags) { return read_and_clear_word(g_out_error, stream, flags); }
 
+MHLA_DEFINE_STALL_SETTER(set_stall_output)
+
 }  // namespace mhla

@@ -150,4 +150,6 @@ int tc_run_summary(const Problem& p, const float* W, void* Wb, void* WbT, int64_
 
 int read_and_clear_summary_error(void* stream, uint32_t* flags) { return read_and_clear_word(g_sum_error, stream, flags); }
 
+MHLA_DEFINE_STALL_SETTER(set_stall_summary)
+
 }  // namespace mhla
