@@ -256,6 +256,44 @@ mhla_status_t mhla_forward_causal(const mhla_tensor_t* q, const mhla_tensor_t* k
                                   void* workspace, size_t workspace_bytes, void* stream,
                                   int32_t path);
 
+/* Device workspace mhla_backward_causal needs (bytes, a multiple of 256).  Host
+ * only; MHLA_ERR_SHAPE when the blocks are not contiguous token ranges. */
+mhla_status_t mhla_backward_causal_workspace_size(const mhla_tensor_t* q, const mhla_shape3_t* grid,
+                                                  const mhla_shape3_t* block, int32_t path, size_t* bytes);
+
+/* Gradients of mhla_forward_causal for chunkwise training ([P2] App. B "Causal
+ * MHLA" trains autoregressive models with the causal form; section 4 "Multi-Head
+ * Mixing" makes W learnable).  The pages print no backward pass; these are the
+ * chain-rule derivatives of the causal form above, for token t of query block
+ * i with C_t = S<_i + W[i][i] P_t and c_t = z<_i + W[i][i] y_t:
+ *   dnum_t = dout_t / den_t,   dden_t = -(dout_t . o_t) / den_t
+ *   dq_t   = (C_t dnum_t + dden_t c_t) * [q_t > 0]
+ *   dS<_i  = sum_{t in i} phi(q_t) dnum_t^T,  dz<_i = sum_{t in i} dden_t phi(q_t)
+ *   dW[i][i] = sum_{t in i} sum_{s in i, s <= t} (phi(q_t) . phi(k_s)) (v_s . dnum_t + dden_t)
+ *   dW[i][j] = <dS<_i, S_j> + dz<_i . z_j for j < i, 0 for j > i (summed over b, h)
+ *   dS_j   = sum_{i > j} W[i][j] dS<_i,       dz_j likewise
+ *   dv_s   = dS_j^T phi(k_s) + W[j][j] sum_{t in j, t >= s} (phi(q_t) . phi(k_s)) dnum_t
+ *   dk_s   = (dS_j v_s + dz_j + W[j][j] sum_{t in j, t >= s} phi(q_t) (dnum_t . v_s + dden_t))
+ *            * [k_s > 0]
+ * The forward's states are recomputed from k, v and W.
+ *   Arguments, aliasing rules and statuses as for mhla_backward; the blocks must
+ *   be contiguous ranges of raster-order tokens as for mhla_forward_causal, else
+ *   MHLA_ERR_SHAPE.  Entries W[i][j] with j > i are never read.
+ *   path: AUTO and SIMT run on CUDA cores (float32 arithmetic, any d <= 128,
+ *   bf16 or float32); TC, FUSED and TC_FUSED return MHLA_ERR_UNSUPPORTED.
+ *   workspace: at least mhla_backward_causal_workspace_size() bytes (about
+ *   3 B H M d (d + 1) + B H N (d + 1) floats), 256-byte aligned, or NULL with
+ *   workspace_bytes == 0 (stream-ordered allocation).
+ * B == 0 or H == 0 writes dW = 0 and nothing else. */
+mhla_status_t mhla_backward_causal(const mhla_tensor_t* q, const mhla_tensor_t* k,
+                                   const mhla_tensor_t* v, const float* W,
+                                   const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                                   const mhla_phi_t* phi, const mhla_tensor_t* dout,
+                                   const mhla_tensor_t* dq, const mhla_tensor_t* dk,
+                                   const mhla_tensor_t* dv, float* dW,
+                                   void* workspace, size_t workspace_bytes, void* stream,
+                                   int32_t path);
+
 /* mhla_forward for callers that must not allocate device memory -- the paper
  * has no counterpart to this; it is a property of the library, not the method.
  * Who needs it: code that runs the forward where device allocation is not

@@ -343,6 +343,48 @@ def test_causal_rejects_malformed_requests_before_any_launch(L):
     assert call_causal(L, *e, (32, 32), (8, 32)) == OK                         # empty batch: nothing queued
 
 
+def call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, W=FAKE + (1 << 36), dW=FAKE + (1 << 37),
+                         phi=(0, 1e-6), ws=None, ws_bytes=0, path=0):
+    return L.mhla_backward_causal(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.c_void_p(W),
+                                  ctypes.byref(mhla.shape3(grid)), ctypes.byref(mhla.shape3(block)),
+                                  ctypes.byref(mhla.Phi(*phi)), ctypes.byref(g), ctypes.byref(dq),
+                                  ctypes.byref(dk), ctypes.byref(dv), ctypes.c_void_p(dW) if dW else None,
+                                  ctypes.c_void_p(ws) if ws else None, ws_bytes, None, path)
+
+
+def test_causal_backward_rejects_malformed_requests_before_any_launch(L):
+    q, k, v, g, dq, dk, dv = seven(2, 1024, 3, 64)
+    grid, block = (1, 1024), (1, 64)
+    assert call_backward_causal(L, q, k, v, g, dq, dk, dv, (32, 32), (4, 4)) == SHAPE   # blocks not contiguous
+    assert call_backward_causal(L, q, k, v, g, dq, dk, dv, (1, 1000), (1, 8)) == SHAPE
+    dk2 = contig(2, 1024, 3, 32, base=dk.data)
+    assert call_backward_causal(L, q, k, v, g, dq, dk2, dv, grid, block) == SHAPE
+    assert call_backward_causal(L, q, k, v, g, dq, dq, dv, grid, block) == INVALID     # dq and dk alias
+    assert call_backward_causal(L, q, k, v, g, dq, dk, g, grid, block) == INVALID      # dv aliases dout
+    assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, W=0) == INVALID
+    assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, dW=0) == INVALID
+    assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, dW=FAKE + (1 << 36) + 64) == INVALID
+    assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, phi=(3, 1e-6)) == INVALID
+    assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, ws=FAKE + 7, ws_bytes=1 << 40) == WORKSPACE
+    assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, ws=FAKE, ws_bytes=16) == WORKSPACE
+    for path in (2, 3, 4):
+        assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, path=path) == UNSUPPORTED
+    assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, path=9) == INVALID
+    n = ctypes.c_size_t()
+    for path in (0, 1):
+        assert L.mhla_backward_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(grid)),
+                                                     ctypes.byref(mhla.shape3(block)), path,
+                                                     ctypes.byref(n)) == OK
+        BH, M, N, d = 6, 16, 1024, 64
+        need = 3 * BH * M * d * (d + 1) * 4 + BH * M * M * 4 + BH * M * 4 + BH * N * (d + 1) * 4
+        assert n.value % 256 == 0 and need <= n.value < need + 6 * 256
+    assert L.mhla_backward_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3((32, 32))),
+                                                 ctypes.byref(mhla.shape3((4, 4))), 0, ctypes.byref(n)) == SHAPE
+    assert L.mhla_backward_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(grid)),
+                                                 ctypes.byref(mhla.shape3(block)), 2,
+                                                 ctypes.byref(n)) == UNSUPPORTED
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     """With the library absent the binding raises on first use; it has no other
     path to fall back on (the package never imports the oracle)."""

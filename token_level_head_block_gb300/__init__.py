@@ -16,6 +16,7 @@ import numpy as np
 __all__ = [
     "MhlaError", "lib", "library_path", "num_blocks", "init_mixing", "workspace_size",
     "select_path", "forward", "forward_causal", "causal_workspace_size", "backward", "backward_workspace_size",
+    "backward_causal", "backward_causal_workspace_size",
     "device_status", "profile_begin", "layer_norm", "lepe_add", "module_forward",
     "module_workspace_size",
     "profile_end", "tensor_desc", "shape3",
@@ -115,6 +116,11 @@ def lib():
                                 P(Tensor), P(Tensor), P(Tensor), P(Tensor), ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int32]
     L.mhla_backward.restype = ctypes.c_int
+    L.mhla_backward_causal_workspace_size.argtypes = [P(Tensor), P(Shape3), P(Shape3), ctypes.c_int32,
+                                                      P(ctypes.c_size_t)]
+    L.mhla_backward_causal_workspace_size.restype = ctypes.c_int
+    L.mhla_backward_causal.argtypes = L.mhla_backward.argtypes
+    L.mhla_backward_causal.restype = ctypes.c_int
     L.mhla_layer_norm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                   ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p]
     L.mhla_layer_norm.restype = ctypes.c_int
@@ -316,6 +322,46 @@ def backward(q, k, v, W, dout, grid, block, phi="relu", eps=1e-6, dq=None, dk=No
                              ctypes.c_void_p(ws_ptr) if ws_ptr else None, ws_bytes,
                              ctypes.c_void_p(sptr) if sptr else None, PATHS[path])
     _check(st, "mhla_backward")
+    return dq, dk, dv, dW
+
+
+def backward_causal_workspace_size(q, grid, block, path="auto"):
+    n = ctypes.c_size_t(0)
+    _check(lib().mhla_backward_causal_workspace_size(ctypes.byref(_desc(q) if not isinstance(q, Tensor) else q),
+                                                     ctypes.byref(shape3(grid)), ctypes.byref(shape3(block)),
+                                                     PATHS[path], ctypes.byref(n)),
+           "mhla_backward_causal_workspace_size")
+    return int(n.value)
+
+
+def backward_causal(q, k, v, W, dout, grid, block, phi="relu", eps=1e-6, dq=None, dk=None, dv=None, dW=None,
+                    workspace=None, stream=None, path="auto"):
+    """Gradients (dq, dk, dv, dW) of ``forward_causal`` given dout = dL/d(out).
+
+    Arguments as for ``backward``; the blocks must be contiguous token ranges
+    as for ``forward_causal``.  dW is zero above the diagonal."""
+    import torch
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dW is None:
+        dW = torch.empty_like(W)
+    for name, x in (("W", W), ("dW", dW)):
+        if not x.is_contiguous() or x.dtype != torch.float32:
+            raise ValueError(f"{name} must be a contiguous float32 tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() *
+                                                            workspace.element_size())
+    st = lib().mhla_backward_causal(ctypes.byref(_desc(q)), ctypes.byref(_desc(k)), ctypes.byref(_desc(v)),
+                                    ctypes.c_void_p(W.data_ptr()), ctypes.byref(shape3(grid)),
+                                    ctypes.byref(shape3(block)), ctypes.byref(Phi(PHIS[phi], float(eps))),
+                                    ctypes.byref(_desc(dout)), ctypes.byref(_desc(dq)), ctypes.byref(_desc(dk)),
+                                    ctypes.byref(_desc(dv)), ctypes.c_void_p(dW.data_ptr()),
+                                    ctypes.c_void_p(ws_ptr) if ws_ptr else None, ws_bytes,
+                                    ctypes.c_void_p(sptr) if sptr else None, PATHS[path])
+    _check(st, "mhla_backward_causal")
     return dq, dk, dv, dW
 
 

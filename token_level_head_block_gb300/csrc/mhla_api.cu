@@ -258,36 +258,36 @@ extern "C" mhla_status_t mhla_backward_workspace_size(const mhla_tensor_t* q, co
   return MHLA_OK;
 }
 
-extern "C" mhla_status_t mhla_backward(const mhla_tensor_t* q, const mhla_tensor_t* k, const mhla_tensor_t* v,
-                                       const float* W, const mhla_shape3_t* grid, const mhla_shape3_t* block,
-                                       const mhla_phi_t* phi, const mhla_tensor_t* dout, const mhla_tensor_t* dq,
-                                       const mhla_tensor_t* dk, const mhla_tensor_t* dv, float* dW,
-                                       void* workspace, size_t workspace_bytes, void* stream, int32_t path) {
-  if (!phi) return MHLA_ERR_INVALID_ARG;
-  Problem p;
-  const int rc = build_problem(q, k, v, dout, grid, block, phi, /*check_alias=*/false, &p);
-  if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+namespace mhla {
+namespace {
+
+// The operand checks both backward entries share: dq, dk, dv shaped like q
+// (check_bwd_operands); every written tensor free of self-overlap and disjoint
+// from everything else (check_bwd_overlaps).
+int check_bwd_operands(const mhla_tensor_t* q, const mhla_tensor_t* dout, const mhla_tensor_t* dq,
+                       const mhla_tensor_t* dk, const mhla_tensor_t* dv, float* dW, BwdOperands* bo) {
   for (const mhla_tensor_t* t : {dq, dk, dv}) {
     const int rt = check_tensor(t);
-    if (rt != MHLA_OK) return static_cast<mhla_status_t>(rt);
+    if (rt != MHLA_OK) return rt;
     if (!same_shape(q, t)) return MHLA_ERR_SHAPE;
   }
-  BwdOperands bo;
-  bo.dout = Operand{dout->data, dout->stride_b, dout->stride_n, dout->stride_h};
-  bo.dq = Operand{dq->data, dq->stride_b, dq->stride_n, dq->stride_h};
-  bo.dk = Operand{dk->data, dk->stride_b, dk->stride_n, dk->stride_h};
-  bo.dv = Operand{dv->data, dv->stride_b, dv->stride_n, dv->stride_h};
-  bo.dW = dW;
-  int sel = 0;
-  const int rp = resolve_bwd_path(p, bo, path, &sel);
-  if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
+  bo->dout = Operand{dout->data, dout->stride_b, dout->stride_n, dout->stride_h};
+  bo->dq = Operand{dq->data, dq->stride_b, dq->stride_n, dq->stride_h};
+  bo->dk = Operand{dk->data, dk->stride_b, dk->stride_n, dk->stride_h};
+  bo->dv = Operand{dv->data, dv->stride_b, dv->stride_n, dv->stride_h};
+  bo->dW = dW;
+  return MHLA_OK;
+}
+
+int check_bwd_overlaps(const Problem& p, const mhla_tensor_t* q, const mhla_tensor_t* k, const mhla_tensor_t* v,
+                       const float* W, const mhla_tensor_t* dout, const mhla_tensor_t* dq, const mhla_tensor_t* dk,
+                       const mhla_tensor_t* dv, const float* dW) {
   if (!W || !dW) return MHLA_ERR_INVALID_ARG;
   const uintptr_t w_bytes = static_cast<uintptr_t>(p.M * p.M) * sizeof(float);
   const uintptr_t dw0 = reinterpret_cast<uintptr_t>(dW), dw1 = dw0 + w_bytes;
   const uintptr_t wi0 = reinterpret_cast<uintptr_t>(W), wi1 = wi0 + w_bytes;
   if (overlaps(dw0, dw1, wi0, wi1)) return MHLA_ERR_INVALID_ARG;
   if (p.B > 0 && p.H > 0) {
-    // Every written tensor is free of self-overlap and overlaps nothing else.
     uintptr_t lo[7], hi[7];
     const mhla_tensor_t* all[7] = {dq, dk, dv, q, k, v, dout};
     for (int a = 0; a < 7; ++a) span(all[a], &lo[a], &hi[a]);
@@ -300,21 +300,109 @@ extern "C" mhla_status_t mhla_backward(const mhla_tensor_t* q, const mhla_tensor
     for (int b = 3; b < 7; ++b)
       if (overlaps(lo[b], hi[b], dw0, dw1)) return MHLA_ERR_INVALID_ARG;
   }
-  const size_t need = (p.B == 0 || p.H == 0) ? 0 : bwd_workspace_for(p, sel);
+  return MHLA_OK;
+}
+
+// Runs a backward launcher with the caller's workspace or a stream-ordered
+// allocation; B == 0 or H == 0 only zeroes dW.
+template <typename Launch>
+int run_bwd(const Problem& p, float* dW, size_t need, void* workspace, size_t workspace_bytes, void* stream,
+            Launch launch) {
   void* ws = workspace;
   if (!ws && workspace_bytes != 0) return MHLA_ERR_WORKSPACE;
   if (ws && (workspace_bytes < need || reinterpret_cast<uintptr_t>(ws) % kAlign != 0)) return MHLA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.B == 0 || p.H == 0)   // no (b, h) contributes: dW is zero
-    return cudaMemsetAsync(dW, 0, w_bytes, s) == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+    return cudaMemsetAsync(dW, 0, static_cast<size_t>(p.M * p.M) * sizeof(float), s) == cudaSuccess ? MHLA_OK
+                                                                                                    : MHLA_ERR_CUDA;
   bool owned = false;
   if (!ws) {
     if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return MHLA_ERR_CUDA;
     owned = true;
   }
-  const int lr = sel == MHLA_PATH_TC ? launch_tc_bwd(p, W, bo, ws, stream) : launch_simt_bwd(p, W, bo, ws, stream);
+  const int lr = launch(ws);
   if (owned && cudaFreeAsync(ws, s) != cudaSuccess && lr == MHLA_OK) return MHLA_ERR_CUDA;
-  return static_cast<mhla_status_t>(lr);
+  return lr;
+}
+
+}  // namespace
+}  // namespace mhla
+
+extern "C" mhla_status_t mhla_backward(const mhla_tensor_t* q, const mhla_tensor_t* k, const mhla_tensor_t* v,
+                                       const float* W, const mhla_shape3_t* grid, const mhla_shape3_t* block,
+                                       const mhla_phi_t* phi, const mhla_tensor_t* dout, const mhla_tensor_t* dq,
+                                       const mhla_tensor_t* dk, const mhla_tensor_t* dv, float* dW,
+                                       void* workspace, size_t workspace_bytes, void* stream, int32_t path) {
+  if (!phi) return MHLA_ERR_INVALID_ARG;
+  Problem p;
+  const int rc = build_problem(q, k, v, dout, grid, block, phi, /*check_alias=*/false, &p);
+  if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+  BwdOperands bo;
+  const int ro = check_bwd_operands(q, dout, dq, dk, dv, dW, &bo);
+  if (ro != MHLA_OK) return static_cast<mhla_status_t>(ro);
+  int sel = 0;
+  const int rp = resolve_bwd_path(p, bo, path, &sel);
+  if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
+  const int rv = check_bwd_overlaps(p, q, k, v, W, dout, dq, dk, dv, dW);
+  if (rv != MHLA_OK) return static_cast<mhla_status_t>(rv);
+  const size_t need = (p.B == 0 || p.H == 0) ? 0 : bwd_workspace_for(p, sel);
+  return static_cast<mhla_status_t>(run_bwd(p, dW, need, workspace, workspace_bytes, stream, [&](void* ws) {
+    return sel == MHLA_PATH_TC ? launch_tc_bwd(p, W, bo, ws, stream) : launch_simt_bwd(p, W, bo, ws, stream);
+  }));
+}
+
+namespace mhla {
+namespace {
+
+// The causal backward runs on CUDA cores; TC is refused until it has a
+// tensor-core pipeline of its own.
+int resolve_causal_bwd_path(int32_t path, int* sel) {
+  if (path == MHLA_PATH_AUTO || path == MHLA_PATH_SIMT) { *sel = MHLA_PATH_SIMT; return MHLA_OK; }
+  if (path == MHLA_PATH_TC || path == MHLA_PATH_FUSED || path == MHLA_PATH_TC_FUSED) return MHLA_ERR_UNSUPPORTED;
+  return MHLA_ERR_INVALID_ARG;
+}
+
+}  // namespace
+}  // namespace mhla
+
+extern "C" mhla_status_t mhla_backward_causal_workspace_size(const mhla_tensor_t* q, const mhla_shape3_t* grid,
+                                                             const mhla_shape3_t* block, int32_t path,
+                                                             size_t* bytes) {
+  if (!bytes) return MHLA_ERR_INVALID_ARG;
+  Problem p;
+  const int rc = build_problem(q, q, q, q, grid, block, nullptr, /*check_alias=*/false, &p);
+  if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+  if (!blocks_contiguous(p)) return MHLA_ERR_SHAPE;
+  int sel = 0;
+  const int rp = resolve_causal_bwd_path(path, &sel);
+  if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
+  *bytes = (p.B == 0 || p.H == 0) ? 0 : simt_causal_bwd_workspace_bytes(p);
+  return MHLA_OK;
+}
+
+extern "C" mhla_status_t mhla_backward_causal(const mhla_tensor_t* q, const mhla_tensor_t* k,
+                                              const mhla_tensor_t* v, const float* W, const mhla_shape3_t* grid,
+                                              const mhla_shape3_t* block, const mhla_phi_t* phi,
+                                              const mhla_tensor_t* dout, const mhla_tensor_t* dq,
+                                              const mhla_tensor_t* dk, const mhla_tensor_t* dv, float* dW,
+                                              void* workspace, size_t workspace_bytes, void* stream, int32_t path) {
+  if (!phi) return MHLA_ERR_INVALID_ARG;
+  Problem p;
+  const int rc = build_problem(q, k, v, dout, grid, block, phi, /*check_alias=*/false, &p);
+  if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
+  if (!blocks_contiguous(p)) return MHLA_ERR_SHAPE;
+  BwdOperands bo;
+  const int ro = check_bwd_operands(q, dout, dq, dk, dv, dW, &bo);
+  if (ro != MHLA_OK) return static_cast<mhla_status_t>(ro);
+  int sel = 0;
+  const int rp = resolve_causal_bwd_path(path, &sel);
+  if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
+  const int rv = check_bwd_overlaps(p, q, k, v, W, dout, dq, dk, dv, dW);
+  if (rv != MHLA_OK) return static_cast<mhla_status_t>(rv);
+  const size_t need = (p.B == 0 || p.H == 0) ? 0 : simt_causal_bwd_workspace_bytes(p);
+  return static_cast<mhla_status_t>(run_bwd(p, dW, need, workspace, workspace_bytes, stream, [&](void* ws) {
+    return launch_simt_causal_bwd(p, W, bo, ws, stream);
+  }));
 }
 
 namespace mhla {

@@ -81,6 +81,11 @@ struct SimtBwdWorkspace {
 };
 size_t simt_bwd_workspace_bytes(const Problem& p);
 int launch_simt_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream);
+// Causal backward on CUDA cores (contiguous blocks, any d <= 128).  Workspace:
+// S_j, the mixed past S<_i (later dS_j), dS<_i, the dW partials and diagonal
+// shares, and dnum_t, dden_t per token (float32).
+size_t simt_causal_bwd_workspace_bytes(const Problem& p);
+int launch_simt_causal_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream);
 
 // Tensor-core backward (bf16, d in {32, 64}, the forward tensor-core path's
 // token geometry, TMA-friendly strides on every operand).  Workspace: Wb and

@@ -100,7 +100,8 @@ constexpr int kMixRows = 8;     // query blocks i per thread
 
 // S~ = W . S per (b, h), treating the d*(d+1) entries of every block as columns
 // (TRANS: W^T . S, the mixing step of the backward pass).
-// (PAST: only source blocks j < i, the mixed past summaries of causal MHLA.)
+// (PAST: only source blocks j < i, the mixed past summaries of causal MHLA;
+// with TRANS, only i > j: the reverse of that mixing in the causal backward.)
 template <bool TRANS, bool PAST = false>
 __global__ void __launch_bounds__(kMixThreads)
 simt_mix(const float* __restrict__ W, const float* __restrict__ Sz, float* __restrict__ Szt,
@@ -117,7 +118,7 @@ simt_mix(const float* __restrict__ W, const float* __restrict__ Sz, float* __res
       const float s = src[j * E];
 #pragma unroll
       for (int u = 0; u < kMixRows; ++u)
-        if (i0 + u < M && (!PAST || j < i0 + u))
+        if (i0 + u < M && (!PAST || (TRANS ? j > i0 + u : j < i0 + u)))
           acc[u] = fmaf(__ldg(TRANS ? W + j * M + i0 + u : W + (i0 + u) * M + j), s, acc[u]);
     }
 #pragma unroll
@@ -481,6 +482,290 @@ __global__ void simt_dw_reduce(const float* __restrict__ part, float* __restrict
   dW[x] = s;
 }
 
+// ============================================================================
+// Causal backward.  The pages print none; [P2] App. B "Causal MHLA" trains
+// with the chunkwise causal form and section 4 makes W learnable, so these are
+// the chain-rule derivatives of simt_causal_output's arithmetic.  Per (b, h)
+// and token t of query block i, with C_t = S<_i + W_ii P_t, c_t = z<_i + W_ii y_t
+// (P_t, y_t the block's prefix sums of phi(k_s) v_s^T and phi(k_s), s <= t):
+//   dnum_t = g_t / den_t,  dden_t = -(g_t . o_t) / den_t
+//   dphi(q_t) = C_t dnum_t + dden_t c_t
+//   dS<_i = sum_t phi(q_t) dnum_t^T,  dz<_i = sum_t dden_t phi(q_t)
+//   dW_ii = sum_t sum_{s <= t} (phi(q_t) . phi(k_s)) (v_s . dnum_t + dden_t)
+//   dW_ij = <dS<_i, S_j> + dz<_i . z_j  (j < i),   0 above the diagonal
+//   dS_j  = sum_{i > j} W_ij dS<_i,  dz_j likewise
+//   dv_s  = dS_j^T phi(k_s) + W_jj sum_{t >= s} (phi(q_t) . phi(k_s)) dnum_t
+//   dphi(k_s) = dS_j v_s + dz_j + W_jj sum_{t >= s} phi(q_t) (dnum_t . v_s + dden_t)
+// (t and s range over the block).  Kernels, in launch order:
+//   simt_summary, simt_mix<false, true>   S_j and the mixed past S<_i, z<_i
+//   simt_causal_bwd_query  per (b, h, i), 32-token chunks in order, the running
+//                          state C in shared memory: dq, dS<_i, dz<_i, the
+//                          (b, h) share of dW_ii, and dnum_t, dden_t to scratch
+//   simt_dw_partial, simt_dw_reduce_causal   dW below the diagonal, plus dW_ii
+//   simt_mix<true, true>   dS_j, dz_j
+//   simt_causal_bwd_key    per (b, h, j), chunks in reverse, the running
+//                          suffix state dS_j + W_jj sum_{later t} phi(q_t) dnum_t^T
+// ============================================================================
+constexpr int kCbThreads = 256;
+constexpr int kCbWarps = kCbThreads / 32;
+constexpr int kCbChunk = 32;    // one chunk token per lane in the score steps
+
+// ENT = ceil(d*d / 256) state entries per thread (P_t and dS<_i in registers).
+template <typename T, int ENT>
+__global__ void __launch_bounds__(kCbThreads)
+simt_causal_bwd_query(const T* __restrict__ q, Operand qo, const T* __restrict__ k, Operand ko,
+                      const T* __restrict__ v, Operand vo, const T* __restrict__ g_out, Operand go,
+                      T* __restrict__ dq, Operand dqo, TokenGeom g, int64_t H, int d, int phi_kind, float eps,
+                      const float* __restrict__ W, const float* __restrict__ Sp, float* __restrict__ dSp,
+                      float* __restrict__ diag, float* __restrict__ dn) {
+  extern __shared__ float sm[];
+  const int E = d * d, P = d + 1;
+  float* st = sm;                          // [d][d + 1] C = S<_i + W_ii P before the chunk
+  float* zs = st + d * P;                  // [d]        c = z<_i + W_ii y before the chunk
+  float* sq = zs + d;                      // [chunk][d]     phi(q_t)
+  float* sk = sq + kCbChunk * d;           // [chunk][d + 1] phi(k_s)   (lanes walk s)
+  float* sv = sk + kCbChunk * P;           // [chunk][d + 1] v_s
+  float* sdn = sv + kCbChunk * P;          // [chunk][d]     dnum_t
+  float* sdd = sdn + kCbChunk * d;         // [chunk]        dden_t
+  float* sab = sdd + kCbChunk;             // [warps][2][chunk] a_s = phi(q_t).phi(k_s), b_s = v_s.dnum_t + dden_t
+  float* red = sab + kCbWarps * 2 * kCbChunk;   // [warps]
+  const int64_t item = blockIdx.x;
+  const int64_t i = item % g.M, bh = item / g.M;
+  const int64_t b = bh / H, h = bh % H;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const float wii = __ldg(W + i * g.M + i);
+  const float* src = Sp + (bh * g.M + i) * static_cast<int64_t>(E + d);
+  for (int e = tid; e < E; e += kCbThreads) st[(e / d) * P + e % d] = src[e];
+  for (int r = tid; r < d; r += kCbThreads) zs[r] = src[E + r];
+  const T* qb = q + b * qo.sb + h * qo.sh;
+  const T* kb = k + b * ko.sb + h * ko.sh;
+  const T* vb = v + b * vo.sb + h * vo.sh;
+  const T* gb = g_out + b * go.sb + h * go.sh;
+  T* dqb = dq + b * dqo.sb + h * dqo.sh;
+  float* dnb = dn + (bh * g.M + i) * g.w * P;   // token rows: dnum_t (d), dden_t
+  float pr[ENT], acc[ENT];
+#pragma unroll
+  for (int m = 0; m < ENT; ++m) pr[m] = acc[m] = 0.0f;
+  float yr = 0.0f, zacc = 0.0f, dw = 0.0f;
+  float* mya = sab + warp * 2 * kCbChunk;
+  float* myb = mya + kCbChunk;
+  for (int64_t s0 = 0; s0 < g.w; s0 += kCbChunk) {
+    const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
+    __syncthreads();   // the state is complete and the previous chunk's rows are free
+    for (int e = tid; e < cnt * d; e += kCbThreads) {
+      const int sl = e / d, c = e % d;
+      const int64_t n = token_of(g, i, s0 + sl);
+      sq[sl * d + c] = phi_f(load_f(qb + n * qo.sn + c), phi_kind, eps);
+      sk[sl * P + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
+      sv[sl * P + c] = load_f(vb + n * vo.sn + c);
+    }
+    __syncthreads();
+    for (int sl = warp; sl < cnt; sl += kCbWarps) {
+      const float* myq = sq + sl * d;
+      float* mydn = sdn + sl * d;
+      float a = 0.0f;
+      if (lane <= sl)
+        for (int r = 0; r < d; ++r) a = fmaf(myq[r], sk[lane * P + r], a);
+      mya[lane] = a;
+      float den = 0.0f;
+      for (int r = lane; r < d; r += 32) den = fmaf(myq[r], zs[r], den);
+      den = warp_sum(fmaf(wii, a, den)) + eps;
+      __syncwarp();
+      const int64_t n = token_of(g, i, s0 + sl);
+      float* dnrow = dnb + (s0 + sl) * P;
+      float go_dot = 0.0f;
+      for (int c = lane; c < d; c += 32) {
+        float num = 0.0f, own = 0.0f;
+        for (int r = 0; r < d; ++r) num = fmaf(myq[r], st[r * P + c], num);
+        for (int s2 = 0; s2 <= sl; ++s2) own = fmaf(mya[s2], sv[s2 * P + c], own);
+        num = fmaf(wii, own, num);
+        const float gc = load_f(gb + n * go.sn + c);
+        go_dot = fmaf(gc, num, go_dot);
+        const float dnc = gc / den;
+        mydn[c] = dnc;
+        dnrow[c] = dnc;
+      }
+      go_dot = warp_sum(go_dot) / den;
+      const float dden = -go_dot / den;
+      if (lane == 0) {
+        sdd[sl] = dden;
+        dnrow[d] = dden;
+      }
+      __syncwarp();
+      float bb = 0.0f;
+      if (lane <= sl) {
+        for (int c = 0; c < d; ++c) bb = fmaf(sv[lane * P + c], mydn[c], bb);
+        bb += dden;
+      }
+      myb[lane] = bb;
+      dw = fmaf(a, bb, dw);   // own-chunk part of dW_ii (a = b = 0 past the token)
+      __syncwarp();
+      for (int r = lane; r < d; r += 32) {
+        float x = dden * zs[r], own = 0.0f;
+        for (int c = 0; c < d; ++c) x = fmaf(st[r * P + c], mydn[c], x);
+        for (int s2 = 0; s2 <= sl; ++s2) own = fmaf(sk[s2 * P + r], myb[s2], own);
+        x = fmaf(wii, own, x);
+        const float qr = load_f(qb + n * qo.sn + r);
+        store_f(dqb + n * dqo.sn + r, qr > 0.0f ? x : 0.0f);
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+    // dS<_i += X (the chunk's sum of phi(q_t) dnum_t^T); dW_ii += <P, X>; then
+    // P and the state advance by the chunk's phi(k_s) v_s^T.
+#pragma unroll
+    for (int m = 0; m < ENT; ++m) {
+      const int e = tid + m * kCbThreads;
+      if (e < E) {
+        const int r = e / d, c = e % d;
+        float x = 0.0f, dp = 0.0f;
+        for (int sl = 0; sl < cnt; ++sl) {
+          x = fmaf(sq[sl * d + r], sdn[sl * d + c], x);
+          dp = fmaf(sk[sl * P + r], sv[sl * P + c], dp);
+        }
+        dw = fmaf(pr[m], x, dw);
+        acc[m] += x;
+        pr[m] += dp;
+        st[r * P + c] = fmaf(wii, dp, st[r * P + c]);
+      }
+    }
+    if (tid < d) {
+      float x = 0.0f, dy = 0.0f;
+      for (int sl = 0; sl < cnt; ++sl) {
+        x = fmaf(sq[sl * d + tid], sdd[sl], x);
+        dy += sk[sl * P + tid];
+      }
+      dw = fmaf(yr, x, dw);
+      zacc += x;
+      yr += dy;
+      zs[tid] = fmaf(wii, dy, zs[tid]);
+    }
+  }
+  float* out = dSp + (bh * g.M + i) * static_cast<int64_t>(E + d);
+#pragma unroll
+  for (int m = 0; m < ENT; ++m) {
+    const int e = tid + m * kCbThreads;
+    if (e < E) out[e] = acc[m];
+  }
+  if (tid < d) out[E + tid] = zacc;
+  dw = warp_sum(dw);
+  if (lane == 0) red[warp] = dw;
+  __syncthreads();
+  if (tid == 0) {
+    float s = 0.0f;
+    for (int w = 0; w < kCbWarps; ++w) s += red[w];
+    diag[bh * g.M + i] = s;
+  }
+}
+
+// One CTA per (b, h, j), chunks of the block in reverse, one warp per source token.
+template <typename T>
+__global__ void __launch_bounds__(kCbThreads)
+simt_causal_bwd_key(const T* __restrict__ q, Operand qo, const T* __restrict__ k, Operand ko,
+                    const T* __restrict__ v, Operand vo, T* __restrict__ dk, Operand dko, T* __restrict__ dv,
+                    Operand dvo, TokenGeom g, int64_t H, int d, int phi_kind, float eps, const float* __restrict__ W,
+                    const float* __restrict__ dS, const float* __restrict__ dn) {
+  extern __shared__ float sm[];
+  const int E = d * d, P = d + 1;
+  float* gs = sm;                          // [d][d + 1] dS_j + W_jj sum over later chunks of phi(q_t) dnum_t^T
+  float* gz = gs + d * P;                  // [d]        dz_j + W_jj sum over later chunks of dden_t phi(q_t)
+  float* sq = gz + d;                      // [chunk][d + 1] phi(q_t)   (lanes walk t)
+  float* sdn = sq + kCbChunk * P;          // [chunk][d + 1] dnum_t
+  float* sdd = sdn + kCbChunk * P;         // [chunk]        dden_t
+  float* sk = sdd + kCbChunk;              // [chunk][d]     phi(k_s)
+  float* sv = sk + kCbChunk * d;           // [chunk][d]     v_s
+  float* sab = sv + kCbChunk * d;          // [warps][2][chunk] a_t = phi(q_t).phi(k_s), b_t = dnum_t.v_s + dden_t
+  const int64_t item = blockIdx.x;
+  const int64_t j = item % g.M, bh = item / g.M;
+  const int64_t b = bh / H, h = bh % H;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const float wjj = __ldg(W + j * g.M + j);
+  const float* src = dS + (bh * g.M + j) * static_cast<int64_t>(E + d);
+  for (int e = tid; e < E; e += kCbThreads) gs[(e / d) * P + e % d] = src[e];
+  for (int r = tid; r < d; r += kCbThreads) gz[r] = src[E + r];
+  const T* qb = q + b * qo.sb + h * qo.sh;
+  const T* kb = k + b * ko.sb + h * ko.sh;
+  const T* vb = v + b * vo.sb + h * vo.sh;
+  T* dkb = dk + b * dko.sb + h * dko.sh;
+  T* dvb = dv + b * dvo.sb + h * dvo.sh;
+  const float* dnb = dn + (bh * g.M + j) * g.w * P;
+  float* mya = sab + warp * 2 * kCbChunk;
+  float* myb = mya + kCbChunk;
+  const int64_t nch = (g.w + kCbChunk - 1) / kCbChunk;
+  for (int64_t ci = nch - 1; ci >= 0; --ci) {
+    const int64_t s0 = ci * kCbChunk;
+    const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
+    __syncthreads();   // the suffix state is complete and the later chunk's rows are free
+    for (int e = tid; e < cnt * d; e += kCbThreads) {
+      const int sl = e / d, c = e % d;
+      const int64_t n = token_of(g, j, s0 + sl);
+      sq[sl * P + c] = phi_f(load_f(qb + n * qo.sn + c), phi_kind, eps);
+      sdn[sl * P + c] = dnb[(s0 + sl) * P + c];
+      sk[sl * d + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
+      sv[sl * d + c] = load_f(vb + n * vo.sn + c);
+    }
+    for (int sl = tid; sl < cnt; sl += kCbThreads) sdd[sl] = dnb[(s0 + sl) * P + d];
+    __syncthreads();
+    for (int sl = warp; sl < cnt; sl += kCbWarps) {
+      const float* myk = sk + sl * d;
+      const float* myv = sv + sl * d;
+      float a = 0.0f, bt = 0.0f;
+      if (lane >= sl && lane < cnt) {   // lane = query token t >= s of this chunk
+        for (int r = 0; r < d; ++r) a = fmaf(sq[lane * P + r], myk[r], a);
+        for (int c = 0; c < d; ++c) bt = fmaf(sdn[lane * P + c], myv[c], bt);
+        bt += sdd[lane];
+      }
+      mya[lane] = a;
+      myb[lane] = bt;
+      __syncwarp();
+      const int64_t n = token_of(g, j, s0 + sl);
+      for (int c = lane; c < d; c += 32) {
+        float x = 0.0f, own = 0.0f;
+        for (int r = 0; r < d; ++r) x = fmaf(myk[r], gs[r * P + c], x);
+        for (int t = sl; t < cnt; ++t) own = fmaf(mya[t], sdn[t * P + c], own);
+        store_f(dvb + n * dvo.sn + c, fmaf(wjj, own, x));
+      }
+      for (int r = lane; r < d; r += 32) {
+        float x = gz[r], own = 0.0f;
+        for (int c = 0; c < d; ++c) x = fmaf(gs[r * P + c], myv[c], x);
+        for (int t = sl; t < cnt; ++t) own = fmaf(sq[t * P + r], myb[t], own);
+        x = fmaf(wjj, own, x);
+        const float kr = load_f(kb + n * ko.sn + r);
+        store_f(dkb + n * dko.sn + r, kr > 0.0f ? x : 0.0f);
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kCbThreads) {
+      const int r = e / d, c = e % d;
+      float x = 0.0f;
+      for (int t = 0; t < cnt; ++t) x = fmaf(sq[t * P + r], sdn[t * P + c], x);
+      gs[r * P + c] = fmaf(wjj, x, gs[r * P + c]);
+    }
+    if (tid < d) {
+      float x = 0.0f;
+      for (int t = 0; t < cnt; ++t) x = fmaf(sdd[t], sq[t * P + tid], x);
+      gz[tid] = fmaf(wjj, x, gz[tid]);
+    }
+  }
+}
+
+// Causal dW: the partials below the diagonal, the query kernel's W_ii shares
+// on it, zero above it; summed over (b, h) in a fixed order.
+__global__ void simt_dw_reduce_causal(const float* __restrict__ part, const float* __restrict__ diag,
+                                      float* __restrict__ dW, int64_t M, int64_t BH) {
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t MM = M * M;
+  if (x >= MM) return;
+  const int64_t i = x / M, j = x % M;
+  float s = 0.0f;
+  if (j < i)
+    for (int64_t bh = 0; bh < BH; ++bh) s += part[bh * MM + x];
+  else if (j == i)
+    for (int64_t bh = 0; bh < BH; ++bh) s += diag[bh * M + i];
+  dW[x] = s;
+}
+
 template <typename T>
 int launch_simt_typed(const Problem& p, const float* W, const SimtWorkspace& ws, cudaStream_t stream) {
   const TokenGeom g = token_geom(p);
@@ -686,6 +971,123 @@ int launch_simt_causal_typed(const Problem& p, const float* W, const SimtWorkspa
   }
 }
 
+struct SimtCausalBwdWorkspace {
+  float* Sz;     // [BH][M][d*(d+1)] S_j, z_j
+  float* Sp;     // [BH][M][d*(d+1)] S<_i, z<_i, later dS_j, dz_j
+  float* dSp;    // [BH][M][d*(d+1)] dS<_i, dz<_i
+  float* part;   // [BH][M][M]       <dS<_i, S_j> + dz<_i . z_j
+  float* diag;   // [BH][M]          the (b, h) share of dW_ii
+  float* dn;     // [BH][N][d + 1]   dnum_t, dden_t in block-slot order
+};
+
+SimtCausalBwdWorkspace simt_causal_bwd_carve(const Problem& p, void* base) {
+  const size_t per = static_cast<size_t>(p.BH()) * p.M * p.d * (p.d + 1) * sizeof(float);
+  const size_t part = static_cast<size_t>(p.BH()) * p.M * p.M * sizeof(float);
+  const size_t diag = static_cast<size_t>(p.BH()) * p.M * sizeof(float);
+  char* c = static_cast<char*>(base);
+  SimtCausalBwdWorkspace ws;
+  ws.Sz = reinterpret_cast<float*>(c);
+  ws.Sp = reinterpret_cast<float*>(c + align_up(per));
+  ws.dSp = reinterpret_cast<float*>(c + 2 * align_up(per));
+  ws.part = reinterpret_cast<float*>(c + 3 * align_up(per));
+  ws.diag = reinterpret_cast<float*>(c + 3 * align_up(per) + align_up(part));
+  ws.dn = reinterpret_cast<float*>(c + 3 * align_up(per) + align_up(part) + align_up(diag));
+  return ws;
+}
+
+template <typename T>
+int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOperands& bo,
+                                 const SimtCausalBwdWorkspace& ws, cudaStream_t stream) {
+  const TokenGeom g = token_geom(p);
+  const int d = static_cast<int>(p.d);
+  const int64_t BH = p.BH();
+  const int64_t items = BH * p.M;
+  if (items > 0x7fffffffLL || BH > 65535) return MHLA_ERR_UNSUPPORTED;
+  const T* qp = static_cast<const T*>(p.q.data);
+  const T* kp = static_cast<const T*>(p.k.data);
+  const T* vp = static_cast<const T*>(p.v.data);
+  const T* gp = static_cast<const T*>(bo.dout.data);
+  T* dqp = static_cast<T*>(bo.dq.data);
+  T* dkp = static_cast<T*>(bo.dk.data);
+  T* dvp = static_cast<T*>(bo.dv.data);
+  const int64_t E = p.d * (p.d + 1);
+  {
+    const size_t sum_smem = 2 * kSumChunk * d * sizeof(float);
+    KernelTimer timer("simt_summary", stream);
+    if (d <= 16)
+      simt_summary<T, 1><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    else if (d <= 32)
+      simt_summary<T, 4><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    else if (d <= 64)
+      simt_summary<T, 16><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    else
+      simt_summary<T, 64><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
+          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  const dim3 mix_grid(static_cast<unsigned>((E + kMixThreads - 1) / kMixThreads),
+                      static_cast<unsigned>((p.M + kMixRows - 1) / kMixRows),
+                      static_cast<unsigned>(std::min<int64_t>(BH, 65535)));
+  if (mix_grid.y > 65535) return MHLA_ERR_UNSUPPORTED;
+  {
+    KernelTimer timer("simt_mix", stream);
+    simt_mix<false, true><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.Sz, ws.Sp, p.M, E, BH);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  {
+    const size_t smem = (d * (d + 1) + d + kCbChunk * (2 * d + 2 * (d + 1) + 1) + kCbWarps * 2 * kCbChunk +
+                         kCbWarps) * sizeof(float);
+    auto launch = [&](auto kern) -> int {
+      if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem)) != cudaSuccess)
+        return MHLA_ERR_CUDA;
+      KernelTimer timer("simt_causal_bwd_query", stream);
+      kern<<<static_cast<unsigned>(items), kCbThreads, smem, stream>>>(
+          qp, p.q, kp, p.k, vp, p.v, gp, bo.dout, dqp, bo.dq, g, p.H, d, p.phi_kind, p.eps, W, ws.Sp, ws.dSp,
+          ws.diag, ws.dn);
+      return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+    };
+    const int rc = d <= 16   ? launch(simt_causal_bwd_query<T, 1>)
+                   : d <= 32 ? launch(simt_causal_bwd_query<T, 4>)
+                   : d <= 64 ? launch(simt_causal_bwd_query<T, 16>)
+                             : launch(simt_causal_bwd_query<T, 64>);
+    if (rc != MHLA_OK) return rc;
+  }
+  {
+    const dim3 grid(static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile),
+                    static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile), static_cast<unsigned>(BH));
+    if (grid.x > 65535) return MHLA_ERR_UNSUPPORTED;
+    KernelTimer timer("simt_dw", stream);
+    simt_dw_partial<<<grid, 256, 0, stream>>>(ws.dSp, ws.Sz, ws.part, p.M, E);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+    const int64_t MM = p.M * p.M;
+    simt_dw_reduce_causal<<<static_cast<unsigned>((MM + 255) / 256), 256, 0, stream>>>(ws.part, ws.diag, bo.dW,
+                                                                                       p.M, BH);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  {
+    KernelTimer timer("simt_mix", stream);
+    simt_mix<true, true><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.dSp, ws.Sp, p.M, E, BH);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  {
+    const size_t smem = (d * (d + 1) + d + kCbChunk * (2 * (d + 1) + 1 + 2 * d) + kCbWarps * 2 * kCbChunk) *
+                        sizeof(float);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(simt_causal_bwd_key<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return MHLA_ERR_CUDA;
+    KernelTimer timer("simt_causal_bwd_key", stream);
+    simt_causal_bwd_key<T><<<static_cast<unsigned>(items), kCbThreads, smem, stream>>>(
+        qp, p.q, kp, p.k, vp, p.v, dkp, bo.dk, dvp, bo.dv, g, p.H, d, p.phi_kind, p.eps, W, ws.Sp, ws.dn);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  }
+  return MHLA_OK;
+}
+
 }  // namespace
 
 int launch_simt_causal(const Problem& p, const float* W, void* workspace, void* stream) {
@@ -730,6 +1132,21 @@ int launch_simt_bwd(const Problem& p, const float* W, const BwdOperands& bo, voi
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.dtype == MHLA_BF16) return launch_simt_bwd_typed<__nv_bfloat16>(p, W, bo, ws, s);
   return launch_simt_bwd_typed<float>(p, W, bo, ws, s);
+}
+
+size_t simt_causal_bwd_workspace_bytes(const Problem& p) {
+  const size_t per = static_cast<size_t>(p.BH()) * p.M * p.d * (p.d + 1) * sizeof(float);
+  const size_t part = static_cast<size_t>(p.BH()) * p.M * p.M * sizeof(float);
+  const size_t diag = static_cast<size_t>(p.BH()) * p.M * sizeof(float);
+  const size_t dn = static_cast<size_t>(p.BH()) * p.M * p.w * (p.d + 1) * sizeof(float);
+  return 3 * align_up(per) + align_up(part) + align_up(diag) + align_up(dn);
+}
+
+int launch_simt_causal_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream) {
+  const SimtCausalBwdWorkspace ws = simt_causal_bwd_carve(p, workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.dtype == MHLA_BF16) return launch_simt_causal_bwd_typed<__nv_bfloat16>(p, W, bo, ws, s);
+  return launch_simt_causal_bwd_typed<float>(p, W, bo, ws, s);
 }
 
 }  // namespace mhla
