@@ -166,6 +166,7 @@ KERNEL_SOURCES = {"tc_summary": ("tc_summary.cu", "tc_fwd_bodies.cuh"), "tc_mix"
                   "tc_dw": "bwd_tc_kernels.cu", "simt_bwd_query": "simt_kernels.cu",
                   "simt_bwd_key": "simt_kernels.cu", "simt_dw": "simt_kernels.cu",
                   "simt_causal_output": "simt_kernels.cu", "tc_causal_tile": "causal_tc_kernels.cu",
+                  "simt_causal_bwd_query": "simt_kernels.cu", "simt_causal_bwd_key": "simt_kernels.cu",
                   "tc_tile_output": "causal_tc_kernels.cu", "mhla_lepe_add": "module_kernels.cu",
                   "mhla_ln_rows": "module_kernels.cu", "mhla_gemm_qkv": "gemm_kernels.cu",
                   "mhla_gemm_out": "gemm_kernels.cu"}
@@ -216,6 +217,10 @@ def kernel_work(wl, name):
         "tc_dw": ("tensor", 2 * M * M * BH * d * (d + 1)), "simt_dw": ("alu", 2 * M * M * BH * d * (d + 1)),
         # causal: read q, k, v, write o
         "simt_causal_output": ("hbm", 4 * io), "tc_causal_tile": ("hbm", 4 * io),
+        # causal backward: read q, k, v, dout, write dq and the float32 dnum, dden
+        # rows; read q, k, v and those rows, write dk, dv
+        "simt_causal_bwd_query": ("hbm", 5 * io + BH * wl.N * (d + 1) * 4),
+        "simt_causal_bwd_key": ("hbm", 5 * io + BH * wl.N * (d + 1) * 4),
         # readout of contiguous 64-token blocks: read q, write o
         "tc_tile_output": ("hbm", 2 * io),
         # module: x -> LayerNorm; qkv = xn W^T; o += lepe(v) (read v, o; write o); y = o W^T
