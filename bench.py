@@ -2,12 +2,13 @@
 """Throughput of the MHLA forward pass on GB300 (tokens/s and HBM roofline).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-                  [--pass forward|backward|causal|module]
+                  [--pass forward|backward|causal|causal_backward|module]
 
 One step = one MHLA forward (summaries, mixing GEMM, outputs) over
 one synthetic batch of the workload, inputs resident in HBM; with
 ``--pass backward`` one step is one backward pass (dq, dk, dv, dW for a seeded
-dout); with ``--pass causal`` one causal (chunkwise) MHLA forward; with ``--pass
+dout); with ``--pass causal`` one causal (chunkwise) MHLA forward and with
+``--pass causal_backward`` its backward pass; with ``--pass
 module`` one forward of the whole module around the core (LayerNorm, qkv
 projection, MHLA, 5 x 5 positional term, output projection) on x [B, N, H * d].  Rank 0 prints one
 JSON line.  With N > 1 (torchrun) every rank runs an independent batch on its own
@@ -38,9 +39,14 @@ from token_level_head_block_gb300.workloads import HEADLINE, WORKLOADS  # noqa: 
 METRIC = "MHLA forward tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
 METRIC_BWD = "MHLA backward (dq, dk, dv, dW) tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
 METRIC_CAUSAL = "causal MHLA forward tokens/sec at 1 GB300; achieved HBM GB/s as fraction of peak"
+METRIC_CAUSAL_BWD = ("causal MHLA backward (dq, dk, dv, dW) tokens/sec at 1 GB300; achieved HBM GB/s as fraction "
+                     "of peak")
 METRIC_MODULE = ("MHLA module forward (LayerNorm, qkv projection, MHLA, 5x5 positional term, output projection) "
                  "tokens/sec at 1 GB300")
-METRICS = {"forward": METRIC, "backward": METRIC_BWD, "causal": METRIC_CAUSAL, "module": METRIC_MODULE}
+METRICS = {"forward": METRIC, "backward": METRIC_BWD, "causal": METRIC_CAUSAL, "causal_backward": METRIC_CAUSAL_BWD,
+           "module": METRIC_MODULE}
+ORACLE_WHAT = {"forward": "oracle (blocked form)", "backward": "backward oracle", "causal": "causal oracle",
+               "causal_backward": "causal backward oracle"}
 UNIT = "tokens/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -263,7 +269,8 @@ def runs_of(n, total, what):
 
 
 def oracle_sample_rate(wl, q, k, v, W, budget_s, max_slices=None, g=None, causal=False):
-    """Times the oracle (the backward oracle when dout g is given) on (b, h)
+    """Times the oracle (the backward oracle when dout g is given; the causal
+    ones with ``causal``) on (b, h)
     slices until budget_s elapses (at least one slice).  Returns (tokens/s,
     slices, seconds); a slice of one head counts N / H tokens."""
     import oracle
@@ -274,7 +281,10 @@ def oracle_sample_rate(wl, q, k, v, W, budget_s, max_slices=None, g=None, causal
     while True:
         b, h = pairs[done % len(pairs)]
         sl = (slice(b, b + 1), slice(None), slice(h, h + 1), slice(None))
-        if causal:
+        if causal and g is not None:
+            oracle.backward_causal(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, as_f64(g[sl]), wl.grid, wl.block,
+                                   phi, wl.eps)
+        elif causal:
             oracle.forward_causal(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, wl.grid, wl.block, phi, wl.eps)
         elif g is None:
             oracle.forward(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, wl.grid, wl.block, phi, wl.eps)
@@ -352,8 +362,8 @@ def run_reference(args, wl):
         }))
         return
     q, k, v = draw_workload(wl)
-    g = draw_dout(wl) if args.pass_ == "backward" else None
-    causal = args.pass_ == "causal"
+    g = draw_dout(wl) if args.pass_ in ("backward", "causal_backward") else None
+    causal = args.pass_ in ("causal", "causal_backward")
     per_step = max(1, args.ref_slices)
     for _ in range(args.warmup):
         oracle_sample_rate(wl, q, k, v, W, 0.0, max_slices=1, g=g, causal=causal)
@@ -364,7 +374,7 @@ def run_reference(args, wl):
     total = sum(times)
     value = args.steps * per_step * wl.N / wl.H / total
     cores = blas_threads()
-    what = {"forward": "oracle (blocked form)", "backward": "backward oracle", "causal": "causal oracle"}[args.pass_]
+    what = ORACLE_WHAT[args.pass_]
     sample = (f"each step: {per_step} of the {wl.B * wl.H} (batch, head) slices of {wl.name}, "
               f"float64 numpy {what}; a slice counts N/H tokens")
     print(json.dumps({
@@ -390,7 +400,7 @@ def run_ours(args, wl):
     dist_init("nccl")
     mhla.lib()
 
-    bwd = args.pass_ == "backward"
+    bwd = args.pass_ in ("backward", "causal_backward")
     module = args.pass_ == "module"
     q_h, k_h, v_h = draw_workload(wl, seed=wl.seed + rank)      # each replica its own batch
     g_h = draw_dout(wl, seed=wl.seed + 100 + rank) if bwd else None
@@ -419,11 +429,14 @@ def run_ours(args, wl):
     elif bwd:
         g = g_h.to(dev)
         dq, dk, dv, dW = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(W)
-        ws = torch.empty(mhla.backward_workspace_size(q, wl.grid, wl.block), dtype=torch.uint8, device=dev)
+        causal_bwd = args.pass_ == "causal_backward"
+        ws_size = mhla.backward_causal_workspace_size if causal_bwd else mhla.backward_workspace_size
+        bwd_call = mhla.backward_causal if causal_bwd else mhla.backward
+        ws = torch.empty(ws_size(q, wl.grid, wl.block), dtype=torch.uint8, device=dev)
 
         def step():
-            mhla.backward(q, k, v, W, g, wl.grid, wl.block, phi=wl.phi, eps=wl.eps, dq=dq, dk=dk, dv=dv, dW=dW,
-                          workspace=ws, stream=stream)
+            bwd_call(q, k, v, W, g, wl.grid, wl.block, phi=wl.phi, eps=wl.eps, dq=dq, dk=dk, dv=dv, dW=dW,
+                     workspace=ws, stream=stream)
     else:
         ws = torch.empty(mhla.workspace_size(q, wl.grid, wl.block, args.path), dtype=torch.uint8, device=dev)
 
@@ -470,22 +483,40 @@ def run_ours(args, wl):
     value = whole_job_throughput(wl.tokens, world, args.steps, max_el)
     ms_per_step = 1e3 * max_el / args.steps
 
-    # e2e: host buffers in pinned memory, copies inside the timed region
+    # e2e: host buffers in pinned memory, copies inside the timed region.  The
+    # batch elements of a forward (plain, causal or module) are independent, so
+    # the step is cut into batch chunks on three streams: the H2D copy of chunk
+    # c + 1, the library call on chunk c and the D2H copy of chunk c - 1 overlap.
+    # The backward's dW sums over the batch, so its copies stay serial.
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (t.pin_memory() for t in (q_h, k_h, v_h))
+        n_chunks = min(wl.B, 8)
+        bounds = [(c * wl.B // n_chunks, (c + 1) * wl.B // n_chunks) for c in range(n_chunks)]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         if module:
             hx, hy = x_h.pin_memory(), torch.empty_like(x_h).pin_memory()
+            ins, outs = [(x, hx)], [(hy, y)]
 
-            def e2e_step():
-                x.copy_(hx, non_blocking=True)
-                step()
-                hy.copy_(y, non_blocking=True)
+            def call(b0, b1):
+                mhla.module_forward(x[b0:b1], params, W, wl.grid, wl.block, wl.H, phi=wl.phi, eps=wl.eps,
+                                    out=y[b0:b1], workspace=ws, stream=stream)
         elif bwd:
             hg = g_h.pin_memory()
             hdq, hdk, hdv = (torch.empty_like(q_h).pin_memory() for _ in range(3))
             hdW = torch.empty(dW.shape, dtype=dW.dtype).pin_memory()
+        else:
+            ho = torch.empty_like(q_h).pin_memory()
+            ins, outs = [(q, hq), (k, hk), (v, hv)], [(ho, out)]
+            causal = args.pass_ == "causal"
 
+            def call(b0, b1):
+                fn = mhla.forward_causal if causal else mhla.forward
+                kw = {} if causal else {"path": args.path}
+                fn(q[b0:b1], k[b0:b1], v[b0:b1], W, wl.grid, wl.block, phi=wl.phi, eps=wl.eps, out=out[b0:b1],
+                   workspace=ws, stream=stream, **kw)
+
+        if bwd:
             def e2e_step():
                 for dst, src in ((q, hq), (k, hk), (v, hv), (g, hg)):
                     dst.copy_(src, non_blocking=True)
@@ -493,14 +524,19 @@ def run_ours(args, wl):
                 for dst, src in ((hdq, dq), (hdk, dk), (hdv, dv), (hdW, dW)):
                     dst.copy_(src, non_blocking=True)
         else:
-            ho = torch.empty_like(q_h).pin_memory()
-
             def e2e_step():
-                q.copy_(hq, non_blocking=True)
-                k.copy_(hk, non_blocking=True)
-                v.copy_(hv, non_blocking=True)
-                step()
-                ho.copy_(out, non_blocking=True)
+                s_in.wait_stream(stream)             # the previous step has fully finished
+                for b0, b1 in bounds:
+                    with torch.cuda.stream(s_in):
+                        for dst, src in ins:
+                            dst[b0:b1].copy_(src[b0:b1], non_blocking=True)
+                    stream.wait_stream(s_in)
+                    call(b0, b1)
+                    s_out.wait_stream(stream)
+                    with torch.cuda.stream(s_out):
+                        for dst, src in outs:
+                            dst[b0:b1].copy_(src[b0:b1], non_blocking=True)
+                stream.wait_stream(s_out)            # the step ends when its last copy has landed
 
         for _ in range(2):
             e2e_step()
@@ -510,7 +546,9 @@ def run_ours(args, wl):
         e2e = {"value": whole_job_throughput(wl.tokens, world, n_e2e, el_e2e), "unit": UNIT,
                "h2d_bytes_per_step": io if module else (4 if bwd else 3) * io,
                "d2h_bytes_per_step": 3 * io + wl.M * wl.M * 4 if bwd else io, "steps": n_e2e,
-               "ms_per_step": 1e3 * el_e2e / n_e2e}
+               "ms_per_step": 1e3 * el_e2e / n_e2e,
+               "copies": "serial on the compute stream (dW sums over the batch)" if bwd else
+                         f"{n_chunks} batch chunks; H2D, library call and D2H on three streams, overlapped"}
 
     # roofline of the dominant kernel, from the per-kernel events of pass B
     peaks, peak_src = load_peaks()
@@ -552,9 +590,8 @@ def run_ours(args, wl):
                          "module oracle"}
     elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, n, el = oracle_sample_rate(wl, q_h, k_h, v_h, W_h, args.cpu_seconds, g=g_h,
-                                         causal=args.pass_ == "causal")
-        what = {"forward": "oracle (blocked form)", "backward": "backward oracle",
-                "causal": "causal oracle"}[args.pass_]
+                                         causal=args.pass_ in ("causal", "causal_backward"))
+        what = ORACLE_WHAT[args.pass_]
         cpu = {"value": rate, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                "sample": f"{runs_of(n, wl.B * wl.H, '(batch, head) slices')} of {wl.name} in {el:.1f} s, "
                          f"float64 numpy {what}; a slice counts N/H tokens"}
@@ -594,7 +631,7 @@ def main():
     ap.add_argument("--sustain", type=float, default=2.0, help="seconds of load before timing (clock samples)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU oracle baseline")
     ap.add_argument("--ref-slices", type=int, default=1, help="(batch, head) slices per reference step")
-    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "causal", "module"], default="forward")
+    ap.add_argument("--pass", dest="pass_", choices=sorted(METRICS), default="forward")
     ap.add_argument("--path", default="auto", choices=["auto", "tc", "tc_fused", "simt", "fused"],
                     help="forward kernels (auto: what the library picks; tc_fused: the single persistent launch)")
     ap.add_argument("--no-e2e", action="store_true")
