@@ -128,26 +128,32 @@ __global__ void __launch_bounds__(256) mhla_ln_rows_half(const __nv_bfloat16* __
 
 // ------------------------------------------------------- LePE (5 x 5 depthwise)
 
-// Persistent CTAs walk 8 x 16 token patches of one frame and 64 channels (32
-// pairs), channel chunk slowest.  Per patch two TMA loads land in one of two
+// Persistent CTAs each walk one contiguous run of 8 x 16 token patches of one
+// frame and 64 channels (32 pairs), channel chunk slowest, so a CTA changes
+// chunk (and reloads the 5 x 5 weights) at most a few times and its
+// neighbouring patches share their halos in L2.  Per patch two TMA loads land in one of two
 // stage buffers: v with its 2-token halo, [12][20][64] bf16, whose out-of-frame
 // elements read as zero (the convolution's padding), and the o tile,
-// [8][16][64] bf16.  Thread (pair q = lane, row y, strip s) convolves kLpSX tokens
-// of its row for its two channels with packed float32 FMAs and adds them into
-// the o tile in place (the 32 lanes of a warp touch 128 contiguous bytes, no
-// bank conflicts); one TMA store then writes the tile back, clipped at the
-// frame and channel edges.  The next patch's loads run while this one is
-// convolved; the 5 x 5 weights are reloaded only when the chunk changes.
+// [8][16][64] bf16.  Eight compute warps: thread (pair q = lane, row y, strip s)
+// convolves kLpSX tokens of its row for its two channels with packed float32
+// FMAs and adds them into the o tile in place (the 32 lanes of a warp touch 128
+// contiguous bytes, no bank conflicts), then reports the stage done.  A ninth
+// warp stores each finished o tile by TMA (clipped at the frame and channel
+// edges); the v patch two ahead loads into the stage at once (the store does not
+// read it), that patch's o tile once the store has read the old one, so the
+// compute warps never wait on a store.
 constexpr int kLpTY = 8, kLpTX = 16, kLpHY = kLpTY + 4, kLpHX = kLpTX + 4;
 constexpr int kLpV = kLpHY * kLpHX * 128;                     // v patch bytes
 constexpr int kLpO = kLpTY * kLpTX * 128;                     // o tile bytes
 constexpr int kLpStage = kLpV + kLpO;
 constexpr int kLpSX = 16;                                     // tokens of a row one thread convolves
-constexpr int kLpThreads = 32 * kLpTY * (kLpTX / kLpSX);      // 256: warp = (row, strip)
-constexpr size_t kLpSmem = 2 * kLpStage + 25 * 64 * 4 + 64 * 4 + 64 + 128;
+constexpr int kLpWorkers = 32 * kLpTY * (kLpTX / kLpSX);      // 256: warp = (row, strip)
+constexpr int kLpThreads = kLpWorkers + 32;                   // + the store / load warp
+constexpr uint32_t kLpBar = 1;                                // named barrier of the compute warps
+constexpr size_t kLpSmem = 2 * kLpStage + 25 * 64 * 4 + 64 * 4 + 4 * 8 + 8 + 128;
 
 struct LpGeom {
-  int64_t ntiles;
+  uint32_t ntiles;                  // below 2^31 (checked on the host)
   int32_t C, B, T, Y, X, ntx, nty;
 };
 
@@ -167,115 +173,158 @@ __global__ void __launch_bounds__(kLpThreads, 2) mhla_lepe_add(const __grid_cons
   uint8_t* stage = smem;                                              // [2] (v patch, o tile)
   float* wsm = reinterpret_cast<float*>(smem + 2 * kLpStage);         // [25 taps][64 channels]
   float* bsm = wsm + 25 * 64;                                         // [64]
-  uint64_t* full = reinterpret_cast<uint64_t*>(bsm + 64);             // [2]
-  volatile uint32_t* abortf = reinterpret_cast<volatile uint32_t*>(full + 2);
+  uint64_t* full = reinterpret_cast<uint64_t*>(bsm + 64);             // [2] patch and o tile landed
+  uint64_t* done = full + 2;                                          // [2] compute warps finished the o tile
+  volatile uint32_t* abortf = reinterpret_cast<volatile uint32_t*>(full + 4);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t frames = static_cast<int64_t>(g.B) * g.T;
+  const uint32_t frames = static_cast<uint32_t>(g.B) * static_cast<uint32_t>(g.T);
+  // this CTA's tiles [t_lo, t_hi)
+  const uint32_t t_lo = static_cast<uint32_t>(static_cast<uint64_t>(g.ntiles) * blockIdx.x / gridDim.x);
+  const uint32_t t_hi = static_cast<uint32_t>(static_cast<uint64_t>(g.ntiles) * (blockIdx.x + 1) / gridDim.x);
 
-  // tile -> (chunk, frame, ty, tx), tx fastest
-  auto decode = [&](int64_t t, int& chunk, int64_t& frame, int& ty, int& tx) {
-    tx = static_cast<int>(t % g.ntx);
-    int64_t r = t / g.ntx;
-    ty = static_cast<int>(r % g.nty);
-    r /= g.nty;
+  // tile -> (chunk, frame, ty, tx), tx fastest (32-bit arithmetic)
+  auto decode = [&](uint32_t t, int& chunk, int64_t& frame, int& ty, int& tx) {
+    tx = static_cast<int>(t % static_cast<uint32_t>(g.ntx));
+    uint32_t r = t / static_cast<uint32_t>(g.ntx);
+    ty = static_cast<int>(r % static_cast<uint32_t>(g.nty));
+    r /= static_cast<uint32_t>(g.nty);
     frame = r % frames;
     chunk = static_cast<int>(r / frames);
   };
-  uint32_t issued[2] = {0u, 0u};
-  auto issue = [&](int st, int64_t t) {
-    int chunk, ty, tx;
-    int64_t frame;
-    decode(t, chunk, frame, ty, tx);
-    const int32_t tf = static_cast<int32_t>(frame % g.T), b = static_cast<int32_t>(frame / g.T);
-    const uint64_t pol = policy_evict_first();
-    mbar_arrive_expect_tx(full + st, kLpStage);
-    tma_load_5d(stage + st * kLpStage, &tm_v, full + st, chunk * 64, tx * kLpTX - 2, ty * kLpTY - 2, tf, b, pol);
-    tma_load_5d(stage + st * kLpStage + kLpV, &tm_o, full + st, chunk * 64, tx * kLpTX, ty * kLpTY, tf, b, pol);
-    ++issued[st];
-  };
-  if (tid == 0) {
-    mbar_init(full, 1);
-    mbar_init(full + 1, 1);
+  if (tid == kLpWorkers) {
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(full + st, 2);            // the v patch and the o tile, loaded separately
+      mbar_init(done + st, kLpWorkers / 32);
+    }
     *abortf = 0u;
     fence_mbar_init();
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_o);
-    for (int st = 0; st < 2; ++st)
-      if (static_cast<int64_t>(blockIdx.x) + st * gridDim.x < g.ntiles) issue(st, blockIdx.x + st * gridDim.x);
   }
   __syncthreads();
 
-  const int y = warp % kLpTY, s = warp / kLpTY;   // output row, strip of kLpSX tokens
-  const int ch = 2 * lane;
-  int cur_chunk = -1;
-  uint32_t k = 0;
-  for (int64_t t = blockIdx.x; t < g.ntiles; t += gridDim.x, ++k) {
-    int chunk, ty, tx;
-    int64_t frame;
-    decode(t, chunk, frame, ty, tx);
-    const int c0 = chunk * 64;
-    const int pairs = min(32, (g.C - c0) / 2);   // a multiple of 4
-    if (chunk != cur_chunk) {                    // the previous patch is done (barrier below)
-      for (int e = tid; e < pairs * 2 * 25; e += kLpThreads) {
-        const int c = e / 25, tap = e % 25;
-        wsm[tap * 64 + c] = weight[static_cast<int64_t>(c0 + c) * 25 + tap];
+  if (warp == kLpWorkers / 32) {
+    // ------------------------------------------------------------ stores and loads
+    if (lane == 0) {
+      uint32_t issued[2] = {0u, 0u};
+      auto issue = [&](int st, uint32_t t, bool v_part) {
+        int chunk, ty, tx;
+        int64_t frame;
+        decode(t, chunk, frame, ty, tx);
+        const int32_t tf = static_cast<int32_t>(frame % g.T), b = static_cast<int32_t>(frame / g.T);
+        const uint64_t pol = policy_evict_first();
+        if (v_part) {
+          mbar_arrive_expect_tx(full + st, kLpV);
+          tma_load_5d(stage + st * kLpStage, &tm_v, full + st, chunk * 64, tx * kLpTX - 2, ty * kLpTY - 2, tf, b,
+                      pol);
+        } else {
+          mbar_arrive_expect_tx(full + st, kLpO);
+          tma_load_5d(stage + st * kLpStage + kLpV, &tm_o, full + st, chunk * 64, tx * kLpTX, ty * kLpTY, tf, b,
+                      pol);
+          ++issued[st];
+        }
+      };
+      for (int st = 0; st < 2; ++st)
+        if (t_lo + st < t_hi) {
+          issue(st, t_lo + st, true);
+          issue(st, t_lo + st, false);
+        }
+      uint32_t k = 0;
+      for (uint32_t t = t_lo; t < t_hi; ++t, ++k) {
+        const int st = static_cast<int>(k & 1u);
+        if (!wait_bounded_on(done + st, (k >> 1) & 1u, abortf, &g_module_error)) break;
+        int chunk, ty, tx;
+        int64_t frame;
+        decode(t, chunk, frame, ty, tx);
+        const int32_t tf = static_cast<int32_t>(frame % g.T), b = static_cast<int32_t>(frame / g.T);
+        tma_store_5d(&tm_o, stage + st * kLpStage + kLpV, chunk * 64, tx * kLpTX, ty * kLpTY, tf, b);
+        bulk_commit_group();
+        if (t + 2 < t_hi) {
+          issue(st, t + 2, true);                 // the compute warps are done with the patch
+          bulk_wait_group_read<0>();              // the store has read the o tile: reload it
+          issue(st, t + 2, false);
+        }
       }
-      for (int e = tid; e < pairs * 2; e += kLpThreads) bsm[e] = bias[c0 + e];
-      cur_chunk = chunk;
+      bulk_wait_group0();
+      for (int st = 0; st < 2; ++st)
+        if (issued[st]) drain_wait_on(full + st, (issued[st] - 1) & 1u, &g_module_error);
     }
-    const int st = static_cast<int>(k & 1u);
-    const bool ok = warp_wait_on(full + st, (k >> 1) & 1u, abortf, &g_module_error);
-    if (!__syncthreads_and(ok)) break;
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const int y = warp % kLpTY, s = warp / kLpTY;   // output row, strip of kLpSX tokens
+    const int ch = 2 * lane;
+    int cur_chunk = -1;
+    uint32_t k = 0;
+    for (uint32_t t = t_lo; t < t_hi; ++t, ++k) {
+      int chunk, ty, tx;
+      int64_t frame;
+      decode(t, chunk, frame, ty, tx);
+      const int c0 = chunk * 64;
+      const int pairs = min(32, (g.C - c0) / 2);   // a multiple of 4
+      if (chunk != cur_chunk) {
+        // the chunk's 64 x 25 weights and 64 biases: every load in flight at once
+        constexpr int kPer = (64 * 25 + kLpWorkers - 1) / kLpWorkers;
+        float wv[kPer];
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) {
+          const int e = tid + r * kLpWorkers;
+          wv[r] = e < pairs * 2 * 25 ? __ldg(weight + static_cast<int64_t>(c0) * 25 + e) : 0.0f;
+        }
+        const float bv = tid < pairs * 2 ? __ldg(bias + c0 + tid) : 0.0f;
+        // every compute warp is done with the previous chunk's weights (the
+        // chunk sequence and every exit below are the same for all of them)
+        named_bar_sync(kLpBar, kLpWorkers);
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) {
+          const int e = tid + r * kLpWorkers;   // = channel * 25 + tap
+          if (e < pairs * 2 * 25) wsm[(e % 25) * 64 + e / 25] = wv[r];
+        }
+        if (tid < pairs * 2) bsm[tid] = bv;
+        cur_chunk = chunk;
+      }
+      const int st = static_cast<int>(k & 1u);
+      const bool ok = warp_wait_on(full + st, (k >> 1) & 1u, abortf, &g_module_error);
+      // one verdict for all compute warps; also orders the weights before their use
+      if (!named_bar_and(kLpBar, kLpWorkers, ok)) break;
 
-    if (lane < pairs) {
-      const uint8_t* pl = stage + st * kLpStage + (y * kLpHX + s * kLpSX) * 128 + lane * 4;
-      uint32_t* ot = reinterpret_cast<uint32_t*>(stage + st * kLpStage + kLpV + (y * kLpTX + s * kLpSX) * 128) + lane;
-      uint64_t acc[kLpSX];
-      const uint64_t bias2 = *reinterpret_cast<const uint64_t*>(bsm + ch);
+      if (lane < pairs) {
+        const uint8_t* pl = stage + st * kLpStage + (y * kLpHX + s * kLpSX) * 128 + lane * 4;
+        uint32_t* ot =
+            reinterpret_cast<uint32_t*>(stage + st * kLpStage + kLpV + (y * kLpTX + s * kLpSX) * 128) + lane;
+        uint64_t acc[kLpSX];
+        const uint64_t bias2 = *reinterpret_cast<const uint64_t*>(bsm + ch);
 #pragma unroll
-      for (int x = 0; x < kLpSX; ++x) acc[x] = bias2;
+        for (int x = 0; x < kLpSX; ++x) acc[x] = bias2;
 #pragma unroll
-      for (int i = 0; i < 5; ++i) {
-        uint64_t vv[kLpSX + 4];
+        for (int i = 0; i < 5; ++i) {
+          uint64_t vv[kLpSX + 4];
 #pragma unroll
-        for (int c = 0; c < kLpSX + 4; ++c) {   // bf16 pair -> float32 pair (exact)
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(pl + (i * kLpHX + c) * 128);
-          vv[c] = static_cast<uint64_t>(w << 16) | (static_cast<uint64_t>(w & 0xFFFF0000u) << 32);
+          for (int c = 0; c < kLpSX + 4; ++c) {   // bf16 pair -> float32 pair (exact)
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(pl + (i * kLpHX + c) * 128);
+            vv[c] = static_cast<uint64_t>(w << 16) | (static_cast<uint64_t>(w & 0xFFFF0000u) << 32);
+          }
+#pragma unroll
+          for (int j = 0; j < 5; ++j) {
+            const uint64_t w2 = *reinterpret_cast<const uint64_t*>(wsm + (i * 5 + j) * 64 + ch);
+#pragma unroll
+            for (int x = 0; x < kLpSX; ++x) acc[x] = fma2(w2, vv[x + j], acc[x]);
+          }
         }
+        // o + (bias + conv), rounded once, in place in the o tile
 #pragma unroll
-        for (int j = 0; j < 5; ++j) {
-          const uint64_t w2 = *reinterpret_cast<const uint64_t*>(wsm + (i * 5 + j) * 64 + ch);
-#pragma unroll
-          for (int x = 0; x < kLpSX; ++x) acc[x] = fma2(w2, vv[x + j], acc[x]);
+        for (int x = 0; x < kLpSX; ++x) {
+          const uint32_t ow = ot[x * 32];
+          const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(&ow);
+          const __nv_bfloat162 r =
+              __floats2bfloat162_rn(__low2float(o2) + __uint_as_float(static_cast<uint32_t>(acc[x])),
+                                    __high2float(o2) + __uint_as_float(static_cast<uint32_t>(acc[x] >> 32)));
+          ot[x * 32] = *reinterpret_cast<const uint32_t*>(&r);
         }
       }
-      // o + (bias + conv), rounded once, in place in the o tile
-#pragma unroll
-      for (int x = 0; x < kLpSX; ++x) {
-        const uint32_t ow = ot[x * 32];
-        const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(&ow);
-        const __nv_bfloat162 r =
-            __floats2bfloat162_rn(__low2float(o2) + __uint_as_float(static_cast<uint32_t>(acc[x])),
-                                  __high2float(o2) + __uint_as_float(static_cast<uint32_t>(acc[x] >> 32)));
-        ot[x * 32] = *reinterpret_cast<const uint32_t*>(&r);
-      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(done + st);
     }
-    fence_proxy_async_smem();
-    __syncthreads();                             // the o tile is complete; the weights are free
-    if (tid == 0) {
-      const int32_t tf = static_cast<int32_t>(frame % g.T), b = static_cast<int32_t>(frame / g.T);
-      tma_store_5d(&tm_o, stage + st * kLpStage + kLpV, c0, tx * kLpTX, ty * kLpTY, tf, b);
-      bulk_commit_group();
-      if (t + 2 * static_cast<int64_t>(gridDim.x) < g.ntiles) {
-        bulk_wait_group_read<0>();               // the store has read the stage: reload it
-        issue(st, t + 2 * gridDim.x);
-      }
-    }
-  }
-  if (tid == 0) {
-    bulk_wait_group0();
-    for (int st = 0; st < 2; ++st)
-      if (issued[st]) drain_wait_on(full + st, (issued[st] - 1) & 1u, &g_module_error);
   }
 }
 
@@ -321,14 +370,16 @@ int launch_lepe_add(const LepeArgs& a, void* stream) {
   g.C = a.C; g.B = static_cast<int32_t>(a.B); g.T = a.T; g.Y = a.Y; g.X = a.X;
   g.ntx = (a.X + kLpTX - 1) / kLpTX;
   g.nty = (a.Y + kLpTY - 1) / kLpTY;
-  g.ntiles = static_cast<int64_t>((a.C + 63) / 64) * a.B * a.T * g.nty * g.ntx;
+  const int64_t ntiles = static_cast<int64_t>((a.C + 63) / 64) * a.B * a.T * g.nty * g.ntx;
+  if (ntiles >= (int64_t{1} << 31)) return MHLA_ERR_UNSUPPORTED;
+  g.ntiles = static_cast<uint32_t>(ntiles);
   // a per-device setting: made on every call, for whichever device is current
   if (cudaFuncSetAttribute(mhla_lepe_add, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kLpSmem)) !=
       cudaSuccess)
     return MHLA_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return MHLA_ERR_CUDA;
-  const int grid = static_cast<int>(std::min<int64_t>(g.ntiles, 2 * static_cast<int64_t>(sms)));
+  const int grid = static_cast<int>(std::min<int64_t>(ntiles, 2 * static_cast<int64_t>(sms)));
   KernelTimer timer("mhla_lepe_add", stream);
   mhla_lepe_add<<<grid, kLpThreads, kLpSmem, static_cast<cudaStream_t>(stream)>>>(tv, to, g, a.weight, a.bias);
   return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
