@@ -161,12 +161,13 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // unit -> (b, h, tile)
+  // unit -> (b, h, tile), in 32-bit arithmetic (n_units < 2^31, checked on the host)
   auto coords = [&](int64_t u, int32_t& b, int32_t& h, int32_t& tile) {
-    tile = static_cast<int32_t>(u % g.nt);
-    const int64_t bh = u / g.nt;
-    h = static_cast<int32_t>(bh % g.H);
-    b = static_cast<int32_t>(bh / g.H);
+    const uint32_t uu = static_cast<uint32_t>(u);
+    tile = static_cast<int32_t>(uu % static_cast<uint32_t>(g.nt));
+    const uint32_t bh = uu / static_cast<uint32_t>(g.nt);
+    h = static_cast<int32_t>(bh % static_cast<uint32_t>(g.H));
+    b = static_cast<int32_t>(bh / static_cast<uint32_t>(g.H));
   };
 
   // stage st: q (k, v) tiles and the state slot of unit u
@@ -322,7 +323,7 @@ tc_causal_tile(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     };
     // W_ii of this row's block in tile u (read ahead of the scores)
     auto row_weight = [&](int64_t u) {
-      const int32_t tile = static_cast<int32_t>(u % g.nt);
+      const int32_t tile = static_cast<int32_t>(static_cast<uint32_t>(u) % static_cast<uint32_t>(g.nt));
       const int32_t blk = (tile * kTile + row) / g.w;
       return INTRA ? __ldg(W + static_cast<int64_t>(blk) * g.M + blk) : 0.0f;
     };
@@ -531,6 +532,7 @@ int launch_ct_tile(const Problem& p, const float* W, int64_t Mu, const __nv_bflo
   g.Mu = static_cast<int32_t>(Mu);
   g.nt = static_cast<int32_t>(p.N / kTile);
   const int64_t n_units = p.BH() * g.nt;
+  if (n_units >= (int64_t{1} << 31)) return MHLA_ERR_UNSUPPORTED;   // the kernel decodes units in 32 bits
   const int sms = device_sm_count();
   if (sms <= 0) return MHLA_ERR_CUDA;
   if (cudaFuncSetAttribute(tc_causal_tile<D, NU, INTRA>, cudaFuncAttributeMaxDynamicSharedMemorySize,

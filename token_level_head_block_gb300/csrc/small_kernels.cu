@@ -199,17 +199,21 @@ tc_small(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
 
   const uint64_t pol_q = policy_evict_first();
   const uint64_t pol_kv = policy_evict_last();   // every query tile of (b, h) reads them
+  // unit -> (b, h, query tile) in 32-bit arithmetic (units < 2^31, checked on the host)
   auto issue_qk = [&](int64_t u) {
-    const int32_t qt = static_cast<int32_t>(u % g.nqt);
-    const int64_t bh = u / g.nqt;
-    const int32_t h = static_cast<int32_t>(bh % g.H), b = static_cast<int32_t>(bh / g.H);
+    const uint32_t uu = static_cast<uint32_t>(u);
+    const int32_t qt = static_cast<int32_t>(uu % static_cast<uint32_t>(g.nqt));
+    const uint32_t bh = uu / static_cast<uint32_t>(g.nqt);
+    const int32_t h = static_cast<int32_t>(bh % static_cast<uint32_t>(g.H));
+    const int32_t b = static_cast<int32_t>(bh / static_cast<uint32_t>(g.H));
     mbar_arrive_expect_tx(full_qk, static_cast<uint32_t>((kQRows + g.KR) * Cfg::ROWB));
     tma_load_4d(sq, &tm_q, full_qk, 0, h, qt * kQRows, b, pol_q);
     tma_load_4d(sk, &tm_k, full_qk, 0, h, 0, b, pol_kv);
   };
   auto issue_v = [&](int64_t u) {
-    const int64_t bh = u / g.nqt;
-    const int32_t h = static_cast<int32_t>(bh % g.H), b = static_cast<int32_t>(bh / g.H);
+    const uint32_t bh = static_cast<uint32_t>(u) / static_cast<uint32_t>(g.nqt);
+    const int32_t h = static_cast<int32_t>(bh % static_cast<uint32_t>(g.H));
+    const int32_t b = static_cast<int32_t>(bh / static_cast<uint32_t>(g.H));
     mbar_arrive_expect_tx(full_v, static_cast<uint32_t>(g.KR * Cfg::ROWB));
     tma_load_4d(sv, &tm_v, full_v, 0, h, 0, b, pol_kv);
   };
@@ -324,9 +328,11 @@ tc_small(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     uint32_t it = 0;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
       const uint32_t par = it & 1u;
-      const int32_t qt = static_cast<int32_t>(u % g.nqt);
-      const int64_t bh = u / g.nqt;
-      const int32_t h = static_cast<int32_t>(bh % g.H), b = static_cast<int32_t>(bh / g.H);
+      const uint32_t uu = static_cast<uint32_t>(u);
+      const int32_t qt = static_cast<int32_t>(uu % static_cast<uint32_t>(g.nqt));
+      const uint32_t bh = uu / static_cast<uint32_t>(g.nqt);
+      const int32_t h = static_cast<int32_t>(bh % static_cast<uint32_t>(g.H));
+      const int32_t b = static_cast<int32_t>(bh / static_cast<uint32_t>(g.H));
 
       // ---- phi in place over the q and k tiles (contiguous)
       if (!small_warp_wait(full_qk, par, abortf)) break;
