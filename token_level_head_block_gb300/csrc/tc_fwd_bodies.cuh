@@ -149,9 +149,10 @@ __device__ __forceinline__ void summary_roles(const CUtensorMap* tm_k, const CUt
       uint64_t fills = 0;
       bool ok = true;
       for (int64_t item = first; ok && item < n_items; item += stride) {
-        const int32_t grp = static_cast<int32_t>(item % G);
-        const int64_t rest = item / G;
-        const int32_t j = static_cast<int32_t>(rest % g.M), b = static_cast<int32_t>(rest / g.M);
+        const uint32_t it32 = static_cast<uint32_t>(item), rest = it32 / static_cast<uint32_t>(G);
+        const int32_t grp = static_cast<int32_t>(it32 - rest * static_cast<uint32_t>(G));
+        const int32_t j = static_cast<int32_t>(rest % static_cast<uint32_t>(g.M));
+        const int32_t b = static_cast<int32_t>(rest / static_cast<uint32_t>(g.M));
         for (int c = 0; c < g.chunks; ++c) {
           if (!wait_bounded_on(bars.empty + s, ph ^ 1u, abortf, err)) { ok = false; break; }
           mbar_arrive_expect_tx(bars.full + s, Cfg::LOADB);
@@ -250,9 +251,10 @@ __device__ __forceinline__ void summary_roles(const CUtensorMap* tm_k, const CUt
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(bars.tempty + acc);
-      const int32_t grp = static_cast<int32_t>(item % G);
-      const int64_t rest = item / G;
-      const int32_t j = static_cast<int32_t>(rest % g.M), b = static_cast<int32_t>(rest / g.M);
+      const uint32_t it32 = static_cast<uint32_t>(item), rest = it32 / static_cast<uint32_t>(G);
+      const int32_t grp = static_cast<int32_t>(it32 - rest * static_cast<uint32_t>(G));
+      const int32_t j = static_cast<int32_t>(rest % static_cast<uint32_t>(g.M));
+      const int32_t b = static_cast<int32_t>(rest / static_cast<uint32_t>(g.M));
       const int32_t h = grp * Cfg::HP + hh;
       if (h < g.H) {
         // Sbuf is blocked by groups of 128 columns: column col of source block j
@@ -728,9 +730,10 @@ __device__ __forceinline__ void output_roles(const CUtensorMap* tm_q, const CUte
       uint64_t fills = 0;
       bool ok = true;
       while (ok && produce_item(sc, bars, cur, item, abortf, err)) {
-        const int32_t h = static_cast<int32_t>(item % g.H);
-        const int64_t rest = item / g.H;
-        const int32_t i = static_cast<int32_t>(rest % g.M), b = static_cast<int32_t>(rest / g.M);
+        const uint32_t it32 = static_cast<uint32_t>(item), rest = it32 / static_cast<uint32_t>(g.H);
+        const int32_t h = static_cast<int32_t>(it32 - rest * static_cast<uint32_t>(g.H));
+        const int32_t i = static_cast<int32_t>(rest % static_cast<uint32_t>(g.M));
+        const int32_t b = static_cast<int32_t>(rest / static_cast<uint32_t>(g.M));
         for (int c = 0; c < g.chunks; ++c) {
           if (!wait_bounded_on(bars.qempty + s, ph ^ 1u, abortf, err)) { ok = false; break; }
           mbar_arrive_expect_tx(bars.qfull + s, Cfg::QT);
@@ -761,8 +764,9 @@ __device__ __forceinline__ void output_roles(const CUtensorMap* tm_q, const CUte
       uint64_t fills = 0;
       int64_t ready_to = -1;            // mixing of batches <= ready_to is complete
       while (next_item(sc, bars, cur, item, false, abortf, err)) {
-        const int64_t h = item % g.H, rest = item / g.H;
-        const int64_t i = rest % g.M, b = rest / g.M;
+        const uint32_t it32 = static_cast<uint32_t>(item), rest = it32 / static_cast<uint32_t>(g.H);
+        const int64_t h = it32 - rest * static_cast<uint32_t>(g.H);
+        const int64_t i = rest % static_cast<uint32_t>(g.M), b = rest / static_cast<uint32_t>(g.M);
         if (sc.mix_done && b > ready_to) {
           if (!wait_counter_on(sc.mix_done + b, mix_target(b, sc.per_b_cols), abortf, err)) break;
           ready_to = b;
@@ -805,9 +809,10 @@ __device__ __forceinline__ void output_roles(const CUtensorMap* tm_q, const CUte
       int npend = 0;
       bool ok = true;
       while (ok && next_item(sc, bars, cur, item, false, abortf, err)) {
-        const int32_t h = static_cast<int32_t>(item % g.H);
-        const int64_t rest = item / g.H;
-        const int32_t i = static_cast<int32_t>(rest % g.M), b = static_cast<int32_t>(rest / g.M);
+        const uint32_t it32 = static_cast<uint32_t>(item), rest = it32 / static_cast<uint32_t>(g.H);
+        const int32_t h = static_cast<int32_t>(it32 - rest * static_cast<uint32_t>(g.H));
+        const int32_t i = static_cast<int32_t>(rest % static_cast<uint32_t>(g.M));
+        const int32_t b = static_cast<int32_t>(rest / static_cast<uint32_t>(g.M));
         for (int c = 0; c < g.chunks; ++c) {
           if (!wait_bounded_on(bars.ostore + s, ph, abortf, err)) { ok = false; break; }
           int32_t x, y, z;
@@ -955,7 +960,10 @@ __device__ __forceinline__ void output_roles(const CUtensorMap* tm_q, const CUte
         if (D == 64 && !PAIR && c + 1 == g.chunks) {
           // the item's last MMA has read its S~ tile and z~ (each read once, by this
           // CTA): their lines leave L2 without a write-back (measured slower at d = 32)
-          const int64_t tile = ((item / g.H) / g.M * g.H + item % g.H) * g.M + (item / g.H) % g.M;
+          const uint32_t it32 = static_cast<uint32_t>(item), rest = it32 / static_cast<uint32_t>(g.H);
+          const uint32_t hh = it32 - rest * static_cast<uint32_t>(g.H);
+          const uint32_t bb = rest / static_cast<uint32_t>(g.M), ii = rest - bb * static_cast<uint32_t>(g.M);
+          const int64_t tile = (static_cast<int64_t>(bb) * g.H + hh) * g.M + ii;
           const int e = 32 * q4 + lane;
           if (e < D * D * 2 / 128) discard_l2_line(reinterpret_cast<const uint8_t*>(St + tile * D * D) + e * 128);
           else if (e < D * D * 2 / 128 + D * 4 / 128)
