@@ -429,24 +429,37 @@ simt_bwd_key(const T* __restrict__ k, Operand ko, const T* __restrict__ v, Opera
 constexpr int kDwTile = 64;     // 64 x 64 outputs per CTA, 4 x 4 per thread
 constexpr int kDwK = 32;        // entries of the contraction staged per step
 
-// part[bh][i][j] = sum_e dSzt[bh][i][e] * Sz[bh][j][e]   (one (b, h) per z index)
+// Contraction splits of the dW partial products: enough CTAs for about two per
+// SM of a 152-SM part, each split at least 512 entries long.
+int64_t dw_splits(const Problem& p) {
+  const int64_t tiles = (p.M + kDwTile - 1) / kDwTile;
+  const int64_t ctas = tiles * tiles * p.BH();
+  const int64_t E = p.d * (p.d + 1);
+  const int64_t want = (304 + ctas - 1) / ctas;
+  return std::max<int64_t>(1, std::min<int64_t>(want, std::max<int64_t>(1, E / 512)));
+}
+
+// part[bh][ks][i][j] = sum over e in split ks of dSzt[bh][i][e] * Sz[bh][j][e]
+// (z index = bh * KS + ks; the KS splits of the contraction cut E into equal
+// column ranges so that a small M still spreads over many CTAs)
 __global__ void __launch_bounds__(256)
 simt_dw_partial(const float* __restrict__ dSzt, const float* __restrict__ Sz, float* __restrict__ part, int64_t M,
-                int64_t E) {
+                int64_t E, int32_t KS) {
   __shared__ float sa[kDwK][kDwTile + 4];
   __shared__ float sb[kDwK][kDwTile + 4];
   const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kDwTile, j0 = static_cast<int64_t>(blockIdx.y) * kDwTile;
-  const int64_t bh = blockIdx.z;
+  const int64_t bh = blockIdx.z / KS, ks = blockIdx.z % KS;
+  const int64_t e_lo = E * ks / KS, e_hi = E * (ks + 1) / KS;
   const float* A = dSzt + bh * M * E;
   const float* Bm = Sz + bh * M * E;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
   float acc[4][4] = {};
-  for (int64_t e0 = 0; e0 < E; e0 += kDwK) {
+  for (int64_t e0 = e_lo; e0 < e_hi; e0 += kDwK) {
     for (int x = threadIdx.x; x < kDwK * kDwTile; x += 256) {
       const int row = x / kDwK, kk = x % kDwK;
       const int64_t e = e0 + kk;
-      sa[kk][row] = (i0 + row < M && e < E) ? A[(i0 + row) * E + e] : 0.0f;
-      sb[kk][row] = (j0 + row < M && e < E) ? Bm[(j0 + row) * E + e] : 0.0f;
+      sa[kk][row] = (i0 + row < M && e < e_hi) ? A[(i0 + row) * E + e] : 0.0f;
+      sb[kk][row] = (j0 + row < M && e < e_hi) ? Bm[(j0 + row) * E + e] : 0.0f;
     }
     __syncthreads();
 #pragma unroll 8
@@ -469,16 +482,17 @@ simt_dw_partial(const float* __restrict__ dSzt, const float* __restrict__ Sz, fl
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const int64_t ii = i0 + ty * 4 + u, jj = j0 + tx * 4 + w;
-      if (ii < M && jj < M) part[(bh * M + ii) * M + jj] = acc[u][w];
+      if (ii < M && jj < M) part[(static_cast<int64_t>(blockIdx.z) * M + ii) * M + jj] = acc[u][w];
     }
 }
 
-// dW = sum over (b, h) of the partials, in a fixed order (deterministic).
-__global__ void simt_dw_reduce(const float* __restrict__ part, float* __restrict__ dW, int64_t MM, int64_t BH) {
+// dW = sum over (b, h) and the contraction splits of the partials (NP = BH *
+// KS of them), in a fixed order (deterministic).
+__global__ void simt_dw_reduce(const float* __restrict__ part, float* __restrict__ dW, int64_t MM, int64_t NP) {
   const int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (x >= MM) return;
   float s = 0.0f;
-  for (int64_t bh = 0; bh < BH; ++bh) s += part[bh * MM + x];
+  for (int64_t n = 0; n < NP; ++n) s += part[n * MM + x];
   dW[x] = s;
 }
 
@@ -753,14 +767,14 @@ simt_causal_bwd_key(const T* __restrict__ q, Operand qo, const T* __restrict__ k
 // Causal dW: the partials below the diagonal, the query kernel's W_ii shares
 // on it, zero above it; summed over (b, h) in a fixed order.
 __global__ void simt_dw_reduce_causal(const float* __restrict__ part, const float* __restrict__ diag,
-                                      float* __restrict__ dW, int64_t M, int64_t BH) {
+                                      float* __restrict__ dW, int64_t M, int64_t BH, int64_t KS) {
   const int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t MM = M * M;
   if (x >= MM) return;
   const int64_t i = x / M, j = x % M;
   float s = 0.0f;
   if (j < i)
-    for (int64_t bh = 0; bh < BH; ++bh) s += part[bh * MM + x];
+    for (int64_t n = 0; n < BH * KS; ++n) s += part[n * MM + x];
   else if (j == i)
     for (int64_t bh = 0; bh < BH; ++bh) s += diag[bh * M + i];
   dW[x] = s;
@@ -885,14 +899,15 @@ int launch_simt_bwd_typed(const Problem& p, const float* W, const BwdOperands& b
   }
   // dW (before the transposed mixing overwrites S~ with dS)
   {
+    const int64_t KS = dw_splits(p);
     const dim3 grid(static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile),
-                    static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile), static_cast<unsigned>(BH));
-    if (grid.x > 65535) return MHLA_ERR_UNSUPPORTED;
+                    static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile), static_cast<unsigned>(BH * KS));
+    if (grid.x > 65535 || BH * KS > 65535) return MHLA_ERR_UNSUPPORTED;
     KernelTimer timer("simt_dw", stream);
-    simt_dw_partial<<<grid, 256, 0, stream>>>(ws.dSzt, ws.Sz, ws.part, p.M, E);
+    simt_dw_partial<<<grid, 256, 0, stream>>>(ws.dSzt, ws.Sz, ws.part, p.M, E, static_cast<int32_t>(KS));
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
     const int64_t MM = p.M * p.M;
-    simt_dw_reduce<<<static_cast<unsigned>((MM + 255) / 256), 256, 0, stream>>>(ws.part, bo.dW, MM, BH);
+    simt_dw_reduce<<<static_cast<unsigned>((MM + 255) / 256), 256, 0, stream>>>(ws.part, bo.dW, MM, BH * KS);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
   // dS = W^T dS~ into the S~ buffer
@@ -982,7 +997,7 @@ struct SimtCausalBwdWorkspace {
 
 SimtCausalBwdWorkspace simt_causal_bwd_carve(const Problem& p, void* base) {
   const size_t per = static_cast<size_t>(p.BH()) * p.M * p.d * (p.d + 1) * sizeof(float);
-  const size_t part = static_cast<size_t>(p.BH()) * p.M * p.M * sizeof(float);
+  const size_t part = static_cast<size_t>(p.BH()) * dw_splits(p) * p.M * p.M * sizeof(float);
   const size_t diag = static_cast<size_t>(p.BH()) * p.M * sizeof(float);
   char* c = static_cast<char*>(base);
   SimtCausalBwdWorkspace ws;
@@ -1057,15 +1072,16 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
     if (rc != MHLA_OK) return rc;
   }
   {
+    const int64_t KS = dw_splits(p);
     const dim3 grid(static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile),
-                    static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile), static_cast<unsigned>(BH));
-    if (grid.x > 65535) return MHLA_ERR_UNSUPPORTED;
+                    static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile), static_cast<unsigned>(BH * KS));
+    if (grid.x > 65535 || BH * KS > 65535) return MHLA_ERR_UNSUPPORTED;
     KernelTimer timer("simt_dw", stream);
-    simt_dw_partial<<<grid, 256, 0, stream>>>(ws.dSp, ws.Sz, ws.part, p.M, E);
+    simt_dw_partial<<<grid, 256, 0, stream>>>(ws.dSp, ws.Sz, ws.part, p.M, E, static_cast<int32_t>(KS));
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
     const int64_t MM = p.M * p.M;
     simt_dw_reduce_causal<<<static_cast<unsigned>((MM + 255) / 256), 256, 0, stream>>>(ws.part, ws.diag, bo.dW,
-                                                                                       p.M, BH);
+                                                                                       p.M, BH, KS);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
   {
@@ -1117,7 +1133,7 @@ int launch_simt(const Problem& p, const float* W, void* workspace, void* stream)
 
 size_t simt_bwd_workspace_bytes(const Problem& p) {
   const size_t per = static_cast<size_t>(p.BH()) * p.M * p.d * (p.d + 1) * sizeof(float);
-  const size_t part = static_cast<size_t>(p.BH()) * p.M * p.M * sizeof(float);
+  const size_t part = static_cast<size_t>(p.BH()) * dw_splits(p) * p.M * p.M * sizeof(float);
   return 3 * align_up(per) + align_up(part);
 }
 
@@ -1136,7 +1152,7 @@ int launch_simt_bwd(const Problem& p, const float* W, const BwdOperands& bo, voi
 
 size_t simt_causal_bwd_workspace_bytes(const Problem& p) {
   const size_t per = static_cast<size_t>(p.BH()) * p.M * p.d * (p.d + 1) * sizeof(float);
-  const size_t part = static_cast<size_t>(p.BH()) * p.M * p.M * sizeof(float);
+  const size_t part = static_cast<size_t>(p.BH()) * dw_splits(p) * p.M * p.M * sizeof(float);
   const size_t diag = static_cast<size_t>(p.BH()) * p.M * sizeof(float);
   const size_t dn = static_cast<size_t>(p.BH()) * p.M * p.w * (p.d + 1) * sizeof(float);
   return 3 * align_up(per) + align_up(part) + align_up(diag) + align_up(dn);
