@@ -1039,13 +1039,25 @@ tc_dw(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensor
   }
 }
 
-// dW = the partial products summed over the splits in a fixed order.
-__global__ void tc_dw_reduce(const float* __restrict__ part, float* __restrict__ dW, int64_t MM, int32_t nsplit) {
-  const int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (x >= MM) return;
+// dW = the partial products summed over the splits in a fixed order: 64
+// outputs per CTA, four threads per output each summing a fixed quarter of
+// the splits in order, then the quarters added in order (deterministic; four
+// loads in flight per output instead of one).
+constexpr int kDwrOut = 64;
+__global__ void __launch_bounds__(256) tc_dw_reduce(const float* __restrict__ part, float* __restrict__ dW,
+                                                    int64_t MM, int32_t nsplit) {
+  __shared__ float quarter[4][kDwrOut];
+  const int o = threadIdx.x % kDwrOut, q = threadIdx.x / kDwrOut;
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * kDwrOut + o;
+  const int32_t k0 = nsplit * q / 4, k1 = nsplit * (q + 1) / 4;
   float s = 0.0f;
-  for (int32_t k = 0; k < nsplit; ++k) s += part[k * MM + x];
-  dW[x] = s;
+  if (x < MM) {
+#pragma unroll 4
+    for (int32_t k = k0; k < k1; ++k) s += part[k * MM + x];
+  }
+  quarter[q][o] = s;
+  __syncthreads();
+  if (q == 0 && x < MM) dW[x] = ((quarter[0][o] + quarter[1][o]) + quarter[2][o]) + quarter[3][o];
 }
 
 // ----------------------------------------------------------------- host side
@@ -1160,7 +1172,8 @@ int launch_tc_bwd_d(const Problem& p, const float* W, const BwdOperands& bo, voi
           ta, tb, static_cast<int32_t>(p.M), L.n_jt, L.JN, L.ngroups, L.nsplit, part);
       if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
       const int64_t MM = p.M * p.M;
-      tc_dw_reduce<<<static_cast<unsigned>((MM + 255) / 256), 256, 0, stream>>>(part, bo.dW, MM, L.nsplit);
+      tc_dw_reduce<<<static_cast<unsigned>((MM + kDwrOut - 1) / kDwrOut), 256, 0, stream>>>(part, bo.dW, MM,
+                                                                                            L.nsplit);
       if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
     }
     rc = tc_run_mix(p, WbT, L.Mp, dSbuf, St, zt, stream, /*discard_input=*/true);   // dS~ is not read again
