@@ -178,3 +178,24 @@ def test_causal_backward_matches_autograd_of_the_dense_form():
     (o * torch.tensor(as_f64(g))).sum().backward()
     for name, a, b in zip(NAMES, got, (qt.grad, kt.grad, vt.grad, Wt.grad)):
         assert normwise(a, b.numpy()) <= TOL["f32"], name
+
+
+def test_causal_backward_workload_sampled_slices():
+    """The causal LM workload at full size (B=4, H=12, N=4096, 64-token blocks), as
+    the backward bench runs it: dq, dk, dv of three (b, h) slices against the
+    oracle on those slices (a slice's gradients depend on that slice alone); dW,
+    which sums over every slice, is checked for its zero upper triangle."""
+    from token_level_head_block_gb300.synth import draw_workload
+    from token_level_head_block_gb300.workloads import WORKLOADS
+    wl = WORKLOADS["lm_causal_4096"]
+    q, k, v = draw_workload(wl)
+    g = draw_dout((wl.B, wl.N, wl.H, wl.d), wl.seed + 100, wl.dtype)
+    W = mhla.init_mixing(wl.grid, wl.block, wl.transform, wl.local_thres, wl.exp_sigma)
+    dq, dk, dv, dW = run(q, k, v, W, g, wl.grid, wl.block, wl.phi, wl.eps)
+    assert np.all(np.isfinite(dW)) and not np.any(dW[np.triu_indices(wl.M, 1)])
+    for b, h in [(0, 0), (wl.B - 1, wl.H - 1), (wl.B // 2, wl.H // 2)]:
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1), slice(None))
+        ref = oracle.backward_causal(as_f64(q[sl]), as_f64(k[sl]), as_f64(v[sl]), W, as_f64(g[sl]), wl.grid,
+                                     wl.block, PHI[wl.phi], wl.eps)
+        for name, a, r in zip(NAMES[:3], (dq, dk, dv), ref[:3]):
+            assert normwise(a[sl], r) <= TOL[wl.dtype], (name, b, h)
