@@ -513,19 +513,34 @@ __global__ void simt_dw_reduce(const float* __restrict__ part, float* __restrict
 // (t and s range over the block).  Kernels, in launch order:
 //   simt_summary, simt_mix<false, true>   S_j and the mixed past S<_i, z<_i
 //   simt_causal_bwd_query  per (b, h, i), 32-token chunks in order, the running
-//                          state C in shared memory: dq, dS<_i, dz<_i, the
-//                          (b, h) share of dW_ii, and dnum_t, dden_t to scratch
+//                          state C in shared memory, each chunk in phases of
+//                          register tiles: dq, dS<_i, dz<_i, the (b, h) share of
+//                          dW_ii, and dnum_t, dden_t to scratch
 //   simt_dw_partial, simt_dw_reduce_causal   dW below the diagonal, plus dW_ii
 //   simt_mix<true, true>   dS_j, dz_j
 //   simt_causal_bwd_key    per (b, h, j), chunks in reverse, the running
-//                          suffix state dS_j + W_jj sum_{later t} phi(q_t) dnum_t^T
+//                          suffix state dS_j + W_jj sum_{later t} phi(q_t) dnum_t^T,
+//                          each chunk in phases of register tiles
 // ============================================================================
 constexpr int kCbThreads = 256;
 constexpr int kCbWarps = kCbThreads / 32;
 constexpr int kCbChunk = 32;    // one chunk token per lane in the score steps
 
-// ENT = ceil(d*d / 256) state entries per thread (P_t and dS<_i in registers).
-template <typename T, int ENT>
+// ENT = ceil(d*d / 256) state entries per thread (P_t and dS<_i in registers);
+// DB = ceil(d / 16) columns per thread in the token x column phases.
+//
+// Per chunk of up to 32 tokens, in phases separated by block barriers, each
+// thread computing a small register tile (2 tokens x DB columns, or a 2 x 2
+// block of the 32 x 32 token pairs) so that every shared-memory operand it
+// loads serves several FMAs:
+//   1  scores a_ts = phi(q_t) . phi(k_s) (s <= t, same chunk) and P = W_ii a
+//   2  den_t = phi(q_t) . c + sum_s P_ts + eps
+//   3  num_t = phi(q_t)^T C + sum_s P_ts v_s; dnum_t = g_t / den_t,
+//      dden_t = -(g_t . num_t) / den_t^2 (a 16-lane reduction per token)
+//   4  b_ts = v_s . dnum_t + dden_t (s <= t); dW_ii += a_ts b_ts
+//   5  dq_t = (C dnum_t + dden_t c + W_ii sum_s b_ts phi(k_s)) * [q_t > 0]
+//   6  the chunk into the running state, dS<_i and dW_ii (as before)
+template <typename T, int ENT, int DB>
 __global__ void __launch_bounds__(kCbThreads)
 simt_causal_bwd_query(const T* __restrict__ q, Operand qo, const T* __restrict__ k, Operand ko,
                       const T* __restrict__ v, Operand vo, const T* __restrict__ g_out, Operand go,
@@ -533,16 +548,20 @@ simt_causal_bwd_query(const T* __restrict__ q, Operand qo, const T* __restrict__
                       const float* __restrict__ W, const float* __restrict__ Sp, float* __restrict__ dSp,
                       float* __restrict__ diag, float* __restrict__ dn) {
   extern __shared__ float sm[];
+  constexpr int CP = kCbChunk + 1;         // padded row of a 32 x 32 token-pair matrix
   const int E = d * d, P = d + 1;
   float* st = sm;                          // [d][d + 1] C = S<_i + W_ii P before the chunk
   float* zs = st + d * P;                  // [d]        c = z<_i + W_ii y before the chunk
-  float* sq = zs + d;                      // [chunk][d]     phi(q_t)
-  float* sk = sq + kCbChunk * d;           // [chunk][d + 1] phi(k_s)   (lanes walk s)
+  float* sq = zs + d;                      // [chunk][d + 1] phi(q_t)
+  float* sk = sq + kCbChunk * P;           // [chunk][d + 1] phi(k_s)
   float* sv = sk + kCbChunk * P;           // [chunk][d + 1] v_s
-  float* sdn = sv + kCbChunk * P;          // [chunk][d]     dnum_t
-  float* sdd = sdn + kCbChunk * d;         // [chunk]        dden_t
-  float* sab = sdd + kCbChunk;             // [warps][2][chunk] a_s = phi(q_t).phi(k_s), b_s = v_s.dnum_t + dden_t
-  float* red = sab + kCbWarps * 2 * kCbChunk;   // [warps]
+  float* sg = sv + kCbChunk * P;           // [chunk][d + 1] g_t
+  float* sdn = sg + kCbChunk * P;          // [chunk][d + 1] dnum_t
+  float* sdd = sdn + kCbChunk * P;         // [chunk]        dden_t
+  float* sden = sdd + kCbChunk;            // [chunk]        den_t
+  float* sa = sden + kCbChunk;             // [chunk][CP]    a_ts (s <= t, else 0)
+  float* sb = sa + kCbChunk * CP;          // [chunk][CP]    b_ts (s <= t, else 0)
+  float* red = sb + kCbChunk * CP;         // [warps]
   const int64_t item = blockIdx.x;
   const int64_t i = item % g.M, bh = item / g.M;
   const int64_t b = bh / H, h = bh % H;
@@ -561,92 +580,224 @@ simt_causal_bwd_query(const T* __restrict__ q, Operand qo, const T* __restrict__
 #pragma unroll
   for (int m = 0; m < ENT; ++m) pr[m] = acc[m] = 0.0f;
   float yr = 0.0f, zacc = 0.0f, dw = 0.0f;
-  float* mya = sab + warp * 2 * kCbChunk;
-  float* myb = mya + kCbChunk;
+  // token x column tiles: tokens 2 tt, 2 tt + 1 (a half-warp shares them), columns cc + 16 j
+  const int tt = tid / 16, cc = tid % 16;
+  const int t0 = 2 * tt, t1 = t0 + 1;
+  // token-pair tiles: rows 2 pi, 2 pi + 1 and columns 2 pj, 2 pj + 1
+  const int pi = tid / 16, pj = tid % 16;
+  // state-entry tiles (phase 6 and the outputs): TB x TB entries per thread
+  constexpr int TB = ENT == 1 ? 1 : ENT == 4 ? 2 : ENT == 16 ? 4 : 8;
+  static_assert(TB * TB == ENT, "ENT is a square");
+  const int r0 = TB * (tid / 16), c0 = TB * (tid % 16);
   for (int64_t s0 = 0; s0 < g.w; s0 += kCbChunk) {
     const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
     __syncthreads();   // the state is complete and the previous chunk's rows are free
     for (int e = tid; e < cnt * d; e += kCbThreads) {
       const int sl = e / d, c = e % d;
       const int64_t n = token_of(g, i, s0 + sl);
-      sq[sl * d + c] = phi_f(load_f(qb + n * qo.sn + c), phi_kind, eps);
+      sq[sl * P + c] = phi_f(load_f(qb + n * qo.sn + c), phi_kind, eps);
       sk[sl * P + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
       sv[sl * P + c] = load_f(vb + n * vo.sn + c);
+      sg[sl * P + c] = load_f(gb + n * go.sn + c);
     }
     __syncthreads();
-    for (int sl = warp; sl < cnt; sl += kCbWarps) {
-      const float* myq = sq + sl * d;
-      float* mydn = sdn + sl * d;
-      float a = 0.0f;
-      if (lane <= sl)
-        for (int r = 0; r < d; ++r) a = fmaf(myq[r], sk[lane * P + r], a);
-      mya[lane] = a;
-      float den = 0.0f;
-      for (int r = lane; r < d; r += 32) den = fmaf(myq[r], zs[r], den);
-      den = warp_sum(fmaf(wii, a, den)) + eps;
-      __syncwarp();
-      const int64_t n = token_of(g, i, s0 + sl);
-      float* dnrow = dnb + (s0 + sl) * P;
-      float go_dot = 0.0f;
-      for (int c = lane; c < d; c += 32) {
-        float num = 0.0f, own = 0.0f;
-        for (int r = 0; r < d; ++r) num = fmaf(myq[r], st[r * P + c], num);
-        for (int s2 = 0; s2 <= sl; ++s2) own = fmaf(mya[s2], sv[s2 * P + c], own);
-        num = fmaf(wii, own, num);
-        const float gc = load_f(gb + n * go.sn + c);
-        go_dot = fmaf(gc, num, go_dot);
-        const float dnc = gc / den;
-        mydn[c] = dnc;
-        dnrow[c] = dnc;
+    // ---- 1: a_ts for every pair of the chunk, a 2 x 2 block per thread (rows
+    // past cnt hold stale values; the select below discards them)
+    {
+      const int ra = 2 * pi, rb = ra + 1, ca = 2 * pj, cb = ca + 1;
+      float x00 = 0.0f, x01 = 0.0f, x10 = 0.0f, x11 = 0.0f;
+      for (int r = 0; r < d; ++r) {
+        const float qa = sq[ra * P + r], qb2 = sq[rb * P + r];
+        const float ka = sk[ca * P + r], kb2 = sk[cb * P + r];
+        x00 = fmaf(qa, ka, x00);
+        x01 = fmaf(qa, kb2, x01);
+        x10 = fmaf(qb2, ka, x10);
+        x11 = fmaf(qb2, kb2, x11);
       }
-      go_dot = warp_sum(go_dot) / den;
-      const float dden = -go_dot / den;
-      if (lane == 0) {
-        sdd[sl] = dden;
-        dnrow[d] = dden;
-      }
-      __syncwarp();
-      float bb = 0.0f;
-      if (lane <= sl) {
-        for (int c = 0; c < d; ++c) bb = fmaf(sv[lane * P + c], mydn[c], bb);
-        bb += dden;
-      }
-      myb[lane] = bb;
-      dw = fmaf(a, bb, dw);   // own-chunk part of dW_ii (a = b = 0 past the token)
-      __syncwarp();
-      for (int r = lane; r < d; r += 32) {
-        float x = dden * zs[r], own = 0.0f;
-        for (int c = 0; c < d; ++c) x = fmaf(st[r * P + c], mydn[c], x);
-        for (int s2 = 0; s2 <= sl; ++s2) own = fmaf(sk[s2 * P + r], myb[s2], own);
-        x = fmaf(wii, own, x);
-        const float qr = load_f(qb + n * qo.sn + r);
-        store_f(dqb + n * dqo.sn + r, qr > 0.0f ? x : 0.0f);
-      }
-      __syncwarp();
+      sa[ra * CP + ca] = (ra < cnt && ca <= ra) ? x00 : 0.0f;
+      sa[ra * CP + cb] = (ra < cnt && cb <= ra) ? x01 : 0.0f;
+      sa[rb * CP + ca] = (rb < cnt && ca <= rb) ? x10 : 0.0f;
+      sa[rb * CP + cb] = (rb < cnt && cb <= rb) ? x11 : 0.0f;
     }
     __syncthreads();
-    // dS<_i += X (the chunk's sum of phi(q_t) dnum_t^T); dW_ii += <P, X>; then
-    // P and the state advance by the chunk's phi(k_s) v_s^T.
+    // ---- 2: den_t, eight threads per token (strided parts, then a fixed-order
+    // shuffle sum over the eight)
+    {
+      const int tok = tid / 8, part = tid % 8;
+      float den = 0.0f, own = 0.0f;
+      for (int r = part; r < d; r += 8) den = fmaf(sq[tok * P + r], zs[r], den);
+      for (int s2 = part; s2 < kCbChunk; s2 += 8) own += sa[tok * CP + s2];
 #pragma unroll
-    for (int m = 0; m < ENT; ++m) {
-      const int e = tid + m * kCbThreads;
-      if (e < E) {
-        const int r = e / d, c = e % d;
-        float x = 0.0f, dp = 0.0f;
-        for (int sl = 0; sl < cnt; ++sl) {
-          x = fmaf(sq[sl * d + r], sdn[sl * d + c], x);
-          dp = fmaf(sk[sl * P + r], sv[sl * P + c], dp);
+      for (int off = 4; off > 0; off >>= 1) {
+        den += __shfl_xor_sync(0xffffffffu, den, off);
+        own += __shfl_xor_sync(0xffffffffu, own, off);
+      }
+      if (part == 0) sden[tok] = fmaf(wii, own, den) + eps;
+    }
+    __syncthreads();
+    // ---- 3: num, dnum, dden (tokens t0, t1; columns cc + 16 j)
+    {
+      float n0[DB], n1[DB], o0[DB], o1[DB];
+#pragma unroll
+      for (int j = 0; j < DB; ++j) n0[j] = n1[j] = o0[j] = o1[j] = 0.0f;
+      for (int r = 0; r < d; ++r) {
+        const float q0 = sq[t0 * P + r], q1 = sq[t1 * P + r];
+#pragma unroll
+        for (int j = 0; j < DB; ++j) {
+          const float cv = st[r * P + cc + 16 * j];   // columns past d read other data, discarded below
+          n0[j] = fmaf(q0, cv, n0[j]);
+          n1[j] = fmaf(q1, cv, n1[j]);
         }
-        dw = fmaf(pr[m], x, dw);
-        acc[m] += x;
-        pr[m] += dp;
-        st[r * P + c] = fmaf(wii, dp, st[r * P + c]);
+      }
+      for (int s2 = 0; s2 < cnt; ++s2) {
+        const float p0 = sa[t0 * CP + s2], p1 = sa[t1 * CP + s2];
+#pragma unroll
+        for (int j = 0; j < DB; ++j) {
+          const float vv = sv[s2 * P + cc + 16 * j];
+          o0[j] = fmaf(p0, vv, o0[j]);
+          o1[j] = fmaf(p1, vv, o1[j]);
+        }
+      }
+      const float den0 = sden[t0], den1 = sden[t1];
+      float go0 = 0.0f, go1 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < DB; ++j) {
+        const int c = cc + 16 * j;
+        if (c < d) {
+          const float g0 = sg[t0 * P + c], g1 = sg[t1 * P + c];
+          go0 = fmaf(g0, fmaf(wii, o0[j], n0[j]), go0);
+          go1 = fmaf(g1, fmaf(wii, o1[j], n1[j]), go1);
+          const float dn0 = g0 / den0, dn1 = g1 / den1;
+          sdn[t0 * P + c] = dn0;
+          sdn[t1 * P + c] = dn1;
+          if (t0 < cnt) dnb[(s0 + t0) * P + c] = dn0;
+          if (t1 < cnt) dnb[(s0 + t1) * P + c] = dn1;
+        }
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) {   // the 16 lanes of this half-warp share t0, t1
+        go0 += __shfl_xor_sync(0xffffffffu, go0, off);
+        go1 += __shfl_xor_sync(0xffffffffu, go1, off);
+      }
+      if (cc == 0) {
+        const float dd0 = -(go0 / den0) / den0, dd1 = -(go1 / den1) / den1;
+        sdd[t0] = dd0;
+        sdd[t1] = dd1;
+        if (t0 < cnt) dnb[(s0 + t0) * P + d] = dd0;
+        if (t1 < cnt) dnb[(s0 + t1) * P + d] = dd1;
+      }
+    }
+    __syncthreads();
+    // ---- 4: b_ts = v_s . dnum_t + dden_t (s <= t), dW_ii's own-chunk part
+    {
+      const int ra = 2 * pi, rb = ra + 1, ca = 2 * pj, cb = ca + 1;
+      float x00 = 0.0f, x01 = 0.0f, x10 = 0.0f, x11 = 0.0f;
+      for (int c = 0; c < d; ++c) {
+        const float na = sdn[ra * P + c], nb = sdn[rb * P + c];
+        const float va = sv[ca * P + c], vb2 = sv[cb * P + c];
+        x00 = fmaf(na, va, x00);
+        x01 = fmaf(na, vb2, x01);
+        x10 = fmaf(nb, va, x10);
+        x11 = fmaf(nb, vb2, x11);
+      }
+      const float da = sdd[ra], db = sdd[rb];
+      const float b00 = (ra < cnt && ca <= ra) ? x00 + da : 0.0f;
+      const float b01 = (ra < cnt && cb <= ra) ? x01 + da : 0.0f;
+      const float b10 = (rb < cnt && ca <= rb) ? x10 + db : 0.0f;
+      const float b11 = (rb < cnt && cb <= rb) ? x11 + db : 0.0f;
+      sb[ra * CP + ca] = b00;
+      sb[ra * CP + cb] = b01;
+      sb[rb * CP + ca] = b10;
+      sb[rb * CP + cb] = b11;
+      // a is zero wherever b is (the same mask)
+      dw = fmaf(sa[ra * CP + ca], b00, dw);
+      dw = fmaf(sa[ra * CP + cb], b01, dw);
+      dw = fmaf(sa[rb * CP + ca], b10, dw);
+      dw = fmaf(sa[rb * CP + cb], b11, dw);
+    }
+    __syncthreads();
+    // ---- 5: dq (tokens t0, t1; rows r = cc + 16 j)
+    {
+      float x0[DB], x1[DB], w0[DB], w1[DB];
+#pragma unroll
+      for (int j = 0; j < DB; ++j) x0[j] = x1[j] = w0[j] = w1[j] = 0.0f;
+      for (int c = 0; c < d; ++c) {
+        const float n0 = sdn[t0 * P + c], n1 = sdn[t1 * P + c];
+#pragma unroll
+        for (int j = 0; j < DB; ++j) {
+          const float cv = st[(cc + 16 * j) * P + c];   // rows past d read other data, discarded below
+          x0[j] = fmaf(cv, n0, x0[j]);
+          x1[j] = fmaf(cv, n1, x1[j]);
+        }
+      }
+      for (int s2 = 0; s2 < cnt; ++s2) {
+        const float b0 = sb[t0 * CP + s2], b1 = sb[t1 * CP + s2];
+#pragma unroll
+        for (int j = 0; j < DB; ++j) {
+          const float kv = sk[s2 * P + cc + 16 * j];
+          w0[j] = fmaf(kv, b0, w0[j]);
+          w1[j] = fmaf(kv, b1, w1[j]);
+        }
+      }
+      const float dd0 = sdd[t0], dd1 = sdd[t1];
+      const int64_t n0t = t0 < cnt ? token_of(g, i, s0 + t0) : 0;
+      const int64_t n1t = t1 < cnt ? token_of(g, i, s0 + t1) : 0;
+#pragma unroll
+      for (int j = 0; j < DB; ++j) {
+        const int r = cc + 16 * j;
+        if (r < d) {
+          const float zr = zs[r];
+          if (t0 < cnt) {
+            const float x = fmaf(wii, w0[j], fmaf(dd0, zr, x0[j]));
+            store_f(dqb + n0t * dqo.sn + r, load_f(qb + n0t * qo.sn + r) > 0.0f ? x : 0.0f);
+          }
+          if (t1 < cnt) {
+            const float x = fmaf(wii, w1[j], fmaf(dd1, zr, x1[j]));
+            store_f(dqb + n1t * dqo.sn + r, load_f(qb + n1t * qo.sn + r) > 0.0f ? x : 0.0f);
+          }
+        }
+      }
+    }
+    __syncthreads();   // phase 6 rewrites the state phase 5 has read
+    // ---- 6: dS<_i += X (the chunk's sum of phi(q_t) dnum_t^T); dW_ii += <P, X>; then
+    // P and the state advance by the chunk's phi(k_s) v_s^T.  Each thread owns a
+    // TB x TB tile of the entries (rows TB (tid / 16) + u, columns TB (tid % 16) + w).
+    {
+      // the X terms go straight into dS<_i and dW_ii (P is this chunk's old value
+      // throughout the loop); the state increments wait in dps
+      float dps[ENT];
+#pragma unroll
+      for (int m = 0; m < ENT; ++m) dps[m] = 0.0f;
+      for (int sl = 0; sl < cnt; ++sl) {
+        float qr[TB], kr[TB], nc[TB], vc[TB];
+#pragma unroll
+        for (int u = 0; u < TB; ++u) {
+          qr[u] = sq[sl * P + r0 + u];   // rows and columns past d read other data, discarded below
+          kr[u] = sk[sl * P + r0 + u];
+          nc[u] = sdn[sl * P + c0 + u];
+          vc[u] = sv[sl * P + c0 + u];
+        }
+#pragma unroll
+        for (int u = 0; u < TB; ++u)
+#pragma unroll
+          for (int w = 0; w < TB; ++w) {
+            const float x = qr[u] * nc[w];
+            acc[u * TB + w] += x;
+            dw = fmaf(pr[u * TB + w], x, dw);
+            dps[u * TB + w] = fmaf(kr[u], vc[w], dps[u * TB + w]);
+          }
+      }
+#pragma unroll
+      for (int m = 0; m < ENT; ++m) {
+        const int r = r0 + m / TB, c = c0 + m % TB;
+        pr[m] += dps[m];
+        if (r < d && c < d) st[r * P + c] = fmaf(wii, dps[m], st[r * P + c]);
       }
     }
     if (tid < d) {
       float x = 0.0f, dy = 0.0f;
       for (int sl = 0; sl < cnt; ++sl) {
-        x = fmaf(sq[sl * d + tid], sdd[sl], x);
+        x = fmaf(sq[sl * P + tid], sdd[sl], x);
         dy += sk[sl * P + tid];
       }
       dw = fmaf(yr, x, dw);
@@ -658,8 +809,8 @@ simt_causal_bwd_query(const T* __restrict__ q, Operand qo, const T* __restrict__
   float* out = dSp + (bh * g.M + i) * static_cast<int64_t>(E + d);
 #pragma unroll
   for (int m = 0; m < ENT; ++m) {
-    const int e = tid + m * kCbThreads;
-    if (e < E) out[e] = acc[m];
+    const int r = r0 + m / TB, c = c0 + m % TB;
+    if (r < d && c < d) out[r * d + c] = acc[m];
   }
   if (tid < d) out[E + tid] = zacc;
   dw = warp_sum(dw);
@@ -672,27 +823,35 @@ simt_causal_bwd_query(const T* __restrict__ q, Operand qo, const T* __restrict__
   }
 }
 
-// One CTA per (b, h, j), chunks of the block in reverse, one warp per source token.
-template <typename T>
+// One CTA per (b, h, j), chunks of the block in reverse, each chunk in phases of
+// register tiles (DB = ceil(d / 16) columns per thread; TB x TB state entries):
+//   1  a_st = phi(k_s) . phi(q_t) and b_st = v_s . dnum_t + dden_t for t >= s
+//   2  dv_s = G^T phi(k_s) + W_jj sum_t a_st dnum_t
+//      dphi(k_s) = G v_s + gz + W_jj sum_t b_st phi(q_t), masked by [k_s > 0]
+//   3  G += W_jj sum_t phi(q_t) dnum_t^T, gz += W_jj sum_t dden_t phi(q_t)
+// with G = dS_j + W_jj sum over later chunks of phi(q_t) dnum_t^T (gz likewise).
+template <typename T, int DB, int TB>
 __global__ void __launch_bounds__(kCbThreads)
 simt_causal_bwd_key(const T* __restrict__ q, Operand qo, const T* __restrict__ k, Operand ko,
                     const T* __restrict__ v, Operand vo, T* __restrict__ dk, Operand dko, T* __restrict__ dv,
                     Operand dvo, TokenGeom g, int64_t H, int d, int phi_kind, float eps, const float* __restrict__ W,
                     const float* __restrict__ dS, const float* __restrict__ dn) {
   extern __shared__ float sm[];
+  constexpr int CP = kCbChunk + 1;
   const int E = d * d, P = d + 1;
-  float* gs = sm;                          // [d][d + 1] dS_j + W_jj sum over later chunks of phi(q_t) dnum_t^T
-  float* gz = gs + d * P;                  // [d]        dz_j + W_jj sum over later chunks of dden_t phi(q_t)
-  float* sq = gz + d;                      // [chunk][d + 1] phi(q_t)   (lanes walk t)
+  float* gs = sm;                          // [d][d + 1] G
+  float* gz = gs + d * P;                  // [d]        gz
+  float* sq = gz + d;                      // [chunk][d + 1] phi(q_t)
   float* sdn = sq + kCbChunk * P;          // [chunk][d + 1] dnum_t
-  float* sdd = sdn + kCbChunk * P;         // [chunk]        dden_t
-  float* sk = sdd + kCbChunk;              // [chunk][d]     phi(k_s)
-  float* sv = sk + kCbChunk * d;           // [chunk][d]     v_s
-  float* sab = sv + kCbChunk * d;          // [warps][2][chunk] a_t = phi(q_t).phi(k_s), b_t = dnum_t.v_s + dden_t
+  float* sk = sdn + kCbChunk * P;          // [chunk][d + 1] phi(k_s)
+  float* sv = sk + kCbChunk * P;           // [chunk][d + 1] v_s
+  float* sdd = sv + kCbChunk * P;          // [chunk]        dden_t
+  float* sa = sdd + kCbChunk;              // [chunk][CP]    a_st (t >= s, else 0)
+  float* sb = sa + kCbChunk * CP;          // [chunk][CP]    b_st (t >= s, else 0)
   const int64_t item = blockIdx.x;
   const int64_t j = item % g.M, bh = item / g.M;
   const int64_t b = bh / H, h = bh % H;
-  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int tid = threadIdx.x;
   const float wjj = __ldg(W + j * g.M + j);
   const float* src = dS + (bh * g.M + j) * static_cast<int64_t>(E + d);
   for (int e = tid; e < E; e += kCbThreads) gs[(e / d) * P + e % d] = src[e];
@@ -703,8 +862,10 @@ simt_causal_bwd_key(const T* __restrict__ q, Operand qo, const T* __restrict__ k
   T* dkb = dk + b * dko.sb + h * dko.sh;
   T* dvb = dv + b * dvo.sb + h * dvo.sh;
   const float* dnb = dn + (bh * g.M + j) * g.w * P;
-  float* mya = sab + warp * 2 * kCbChunk;
-  float* myb = mya + kCbChunk;
+  const int tt = tid / 16, cc = tid % 16;          // sources 2 tt, 2 tt + 1; columns cc + 16 j
+  const int s0t = 2 * tt, s1t = s0t + 1;
+  const int pi = tid / 16, pj = tid % 16;          // pair tiles: sources 2 pi (+1), queries 2 pj (+1)
+  const int r0 = TB * (tid / 16), c0 = TB * (tid % 16);   // state tile
   const int64_t nch = (g.w + kCbChunk - 1) / kCbChunk;
   for (int64_t ci = nch - 1; ci >= 0; --ci) {
     const int64_t s0 = ci * kCbChunk;
@@ -715,46 +876,119 @@ simt_causal_bwd_key(const T* __restrict__ q, Operand qo, const T* __restrict__ k
       const int64_t n = token_of(g, j, s0 + sl);
       sq[sl * P + c] = phi_f(load_f(qb + n * qo.sn + c), phi_kind, eps);
       sdn[sl * P + c] = dnb[(s0 + sl) * P + c];
-      sk[sl * d + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
-      sv[sl * d + c] = load_f(vb + n * vo.sn + c);
+      sk[sl * P + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
+      sv[sl * P + c] = load_f(vb + n * vo.sn + c);
     }
     for (int sl = tid; sl < cnt; sl += kCbThreads) sdd[sl] = dnb[(s0 + sl) * P + d];
     __syncthreads();
-    for (int sl = warp; sl < cnt; sl += kCbWarps) {
-      const float* myk = sk + sl * d;
-      const float* myv = sv + sl * d;
-      float a = 0.0f, bt = 0.0f;
-      if (lane >= sl && lane < cnt) {   // lane = query token t >= s of this chunk
-        for (int r = 0; r < d; ++r) a = fmaf(sq[lane * P + r], myk[r], a);
-        for (int c = 0; c < d; ++c) bt = fmaf(sdn[lane * P + c], myv[c], bt);
-        bt += sdd[lane];
+    // ---- 1: a_st and b_st, 2 x 2 blocks (sources ra, rb; queries ca, cb)
+    {
+      const int ra = 2 * pi, rb = ra + 1, ca = 2 * pj, cb = ca + 1;
+      float a00 = 0.0f, a01 = 0.0f, a10 = 0.0f, a11 = 0.0f;
+      float b00 = 0.0f, b01 = 0.0f, b10 = 0.0f, b11 = 0.0f;
+      for (int r = 0; r < d; ++r) {
+        const float ka = sk[ra * P + r], kb2 = sk[rb * P + r], qa = sq[ca * P + r], qb2 = sq[cb * P + r];
+        const float va = sv[ra * P + r], vb2 = sv[rb * P + r], na = sdn[ca * P + r], nb = sdn[cb * P + r];
+        a00 = fmaf(ka, qa, a00);
+        a01 = fmaf(ka, qb2, a01);
+        a10 = fmaf(kb2, qa, a10);
+        a11 = fmaf(kb2, qb2, a11);
+        b00 = fmaf(va, na, b00);
+        b01 = fmaf(va, nb, b01);
+        b10 = fmaf(vb2, na, b10);
+        b11 = fmaf(vb2, nb, b11);
       }
-      mya[lane] = a;
-      myb[lane] = bt;
-      __syncwarp();
-      const int64_t n = token_of(g, j, s0 + sl);
-      for (int c = lane; c < d; c += 32) {
-        float x = 0.0f, own = 0.0f;
-        for (int r = 0; r < d; ++r) x = fmaf(myk[r], gs[r * P + c], x);
-        for (int t = sl; t < cnt; ++t) own = fmaf(mya[t], sdn[t * P + c], own);
-        store_f(dvb + n * dvo.sn + c, fmaf(wjj, own, x));
-      }
-      for (int r = lane; r < d; r += 32) {
-        float x = gz[r], own = 0.0f;
-        for (int c = 0; c < d; ++c) x = fmaf(gs[r * P + c], myv[c], x);
-        for (int t = sl; t < cnt; ++t) own = fmaf(sq[t * P + r], myb[t], own);
-        x = fmaf(wjj, own, x);
-        const float kr = load_f(kb + n * ko.sn + r);
-        store_f(dkb + n * dko.sn + r, kr > 0.0f ? x : 0.0f);
-      }
-      __syncwarp();
+      const float dda = sdd[ca], ddb = sdd[cb];
+      const bool m00 = ca < cnt && ca >= ra, m01 = cb < cnt && cb >= ra;
+      const bool m10 = ca < cnt && ca >= rb, m11 = cb < cnt && cb >= rb;
+      sa[ra * CP + ca] = m00 ? a00 : 0.0f;
+      sa[ra * CP + cb] = m01 ? a01 : 0.0f;
+      sa[rb * CP + ca] = m10 ? a10 : 0.0f;
+      sa[rb * CP + cb] = m11 ? a11 : 0.0f;
+      sb[ra * CP + ca] = m00 ? b00 + dda : 0.0f;
+      sb[ra * CP + cb] = m01 ? b01 + ddb : 0.0f;
+      sb[rb * CP + ca] = m10 ? b10 + dda : 0.0f;
+      sb[rb * CP + cb] = m11 ? b11 + ddb : 0.0f;
     }
     __syncthreads();
-    for (int e = tid; e < E; e += kCbThreads) {
-      const int r = e / d, c = e % d;
-      float x = 0.0f;
-      for (int t = 0; t < cnt; ++t) x = fmaf(sq[t * P + r], sdn[t * P + c], x);
-      gs[r * P + c] = fmaf(wjj, x, gs[r * P + c]);
+    // ---- 2: dv and dk of sources s0t, s1t (columns / rows cc + 16 j)
+    {
+      float v0[DB], v1[DB], w0[DB], w1[DB];
+#pragma unroll
+      for (int jj = 0; jj < DB; ++jj) v0[jj] = v1[jj] = w0[jj] = w1[jj] = 0.0f;
+      // G^T phi(k_s) (column c of G) and G v_s (row r of G): one pass over the inner index
+      for (int x = 0; x < d; ++x) {
+        const float k0 = sk[s0t * P + x], k1 = sk[s1t * P + x];
+        const float e0 = sv[s0t * P + x], e1 = sv[s1t * P + x];
+#pragma unroll
+        for (int jj = 0; jj < DB; ++jj) {
+          const float gcol = gs[x * P + cc + 16 * jj];    // G[x][c]   (past d: other data, discarded)
+          const float grow = gs[(cc + 16 * jj) * P + x];  // G[r][x]
+          v0[jj] = fmaf(k0, gcol, v0[jj]);
+          v1[jj] = fmaf(k1, gcol, v1[jj]);
+          w0[jj] = fmaf(grow, e0, w0[jj]);
+          w1[jj] = fmaf(grow, e1, w1[jj]);
+        }
+      }
+      float ov0[DB], ov1[DB], ok0[DB], ok1[DB];
+#pragma unroll
+      for (int jj = 0; jj < DB; ++jj) ov0[jj] = ov1[jj] = ok0[jj] = ok1[jj] = 0.0f;
+      for (int t = 0; t < cnt; ++t) {
+        const float a0 = sa[s0t * CP + t], a1 = sa[s1t * CP + t];
+        const float b0 = sb[s0t * CP + t], b1 = sb[s1t * CP + t];
+#pragma unroll
+        for (int jj = 0; jj < DB; ++jj) {
+          const float nv = sdn[t * P + cc + 16 * jj];
+          const float qv = sq[t * P + cc + 16 * jj];
+          ov0[jj] = fmaf(a0, nv, ov0[jj]);
+          ov1[jj] = fmaf(a1, nv, ov1[jj]);
+          ok0[jj] = fmaf(b0, qv, ok0[jj]);
+          ok1[jj] = fmaf(b1, qv, ok1[jj]);
+        }
+      }
+      const int64_t n0t = s0t < cnt ? token_of(g, j, s0 + s0t) : 0;
+      const int64_t n1t = s1t < cnt ? token_of(g, j, s0 + s1t) : 0;
+#pragma unroll
+      for (int jj = 0; jj < DB; ++jj) {
+        const int c = cc + 16 * jj;
+        if (c < d) {
+          const float zr = gz[c];
+          if (s0t < cnt) {
+            store_f(dvb + n0t * dvo.sn + c, fmaf(wjj, ov0[jj], v0[jj]));
+            const float x = fmaf(wjj, ok0[jj], w0[jj] + zr);
+            store_f(dkb + n0t * dko.sn + c, load_f(kb + n0t * ko.sn + c) > 0.0f ? x : 0.0f);
+          }
+          if (s1t < cnt) {
+            store_f(dvb + n1t * dvo.sn + c, fmaf(wjj, ov1[jj], v1[jj]));
+            const float x = fmaf(wjj, ok1[jj], w1[jj] + zr);
+            store_f(dkb + n1t * dko.sn + c, load_f(kb + n1t * ko.sn + c) > 0.0f ? x : 0.0f);
+          }
+        }
+      }
+    }
+    __syncthreads();   // phase 3 rewrites G, which phase 2 has read
+    // ---- 3: G += W_jj sum_t phi(q_t) dnum_t^T (a TB x TB tile per thread), gz likewise
+    {
+      float x[TB * TB];
+#pragma unroll
+      for (int m = 0; m < TB * TB; ++m) x[m] = 0.0f;
+      for (int t = 0; t < cnt; ++t) {
+        float qr[TB], nc[TB];
+#pragma unroll
+        for (int u = 0; u < TB; ++u) {
+          qr[u] = sq[t * P + r0 + u];
+          nc[u] = sdn[t * P + c0 + u];
+        }
+#pragma unroll
+        for (int u = 0; u < TB; ++u)
+#pragma unroll
+          for (int w = 0; w < TB; ++w) x[u * TB + w] = fmaf(qr[u], nc[w], x[u * TB + w]);
+      }
+#pragma unroll
+      for (int m = 0; m < TB * TB; ++m) {
+        const int r = r0 + m / TB, c = c0 + m % TB;
+        if (r < d && c < d) gs[r * P + c] = fmaf(wjj, x[m], gs[r * P + c]);
+      }
     }
     if (tid < d) {
       float x = 0.0f;
@@ -1053,7 +1287,7 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
   {
-    const size_t smem = (d * (d + 1) + d + kCbChunk * (2 * d + 2 * (d + 1) + 1) + kCbWarps * 2 * kCbChunk +
+    const size_t smem = (d * (d + 1) + d + 5 * kCbChunk * (d + 1) + 2 * kCbChunk + 2 * kCbChunk * (kCbChunk + 1) +
                          kCbWarps) * sizeof(float);
     auto launch = [&](auto kern) -> int {
       if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1065,10 +1299,10 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
           ws.diag, ws.dn);
       return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
     };
-    const int rc = d <= 16   ? launch(simt_causal_bwd_query<T, 1>)
-                   : d <= 32 ? launch(simt_causal_bwd_query<T, 4>)
-                   : d <= 64 ? launch(simt_causal_bwd_query<T, 16>)
-                             : launch(simt_causal_bwd_query<T, 64>);
+    const int rc = d <= 16   ? launch(simt_causal_bwd_query<T, 1, 1>)
+                   : d <= 32 ? launch(simt_causal_bwd_query<T, 4, 2>)
+                   : d <= 64 ? launch(simt_causal_bwd_query<T, 16, 4>)
+                             : launch(simt_causal_bwd_query<T, 64, 8>);
     if (rc != MHLA_OK) return rc;
   }
   {
@@ -1090,18 +1324,22 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
   {
-    const size_t smem = (d * (d + 1) + d + kCbChunk * (2 * (d + 1) + 1 + 2 * d) + kCbWarps * 2 * kCbChunk) *
+    const size_t smem = (d * (d + 1) + d + 4 * kCbChunk * (d + 1) + kCbChunk + 2 * kCbChunk * (kCbChunk + 1)) *
                         sizeof(float);
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(simt_causal_bwd_key<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return MHLA_ERR_CUDA;
-    KernelTimer timer("simt_causal_bwd_key", stream);
-    simt_causal_bwd_key<T><<<static_cast<unsigned>(items), kCbThreads, smem, stream>>>(
-        qp, p.q, kp, p.k, vp, p.v, dkp, bo.dk, dvp, bo.dv, g, p.H, d, p.phi_kind, p.eps, W, ws.Sp, ws.dn);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+    auto launch = [&](auto kern) -> int {
+      if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem)) != cudaSuccess)
+        return MHLA_ERR_CUDA;
+      KernelTimer timer("simt_causal_bwd_key", stream);
+      kern<<<static_cast<unsigned>(items), kCbThreads, smem, stream>>>(
+          qp, p.q, kp, p.k, vp, p.v, dkp, bo.dk, dvp, bo.dv, g, p.H, d, p.phi_kind, p.eps, W, ws.Sp, ws.dn);
+      return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+    };
+    return d <= 16   ? launch(simt_causal_bwd_key<T, 1, 1>)
+           : d <= 32 ? launch(simt_causal_bwd_key<T, 2, 2>)
+           : d <= 64 ? launch(simt_causal_bwd_key<T, 4, 4>)
+                     : launch(simt_causal_bwd_key<T, 8, 8>);
   }
-  return MHLA_OK;
 }
 
 }  // namespace
