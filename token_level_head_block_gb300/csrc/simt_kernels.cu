@@ -41,15 +41,19 @@ __device__ __forceinline__ int64_t token_of(const TokenGeom& g, int64_t j, int64
 
 constexpr int kSumThreads = 256;
 constexpr int kSumChunk = 32;   // tokens staged in shared memory per step
+constexpr int kSumLanes = kSumThreads / kSumChunk;   // threads staging one token row
 
-// One CTA per (b, h, j).  ENT = ceil(d*d / 256) accumulators per thread.
-template <typename T, int ENT>
+// One CTA per (b, h, j).  Thread (ty, tx) = (tid / 16, tid % 16) accumulates
+// the TB x TB tile of S_j at rows TB ty.., columns TB tx.. (16 TB >= d): per
+// token, TB values of phi(k) and TB of v feed TB * TB products.  Every entry
+// sums its tokens in slot order.
+template <typename T, int TB>
 __global__ void __launch_bounds__(kSumThreads)
 simt_summary(const T* __restrict__ k, const T* __restrict__ v, Operand ko, Operand vo, TokenGeom g,
              int64_t H, int d, int phi_kind, float eps, float* __restrict__ Sz) {
-  extern __shared__ float sm[];
-  float* sk = sm;                    // [kSumChunk][d]  phi(k)
-  float* sv = sm + kSumChunk * d;    // [kSumChunk][d]  v
+  extern __shared__ __align__(16) float sum_sm[];
+  float* sk = sum_sm;                    // [kSumChunk][d]  phi(k)
+  float* sv = sum_sm + kSumChunk * d;    // [kSumChunk][d]  v, then 16 TB floats of slack
   const int64_t item = blockIdx.x;
   const int64_t j = item % g.M, bh = item / g.M;
   const int64_t b = bh / H, h = bh % H;
@@ -57,30 +61,59 @@ simt_summary(const T* __restrict__ k, const T* __restrict__ v, Operand ko, Opera
   const int E = d * d;
   const T* kb = k + b * ko.sb + h * ko.sh;
   const T* vb = v + b * vo.sb + h * vo.sh;
+  const int r0 = TB * (tid / 16), c0 = TB * (tid % 16);
+  const int srow = tid / kSumLanes, spart = tid % kSumLanes;
 
-  float acc[ENT];
+  float acc[TB * TB];
 #pragma unroll
-  for (int m = 0; m < ENT; ++m) acc[m] = 0.0f;
+  for (int m = 0; m < TB * TB; ++m) acc[m] = 0.0f;
   float zacc = 0.0f;
 
   for (int64_t s0 = 0; s0 < g.w; s0 += kSumChunk) {
     const int cnt = static_cast<int>(g.w - s0 < kSumChunk ? g.w - s0 : kSumChunk);
-    for (int e = tid; e < cnt * d; e += kSumThreads) {
-      const int sl = e / d, c = e % d;
-      const int64_t n = token_of(g, j, s0 + sl);
-      sk[sl * d + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
-      sv[sl * d + c] = load_f(vb + n * vo.sn + c);
+    if (srow < cnt) {
+      const int64_t n = token_of(g, j, s0 + srow);
+      for (int c = spart; c < d; c += kSumLanes) {
+        sk[srow * d + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
+        sv[srow * d + c] = load_f(vb + n * vo.sn + c);
+      }
     }
     __syncthreads();
+    auto scalar_steps = [&]() {
+      for (int sl = 0; sl < cnt; ++sl) {
+        float kr[TB], vc[TB];
 #pragma unroll
-    for (int m = 0; m < ENT; ++m) {
-      const int e = tid + m * kSumThreads;
-      if (e < E) {
-        const int r = e / d, c = e % d;
-        float a = acc[m];
-        for (int sl = 0; sl < cnt; ++sl) a = fmaf(sk[sl * d + r], sv[sl * d + c], a);
-        acc[m] = a;
+        for (int u = 0; u < TB; ++u) {
+          kr[u] = sk[sl * d + r0 + u];
+          vc[u] = sv[sl * d + c0 + u];
+        }
+#pragma unroll
+        for (int u = 0; u < TB; ++u)
+#pragma unroll
+          for (int w = 0; w < TB; ++w) acc[u * TB + w] = fmaf(kr[u], vc[w], acc[u * TB + w]);
       }
+    };
+    if constexpr (TB % 4 == 0) {
+      if (d % 4 == 0) {
+        for (int sl = 0; sl < cnt; ++sl) {
+          float kr[TB], vc[TB];
+#pragma unroll
+          for (int u = 0; u < TB; u += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(sk + sl * d + r0 + u);
+            const float4 c = *reinterpret_cast<const float4*>(sv + sl * d + c0 + u);
+            kr[u] = a.x, kr[u + 1] = a.y, kr[u + 2] = a.z, kr[u + 3] = a.w;
+            vc[u] = c.x, vc[u + 1] = c.y, vc[u + 2] = c.z, vc[u + 3] = c.w;
+          }
+#pragma unroll
+          for (int u = 0; u < TB; ++u)
+#pragma unroll
+            for (int w = 0; w < TB; ++w) acc[u * TB + w] = fmaf(kr[u], vc[w], acc[u * TB + w]);
+        }
+      } else {
+        scalar_steps();
+      }
+    } else {
+      scalar_steps();
     }
     if (tid < d)
       for (int sl = 0; sl < cnt; ++sl) zacc += sk[sl * d + tid];
@@ -88,43 +121,126 @@ simt_summary(const T* __restrict__ k, const T* __restrict__ v, Operand ko, Opera
   }
   float* out = Sz + (bh * g.M + j) * static_cast<int64_t>(E + d);
 #pragma unroll
-  for (int m = 0; m < ENT; ++m) {
-    const int e = tid + m * kSumThreads;
-    if (e < E) out[e] = acc[m];
+  for (int m = 0; m < TB * TB; ++m) {
+    const int r = r0 + m / TB, c = c0 + m % TB;
+    if (r < d && c < d) out[r * d + c] = acc[m];
   }
   if (tid < d) out[E + tid] = zacc;
 }
 
-constexpr int kMixThreads = 128;
-constexpr int kMixRows = 8;     // query blocks i per thread
+// S_j, z_j of every (b, h, j) into Sz.
+template <typename T>
+int launch_summary(const Problem& p, const TokenGeom& g, float* Sz, cudaStream_t stream) {
+  const int d = static_cast<int>(p.d);
+  const int64_t items = p.BH() * p.M;
+  const size_t smem = (2 * kSumChunk * d + 16 * 8) * sizeof(float);
+  const T* kp = static_cast<const T*>(p.k.data);
+  const T* vp = static_cast<const T*>(p.v.data);
+  auto launch = [&](auto kern) -> int {
+    KernelTimer timer("simt_summary", stream);
+    kern<<<static_cast<unsigned>(items), kSumThreads, smem, stream>>>(kp, vp, p.k, p.v, g, p.H, d, p.phi_kind,
+                                                                      p.eps, Sz);
+    return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+  };
+  return d <= 16   ? launch(simt_summary<T, 1>)
+         : d <= 32 ? launch(simt_summary<T, 2>)
+         : d <= 64 ? launch(simt_summary<T, 4>)
+                   : launch(simt_summary<T, 8>);
+}
+
+constexpr int kMixThreads = 256;
+constexpr int kMixTileI = 64;    // output blocks per CTA, 8 per warp
+constexpr int kMixTileE = 128;   // entries per CTA, 4 per lane (stride 32)
+constexpr int kMixK = 32;        // source blocks staged per step
 
 // S~ = W . S per (b, h), treating the d*(d+1) entries of every block as columns
 // (TRANS: W^T . S, the mixing step of the backward pass).
 // (PAST: only source blocks j < i, the mixed past summaries of causal MHLA;
 // with TRANS, only i > j: the reverse of that mixing in the causal backward.)
+// A CTA holds a 64-block x 128-entry tile of the output; W's 64 x 32 slab and
+// the sources' 32 x 128 slab go through shared memory, and each thread keeps
+// 8 x 4 sums.  Every output sums its sources in ascending order, skipping the
+// ones that PAST excludes.
 template <bool TRANS, bool PAST = false>
 __global__ void __launch_bounds__(kMixThreads)
 simt_mix(const float* __restrict__ W, const float* __restrict__ Sz, float* __restrict__ Szt,
          int64_t M, int64_t E, int64_t BH) {
-  const int64_t e = static_cast<int64_t>(blockIdx.x) * kMixThreads + threadIdx.x;
-  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * kMixRows;
-  if (e >= E) return;
+  __shared__ __align__(16) float wsl[kMixK][kMixTileI + 4];   // wsl[jj][r]: weight of source j0 + jj in row i0 + r
+  __shared__ float ssl[kMixK][kMixTileE];                     // ssl[jj][c]: source j0 + jj, entry e0 + c
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int64_t e0 = static_cast<int64_t>(blockIdx.x) * kMixTileE;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * kMixTileI;
+  const int64_t ia = i0 + 8 * warp;   // this warp's first output block
+  // sources that reach some row of the tile
+  const int64_t jb = PAST && TRANS ? i0 + 1 : 0;
+  const int64_t je = PAST && !TRANS ? std::min<int64_t>(M, i0 + kMixTileI - 1) : M;
   for (int64_t bh = blockIdx.z; bh < BH; bh += gridDim.z) {
-    float acc[kMixRows];
+    float acc[8][4];
 #pragma unroll
-    for (int u = 0; u < kMixRows; ++u) acc[u] = 0.0f;
-    const float* src = Sz + bh * M * E + e;
-    for (int64_t j = 0; j < M; ++j) {
-      const float s = src[j * E];
+    for (int u = 0; u < 8; ++u)
 #pragma unroll
-      for (int u = 0; u < kMixRows; ++u)
-        if (i0 + u < M && (!PAST || (TRANS ? j > i0 + u : j < i0 + u)))
-          acc[u] = fmaf(__ldg(TRANS ? W + j * M + i0 + u : W + (i0 + u) * M + j), s, acc[u]);
+      for (int w = 0; w < 4; ++w) acc[u][w] = 0.0f;
+    const float* src = Sz + bh * M * E;
+    for (int64_t j0 = jb; j0 < je; j0 += kMixK) {
+      __syncthreads();   // the previous slab is consumed
+      for (int x = tid; x < kMixK * kMixTileI; x += kMixThreads) {
+        const int jj = TRANS ? x / kMixTileI : x % kMixK;
+        const int r = TRANS ? x % kMixTileI : x / kMixK;
+        const int64_t i = i0 + r, j = j0 + jj;
+        float wv = 0.0f;
+        if (i < M && j < je) wv = __ldg(TRANS ? W + j * M + i : W + i * M + j);
+        wsl[jj][r] = wv;
+      }
+      for (int x = tid; x < kMixK * kMixTileE; x += kMixThreads) {
+        const int jj = x / kMixTileE, c = x % kMixTileE;
+        const int64_t j = j0 + jj, e = e0 + c;
+        ssl[jj][c] = j < je && e < E ? src[j * E + e] : 0.0f;
+      }
+      __syncthreads();
+      const int cnt = static_cast<int>(je - j0 < kMixK ? je - j0 : kMixK);
+      for (int jj = 0; jj < cnt; ++jj) {
+        const int64_t j = j0 + jj;
+        const float4 wa = *reinterpret_cast<const float4*>(&wsl[jj][8 * warp]);
+        const float4 wb = *reinterpret_cast<const float4*>(&wsl[jj][8 * warp + 4]);
+        const float wr[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+        float sc[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) sc[w] = ssl[jj][lane + 32 * w];
+        if (!PAST || (TRANS ? j > ia + 7 : j < ia)) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(wr[u], sc[w], acc[u][w]);
+        } else if (TRANS ? j > ia : j < ia + 7) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (TRANS ? j > ia + u : j < ia + u)
+#pragma unroll
+              for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(wr[u], sc[w], acc[u][w]);
+        }
+      }
     }
 #pragma unroll
-    for (int u = 0; u < kMixRows; ++u)
-      if (i0 + u < M) Szt[(bh * M + i0 + u) * E + e] = acc[u];
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int64_t i = ia + u, e = e0 + lane + 32 * w;
+        if (i < M && e < E) Szt[(bh * M + i) * E + e] = acc[u][w];
+      }
   }
+}
+
+// dst = W . src (TRANS: W^T . src), PAST as simt_mix, per (b, h).
+template <bool TRANS, bool PAST>
+int launch_mix(const float* W, const float* src, float* dst, int64_t M, int64_t E, int64_t BH,
+               cudaStream_t stream) {
+  const int64_t gx = (E + kMixTileE - 1) / kMixTileE, gy = (M + kMixTileI - 1) / kMixTileI;
+  if (gx > 0x7fffffffLL || gy > 65535) return MHLA_ERR_UNSUPPORTED;
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
+                  static_cast<unsigned>(std::min<int64_t>(BH, 65535)));
+  KernelTimer timer("simt_mix", stream);
+  simt_mix<TRANS, PAST><<<grid, kMixThreads, 0, stream>>>(W, src, dst, M, E, BH);
+  return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
 }
 
 constexpr int kOutThreads = 256;
@@ -1021,38 +1137,13 @@ int launch_simt_typed(const Problem& p, const float* W, const SimtWorkspace& ws,
   const int64_t BH = p.BH();
   const int64_t items = BH * p.M;
   if (items > 0x7fffffffLL) return MHLA_ERR_UNSUPPORTED;
-  const size_t sum_smem = 2 * kSumChunk * d * sizeof(float);
   const T* qp = static_cast<const T*>(p.q.data);
-  const T* kp = static_cast<const T*>(p.k.data);
-  const T* vp = static_cast<const T*>(p.v.data);
   T* op = static_cast<T*>(p.o.data);
-  {
-    KernelTimer timer("simt_summary", stream);
-    if (d <= 16)
-      simt_summary<T, 1><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else if (d <= 32)
-      simt_summary<T, 4><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else if (d <= 64)
-      simt_summary<T, 16><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else
-      simt_summary<T, 64><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
+  if (const int rc = launch_summary<T>(p, g, ws.Sz, stream); rc != MHLA_OK) return rc;
 
   const int64_t E = p.d * (p.d + 1);
-  const dim3 mix_grid(static_cast<unsigned>((E + kMixThreads - 1) / kMixThreads),
-                      static_cast<unsigned>((p.M + kMixRows - 1) / kMixRows),
-                      static_cast<unsigned>(std::min<int64_t>(BH, 65535)));
-  if (mix_grid.y > 65535) return MHLA_ERR_UNSUPPORTED;
-  {
-    KernelTimer timer("simt_mix", stream);
-    simt_mix<false><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.Sz, ws.Szt, p.M, E, BH);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
+  if (const int rc = launch_mix<false, false>(W, ws.Sz, ws.Szt, p.M, E, BH, stream); rc != MHLA_OK)
+    return rc;
 
   const size_t out_smem = (E + p.d + kOutWarps * p.d) * sizeof(float);
   if (out_smem > 48 * 1024) {
@@ -1087,32 +1178,9 @@ int launch_simt_bwd_typed(const Problem& p, const float* W, const BwdOperands& b
   const int64_t E = p.d * (p.d + 1);
 
   // forward summaries and mixing, recomputed
-  {
-    const size_t sum_smem = 2 * kSumChunk * d * sizeof(float);
-    KernelTimer timer("simt_summary", stream);
-    if (d <= 16)
-      simt_summary<T, 1><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else if (d <= 32)
-      simt_summary<T, 4><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else if (d <= 64)
-      simt_summary<T, 16><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else
-      simt_summary<T, 64><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
-  const dim3 mix_grid(static_cast<unsigned>((E + kMixThreads - 1) / kMixThreads),
-                      static_cast<unsigned>((p.M + kMixRows - 1) / kMixRows),
-                      static_cast<unsigned>(std::min<int64_t>(BH, 65535)));
-  if (mix_grid.y > 65535) return MHLA_ERR_UNSUPPORTED;
-  {
-    KernelTimer timer("simt_mix", stream);
-    simt_mix<false><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.Sz, ws.Szt, p.M, E, BH);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
+  if (const int rc = launch_summary<T>(p, g, ws.Sz, stream); rc != MHLA_OK) return rc;
+  if (const int rc = launch_mix<false, false>(W, ws.Sz, ws.Szt, p.M, E, BH, stream); rc != MHLA_OK)
+    return rc;
   // query blocks: dq, dS~, dz~
   {
     const size_t smem = (d * (d + 1) + d + 2 * kBwdChunk * d + kBwdChunk) * sizeof(float);
@@ -1145,11 +1213,8 @@ int launch_simt_bwd_typed(const Problem& p, const float* W, const BwdOperands& b
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
   // dS = W^T dS~ into the S~ buffer
-  {
-    KernelTimer timer("simt_mix", stream);
-    simt_mix<true><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.dSzt, ws.Szt, p.M, E, BH);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
+  if (const int rc = launch_mix<true, false>(W, ws.dSzt, ws.Szt, p.M, E, BH, stream); rc != MHLA_OK)
+    return rc;
   // source blocks: dk, dv
   {
     const size_t smem = (d * (d + 1) + d + 2 * kBwdWarps * d) * sizeof(float);
@@ -1175,33 +1240,10 @@ int launch_simt_causal_typed(const Problem& p, const float* W, const SimtWorkspa
   const T* kp = static_cast<const T*>(p.k.data);
   const T* vp = static_cast<const T*>(p.v.data);
   T* op = static_cast<T*>(p.o.data);
-  {
-    const size_t sum_smem = 2 * kSumChunk * d * sizeof(float);
-    KernelTimer timer("simt_summary", stream);
-    if (d <= 16)
-      simt_summary<T, 1><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else if (d <= 32)
-      simt_summary<T, 4><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else if (d <= 64)
-      simt_summary<T, 16><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else
-      simt_summary<T, 64><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
+  if (const int rc = launch_summary<T>(p, g, ws.Sz, stream); rc != MHLA_OK) return rc;
   const int64_t E = p.d * (p.d + 1);
-  const dim3 mix_grid(static_cast<unsigned>((E + kMixThreads - 1) / kMixThreads),
-                      static_cast<unsigned>((p.M + kMixRows - 1) / kMixRows),
-                      static_cast<unsigned>(std::min<int64_t>(BH, 65535)));
-  if (mix_grid.y > 65535) return MHLA_ERR_UNSUPPORTED;
-  {
-    KernelTimer timer("simt_mix", stream);
-    simt_mix<false, true><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.Sz, ws.Szt, p.M, E, BH);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
+  if (const int rc = launch_mix<false, true>(W, ws.Sz, ws.Szt, p.M, E, BH, stream); rc != MHLA_OK)
+    return rc;
   {
     const size_t smem = (d * d + d + kCausalChunk * (3 * d + 1) + kCausalWarps * kCausalChunk) * sizeof(float);
     auto launch = [&](auto kern) -> int {
@@ -1260,32 +1302,9 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
   T* dkp = static_cast<T*>(bo.dk.data);
   T* dvp = static_cast<T*>(bo.dv.data);
   const int64_t E = p.d * (p.d + 1);
-  {
-    const size_t sum_smem = 2 * kSumChunk * d * sizeof(float);
-    KernelTimer timer("simt_summary", stream);
-    if (d <= 16)
-      simt_summary<T, 1><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else if (d <= 32)
-      simt_summary<T, 4><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else if (d <= 64)
-      simt_summary<T, 16><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    else
-      simt_summary<T, 64><<<static_cast<unsigned>(items), kSumThreads, sum_smem, stream>>>(
-          kp, vp, p.k, p.v, g, p.H, d, p.phi_kind, p.eps, ws.Sz);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
-  const dim3 mix_grid(static_cast<unsigned>((E + kMixThreads - 1) / kMixThreads),
-                      static_cast<unsigned>((p.M + kMixRows - 1) / kMixRows),
-                      static_cast<unsigned>(std::min<int64_t>(BH, 65535)));
-  if (mix_grid.y > 65535) return MHLA_ERR_UNSUPPORTED;
-  {
-    KernelTimer timer("simt_mix", stream);
-    simt_mix<false, true><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.Sz, ws.Sp, p.M, E, BH);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
+  if (const int rc = launch_summary<T>(p, g, ws.Sz, stream); rc != MHLA_OK) return rc;
+  if (const int rc = launch_mix<false, true>(W, ws.Sz, ws.Sp, p.M, E, BH, stream); rc != MHLA_OK)
+    return rc;
   {
     const size_t smem = (d * (d + 1) + d + 5 * kCbChunk * (d + 1) + 2 * kCbChunk + 2 * kCbChunk * (kCbChunk + 1) +
                          kCbWarps) * sizeof(float);
@@ -1318,11 +1337,8 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
                                                                                        p.M, BH, KS);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
-  {
-    KernelTimer timer("simt_mix", stream);
-    simt_mix<true, true><<<mix_grid, kMixThreads, 0, stream>>>(W, ws.dSp, ws.Sp, p.M, E, BH);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-  }
+  if (const int rc = launch_mix<true, true>(W, ws.dSp, ws.Sp, p.M, E, BH, stream); rc != MHLA_OK)
+    return rc;
   {
     const size_t smem = (d * (d + 1) + d + 4 * kCbChunk * (d + 1) + kCbChunk + 2 * kCbChunk * (kCbChunk + 1)) *
                         sizeof(float);
