@@ -376,7 +376,7 @@ def test_causal_backward_rejects_malformed_requests_before_any_launch(L):
                                                      ctypes.byref(mhla.shape3(block)), path,
                                                      ctypes.byref(n)) == OK
         BH, M, N, d = 6, 16, 1024, 64
-        KS = 8   # the dW partial products split d (d + 1) = 4160 entries in 8 runs (6 tiles are too few CTAs)
+        KS = 16  # the dW partial products split d (d + 1) = 4160 entries in 16 runs (6 tiles are too few CTAs)
         need = 3 * BH * M * d * (d + 1) * 4 + BH * KS * M * M * 4 + BH * M * 4 + BH * N * (d + 1) * 4
         assert n.value % 256 == 0 and need <= n.value < need + 6 * 256
     assert L.mhla_backward_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3((32, 32))),

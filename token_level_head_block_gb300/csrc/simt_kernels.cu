@@ -24,6 +24,21 @@ __device__ __forceinline__ float load_f(const __nv_bfloat16* p) { return __bfloa
 __device__ __forceinline__ void store_f(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_f(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
+// Asynchronous 4-byte global -> shared copies (any alignment); a copy with
+// full = false reads nothing and writes zero.  wait<N> returns once at most N
+// of this thread's committed groups are still in flight.
+__device__ __forceinline__ void cp_async_f32(float* dst, const float* src, bool full) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(full ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ float phi_f(float x, int kind, float eps) {
   const float r = fmaxf(x, 0.0f);
   return kind == MHLA_PHI_RELU_EPS ? r + eps : r;
@@ -151,22 +166,25 @@ int launch_summary(const Problem& p, const TokenGeom& g, float* Sz, cudaStream_t
 constexpr int kMixThreads = 256;
 constexpr int kMixTileI = 64;    // output blocks per CTA, 8 per warp
 constexpr int kMixTileE = 128;   // entries per CTA, 4 per lane (stride 32)
-constexpr int kMixK = 32;        // source blocks staged per step
+constexpr int kMixK = 16;        // source blocks per slab
+constexpr int kMixStages = 4;    // slabs in flight
+constexpr int kMixWRow = kMixTileI + 4;
+constexpr int kMixStage = kMixK * kMixWRow + kMixK * kMixTileE;   // floats per stage
+constexpr size_t kMixSmem = static_cast<size_t>(kMixStages) * kMixStage * sizeof(float);
 
 // S~ = W . S per (b, h), treating the d*(d+1) entries of every block as columns
 // (TRANS: W^T . S, the mixing step of the backward pass).
 // (PAST: only source blocks j < i, the mixed past summaries of causal MHLA;
 // with TRANS, only i > j: the reverse of that mixing in the causal backward.)
-// A CTA holds a 64-block x 128-entry tile of the output; W's 64 x 32 slab and
-// the sources' 32 x 128 slab go through shared memory, and each thread keeps
-// 8 x 4 sums.  Every output sums its sources in ascending order, skipping the
-// ones that PAST excludes.
+// A CTA holds a 64-block x 128-entry tile of the output; W's 64 x 16 slabs and
+// the sources' 16 x 128 slabs go through shared memory in a four-stage cp.async
+// ring, and each thread keeps 8 x 4 sums.  Every output sums its sources in
+// ascending order, skipping the ones that PAST excludes.
 template <bool TRANS, bool PAST = false>
 __global__ void __launch_bounds__(kMixThreads)
 simt_mix(const float* __restrict__ W, const float* __restrict__ Sz, float* __restrict__ Szt,
          int64_t M, int64_t E, int64_t BH) {
-  __shared__ __align__(16) float wsl[kMixK][kMixTileI + 4];   // wsl[jj][r]: weight of source j0 + jj in row i0 + r
-  __shared__ float ssl[kMixK][kMixTileE];                     // ssl[jj][c]: source j0 + jj, entry e0 + c
+  extern __shared__ __align__(16) float mix_sm[];   // [stage]: W slab [jj][kMixWRow], then source slab [jj][128]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int64_t e0 = static_cast<int64_t>(blockIdx.x) * kMixTileE;
   const int64_t i0 = static_cast<int64_t>(blockIdx.y) * kMixTileI;
@@ -174,38 +192,56 @@ simt_mix(const float* __restrict__ W, const float* __restrict__ Sz, float* __res
   // sources that reach some row of the tile
   const int64_t jb = PAST && TRANS ? i0 + 1 : 0;
   const int64_t je = PAST && !TRANS ? std::min<int64_t>(M, i0 + kMixTileI - 1) : M;
+  const int64_t nslab = je > jb ? (je - jb + kMixK - 1) / kMixK : 0;
   for (int64_t bh = blockIdx.z; bh < BH; bh += gridDim.z) {
+    const float* src = Sz + bh * M * E;
+    // slab n into stage n % kMixStages (nothing past the last slab; the commit
+    // keeps one group per slot either way)
+    auto stage = [&](int64_t n) {
+      if (n < nslab) {
+        float* ws = mix_sm + (n % kMixStages) * kMixStage;
+        float* ss = ws + kMixK * kMixWRow;
+        const int64_t j0 = jb + n * kMixK;
+        for (int x = tid; x < kMixK * kMixTileI; x += kMixThreads) {
+          const int jj = TRANS ? x / kMixTileI : x % kMixK;
+          const int r = TRANS ? x % kMixTileI : x / kMixK;
+          const int64_t i = i0 + r, j = j0 + jj;
+          const bool in = i < M && j < je;
+          cp_async_f32(ws + jj * kMixWRow + r, in ? (TRANS ? W + j * M + i : W + i * M + j) : W, in);
+        }
+        for (int x = tid; x < kMixK * kMixTileE; x += kMixThreads) {
+          const int jj = x / kMixTileE, c = x % kMixTileE;
+          const int64_t j = j0 + jj, e = e0 + c;
+          const bool in = j < je && e < E;
+          cp_async_f32(ss + jj * kMixTileE + c, in ? src + j * E + e : src, in);
+        }
+      }
+      cp_async_commit();
+    };
     float acc[8][4];
 #pragma unroll
     for (int u = 0; u < 8; ++u)
 #pragma unroll
       for (int w = 0; w < 4; ++w) acc[u][w] = 0.0f;
-    const float* src = Sz + bh * M * E;
-    for (int64_t j0 = jb; j0 < je; j0 += kMixK) {
-      __syncthreads();   // the previous slab is consumed
-      for (int x = tid; x < kMixK * kMixTileI; x += kMixThreads) {
-        const int jj = TRANS ? x / kMixTileI : x % kMixK;
-        const int r = TRANS ? x % kMixTileI : x / kMixK;
-        const int64_t i = i0 + r, j = j0 + jj;
-        float wv = 0.0f;
-        if (i < M && j < je) wv = __ldg(TRANS ? W + j * M + i : W + i * M + j);
-        wsl[jj][r] = wv;
-      }
-      for (int x = tid; x < kMixK * kMixTileE; x += kMixThreads) {
-        const int jj = x / kMixTileE, c = x % kMixTileE;
-        const int64_t j = j0 + jj, e = e0 + c;
-        ssl[jj][c] = j < je && e < E ? src[j * E + e] : 0.0f;
-      }
-      __syncthreads();
+    __syncthreads();   // the previous (b, h) has finished with every stage
+#pragma unroll
+    for (int n = 0; n < kMixStages - 1; ++n) stage(n);
+    for (int64_t n = 0; n < nslab; ++n) {
+      cp_async_wait<kMixStages - 2>();   // slab n has landed (this thread's copies)
+      __syncthreads();                   // everyone's copies, and slab n - 1's stage is free
+      stage(n + kMixStages - 1);
+      const float* ws = mix_sm + (n % kMixStages) * kMixStage;
+      const float* ss = ws + kMixK * kMixWRow;
+      const int64_t j0 = jb + n * kMixK;
       const int cnt = static_cast<int>(je - j0 < kMixK ? je - j0 : kMixK);
       for (int jj = 0; jj < cnt; ++jj) {
         const int64_t j = j0 + jj;
-        const float4 wa = *reinterpret_cast<const float4*>(&wsl[jj][8 * warp]);
-        const float4 wb = *reinterpret_cast<const float4*>(&wsl[jj][8 * warp + 4]);
+        const float4 wa = *reinterpret_cast<const float4*>(ws + jj * kMixWRow + 8 * warp);
+        const float4 wb = *reinterpret_cast<const float4*>(ws + jj * kMixWRow + 8 * warp + 4);
         const float wr[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
         float sc[4];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) sc[w] = ssl[jj][lane + 32 * w];
+        for (int w = 0; w < 4; ++w) sc[w] = ss[jj * kMixTileE + lane + 32 * w];
         if (!PAST || (TRANS ? j > ia + 7 : j < ia)) {
 #pragma unroll
           for (int u = 0; u < 8; ++u)
@@ -220,6 +256,7 @@ simt_mix(const float* __restrict__ W, const float* __restrict__ Sz, float* __res
         }
       }
     }
+    cp_async_wait<0>();   // only empty groups remain; nothing may land after the next (b, h) starts
 #pragma unroll
     for (int u = 0; u < 8; ++u)
 #pragma unroll
@@ -238,8 +275,11 @@ int launch_mix(const float* W, const float* src, float* dst, int64_t M, int64_t 
   if (gx > 0x7fffffffLL || gy > 65535) return MHLA_ERR_UNSUPPORTED;
   const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
                   static_cast<unsigned>(std::min<int64_t>(BH, 65535)));
+  if (cudaFuncSetAttribute(simt_mix<TRANS, PAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kMixSmem)) != cudaSuccess)
+    return MHLA_ERR_CUDA;
   KernelTimer timer("simt_mix", stream);
-  simt_mix<TRANS, PAST><<<grid, kMixThreads, 0, stream>>>(W, src, dst, M, E, BH);
+  simt_mix<TRANS, PAST><<<grid, kMixThreads, kMixSmem, stream>>>(W, src, dst, M, E, BH);
   return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
 }
 
@@ -545,53 +585,64 @@ simt_bwd_key(const T* __restrict__ k, Operand ko, const T* __restrict__ v, Opera
 constexpr int kDwTile = 64;     // 64 x 64 outputs per CTA, 4 x 4 per thread
 constexpr int kDwK = 32;        // entries of the contraction staged per step
 
-// Contraction splits of the dW partial products: enough CTAs for about two per
-// SM of a 152-SM part, each split at least 512 entries long.
+// Contraction splits of the dW partial products: about one wave of CTAs at
+// four per SM of a 152-SM part, each split at least 256 entries long.
 int64_t dw_splits(const Problem& p) {
   const int64_t tiles = (p.M + kDwTile - 1) / kDwTile;
   const int64_t ctas = tiles * tiles * p.BH();
   const int64_t E = p.d * (p.d + 1);
-  const int64_t want = (304 + ctas - 1) / ctas;
-  return std::max<int64_t>(1, std::min<int64_t>(want, std::max<int64_t>(1, E / 512)));
+  const int64_t want = 608 / ctas;
+  return std::max<int64_t>(1, std::min<int64_t>(want, std::max<int64_t>(1, E / 256)));
 }
 
 // part[bh][ks][i][j] = sum over e in split ks of dSzt[bh][i][e] * Sz[bh][j][e]
 // (z index = bh * KS + ks; the KS splits of the contraction cut E into equal
-// column ranges so that a small M still spreads over many CTAs)
+// column ranges so that a small M still spreads over many CTAs).  The 32-entry
+// slabs of both operands are double-buffered: cp.async fills the next slab
+// while the current one is multiplied.
 __global__ void __launch_bounds__(256)
 simt_dw_partial(const float* __restrict__ dSzt, const float* __restrict__ Sz, float* __restrict__ part, int64_t M,
                 int64_t E, int32_t KS) {
-  __shared__ float sa[kDwK][kDwTile + 4];
-  __shared__ float sb[kDwK][kDwTile + 4];
+  __shared__ __align__(16) float sa[2][kDwK][kDwTile + 4];
+  __shared__ __align__(16) float sb[2][kDwK][kDwTile + 4];
   const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kDwTile, j0 = static_cast<int64_t>(blockIdx.y) * kDwTile;
   const int64_t bh = blockIdx.z / KS, ks = blockIdx.z % KS;
   const int64_t e_lo = E * ks / KS, e_hi = E * (ks + 1) / KS;
   const float* A = dSzt + bh * M * E;
   const float* Bm = Sz + bh * M * E;
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float acc[4][4] = {};
-  for (int64_t e0 = e_lo; e0 < e_hi; e0 += kDwK) {
+  auto stage = [&](int buf, int64_t e0) {
     for (int x = threadIdx.x; x < kDwK * kDwTile; x += 256) {
       const int row = x / kDwK, kk = x % kDwK;
       const int64_t e = e0 + kk;
-      sa[kk][row] = (i0 + row < M && e < e_hi) ? A[(i0 + row) * E + e] : 0.0f;
-      sb[kk][row] = (j0 + row < M && e < e_hi) ? Bm[(j0 + row) * E + e] : 0.0f;
+      const bool ina = i0 + row < M && e < e_hi, inb = j0 + row < M && e < e_hi;
+      cp_async_f32(&sa[buf][kk][row], ina ? A + (i0 + row) * E + e : A, ina);
+      cp_async_f32(&sb[buf][kk][row], inb ? Bm + (j0 + row) * E + e : Bm, inb);
+    }
+    cp_async_commit();
+  };
+  float acc[4][4] = {};
+  if (e_lo < e_hi) stage(0, e_lo);
+  int buf = 0;
+  for (int64_t e0 = e_lo; e0 < e_hi; e0 += kDwK, buf ^= 1) {
+    if (e0 + kDwK < e_hi) {
+      stage(buf ^ 1, e0 + kDwK);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
 #pragma unroll 8
     for (int kk = 0; kk < kDwK; ++kk) {
-      float a[4], bb[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        a[u] = sa[kk][ty * 4 + u];
-        bb[u] = sb[kk][tx * 4 + u];
-      }
+      const float4 a4 = *reinterpret_cast<const float4*>(&sa[buf][kk][ty * 4]);
+      const float4 b4 = *reinterpret_cast<const float4*>(&sb[buf][kk][tx * 4]);
+      const float a[4] = {a4.x, a4.y, a4.z, a4.w}, bb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
       for (int u = 0; u < 4; ++u)
 #pragma unroll
         for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(a[u], bb[w], acc[u][w]);
     }
-    __syncthreads();
+    __syncthreads();   // the next iteration refills this buffer's partner, then this one
   }
 #pragma unroll
   for (int u = 0; u < 4; ++u)
@@ -602,14 +653,27 @@ simt_dw_partial(const float* __restrict__ dSzt, const float* __restrict__ Sz, fl
     }
 }
 
+constexpr int kDwrWarps = 8;
+
 // dW = sum over (b, h) and the contraction splits of the partials (NP = BH *
-// KS of them), in a fixed order (deterministic).
-__global__ void simt_dw_reduce(const float* __restrict__ part, float* __restrict__ dW, int64_t MM, int64_t NP) {
-  const int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (x >= MM) return;
+// KS of them), in a fixed order (deterministic): a CTA owns 32 consecutive
+// outputs, warp w sums partials w, w + 8, ... of output x0 + lane, then the
+// eight warp sums are added in warp order.
+__global__ void __launch_bounds__(kDwrWarps * 32)
+simt_dw_reduce(const float* __restrict__ part, float* __restrict__ dW, int64_t MM, int64_t NP) {
+  __shared__ float red[kDwrWarps][32];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   float s = 0.0f;
-  for (int64_t n = 0; n < NP; ++n) s += part[n * MM + x];
-  dW[x] = s;
+  if (x < MM)
+    for (int64_t n = warp; n < NP; n += kDwrWarps) s += part[n * MM + x];
+  red[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && x < MM) {
+    float r = 0.0f;
+    for (int w = 0; w < kDwrWarps; ++w) r += red[w][lane];
+    dW[x] = r;
+  }
 }
 
 // ============================================================================
@@ -641,6 +705,7 @@ __global__ void simt_dw_reduce(const float* __restrict__ part, float* __restrict
 constexpr int kCbThreads = 256;
 constexpr int kCbWarps = kCbThreads / 32;
 constexpr int kCbChunk = 32;    // one chunk token per lane in the score steps
+constexpr int kCbRowLanes = kCbThreads / kCbChunk;   // threads staging one token row
 
 // ENT = ceil(d*d / 256) state entries per thread (P_t and dS<_i in registers);
 // DB = ceil(d / 16) columns per thread in the token x column phases.
@@ -705,16 +770,21 @@ simt_causal_bwd_query(const T* __restrict__ q, Operand qo, const T* __restrict__
   constexpr int TB = ENT == 1 ? 1 : ENT == 4 ? 2 : ENT == 16 ? 4 : 8;
   static_assert(TB * TB == ENT, "ENT is a square");
   const int r0 = TB * (tid / 16), c0 = TB * (tid % 16);
+  // staging: one token row per kCbRowLanes threads; the blocks are contiguous
+  // token ranges, so slot s of the block is token nb + s
+  const int srow = tid / kCbRowLanes, spart = tid % kCbRowLanes;
+  const int64_t nb = token_of(g, i, 0);
   for (int64_t s0 = 0; s0 < g.w; s0 += kCbChunk) {
     const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
     __syncthreads();   // the state is complete and the previous chunk's rows are free
-    for (int e = tid; e < cnt * d; e += kCbThreads) {
-      const int sl = e / d, c = e % d;
-      const int64_t n = token_of(g, i, s0 + sl);
-      sq[sl * P + c] = phi_f(load_f(qb + n * qo.sn + c), phi_kind, eps);
-      sk[sl * P + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
-      sv[sl * P + c] = load_f(vb + n * vo.sn + c);
-      sg[sl * P + c] = load_f(gb + n * go.sn + c);
+    if (srow < cnt) {
+      const int64_t n = nb + s0 + srow;
+      for (int c = spart; c < d; c += kCbRowLanes) {
+        sq[srow * P + c] = phi_f(load_f(qb + n * qo.sn + c), phi_kind, eps);
+        sk[srow * P + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
+        sv[srow * P + c] = load_f(vb + n * vo.sn + c);
+        sg[srow * P + c] = load_f(gb + n * go.sn + c);
+      }
     }
     __syncthreads();
     // ---- 1: a_ts for every pair of the chunk, a 2 x 2 block per thread (rows
@@ -856,8 +926,8 @@ simt_causal_bwd_query(const T* __restrict__ q, Operand qo, const T* __restrict__
         }
       }
       const float dd0 = sdd[t0], dd1 = sdd[t1];
-      const int64_t n0t = t0 < cnt ? token_of(g, i, s0 + t0) : 0;
-      const int64_t n1t = t1 < cnt ? token_of(g, i, s0 + t1) : 0;
+      const int64_t n0t = t0 < cnt ? nb + s0 + t0 : 0;
+      const int64_t n1t = t1 < cnt ? nb + s0 + t1 : 0;
 #pragma unroll
       for (int j = 0; j < DB; ++j) {
         const int r = cc + 16 * j;
@@ -982,18 +1052,21 @@ simt_causal_bwd_key(const T* __restrict__ q, Operand qo, const T* __restrict__ k
   const int s0t = 2 * tt, s1t = s0t + 1;
   const int pi = tid / 16, pj = tid % 16;          // pair tiles: sources 2 pi (+1), queries 2 pj (+1)
   const int r0 = TB * (tid / 16), c0 = TB * (tid % 16);   // state tile
+  const int srow = tid / kCbRowLanes, spart = tid % kCbRowLanes;   // staging, as in the query kernel
+  const int64_t nb = token_of(g, j, 0);
   const int64_t nch = (g.w + kCbChunk - 1) / kCbChunk;
   for (int64_t ci = nch - 1; ci >= 0; --ci) {
     const int64_t s0 = ci * kCbChunk;
     const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
     __syncthreads();   // the suffix state is complete and the later chunk's rows are free
-    for (int e = tid; e < cnt * d; e += kCbThreads) {
-      const int sl = e / d, c = e % d;
-      const int64_t n = token_of(g, j, s0 + sl);
-      sq[sl * P + c] = phi_f(load_f(qb + n * qo.sn + c), phi_kind, eps);
-      sdn[sl * P + c] = dnb[(s0 + sl) * P + c];
-      sk[sl * P + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
-      sv[sl * P + c] = load_f(vb + n * vo.sn + c);
+    if (srow < cnt) {
+      const int64_t n = nb + s0 + srow;
+      for (int c = spart; c < d; c += kCbRowLanes) {
+        sq[srow * P + c] = phi_f(load_f(qb + n * qo.sn + c), phi_kind, eps);
+        sdn[srow * P + c] = dnb[(s0 + srow) * P + c];
+        sk[srow * P + c] = phi_f(load_f(kb + n * ko.sn + c), phi_kind, eps);
+        sv[srow * P + c] = load_f(vb + n * vo.sn + c);
+      }
     }
     for (int sl = tid; sl < cnt; sl += kCbThreads) sdd[sl] = dnb[(s0 + sl) * P + d];
     __syncthreads();
@@ -1062,8 +1135,8 @@ simt_causal_bwd_key(const T* __restrict__ q, Operand qo, const T* __restrict__ k
           ok1[jj] = fmaf(b1, qv, ok1[jj]);
         }
       }
-      const int64_t n0t = s0t < cnt ? token_of(g, j, s0 + s0t) : 0;
-      const int64_t n1t = s1t < cnt ? token_of(g, j, s0 + s1t) : 0;
+      const int64_t n0t = s0t < cnt ? nb + s0 + s0t : 0;
+      const int64_t n1t = s1t < cnt ? nb + s0 + s1t : 0;
 #pragma unroll
       for (int jj = 0; jj < DB; ++jj) {
         const int c = cc + 16 * jj;
@@ -1115,19 +1188,27 @@ simt_causal_bwd_key(const T* __restrict__ q, Operand qo, const T* __restrict__ k
 }
 
 // Causal dW: the partials below the diagonal, the query kernel's W_ii shares
-// on it, zero above it; summed over (b, h) in a fixed order.
-__global__ void simt_dw_reduce_causal(const float* __restrict__ part, const float* __restrict__ diag,
-                                      float* __restrict__ dW, int64_t M, int64_t BH, int64_t KS) {
-  const int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+// on it, zero above it; summed in a fixed order, laid out as simt_dw_reduce.
+__global__ void __launch_bounds__(kDwrWarps * 32)
+simt_dw_reduce_causal(const float* __restrict__ part, const float* __restrict__ diag, float* __restrict__ dW,
+                      int64_t M, int64_t BH, int64_t KS) {
+  __shared__ float red[kDwrWarps][32];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t MM = M * M;
-  if (x >= MM) return;
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   const int64_t i = x / M, j = x % M;
   float s = 0.0f;
-  if (j < i)
-    for (int64_t n = 0; n < BH * KS; ++n) s += part[n * MM + x];
-  else if (j == i)
-    for (int64_t bh = 0; bh < BH; ++bh) s += diag[bh * M + i];
-  dW[x] = s;
+  if (x < MM && j < i)
+    for (int64_t n = warp; n < BH * KS; n += kDwrWarps) s += part[n * MM + x];
+  else if (x < MM && j == i)
+    for (int64_t bh = warp; bh < BH; bh += kDwrWarps) s += diag[bh * M + i];
+  red[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && x < MM) {
+    float r = 0.0f;
+    for (int w = 0; w < kDwrWarps; ++w) r += red[w][lane];
+    dW[x] = r;
+  }
 }
 
 template <typename T>
@@ -1209,7 +1290,8 @@ int launch_simt_bwd_typed(const Problem& p, const float* W, const BwdOperands& b
     simt_dw_partial<<<grid, 256, 0, stream>>>(ws.dSzt, ws.Sz, ws.part, p.M, E, static_cast<int32_t>(KS));
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
     const int64_t MM = p.M * p.M;
-    simt_dw_reduce<<<static_cast<unsigned>((MM + 255) / 256), 256, 0, stream>>>(ws.part, bo.dW, MM, BH * KS);
+    simt_dw_reduce<<<static_cast<unsigned>((MM + 31) / 32), kDwrWarps * 32, 0, stream>>>(ws.part, bo.dW, MM,
+                                                                                         BH * KS);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
   // dS = W^T dS~ into the S~ buffer
@@ -1333,8 +1415,8 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
     simt_dw_partial<<<grid, 256, 0, stream>>>(ws.dSp, ws.Sz, ws.part, p.M, E, static_cast<int32_t>(KS));
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
     const int64_t MM = p.M * p.M;
-    simt_dw_reduce_causal<<<static_cast<unsigned>((MM + 255) / 256), 256, 0, stream>>>(ws.part, ws.diag, bo.dW,
-                                                                                       p.M, BH, KS);
+    simt_dw_reduce_causal<<<static_cast<unsigned>((MM + 31) / 32), kDwrWarps * 32, 0, stream>>>(
+        ws.part, ws.diag, bo.dW, p.M, BH, KS);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
   if (const int rc = launch_mix<true, true>(W, ws.dSp, ws.Sp, p.M, E, BH, stream); rc != MHLA_OK)
