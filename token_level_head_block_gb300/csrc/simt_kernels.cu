@@ -1187,6 +1187,630 @@ simt_causal_bwd_key(const T* __restrict__ q, Operand qo, const T* __restrict__ k
   }
 }
 
+// Vector loads and stores of V consecutive floats (V = 1, 2 or 4; the address
+// aligned to V floats).
+template <int V>
+__device__ __forceinline__ void ldv(const float* p, float (&x)[V]) {
+  if constexpr (V == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(p);
+    x[0] = t.x, x[1] = t.y, x[2] = t.z, x[3] = t.w;
+  } else if constexpr (V == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(p);
+    x[0] = t.x, x[1] = t.y;
+  } else {
+    x[0] = *p;
+  }
+}
+template <int V>
+__device__ __forceinline__ void stv(float* p, const float (&x)[V]) {
+  if constexpr (V == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  } else if constexpr (V == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+  } else {
+    *p = x[0];
+  }
+}
+
+// The same arithmetic as simt_causal_bwd_query for d = D in {32, 64}, laid out
+// for 16-byte shared-memory vectors: token and state rows padded to D + 4
+// floats, the state C kept row-major and transposed (C^T feeds dq), token-pair
+// tiles {p, p + 16} x {q, q + 16} (so one warp's vector reads fall in distinct
+// banks), V = D / 16 columns per thread in the token x column phases, and V x V
+// state entries per thread.  Chunk rows past the block's end are zero, so
+// every loop runs the full 32 tokens.  Per chunk the thread first sums
+// X = sum_t phi(q_t) dnum_t^T over its entries, then adds X to dS<_i and
+// <P, X> to dW_ii.
+template <typename T, int D>
+__global__ void __launch_bounds__(kCbThreads, 2)
+simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict__ k, Operand ko,
+                        const T* __restrict__ v, Operand vo, const T* __restrict__ g_out, Operand go,
+                        T* __restrict__ dq, Operand dqo, TokenGeom g, int64_t H, int phi_kind, float eps,
+                        const float* __restrict__ W, const float* __restrict__ Sp, float* __restrict__ dSp,
+                        float* __restrict__ diag, float* __restrict__ dn) {
+  constexpr int V = D / 16;
+  constexpr int P = D + 4;                 // padded token / state row
+  constexpr int CP = kCbChunk + 4;         // padded row of a 32 x 32 token-pair matrix
+  constexpr int E = D * D, PD = D + 1;     // PD: the dnum / dden scratch row
+  extern __shared__ __align__(16) float cbq_sm[];
+  float* st = cbq_sm;                      // [D][P] C = S<_i + W_ii P before the chunk
+  float* stT = st + D * P;                 // [D][P] C^T
+  float* zs = stT + D * P;                 // [D]    c = z<_i + W_ii y before the chunk
+  float* sq = zs + D;                      // [chunk][P] phi(q_t)
+  float* sk = sq + kCbChunk * P;           // [chunk][P] phi(k_s)
+  float* sv = sk + kCbChunk * P;           // [chunk][P] v_s
+  float* sg = sv + kCbChunk * P;           // [chunk][P] g_t
+  float* sdn = sg + kCbChunk * P;          // [chunk][P] dnum_t
+  float* sdd = sdn + kCbChunk * P;         // [chunk]    dden_t
+  float* sden = sdd + kCbChunk;            // [chunk]    den_t
+  float* sa = sden + kCbChunk;             // [chunk][CP] a_ts (s <= t, else 0)
+  float* sb = sa + kCbChunk * CP;          // [chunk][CP] b_ts (s <= t, else 0)
+  float* red = sb + kCbChunk * CP;         // [warps]
+  const int64_t item = blockIdx.x;
+  const int64_t i = item % g.M, bh = item / g.M;
+  const int64_t b = bh / H, h = bh % H;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const float wii = __ldg(W + i * g.M + i);
+  const float* src = Sp + (bh * g.M + i) * static_cast<int64_t>(E + D);
+  for (int e = tid; e < E; e += kCbThreads) {
+    const int r = e / D, c = e % D;
+    const float x = src[e];
+    st[r * P + c] = x;
+    stT[c * P + r] = x;
+  }
+  for (int r = tid; r < D; r += kCbThreads) zs[r] = src[E + r];
+  const T* qb = q + b * qo.sb + h * qo.sh;
+  const T* kb = k + b * ko.sb + h * ko.sh;
+  const T* vb = v + b * vo.sb + h * vo.sh;
+  const T* gb = g_out + b * go.sb + h * go.sh;
+  T* dqb = dq + b * dqo.sb + h * dqo.sh;
+  float* dnb = dn + (bh * g.M + i) * g.w * PD;   // token rows: dnum_t (D), dden_t
+  float pr[V * V], acc[V * V];
+#pragma unroll
+  for (int m = 0; m < V * V; ++m) pr[m] = acc[m] = 0.0f;
+  float yr = 0.0f, zacc = 0.0f, dw = 0.0f;
+  const int tt = tid / 16, cc = tid % 16;
+  const int t0 = 2 * tt, t1 = t0 + 1;      // token x column tiles: tokens t0, t1; columns c0 ..
+  const int c0 = V * cc;
+  const int r0 = V * tt;                   // state tile: rows r0 .., columns c0 ..
+  const int pi = tid / 16, pj = tid % 16;  // token-pair tiles: rows pi, pi + 16; columns pj, pj + 16
+  const int srow = tid / kCbRowLanes, spart = tid % kCbRowLanes;
+  const int64_t nb = token_of(g, i, 0);    // contiguous blocks: slot s is token nb + s
+  for (int64_t s0 = 0; s0 < g.w; s0 += kCbChunk) {
+    const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
+    __syncthreads();   // the state is complete and the previous chunk's rows are free
+    {
+      const bool live = srow < cnt;
+      const int64_t n = nb + s0 + srow;
+#pragma unroll
+      for (int c = 4 * spart; c < D; c += 4 * kCbRowLanes) {
+        float xq[4], xk[4], xv[4], xg[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          xq[u] = live ? phi_f(load_f(qb + n * qo.sn + c + u), phi_kind, eps) : 0.0f;
+          xk[u] = live ? phi_f(load_f(kb + n * ko.sn + c + u), phi_kind, eps) : 0.0f;
+          xv[u] = live ? load_f(vb + n * vo.sn + c + u) : 0.0f;
+          xg[u] = live ? load_f(gb + n * go.sn + c + u) : 0.0f;
+        }
+        stv<4>(sq + srow * P + c, xq);
+        stv<4>(sk + srow * P + c, xk);
+        stv<4>(sv + srow * P + c, xv);
+        stv<4>(sg + srow * P + c, xg);
+      }
+    }
+    __syncthreads();
+    // ---- 1: a_ts (s <= t); the block (pi, pj + 16) lies above the diagonal
+    {
+      const int ra = pi, rb = pi + 16, ca = pj, cb = pj + 16;
+      float x00 = 0.0f, x10 = 0.0f, x11 = 0.0f;
+#pragma unroll 4
+      for (int r = 0; r < D; r += V) {
+        float qa[V], qc[V], ka[V], kc[V];
+        ldv<V>(sq + ra * P + r, qa);
+        ldv<V>(sq + rb * P + r, qc);
+        ldv<V>(sk + ca * P + r, ka);
+        ldv<V>(sk + cb * P + r, kc);
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          x00 = fmaf(qa[u], ka[u], x00);
+          x10 = fmaf(qc[u], ka[u], x10);
+          x11 = fmaf(qc[u], kc[u], x11);
+        }
+      }
+      sa[ra * CP + ca] = (ra < cnt && ca <= ra) ? x00 : 0.0f;
+      sa[ra * CP + cb] = 0.0f;
+      sa[rb * CP + ca] = rb < cnt ? x10 : 0.0f;
+      sa[rb * CP + cb] = (rb < cnt && cb <= rb) ? x11 : 0.0f;
+    }
+    __syncthreads();
+    // ---- 2: den_t, eight threads per token, then a fixed-order shuffle sum
+    {
+      const int tok = tid / 8, part = tid % 8;
+      float den = 0.0f;
+#pragma unroll
+      for (int r = V * part; r < D; r += 8 * V) {
+        float qv[V], zv[V];
+        ldv<V>(sq + tok * P + r, qv);
+        ldv<V>(zs + r, zv);
+#pragma unroll
+        for (int u = 0; u < V; ++u) den = fmaf(qv[u], zv[u], den);
+      }
+      float av[4];
+      ldv<4>(sa + tok * CP + 4 * part, av);
+      float own = ((av[0] + av[1]) + av[2]) + av[3];
+#pragma unroll
+      for (int off = 4; off > 0; off >>= 1) {
+        den += __shfl_xor_sync(0xffffffffu, den, off);
+        own += __shfl_xor_sync(0xffffffffu, own, off);
+      }
+      if (part == 0) sden[tok] = fmaf(wii, own, den) + eps;
+    }
+    __syncthreads();
+    // ---- 3: num, dnum, dden (tokens t0, t1; columns c0 ..)
+    {
+      float n0[V], n1[V], o0[V], o1[V];
+#pragma unroll
+      for (int w = 0; w < V; ++w) n0[w] = n1[w] = o0[w] = o1[w] = 0.0f;
+#pragma unroll 2
+      for (int r = 0; r < D; r += V) {
+        float qa[V], qc[V];
+        ldv<V>(sq + t0 * P + r, qa);
+        ldv<V>(sq + t1 * P + r, qc);
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          float cv[V];
+          ldv<V>(st + (r + u) * P + c0, cv);
+#pragma unroll
+          for (int w = 0; w < V; ++w) {
+            n0[w] = fmaf(qa[u], cv[w], n0[w]);
+            n1[w] = fmaf(qc[u], cv[w], n1[w]);
+          }
+        }
+      }
+#pragma unroll 2
+      for (int s = 0; s < kCbChunk; s += V) {
+        float pa[V], pc[V];
+        ldv<V>(sa + t0 * CP + s, pa);
+        ldv<V>(sa + t1 * CP + s, pc);
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          float vv[V];
+          ldv<V>(sv + (s + u) * P + c0, vv);
+#pragma unroll
+          for (int w = 0; w < V; ++w) {
+            o0[w] = fmaf(pa[u], vv[w], o0[w]);
+            o1[w] = fmaf(pc[u], vv[w], o1[w]);
+          }
+        }
+      }
+      const float den0 = sden[t0], den1 = sden[t1];
+      float g0[V], g1[V], d0[V], d1[V];
+      ldv<V>(sg + t0 * P + c0, g0);
+      ldv<V>(sg + t1 * P + c0, g1);
+      float go0 = 0.0f, go1 = 0.0f;
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        go0 = fmaf(g0[w], fmaf(wii, o0[w], n0[w]), go0);
+        go1 = fmaf(g1[w], fmaf(wii, o1[w], n1[w]), go1);
+        d0[w] = t0 < cnt ? g0[w] / den0 : 0.0f;   // rows past the block stay zero
+        d1[w] = t1 < cnt ? g1[w] / den1 : 0.0f;
+      }
+      stv<V>(sdn + t0 * P + c0, d0);
+      stv<V>(sdn + t1 * P + c0, d1);
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        if (t0 < cnt) dnb[(s0 + t0) * PD + c0 + w] = d0[w];
+        if (t1 < cnt) dnb[(s0 + t1) * PD + c0 + w] = d1[w];
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) {   // the 16 lanes of this half-warp share t0, t1
+        go0 += __shfl_xor_sync(0xffffffffu, go0, off);
+        go1 += __shfl_xor_sync(0xffffffffu, go1, off);
+      }
+      if (cc == 0) {
+        const float dd0 = t0 < cnt ? -(go0 / den0) / den0 : 0.0f;
+        const float dd1 = t1 < cnt ? -(go1 / den1) / den1 : 0.0f;
+        sdd[t0] = dd0;
+        sdd[t1] = dd1;
+        if (t0 < cnt) dnb[(s0 + t0) * PD + D] = dd0;
+        if (t1 < cnt) dnb[(s0 + t1) * PD + D] = dd1;
+      }
+    }
+    __syncthreads();
+    // ---- 4: b_ts = v_s . dnum_t + dden_t (s <= t), dW_ii's own-chunk part
+    {
+      const int ra = pi, rb = pi + 16, ca = pj, cb = pj + 16;
+      float x00 = 0.0f, x10 = 0.0f, x11 = 0.0f;
+#pragma unroll 4
+      for (int c = 0; c < D; c += V) {
+        float na[V], nc[V], va[V], vc[V];
+        ldv<V>(sdn + ra * P + c, na);
+        ldv<V>(sdn + rb * P + c, nc);
+        ldv<V>(sv + ca * P + c, va);
+        ldv<V>(sv + cb * P + c, vc);
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          x00 = fmaf(na[u], va[u], x00);
+          x10 = fmaf(nc[u], va[u], x10);
+          x11 = fmaf(nc[u], vc[u], x11);
+        }
+      }
+      const float da = sdd[ra], dc = sdd[rb];
+      const float b00 = (ra < cnt && ca <= ra) ? x00 + da : 0.0f;
+      const float b10 = rb < cnt ? x10 + dc : 0.0f;
+      const float b11 = (rb < cnt && cb <= rb) ? x11 + dc : 0.0f;
+      sb[ra * CP + ca] = b00;
+      sb[ra * CP + cb] = 0.0f;
+      sb[rb * CP + ca] = b10;
+      sb[rb * CP + cb] = b11;
+      dw = fmaf(sa[ra * CP + ca], b00, dw);   // a is zero wherever b is (the same mask)
+      dw = fmaf(sa[rb * CP + ca], b10, dw);
+      dw = fmaf(sa[rb * CP + cb], b11, dw);
+    }
+    __syncthreads();
+    // ---- 5: dq (tokens t0, t1; rows c0 ..), C dnum_t from the transposed state
+    {
+      float x0[V], x1[V], w0[V], w1[V];
+#pragma unroll
+      for (int w = 0; w < V; ++w) x0[w] = x1[w] = w0[w] = w1[w] = 0.0f;
+#pragma unroll 2
+      for (int c = 0; c < D; c += V) {
+        float na[V], nc[V];
+        ldv<V>(sdn + t0 * P + c, na);
+        ldv<V>(sdn + t1 * P + c, nc);
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          float cv[V];
+          ldv<V>(stT + (c + u) * P + c0, cv);   // C[c0 + w][c + u]
+#pragma unroll
+          for (int w = 0; w < V; ++w) {
+            x0[w] = fmaf(cv[w], na[u], x0[w]);
+            x1[w] = fmaf(cv[w], nc[u], x1[w]);
+          }
+        }
+      }
+#pragma unroll 2
+      for (int s = 0; s < kCbChunk; s += V) {
+        float ba[V], bc[V];
+        ldv<V>(sb + t0 * CP + s, ba);
+        ldv<V>(sb + t1 * CP + s, bc);
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          float kv[V];
+          ldv<V>(sk + (s + u) * P + c0, kv);
+#pragma unroll
+          for (int w = 0; w < V; ++w) {
+            w0[w] = fmaf(kv[w], ba[u], w0[w]);
+            w1[w] = fmaf(kv[w], bc[u], w1[w]);
+          }
+        }
+      }
+      const float dd0 = sdd[t0], dd1 = sdd[t1];
+      const int64_t n0t = nb + s0 + t0, n1t = nb + s0 + t1;
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        const int r = c0 + w;
+        const float zr = zs[r];
+        if (t0 < cnt) {
+          const float x = fmaf(wii, w0[w], fmaf(dd0, zr, x0[w]));
+          store_f(dqb + n0t * dqo.sn + r, load_f(qb + n0t * qo.sn + r) > 0.0f ? x : 0.0f);
+        }
+        if (t1 < cnt) {
+          const float x = fmaf(wii, w1[w], fmaf(dd1, zr, x1[w]));
+          store_f(dqb + n1t * dqo.sn + r, load_f(qb + n1t * qo.sn + r) > 0.0f ? x : 0.0f);
+        }
+      }
+    }
+    __syncthreads();   // phase 6 rewrites the state phase 5 has read
+    // ---- 6: X = sum_t phi(q_t) dnum_t^T and the chunk's phi(k_s) v_s^T over this
+    // thread's V x V entries; then dS<_i += X, dW_ii += <P, X>, P and the state advance
+    {
+      float X[V * V], dps[V * V];
+#pragma unroll
+      for (int m = 0; m < V * V; ++m) X[m] = dps[m] = 0.0f;
+#pragma unroll 4
+      for (int sl = 0; sl < kCbChunk; ++sl) {
+        float qr[V], kr[V], nc[V], vc[V];
+        ldv<V>(sq + sl * P + r0, qr);
+        ldv<V>(sk + sl * P + r0, kr);
+        ldv<V>(sdn + sl * P + c0, nc);
+        ldv<V>(sv + sl * P + c0, vc);
+#pragma unroll
+        for (int u = 0; u < V; ++u)
+#pragma unroll
+          for (int w = 0; w < V; ++w) {
+            X[u * V + w] = fmaf(qr[u], nc[w], X[u * V + w]);
+            dps[u * V + w] = fmaf(kr[u], vc[w], dps[u * V + w]);
+          }
+      }
+#pragma unroll
+      for (int m = 0; m < V * V; ++m) {
+        dw = fmaf(pr[m], X[m], dw);
+        acc[m] += X[m];
+        pr[m] += dps[m];
+      }
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        float cur[V];
+        ldv<V>(st + (r0 + u) * P + c0, cur);
+#pragma unroll
+        for (int w = 0; w < V; ++w) cur[w] = fmaf(wii, dps[u * V + w], cur[w]);
+        stv<V>(st + (r0 + u) * P + c0, cur);
+      }
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        float cur[V];
+        ldv<V>(stT + (c0 + w) * P + r0, cur);
+#pragma unroll
+        for (int u = 0; u < V; ++u) cur[u] = fmaf(wii, dps[u * V + w], cur[u]);
+        stv<V>(stT + (c0 + w) * P + r0, cur);
+      }
+    }
+    if (tid < D) {
+      float x = 0.0f, dy = 0.0f;
+      for (int sl = 0; sl < kCbChunk; ++sl) {
+        x = fmaf(sq[sl * P + tid], sdd[sl], x);
+        dy += sk[sl * P + tid];
+      }
+      dw = fmaf(yr, x, dw);
+      zacc += x;
+      yr += dy;
+      zs[tid] = fmaf(wii, dy, zs[tid]);
+    }
+  }
+  float* out = dSp + (bh * g.M + i) * static_cast<int64_t>(E + D);
+#pragma unroll
+  for (int u = 0; u < V; ++u) {
+    float row[V];
+#pragma unroll
+    for (int w = 0; w < V; ++w) row[w] = acc[u * V + w];
+    stv<V>(out + (r0 + u) * D + c0, row);
+  }
+  if (tid < D) out[E + tid] = zacc;
+  dw = warp_sum(dw);
+  if (lane == 0) red[warp] = dw;
+  __syncthreads();
+  if (tid == 0) {
+    float s = 0.0f;
+    for (int w = 0; w < kCbWarps; ++w) s += red[w];
+    diag[bh * g.M + i] = s;
+  }
+}
+
+// The same arithmetic as simt_causal_bwd_key for d = D in {32, 64}, laid out as
+// simt_causal_bwd_query_v: padded rows, 16-byte vectors, G kept row-major and
+// transposed (G feeds dv, G^T feeds dk), token-pair tiles {p, p + 16} x
+// {q, q + 16}, zero rows past the block's end.
+template <typename T, int D>
+__global__ void __launch_bounds__(kCbThreads, 2)
+simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__ k, Operand ko,
+                      const T* __restrict__ v, Operand vo, T* __restrict__ dk, Operand dko, T* __restrict__ dv,
+                      Operand dvo, TokenGeom g, int64_t H, int phi_kind, float eps, const float* __restrict__ W,
+                      const float* __restrict__ dS, const float* __restrict__ dn) {
+  constexpr int V = D / 16;
+  constexpr int P = D + 4;
+  constexpr int CP = kCbChunk + 4;
+  constexpr int E = D * D, PD = D + 1;
+  extern __shared__ __align__(16) float cbk_sm[];
+  float* gs = cbk_sm;                      // [D][P] G
+  float* gsT = gs + D * P;                 // [D][P] G^T
+  float* gz = gsT + D * P;                 // [D]    gz
+  float* sq = gz + D;                      // [chunk][P] phi(q_t)
+  float* sdn = sq + kCbChunk * P;          // [chunk][P] dnum_t
+  float* sk = sdn + kCbChunk * P;          // [chunk][P] phi(k_s)
+  float* sv = sk + kCbChunk * P;           // [chunk][P] v_s
+  float* sdd = sv + kCbChunk * P;          // [chunk]    dden_t
+  float* sa = sdd + kCbChunk;              // [chunk][CP] a_st (t >= s, else 0)
+  float* sb = sa + kCbChunk * CP;          // [chunk][CP] b_st (t >= s, else 0)
+  const int64_t item = blockIdx.x;
+  const int64_t j = item % g.M, bh = item / g.M;
+  const int64_t b = bh / H, h = bh % H;
+  const int tid = threadIdx.x;
+  const float wjj = __ldg(W + j * g.M + j);
+  const float* src = dS + (bh * g.M + j) * static_cast<int64_t>(E + D);
+  for (int e = tid; e < E; e += kCbThreads) {
+    const int r = e / D, c = e % D;
+    const float x = src[e];
+    gs[r * P + c] = x;
+    gsT[c * P + r] = x;
+  }
+  for (int r = tid; r < D; r += kCbThreads) gz[r] = src[E + r];
+  const T* qb = q + b * qo.sb + h * qo.sh;
+  const T* kb = k + b * ko.sb + h * ko.sh;
+  const T* vb = v + b * vo.sb + h * vo.sh;
+  T* dkb = dk + b * dko.sb + h * dko.sh;
+  T* dvb = dv + b * dvo.sb + h * dvo.sh;
+  const float* dnb = dn + (bh * g.M + j) * g.w * PD;
+  const int tt = tid / 16, cc = tid % 16;
+  const int s0t = 2 * tt, s1t = s0t + 1;   // sources s0t, s1t; columns c0 ..
+  const int c0 = V * cc;
+  const int r0 = V * tt;                   // state tile: rows r0 .., columns c0 ..
+  const int pi = tid / 16, pj = tid % 16;  // pair tiles: sources pi, pi + 16; queries pj, pj + 16
+  const int srow = tid / kCbRowLanes, spart = tid % kCbRowLanes;
+  const int64_t nb = token_of(g, j, 0);
+  const int64_t nch = (g.w + kCbChunk - 1) / kCbChunk;
+  for (int64_t ci = nch - 1; ci >= 0; --ci) {
+    const int64_t s0 = ci * kCbChunk;
+    const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
+    __syncthreads();   // the suffix state is complete and the later chunk's rows are free
+    {
+      const bool live = srow < cnt;
+      const int64_t n = nb + s0 + srow;
+#pragma unroll
+      for (int c = 4 * spart; c < D; c += 4 * kCbRowLanes) {
+        float xq[4], xn[4], xk[4], xv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          xq[u] = live ? phi_f(load_f(qb + n * qo.sn + c + u), phi_kind, eps) : 0.0f;
+          xn[u] = live ? dnb[(s0 + srow) * PD + c + u] : 0.0f;
+          xk[u] = live ? phi_f(load_f(kb + n * ko.sn + c + u), phi_kind, eps) : 0.0f;
+          xv[u] = live ? load_f(vb + n * vo.sn + c + u) : 0.0f;
+        }
+        stv<4>(sq + srow * P + c, xq);
+        stv<4>(sdn + srow * P + c, xn);
+        stv<4>(sk + srow * P + c, xk);
+        stv<4>(sv + srow * P + c, xv);
+      }
+    }
+    if (tid < kCbChunk) sdd[tid] = tid < cnt ? dnb[(s0 + tid) * PD + D] : 0.0f;
+    __syncthreads();
+    // ---- 1: a_st and b_st (t >= s); the block (pi + 16, pj) lies below the diagonal
+    {
+      const int ra = pi, rb = pi + 16, ca = pj, cb = pj + 16;
+      float a00 = 0.0f, a01 = 0.0f, a11 = 0.0f, b00 = 0.0f, b01 = 0.0f, b11 = 0.0f;
+#pragma unroll 2
+      for (int r = 0; r < D; r += V) {
+        float ka[V], kc[V], qa[V], qc[V], va[V], vc[V], na[V], nc[V];
+        ldv<V>(sk + ra * P + r, ka);
+        ldv<V>(sk + rb * P + r, kc);
+        ldv<V>(sq + ca * P + r, qa);
+        ldv<V>(sq + cb * P + r, qc);
+        ldv<V>(sv + ra * P + r, va);
+        ldv<V>(sv + rb * P + r, vc);
+        ldv<V>(sdn + ca * P + r, na);
+        ldv<V>(sdn + cb * P + r, nc);
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          a00 = fmaf(ka[u], qa[u], a00);
+          a01 = fmaf(ka[u], qc[u], a01);
+          a11 = fmaf(kc[u], qc[u], a11);
+          b00 = fmaf(va[u], na[u], b00);
+          b01 = fmaf(va[u], nc[u], b01);
+          b11 = fmaf(vc[u], nc[u], b11);
+        }
+      }
+      const float dda = sdd[ca], ddc = sdd[cb];
+      const bool m00 = ca < cnt && ca >= ra, m01 = cb < cnt, m11 = cb < cnt && cb >= rb;
+      sa[ra * CP + ca] = m00 ? a00 : 0.0f;
+      sa[ra * CP + cb] = m01 ? a01 : 0.0f;
+      sa[rb * CP + ca] = 0.0f;
+      sa[rb * CP + cb] = m11 ? a11 : 0.0f;
+      sb[ra * CP + ca] = m00 ? b00 + dda : 0.0f;
+      sb[ra * CP + cb] = m01 ? b01 + ddc : 0.0f;
+      sb[rb * CP + ca] = 0.0f;
+      sb[rb * CP + cb] = m11 ? b11 + ddc : 0.0f;
+    }
+    __syncthreads();
+    // ---- 2: dv and dk of sources s0t, s1t (columns / rows c0 ..)
+    {
+      float v0[V], v1[V], w0[V], w1[V];
+#pragma unroll
+      for (int w = 0; w < V; ++w) v0[w] = v1[w] = w0[w] = w1[w] = 0.0f;
+#pragma unroll 2
+      for (int x = 0; x < D; x += V) {
+        float ka[V], kc[V], ea[V], ec[V];
+        ldv<V>(sk + s0t * P + x, ka);
+        ldv<V>(sk + s1t * P + x, kc);
+        ldv<V>(sv + s0t * P + x, ea);
+        ldv<V>(sv + s1t * P + x, ec);
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          float gcol[V], grow[V];
+          ldv<V>(gs + (x + u) * P + c0, gcol);    // G[x + u][c0 + w]
+          ldv<V>(gsT + (x + u) * P + c0, grow);   // G[c0 + w][x + u]
+#pragma unroll
+          for (int w = 0; w < V; ++w) {
+            v0[w] = fmaf(ka[u], gcol[w], v0[w]);
+            v1[w] = fmaf(kc[u], gcol[w], v1[w]);
+            w0[w] = fmaf(grow[w], ea[u], w0[w]);
+            w1[w] = fmaf(grow[w], ec[u], w1[w]);
+          }
+        }
+      }
+      float ov0[V], ov1[V], ok0[V], ok1[V];
+#pragma unroll
+      for (int w = 0; w < V; ++w) ov0[w] = ov1[w] = ok0[w] = ok1[w] = 0.0f;
+#pragma unroll 2
+      for (int t = 0; t < kCbChunk; t += V) {
+        float aa[V], ac[V], ba[V], bc[V];
+        ldv<V>(sa + s0t * CP + t, aa);
+        ldv<V>(sa + s1t * CP + t, ac);
+        ldv<V>(sb + s0t * CP + t, ba);
+        ldv<V>(sb + s1t * CP + t, bc);
+#pragma unroll
+        for (int u = 0; u < V; ++u) {
+          float nv[V], qv[V];
+          ldv<V>(sdn + (t + u) * P + c0, nv);
+          ldv<V>(sq + (t + u) * P + c0, qv);
+#pragma unroll
+          for (int w = 0; w < V; ++w) {
+            ov0[w] = fmaf(aa[u], nv[w], ov0[w]);
+            ov1[w] = fmaf(ac[u], nv[w], ov1[w]);
+            ok0[w] = fmaf(ba[u], qv[w], ok0[w]);
+            ok1[w] = fmaf(bc[u], qv[w], ok1[w]);
+          }
+        }
+      }
+      const int64_t n0t = nb + s0 + s0t, n1t = nb + s0 + s1t;
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        const int c = c0 + w;
+        const float zr = gz[c];
+        if (s0t < cnt) {
+          store_f(dvb + n0t * dvo.sn + c, fmaf(wjj, ov0[w], v0[w]));
+          const float x = fmaf(wjj, ok0[w], w0[w] + zr);
+          store_f(dkb + n0t * dko.sn + c, load_f(kb + n0t * ko.sn + c) > 0.0f ? x : 0.0f);
+        }
+        if (s1t < cnt) {
+          store_f(dvb + n1t * dvo.sn + c, fmaf(wjj, ov1[w], v1[w]));
+          const float x = fmaf(wjj, ok1[w], w1[w] + zr);
+          store_f(dkb + n1t * dko.sn + c, load_f(kb + n1t * ko.sn + c) > 0.0f ? x : 0.0f);
+        }
+      }
+    }
+    __syncthreads();   // phase 3 rewrites G, which phase 2 has read
+    // ---- 3: G += W_jj sum_t phi(q_t) dnum_t^T (V x V entries per thread), gz likewise
+    {
+      float X[V * V];
+#pragma unroll
+      for (int m = 0; m < V * V; ++m) X[m] = 0.0f;
+#pragma unroll 4
+      for (int t = 0; t < kCbChunk; ++t) {
+        float qr[V], nc[V];
+        ldv<V>(sq + t * P + r0, qr);
+        ldv<V>(sdn + t * P + c0, nc);
+#pragma unroll
+        for (int u = 0; u < V; ++u)
+#pragma unroll
+          for (int w = 0; w < V; ++w) X[u * V + w] = fmaf(qr[u], nc[w], X[u * V + w]);
+      }
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        float cur[V];
+        ldv<V>(gs + (r0 + u) * P + c0, cur);
+#pragma unroll
+        for (int w = 0; w < V; ++w) cur[w] = fmaf(wjj, X[u * V + w], cur[w]);
+        stv<V>(gs + (r0 + u) * P + c0, cur);
+      }
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        float cur[V];
+        ldv<V>(gsT + (c0 + w) * P + r0, cur);
+#pragma unroll
+        for (int u = 0; u < V; ++u) cur[u] = fmaf(wjj, X[u * V + w], cur[u]);
+        stv<V>(gsT + (c0 + w) * P + r0, cur);
+      }
+    }
+    if (tid < D) {
+      float x = 0.0f;
+      for (int t = 0; t < kCbChunk; ++t) x = fmaf(sdd[t], sq[t * P + tid], x);
+      gz[tid] = fmaf(wjj, x, gz[tid]);
+    }
+  }
+}
+
+// Shared memory of the vector-layout causal backward kernels, d = D.
+constexpr size_t cbv_query_smem(int D) {
+  return static_cast<size_t>(2 * D * (D + 4) + D + 5 * kCbChunk * (D + 4) + 2 * kCbChunk +
+                             2 * kCbChunk * (kCbChunk + 4) + kCbWarps) *
+         sizeof(float);
+}
+constexpr size_t cbv_key_smem(int D) {
+  return static_cast<size_t>(2 * D * (D + 4) + D + 4 * kCbChunk * (D + 4) + kCbChunk +
+                             2 * kCbChunk * (kCbChunk + 4)) *
+         sizeof(float);
+}
+
 // Causal dW: the partials below the diagonal, the query kernel's W_ii shares
 // on it, zero above it; summed in a fixed order, laid out as simt_dw_reduce.
 __global__ void __launch_bounds__(kDwrWarps * 32)
@@ -1400,7 +2024,20 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
           ws.diag, ws.dn);
       return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
     };
-    const int rc = d <= 16   ? launch(simt_causal_bwd_query<T, 1, 1>)
+    // d = 32, 64: the vector layout
+    auto launch_v = [&](auto kern, size_t vsmem) -> int {
+      if (vsmem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    static_cast<int>(vsmem)) != cudaSuccess)
+        return MHLA_ERR_CUDA;
+      KernelTimer timer("simt_causal_bwd_query", stream);
+      kern<<<static_cast<unsigned>(items), kCbThreads, vsmem, stream>>>(
+          qp, p.q, kp, p.k, vp, p.v, gp, bo.dout, dqp, bo.dq, g, p.H, p.phi_kind, p.eps, W, ws.Sp, ws.dSp,
+          ws.diag, ws.dn);
+      return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+    };
+    const int rc = d == 64   ? launch_v(simt_causal_bwd_query_v<T, 64>, cbv_query_smem(64))
+                   : d == 32 ? launch_v(simt_causal_bwd_query_v<T, 32>, cbv_query_smem(32))
+                   : d <= 16 ? launch(simt_causal_bwd_query<T, 1, 1>)
                    : d <= 32 ? launch(simt_causal_bwd_query<T, 4, 2>)
                    : d <= 64 ? launch(simt_causal_bwd_query<T, 16, 4>)
                              : launch(simt_causal_bwd_query<T, 64, 8>);
@@ -1433,7 +2070,18 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
           qp, p.q, kp, p.k, vp, p.v, dkp, bo.dk, dvp, bo.dv, g, p.H, d, p.phi_kind, p.eps, W, ws.Sp, ws.dn);
       return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
     };
-    return d <= 16   ? launch(simt_causal_bwd_key<T, 1, 1>)
+    auto launch_v = [&](auto kern, size_t vsmem) -> int {
+      if (vsmem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    static_cast<int>(vsmem)) != cudaSuccess)
+        return MHLA_ERR_CUDA;
+      KernelTimer timer("simt_causal_bwd_key", stream);
+      kern<<<static_cast<unsigned>(items), kCbThreads, vsmem, stream>>>(
+          qp, p.q, kp, p.k, vp, p.v, dkp, bo.dk, dvp, bo.dv, g, p.H, p.phi_kind, p.eps, W, ws.Sp, ws.dn);
+      return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+    };
+    return d == 64   ? launch_v(simt_causal_bwd_key_v<T, 64>, cbv_key_smem(64))
+           : d == 32 ? launch_v(simt_causal_bwd_key_v<T, 32>, cbv_key_smem(32))
+           : d <= 16 ? launch(simt_causal_bwd_key<T, 1, 1>)
            : d <= 32 ? launch(simt_causal_bwd_key<T, 2, 2>)
            : d <= 64 ? launch(simt_causal_bwd_key<T, 4, 4>)
                      : launch(simt_causal_bwd_key<T, 8, 8>);
