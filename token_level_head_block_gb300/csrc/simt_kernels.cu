@@ -1212,15 +1212,21 @@ __device__ __forceinline__ void stv(float* p, const float (&x)[V]) {
   }
 }
 
-// The same arithmetic as simt_causal_bwd_query for d = D in {32, 64}, laid out
-// for 16-byte shared-memory vectors: token and state rows padded to D + 4
-// floats, the state C kept row-major and transposed (C^T feeds dq), token-pair
-// tiles {p, p + 16} x {q, q + 16} (so one warp's vector reads fall in distinct
-// banks), V = D / 16 columns per thread in the token x column phases, and V x V
-// state entries per thread.  Chunk rows past the block's end are zero, so
-// every loop runs the full 32 tokens.  Per chunk the thread first sums
-// X = sum_t phi(q_t) dnum_t^T over its entries, then adds X to dS<_i and
-// <P, X> to dW_ii.
+// The causal backward's query side for d = D in {32, 64}, laid out for 16-byte
+// shared-memory vectors (token and state rows padded to D + 4 floats) and
+// rearranged so that one product of the state serves two terms: with
+// u_t = C g_t,
+//   C dnum_t = u_t / den_t   and   g_t . num_t = phi(q_t) . u_t + W_ii sum_s a_ts e_ts,
+// e_ts = g_t . v_s, so b_ts = e_ts / den_t + dden_t needs no second pass over the
+// columns.  Only C^T is kept (u reads it by rows).  Per 32-token chunk:
+//   1  a_ts = phi(q_t) . phi(k_s) and e_ts (s <= t), pair tiles {p, p + 16} x {q, q + 16}
+//   2  per token, over the 16 lanes of a half-warp (V = D / 16 columns each):
+//      u_t, den_t, g_t . num_t, dnum_t, dden_t, b_ts, dW_ii's own-chunk part
+//   3  dq_t = u_t / den_t + dden_t c + W_ii sum_s b_ts phi(k_s), masked by [q_t > 0]
+//   4  X = sum_t phi(q_t) dnum_t^T over V x V entries per thread: dS<_i += X,
+//      dW_ii += <P, X>; then (unless the block ends here) P and C^T advance by
+//      the chunk's phi(k_s) v_s^T
+// Chunk rows past the block's end are zero, so every loop runs the full 32 tokens.
 template <typename T, int D>
 __global__ void __launch_bounds__(kCbThreads, 2)
 simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict__ k, Operand ko,
@@ -1233,8 +1239,7 @@ simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict
   constexpr int CP = kCbChunk + 4;         // padded row of a 32 x 32 token-pair matrix
   constexpr int E = D * D, PD = D + 1;     // PD: the dnum / dden scratch row
   extern __shared__ __align__(16) float cbq_sm[];
-  float* st = cbq_sm;                      // [D][P] C = S<_i + W_ii P before the chunk
-  float* stT = st + D * P;                 // [D][P] C^T
+  float* stT = cbq_sm;                     // [D][P] C^T, C = S<_i + W_ii P before the chunk
   float* zs = stT + D * P;                 // [D]    c = z<_i + W_ii y before the chunk
   float* sq = zs + D;                      // [chunk][P] phi(q_t)
   float* sk = sq + kCbChunk * P;           // [chunk][P] phi(k_s)
@@ -1242,22 +1247,16 @@ simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict
   float* sg = sv + kCbChunk * P;           // [chunk][P] g_t
   float* sdn = sg + kCbChunk * P;          // [chunk][P] dnum_t
   float* sdd = sdn + kCbChunk * P;         // [chunk]    dden_t
-  float* sden = sdd + kCbChunk;            // [chunk]    den_t
-  float* sa = sden + kCbChunk;             // [chunk][CP] a_ts (s <= t, else 0)
-  float* sb = sa + kCbChunk * CP;          // [chunk][CP] b_ts (s <= t, else 0)
-  float* red = sb + kCbChunk * CP;         // [warps]
+  float* sa = sdd + kCbChunk;              // [chunk][CP] a_ts (s <= t, else 0)
+  float* se = sa + kCbChunk * CP;          // [chunk][CP] e_ts, then b_ts (s <= t, else 0)
+  float* red = se + kCbChunk * CP;         // [warps]
   const int64_t item = blockIdx.x;
   const int64_t i = item % g.M, bh = item / g.M;
   const int64_t b = bh / H, h = bh % H;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const float wii = __ldg(W + i * g.M + i);
   const float* src = Sp + (bh * g.M + i) * static_cast<int64_t>(E + D);
-  for (int e = tid; e < E; e += kCbThreads) {
-    const int r = e / D, c = e % D;
-    const float x = src[e];
-    st[r * P + c] = x;
-    stT[c * P + r] = x;
-  }
+  for (int e = tid; e < E; e += kCbThreads) stT[(e % D) * P + e / D] = src[e];
   for (int r = tid; r < D; r += kCbThreads) zs[r] = src[E + r];
   const T* qb = q + b * qo.sb + h * qo.sh;
   const T* kb = k + b * ko.sb + h * ko.sh;
@@ -1270,14 +1269,15 @@ simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict
   for (int m = 0; m < V * V; ++m) pr[m] = acc[m] = 0.0f;
   float yr = 0.0f, zacc = 0.0f, dw = 0.0f;
   const int tt = tid / 16, cc = tid % 16;
-  const int t0 = 2 * tt, t1 = t0 + 1;      // token x column tiles: tokens t0, t1; columns c0 ..
+  const int t0 = 2 * tt, t1 = t0 + 1;      // per-token steps: tokens t0, t1; columns c0 ..
   const int c0 = V * cc;
   const int r0 = V * tt;                   // state tile: rows r0 .., columns c0 ..
-  const int pi = tid / 16, pj = tid % 16;  // token-pair tiles: rows pi, pi + 16; columns pj, pj + 16
+  const int pi = tid / 16, pj = tid % 16;  // pair tiles: tokens pi, pi + 16; sources pj, pj + 16
   const int srow = tid / kCbRowLanes, spart = tid % kCbRowLanes;
   const int64_t nb = token_of(g, i, 0);    // contiguous blocks: slot s is token nb + s
   for (int64_t s0 = 0; s0 < g.w; s0 += kCbChunk) {
     const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
+    const bool more = s0 + kCbChunk < g.w;   // a later chunk of the block reads the advanced state
     __syncthreads();   // the state is complete and the previous chunk's rows are free
     {
       const bool live = srow < cnt;
@@ -1299,181 +1299,145 @@ simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict
       }
     }
     __syncthreads();
-    // ---- 1: a_ts (s <= t); the block (pi, pj + 16) lies above the diagonal
+    // ---- 1: a_ts and e_ts (s <= t); the block (pi, pj + 16) lies above the diagonal
     {
       const int ra = pi, rb = pi + 16, ca = pj, cb = pj + 16;
-      float x00 = 0.0f, x10 = 0.0f, x11 = 0.0f;
-#pragma unroll 4
+      float a00 = 0.0f, a10 = 0.0f, a11 = 0.0f, e00 = 0.0f, e10 = 0.0f, e11 = 0.0f;
+#pragma unroll 2
       for (int r = 0; r < D; r += V) {
-        float qa[V], qc[V], ka[V], kc[V];
+        float qa[V], qc[V], ka[V], kc[V], ga[V], gc[V], va[V], vc[V];
         ldv<V>(sq + ra * P + r, qa);
         ldv<V>(sq + rb * P + r, qc);
         ldv<V>(sk + ca * P + r, ka);
         ldv<V>(sk + cb * P + r, kc);
+        ldv<V>(sg + ra * P + r, ga);
+        ldv<V>(sg + rb * P + r, gc);
+        ldv<V>(sv + ca * P + r, va);
+        ldv<V>(sv + cb * P + r, vc);
 #pragma unroll
         for (int u = 0; u < V; ++u) {
-          x00 = fmaf(qa[u], ka[u], x00);
-          x10 = fmaf(qc[u], ka[u], x10);
-          x11 = fmaf(qc[u], kc[u], x11);
+          a00 = fmaf(qa[u], ka[u], a00);
+          a10 = fmaf(qc[u], ka[u], a10);
+          a11 = fmaf(qc[u], kc[u], a11);
+          e00 = fmaf(ga[u], va[u], e00);
+          e10 = fmaf(gc[u], va[u], e10);
+          e11 = fmaf(gc[u], vc[u], e11);
         }
       }
-      sa[ra * CP + ca] = (ra < cnt && ca <= ra) ? x00 : 0.0f;
+      const bool m00 = ra < cnt && ca <= ra, m10 = rb < cnt, m11 = rb < cnt && cb <= rb;
+      sa[ra * CP + ca] = m00 ? a00 : 0.0f;
       sa[ra * CP + cb] = 0.0f;
-      sa[rb * CP + ca] = rb < cnt ? x10 : 0.0f;
-      sa[rb * CP + cb] = (rb < cnt && cb <= rb) ? x11 : 0.0f;
+      sa[rb * CP + ca] = m10 ? a10 : 0.0f;
+      sa[rb * CP + cb] = m11 ? a11 : 0.0f;
+      se[ra * CP + ca] = m00 ? e00 : 0.0f;
+      se[ra * CP + cb] = 0.0f;
+      se[rb * CP + ca] = m10 ? e10 : 0.0f;
+      se[rb * CP + cb] = m11 ? e11 : 0.0f;
     }
     __syncthreads();
-    // ---- 2: den_t, eight threads per token, then a fixed-order shuffle sum
+    // ---- 2: per token (t0, t1 on the 16 lanes of a half-warp; columns / rows c0 ..)
+    float x0[V], x1[V];   // C dnum_t + dden_t c, this lane's rows
     {
-      const int tok = tid / 8, part = tid % 8;
-      float den = 0.0f;
+      float u0[V], u1[V];
 #pragma unroll
-      for (int r = V * part; r < D; r += 8 * V) {
-        float qv[V], zv[V];
-        ldv<V>(sq + tok * P + r, qv);
-        ldv<V>(zs + r, zv);
-#pragma unroll
-        for (int u = 0; u < V; ++u) den = fmaf(qv[u], zv[u], den);
-      }
-      float av[4];
-      ldv<4>(sa + tok * CP + 4 * part, av);
-      float own = ((av[0] + av[1]) + av[2]) + av[3];
-#pragma unroll
-      for (int off = 4; off > 0; off >>= 1) {
-        den += __shfl_xor_sync(0xffffffffu, den, off);
-        own += __shfl_xor_sync(0xffffffffu, own, off);
-      }
-      if (part == 0) sden[tok] = fmaf(wii, own, den) + eps;
-    }
-    __syncthreads();
-    // ---- 3: num, dnum, dden (tokens t0, t1; columns c0 ..)
-    {
-      float n0[V], n1[V], o0[V], o1[V];
-#pragma unroll
-      for (int w = 0; w < V; ++w) n0[w] = n1[w] = o0[w] = o1[w] = 0.0f;
-#pragma unroll 2
-      for (int r = 0; r < D; r += V) {
-        float qa[V], qc[V];
-        ldv<V>(sq + t0 * P + r, qa);
-        ldv<V>(sq + t1 * P + r, qc);
-#pragma unroll
-        for (int u = 0; u < V; ++u) {
-          float cv[V];
-          ldv<V>(st + (r + u) * P + c0, cv);
-#pragma unroll
-          for (int w = 0; w < V; ++w) {
-            n0[w] = fmaf(qa[u], cv[w], n0[w]);
-            n1[w] = fmaf(qc[u], cv[w], n1[w]);
-          }
-        }
-      }
-#pragma unroll 2
-      for (int s = 0; s < kCbChunk; s += V) {
-        float pa[V], pc[V];
-        ldv<V>(sa + t0 * CP + s, pa);
-        ldv<V>(sa + t1 * CP + s, pc);
-#pragma unroll
-        for (int u = 0; u < V; ++u) {
-          float vv[V];
-          ldv<V>(sv + (s + u) * P + c0, vv);
-#pragma unroll
-          for (int w = 0; w < V; ++w) {
-            o0[w] = fmaf(pa[u], vv[w], o0[w]);
-            o1[w] = fmaf(pc[u], vv[w], o1[w]);
-          }
-        }
-      }
-      const float den0 = sden[t0], den1 = sden[t1];
-      float g0[V], g1[V], d0[V], d1[V];
-      ldv<V>(sg + t0 * P + c0, g0);
-      ldv<V>(sg + t1 * P + c0, g1);
-      float go0 = 0.0f, go1 = 0.0f;
-#pragma unroll
-      for (int w = 0; w < V; ++w) {
-        go0 = fmaf(g0[w], fmaf(wii, o0[w], n0[w]), go0);
-        go1 = fmaf(g1[w], fmaf(wii, o1[w], n1[w]), go1);
-        d0[w] = t0 < cnt ? g0[w] / den0 : 0.0f;   // rows past the block stay zero
-        d1[w] = t1 < cnt ? g1[w] / den1 : 0.0f;
-      }
-      stv<V>(sdn + t0 * P + c0, d0);
-      stv<V>(sdn + t1 * P + c0, d1);
-#pragma unroll
-      for (int w = 0; w < V; ++w) {
-        if (t0 < cnt) dnb[(s0 + t0) * PD + c0 + w] = d0[w];
-        if (t1 < cnt) dnb[(s0 + t1) * PD + c0 + w] = d1[w];
-      }
-#pragma unroll
-      for (int off = 8; off > 0; off >>= 1) {   // the 16 lanes of this half-warp share t0, t1
-        go0 += __shfl_xor_sync(0xffffffffu, go0, off);
-        go1 += __shfl_xor_sync(0xffffffffu, go1, off);
-      }
-      if (cc == 0) {
-        const float dd0 = t0 < cnt ? -(go0 / den0) / den0 : 0.0f;
-        const float dd1 = t1 < cnt ? -(go1 / den1) / den1 : 0.0f;
-        sdd[t0] = dd0;
-        sdd[t1] = dd1;
-        if (t0 < cnt) dnb[(s0 + t0) * PD + D] = dd0;
-        if (t1 < cnt) dnb[(s0 + t1) * PD + D] = dd1;
-      }
-    }
-    __syncthreads();
-    // ---- 4: b_ts = v_s . dnum_t + dden_t (s <= t), dW_ii's own-chunk part
-    {
-      const int ra = pi, rb = pi + 16, ca = pj, cb = pj + 16;
-      float x00 = 0.0f, x10 = 0.0f, x11 = 0.0f;
-#pragma unroll 4
-      for (int c = 0; c < D; c += V) {
-        float na[V], nc[V], va[V], vc[V];
-        ldv<V>(sdn + ra * P + c, na);
-        ldv<V>(sdn + rb * P + c, nc);
-        ldv<V>(sv + ca * P + c, va);
-        ldv<V>(sv + cb * P + c, vc);
-#pragma unroll
-        for (int u = 0; u < V; ++u) {
-          x00 = fmaf(na[u], va[u], x00);
-          x10 = fmaf(nc[u], va[u], x10);
-          x11 = fmaf(nc[u], vc[u], x11);
-        }
-      }
-      const float da = sdd[ra], dc = sdd[rb];
-      const float b00 = (ra < cnt && ca <= ra) ? x00 + da : 0.0f;
-      const float b10 = rb < cnt ? x10 + dc : 0.0f;
-      const float b11 = (rb < cnt && cb <= rb) ? x11 + dc : 0.0f;
-      sb[ra * CP + ca] = b00;
-      sb[ra * CP + cb] = 0.0f;
-      sb[rb * CP + ca] = b10;
-      sb[rb * CP + cb] = b11;
-      dw = fmaf(sa[ra * CP + ca], b00, dw);   // a is zero wherever b is (the same mask)
-      dw = fmaf(sa[rb * CP + ca], b10, dw);
-      dw = fmaf(sa[rb * CP + cb], b11, dw);
-    }
-    __syncthreads();
-    // ---- 5: dq (tokens t0, t1; rows c0 ..), C dnum_t from the transposed state
-    {
-      float x0[V], x1[V], w0[V], w1[V];
-#pragma unroll
-      for (int w = 0; w < V; ++w) x0[w] = x1[w] = w0[w] = w1[w] = 0.0f;
+      for (int w = 0; w < V; ++w) u0[w] = u1[w] = 0.0f;
 #pragma unroll 2
       for (int c = 0; c < D; c += V) {
-        float na[V], nc[V];
-        ldv<V>(sdn + t0 * P + c, na);
-        ldv<V>(sdn + t1 * P + c, nc);
+        float ga[V], gc[V];
+        ldv<V>(sg + t0 * P + c, ga);
+        ldv<V>(sg + t1 * P + c, gc);
 #pragma unroll
         for (int u = 0; u < V; ++u) {
           float cv[V];
           ldv<V>(stT + (c + u) * P + c0, cv);   // C[c0 + w][c + u]
 #pragma unroll
           for (int w = 0; w < V; ++w) {
-            x0[w] = fmaf(cv[w], na[u], x0[w]);
-            x1[w] = fmaf(cv[w], nc[u], x1[w]);
+            u0[w] = fmaf(cv[w], ga[u], u0[w]);
+            u1[w] = fmaf(cv[w], gc[u], u1[w]);
           }
         }
       }
+      float qa[V], qc[V], zv[V], gva[V], gvc[V];
+      ldv<V>(sq + t0 * P + c0, qa);
+      ldv<V>(sq + t1 * P + c0, qc);
+      ldv<V>(zs + c0, zv);
+      ldv<V>(sg + t0 * P + c0, gva);
+      ldv<V>(sg + t1 * P + c0, gvc);
+      float den0 = 0.0f, den1 = 0.0f, go0 = 0.0f, go1 = 0.0f;
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        den0 = fmaf(qa[w], zv[w], den0);
+        den1 = fmaf(qc[w], zv[w], den1);
+        go0 = fmaf(qa[w], u0[w], go0);
+        go1 = fmaf(qc[w], u1[w], go1);
+      }
+      // this lane's own-chunk sources s = cc, cc + 16
+      const float a0a = sa[t0 * CP + cc], a0b = sa[t0 * CP + cc + 16];
+      const float a1a = sa[t1 * CP + cc], a1b = sa[t1 * CP + cc + 16];
+      const float e0a = se[t0 * CP + cc], e0b = se[t0 * CP + cc + 16];
+      const float e1a = se[t1 * CP + cc], e1b = se[t1 * CP + cc + 16];
+      den0 = fmaf(wii, a0a + a0b, den0);
+      den1 = fmaf(wii, a1a + a1b, den1);
+      go0 = fmaf(wii, fmaf(a0a, e0a, a0b * e0b), go0);
+      go1 = fmaf(wii, fmaf(a1a, e1a, a1b * e1b), go1);
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) {   // the 16 lanes of this half-warp share t0, t1
+        den0 += __shfl_xor_sync(0xffffffffu, den0, off);
+        den1 += __shfl_xor_sync(0xffffffffu, den1, off);
+        go0 += __shfl_xor_sync(0xffffffffu, go0, off);
+        go1 += __shfl_xor_sync(0xffffffffu, go1, off);
+      }
+      den0 += eps;
+      den1 += eps;
+      const bool l0 = t0 < cnt, l1 = t1 < cnt;   // rows past the block stay zero
+      const float dd0 = l0 ? -(go0 / den0) / den0 : 0.0f;
+      const float dd1 = l1 ? -(go1 / den1) / den1 : 0.0f;
+      float dn0[V], dn1[V];
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        dn0[w] = l0 ? gva[w] / den0 : 0.0f;
+        dn1[w] = l1 ? gvc[w] / den1 : 0.0f;
+        x0[w] = fmaf(dd0, zv[w], u0[w] / den0);
+        x1[w] = fmaf(dd1, zv[w], u1[w] / den1);
+      }
+      stv<V>(sdn + t0 * P + c0, dn0);
+      stv<V>(sdn + t1 * P + c0, dn1);
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        if (l0) dnb[(s0 + t0) * PD + c0 + w] = dn0[w];
+        if (l1) dnb[(s0 + t1) * PD + c0 + w] = dn1[w];
+      }
+      if (cc == 0) {
+        sdd[t0] = dd0;
+        sdd[t1] = dd1;
+        if (l0) dnb[(s0 + t0) * PD + D] = dd0;
+        if (l1) dnb[(s0 + t1) * PD + D] = dd1;
+      }
+      // b_ts = e_ts / den_t + dden_t (s <= t) in place of e_ts; dW_ii's own-chunk part
+      const float b0a = (l0 && cc <= t0) ? e0a / den0 + dd0 : 0.0f;
+      const float b0b = (l0 && cc + 16 <= t0) ? e0b / den0 + dd0 : 0.0f;
+      const float b1a = (l1 && cc <= t1) ? e1a / den1 + dd1 : 0.0f;
+      const float b1b = (l1 && cc + 16 <= t1) ? e1b / den1 + dd1 : 0.0f;
+      se[t0 * CP + cc] = b0a;
+      se[t0 * CP + cc + 16] = b0b;
+      se[t1 * CP + cc] = b1a;
+      se[t1 * CP + cc + 16] = b1b;
+      dw = fmaf(a0a, b0a, dw);
+      dw = fmaf(a0b, b0b, dw);
+      dw = fmaf(a1a, b1a, dw);
+      dw = fmaf(a1b, b1b, dw);
+    }
+    __syncthreads();
+    // ---- 3: dq (tokens t0, t1; rows c0 ..)
+    {
+      float w0[V], w1[V];
+#pragma unroll
+      for (int w = 0; w < V; ++w) w0[w] = w1[w] = 0.0f;
 #pragma unroll 2
       for (int s = 0; s < kCbChunk; s += V) {
         float ba[V], bc[V];
-        ldv<V>(sb + t0 * CP + s, ba);
-        ldv<V>(sb + t1 * CP + s, bc);
+        ldv<V>(se + t0 * CP + s, ba);
+        ldv<V>(se + t1 * CP + s, bc);
 #pragma unroll
         for (int u = 0; u < V; ++u) {
           float kv[V];
@@ -1485,43 +1449,53 @@ simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict
           }
         }
       }
-      const float dd0 = sdd[t0], dd1 = sdd[t1];
       const int64_t n0t = nb + s0 + t0, n1t = nb + s0 + t1;
 #pragma unroll
       for (int w = 0; w < V; ++w) {
         const int r = c0 + w;
-        const float zr = zs[r];
         if (t0 < cnt) {
-          const float x = fmaf(wii, w0[w], fmaf(dd0, zr, x0[w]));
+          const float x = fmaf(wii, w0[w], x0[w]);
           store_f(dqb + n0t * dqo.sn + r, load_f(qb + n0t * qo.sn + r) > 0.0f ? x : 0.0f);
         }
         if (t1 < cnt) {
-          const float x = fmaf(wii, w1[w], fmaf(dd1, zr, x1[w]));
+          const float x = fmaf(wii, w1[w], x1[w]);
           store_f(dqb + n1t * dqo.sn + r, load_f(qb + n1t * qo.sn + r) > 0.0f ? x : 0.0f);
         }
       }
     }
-    __syncthreads();   // phase 6 rewrites the state phase 5 has read
-    // ---- 6: X = sum_t phi(q_t) dnum_t^T and the chunk's phi(k_s) v_s^T over this
-    // thread's V x V entries; then dS<_i += X, dW_ii += <P, X>, P and the state advance
+    // ---- 4: X and, unless the block ends here, the chunk's phi(k_s) v_s^T over this
+    // thread's V x V entries (no barrier before: steps 2 and 3 are done with C^T)
     {
       float X[V * V], dps[V * V];
 #pragma unroll
       for (int m = 0; m < V * V; ++m) X[m] = dps[m] = 0.0f;
+      if (more) {
 #pragma unroll 4
-      for (int sl = 0; sl < kCbChunk; ++sl) {
-        float qr[V], kr[V], nc[V], vc[V];
-        ldv<V>(sq + sl * P + r0, qr);
-        ldv<V>(sk + sl * P + r0, kr);
-        ldv<V>(sdn + sl * P + c0, nc);
-        ldv<V>(sv + sl * P + c0, vc);
+        for (int sl = 0; sl < kCbChunk; ++sl) {
+          float qr[V], kr[V], nc[V], vc[V];
+          ldv<V>(sq + sl * P + r0, qr);
+          ldv<V>(sk + sl * P + r0, kr);
+          ldv<V>(sdn + sl * P + c0, nc);
+          ldv<V>(sv + sl * P + c0, vc);
 #pragma unroll
-        for (int u = 0; u < V; ++u)
+          for (int u = 0; u < V; ++u)
 #pragma unroll
-          for (int w = 0; w < V; ++w) {
-            X[u * V + w] = fmaf(qr[u], nc[w], X[u * V + w]);
-            dps[u * V + w] = fmaf(kr[u], vc[w], dps[u * V + w]);
-          }
+            for (int w = 0; w < V; ++w) {
+              X[u * V + w] = fmaf(qr[u], nc[w], X[u * V + w]);
+              dps[u * V + w] = fmaf(kr[u], vc[w], dps[u * V + w]);
+            }
+        }
+      } else {
+#pragma unroll 4
+        for (int sl = 0; sl < kCbChunk; ++sl) {
+          float qr[V], nc[V];
+          ldv<V>(sq + sl * P + r0, qr);
+          ldv<V>(sdn + sl * P + c0, nc);
+#pragma unroll
+          for (int u = 0; u < V; ++u)
+#pragma unroll
+            for (int w = 0; w < V; ++w) X[u * V + w] = fmaf(qr[u], nc[w], X[u * V + w]);
+        }
       }
 #pragma unroll
       for (int m = 0; m < V * V; ++m) {
@@ -1529,21 +1503,15 @@ simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict
         acc[m] += X[m];
         pr[m] += dps[m];
       }
+      if (more) {
 #pragma unroll
-      for (int u = 0; u < V; ++u) {
-        float cur[V];
-        ldv<V>(st + (r0 + u) * P + c0, cur);
+        for (int w = 0; w < V; ++w) {
+          float cur[V];
+          ldv<V>(stT + (c0 + w) * P + r0, cur);
 #pragma unroll
-        for (int w = 0; w < V; ++w) cur[w] = fmaf(wii, dps[u * V + w], cur[w]);
-        stv<V>(st + (r0 + u) * P + c0, cur);
-      }
-#pragma unroll
-      for (int w = 0; w < V; ++w) {
-        float cur[V];
-        ldv<V>(stT + (c0 + w) * P + r0, cur);
-#pragma unroll
-        for (int u = 0; u < V; ++u) cur[u] = fmaf(wii, dps[u * V + w], cur[u]);
-        stv<V>(stT + (c0 + w) * P + r0, cur);
+          for (int u = 0; u < V; ++u) cur[u] = fmaf(wii, dps[u * V + w], cur[u]);
+          stv<V>(stT + (c0 + w) * P + r0, cur);
+        }
       }
     }
     if (tid < D) {
@@ -1580,7 +1548,8 @@ simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict
 // The same arithmetic as simt_causal_bwd_key for d = D in {32, 64}, laid out as
 // simt_causal_bwd_query_v: padded rows, 16-byte vectors, G kept row-major and
 // transposed (G feeds dv, G^T feeds dk), token-pair tiles {p, p + 16} x
-// {q, q + 16}, zero rows past the block's end.
+// {q, q + 16}, zero rows past the block's end; the block's first chunk (the
+// last one taken) skips the update of G.
 template <typename T, int D>
 __global__ void __launch_bounds__(kCbThreads, 2)
 simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__ k, Operand ko,
@@ -1758,7 +1727,8 @@ simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__
         }
       }
     }
-    __syncthreads();   // phase 3 rewrites G, which phase 2 has read
+    if (ci == 0) break;   // the block's first chunk: nothing reads the suffix state after it
+    __syncthreads();      // phase 3 rewrites G, which phase 2 has read
     // ---- 3: G += W_jj sum_t phi(q_t) dnum_t^T (V x V entries per thread), gz likewise
     {
       float X[V * V];
@@ -1801,8 +1771,8 @@ simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__
 
 // Shared memory of the vector-layout causal backward kernels, d = D.
 constexpr size_t cbv_query_smem(int D) {
-  return static_cast<size_t>(2 * D * (D + 4) + D + 5 * kCbChunk * (D + 4) + 2 * kCbChunk +
-                             2 * kCbChunk * (kCbChunk + 4) + kCbWarps) *
+  return static_cast<size_t>(D * (D + 4) + D + 5 * kCbChunk * (D + 4) + kCbChunk + 2 * kCbChunk * (kCbChunk + 4) +
+                             kCbWarps) *
          sizeof(float);
 }
 constexpr size_t cbv_key_smem(int D) {
