@@ -1591,8 +1591,7 @@ simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__
   T* dvb = dv + b * dvo.sb + h * dvo.sh;
   const float* dnb = dn + (bh * g.M + j) * g.w * PD;
   const int tt = tid / 16, cc = tid % 16;
-  const int s0t = 2 * tt, s1t = s0t + 1;   // sources s0t, s1t; columns c0 ..
-  const int c0 = V * cc;
+  const int c0 = V * cc;                   // columns c0 .. of the dv / dk and state steps
   const int r0 = V * tt;                   // state tile: rows r0 .., columns c0 ..
   const int pi = tid / 16, pj = tid % 16;  // pair tiles: sources pi, pi + 16; queries pj, pj + 16
   const int srow = tid / kCbRowLanes, spart = tid % kCbRowLanes;
@@ -1660,70 +1659,68 @@ simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__
       sb[rb * CP + cb] = m11 ? b11 + ddc : 0.0f;
     }
     __syncthreads();
-    // ---- 2: dv and dk of sources s0t, s1t (columns / rows c0 ..)
+    // ---- 2: warps 0-3 form dv, warps 4-7 dk; a thread takes 4 sources x V columns:
+    //   dv_s[c] = sum_x phi(k_s)[x] G[x][c] + W_jj sum_t a_st dnum_t[c]
+    //   dk_s[r] = (sum_x G[r][x] v_s[x] + gz[r] + W_jj sum_t b_st phi(q_t)[r]) [k_s > 0]
     {
-      float v0[V], v1[V], w0[V], w1[V];
+      const bool kside = tid >= kCbThreads / 2;
+      const int sb4 = 4 * ((tid % (kCbThreads / 2)) / 16);   // sources sb4 .. sb4 + 3
+      const float* opd = kside ? sv : sk;
+      const float* gm = kside ? gsT : gs;                    // gm[x][c0 + w]: G[x][c] or G[r][x]
+      const float* pm = kside ? sb : sa;
+      const float* tm = kside ? sq : sdn;
+      float ga[4][V], pa[4][V];
 #pragma unroll
-      for (int w = 0; w < V; ++w) v0[w] = v1[w] = w0[w] = w1[w] = 0.0f;
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int w = 0; w < V; ++w) ga[jj][w] = pa[jj][w] = 0.0f;
 #pragma unroll 2
       for (int x = 0; x < D; x += V) {
-        float ka[V], kc[V], ea[V], ec[V];
-        ldv<V>(sk + s0t * P + x, ka);
-        ldv<V>(sk + s1t * P + x, kc);
-        ldv<V>(sv + s0t * P + x, ea);
-        ldv<V>(sv + s1t * P + x, ec);
+        float o[4][V];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) ldv<V>(opd + (sb4 + jj) * P + x, o[jj]);
 #pragma unroll
         for (int u = 0; u < V; ++u) {
-          float gcol[V], grow[V];
-          ldv<V>(gs + (x + u) * P + c0, gcol);    // G[x + u][c0 + w]
-          ldv<V>(gsT + (x + u) * P + c0, grow);   // G[c0 + w][x + u]
+          float gv[V];
+          ldv<V>(gm + (x + u) * P + c0, gv);
 #pragma unroll
-          for (int w = 0; w < V; ++w) {
-            v0[w] = fmaf(ka[u], gcol[w], v0[w]);
-            v1[w] = fmaf(kc[u], gcol[w], v1[w]);
-            w0[w] = fmaf(grow[w], ea[u], w0[w]);
-            w1[w] = fmaf(grow[w], ec[u], w1[w]);
-          }
+          for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int w = 0; w < V; ++w) ga[jj][w] = fmaf(o[jj][u], gv[w], ga[jj][w]);
         }
       }
-      float ov0[V], ov1[V], ok0[V], ok1[V];
-#pragma unroll
-      for (int w = 0; w < V; ++w) ov0[w] = ov1[w] = ok0[w] = ok1[w] = 0.0f;
 #pragma unroll 2
       for (int t = 0; t < kCbChunk; t += V) {
-        float aa[V], ac[V], ba[V], bc[V];
-        ldv<V>(sa + s0t * CP + t, aa);
-        ldv<V>(sa + s1t * CP + t, ac);
-        ldv<V>(sb + s0t * CP + t, ba);
-        ldv<V>(sb + s1t * CP + t, bc);
+        float pv[4][V];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) ldv<V>(pm + (sb4 + jj) * CP + t, pv[jj]);
 #pragma unroll
         for (int u = 0; u < V; ++u) {
-          float nv[V], qv[V];
-          ldv<V>(sdn + (t + u) * P + c0, nv);
-          ldv<V>(sq + (t + u) * P + c0, qv);
+          float tv[V];
+          ldv<V>(tm + (t + u) * P + c0, tv);
 #pragma unroll
-          for (int w = 0; w < V; ++w) {
-            ov0[w] = fmaf(aa[u], nv[w], ov0[w]);
-            ov1[w] = fmaf(ac[u], nv[w], ov1[w]);
-            ok0[w] = fmaf(ba[u], qv[w], ok0[w]);
-            ok1[w] = fmaf(bc[u], qv[w], ok1[w]);
-          }
+          for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int w = 0; w < V; ++w) pa[jj][w] = fmaf(pv[jj][u], tv[w], pa[jj][w]);
         }
       }
-      const int64_t n0t = nb + s0 + s0t, n1t = nb + s0 + s1t;
+      float zv[V];
+      ldv<V>(gz + c0, zv);
 #pragma unroll
-      for (int w = 0; w < V; ++w) {
-        const int c = c0 + w;
-        const float zr = gz[c];
-        if (s0t < cnt) {
-          store_f(dvb + n0t * dvo.sn + c, fmaf(wjj, ov0[w], v0[w]));
-          const float x = fmaf(wjj, ok0[w], w0[w] + zr);
-          store_f(dkb + n0t * dko.sn + c, load_f(kb + n0t * ko.sn + c) > 0.0f ? x : 0.0f);
-        }
-        if (s1t < cnt) {
-          store_f(dvb + n1t * dvo.sn + c, fmaf(wjj, ov1[w], v1[w]));
-          const float x = fmaf(wjj, ok1[w], w1[w] + zr);
-          store_f(dkb + n1t * dko.sn + c, load_f(kb + n1t * ko.sn + c) > 0.0f ? x : 0.0f);
+      for (int jj = 0; jj < 4; ++jj) {
+        const int s = sb4 + jj;
+        if (s < cnt) {
+          const int64_t n = nb + s0 + s;
+#pragma unroll
+          for (int w = 0; w < V; ++w) {
+            const int c = c0 + w;
+            if (kside) {
+              const float x = fmaf(wjj, pa[jj][w], ga[jj][w] + zv[w]);
+              store_f(dkb + n * dko.sn + c, load_f(kb + n * ko.sn + c) > 0.0f ? x : 0.0f);
+            } else {
+              store_f(dvb + n * dvo.sn + c, fmaf(wjj, pa[jj][w], ga[jj][w]));
+            }
+          }
         }
       }
     }
