@@ -85,6 +85,9 @@ CASES = {
     "seq_d64_bf16": (2, 3, 64, (1, 512), (1, 64), "bf16"),
     "seq_ragged_chunk_d32_bf16": (1, 2, 32, (1, 300), (1, 50), "bf16"),   # 50 = 32 + 18 tokens per block
     "seq_long_blocks_d64_bf16": (1, 2, 64, (1, 1024), (1, 256), "bf16"),  # 8 chunks per block
+    "seq_ragged_chunk_d64_f32": (1, 2, 64, (1, 280), (1, 70), "f32"),     # 70 = 2 x 32 + 6 tokens per block
+    "seq_short_blocks_d64_bf16": (2, 2, 64, (1, 200), (1, 20), "bf16"),  # one part-filled chunk per block
+    "frames_d32_bf16": (1, 2, 32, (4, 8, 8), (1, 8, 8), "bf16"),         # whole 64-token frames
     "seq_d64_f32": (1, 2, 64, (1, 256), (1, 32), "f32"),
     "rows_d48_f32": (2, 2, 48, (12, 10), (3, 10), "f32"),
     "rows_d128_bf16": (1, 2, 128, (8, 16), (2, 16), "bf16"),
