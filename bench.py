@@ -173,6 +173,7 @@ KERNEL_SOURCES = {"tc_summary": ("tc_summary.cu", "tc_fwd_bodies.cuh"), "tc_mix"
                   "simt_bwd_key": "simt_kernels.cu", "simt_dw": "simt_kernels.cu",
                   "simt_causal_output": "simt_kernels.cu", "tc_causal_tile": "causal_tc_kernels.cu",
                   "simt_causal_bwd_query": "simt_kernels.cu", "simt_causal_bwd_key": "simt_kernels.cu",
+                  "simt_states_from_tc": "simt_kernels.cu",
                   "tc_tile_output": "causal_tc_kernels.cu", "mhla_lepe_add": "module_kernels.cu",
                   "mhla_ln_rows": "module_kernels.cu", "mhla_gemm_qkv": "gemm_kernels.cu",
                   "mhla_gemm_out": "gemm_kernels.cu"}
@@ -227,6 +228,8 @@ def kernel_work(wl, name):
         # rows; read q, k, v and those rows, write dk, dv
         "simt_causal_bwd_query": ("hbm", 5 * io + BH * wl.N * (d + 1) * 4),
         "simt_causal_bwd_key": ("hbm", 5 * io + BH * wl.N * (d + 1) * 4),
+        # the tensor-core summaries (bf16) and states (bf16 S<, float32 z<) to float32
+        "simt_states_from_tc": ("hbm", BH * M * (d * (d + 1) * 2 + d * d * 2 + d * 4 + 2 * d * (d + 1) * 4)),
         # readout of contiguous 64-token blocks: read q, write o
         "tc_tile_output": ("hbm", 2 * io),
         # module: x -> LayerNorm; qkv = xn W^T; o += lepe(v) (read v, o; write o); y = o W^T

@@ -279,10 +279,16 @@ mhla_status_t mhla_backward_causal_workspace_size(const mhla_tensor_t* q, const 
  *   Arguments, aliasing rules and statuses as for mhla_backward; the blocks must
  *   be contiguous ranges of raster-order tokens as for mhla_forward_causal, else
  *   MHLA_ERR_SHAPE.  Entries W[i][j] with j > i are never read.
- *   path: AUTO and SIMT run on CUDA cores (float32 arithmetic, any d <= 128,
- *   bf16 or float32); TC, FUSED and TC_FUSED return MHLA_ERR_UNSUPPORTED.
- *   workspace: at least mhla_backward_causal_workspace_size() bytes (about
- *   3 B H M d (d + 1) + B H N (d + 1) floats), 256-byte aligned, or NULL with
+ *   path: the per-token steps run on CUDA cores (float32 arithmetic, any
+ *   d <= 128, bf16 or float32).  SIMT: the recomputed summaries S_j and mixed
+ *   past S<_i too.  TC: those two steps on the tensor-core causal forward's
+ *   summary and mixing kernels (bf16 MMA operands, float32 accumulation), when
+ *   that path takes the problem and every block is one of its units (w = 64 or
+ *   128 tokens), else MHLA_ERR_UNSUPPORTED.  AUTO: TC when it applies, else
+ *   SIMT.  FUSED and TC_FUSED return MHLA_ERR_UNSUPPORTED.
+ *   workspace: at least mhla_backward_causal_workspace_size() bytes for the same
+ *   path (about 3 B H M d (d + 1) + B H N (d + 1) floats, plus the tensor-core
+ *   summaries and states for TC), 256-byte aligned, or NULL with
  *   workspace_bytes == 0 (stream-ordered allocation).
  * B == 0 or H == 0 writes dW = 0 and nothing else. */
 mhla_status_t mhla_backward_causal(const mhla_tensor_t* q, const mhla_tensor_t* k,

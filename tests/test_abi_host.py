@@ -367,21 +367,29 @@ def test_causal_backward_rejects_malformed_requests_before_any_launch(L):
     assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, phi=(3, 1e-6)) == INVALID
     assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, ws=FAKE + 7, ws_bytes=1 << 40) == WORKSPACE
     assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, ws=FAKE, ws_bytes=16) == WORKSPACE
-    for path in (2, 3, 4):
+    for path in (3, 4):
         assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, path=path) == UNSUPPORTED
+    # TC (tensor-core summaries and mixing) takes bf16, d = 64, 64-token blocks; it
+    # gets as far as the workspace check here
+    assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, ws=FAKE, ws_bytes=16, path=2) == WORKSPACE
+    f32 = seven(2, 1024, 3, 64, "f32")
+    assert call_backward_causal(L, *f32, grid, block, path=2) == UNSUPPORTED          # float32 inputs
+    assert call_backward_causal(L, q, k, v, g, dq, dk, dv, (1, 1024), (1, 256), path=2) == UNSUPPORTED  # w = 256
     assert call_backward_causal(L, q, k, v, g, dq, dk, dv, grid, block, path=9) == INVALID
     n = ctypes.c_size_t()
-    for path in (0, 1):
+    BH, M, N, d = 6, 16, 1024, 64
+    KS = 16  # the dW partial products split d (d + 1) = 4160 entries in 16 runs (6 tiles are too few CTAs)
+    need = 3 * BH * M * d * (d + 1) * 4 + BH * KS * M * M * 4 + BH * M * 4 + BH * N * (d + 1) * 4
+    groups = (BH * (d + 1) * d + 127) // 128
+    tc = M * M * 2 + M * groups * 128 * 2 + BH * M * d * d * 2 + BH * M * d * 4   # W', summaries, states
+    for path, extra in ((0, tc), (1, 0), (2, tc)):
         assert L.mhla_backward_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(grid)),
                                                      ctypes.byref(mhla.shape3(block)), path,
                                                      ctypes.byref(n)) == OK
-        BH, M, N, d = 6, 16, 1024, 64
-        KS = 16  # the dW partial products split d (d + 1) = 4160 entries in 16 runs (6 tiles are too few CTAs)
-        need = 3 * BH * M * d * (d + 1) * 4 + BH * KS * M * M * 4 + BH * M * 4 + BH * N * (d + 1) * 4
-        assert n.value % 256 == 0 and need <= n.value < need + 6 * 256
+        assert n.value % 256 == 0 and need + extra <= n.value < need + extra + 11 * 256, path
     assert L.mhla_backward_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3((32, 32))),
                                                  ctypes.byref(mhla.shape3((4, 4))), 0, ctypes.byref(n)) == SHAPE
-    assert L.mhla_backward_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(grid)),
+    assert L.mhla_backward_causal_workspace_size(ctypes.byref(f32[0]), ctypes.byref(mhla.shape3(grid)),
                                                  ctypes.byref(mhla.shape3(block)), 2,
                                                  ctypes.byref(n)) == UNSUPPORTED
 

@@ -68,8 +68,8 @@ def dw_term_scale(q, k, v, W, g, grid, block, phi_kind, eps):
     return float(scale.max())
 
 
-def check(case, q, k, v, W, g, grid, block, dtype, phi="relu", eps=1e-6):
-    got = run(q, k, v, W, g, grid, block, phi, eps)
+def check(case, q, k, v, W, g, grid, block, dtype, phi="relu", eps=1e-6, path="auto"):
+    got = run(q, k, v, W, g, grid, block, phi, eps, path=path)
     args = (as_f64(q), as_f64(k), as_f64(v), W, as_f64(g), grid, block, PHI[phi], eps)
     ref = oracle.backward_causal(*args)
     errs = {name: normwise(a, b) for name, a, b in zip(NAMES, got, ref)}
@@ -110,6 +110,20 @@ def test_causal_backward_matches_oracle(name, phi):
     g = draw_dout((B, N, H, d), 82, dtype)
     W = draw_matrix(oracle.num_blocks(grid, block), seed=83)      # asymmetric; the upper triangle must not matter
     check(f"{name}/{phi}", q, k, v, W, g, grid, block, dtype, phi, eps)
+
+
+@pytest.mark.parametrize("path", ["simt", "tc"])
+@pytest.mark.parametrize("grid,block", [((1, 512), (1, 64)), ((1, 768), (1, 128)), ((4, 8, 8), (1, 8, 8))])
+def test_causal_backward_both_ways_to_the_states(path, grid, block):
+    """The summaries and the mixed past formed on CUDA cores (SIMT) or by the
+    tensor-core causal forward's kernels (TC: bf16 operands), each against the
+    oracle, on the shapes TC takes: blocks of 64 and 128 tokens, whole frames."""
+    B, H, d = 2, 3, 64
+    N = int(np.prod(grid))
+    q, k, v = draw_qkv(B, N, H, d, seed=96, dtype="bf16")
+    g = draw_dout((B, N, H, d), 97, "bf16")
+    W = draw_matrix(oracle.num_blocks(grid, block), seed=98)
+    check(f"{path}/{grid}/{block}", q, k, v, W, g, grid, block, "bf16", "relu_eps", 1e-6, path=path)
 
 
 def test_causal_backward_ignores_w_above_the_diagonal_and_is_deterministic():

@@ -603,6 +603,25 @@ int launch_tc_tile_forward(const Problem& p, const float* W, void* Wb, int64_t M
   return p.d == 64 ? launch_ct_tile<64, 2, false>(p, W, p.M, st, zt, s) : launch_ct_tile<32, 2, false>(p, W, p.M, st, zt, s);
 }
 
+bool tc_causal_states_eligible(const Problem& p) { return (p.w == 64 || p.w == 128) && tc_causal_eligible(p); }
+
+size_t tc_causal_states_bytes(const Problem& p) { return ct_layout(p).total; }
+
+int launch_tc_causal_states(const Problem& p, const float* W, void* region, void* stream, CausalStates* out) {
+  const CtLayout L = ct_layout(p);   // U = w: the units are the blocks, W' is W's strict lower triangle
+  char* ws = static_cast<char*>(region);
+  auto* Wu = reinterpret_cast<__nv_bfloat16*>(ws + L.wu_off);
+  auto* St = reinterpret_cast<__nv_bfloat16*>(ws + L.st_off);
+  auto* zt = reinterpret_cast<float*>(ws + L.zt_off);
+  const Problem pu = unit_problem(p, L.U);
+  int rc = tc_run_summary(pu, W, Wu, nullptr, L.Mp, ws + L.sbuf_off, stream, static_cast<int32_t>(p.M), 1);
+  if (rc == MHLA_OK) rc = tc_run_mix(pu, Wu, L.Mp, ws + L.sbuf_off, St, zt, stream, /*discard_input=*/false);
+  out->Sbuf = ws + L.sbuf_off;
+  out->St = St;
+  out->zt = zt;
+  return rc;
+}
+
 int read_and_clear_causal_error(void* stream, uint32_t* flags) {
   return read_and_clear_word(g_causal_error, stream, flags);
 }

@@ -354,11 +354,22 @@ extern "C" mhla_status_t mhla_backward(const mhla_tensor_t* q, const mhla_tensor
 namespace mhla {
 namespace {
 
-// The causal backward runs on CUDA cores; TC is refused until it has a
-// tensor-core pipeline of its own.
-int resolve_causal_bwd_path(int32_t path, int* sel) {
-  if (path == MHLA_PATH_AUTO || path == MHLA_PATH_SIMT) { *sel = MHLA_PATH_SIMT; return MHLA_OK; }
-  if (path == MHLA_PATH_TC || path == MHLA_PATH_FUSED || path == MHLA_PATH_TC_FUSED) return MHLA_ERR_UNSUPPORTED;
+// The causal backward's token kernels run on CUDA cores.  TC: the summaries and
+// the mixing come from the tensor-core causal forward's kernels (every block one
+// unit of its tiling); AUTO takes that whenever it applies.  SIMT: CUDA cores
+// throughout.
+int resolve_causal_bwd_path(const Problem& p, int32_t path, int* sel) {
+  if (path == MHLA_PATH_AUTO) {
+    *sel = tc_causal_states_eligible(p) ? MHLA_PATH_TC : MHLA_PATH_SIMT;
+    return MHLA_OK;
+  }
+  if (path == MHLA_PATH_SIMT) { *sel = MHLA_PATH_SIMT; return MHLA_OK; }
+  if (path == MHLA_PATH_TC) {
+    if (!tc_causal_states_eligible(p)) return MHLA_ERR_UNSUPPORTED;
+    *sel = MHLA_PATH_TC;
+    return MHLA_OK;
+  }
+  if (path == MHLA_PATH_FUSED || path == MHLA_PATH_TC_FUSED) return MHLA_ERR_UNSUPPORTED;
   return MHLA_ERR_INVALID_ARG;
 }
 
@@ -374,9 +385,9 @@ extern "C" mhla_status_t mhla_backward_causal_workspace_size(const mhla_tensor_t
   if (rc != MHLA_OK) return static_cast<mhla_status_t>(rc);
   if (!blocks_contiguous(p)) return MHLA_ERR_SHAPE;
   int sel = 0;
-  const int rp = resolve_causal_bwd_path(path, &sel);
+  const int rp = resolve_causal_bwd_path(p, path, &sel);
   if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
-  *bytes = (p.B == 0 || p.H == 0) ? 0 : simt_causal_bwd_workspace_bytes(p);
+  *bytes = (p.B == 0 || p.H == 0) ? 0 : simt_causal_bwd_workspace_bytes(p, sel == MHLA_PATH_TC);
   return MHLA_OK;
 }
 
@@ -395,13 +406,14 @@ extern "C" mhla_status_t mhla_backward_causal(const mhla_tensor_t* q, const mhla
   const int ro = check_bwd_operands(q, dout, dq, dk, dv, dW, &bo);
   if (ro != MHLA_OK) return static_cast<mhla_status_t>(ro);
   int sel = 0;
-  const int rp = resolve_causal_bwd_path(path, &sel);
+  const int rp = resolve_causal_bwd_path(p, path, &sel);
   if (rp != MHLA_OK) return static_cast<mhla_status_t>(rp);
   const int rv = check_bwd_overlaps(p, q, k, v, W, dout, dq, dk, dv, dW);
   if (rv != MHLA_OK) return static_cast<mhla_status_t>(rv);
-  const size_t need = (p.B == 0 || p.H == 0) ? 0 : simt_causal_bwd_workspace_bytes(p);
+  const bool tc_states = sel == MHLA_PATH_TC;
+  const size_t need = (p.B == 0 || p.H == 0) ? 0 : simt_causal_bwd_workspace_bytes(p, tc_states);
   return static_cast<mhla_status_t>(run_bwd(p, dW, need, workspace, workspace_bytes, stream, [&](void* ws) {
-    return launch_simt_causal_bwd(p, W, bo, ws, stream);
+    return launch_simt_causal_bwd(p, W, bo, ws, stream, tc_states);
   }));
 }
 

@@ -83,9 +83,25 @@ size_t simt_bwd_workspace_bytes(const Problem& p);
 int launch_simt_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream);
 // Causal backward on CUDA cores (contiguous blocks, any d <= 128).  Workspace:
 // S_j, the mixed past S<_i (later dS_j), dS<_i, the dW partials and diagonal
-// shares, and dnum_t, dden_t per token (float32).
-size_t simt_causal_bwd_workspace_bytes(const Problem& p);
-int launch_simt_causal_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream);
+// shares, and dnum_t, dden_t per token (float32); with tc_states, then the
+// region of launch_tc_causal_states, whose summaries and states replace the
+// CUDA-core summary and mixing steps.
+size_t simt_causal_bwd_workspace_bytes(const Problem& p, bool tc_states);
+int launch_simt_causal_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream,
+                           bool tc_states);
+// The tensor-core causal forward's first two steps kept for the backward when
+// every block is one unit (w = 64 or 128, and tc_causal_eligible): the block
+// summaries S_j (Sbuf: bf16, the (b, h, entry) columns in groups of 128, one
+// row of each group per block, entries S_j row-major then z_j) and the mixed
+// past S<_i (St: bf16 [BH][M][d][d] row-major; zt: float32 [BH][M][d]).
+struct CausalStates {
+  const void* Sbuf;
+  const void* St;
+  const float* zt;
+};
+bool tc_causal_states_eligible(const Problem& p);
+size_t tc_causal_states_bytes(const Problem& p);
+int launch_tc_causal_states(const Problem& p, const float* W, void* region, void* stream, CausalStates* out);
 
 // Tensor-core backward (bf16, d in {32, 64}, the forward tensor-core path's
 // token geometry, TMA-friendly strides on every operand).  Workspace: Wb and

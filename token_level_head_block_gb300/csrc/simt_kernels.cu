@@ -1935,6 +1935,49 @@ int launch_simt_causal_typed(const Problem& p, const float* W, const SimtWorkspa
   }
 }
 
+// The tensor-core causal forward's block summaries and mixed past (bf16 Sbuf,
+// St; float32 zt) as the float32 [BH][M][d(d+1)] buffers of the kernels above:
+// Sz[bh][j][e] = Sbuf column bh d(d+1) + e of block j, Sp[bh][i] = S<_i row-major
+// then z<_i.  One CTA per (b, h, block), each thread eight consecutive entries
+// (d(d+1) and d^2 are multiples of 8 for d in {32, 64}, so an eight-entry run
+// stays inside one 128-column group of Sbuf and inside S< or z<).
+constexpr int kStThreads = 256;
+__global__ void __launch_bounds__(kStThreads)
+simt_states_from_tc(const __nv_bfloat16* __restrict__ Sbuf, const __nv_bfloat16* __restrict__ St,
+                    const float* __restrict__ zt, float* __restrict__ Sz, float* __restrict__ Sp, int64_t M, int d,
+                    int64_t items) {
+  const int E = d * d, E1 = E + d;
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    const int64_t bh = it / M, j = it % M;
+    for (int e = 8 * threadIdx.x; e < E1; e += 8 * kStThreads) {
+      const int64_t col = bh * E1 + e;
+      const uint4 sb = *reinterpret_cast<const uint4*>(Sbuf + ((col >> 7) * M + j) * 128 + (col & 127));
+      float4 lo, hi;
+      lo.x = __uint_as_float(sb.x << 16), lo.y = __uint_as_float(sb.x & 0xffff0000u);
+      lo.z = __uint_as_float(sb.y << 16), lo.w = __uint_as_float(sb.y & 0xffff0000u);
+      hi.x = __uint_as_float(sb.z << 16), hi.y = __uint_as_float(sb.z & 0xffff0000u);
+      hi.z = __uint_as_float(sb.w << 16), hi.w = __uint_as_float(sb.w & 0xffff0000u);
+      float4* zdst = reinterpret_cast<float4*>(Sz + it * E1 + e);
+      zdst[0] = lo;
+      zdst[1] = hi;
+      if (e < E) {
+        const uint4 s = *reinterpret_cast<const uint4*>(St + it * E + e);
+        lo.x = __uint_as_float(s.x << 16), lo.y = __uint_as_float(s.x & 0xffff0000u);
+        lo.z = __uint_as_float(s.y << 16), lo.w = __uint_as_float(s.y & 0xffff0000u);
+        hi.x = __uint_as_float(s.z << 16), hi.y = __uint_as_float(s.z & 0xffff0000u);
+        hi.z = __uint_as_float(s.w << 16), hi.w = __uint_as_float(s.w & 0xffff0000u);
+      } else {
+        const float4* z = reinterpret_cast<const float4*>(zt + it * d + (e - E));
+        lo = z[0];
+        hi = z[1];
+      }
+      float4* pdst = reinterpret_cast<float4*>(Sp + it * E1 + e);
+      pdst[0] = lo;
+      pdst[1] = hi;
+    }
+  }
+}
+
 struct SimtCausalBwdWorkspace {
   float* Sz;     // [BH][M][d*(d+1)] S_j, z_j
   float* Sp;     // [BH][M][d*(d+1)] S<_i, z<_i, later dS_j, dz_j
@@ -1942,6 +1985,7 @@ struct SimtCausalBwdWorkspace {
   float* part;   // [BH][M][M]       <dS<_i, S_j> + dz<_i . z_j
   float* diag;   // [BH][M]          the (b, h) share of dW_ii
   float* dn;     // [BH][N][d + 1]   dnum_t, dden_t in block-slot order
+  void* tc;      // the region of launch_tc_causal_states (tensor-core summaries and mixing), or null
 };
 
 SimtCausalBwdWorkspace simt_causal_bwd_carve(const Problem& p, void* base) {
@@ -1956,6 +2000,7 @@ SimtCausalBwdWorkspace simt_causal_bwd_carve(const Problem& p, void* base) {
   ws.part = reinterpret_cast<float*>(c + 3 * align_up(per));
   ws.diag = reinterpret_cast<float*>(c + 3 * align_up(per) + align_up(part));
   ws.dn = reinterpret_cast<float*>(c + 3 * align_up(per) + align_up(part) + align_up(diag));
+  ws.tc = nullptr;
   return ws;
 }
 
@@ -1975,9 +2020,19 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
   T* dkp = static_cast<T*>(bo.dk.data);
   T* dvp = static_cast<T*>(bo.dv.data);
   const int64_t E = p.d * (p.d + 1);
-  if (const int rc = launch_summary<T>(p, g, ws.Sz, stream); rc != MHLA_OK) return rc;
-  if (const int rc = launch_mix<false, true>(W, ws.Sz, ws.Sp, p.M, E, BH, stream); rc != MHLA_OK)
-    return rc;
+  if (ws.tc) {   // S_j and S<_i from the tensor-core causal forward's summary and mixing kernels
+    CausalStates cs;
+    if (const int rc = launch_tc_causal_states(p, W, ws.tc, stream, &cs); rc != MHLA_OK) return rc;
+    KernelTimer timer("simt_states_from_tc", stream);
+    simt_states_from_tc<<<static_cast<unsigned>(items), kStThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(cs.Sbuf),
+                                                         static_cast<const __nv_bfloat16*>(cs.St), cs.zt, ws.Sz,
+                                                         ws.Sp, p.M, d, items);
+    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  } else {
+    if (const int rc = launch_summary<T>(p, g, ws.Sz, stream); rc != MHLA_OK) return rc;
+    if (const int rc = launch_mix<false, true>(W, ws.Sz, ws.Sp, p.M, E, BH, stream); rc != MHLA_OK)
+      return rc;
+  }
   {
     const size_t smem = (d * (d + 1) + d + 5 * kCbChunk * (d + 1) + 2 * kCbChunk + 2 * kCbChunk * (kCbChunk + 1) +
                          kCbWarps) * sizeof(float);
@@ -2101,16 +2156,24 @@ int launch_simt_bwd(const Problem& p, const float* W, const BwdOperands& bo, voi
   return launch_simt_bwd_typed<float>(p, W, bo, ws, s);
 }
 
-size_t simt_causal_bwd_workspace_bytes(const Problem& p) {
+namespace {
+size_t simt_causal_bwd_own_bytes(const Problem& p) {
   const size_t per = static_cast<size_t>(p.BH()) * p.M * p.d * (p.d + 1) * sizeof(float);
   const size_t part = static_cast<size_t>(p.BH()) * dw_splits(p) * p.M * p.M * sizeof(float);
   const size_t diag = static_cast<size_t>(p.BH()) * p.M * sizeof(float);
   const size_t dn = static_cast<size_t>(p.BH()) * p.M * p.w * (p.d + 1) * sizeof(float);
   return 3 * align_up(per) + align_up(part) + align_up(diag) + align_up(dn);
 }
+}  // namespace
 
-int launch_simt_causal_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream) {
-  const SimtCausalBwdWorkspace ws = simt_causal_bwd_carve(p, workspace);
+size_t simt_causal_bwd_workspace_bytes(const Problem& p, bool tc_states) {
+  return simt_causal_bwd_own_bytes(p) + (tc_states ? align_up(tc_causal_states_bytes(p)) : 0);
+}
+
+int launch_simt_causal_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream,
+                           bool tc_states) {
+  SimtCausalBwdWorkspace ws = simt_causal_bwd_carve(p, workspace);
+  if (tc_states) ws.tc = static_cast<char*>(workspace) + simt_causal_bwd_own_bytes(p);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.dtype == MHLA_BF16) return launch_simt_causal_bwd_typed<__nv_bfloat16>(p, W, bo, ws, s);
   return launch_simt_causal_bwd_typed<float>(p, W, bo, ws, s);
