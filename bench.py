@@ -608,7 +608,9 @@ def run_ours(args, wl):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic",
             "config": {**wl.describe(), "pass": args.pass_,
-                       "path": ("tc" if "tc_bwd_query" in prof else "simt") if bwd else
+                       "path": ("tc (summaries, mixing) + simt (token steps)" if "tc_summary" in prof else "simt")
+                               if args.pass_ == "causal_backward" else
+                               ("tc" if "tc_bwd_query" in prof else "simt") if bwd else
                                ("module (core: " + path + ")") if module else
                                (("tc" if "tc_causal_tile" in prof else "simt") if args.pass_ == "causal" else path),
                        "global_batch": wl.B * world, "seq_len": wl.N,

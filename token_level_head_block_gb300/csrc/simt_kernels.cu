@@ -167,7 +167,7 @@ constexpr int kMixThreads = 256;
 constexpr int kMixTileI = 64;    // output blocks per CTA, 8 per warp
 constexpr int kMixTileE = 128;   // entries per CTA, 4 per lane (stride 32)
 constexpr int kMixK = 16;        // source blocks per slab
-constexpr int kMixStages = 4;    // slabs in flight
+constexpr int kMixStages = 3;    // slabs in flight (within 48 KB of shared memory)
 constexpr int kMixWRow = kMixTileI + 4;
 constexpr int kMixStage = kMixK * kMixWRow + kMixK * kMixTileE;   // floats per stage
 constexpr size_t kMixSmem = static_cast<size_t>(kMixStages) * kMixStage * sizeof(float);
@@ -177,7 +177,7 @@ constexpr size_t kMixSmem = static_cast<size_t>(kMixStages) * kMixStage * sizeof
 // (PAST: only source blocks j < i, the mixed past summaries of causal MHLA;
 // with TRANS, only i > j: the reverse of that mixing in the causal backward.)
 // A CTA holds a 64-block x 128-entry tile of the output; W's 64 x 16 slabs and
-// the sources' 16 x 128 slabs go through shared memory in a four-stage cp.async
+// the sources' 16 x 128 slabs go through shared memory in a three-stage cp.async
 // ring, and each thread keeps 8 x 4 sums.  Every output sums its sources in
 // ascending order, skipping the ones that PAST excludes.
 template <bool TRANS, bool PAST = false>
@@ -275,9 +275,7 @@ int launch_mix(const float* W, const float* src, float* dst, int64_t M, int64_t 
   if (gx > 0x7fffffffLL || gy > 65535) return MHLA_ERR_UNSUPPORTED;
   const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
                   static_cast<unsigned>(std::min<int64_t>(BH, 65535)));
-  if (cudaFuncSetAttribute(simt_mix<TRANS, PAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kMixSmem)) != cudaSuccess)
-    return MHLA_ERR_CUDA;
+  static_assert(kMixSmem <= 48 * 1024, "no opt-in attribute needed");
   KernelTimer timer("simt_mix", stream);
   simt_mix<TRANS, PAST><<<grid, kMixThreads, kMixSmem, stream>>>(W, src, dst, M, E, BH);
   return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
