@@ -126,6 +126,16 @@ def test_causal_backward_both_ways_to_the_states(path, grid, block):
     check(f"{path}/{grid}/{block}", q, k, v, W, g, grid, block, "bf16", "relu_eps", 1e-6, path=path)
 
 
+def test_causal_backward_tc_states_past_the_resident_mixing():
+    """M = 320 blocks: the tensor-core mixing streams W instead of holding it in
+    shared memory; the summaries it reads must survive it for dW."""
+    B, N, H, d, grid, block = 1, 20480, 1, 64, (1, 20480), (1, 64)
+    q, k, v = draw_qkv(B, N, H, d, seed=99, dtype="bf16")
+    g = draw_dout((B, N, H, d), 100, "bf16")
+    W = draw_matrix(320, seed=101)
+    check("tc/M320", q, k, v, W, g, grid, block, "bf16", path="tc")
+
+
 def test_causal_backward_ignores_w_above_the_diagonal_and_is_deterministic():
     B, H, d, grid, block = 2, 2, 32, (1, 256), (1, 32)
     q, k, v = draw_qkv(B, 256, H, d, seed=84, dtype="f32")
