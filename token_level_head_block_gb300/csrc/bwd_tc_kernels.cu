@@ -1216,6 +1216,35 @@ int launch_tc_bwd(const Problem& p, const float* W, const BwdOperands& bo, void*
   return launch_tc_bwd_d<32>(p, W, bo, workspace, s);
 }
 
+int64_t tc_dw_part_floats(const Problem& p) {
+  const BwdLayout L = bwd_layout(p);
+  return static_cast<int64_t>(L.nsplit) * p.M * p.M;
+}
+
+int tc_run_dw(const Problem& p, const void* dSbuf, const void* Sbuf, float* part, float* dW, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const BwdLayout L = bwd_layout(p);
+  CUtensorMap ta, tb;
+  const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(L.ngroups)};
+  const cuuint64_t strides[2] = {256u, static_cast<cuuint64_t>(p.M * 256)};
+  const cuuint32_t abox[3] = {64u, static_cast<cuuint32_t>(DwCfg::IT), 1u};
+  const cuuint32_t bbox[3] = {64u, static_cast<cuuint32_t>(L.JN), 1u};
+  if (!encode_tensor_map(&ta, 3, const_cast<void*>(dSbuf), dims, strides, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map(&tb, 3, const_cast<void*>(Sbuf), dims, strides, bbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MHLA_ERR_CUDA;
+  if (cudaFuncSetAttribute(tc_dw, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(DwCfg::SMEM)) !=
+      cudaSuccess)
+    return MHLA_ERR_CUDA;
+  const int64_t ctas = static_cast<int64_t>(L.n_it) * L.n_jt * L.nsplit;
+  KernelTimer timer("tc_dw", s);
+  tc_dw<<<static_cast<unsigned>(ctas), kDwThreads, DwCfg::SMEM, s>>>(ta, tb, static_cast<int32_t>(p.M), L.n_jt, L.JN,
+                                                                     L.ngroups, L.nsplit, part);
+  if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  const int64_t MM = p.M * p.M;
+  tc_dw_reduce<<<static_cast<unsigned>((MM + kDwrOut - 1) / kDwrOut), 256, 0, s>>>(part, dW, MM, L.nsplit);
+  return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+}
+
 int read_and_clear_bwd_error(void* stream, uint32_t* flags) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned int host = 0;

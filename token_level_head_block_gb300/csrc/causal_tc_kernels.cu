@@ -619,7 +619,15 @@ int launch_tc_causal_states(const Problem& p, const float* W, void* region, void
   out->Sbuf = ws + L.sbuf_off;
   out->St = St;
   out->zt = zt;
+  out->Wu = Wu;
+  out->Mp = L.Mp;
   return rc;
+}
+
+int launch_tc_causal_mix(const Problem& p, const void* Wm, int64_t Mp, const void* Sbuf, void* St, float* zt,
+                         void* stream) {
+  const CtLayout L = ct_layout(p);
+  return tc_run_mix(unit_problem(p, L.U), Wm, Mp, Sbuf, St, zt, stream, /*discard_input=*/true);
 }
 
 int read_and_clear_causal_error(void* stream, uint32_t* flags) {

@@ -95,13 +95,24 @@ int launch_simt_causal_bwd(const Problem& p, const float* W, const BwdOperands& 
 // row of each group per block, entries S_j row-major then z_j) and the mixed
 // past S<_i (St: bf16 [BH][M][d][d] row-major; zt: float32 [BH][M][d]).
 struct CausalStates {
-  const void* Sbuf;
-  const void* St;
-  const float* zt;
+  void* Sbuf;
+  void* St;
+  float* zt;
+  void* Wu;      // bf16 [M][Mp]: the mixing matrix of the states, free for reuse after them
+  int64_t Mp;
 };
+// dW[i][j] = sum over every summary column of dSbuf[i] . Sbuf[j] (both in the
+// summary layout above, padding columns zero), by the tensor-core backward's
+// dW kernel; part holds tc_dw_part_floats(p) floats.
+int64_t tc_dw_part_floats(const Problem& p);
+int tc_run_dw(const Problem& p, const void* dSbuf, const void* Sbuf, float* part, float* dW, void* stream);
 bool tc_causal_states_eligible(const Problem& p);
 size_t tc_causal_states_bytes(const Problem& p);
 int launch_tc_causal_states(const Problem& p, const float* W, void* region, void* stream, CausalStates* out);
+// One mixing GEMM of the tensor-core causal forward on the same problem:
+// [St | zt] (its layout) = Wm (bf16 [M][Mp]) times the summary-layout Sbuf.
+int launch_tc_causal_mix(const Problem& p, const void* Wm, int64_t Mp, const void* Sbuf, void* St, float* zt,
+                         void* stream);
 
 // Tensor-core backward (bf16, d in {32, 64}, the forward tensor-core path's
 // token geometry, TMA-friendly strides on every operand).  Workspace: Wb and

@@ -1933,46 +1933,104 @@ int launch_simt_causal_typed(const Problem& p, const float* W, const SimtWorkspa
   }
 }
 
-// The tensor-core causal forward's block summaries and mixed past (bf16 Sbuf,
-// St; float32 zt) as the float32 [BH][M][d(d+1)] buffers of the kernels above:
-// Sz[bh][j][e] = Sbuf column bh d(d+1) + e of block j, Sp[bh][i] = S<_i row-major
-// then z<_i.  One CTA per (b, h, block), each thread eight consecutive entries
-// (d(d+1) and d^2 are multiples of 8 for d in {32, 64}, so an eight-entry run
-// stays inside one 128-column group of Sbuf and inside S< or z<).
+// Helpers of the causal backward's TC path, between the tensor-core causal
+// forward's layouts (Sbuf: bf16, the (b, h, entry) columns in groups of 128, one
+// row per block; St: bf16 [BH][M][d][d] row-major; zt: float32 [BH][M][d]) and
+// the float32 [BH][M][d(d+1)] rows of the token kernels.  One CTA per (b, h,
+// block), eight consecutive entries per thread: for d in {32, 64}, d(d+1) and d^2
+// are multiples of 8, so a run stays inside one 128-column group of Sbuf and
+// inside S or z.
 constexpr int kStThreads = 256;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 s, float4& lo, float4& hi) {
+  lo.x = __uint_as_float(s.x << 16), lo.y = __uint_as_float(s.x & 0xffff0000u);
+  lo.z = __uint_as_float(s.y << 16), lo.w = __uint_as_float(s.y & 0xffff0000u);
+  hi.x = __uint_as_float(s.z << 16), hi.y = __uint_as_float(s.z & 0xffff0000u);
+  hi.z = __uint_as_float(s.w << 16), hi.w = __uint_as_float(s.w & 0xffff0000u);
+}
+
+// Two floats rounded to bf16 (round to nearest even), packed low then high.
+__device__ __forceinline__ uint32_t pack_bf16_rn(float a, float b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+}
+
+// Sp[bh][i] = St[bh][i] row-major, then zt[bh][i].
 __global__ void __launch_bounds__(kStThreads)
-simt_states_from_tc(const __nv_bfloat16* __restrict__ Sbuf, const __nv_bfloat16* __restrict__ St,
-                    const float* __restrict__ zt, float* __restrict__ Sz, float* __restrict__ Sp, int64_t M, int d,
-                    int64_t items) {
+simt_states_to_f32(const __nv_bfloat16* __restrict__ St, const float* __restrict__ zt, float* __restrict__ Sp, int d,
+                   int64_t items) {
   const int E = d * d, E1 = E + d;
   for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-    const int64_t bh = it / M, j = it % M;
     for (int e = 8 * threadIdx.x; e < E1; e += 8 * kStThreads) {
-      const int64_t col = bh * E1 + e;
-      const uint4 sb = *reinterpret_cast<const uint4*>(Sbuf + ((col >> 7) * M + j) * 128 + (col & 127));
       float4 lo, hi;
-      lo.x = __uint_as_float(sb.x << 16), lo.y = __uint_as_float(sb.x & 0xffff0000u);
-      lo.z = __uint_as_float(sb.y << 16), lo.w = __uint_as_float(sb.y & 0xffff0000u);
-      hi.x = __uint_as_float(sb.z << 16), hi.y = __uint_as_float(sb.z & 0xffff0000u);
-      hi.z = __uint_as_float(sb.w << 16), hi.w = __uint_as_float(sb.w & 0xffff0000u);
-      float4* zdst = reinterpret_cast<float4*>(Sz + it * E1 + e);
-      zdst[0] = lo;
-      zdst[1] = hi;
       if (e < E) {
-        const uint4 s = *reinterpret_cast<const uint4*>(St + it * E + e);
-        lo.x = __uint_as_float(s.x << 16), lo.y = __uint_as_float(s.x & 0xffff0000u);
-        lo.z = __uint_as_float(s.y << 16), lo.w = __uint_as_float(s.y & 0xffff0000u);
-        hi.x = __uint_as_float(s.z << 16), hi.y = __uint_as_float(s.z & 0xffff0000u);
-        hi.z = __uint_as_float(s.w << 16), hi.w = __uint_as_float(s.w & 0xffff0000u);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(St + it * E + e), lo, hi);
       } else {
         const float4* z = reinterpret_cast<const float4*>(zt + it * d + (e - E));
         lo = z[0];
         hi = z[1];
       }
-      float4* pdst = reinterpret_cast<float4*>(Sp + it * E1 + e);
-      pdst[0] = lo;
-      pdst[1] = hi;
+      float4* dst = reinterpret_cast<float4*>(Sp + it * E1 + e);
+      dst[0] = lo;
+      dst[1] = hi;
     }
+  }
+}
+
+// dSbuf (summary layout) = dSp rounded to bf16; the padding columns of the last
+// group (past BH d(d+1)) are zeroed in dSbuf and in the forward's Sbuf, whose
+// whole groups the dW product reads.
+__global__ void __launch_bounds__(kStThreads)
+simt_ds_to_summary(const float* __restrict__ dSp, __nv_bfloat16* __restrict__ dSbuf, __nv_bfloat16* __restrict__ Sbuf,
+                   int64_t M, int d, int64_t BH, int64_t ngroups) {
+  const int E1 = d * d + d;
+  const int64_t items = BH * M;
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    const int64_t bh = it / M, i = it % M;
+    for (int e = 8 * threadIdx.x; e < E1; e += 8 * kStThreads) {
+      const int64_t col = bh * E1 + e;
+      const float4* src = reinterpret_cast<const float4*>(dSp + it * E1 + e);
+      const float4 lo = src[0], hi = src[1];
+      uint4 o;
+      o.x = pack_bf16_rn(lo.x, lo.y), o.y = pack_bf16_rn(lo.z, lo.w);
+      o.z = pack_bf16_rn(hi.x, hi.y), o.w = pack_bf16_rn(hi.z, hi.w);
+      *reinterpret_cast<uint4*>(dSbuf + ((col >> 7) * M + i) * 128 + (col & 127)) = o;
+    }
+    if (bh == BH - 1) {
+      const int64_t c0 = BH * E1, c1 = ngroups * 128;
+      for (int64_t col = c0 + threadIdx.x; col < c1; col += kStThreads) {
+        const int64_t at = ((col >> 7) * M + i) * 128 + (col & 127);
+        dSbuf[at] = __float2bfloat16_rn(0.0f);
+        Sbuf[at] = __float2bfloat16_rn(0.0f);
+      }
+    }
+  }
+}
+
+// Wm[j][i] = W[i][j] for i > j, else 0 (bf16 [M][Mp]): dS_j = sum_{i > j} W[i][j] dS<_i
+// as one mixing GEMM.
+__global__ void simt_w_strict_lower_t(const float* __restrict__ W, __nv_bfloat16* __restrict__ Wm, int64_t M,
+                                      int64_t Mp) {
+  const int64_t n = M * Mp;
+  for (int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < n;
+       x += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t j = x / Mp, i = x % Mp;
+    Wm[x] = __float2bfloat16_rn(i < M && i > j ? W[i * M + j] : 0.0f);
+  }
+}
+
+// dW of the full product (every (i, j)) made causal: the query kernel's W_ii
+// shares on the diagonal (summed over (b, h) in order), zero above it.
+__global__ void simt_dw_causal_fix(float* __restrict__ dW, const float* __restrict__ diag, int64_t M, int64_t BH) {
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (x >= M * M) return;
+  const int64_t i = x / M, j = x % M;
+  if (j > i) {
+    dW[x] = 0.0f;
+  } else if (j == i) {
+    float s = 0.0f;
+    for (int64_t bh = 0; bh < BH; ++bh) s += diag[bh * M + i];
+    dW[x] = s;
   }
 }
 
@@ -1984,6 +2042,7 @@ struct SimtCausalBwdWorkspace {
   float* diag;   // [BH][M]          the (b, h) share of dW_ii
   float* dn;     // [BH][N][d + 1]   dnum_t, dden_t in block-slot order
   void* tc;      // the region of launch_tc_causal_states (tensor-core summaries and mixing), or null
+  float* tcpart; // the tensor-core dW product's split partials (path TC)
 };
 
 SimtCausalBwdWorkspace simt_causal_bwd_carve(const Problem& p, void* base) {
@@ -1999,6 +2058,7 @@ SimtCausalBwdWorkspace simt_causal_bwd_carve(const Problem& p, void* base) {
   ws.diag = reinterpret_cast<float*>(c + 3 * align_up(per) + align_up(part));
   ws.dn = reinterpret_cast<float*>(c + 3 * align_up(per) + align_up(part) + align_up(diag));
   ws.tc = nullptr;
+  ws.tcpart = nullptr;
   return ws;
 }
 
@@ -2018,14 +2078,19 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
   T* dkp = static_cast<T*>(bo.dk.data);
   T* dvp = static_cast<T*>(bo.dv.data);
   const int64_t E = p.d * (p.d + 1);
-  if (ws.tc) {   // S_j and S<_i from the tensor-core causal forward's summary and mixing kernels
-    CausalStates cs;
+  // path TC: S_j (kept in the summary layout) and S<_i from the tensor-core causal
+  // forward's summary and mixing kernels; later the dW product and the mixing of
+  // dS on the tensor cores as well
+  CausalStates cs{};
+  auto to_f32 = [&]() -> int {
+    KernelTimer timer("simt_states_to_f32", stream);
+    simt_states_to_f32<<<static_cast<unsigned>(items), kStThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(cs.St), cs.zt, ws.Sp, d, items);
+    return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+  };
+  if (ws.tc) {
     if (const int rc = launch_tc_causal_states(p, W, ws.tc, stream, &cs); rc != MHLA_OK) return rc;
-    KernelTimer timer("simt_states_from_tc", stream);
-    simt_states_from_tc<<<static_cast<unsigned>(items), kStThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(cs.Sbuf),
-                                                         static_cast<const __nv_bfloat16*>(cs.St), cs.zt, ws.Sz,
-                                                         ws.Sp, p.M, d, items);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+    if (const int rc = to_f32(); rc != MHLA_OK) return rc;
   } else {
     if (const int rc = launch_summary<T>(p, g, ws.Sz, stream); rc != MHLA_OK) return rc;
     if (const int rc = launch_mix<false, true>(W, ws.Sz, ws.Sp, p.M, E, BH, stream); rc != MHLA_OK)
@@ -2063,21 +2128,51 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
                              : launch(simt_causal_bwd_query<T, 64, 8>);
     if (rc != MHLA_OK) return rc;
   }
-  {
-    const int64_t KS = dw_splits(p);
-    const dim3 grid(static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile),
-                    static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile), static_cast<unsigned>(BH * KS));
-    if (grid.x > 65535 || BH * KS > 65535) return MHLA_ERR_UNSUPPORTED;
-    KernelTimer timer("simt_dw", stream);
-    simt_dw_partial<<<grid, 256, 0, stream>>>(ws.dSp, ws.Sz, ws.part, p.M, E, static_cast<int32_t>(KS));
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-    const int64_t MM = p.M * p.M;
-    simt_dw_reduce_causal<<<static_cast<unsigned>((MM + 31) / 32), kDwrWarps * 32, 0, stream>>>(
-        ws.part, ws.diag, bo.dW, p.M, BH, KS);
-    if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+  const int64_t MM = p.M * p.M;
+  if (ws.tc) {
+    // dS<_i into the summary layout (over the float32 S_j buffer, unused on this
+    // path); dW = <dS<_i, S_j> for every (i, j) on the tensor cores, then made
+    // causal; dS_j = sum_{i > j} W[i][j] dS<_i as a mixing GEMM with W's strict
+    // lower triangle transposed (in the states' matrix slot), back to float32
+    auto* dSbuf = reinterpret_cast<__nv_bfloat16*>(ws.Sz);
+    const int64_t ngroups = (BH * E + 127) / 128;
+    {
+      KernelTimer timer("simt_ds_to_summary", stream);
+      simt_ds_to_summary<<<static_cast<unsigned>(items), kStThreads, 0, stream>>>(
+          ws.dSp, dSbuf, static_cast<__nv_bfloat16*>(cs.Sbuf), p.M, d, BH, ngroups);
+      if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+    }
+    if (const int rc = tc_run_dw(p, dSbuf, cs.Sbuf, ws.tcpart, bo.dW, stream); rc != MHLA_OK) return rc;
+    {
+      KernelTimer timer("simt_dw_causal_fix", stream);
+      simt_dw_causal_fix<<<static_cast<unsigned>((MM + 255) / 256), 256, 0, stream>>>(bo.dW, ws.diag, p.M, BH);
+      if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+    }
+    {
+      const int64_t n = p.M * cs.Mp;
+      KernelTimer timer("simt_w_strict_lower_t", stream);
+      simt_w_strict_lower_t<<<static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 65535)), 256, 0, stream>>>(
+          W, static_cast<__nv_bfloat16*>(cs.Wu), p.M, cs.Mp);
+      if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+    }
+    if (const int rc = launch_tc_causal_mix(p, cs.Wu, cs.Mp, dSbuf, cs.St, cs.zt, stream); rc != MHLA_OK) return rc;
+    if (const int rc = to_f32(); rc != MHLA_OK) return rc;
+  } else {
+    {
+      const int64_t KS = dw_splits(p);
+      const dim3 grid(static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile),
+                      static_cast<unsigned>((p.M + kDwTile - 1) / kDwTile), static_cast<unsigned>(BH * KS));
+      if (grid.x > 65535 || BH * KS > 65535) return MHLA_ERR_UNSUPPORTED;
+      KernelTimer timer("simt_dw", stream);
+      simt_dw_partial<<<grid, 256, 0, stream>>>(ws.dSp, ws.Sz, ws.part, p.M, E, static_cast<int32_t>(KS));
+      if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+      simt_dw_reduce_causal<<<static_cast<unsigned>((MM + 31) / 32), kDwrWarps * 32, 0, stream>>>(
+          ws.part, ws.diag, bo.dW, p.M, BH, KS);
+      if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
+    }
+    if (const int rc = launch_mix<true, true>(W, ws.dSp, ws.Sp, p.M, E, BH, stream); rc != MHLA_OK)
+      return rc;
   }
-  if (const int rc = launch_mix<true, true>(W, ws.dSp, ws.Sp, p.M, E, BH, stream); rc != MHLA_OK)
-    return rc;
   {
     const size_t smem = (d * (d + 1) + d + 4 * kCbChunk * (d + 1) + kCbChunk + 2 * kCbChunk * (kCbChunk + 1)) *
                         sizeof(float);
@@ -2165,13 +2260,17 @@ size_t simt_causal_bwd_own_bytes(const Problem& p) {
 }  // namespace
 
 size_t simt_causal_bwd_workspace_bytes(const Problem& p, bool tc_states) {
-  return simt_causal_bwd_own_bytes(p) + (tc_states ? align_up(tc_causal_states_bytes(p)) : 0);
+  return simt_causal_bwd_own_bytes(p) +
+         (tc_states ? align_up(tc_causal_states_bytes(p)) + align_up(tc_dw_part_floats(p) * sizeof(float)) : 0);
 }
 
 int launch_simt_causal_bwd(const Problem& p, const float* W, const BwdOperands& bo, void* workspace, void* stream,
                            bool tc_states) {
   SimtCausalBwdWorkspace ws = simt_causal_bwd_carve(p, workspace);
-  if (tc_states) ws.tc = static_cast<char*>(workspace) + simt_causal_bwd_own_bytes(p);
+  if (tc_states) {
+    ws.tc = static_cast<char*>(workspace) + simt_causal_bwd_own_bytes(p);
+    ws.tcpart = reinterpret_cast<float*>(static_cast<char*>(ws.tc) + align_up(tc_causal_states_bytes(p)));
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p.dtype == MHLA_BF16) return launch_simt_causal_bwd_typed<__nv_bfloat16>(p, W, bo, ws, s);
   return launch_simt_causal_bwd_typed<float>(p, W, bo, ws, s);
