@@ -174,7 +174,7 @@ KERNEL_SOURCES = {"tc_summary": ("tc_summary.cu", "tc_fwd_bodies.cuh"), "tc_mix"
                   "simt_causal_output": "simt_kernels.cu", "tc_causal_tile": "causal_tc_kernels.cu",
                   "simt_causal_bwd_query": "simt_kernels.cu", "simt_causal_bwd_key": "simt_kernels.cu",
                   "simt_states_to_f32": "simt_kernels.cu", "simt_ds_to_summary": "simt_kernels.cu",
-                  "simt_w_strict_lower_t": "simt_kernels.cu", "simt_dw_causal_fix": "simt_kernels.cu",
+                  "simt_dw_causal_and_wt": "simt_kernels.cu",
                   "tc_tile_output": "causal_tc_kernels.cu", "mhla_lepe_add": "module_kernels.cu",
                   "mhla_ln_rows": "module_kernels.cu", "mhla_gemm_qkv": "gemm_kernels.cu",
                   "mhla_gemm_out": "gemm_kernels.cu"}
@@ -233,8 +233,7 @@ def kernel_work(wl, name):
         # bf16 summary layout; W's strict lower triangle transposed; dW made causal
         "simt_states_to_f32": ("hbm", BH * M * (d * d * 2 + d * 4 + d * (d + 1) * 4)),
         "simt_ds_to_summary": ("hbm", BH * M * d * (d + 1) * (4 + 2)),
-        "simt_w_strict_lower_t": ("hbm", M * M * (4 + 2)),
-        "simt_dw_causal_fix": ("hbm", 2 * M * M * 4 + BH * M * 4),
+        "simt_dw_causal_and_wt": ("hbm", M * M * (4 + 2) + 2 * M * M * 4 + BH * M * 4),
         # readout of contiguous 64-token blocks: read q, write o
         "tc_tile_output": ("hbm", 2 * io),
         # module: x -> LayerNorm; qkv = xn W^T; o += lepe(v) (read v, o; write o); y = o W^T

@@ -2007,30 +2007,29 @@ simt_ds_to_summary(const float* __restrict__ dSp, __nv_bfloat16* __restrict__ dS
   }
 }
 
-// Wm[j][i] = W[i][j] for i > j, else 0 (bf16 [M][Mp]): dS_j = sum_{i > j} W[i][j] dS<_i
-// as one mixing GEMM.
-__global__ void simt_w_strict_lower_t(const float* __restrict__ W, __nv_bfloat16* __restrict__ Wm, int64_t M,
-                                      int64_t Mp) {
+// Between the dW product and the mixing of dS, one pass over M x M:
+//   dW made causal: the query kernel's W_ii shares on the diagonal (summed over
+//   (b, h) in order), zero above it (the product below it stays);
+//   Wm[j][i] = W[i][j] for i > j, else 0 (bf16 [M][Mp]), so that
+//   dS_j = sum_{i > j} W[i][j] dS<_i is one mixing GEMM.
+__global__ void simt_dw_causal_and_wt(float* __restrict__ dW, const float* __restrict__ diag,
+                                      const float* __restrict__ W, __nv_bfloat16* __restrict__ Wm, int64_t M,
+                                      int64_t Mp, int64_t BH) {
   const int64_t n = M * Mp;
   for (int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < n;
        x += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t j = x / Mp, i = x % Mp;
-    Wm[x] = __float2bfloat16_rn(i < M && i > j ? W[i * M + j] : 0.0f);
-  }
-}
-
-// dW of the full product (every (i, j)) made causal: the query kernel's W_ii
-// shares on the diagonal (summed over (b, h) in order), zero above it.
-__global__ void simt_dw_causal_fix(float* __restrict__ dW, const float* __restrict__ diag, int64_t M, int64_t BH) {
-  const int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (x >= M * M) return;
-  const int64_t i = x / M, j = x % M;
-  if (j > i) {
-    dW[x] = 0.0f;
-  } else if (j == i) {
-    float s = 0.0f;
-    for (int64_t bh = 0; bh < BH; ++bh) s += diag[bh * M + i];
-    dW[x] = s;
+    const int64_t r = x / Mp, c = x % Mp;
+    Wm[x] = __float2bfloat16_rn(c < M && c > r ? W[c * M + r] : 0.0f);
+    if (c < M) {
+      float* out = dW + r * M + c;
+      if (c > r) {
+        *out = 0.0f;
+      } else if (c == r) {
+        float s = 0.0f;
+        for (int64_t bh = 0; bh < BH; ++bh) s += diag[bh * M + r];
+        *out = s;
+      }
+    }
   }
 }
 
@@ -2144,15 +2143,10 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
     }
     if (const int rc = tc_run_dw(p, dSbuf, cs.Sbuf, ws.tcpart, bo.dW, stream); rc != MHLA_OK) return rc;
     {
-      KernelTimer timer("simt_dw_causal_fix", stream);
-      simt_dw_causal_fix<<<static_cast<unsigned>((MM + 255) / 256), 256, 0, stream>>>(bo.dW, ws.diag, p.M, BH);
-      if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
-    }
-    {
       const int64_t n = p.M * cs.Mp;
-      KernelTimer timer("simt_w_strict_lower_t", stream);
-      simt_w_strict_lower_t<<<static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 65535)), 256, 0, stream>>>(
-          W, static_cast<__nv_bfloat16*>(cs.Wu), p.M, cs.Mp);
+      KernelTimer timer("simt_dw_causal_and_wt", stream);
+      simt_dw_causal_and_wt<<<static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 65535)), 256, 0, stream>>>(
+          bo.dW, ws.diag, W, static_cast<__nv_bfloat16*>(cs.Wu), p.M, cs.Mp, BH);
       if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
     }
     if (const int rc = launch_tc_causal_mix(p, cs.Wu, cs.Mp, dSbuf, cs.St, cs.zt, stream); rc != MHLA_OK) return rc;
