@@ -2008,28 +2008,29 @@ simt_ds_to_summary(const float* __restrict__ dSp, __nv_bfloat16* __restrict__ dS
 }
 
 // Between the dW product and the mixing of dS, one pass over M x M:
-//   dW made causal: the query kernel's W_ii shares on the diagonal (summed over
-//   (b, h) in order), zero above it (the product below it stays);
+//   dW made causal: zero above the diagonal (the product below it stays), and on
+//   it the query kernel's W_ii shares summed over (b, h) by one warp per
+//   diagonal entry (lane-strided, then a fixed-order shuffle sum);
 //   Wm[j][i] = W[i][j] for i > j, else 0 (bf16 [M][Mp]), so that
 //   dS_j = sum_{i > j} W[i][j] dS<_i is one mixing GEMM.
+// The grid covers max(M Mp, 32 M) threads in whole warps.
 __global__ void simt_dw_causal_and_wt(float* __restrict__ dW, const float* __restrict__ diag,
                                       const float* __restrict__ W, __nv_bfloat16* __restrict__ Wm, int64_t M,
                                       int64_t Mp, int64_t BH) {
-  const int64_t n = M * Mp;
-  for (int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < n;
-       x += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (x < M * Mp) {
     const int64_t r = x / Mp, c = x % Mp;
     Wm[x] = __float2bfloat16_rn(c < M && c > r ? W[c * M + r] : 0.0f);
-    if (c < M) {
-      float* out = dW + r * M + c;
-      if (c > r) {
-        *out = 0.0f;
-      } else if (c == r) {
-        float s = 0.0f;
-        for (int64_t bh = 0; bh < BH; ++bh) s += diag[bh * M + r];
-        *out = s;
-      }
-    }
+    if (c < M && c > r) dW[r * M + c] = 0.0f;
+  }
+  if (x < 32 * M) {   // whole warps: 32 M is a multiple of the warp
+    const int64_t r = x / 32;
+    const int lane = static_cast<int>(x % 32);
+    float s = 0.0f;
+    for (int64_t bh = lane; bh < BH; bh += 32) s += diag[bh * M + r];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) dW[r * M + r] = s;
   }
 }
 
@@ -2143,9 +2144,10 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
     }
     if (const int rc = tc_run_dw(p, dSbuf, cs.Sbuf, ws.tcpart, bo.dW, stream); rc != MHLA_OK) return rc;
     {
-      const int64_t n = p.M * cs.Mp;
+      const int64_t n = std::max<int64_t>(p.M * cs.Mp, 32 * p.M);
+      if ((n + 255) / 256 > 0x7fffffffLL) return MHLA_ERR_UNSUPPORTED;
       KernelTimer timer("simt_dw_causal_and_wt", stream);
-      simt_dw_causal_and_wt<<<static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 65535)), 256, 0, stream>>>(
+      simt_dw_causal_and_wt<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
           bo.dW, ws.diag, W, static_cast<__nv_bfloat16*>(cs.Wu), p.M, cs.Mp, BH);
       if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
     }
