@@ -173,7 +173,7 @@ KERNEL_SOURCES = {"tc_summary": ("tc_summary.cu", "tc_fwd_bodies.cuh"), "tc_mix"
                   "simt_bwd_key": "simt_kernels.cu", "simt_dw": "simt_kernels.cu",
                   "simt_causal_output": "simt_kernels.cu", "tc_causal_tile": "causal_tc_kernels.cu",
                   "simt_causal_bwd_query": "simt_kernels.cu", "simt_causal_bwd_key": "simt_kernels.cu",
-                  "simt_states_to_f32": "simt_kernels.cu", "simt_ds_to_summary": "simt_kernels.cu",
+                  "simt_ds_to_summary": "simt_kernels.cu",
                   "simt_dw_causal_and_wt": "simt_kernels.cu",
                   "tc_tile_output": "causal_tc_kernels.cu", "mhla_lepe_add": "module_kernels.cu",
                   "mhla_ln_rows": "module_kernels.cu", "mhla_gemm_qkv": "gemm_kernels.cu",
@@ -229,9 +229,8 @@ def kernel_work(wl, name):
         # rows; read q, k, v and those rows, write dk, dv
         "simt_causal_bwd_query": ("hbm", 5 * io + BH * wl.N * (d + 1) * 4),
         "simt_causal_bwd_key": ("hbm", 5 * io + BH * wl.N * (d + 1) * 4),
-        # causal backward, path TC: states (bf16 S, float32 z) to float32 rows; dS< to the
-        # bf16 summary layout; W's strict lower triangle transposed; dW made causal
-        "simt_states_to_f32": ("hbm", BH * M * (d * d * 2 + d * 4 + d * (d + 1) * 4)),
+        # causal backward, path TC: dS< to the bf16 summary layout; dW made causal and
+        # W's strict lower triangle transposed
         "simt_ds_to_summary": ("hbm", BH * M * d * (d + 1) * (4 + 2)),
         "simt_dw_causal_and_wt": ("hbm", M * M * (4 + 2) + 2 * M * M * 4 + BH * M * 4),
         # readout of contiguous 64-token blocks: read q, write o

@@ -1231,7 +1231,8 @@ simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict
                         const T* __restrict__ v, Operand vo, const T* __restrict__ g_out, Operand go,
                         T* __restrict__ dq, Operand dqo, TokenGeom g, int64_t H, int phi_kind, float eps,
                         const float* __restrict__ W, const float* __restrict__ Sp, float* __restrict__ dSp,
-                        float* __restrict__ diag, float* __restrict__ dn) {
+                        float* __restrict__ diag, float* __restrict__ dn, const __nv_bfloat16* __restrict__ Stb,
+                        const float* __restrict__ ztb) {
   constexpr int V = D / 16;
   constexpr int P = D + 4;                 // padded token / state row
   constexpr int CP = kCbChunk + 4;         // padded row of a 32 x 32 token-pair matrix
@@ -1253,9 +1254,17 @@ simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict
   const int64_t b = bh / H, h = bh % H;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const float wii = __ldg(W + i * g.M + i);
-  const float* src = Sp + (bh * g.M + i) * static_cast<int64_t>(E + D);
-  for (int e = tid; e < E; e += kCbThreads) stT[(e % D) * P + e / D] = src[e];
-  for (int r = tid; r < D; r += kCbThreads) zs[r] = src[E + r];
+  // S<_i and z<_i: float32 rows of Sp, or (Stb non-null) the tensor-core states
+  // (bf16 row-major S<_i, float32 z<_i)
+  const int64_t si = bh * g.M + i;
+  if (Stb) {
+    for (int e = tid; e < E; e += kCbThreads) stT[(e % D) * P + e / D] = __bfloat162float(Stb[si * E + e]);
+    for (int r = tid; r < D; r += kCbThreads) zs[r] = ztb[si * D + r];
+  } else {
+    const float* src = Sp + si * static_cast<int64_t>(E + D);
+    for (int e = tid; e < E; e += kCbThreads) stT[(e % D) * P + e / D] = src[e];
+    for (int r = tid; r < D; r += kCbThreads) zs[r] = src[E + r];
+  }
   const T* qb = q + b * qo.sb + h * qo.sh;
   const T* kb = k + b * ko.sb + h * ko.sh;
   const T* vb = v + b * vo.sb + h * vo.sh;
@@ -1553,7 +1562,8 @@ __global__ void __launch_bounds__(kCbThreads, 2)
 simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__ k, Operand ko,
                       const T* __restrict__ v, Operand vo, T* __restrict__ dk, Operand dko, T* __restrict__ dv,
                       Operand dvo, TokenGeom g, int64_t H, int phi_kind, float eps, const float* __restrict__ W,
-                      const float* __restrict__ dS, const float* __restrict__ dn) {
+                      const float* __restrict__ dS, const float* __restrict__ dn,
+                      const __nv_bfloat16* __restrict__ Stb, const float* __restrict__ ztb) {
   constexpr int V = D / 16;
   constexpr int P = D + 4;
   constexpr int CP = kCbChunk + 4;
@@ -1574,14 +1584,17 @@ simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__
   const int64_t b = bh / H, h = bh % H;
   const int tid = threadIdx.x;
   const float wjj = __ldg(W + j * g.M + j);
-  const float* src = dS + (bh * g.M + j) * static_cast<int64_t>(E + D);
+  // dS_j and dz_j: float32 rows of dS, or (Stb non-null) the tensor-core mixing's
+  // output (bf16 row-major dS_j, float32 dz_j)
+  const int64_t sj = bh * g.M + j;
+  const float* src = dS + sj * static_cast<int64_t>(E + D);
   for (int e = tid; e < E; e += kCbThreads) {
     const int r = e / D, c = e % D;
-    const float x = src[e];
+    const float x = Stb ? __bfloat162float(Stb[sj * E + e]) : src[e];
     gs[r * P + c] = x;
     gsT[c * P + r] = x;
   }
-  for (int r = tid; r < D; r += kCbThreads) gz[r] = src[E + r];
+  for (int r = tid; r < D; r += kCbThreads) gz[r] = Stb ? ztb[sj * D + r] : src[E + r];
   const T* qb = q + b * qo.sb + h * qo.sh;
   const T* kb = k + b * ko.sb + h * ko.sh;
   const T* vb = v + b * vo.sb + h * vo.sh;
@@ -1933,48 +1946,17 @@ int launch_simt_causal_typed(const Problem& p, const float* W, const SimtWorkspa
   }
 }
 
-// Helpers of the causal backward's TC path, between the tensor-core causal
-// forward's layouts (Sbuf: bf16, the (b, h, entry) columns in groups of 128, one
-// row per block; St: bf16 [BH][M][d][d] row-major; zt: float32 [BH][M][d]) and
-// the float32 [BH][M][d(d+1)] rows of the token kernels.  One CTA per (b, h,
-// block), eight consecutive entries per thread: for d in {32, 64}, d(d+1) and d^2
-// are multiples of 8, so a run stays inside one 128-column group of Sbuf and
-// inside S or z.
+// Helpers of the causal backward's TC path, between the float32 [BH][M][d(d+1)]
+// rows of the token kernels and the tensor-core causal forward's summary layout
+// (Sbuf: bf16, the (b, h, entry) columns in groups of 128, one row per block).
+// One CTA per (b, h, block), eight consecutive entries per thread: for d in
+// {32, 64}, d(d+1) is a multiple of 8, so a run stays inside one 128-column group.
 constexpr int kStThreads = 256;
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 s, float4& lo, float4& hi) {
-  lo.x = __uint_as_float(s.x << 16), lo.y = __uint_as_float(s.x & 0xffff0000u);
-  lo.z = __uint_as_float(s.y << 16), lo.w = __uint_as_float(s.y & 0xffff0000u);
-  hi.x = __uint_as_float(s.z << 16), hi.y = __uint_as_float(s.z & 0xffff0000u);
-  hi.z = __uint_as_float(s.w << 16), hi.w = __uint_as_float(s.w & 0xffff0000u);
-}
 
 // Two floats rounded to bf16 (round to nearest even), packed low then high.
 __device__ __forceinline__ uint32_t pack_bf16_rn(float a, float b) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
-}
-
-// Sp[bh][i] = St[bh][i] row-major, then zt[bh][i].
-__global__ void __launch_bounds__(kStThreads)
-simt_states_to_f32(const __nv_bfloat16* __restrict__ St, const float* __restrict__ zt, float* __restrict__ Sp, int d,
-                   int64_t items) {
-  const int E = d * d, E1 = E + d;
-  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-    for (int e = 8 * threadIdx.x; e < E1; e += 8 * kStThreads) {
-      float4 lo, hi;
-      if (e < E) {
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(St + it * E + e), lo, hi);
-      } else {
-        const float4* z = reinterpret_cast<const float4*>(zt + it * d + (e - E));
-        lo = z[0];
-        hi = z[1];
-      }
-      float4* dst = reinterpret_cast<float4*>(Sp + it * E1 + e);
-      dst[0] = lo;
-      dst[1] = hi;
-    }
-  }
 }
 
 // dSbuf (summary layout) = dSp rounded to bf16; the padding columns of the last
@@ -2082,15 +2064,8 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
   // forward's summary and mixing kernels; later the dW product and the mixing of
   // dS on the tensor cores as well
   CausalStates cs{};
-  auto to_f32 = [&]() -> int {
-    KernelTimer timer("simt_states_to_f32", stream);
-    simt_states_to_f32<<<static_cast<unsigned>(items), kStThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(cs.St), cs.zt, ws.Sp, d, items);
-    return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
-  };
-  if (ws.tc) {
+  if (ws.tc) {   // the token kernels read S<_i (later dS_j) from the tensor-core layout
     if (const int rc = launch_tc_causal_states(p, W, ws.tc, stream, &cs); rc != MHLA_OK) return rc;
-    if (const int rc = to_f32(); rc != MHLA_OK) return rc;
   } else {
     if (const int rc = launch_summary<T>(p, g, ws.Sz, stream); rc != MHLA_OK) return rc;
     if (const int rc = launch_mix<false, true>(W, ws.Sz, ws.Sp, p.M, E, BH, stream); rc != MHLA_OK)
@@ -2117,7 +2092,7 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
       KernelTimer timer("simt_causal_bwd_query", stream);
       kern<<<static_cast<unsigned>(items), kCbThreads, vsmem, stream>>>(
           qp, p.q, kp, p.k, vp, p.v, gp, bo.dout, dqp, bo.dq, g, p.H, p.phi_kind, p.eps, W, ws.Sp, ws.dSp,
-          ws.diag, ws.dn);
+          ws.diag, ws.dn, static_cast<const __nv_bfloat16*>(cs.St), cs.zt);
       return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
     };
     const int rc = d == 64   ? launch_v(simt_causal_bwd_query_v<T, 64>, cbv_query_smem(64))
@@ -2152,7 +2127,6 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
       if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
     }
     if (const int rc = launch_tc_causal_mix(p, cs.Wu, cs.Mp, dSbuf, cs.St, cs.zt, stream); rc != MHLA_OK) return rc;
-    if (const int rc = to_f32(); rc != MHLA_OK) return rc;
   } else {
     {
       const int64_t KS = dw_splits(p);
@@ -2187,7 +2161,8 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
         return MHLA_ERR_CUDA;
       KernelTimer timer("simt_causal_bwd_key", stream);
       kern<<<static_cast<unsigned>(items), kCbThreads, vsmem, stream>>>(
-          qp, p.q, kp, p.k, vp, p.v, dkp, bo.dk, dvp, bo.dv, g, p.H, p.phi_kind, p.eps, W, ws.Sp, ws.dn);
+          qp, p.q, kp, p.k, vp, p.v, dkp, bo.dk, dvp, bo.dv, g, p.H, p.phi_kind, p.eps, W, ws.Sp, ws.dn,
+          static_cast<const __nv_bfloat16*>(cs.St), cs.zt);
       return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
     };
     return d == 64   ? launch_v(simt_causal_bwd_key_v<T, 64>, cbv_key_smem(64))
