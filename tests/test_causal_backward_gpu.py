@@ -126,6 +126,20 @@ def test_causal_backward_both_ways_to_the_states(path, grid, block):
     check(f"{path}/{grid}/{block}", q, k, v, W, g, grid, block, "bf16", "relu_eps", 1e-6, path=path)
 
 
+def test_causal_backward_tc_path_padding_columns_and_repeatability():
+    """B H = 3 at d = 64: the summary layout's last 128-column group is half
+    padding, which the dW product reads and must see as zero; and the TC path's
+    reductions run in a fixed order, so two calls agree bit for bit."""
+    B, N, H, d, grid, block = 1, 512, 3, 64, (1, 512), (1, 64)
+    q, k, v = draw_qkv(B, N, H, d, seed=102, dtype="bf16")
+    g = draw_dout((B, N, H, d), 103, "bf16")
+    W = draw_matrix(8, seed=104)
+    a = check("tc/BH3", q, k, v, W, g, grid, block, "bf16", path="tc")
+    b = run(q, k, v, W, g, grid, block, path="tc")
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
 def test_causal_backward_tc_states_past_the_resident_mixing():
     """M = 320 blocks: the tensor-core mixing streams W instead of holding it in
     shared memory; the summaries it reads must survive it for dW."""
