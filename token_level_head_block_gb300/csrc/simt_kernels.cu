@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "mhla_internal.h"
 
@@ -1552,6 +1553,397 @@ simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict
   }
 }
 
+// Warp-level bf16 tensor-core products for the causal backward's per-chunk
+// steps (PTX mma.sync m16n8k16, float32 accumulation).  Fragments are built from
+// float32 shared memory, rounded to bf16 (round to nearest even): with
+// g = lane / 4 and t = lane % 4, A holds rows g, g + 8 at columns 2t, 2t + 1 and
+// 2t + 8, 2t + 9; B holds column g at rows 2t, 2t + 1 and 2t + 8, 2t + 9; the
+// accumulator holds rows g, g + 8 at columns 2t, 2t + 1.
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// A[m][k] = s[(m0 + m) ld + k0 + k]: rows of A, k contiguous (ld even)
+__device__ __forceinline__ void frag_a_rows(const float* s, int ld, int m0, int k0, int lane, uint32_t (&a)[4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const float* p = s + (m0 + g) * ld + k0 + 2 * t;
+  const float2 x0 = *reinterpret_cast<const float2*>(p);
+  const float2 x1 = *reinterpret_cast<const float2*>(p + 8 * ld);
+  const float2 x2 = *reinterpret_cast<const float2*>(p + 8);
+  const float2 x3 = *reinterpret_cast<const float2*>(p + 8 * ld + 8);
+  a[0] = bf16x2(x0.x, x0.y);
+  a[1] = bf16x2(x1.x, x1.y);
+  a[2] = bf16x2(x2.x, x2.y);
+  a[3] = bf16x2(x3.x, x3.y);
+}
+// A[m][k] = s[(k0 + k) ld + m0 + m]: the transpose of rows of k, m contiguous
+__device__ __forceinline__ void frag_a_cols(const float* s, int ld, int m0, int k0, int lane, uint32_t (&a)[4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const float* p = s + (k0 + 2 * t) * ld + m0 + g;
+  a[0] = bf16x2(p[0], p[ld]);
+  a[1] = bf16x2(p[8], p[ld + 8]);
+  a[2] = bf16x2(p[8 * ld], p[9 * ld]);
+  a[3] = bf16x2(p[8 * ld + 8], p[9 * ld + 8]);
+}
+// B[k][n] = s[(n0 + n) ld + k0 + k]: rows of n, k contiguous (ld even)
+__device__ __forceinline__ void frag_b_rows(const float* s, int ld, int n0, int k0, int lane, uint32_t (&b)[2]) {
+  const int g = lane >> 2, t = lane & 3;
+  const float* p = s + (n0 + g) * ld + k0 + 2 * t;
+  const float2 x0 = *reinterpret_cast<const float2*>(p);
+  const float2 x1 = *reinterpret_cast<const float2*>(p + 8);
+  b[0] = bf16x2(x0.x, x0.y);
+  b[1] = bf16x2(x1.x, x1.y);
+}
+// B[k][n] = s[(k0 + k) ld + n0 + n]: rows of k, n contiguous
+__device__ __forceinline__ void frag_b_cols(const float* s, int ld, int n0, int k0, int lane, uint32_t (&b)[2]) {
+  const int g = lane >> 2, t = lane & 3;
+  const float* p = s + (k0 + 2 * t) * ld + n0 + g;
+  b[0] = bf16x2(p[0], p[ld]);
+  b[1] = bf16x2(p[8 * ld], p[9 * ld]);
+}
+
+// The causal backward's query side for bf16 inputs and d = D in {32, 64}: the
+// arithmetic of simt_causal_bwd_query_v with its products on warp-level tensor
+// cores (operands rounded to bf16 from the float32 rows in shared memory,
+// float32 accumulation): the pair dots a = phi(Q) phi(K)^T and e = G V^T,
+// u = G C^T, the b sum B phi(K), and per chunk X = phi(Q)^T dnum and
+// phi(K)^T V.  The per-token steps (den, g . num, dnum, dden, b, dq) stay on CUDA
+// cores between them; the state C is kept row-major, and each warp owns a fixed
+// set of 16 x 8 tiles of X, of dS<_i and of the prefix state P.
+template <int D>
+__global__ void __launch_bounds__(kCbThreads, 2)
+simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const __nv_bfloat16* __restrict__ k,
+                          Operand ko, const __nv_bfloat16* __restrict__ v, Operand vo,
+                          const __nv_bfloat16* __restrict__ g_out, Operand go, __nv_bfloat16* __restrict__ dq,
+                          Operand dqo, TokenGeom g, int64_t H, int phi_kind, float eps, const float* __restrict__ W,
+                          const float* __restrict__ Sp, float* __restrict__ dSp, float* __restrict__ diag,
+                          float* __restrict__ dn, const __nv_bfloat16* __restrict__ Stb,
+                          const float* __restrict__ ztb) {
+  constexpr int V = D / 16;
+  constexpr int P = D + 4;                 // padded token / state row (even: 8-byte fragment loads)
+  constexpr int CP = kCbChunk + 4;         // padded row of a 32 x 32 token-pair matrix
+  constexpr int E = D * D, PD = D + 1;     // PD: the dnum / dden scratch row
+  constexpr int NMT = D / 16, NNT = D / 8; // 16 x 8 tiles of a D x D state
+  constexpr int WPM = kCbWarps / NMT;      // warps per row tile of the state
+  constexpr int NPW = NNT / WPM;           // state tiles per warp (D = 64: 4, D = 32: 1)
+  constexpr int TPW = NNT / 4;             // chunk x D tiles per warp (2 row tiles x NNT over 8 warps)
+  extern __shared__ __align__(16) float cbm_sm[];
+  float* st = cbm_sm;                      // [D][P] C = S<_i + W_ii P before the chunk, row-major
+  float* zs = st + D * P;                  // [D]    c = z<_i + W_ii y before the chunk
+  float* sq = zs + D;                      // [chunk][P] phi(q_t)
+  float* sk = sq + kCbChunk * P;           // [chunk][P] phi(k_s)
+  float* sv = sk + kCbChunk * P;           // [chunk][P] v_s
+  float* sg = sv + kCbChunk * P;           // [chunk][P] g_t
+  float* sdn = sg + kCbChunk * P;          // [chunk][P] dnum_t
+  float* su = sdn + kCbChunk * P;          // [chunk][P] u_t = C g_t, then (B phi(K))_t
+  float* sdd = su + kCbChunk * P;          // [chunk]    dden_t
+  float* sa = sdd + kCbChunk;              // [chunk][CP] a_ts (s <= t, else 0)
+  float* se = sa + kCbChunk * CP;          // [chunk][CP] e_ts, then b_ts (s <= t, else 0)
+  float* red = se + kCbChunk * CP;         // [warps]
+  const int64_t item = blockIdx.x;
+  const int64_t i = item % g.M, bh = item / g.M;
+  const int64_t b = bh / H, h = bh % H;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const float wii = __ldg(W + i * g.M + i);
+  // S<_i and z<_i: float32 rows of Sp, or (Stb non-null) the tensor-core states
+  const int64_t si = bh * g.M + i;
+  if (Stb) {
+    for (int e = tid; e < E; e += kCbThreads) st[(e / D) * P + e % D] = __bfloat162float(Stb[si * E + e]);
+    for (int r = tid; r < D; r += kCbThreads) zs[r] = ztb[si * D + r];
+  } else {
+    const float* src = Sp + si * static_cast<int64_t>(E + D);
+    for (int e = tid; e < E; e += kCbThreads) st[(e / D) * P + e % D] = src[e];
+    for (int r = tid; r < D; r += kCbThreads) zs[r] = src[E + r];
+  }
+  const __nv_bfloat16* qb = q + b * qo.sb + h * qo.sh;
+  const __nv_bfloat16* kb = k + b * ko.sb + h * ko.sh;
+  const __nv_bfloat16* vb = v + b * vo.sb + h * vo.sh;
+  const __nv_bfloat16* gb = g_out + b * go.sb + h * go.sh;
+  __nv_bfloat16* dqb = dq + b * dqo.sb + h * dqo.sh;
+  float* dnb = dn + (bh * g.M + i) * g.w * PD;   // token rows: dnum_t (D), dden_t
+  const int g8 = lane >> 2, t4 = lane & 3;      // accumulator rows g8, g8 + 8; columns 2 t4, 2 t4 + 1
+  const int smt = warp / WPM, snt0 = (warp % WPM) * NPW;   // this warp's state tiles
+  float pr[NPW][4], acc[NPW][4];
+#pragma unroll
+  for (int j = 0; j < NPW; ++j)
+#pragma unroll
+    for (int e4 = 0; e4 < 4; ++e4) pr[j][e4] = acc[j][e4] = 0.0f;
+  float yr = 0.0f, zacc = 0.0f, dw = 0.0f;
+  const int tt = tid / 16, cc = tid % 16;
+  const int t0 = 2 * tt, t1 = t0 + 1;      // per-token steps: tokens t0, t1; columns c0 ..
+  const int c0 = V * cc;
+  const int srow = tid / kCbRowLanes, spart = tid % kCbRowLanes;
+  const int64_t nb = token_of(g, i, 0);    // contiguous blocks: slot s is token nb + s
+  // a chunk x D product of this warp's tiles (rows 16 (warp & 1) .., columns
+  // 8 ((warp >> 1) TPW + j)) into rows of dst
+  auto chunk_by_d = [&](const float* A, int lda, int kdim, auto load_b, float* dst) {
+    const int mt = warp & 1, ntb = (warp >> 1) * TPW;
+    float cf[TPW][4];
+#pragma unroll
+    for (int j = 0; j < TPW; ++j)
+#pragma unroll
+      for (int e4 = 0; e4 < 4; ++e4) cf[j][e4] = 0.0f;
+    for (int ks = 0; ks < kdim / 16; ++ks) {
+      uint32_t af[4];
+      frag_a_rows(A, lda, 16 * mt, 16 * ks, lane, af);
+#pragma unroll
+      for (int j = 0; j < TPW; ++j) {
+        uint32_t bf[2];
+        load_b(8 * (ntb + j), 16 * ks, bf);
+        mma_m16n8k16(cf[j], af, bf);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < TPW; ++j)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2)
+        *reinterpret_cast<float2*>(dst + (16 * mt + g8 + 8 * h2) * P + 8 * (ntb + j) + 2 * t4) =
+            make_float2(cf[j][2 * h2], cf[j][2 * h2 + 1]);
+  };
+  for (int64_t s0 = 0; s0 < g.w; s0 += kCbChunk) {
+    const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
+    const bool more = s0 + kCbChunk < g.w;   // a later chunk of the block reads the advanced state
+    __syncthreads();   // the state is complete and the previous chunk's rows are free
+    {
+      const bool live = srow < cnt;
+      const int64_t n = nb + s0 + srow;
+#pragma unroll
+      for (int c = 4 * spart; c < D; c += 4 * kCbRowLanes) {
+        float xq[4], xk[4], xv[4], xg[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          xq[u] = live ? phi_f(load_f(qb + n * qo.sn + c + u), phi_kind, eps) : 0.0f;
+          xk[u] = live ? phi_f(load_f(kb + n * ko.sn + c + u), phi_kind, eps) : 0.0f;
+          xv[u] = live ? load_f(vb + n * vo.sn + c + u) : 0.0f;
+          xg[u] = live ? load_f(gb + n * go.sn + c + u) : 0.0f;
+        }
+        stv<4>(sq + srow * P + c, xq);
+        stv<4>(sk + srow * P + c, xk);
+        stv<4>(sv + srow * P + c, xv);
+        stv<4>(sg + srow * P + c, xg);
+      }
+    }
+    __syncthreads();
+    // ---- 1: a = phi(Q) phi(K)^T (warps 0-3) and e = G V^T (warps 4-7), kept for s <= t
+    {
+      const int mat = warp >> 2, mt = (warp >> 1) & 1, nt0 = (warp & 1) * 2;
+      const float* A = mat ? sg : sq;
+      const float* Bm = mat ? sv : sk;
+      float* dst = mat ? se : sa;
+      float cf[2][4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) cf[j][e4] = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t af[4];
+        frag_a_rows(A, P, 16 * mt, 16 * ks, lane, af);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint32_t bf[2];
+          frag_b_rows(Bm, P, 8 * (nt0 + j), 16 * ks, lane, bf);
+          mma_m16n8k16(cf[j], af, bf);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const int row = 16 * mt + g8 + 8 * (e4 >> 1), col = 8 * (nt0 + j) + 2 * t4 + (e4 & 1);
+          dst[row * CP + col] = (row < cnt && col <= row) ? cf[j][e4] : 0.0f;
+        }
+    }
+    __syncthreads();
+    // ---- 2: u = G C^T into su (B[c][r] = C[r][c], rows of C)
+    chunk_by_d(sg, P, D, [&](int n0, int k0, uint32_t(&bf)[2]) { frag_b_rows(st, P, n0, k0, lane, bf); }, su);
+    __syncthreads();
+    // ---- 3: per token (t0, t1 on the 16 lanes of a half-warp; columns / rows c0 ..):
+    // den_t, g_t . num_t, dnum_t, dden_t, b_ts, dW_ii's own-chunk part
+    float x0[V], x1[V];   // C dnum_t + dden_t c, this lane's rows
+    {
+      float u0[V], u1[V];
+      ldv<V>(su + t0 * P + c0, u0);
+      ldv<V>(su + t1 * P + c0, u1);
+      float qa[V], qc[V], zv[V], gva[V], gvc[V];
+      ldv<V>(sq + t0 * P + c0, qa);
+      ldv<V>(sq + t1 * P + c0, qc);
+      ldv<V>(zs + c0, zv);
+      ldv<V>(sg + t0 * P + c0, gva);
+      ldv<V>(sg + t1 * P + c0, gvc);
+      float den0 = 0.0f, den1 = 0.0f, go0 = 0.0f, go1 = 0.0f;
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        den0 = fmaf(qa[w], zv[w], den0);
+        den1 = fmaf(qc[w], zv[w], den1);
+        go0 = fmaf(qa[w], u0[w], go0);
+        go1 = fmaf(qc[w], u1[w], go1);
+      }
+      // this lane's own-chunk sources s = cc, cc + 16
+      const float a0a = sa[t0 * CP + cc], a0b = sa[t0 * CP + cc + 16];
+      const float a1a = sa[t1 * CP + cc], a1b = sa[t1 * CP + cc + 16];
+      const float e0a = se[t0 * CP + cc], e0b = se[t0 * CP + cc + 16];
+      const float e1a = se[t1 * CP + cc], e1b = se[t1 * CP + cc + 16];
+      den0 = fmaf(wii, a0a + a0b, den0);
+      den1 = fmaf(wii, a1a + a1b, den1);
+      go0 = fmaf(wii, fmaf(a0a, e0a, a0b * e0b), go0);
+      go1 = fmaf(wii, fmaf(a1a, e1a, a1b * e1b), go1);
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) {   // the 16 lanes of this half-warp share t0, t1
+        den0 += __shfl_xor_sync(0xffffffffu, den0, off);
+        den1 += __shfl_xor_sync(0xffffffffu, den1, off);
+        go0 += __shfl_xor_sync(0xffffffffu, go0, off);
+        go1 += __shfl_xor_sync(0xffffffffu, go1, off);
+      }
+      den0 += eps;
+      den1 += eps;
+      const bool l0 = t0 < cnt, l1 = t1 < cnt;   // rows past the block stay zero
+      const float dd0 = l0 ? -(go0 / den0) / den0 : 0.0f;
+      const float dd1 = l1 ? -(go1 / den1) / den1 : 0.0f;
+      float dn0[V], dn1[V];
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        dn0[w] = l0 ? gva[w] / den0 : 0.0f;
+        dn1[w] = l1 ? gvc[w] / den1 : 0.0f;
+        x0[w] = fmaf(dd0, zv[w], u0[w] / den0);
+        x1[w] = fmaf(dd1, zv[w], u1[w] / den1);
+      }
+      stv<V>(sdn + t0 * P + c0, dn0);
+      stv<V>(sdn + t1 * P + c0, dn1);
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        if (l0) dnb[(s0 + t0) * PD + c0 + w] = dn0[w];
+        if (l1) dnb[(s0 + t1) * PD + c0 + w] = dn1[w];
+      }
+      if (cc == 0) {
+        sdd[t0] = dd0;
+        sdd[t1] = dd1;
+        if (l0) dnb[(s0 + t0) * PD + D] = dd0;
+        if (l1) dnb[(s0 + t1) * PD + D] = dd1;
+      }
+      // b_ts = e_ts / den_t + dden_t (s <= t) in place of e_ts; dW_ii's own-chunk part
+      const float b0a = (l0 && cc <= t0) ? e0a / den0 + dd0 : 0.0f;
+      const float b0b = (l0 && cc + 16 <= t0) ? e0b / den0 + dd0 : 0.0f;
+      const float b1a = (l1 && cc <= t1) ? e1a / den1 + dd1 : 0.0f;
+      const float b1b = (l1 && cc + 16 <= t1) ? e1b / den1 + dd1 : 0.0f;
+      se[t0 * CP + cc] = b0a;
+      se[t0 * CP + cc + 16] = b0b;
+      se[t1 * CP + cc] = b1a;
+      se[t1 * CP + cc + 16] = b1b;
+      dw = fmaf(a0a, b0a, dw);
+      dw = fmaf(a0b, b0b, dw);
+      dw = fmaf(a1a, b1a, dw);
+      dw = fmaf(a1b, b1b, dw);
+    }
+    __syncthreads();
+    // ---- 4: Y = B phi(K) into su (B[s][r] = phi(k_s)[r], rows of phi(K))
+    chunk_by_d(se, CP, kCbChunk, [&](int n0, int k0, uint32_t(&bf)[2]) { frag_b_cols(sk, P, n0, k0, lane, bf); },
+               su);
+    __syncthreads();
+    // ---- 5: dq = u_t / den_t + dden_t c + W_ii Y_t, masked by [q_t > 0] (tokens t0, t1; rows c0 ..)
+    {
+      float w0[V], w1[V];
+      ldv<V>(su + t0 * P + c0, w0);
+      ldv<V>(su + t1 * P + c0, w1);
+      const int64_t n0t = nb + s0 + t0, n1t = nb + s0 + t1;
+#pragma unroll
+      for (int w = 0; w < V; ++w) {
+        const int r = c0 + w;
+        if (t0 < cnt) {
+          const float x = fmaf(wii, w0[w], x0[w]);
+          store_f(dqb + n0t * dqo.sn + r, load_f(qb + n0t * qo.sn + r) > 0.0f ? x : 0.0f);
+        }
+        if (t1 < cnt) {
+          const float x = fmaf(wii, w1[w], x1[w]);
+          store_f(dqb + n1t * dqo.sn + r, load_f(qb + n1t * qo.sn + r) > 0.0f ? x : 0.0f);
+        }
+      }
+    }
+    // ---- 6: X = phi(Q)^T dnum and, unless the block ends here, phi(K)^T V over this
+    // warp's state tiles (no barrier before: steps 2 to 5 are done with C); then
+    // dS<_i += X, dW_ii += <P, X>, P and C advance
+    {
+      float X[NPW][4], dps[NPW][4];
+#pragma unroll
+      for (int j = 0; j < NPW; ++j)
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) X[j][e4] = dps[j][e4] = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < kCbChunk / 16; ++ks) {
+        uint32_t aq[4];
+        frag_a_cols(sq, P, 16 * smt, 16 * ks, lane, aq);   // A[r][t] = phi(q_t)[r]
+#pragma unroll
+        for (int j = 0; j < NPW; ++j) {
+          uint32_t bn[2];
+          frag_b_cols(sdn, P, 8 * (snt0 + j), 16 * ks, lane, bn);   // B[t][c] = dnum_t[c]
+          mma_m16n8k16(X[j], aq, bn);
+        }
+        if (more) {
+          uint32_t ak[4];
+          frag_a_cols(sk, P, 16 * smt, 16 * ks, lane, ak);
+#pragma unroll
+          for (int j = 0; j < NPW; ++j) {
+            uint32_t bv[2];
+            frag_b_cols(sv, P, 8 * (snt0 + j), 16 * ks, lane, bv);
+            mma_m16n8k16(dps[j], ak, bv);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NPW; ++j)
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          dw = fmaf(pr[j][e4], X[j][e4], dw);
+          acc[j][e4] += X[j][e4];
+          pr[j][e4] += dps[j][e4];
+        }
+      if (more) {
+#pragma unroll
+        for (int j = 0; j < NPW; ++j)
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            float* cs = st + (16 * smt + g8 + 8 * (e4 >> 1)) * P + 8 * (snt0 + j) + 2 * t4 + (e4 & 1);
+            *cs = fmaf(wii, dps[j][e4], *cs);
+          }
+      }
+    }
+    if (tid < D) {
+      float x = 0.0f, dy = 0.0f;
+      for (int sl = 0; sl < kCbChunk; ++sl) {
+        x = fmaf(sq[sl * P + tid], sdd[sl], x);
+        dy += sk[sl * P + tid];
+      }
+      dw = fmaf(yr, x, dw);
+      zacc += x;
+      yr += dy;
+      zs[tid] = fmaf(wii, dy, zs[tid]);
+    }
+  }
+  float* out = dSp + (bh * g.M + i) * static_cast<int64_t>(E + D);
+#pragma unroll
+  for (int j = 0; j < NPW; ++j)
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2)
+      *reinterpret_cast<float2*>(out + (16 * smt + g8 + 8 * h2) * D + 8 * (snt0 + j) + 2 * t4) =
+          make_float2(acc[j][2 * h2], acc[j][2 * h2 + 1]);
+  if (tid < D) out[E + tid] = zacc;
+  dw = warp_sum(dw);
+  if (lane == 0) red[warp] = dw;
+  __syncthreads();
+  if (tid == 0) {
+    float s = 0.0f;
+    for (int w = 0; w < kCbWarps; ++w) s += red[w];
+    diag[bh * g.M + i] = s;
+  }
+}
+
 // The same arithmetic as simt_causal_bwd_key for d = D in {32, 64}, laid out as
 // simt_causal_bwd_query_v: padded rows, 16-byte vectors, G kept row-major and
 // transposed (G feeds dv, G^T feeds dk), token-pair tiles {p, p + 16} x
@@ -1780,6 +2172,11 @@ simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__
 // Shared memory of the vector-layout causal backward kernels, d = D.
 constexpr size_t cbv_query_smem(int D) {
   return static_cast<size_t>(D * (D + 4) + D + 5 * kCbChunk * (D + 4) + kCbChunk + 2 * kCbChunk * (kCbChunk + 4) +
+                             kCbWarps) *
+         sizeof(float);
+}
+constexpr size_t cbm_query_smem(int D) {
+  return static_cast<size_t>(D * (D + 4) + D + 6 * kCbChunk * (D + 4) + kCbChunk + 2 * kCbChunk * (kCbChunk + 4) +
                              kCbWarps) *
          sizeof(float);
 }
@@ -2095,12 +2492,19 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
           ws.diag, ws.dn, static_cast<const __nv_bfloat16*>(cs.St), cs.zt);
       return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
     };
-    const int rc = d == 64   ? launch_v(simt_causal_bwd_query_v<T, 64>, cbv_query_smem(64))
-                   : d == 32 ? launch_v(simt_causal_bwd_query_v<T, 32>, cbv_query_smem(32))
-                   : d <= 16 ? launch(simt_causal_bwd_query<T, 1, 1>)
-                   : d <= 32 ? launch(simt_causal_bwd_query<T, 4, 2>)
-                   : d <= 64 ? launch(simt_causal_bwd_query<T, 16, 4>)
-                             : launch(simt_causal_bwd_query<T, 64, 8>);
+    int rc = -1;
+    if constexpr (std::is_same_v<T, __nv_bfloat16>) {   // bf16: the products on warp-level tensor cores
+      if (d == 64) rc = launch_v(simt_causal_bwd_query_mma<64>, cbm_query_smem(64));
+      if (d == 32) rc = launch_v(simt_causal_bwd_query_mma<32>, cbm_query_smem(32));
+    } else {                                            // float32: every product on CUDA cores
+      if (d == 64) rc = launch_v(simt_causal_bwd_query_v<T, 64>, cbv_query_smem(64));
+      if (d == 32) rc = launch_v(simt_causal_bwd_query_v<T, 32>, cbv_query_smem(32));
+    }
+    if (rc == -1)
+      rc = d <= 16   ? launch(simt_causal_bwd_query<T, 1, 1>)
+         : d <= 32 ? launch(simt_causal_bwd_query<T, 4, 2>)
+         : d <= 64 ? launch(simt_causal_bwd_query<T, 16, 4>)
+                   : launch(simt_causal_bwd_query<T, 64, 8>);
     if (rc != MHLA_OK) return rc;
   }
   const int64_t MM = p.M * p.M;
