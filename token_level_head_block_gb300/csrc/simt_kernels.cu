@@ -2169,6 +2169,213 @@ simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__
   }
 }
 
+// The causal backward's key side for bf16 inputs and d = D in {32, 64}: the
+// arithmetic of simt_causal_bwd_key_v with its products on warp-level tensor
+// cores (operands rounded to bf16 from the float32 rows in shared memory,
+// float32 accumulation): the pair dots a = phi(K) phi(Q)^T and b = V dnum^T
+// (+ dden_t), dv = phi(K) G + W_jj a dnum, dk = V G^T + W_jj b phi(Q) (G row-major
+// serves both), and the suffix-state update phi(Q)^T dnum.  dv and dk go from
+// the accumulators to global memory.
+template <int D>
+__global__ void __launch_bounds__(kCbThreads, 2)
+simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const __nv_bfloat16* __restrict__ k,
+                        Operand ko, const __nv_bfloat16* __restrict__ v, Operand vo, __nv_bfloat16* __restrict__ dk,
+                        Operand dko, __nv_bfloat16* __restrict__ dv, Operand dvo, TokenGeom g, int64_t H, int phi_kind,
+                        float eps, const float* __restrict__ W, const float* __restrict__ dS,
+                        const float* __restrict__ dn, const __nv_bfloat16* __restrict__ Stb,
+                        const float* __restrict__ ztb) {
+  constexpr int P = D + 4;
+  constexpr int CP = kCbChunk + 4;
+  constexpr int E = D * D, PD = D + 1;
+  constexpr int NMT = D / 16, NNT = D / 8; // 16 x 8 tiles of a D x D state
+  constexpr int WPM = kCbWarps / NMT;      // warps per row tile of the state
+  constexpr int NPW = NNT / WPM;           // state tiles per warp
+  constexpr int OPW = NNT / 2;             // chunk x D tiles per warp of a warp half (2 row tiles x NNT over 4)
+  extern __shared__ __align__(16) float ckm_sm[];
+  float* gs = ckm_sm;                      // [D][P] G = dS_j + W_jj sum over later chunks, row-major
+  float* gz = gs + D * P;                  // [D]    gz
+  float* sq = gz + D;                      // [chunk][P] phi(q_t)
+  float* sdn = sq + kCbChunk * P;          // [chunk][P] dnum_t
+  float* sk = sdn + kCbChunk * P;          // [chunk][P] phi(k_s)
+  float* sv = sk + kCbChunk * P;           // [chunk][P] v_s
+  float* sdd = sv + kCbChunk * P;          // [chunk]    dden_t
+  float* sa = sdd + kCbChunk;              // [chunk][CP] a_st (t >= s, else 0)
+  float* sb = sa + kCbChunk * CP;          // [chunk][CP] b_st (t >= s, else 0)
+  const int64_t item = blockIdx.x;
+  const int64_t j = item % g.M, bh = item / g.M;
+  const int64_t b = bh / H, h = bh % H;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const float wjj = __ldg(W + j * g.M + j);
+  // dS_j and dz_j: float32 rows of dS, or (Stb non-null) the tensor-core mixing's
+  // output (bf16 row-major dS_j, float32 dz_j)
+  const int64_t sj = bh * g.M + j;
+  const float* src = dS + sj * static_cast<int64_t>(E + D);
+  for (int e = tid; e < E; e += kCbThreads)
+    gs[(e / D) * P + e % D] = Stb ? __bfloat162float(Stb[sj * E + e]) : src[e];
+  for (int r = tid; r < D; r += kCbThreads) gz[r] = Stb ? ztb[sj * D + r] : src[E + r];
+  const __nv_bfloat16* qb = q + b * qo.sb + h * qo.sh;
+  const __nv_bfloat16* kb = k + b * ko.sb + h * ko.sh;
+  const __nv_bfloat16* vb = v + b * vo.sb + h * vo.sh;
+  __nv_bfloat16* dkb = dk + b * dko.sb + h * dko.sh;
+  __nv_bfloat16* dvb = dv + b * dvo.sb + h * dvo.sh;
+  const float* dnb = dn + (bh * g.M + j) * g.w * PD;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int smt = warp / WPM, snt0 = (warp % WPM) * NPW;   // this warp's state tiles
+  const int srow = tid / kCbRowLanes, spart = tid % kCbRowLanes;
+  const int64_t nb = token_of(g, j, 0);
+  const int64_t nch = (g.w + kCbChunk - 1) / kCbChunk;
+  for (int64_t ci = nch - 1; ci >= 0; --ci) {
+    const int64_t s0 = ci * kCbChunk;
+    const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
+    __syncthreads();   // the suffix state is complete and the later chunk's rows are free
+    {
+      const bool live = srow < cnt;
+      const int64_t n = nb + s0 + srow;
+#pragma unroll
+      for (int c = 4 * spart; c < D; c += 4 * kCbRowLanes) {
+        float xq[4], xn[4], xk[4], xv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          xq[u] = live ? phi_f(load_f(qb + n * qo.sn + c + u), phi_kind, eps) : 0.0f;
+          xn[u] = live ? dnb[(s0 + srow) * PD + c + u] : 0.0f;
+          xk[u] = live ? phi_f(load_f(kb + n * ko.sn + c + u), phi_kind, eps) : 0.0f;
+          xv[u] = live ? load_f(vb + n * vo.sn + c + u) : 0.0f;
+        }
+        stv<4>(sq + srow * P + c, xq);
+        stv<4>(sdn + srow * P + c, xn);
+        stv<4>(sk + srow * P + c, xk);
+        stv<4>(sv + srow * P + c, xv);
+      }
+    }
+    if (tid < kCbChunk) sdd[tid] = tid < cnt ? dnb[(s0 + tid) * PD + D] : 0.0f;
+    __syncthreads();
+    // ---- 1: a = phi(K) phi(Q)^T (warps 0-3) and b = V dnum^T + dden_t (warps 4-7), kept for t >= s
+    {
+      const int mat = warp >> 2, mt = (warp >> 1) & 1, nt0 = (warp & 1) * 2;
+      const float* A = mat ? sv : sk;
+      const float* Bm = mat ? sdn : sq;
+      float* dst = mat ? sb : sa;
+      float cf[2][4];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) cf[jj][e4] = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t af[4];
+        frag_a_rows(A, P, 16 * mt, 16 * ks, lane, af);
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          uint32_t bf[2];
+          frag_b_rows(Bm, P, 8 * (nt0 + jj), 16 * ks, lane, bf);
+          mma_m16n8k16(cf[jj], af, bf);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const int row = 16 * mt + g8 + 8 * (e4 >> 1), col = 8 * (nt0 + jj) + 2 * t4 + (e4 & 1);
+          const bool keep = col < cnt && col >= row;   // source row s, query col t >= s
+          dst[row * CP + col] = keep ? cf[jj][e4] + (mat ? sdd[col] : 0.0f) : 0.0f;
+        }
+    }
+    __syncthreads();
+    // ---- 2: dv (warps 0-3) and dk (warps 4-7) of this warp's tiles, straight to memory:
+    //   dv_s = sum_x phi(k_s)[x] G[x][.] + W_jj sum_t a_st dnum_t
+    //   dk_s = (sum_x G[.][x] v_s[x] + gz + W_jj sum_t b_st phi(q_t)) [k_s > 0]
+    {
+      const bool kside = warp >= kCbWarps / 2;
+      const int mt = warp & 1, ntb = ((warp >> 1) & 1) * OPW;
+      float c1[OPW][4], c2[OPW][4];
+#pragma unroll
+      for (int jj = 0; jj < OPW; ++jj)
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) c1[jj][e4] = c2[jj][e4] = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t af[4];
+        frag_a_rows(kside ? sv : sk, P, 16 * mt, 16 * ks, lane, af);
+#pragma unroll
+        for (int jj = 0; jj < OPW; ++jj) {
+          uint32_t bf[2];
+          if (kside)
+            frag_b_rows(gs, P, 8 * (ntb + jj), 16 * ks, lane, bf);   // B[x][r] = G[r][x]
+          else
+            frag_b_cols(gs, P, 8 * (ntb + jj), 16 * ks, lane, bf);   // B[x][c] = G[x][c]
+          mma_m16n8k16(c1[jj], af, bf);
+        }
+      }
+#pragma unroll
+      for (int ks = 0; ks < kCbChunk / 16; ++ks) {
+        uint32_t af[4];
+        frag_a_rows(kside ? sb : sa, CP, 16 * mt, 16 * ks, lane, af);
+#pragma unroll
+        for (int jj = 0; jj < OPW; ++jj) {
+          uint32_t bf[2];
+          frag_b_cols(kside ? sq : sdn, P, 8 * (ntb + jj), 16 * ks, lane, bf);   // B[t][.] = row t
+          mma_m16n8k16(c2[jj], af, bf);
+        }
+      }
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int s = 16 * mt + g8 + 8 * h2;
+        if (s < cnt) {
+          const int64_t n = nb + s0 + s;
+#pragma unroll
+          for (int jj = 0; jj < OPW; ++jj) {
+            const int c = 8 * (ntb + jj) + 2 * t4;
+            float x0 = fmaf(wjj, c2[jj][2 * h2], c1[jj][2 * h2]);
+            float x1 = fmaf(wjj, c2[jj][2 * h2 + 1], c1[jj][2 * h2 + 1]);
+            if (kside) {
+              x0 = load_f(kb + n * ko.sn + c) > 0.0f ? x0 + gz[c] : 0.0f;
+              x1 = load_f(kb + n * ko.sn + c + 1) > 0.0f ? x1 + gz[c + 1] : 0.0f;
+              store_f(dkb + n * dko.sn + c, x0);
+              store_f(dkb + n * dko.sn + c + 1, x1);
+            } else {
+              store_f(dvb + n * dvo.sn + c, x0);
+              store_f(dvb + n * dvo.sn + c + 1, x1);
+            }
+          }
+        }
+      }
+    }
+    if (ci == 0) break;   // the block's first chunk: nothing reads the suffix state after it
+    __syncthreads();      // the G update below rewrites G, which step 2 has read
+    // ---- 3: G += W_jj phi(Q)^T dnum over this warp's state tiles, gz likewise
+    {
+      float X[NPW][4];
+#pragma unroll
+      for (int jj = 0; jj < NPW; ++jj)
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) X[jj][e4] = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < kCbChunk / 16; ++ks) {
+        uint32_t aq[4];
+        frag_a_cols(sq, P, 16 * smt, 16 * ks, lane, aq);   // A[r][t] = phi(q_t)[r]
+#pragma unroll
+        for (int jj = 0; jj < NPW; ++jj) {
+          uint32_t bn[2];
+          frag_b_cols(sdn, P, 8 * (snt0 + jj), 16 * ks, lane, bn);   // B[t][c] = dnum_t[c]
+          mma_m16n8k16(X[jj], aq, bn);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < NPW; ++jj)
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          float* gp = gs + (16 * smt + g8 + 8 * (e4 >> 1)) * P + 8 * (snt0 + jj) + 2 * t4 + (e4 & 1);
+          *gp = fmaf(wjj, X[jj][e4], *gp);
+        }
+    }
+    if (tid < D) {
+      float x = 0.0f;
+      for (int t = 0; t < kCbChunk; ++t) x = fmaf(sdd[t], sq[t * P + tid], x);
+      gz[tid] = fmaf(wjj, x, gz[tid]);
+    }
+  }
+}
+
 // Shared memory of the vector-layout causal backward kernels, d = D.
 constexpr size_t cbv_query_smem(int D) {
   return static_cast<size_t>(D * (D + 4) + D + 5 * kCbChunk * (D + 4) + kCbChunk + 2 * kCbChunk * (kCbChunk + 4) +
@@ -2178,6 +2385,10 @@ constexpr size_t cbv_query_smem(int D) {
 constexpr size_t cbm_query_smem(int D) {
   return static_cast<size_t>(D * (D + 4) + D + 6 * kCbChunk * (D + 4) + kCbChunk + 2 * kCbChunk * (kCbChunk + 4) +
                              kCbWarps) *
+         sizeof(float);
+}
+constexpr size_t cbm_key_smem(int D) {
+  return static_cast<size_t>(D * (D + 4) + D + 4 * kCbChunk * (D + 4) + kCbChunk + 2 * kCbChunk * (kCbChunk + 4)) *
          sizeof(float);
 }
 constexpr size_t cbv_key_smem(int D) {
@@ -2569,9 +2780,14 @@ int launch_simt_causal_bwd_typed(const Problem& p, const float* W, const BwdOper
           static_cast<const __nv_bfloat16*>(cs.St), cs.zt);
       return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
     };
-    return d == 64   ? launch_v(simt_causal_bwd_key_v<T, 64>, cbv_key_smem(64))
-           : d == 32 ? launch_v(simt_causal_bwd_key_v<T, 32>, cbv_key_smem(32))
-           : d <= 16 ? launch(simt_causal_bwd_key<T, 1, 1>)
+    if constexpr (std::is_same_v<T, __nv_bfloat16>) {   // bf16: the products on warp-level tensor cores
+      if (d == 64) return launch_v(simt_causal_bwd_key_mma<64>, cbm_key_smem(64));
+      if (d == 32) return launch_v(simt_causal_bwd_key_mma<32>, cbm_key_smem(32));
+    } else {                                            // float32: every product on CUDA cores
+      if (d == 64) return launch_v(simt_causal_bwd_key_v<T, 64>, cbv_key_smem(64));
+      if (d == 32) return launch_v(simt_causal_bwd_key_v<T, 32>, cbv_key_smem(32));
+    }
+    return d <= 16   ? launch(simt_causal_bwd_key<T, 1, 1>)
            : d <= 32 ? launch(simt_causal_bwd_key<T, 2, 2>)
            : d <= 64 ? launch(simt_causal_bwd_key<T, 4, 4>)
                      : launch(simt_causal_bwd_key<T, 8, 8>);
