@@ -1647,6 +1647,7 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
   float* sa = sdd + kCbChunk;              // [chunk][CP] a_ts (s <= t, else 0)
   float* se = sa + kCbChunk * CP;          // [chunk][CP] e_ts, then b_ts (s <= t, else 0)
   float* red = se + kCbChunk * CP;         // [warps]
+  uint32_t* qpos = reinterpret_cast<uint32_t*>(red + kCbWarps);   // [chunk][D / 32] bits [q_t > 0]
   const int64_t item = blockIdx.x;
   const int64_t i = item % g.M, bh = item / g.M;
   const int64_t b = bh / H, h = bh % H;
@@ -1717,13 +1718,21 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
 #pragma unroll
       for (int c = 4 * spart; c < D; c += 4 * kCbRowLanes) {
         float xq[4], xk[4], xv[4], xg[4];
+        uint32_t pos = 0;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          xq[u] = live ? phi_f(load_f(qb + n * qo.sn + c + u), phi_kind, eps) : 0.0f;
+          const float xr = live ? load_f(qb + n * qo.sn + c + u) : 0.0f;
+          pos |= (xr > 0.0f ? 1u : 0u) << u;
+          xq[u] = live ? phi_f(xr, phi_kind, eps) : 0.0f;
           xk[u] = live ? phi_f(load_f(kb + n * ko.sn + c + u), phi_kind, eps) : 0.0f;
           xv[u] = live ? load_f(vb + n * vo.sn + c + u) : 0.0f;
           xg[u] = live ? load_f(gb + n * go.sn + c + u) : 0.0f;
         }
+        // the eight lanes of this row hold columns c % 32 = 4 spart .. of one word
+        pos <<= (c & 31);
+#pragma unroll
+        for (int off = 1; off < kCbRowLanes; off <<= 1) pos |= __shfl_xor_sync(0xffffffffu, pos, off);
+        if (spart == 0) qpos[srow * (D / 32) + c / 32] = pos;
         stv<4>(sq + srow * P + c, xq);
         stv<4>(sk + srow * P + c, xk);
         stv<4>(sv + srow * P + c, xv);
@@ -1858,11 +1867,11 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
         const int r = c0 + w;
         if (t0 < cnt) {
           const float x = fmaf(wii, w0[w], x0[w]);
-          store_f(dqb + n0t * dqo.sn + r, load_f(qb + n0t * qo.sn + r) > 0.0f ? x : 0.0f);
+          store_f(dqb + n0t * dqo.sn + r, (qpos[t0 * (D / 32) + r / 32] >> (r & 31)) & 1u ? x : 0.0f);
         }
         if (t1 < cnt) {
           const float x = fmaf(wii, w1[w], x1[w]);
-          store_f(dqb + n1t * dqo.sn + r, load_f(qb + n1t * qo.sn + r) > 0.0f ? x : 0.0f);
+          store_f(dqb + n1t * dqo.sn + r, (qpos[t1 * (D / 32) + r / 32] >> (r & 31)) & 1u ? x : 0.0f);
         }
       }
     }
@@ -2201,6 +2210,7 @@ simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const _
   float* sdd = sv + kCbChunk * P;          // [chunk]    dden_t
   float* sa = sdd + kCbChunk;              // [chunk][CP] a_st (t >= s, else 0)
   float* sb = sa + kCbChunk * CP;          // [chunk][CP] b_st (t >= s, else 0)
+  uint32_t* kpos = reinterpret_cast<uint32_t*>(sb + kCbChunk * CP);   // [chunk][D / 32] bits [k_s > 0]
   const int64_t item = blockIdx.x;
   const int64_t j = item % g.M, bh = item / g.M;
   const int64_t b = bh / H, h = bh % H;
@@ -2234,13 +2244,20 @@ simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const _
 #pragma unroll
       for (int c = 4 * spart; c < D; c += 4 * kCbRowLanes) {
         float xq[4], xn[4], xk[4], xv[4];
+        uint32_t pos = 0;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
+          const float xr = live ? load_f(kb + n * ko.sn + c + u) : 0.0f;
+          pos |= (xr > 0.0f ? 1u : 0u) << u;
           xq[u] = live ? phi_f(load_f(qb + n * qo.sn + c + u), phi_kind, eps) : 0.0f;
           xn[u] = live ? dnb[(s0 + srow) * PD + c + u] : 0.0f;
-          xk[u] = live ? phi_f(load_f(kb + n * ko.sn + c + u), phi_kind, eps) : 0.0f;
+          xk[u] = live ? phi_f(xr, phi_kind, eps) : 0.0f;
           xv[u] = live ? load_f(vb + n * vo.sn + c + u) : 0.0f;
         }
+        pos <<= (c & 31);   // one word's columns over the eight lanes of this row
+#pragma unroll
+        for (int off = 1; off < kCbRowLanes; off <<= 1) pos |= __shfl_xor_sync(0xffffffffu, pos, off);
+        if (spart == 0) kpos[srow * (D / 32) + c / 32] = pos;
         stv<4>(sq + srow * P + c, xq);
         stv<4>(sdn + srow * P + c, xn);
         stv<4>(sk + srow * P + c, xk);
@@ -2328,8 +2345,9 @@ simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const _
             float x0 = fmaf(wjj, c2[jj][2 * h2], c1[jj][2 * h2]);
             float x1 = fmaf(wjj, c2[jj][2 * h2 + 1], c1[jj][2 * h2 + 1]);
             if (kside) {
-              x0 = load_f(kb + n * ko.sn + c) > 0.0f ? x0 + gz[c] : 0.0f;
-              x1 = load_f(kb + n * ko.sn + c + 1) > 0.0f ? x1 + gz[c + 1] : 0.0f;
+              const uint32_t word = kpos[s * (D / 32) + c / 32] >> (c & 31);
+              x0 = word & 1u ? x0 + gz[c] : 0.0f;
+              x1 = word & 2u ? x1 + gz[c + 1] : 0.0f;
               store_f(dkb + n * dko.sn + c, x0);
               store_f(dkb + n * dko.sn + c + 1, x1);
             } else {
@@ -2384,11 +2402,12 @@ constexpr size_t cbv_query_smem(int D) {
 }
 constexpr size_t cbm_query_smem(int D) {
   return static_cast<size_t>(D * (D + 4) + D + 6 * kCbChunk * (D + 4) + kCbChunk + 2 * kCbChunk * (kCbChunk + 4) +
-                             kCbWarps) *
+                             kCbWarps + kCbChunk * (D / 32)) *
          sizeof(float);
 }
 constexpr size_t cbm_key_smem(int D) {
-  return static_cast<size_t>(D * (D + 4) + D + 4 * kCbChunk * (D + 4) + kCbChunk + 2 * kCbChunk * (kCbChunk + 4)) *
+  return static_cast<size_t>(D * (D + 4) + D + 4 * kCbChunk * (D + 4) + kCbChunk + 2 * kCbChunk * (kCbChunk + 4) +
+                             kCbChunk * (D / 32)) *
          sizeof(float);
 }
 constexpr size_t cbv_key_smem(int D) {
