@@ -2186,7 +2186,7 @@ simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__
 // serves both), and the suffix-state update phi(Q)^T dnum.  dv and dk go from
 // the accumulators to global memory.
 template <int D>
-__global__ void __launch_bounds__(kCbThreads, 2)
+__global__ void __launch_bounds__(kCbThreads, 3)
 simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const __nv_bfloat16* __restrict__ k,
                         Operand ko, const __nv_bfloat16* __restrict__ v, Operand vo, __nv_bfloat16* __restrict__ dk,
                         Operand dko, __nv_bfloat16* __restrict__ dv, Operand dvo, TokenGeom g, int64_t H, int phi_kind,
