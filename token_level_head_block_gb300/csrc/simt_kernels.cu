@@ -1618,7 +1618,7 @@ __device__ __forceinline__ void frag_b_cols(const float* s, int ld, int n0, int 
 // cores between them; the state C is kept row-major, and each warp owns a fixed
 // set of 16 x 8 tiles of X, of dS<_i and of the prefix state P.
 template <int D>
-__global__ void __launch_bounds__(kCbThreads, 2)
+__global__ void __launch_bounds__(kCbThreads, 3)
 simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const __nv_bfloat16* __restrict__ k,
                           Operand ko, const __nv_bfloat16* __restrict__ v, Operand vo,
                           const __nv_bfloat16* __restrict__ g_out, Operand go, __nv_bfloat16* __restrict__ dq,
@@ -1640,9 +1640,9 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
   float* sq = zs + D;                      // [chunk][P] phi(q_t)
   float* sk = sq + kCbChunk * P;           // [chunk][P] phi(k_s)
   float* sv = sk + kCbChunk * P;           // [chunk][P] v_s
-  float* sg = sv + kCbChunk * P;           // [chunk][P] g_t
-  float* sdn = sg + kCbChunk * P;          // [chunk][P] dnum_t
-  float* su = sdn + kCbChunk * P;          // [chunk][P] u_t = C g_t, then (B phi(K))_t
+  float* sg = sv + kCbChunk * P;           // [chunk][P] g_t, then dnum_t: each lane of the
+  float* sdn = sg;                         //   per-token step reads its own g_t entries first
+  float* su = sg + kCbChunk * P;           // [chunk][P] u_t = C g_t, then (B phi(K))_t
   float* sdd = su + kCbChunk * P;          // [chunk]    dden_t
   float* sa = sdd + kCbChunk;              // [chunk][CP] a_ts (s <= t, else 0)
   float* se = sa + kCbChunk * CP;          // [chunk][CP] e_ts, then b_ts (s <= t, else 0)
@@ -1684,7 +1684,8 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
   const int64_t nb = token_of(g, i, 0);    // contiguous blocks: slot s is token nb + s
   // a chunk x D product of this warp's tiles (rows 16 (warp & 1) .., columns
   // 8 ((warp >> 1) TPW + j)) into rows of dst
-  auto chunk_by_d = [&](const float* A, int lda, int kdim, auto load_b, float* dst) {
+  // (scale != 0: dst += scale * product, else dst = product)
+  auto chunk_by_d = [&](const float* A, int lda, int kdim, auto load_b, float* dst, float scale) {
     const int mt = warp & 1, ntb = (warp >> 1) * TPW;
     float cf[TPW][4];
 #pragma unroll
@@ -1704,9 +1705,15 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
 #pragma unroll
     for (int j = 0; j < TPW; ++j)
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2)
-        *reinterpret_cast<float2*>(dst + (16 * mt + g8 + 8 * h2) * P + 8 * (ntb + j) + 2 * t4) =
-            make_float2(cf[j][2 * h2], cf[j][2 * h2 + 1]);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float2* o2 = reinterpret_cast<float2*>(dst + (16 * mt + g8 + 8 * h2) * P + 8 * (ntb + j) + 2 * t4);
+        if (scale != 0.0f) {
+          const float2 x = *o2;
+          *o2 = make_float2(fmaf(scale, cf[j][2 * h2], x.x), fmaf(scale, cf[j][2 * h2 + 1], x.y));
+        } else {
+          *o2 = make_float2(cf[j][2 * h2], cf[j][2 * h2 + 1]);
+        }
+      }
   };
   for (int64_t s0 = 0; s0 < g.w; s0 += kCbChunk) {
     const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
@@ -1772,12 +1779,14 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
     }
     __syncthreads();
     // ---- 2: u = G C^T into su (B[c][r] = C[r][c], rows of C)
-    chunk_by_d(sg, P, D, [&](int n0, int k0, uint32_t(&bf)[2]) { frag_b_rows(st, P, n0, k0, lane, bf); }, su);
+    chunk_by_d(sg, P, D, [&](int n0, int k0, uint32_t(&bf)[2]) { frag_b_rows(st, P, n0, k0, lane, bf); }, su,
+               0.0f);
     __syncthreads();
     // ---- 3: per token (t0, t1 on the 16 lanes of a half-warp; columns / rows c0 ..):
-    // den_t, g_t . num_t, dnum_t, dden_t, b_ts, dW_ii's own-chunk part
-    float x0[V], x1[V];   // C dnum_t + dden_t c, this lane's rows
+    // den_t, g_t . num_t, dnum_t, dden_t, b_ts, dW_ii's own-chunk part; the lane's
+    // entries of u_t are replaced by those of C dnum_t + dden_t c
     {
+      float x0[V], x1[V];
       float u0[V], u1[V];
       ldv<V>(su + t0 * P + c0, u0);
       ldv<V>(su + t1 * P + c0, u1);
@@ -1826,6 +1835,8 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
       }
       stv<V>(sdn + t0 * P + c0, dn0);
       stv<V>(sdn + t1 * P + c0, dn1);
+      stv<V>(su + t0 * P + c0, x0);
+      stv<V>(su + t1 * P + c0, x1);
 #pragma unroll
       for (int w = 0; w < V; ++w) {
         if (l0) dnb[(s0 + t0) * PD + c0 + w] = dn0[w];
@@ -1852,11 +1863,11 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
       dw = fmaf(a1b, b1b, dw);
     }
     __syncthreads();
-    // ---- 4: Y = B phi(K) into su (B[s][r] = phi(k_s)[r], rows of phi(K))
+    // ---- 4: su += W_ii B phi(K) (B[s][r] = phi(k_s)[r], rows of phi(K)): dq before its mask
     chunk_by_d(se, CP, kCbChunk, [&](int n0, int k0, uint32_t(&bf)[2]) { frag_b_cols(sk, P, n0, k0, lane, bf); },
-               su);
+               su, wii);
     __syncthreads();
-    // ---- 5: dq = u_t / den_t + dden_t c + W_ii Y_t, masked by [q_t > 0] (tokens t0, t1; rows c0 ..)
+    // ---- 5: dq_t = (u_t / den_t + dden_t c + W_ii Y_t) [q_t > 0] (tokens t0, t1; rows c0 ..)
     {
       float w0[V], w1[V];
       ldv<V>(su + t0 * P + c0, w0);
@@ -1865,25 +1876,21 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
 #pragma unroll
       for (int w = 0; w < V; ++w) {
         const int r = c0 + w;
-        if (t0 < cnt) {
-          const float x = fmaf(wii, w0[w], x0[w]);
-          store_f(dqb + n0t * dqo.sn + r, (qpos[t0 * (D / 32) + r / 32] >> (r & 31)) & 1u ? x : 0.0f);
-        }
-        if (t1 < cnt) {
-          const float x = fmaf(wii, w1[w], x1[w]);
-          store_f(dqb + n1t * dqo.sn + r, (qpos[t1 * (D / 32) + r / 32] >> (r & 31)) & 1u ? x : 0.0f);
-        }
+        if (t0 < cnt)
+          store_f(dqb + n0t * dqo.sn + r, (qpos[t0 * (D / 32) + r / 32] >> (r & 31)) & 1u ? w0[w] : 0.0f);
+        if (t1 < cnt)
+          store_f(dqb + n1t * dqo.sn + r, (qpos[t1 * (D / 32) + r / 32] >> (r & 31)) & 1u ? w1[w] : 0.0f);
       }
     }
-    // ---- 6: X = phi(Q)^T dnum and, unless the block ends here, phi(K)^T V over this
-    // warp's state tiles (no barrier before: steps 2 to 5 are done with C); then
-    // dS<_i += X, dW_ii += <P, X>, P and C advance
+    // ---- 6: X = phi(Q)^T dnum over this warp's state tiles (no barrier before: steps 2
+    // to 5 are done with C): dS<_i += X, dW_ii += <P, X>; then, unless the block ends
+    // here, phi(K)^T V: P and C advance
     {
-      float X[NPW][4], dps[NPW][4];
+      float X[NPW][4];
 #pragma unroll
       for (int j = 0; j < NPW; ++j)
 #pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) X[j][e4] = dps[j][e4] = 0.0f;
+        for (int e4 = 0; e4 < 4; ++e4) X[j][e4] = 0.0f;
 #pragma unroll
       for (int ks = 0; ks < kCbChunk / 16; ++ks) {
         uint32_t aq[4];
@@ -1894,16 +1901,6 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
           frag_b_cols(sdn, P, 8 * (snt0 + j), 16 * ks, lane, bn);   // B[t][c] = dnum_t[c]
           mma_m16n8k16(X[j], aq, bn);
         }
-        if (more) {
-          uint32_t ak[4];
-          frag_a_cols(sk, P, 16 * smt, 16 * ks, lane, ak);
-#pragma unroll
-          for (int j = 0; j < NPW; ++j) {
-            uint32_t bv[2];
-            frag_b_cols(sv, P, 8 * (snt0 + j), 16 * ks, lane, bv);
-            mma_m16n8k16(dps[j], ak, bv);
-          }
-        }
       }
 #pragma unroll
       for (int j = 0; j < NPW; ++j)
@@ -1911,17 +1908,33 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
         for (int e4 = 0; e4 < 4; ++e4) {
           dw = fmaf(pr[j][e4], X[j][e4], dw);
           acc[j][e4] += X[j][e4];
-          pr[j][e4] += dps[j][e4];
         }
-      if (more) {
+    }
+    if (more) {
+      float dps[NPW][4];
 #pragma unroll
-        for (int j = 0; j < NPW; ++j)
+      for (int j = 0; j < NPW; ++j)
 #pragma unroll
-          for (int e4 = 0; e4 < 4; ++e4) {
-            float* cs = st + (16 * smt + g8 + 8 * (e4 >> 1)) * P + 8 * (snt0 + j) + 2 * t4 + (e4 & 1);
-            *cs = fmaf(wii, dps[j][e4], *cs);
-          }
+        for (int e4 = 0; e4 < 4; ++e4) dps[j][e4] = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < kCbChunk / 16; ++ks) {
+        uint32_t ak[4];
+        frag_a_cols(sk, P, 16 * smt, 16 * ks, lane, ak);   // A[r][s] = phi(k_s)[r]
+#pragma unroll
+        for (int j = 0; j < NPW; ++j) {
+          uint32_t bv[2];
+          frag_b_cols(sv, P, 8 * (snt0 + j), 16 * ks, lane, bv);   // B[s][c] = v_s[c]
+          mma_m16n8k16(dps[j], ak, bv);
+        }
       }
+#pragma unroll
+      for (int j = 0; j < NPW; ++j)
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          pr[j][e4] += dps[j][e4];
+          float* cs = st + (16 * smt + g8 + 8 * (e4 >> 1)) * P + 8 * (snt0 + j) + 2 * t4 + (e4 & 1);
+          *cs = fmaf(wii, dps[j][e4], *cs);
+        }
     }
     if (tid < D) {
       float x = 0.0f, dy = 0.0f;
@@ -2401,7 +2414,7 @@ constexpr size_t cbv_query_smem(int D) {
          sizeof(float);
 }
 constexpr size_t cbm_query_smem(int D) {
-  return static_cast<size_t>(D * (D + 4) + D + 6 * kCbChunk * (D + 4) + kCbChunk + 2 * kCbChunk * (kCbChunk + 4) +
+  return static_cast<size_t>(D * (D + 4) + D + 5 * kCbChunk * (D + 4) + kCbChunk + 2 * kCbChunk * (kCbChunk + 4) +
                              kCbWarps + kCbChunk * (D / 32)) *
          sizeof(float);
 }
