@@ -2195,8 +2195,9 @@ simt_causal_bwd_key_v(const T* __restrict__ q, Operand qo, const T* __restrict__
 // arithmetic of simt_causal_bwd_key_v with its products on warp-level tensor
 // cores (operands rounded to bf16 from the float32 rows in shared memory,
 // float32 accumulation): the pair dots a = phi(K) phi(Q)^T and b = V dnum^T
-// (+ dden_t), dv = phi(K) G + W_jj a dnum, dk = V G^T + W_jj b phi(Q) (G row-major
-// serves both), and the suffix-state update phi(Q)^T dnum.  dv and dk go from
+// (+ dden_t), kept scaled by W_jj, dv = phi(K) G + (W_jj a) dnum and
+// dk = V G^T + (W_jj b) phi(Q) (G row-major serves both; each in one
+// accumulator), and the suffix-state update phi(Q)^T dnum.  dv and dk go from
 // the accumulators to global memory.
 template <int D>
 __global__ void __launch_bounds__(kCbThreads, 3)
@@ -2221,8 +2222,8 @@ simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const _
   float* sk = sdn + kCbChunk * P;          // [chunk][P] phi(k_s)
   float* sv = sk + kCbChunk * P;           // [chunk][P] v_s
   float* sdd = sv + kCbChunk * P;          // [chunk]    dden_t
-  float* sa = sdd + kCbChunk;              // [chunk][CP] a_st (t >= s, else 0)
-  float* sb = sa + kCbChunk * CP;          // [chunk][CP] b_st (t >= s, else 0)
+  float* sa = sdd + kCbChunk;              // [chunk][CP] W_jj a_st (t >= s, else 0)
+  float* sb = sa + kCbChunk * CP;          // [chunk][CP] W_jj b_st (t >= s, else 0)
   uint32_t* kpos = reinterpret_cast<uint32_t*>(sb + kCbChunk * CP);   // [chunk][D / 32] bits [k_s > 0]
   const int64_t item = blockIdx.x;
   const int64_t j = item % g.M, bh = item / g.M;
@@ -2307,7 +2308,7 @@ simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const _
         for (int e4 = 0; e4 < 4; ++e4) {
           const int row = 16 * mt + g8 + 8 * (e4 >> 1), col = 8 * (nt0 + jj) + 2 * t4 + (e4 & 1);
           const bool keep = col < cnt && col >= row;   // source row s, query col t >= s
-          dst[row * CP + col] = keep ? cf[jj][e4] + (mat ? sdd[col] : 0.0f) : 0.0f;
+          dst[row * CP + col] = keep ? wjj * (cf[jj][e4] + (mat ? sdd[col] : 0.0f)) : 0.0f;
         }
     }
     __syncthreads();
@@ -2317,11 +2318,11 @@ simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const _
     {
       const bool kside = warp >= kCbWarps / 2;
       const int mt = warp & 1, ntb = ((warp >> 1) & 1) * OPW;
-      float c1[OPW][4], c2[OPW][4];
+      float c1[OPW][4];   // both products (the pair matrices carry W_jj) in one accumulator
 #pragma unroll
       for (int jj = 0; jj < OPW; ++jj)
 #pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) c1[jj][e4] = c2[jj][e4] = 0.0f;
+        for (int e4 = 0; e4 < 4; ++e4) c1[jj][e4] = 0.0f;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t af[4];
@@ -2344,7 +2345,7 @@ simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const _
         for (int jj = 0; jj < OPW; ++jj) {
           uint32_t bf[2];
           frag_b_cols(kside ? sq : sdn, P, 8 * (ntb + jj), 16 * ks, lane, bf);   // B[t][.] = row t
-          mma_m16n8k16(c2[jj], af, bf);
+          mma_m16n8k16(c1[jj], af, bf);
         }
       }
 #pragma unroll
@@ -2355,8 +2356,7 @@ simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const _
 #pragma unroll
           for (int jj = 0; jj < OPW; ++jj) {
             const int c = 8 * (ntb + jj) + 2 * t4;
-            float x0 = fmaf(wjj, c2[jj][2 * h2], c1[jj][2 * h2]);
-            float x1 = fmaf(wjj, c2[jj][2 * h2 + 1], c1[jj][2 * h2 + 1]);
+            float x0 = c1[jj][2 * h2], x1 = c1[jj][2 * h2 + 1];
             if (kside) {
               const uint32_t word = kpos[s * (D / 32) + c / 32] >> (c & 31);
               x0 = word & 1u ? x0 + gz[c] : 0.0f;
