@@ -611,7 +611,8 @@ def run_ours(args, wl):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic",
             "config": {**wl.describe(), "pass": args.pass_,
-                       "path": ("tc (summaries, mixing) + simt (token steps)" if "tc_summary" in prof else "simt")
+                       "path": ("tc (summaries, mixings, dW) + warp-level mma (per-token steps)" if "tc_summary" in prof
+                                else "simt")
                                if args.pass_ == "causal_backward" else
                                ("tc" if "tc_bwd_query" in prof else "simt") if bwd else
                                ("module (core: " + path + ")") if module else
