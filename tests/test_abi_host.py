@@ -379,7 +379,7 @@ def test_causal_backward_rejects_malformed_requests_before_any_launch(L):
     n = ctypes.c_size_t()
     BH, M, N, d = 6, 16, 1024, 64
     KS = 16  # the dW partial products split d (d + 1) = 4160 entries in 16 runs (6 tiles are too few CTAs)
-    need = 3 * BH * M * d * (d + 1) * 4 + BH * KS * M * M * 4 + BH * M * 4 + BH * N * (d + 1) * 4
+    need = 3 * BH * M * d * (d + 1) * 4 + BH * KS * M * M * 4 + BH * M * 4 + BH * N * (d + 4) * 4
     groups = (BH * (d + 1) * d + 127) // 128
     nsplit = min(groups, 152)   # the tensor-core dW product's splits (one 256 x 256 tile here)
     tc = M * M * 2 + M * groups * 128 * 2 + BH * M * d * d * 2 + BH * M * d * 4 + nsplit * M * M * 4

@@ -1553,6 +1553,16 @@ simt_causal_bwd_query_v(const T* __restrict__ q, Operand qo, const T* __restrict
   }
 }
 
+// Four consecutive bf16 from global memory (8-byte aligned) as floats: a bf16 is
+// the upper half of the float with the same bits.
+__device__ __forceinline__ void ld4_bf16(const __nv_bfloat16* p, float (&x)[4]) {
+  const uint2 r = *reinterpret_cast<const uint2*>(p);
+  x[0] = __uint_as_float(r.x << 16);
+  x[1] = __uint_as_float(r.x & 0xffff0000u);
+  x[2] = __uint_as_float(r.y << 16);
+  x[3] = __uint_as_float(r.y & 0xffff0000u);
+}
+
 // Warp-level bf16 tensor-core products for the causal backward's per-chunk
 // steps (PTX mma.sync m16n8k16, float32 accumulation).  Fragments are built from
 // float32 shared memory, rounded to bf16 (round to nearest even): with
@@ -1629,7 +1639,7 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
   constexpr int V = D / 16;
   constexpr int P = D + 4;                 // padded token / state row (even: 8-byte fragment loads)
   constexpr int CP = kCbChunk + 4;         // padded row of a 32 x 32 token-pair matrix
-  constexpr int E = D * D, PD = D + 1;     // PD: the dnum / dden scratch row
+  constexpr int E = D * D, PD = D + 4;     // PD: the dnum / dden scratch row (16-byte aligned)
   constexpr int NMT = D / 16, NNT = D / 8; // 16 x 8 tiles of a D x D state
   constexpr int WPM = kCbWarps / NMT;      // warps per row tile of the state
   constexpr int NPW = NNT / WPM;           // state tiles per warp (D = 64: 4, D = 32: 1)
@@ -1682,6 +1692,10 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
   const int c0 = V * cc;
   const int srow = tid / kCbRowLanes, spart = tid % kCbRowLanes;
   const int64_t nb = token_of(g, i, 0);    // contiguous blocks: slot s is token nb + s
+  // rows that start on 8-byte boundaries load four bf16 at a time
+  const bool vec = ((reinterpret_cast<uintptr_t>(qb) | reinterpret_cast<uintptr_t>(kb) |
+                     reinterpret_cast<uintptr_t>(vb) | reinterpret_cast<uintptr_t>(gb)) & 7) == 0 &&
+                   ((qo.sn | ko.sn | vo.sn | go.sn) & 3) == 0;
   // a chunk x D product of this warp's tiles (rows 16 (warp & 1) .., columns
   // 8 ((warp >> 1) TPW + j)) into rows of dst
   // (scale != 0: dst += scale * product, else dst = product)
@@ -1725,15 +1739,29 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
 #pragma unroll
       for (int c = 4 * spart; c < D; c += 4 * kCbRowLanes) {
         float xq[4], xk[4], xv[4], xg[4];
+        if (!live) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) xq[u] = xk[u] = xv[u] = xg[u] = 0.0f;
+        } else if (vec) {
+          ld4_bf16(qb + n * qo.sn + c, xq);
+          ld4_bf16(kb + n * ko.sn + c, xk);
+          ld4_bf16(vb + n * vo.sn + c, xv);
+          ld4_bf16(gb + n * go.sn + c, xg);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            xq[u] = load_f(qb + n * qo.sn + c + u);
+            xk[u] = load_f(kb + n * ko.sn + c + u);
+            xv[u] = load_f(vb + n * vo.sn + c + u);
+            xg[u] = load_f(gb + n * go.sn + c + u);
+          }
+        }
         uint32_t pos = 0;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float xr = live ? load_f(qb + n * qo.sn + c + u) : 0.0f;
-          pos |= (xr > 0.0f ? 1u : 0u) << u;
-          xq[u] = live ? phi_f(xr, phi_kind, eps) : 0.0f;
-          xk[u] = live ? phi_f(load_f(kb + n * ko.sn + c + u), phi_kind, eps) : 0.0f;
-          xv[u] = live ? load_f(vb + n * vo.sn + c + u) : 0.0f;
-          xg[u] = live ? load_f(gb + n * go.sn + c + u) : 0.0f;
+          pos |= (xq[u] > 0.0f ? 1u : 0u) << u;
+          xq[u] = live ? phi_f(xq[u], phi_kind, eps) : 0.0f;
+          xk[u] = live ? phi_f(xk[u], phi_kind, eps) : 0.0f;
         }
         // the eight lanes of this row hold columns c % 32 = 4 spart .. of one word
         pos <<= (c & 31);
@@ -2209,7 +2237,7 @@ simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const _
                         const float* __restrict__ ztb) {
   constexpr int P = D + 4;
   constexpr int CP = kCbChunk + 4;
-  constexpr int E = D * D, PD = D + 1;
+  constexpr int E = D * D, PD = D + 4;     // the dnum / dden scratch row (16-byte aligned)
   constexpr int NMT = D / 16, NNT = D / 8; // 16 x 8 tiles of a D x D state
   constexpr int WPM = kCbWarps / NMT;      // warps per row tile of the state
   constexpr int NPW = NNT / WPM;           // state tiles per warp
@@ -2248,6 +2276,10 @@ simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const _
   const int srow = tid / kCbRowLanes, spart = tid % kCbRowLanes;
   const int64_t nb = token_of(g, j, 0);
   const int64_t nch = (g.w + kCbChunk - 1) / kCbChunk;
+  // rows that start on 8-byte boundaries load four bf16 at a time
+  const bool vec = ((reinterpret_cast<uintptr_t>(qb) | reinterpret_cast<uintptr_t>(kb) |
+                     reinterpret_cast<uintptr_t>(vb)) & 7) == 0 &&
+                   ((qo.sn | ko.sn | vo.sn) & 3) == 0;
   for (int64_t ci = nch - 1; ci >= 0; --ci) {
     const int64_t s0 = ci * kCbChunk;
     const int cnt = static_cast<int>(g.w - s0 < kCbChunk ? g.w - s0 : kCbChunk);
@@ -2258,15 +2290,30 @@ simt_causal_bwd_key_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const _
 #pragma unroll
       for (int c = 4 * spart; c < D; c += 4 * kCbRowLanes) {
         float xq[4], xn[4], xk[4], xv[4];
+        if (!live) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) xq[u] = xn[u] = xk[u] = xv[u] = 0.0f;
+        } else {
+          ldv<4>(dnb + (s0 + srow) * PD + c, xn);
+          if (vec) {
+            ld4_bf16(qb + n * qo.sn + c, xq);
+            ld4_bf16(kb + n * ko.sn + c, xk);
+            ld4_bf16(vb + n * vo.sn + c, xv);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              xq[u] = load_f(qb + n * qo.sn + c + u);
+              xk[u] = load_f(kb + n * ko.sn + c + u);
+              xv[u] = load_f(vb + n * vo.sn + c + u);
+            }
+          }
+        }
         uint32_t pos = 0;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float xr = live ? load_f(kb + n * ko.sn + c + u) : 0.0f;
-          pos |= (xr > 0.0f ? 1u : 0u) << u;
-          xq[u] = live ? phi_f(load_f(qb + n * qo.sn + c + u), phi_kind, eps) : 0.0f;
-          xn[u] = live ? dnb[(s0 + srow) * PD + c + u] : 0.0f;
-          xk[u] = live ? phi_f(xr, phi_kind, eps) : 0.0f;
-          xv[u] = live ? load_f(vb + n * vo.sn + c + u) : 0.0f;
+          pos |= (xk[u] > 0.0f ? 1u : 0u) << u;
+          xq[u] = live ? phi_f(xq[u], phi_kind, eps) : 0.0f;
+          xk[u] = live ? phi_f(xk[u], phi_kind, eps) : 0.0f;
         }
         pos <<= (c & 31);   // one word's columns over the eight lanes of this row
 #pragma unroll
@@ -2877,7 +2924,8 @@ size_t simt_causal_bwd_own_bytes(const Problem& p) {
   const size_t per = static_cast<size_t>(p.BH()) * p.M * p.d * (p.d + 1) * sizeof(float);
   const size_t part = static_cast<size_t>(p.BH()) * dw_splits(p) * p.M * p.M * sizeof(float);
   const size_t diag = static_cast<size_t>(p.BH()) * p.M * sizeof(float);
-  const size_t dn = static_cast<size_t>(p.BH()) * p.M * p.w * (p.d + 1) * sizeof(float);
+  // dnum / dden rows of d + 1 floats, at a stride of d + 4 on the bf16 warp-MMA kernels
+  const size_t dn = static_cast<size_t>(p.BH()) * p.M * p.w * (p.d + 4) * sizeof(float);
   return 3 * align_up(per) + align_up(part) + align_up(diag) + align_up(dn);
 }
 }  // namespace
