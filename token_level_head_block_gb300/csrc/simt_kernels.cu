@@ -1851,25 +1851,23 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
       den0 += eps;
       den1 += eps;
       const bool l0 = t0 < cnt, l1 = t1 < cnt;   // rows past the block stay zero
-      const float dd0 = l0 ? -(go0 / den0) / den0 : 0.0f;
-      const float dd1 = l1 ? -(go1 / den1) / den1 : 0.0f;
+      const float rd0 = 1.0f / den0, rd1 = 1.0f / den1;   // one division per token
+      const float dd0 = l0 ? -(go0 * rd0) * rd0 : 0.0f;
+      const float dd1 = l1 ? -(go1 * rd1) * rd1 : 0.0f;
       float dn0[V], dn1[V];
 #pragma unroll
       for (int w = 0; w < V; ++w) {
-        dn0[w] = l0 ? gva[w] / den0 : 0.0f;
-        dn1[w] = l1 ? gvc[w] / den1 : 0.0f;
-        x0[w] = fmaf(dd0, zv[w], u0[w] / den0);
-        x1[w] = fmaf(dd1, zv[w], u1[w] / den1);
+        dn0[w] = l0 ? gva[w] * rd0 : 0.0f;
+        dn1[w] = l1 ? gvc[w] * rd1 : 0.0f;
+        x0[w] = fmaf(dd0, zv[w], u0[w] * rd0);
+        x1[w] = fmaf(dd1, zv[w], u1[w] * rd1);
       }
       stv<V>(sdn + t0 * P + c0, dn0);
       stv<V>(sdn + t1 * P + c0, dn1);
       stv<V>(su + t0 * P + c0, x0);
       stv<V>(su + t1 * P + c0, x1);
-#pragma unroll
-      for (int w = 0; w < V; ++w) {
-        if (l0) dnb[(s0 + t0) * PD + c0 + w] = dn0[w];
-        if (l1) dnb[(s0 + t1) * PD + c0 + w] = dn1[w];
-      }
+      if (l0) stv<V>(dnb + (s0 + t0) * PD + c0, dn0);
+      if (l1) stv<V>(dnb + (s0 + t1) * PD + c0, dn1);
       if (cc == 0) {
         sdd[t0] = dd0;
         sdd[t1] = dd1;
@@ -1877,10 +1875,10 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
         if (l1) dnb[(s0 + t1) * PD + D] = dd1;
       }
       // b_ts = e_ts / den_t + dden_t (s <= t) in place of e_ts; dW_ii's own-chunk part
-      const float b0a = (l0 && cc <= t0) ? e0a / den0 + dd0 : 0.0f;
-      const float b0b = (l0 && cc + 16 <= t0) ? e0b / den0 + dd0 : 0.0f;
-      const float b1a = (l1 && cc <= t1) ? e1a / den1 + dd1 : 0.0f;
-      const float b1b = (l1 && cc + 16 <= t1) ? e1b / den1 + dd1 : 0.0f;
+      const float b0a = (l0 && cc <= t0) ? fmaf(e0a, rd0, dd0) : 0.0f;
+      const float b0b = (l0 && cc + 16 <= t0) ? fmaf(e0b, rd0, dd0) : 0.0f;
+      const float b1a = (l1 && cc <= t1) ? fmaf(e1a, rd1, dd1) : 0.0f;
+      const float b1b = (l1 && cc + 16 <= t1) ? fmaf(e1b, rd1, dd1) : 0.0f;
       se[t0 * CP + cc] = b0a;
       se[t0 * CP + cc + 16] = b0b;
       se[t1 * CP + cc] = b1a;
