@@ -1810,83 +1810,61 @@ simt_causal_bwd_query_mma(const __nv_bfloat16* __restrict__ q, Operand qo, const
     chunk_by_d(sg, P, D, [&](int n0, int k0, uint32_t(&bf)[2]) { frag_b_rows(st, P, n0, k0, lane, bf); }, su,
                0.0f);
     __syncthreads();
-    // ---- 3: per token (t0, t1 on the 16 lanes of a half-warp; columns / rows c0 ..):
-    // den_t, g_t . num_t, dnum_t, dden_t, b_ts, dW_ii's own-chunk part; the lane's
-    // entries of u_t are replaced by those of C dnum_t + dden_t c
+    // ---- 3: per token (tokens t0, t1 in turn on the 16 lanes of a half-warp; columns /
+    // rows c0 ..): den_t, g_t . num_t, dnum_t, dden_t, b_ts, dW_ii's own-chunk part; the
+    // lane's entries of u_t are replaced by those of C dnum_t + dden_t c, and of g_t by
+    // those of dnum_t
     {
-      float x0[V], x1[V];
-      float u0[V], u1[V];
-      ldv<V>(su + t0 * P + c0, u0);
-      ldv<V>(su + t1 * P + c0, u1);
-      float qa[V], qc[V], zv[V], gva[V], gvc[V];
-      ldv<V>(sq + t0 * P + c0, qa);
-      ldv<V>(sq + t1 * P + c0, qc);
+      float zv[V];
       ldv<V>(zs + c0, zv);
-      ldv<V>(sg + t0 * P + c0, gva);
-      ldv<V>(sg + t1 * P + c0, gvc);
-      float den0 = 0.0f, den1 = 0.0f, go0 = 0.0f, go1 = 0.0f;
+#pragma unroll 1
+      for (int tk = 0; tk < 2; ++tk) {
+        const int tq = t0 + tk;
+        float uu[V], qv[V], gv[V];
+        ldv<V>(su + tq * P + c0, uu);
+        ldv<V>(sq + tq * P + c0, qv);
+        ldv<V>(sg + tq * P + c0, gv);
+        float den = 0.0f, gov = 0.0f;
 #pragma unroll
-      for (int w = 0; w < V; ++w) {
-        den0 = fmaf(qa[w], zv[w], den0);
-        den1 = fmaf(qc[w], zv[w], den1);
-        go0 = fmaf(qa[w], u0[w], go0);
-        go1 = fmaf(qc[w], u1[w], go1);
-      }
-      // this lane's own-chunk sources s = cc, cc + 16
-      const float a0a = sa[t0 * CP + cc], a0b = sa[t0 * CP + cc + 16];
-      const float a1a = sa[t1 * CP + cc], a1b = sa[t1 * CP + cc + 16];
-      const float e0a = se[t0 * CP + cc], e0b = se[t0 * CP + cc + 16];
-      const float e1a = se[t1 * CP + cc], e1b = se[t1 * CP + cc + 16];
-      den0 = fmaf(wii, a0a + a0b, den0);
-      den1 = fmaf(wii, a1a + a1b, den1);
-      go0 = fmaf(wii, fmaf(a0a, e0a, a0b * e0b), go0);
-      go1 = fmaf(wii, fmaf(a1a, e1a, a1b * e1b), go1);
+        for (int w = 0; w < V; ++w) {
+          den = fmaf(qv[w], zv[w], den);
+          gov = fmaf(qv[w], uu[w], gov);
+        }
+        // this lane's own-chunk sources s = cc, cc + 16
+        const float aa = sa[tq * CP + cc], ab = sa[tq * CP + cc + 16];
+        const float ea = se[tq * CP + cc], eb = se[tq * CP + cc + 16];
+        den = fmaf(wii, aa + ab, den);
+        gov = fmaf(wii, fmaf(aa, ea, ab * eb), gov);
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) {   // the 16 lanes of this half-warp share t0, t1
-        den0 += __shfl_xor_sync(0xffffffffu, den0, off);
-        den1 += __shfl_xor_sync(0xffffffffu, den1, off);
-        go0 += __shfl_xor_sync(0xffffffffu, go0, off);
-        go1 += __shfl_xor_sync(0xffffffffu, go1, off);
-      }
-      den0 += eps;
-      den1 += eps;
-      const bool l0 = t0 < cnt, l1 = t1 < cnt;   // rows past the block stay zero
-      const float rd0 = 1.0f / den0, rd1 = 1.0f / den1;   // one division per token
-      const float dd0 = l0 ? -(go0 * rd0) * rd0 : 0.0f;
-      const float dd1 = l1 ? -(go1 * rd1) * rd1 : 0.0f;
-      float dn0[V], dn1[V];
+        for (int off = 8; off > 0; off >>= 1) {   // the 16 lanes of this half-warp share the token
+          den += __shfl_xor_sync(0xffffffffu, den, off);
+          gov += __shfl_xor_sync(0xffffffffu, gov, off);
+        }
+        den += eps;
+        const bool live = tq < cnt;   // rows past the block stay zero
+        const float rd = 1.0f / den;  // one division per token
+        const float dd = live ? -(gov * rd) * rd : 0.0f;
+        float dnv[V], xv[V];
 #pragma unroll
-      for (int w = 0; w < V; ++w) {
-        dn0[w] = l0 ? gva[w] * rd0 : 0.0f;
-        dn1[w] = l1 ? gvc[w] * rd1 : 0.0f;
-        x0[w] = fmaf(dd0, zv[w], u0[w] * rd0);
-        x1[w] = fmaf(dd1, zv[w], u1[w] * rd1);
+        for (int w = 0; w < V; ++w) {
+          dnv[w] = live ? gv[w] * rd : 0.0f;
+          xv[w] = fmaf(dd, zv[w], uu[w] * rd);
+        }
+        stv<V>(sdn + tq * P + c0, dnv);
+        stv<V>(su + tq * P + c0, xv);
+        if (live) stv<V>(dnb + (s0 + tq) * PD + c0, dnv);
+        if (cc == 0) {
+          sdd[tq] = dd;
+          if (live) dnb[(s0 + tq) * PD + D] = dd;
+        }
+        // b_ts = e_ts / den_t + dden_t (s <= t) in place of e_ts; dW_ii's own-chunk part
+        const float ba = (live && cc <= tq) ? fmaf(ea, rd, dd) : 0.0f;
+        const float bb = (live && cc + 16 <= tq) ? fmaf(eb, rd, dd) : 0.0f;
+        se[tq * CP + cc] = ba;
+        se[tq * CP + cc + 16] = bb;
+        dw = fmaf(aa, ba, dw);
+        dw = fmaf(ab, bb, dw);
       }
-      stv<V>(sdn + t0 * P + c0, dn0);
-      stv<V>(sdn + t1 * P + c0, dn1);
-      stv<V>(su + t0 * P + c0, x0);
-      stv<V>(su + t1 * P + c0, x1);
-      if (l0) stv<V>(dnb + (s0 + t0) * PD + c0, dn0);
-      if (l1) stv<V>(dnb + (s0 + t1) * PD + c0, dn1);
-      if (cc == 0) {
-        sdd[t0] = dd0;
-        sdd[t1] = dd1;
-        if (l0) dnb[(s0 + t0) * PD + D] = dd0;
-        if (l1) dnb[(s0 + t1) * PD + D] = dd1;
-      }
-      // b_ts = e_ts / den_t + dden_t (s <= t) in place of e_ts; dW_ii's own-chunk part
-      const float b0a = (l0 && cc <= t0) ? fmaf(e0a, rd0, dd0) : 0.0f;
-      const float b0b = (l0 && cc + 16 <= t0) ? fmaf(e0b, rd0, dd0) : 0.0f;
-      const float b1a = (l1 && cc <= t1) ? fmaf(e1a, rd1, dd1) : 0.0f;
-      const float b1b = (l1 && cc + 16 <= t1) ? fmaf(e1b, rd1, dd1) : 0.0f;
-      se[t0 * CP + cc] = b0a;
-      se[t0 * CP + cc + 16] = b0b;
-      se[t1 * CP + cc] = b1a;
-      se[t1 * CP + cc + 16] = b1b;
-      dw = fmaf(a0a, b0a, dw);
-      dw = fmaf(a0b, b0b, dw);
-      dw = fmaf(a1a, b1a, dw);
-      dw = fmaf(a1b, b1b, dw);
     }
     __syncthreads();
     // ---- 4: su += W_ii B phi(K) (B[s][r] = phi(k_s)[r], rows of phi(K)): dq before its mask
