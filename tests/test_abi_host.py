@@ -292,9 +292,9 @@ def test_backward_workspace_size(L):
     assert simt <= sizes[1] < simt + 4 * 256
     groups = (BH * (d + 1) * d + 127) // 128
     tc = 2 * M * M * 2 + 2 * M * groups * 128 * 2 + BH * M * d * d * 2 + BH * M * d * 4
-    # + the dW partial products: one 256 x 256 tile of dW (M = 256) split over up to 152 CTAs
+    # + the dW partial products: one 256 x 256 tile of dW (M = 256) split over up to 100 CTAs
     tiles = ((M + 255) // 256) ** 2
-    nsplit = min(groups, -(-152 // tiles))
+    nsplit = min(groups, -(-100 // tiles))
     assert tc < sizes[2] <= tc + nsplit * M * M * 4 + 8 * 256
     assert sizes[0] == max(sizes[1], sizes[2])                         # AUTO: enough for either path
     assert L.mhla_backward_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(wl.grid)),
@@ -381,7 +381,7 @@ def test_causal_backward_rejects_malformed_requests_before_any_launch(L):
     KS = 16  # the dW partial products split d (d + 1) = 4160 entries in 16 runs (6 tiles are too few CTAs)
     need = 3 * BH * M * d * (d + 1) * 4 + BH * KS * M * M * 4 + BH * M * 4 + BH * N * (d + 4) * 4
     groups = (BH * (d + 1) * d + 127) // 128
-    nsplit = min(groups, 152)   # the tensor-core dW product's splits (one 256 x 256 tile here)
+    nsplit = min(groups, 152)   # the tensor-core dW product's splits (a small tile: one per SM)
     tc = M * M * 2 + M * groups * 128 * 2 + BH * M * d * d * 2 + BH * M * d * 4 + nsplit * M * M * 4
     for path, extra in ((0, tc), (1, 0), (2, tc)):
         assert L.mhla_backward_causal_workspace_size(ctypes.byref(q), ctypes.byref(mhla.shape3(grid)),

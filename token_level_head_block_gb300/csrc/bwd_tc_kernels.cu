@@ -1068,9 +1068,12 @@ struct BwdLayout {
   int32_t n_it, n_jt, JN, nsplit;
 };
 
-// CTAs the dW product is split over (about one per SM of a GB300); a constant,
-// so that the workspace size does not depend on the device.
-constexpr int64_t kDwTargetCtas = 152;
+// CTAs the dW product is split over: every split writes an M x M float32 tile
+// that the reduction reads back, so large tiles take about two thirds of a
+// GB300's SMs (M = 256, DiT-S/2: 152 splits 46 us, 100: 40, 38: 49) and small ones
+// one per SM (M = 64: 152 splits 27 us, 100: 30); constants, so that the workspace
+// size does not depend on the device.
+inline int64_t dw_target_ctas(int64_t M) { return M >= 192 ? 100 : 152; }
 
 BwdLayout bwd_layout(const Problem& p) {
   BwdLayout L;
@@ -1082,7 +1085,7 @@ BwdLayout bwd_layout(const Problem& p) {
   L.JN = static_cast<int32_t>(std::min<int64_t>(DwCfg::JT, (p.M + 15) / 16 * 16));
   const int64_t tiles = static_cast<int64_t>(L.n_it) * L.n_jt;
   L.nsplit = static_cast<int32_t>(
-      std::max<int64_t>(1, std::min<int64_t>(L.ngroups, (kDwTargetCtas + tiles - 1) / tiles)));
+      std::max<int64_t>(1, std::min<int64_t>(L.ngroups, (dw_target_ctas(p.M) + tiles - 1) / tiles)));
   size_t off = 0;
   L.wb_off = off;
   off += align_up(static_cast<size_t>(p.M) * L.Mp * 2);
