@@ -58,6 +58,28 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   volatile uint32_t* abortf = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    sum_init<D>(bars);
+    *abortf = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  sum_fill_ones<D>(stages, threadIdx.x, kTcThreads);
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // Launched as a dependent grid: the set-up above overlaps the previous kernel's
+  // tail; W, k and v (which that kernel may have written) are read only after it.
+  grid_dep_wait();
   // W rounded to bf16 for the mixing GEMM, [M][Mp] with zero padding (and, when
   // WbT is given, W^T likewise); every CTA converts a slice (the GEMM runs after
   // this kernel on the same stream).  Wb null: summaries only.  upb > 0: the
@@ -82,25 +104,6 @@ tc_summary(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
       if (WbT) WbT[e] = __float2bfloat16_rn(j < g.M ? W[j * g.M + i] : 0.0f);   // W^T for the backward
     }
   }
-  if (threadIdx.x == 0) {
-    sum_init<D>(bars);
-    *abortf = 0u;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-    tmem_relinquish();
-  }
-  sum_fill_ones<D>(stages, threadIdx.x, kTcThreads);
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
   summary_roles<D>(&tm_k, &tm_v, g, G, blockIdx.x, gridDim.x, n_items, phi_kind, eps, Sbuf, stages, bars, tmem,
                    abortf, &g_sum_error, nullptr);
   tc_fence_before();
@@ -131,9 +134,10 @@ int run_summary(const Problem& p, const float* W, __nv_bfloat16* Wb, __nv_bfloat
   const int per_sm = std::max(1, occupancy(tc_summary<D>, kTcThreads, SMEM));
   const int grid = static_cast<int>(std::min<int64_t>(n_items, static_cast<int64_t>(sms) * per_sm));
   KernelTimer timer("tc_summary", stream);
-  tc_summary<D><<<grid, kTcThreads, SMEM, stream>>>(tk, tv, make_geom(p, c64), G, n_items, p.phi_kind, p.eps,
-                                                         Sbuf, W, Wb, WbT, Mp, Mw, upb);
-  return cudaGetLastError() == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
+  const cudaError_t e = launch_dependent(tc_summary<D>, dim3(grid), dim3(kTcThreads), SMEM, stream, tk, tv,
+                                         make_geom(p, c64), G, n_items, p.phi_kind, p.eps, Sbuf, W, Wb, WbT, Mp, Mw,
+                                         upb);
+  return e == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA;
 }
 
 }  // namespace
