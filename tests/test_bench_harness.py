@@ -81,3 +81,24 @@ def test_reference_arm_prints_one_contract_line(pass_):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_rotation_keeps_small_steps_out_of_l2():
+    import torch
+
+    l2 = 1000
+    # a step that alone moves more than 1.5x L2: one set, the tensors themselves
+    big = [torch.zeros(2000, dtype=torch.uint8)]
+    sets, nbytes = bench.rotation(big, l2)
+    assert len(sets) == 1 and sets[0][0] is big[0] and nbytes == 2000
+    # a small step: enough copies that a set is touched again only after > 1.5x L2
+    q, o = torch.arange(50, dtype=torch.int32), torch.zeros(50, dtype=torch.int32)   # 400 bytes a step
+    sets, nbytes = bench.rotation([q, o], l2)
+    assert nbytes == 400
+    assert (len(sets) - 1) * nbytes > 1.5 * l2
+    assert sets[0][0] is q
+    for s in sets[1:]:
+        assert torch.equal(s[0], q) and s[0].data_ptr() != q.data_ptr() and s[1].data_ptr() != o.data_ptr()
+    # never more than the cap
+    sets, _ = bench.rotation([torch.zeros(1, dtype=torch.uint8)], l2)
+    assert len(sets) == bench.ROTATE_CAP

@@ -33,7 +33,9 @@
 //            into the denominator; each warpgroup scales half of the output
 //            columns by 1 / (den + eps), rounds to bf16 and stores them.
 // The next unit's q and k tiles load once MMA 1 has read the current ones, its
-// values once MMA 2 has; the first unit's loads overlap the set-up of W.
+// values once MMA 2 has; the first unit's loads overlap the set-up of W.  The
+// workers apply phi to the next unit between forming P and writing the output,
+// so that phi runs under MMA 2 and the next unit's MMA 1 under the output.
 //
 // Every wait is bounded (2 s of %globaltimer, 2^28 polls); a wait that gives
 // up sets bit 0 of this file's device error word and a per-CTA abort flag so
@@ -265,21 +267,25 @@ tc_small(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
+      // MMA 1 (scores) of the unit whose phi the workers have just applied
+      auto issue_mma1 = [&]() {
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(128, g.KR, /*a K-major*/ false, /*b K-major*/ false);
+        const uint32_t qa = smem_u32(sq), ka = smem_u32(sk);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_bf16(tmem, smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
+                   smem_desc(ka + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT), idesc, ks > 0 ? 1u : 0u);
+        mma_commit(done1);
+        ++n_m1;
+      };
+      if (static_cast<int64_t>(blockIdx.x) < n_units) {
+        if (small_wait(phid, 0u, abortf)) issue_mma1();
+        else ok = false;
+      }
       for (int64_t u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++it) {
         const uint32_t par = it & 1u;
         const int64_t next = u + gridDim.x;
-        if (!small_wait(phid, par, abortf)) break;
-        tc_fence_after();
-        {
-          const uint32_t idesc = idesc_bf16_f32(128, g.KR, /*a K-major*/ false, /*b K-major*/ false);
-          const uint32_t qa = smem_u32(sq), ka = smem_u32(sk);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem, smem_desc(qa + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
-                     smem_desc(ka + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT), idesc, ks > 0 ? 1u : 0u);
-          mma_commit(done1);
-          ++n_m1;
-        }
         if (!small_wait(done1, par, abortf)) break;
         if (next < n_units) {   // q and k consumed: the next unit's may land
           issue_qk(next);
@@ -303,6 +309,12 @@ tc_small(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         if (!ok) break;
         mma_commit(done2);
         ++n_m2;
+        // The next unit's scores go in behind MMA 2 as soon as its phi is
+        // applied: the workers have read this unit's scores before that.
+        if (next < n_units) {
+          if (!small_wait(phid, par ^ 1u, abortf)) break;
+          issue_mma1();
+        }
         if (!small_wait(done2, par, abortf)) break;
         if (next < n_units) {   // values consumed
           issue_v(next);
@@ -325,8 +337,22 @@ tc_small(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
     const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
     const int swr = row & 7;                // 128-byte swizzle phase of this thread's P row
     const int n16 = (kQRows + g.KR) * Cfg::ROWB / 16;
+    // phi in place over the q and k tiles (contiguous) of the unit with
+    // copy phase par; false when the wait gives up
+    auto apply_phi = [&](uint32_t par) {
+      if (!small_warp_wait(full_qk, par, abortf)) return false;
+      uint4* base = reinterpret_cast<uint4*>(sq);
+      for (int e = tid; e < n16; e += kWorkers) base[e] = phi8(base[e], add_eps, eps2);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(phid);
+      return true;
+    };
+    // Per unit: P, then phi of the next unit (under MMA 2), then the output
+    // (under the next unit's MMA 1).
     uint32_t it = 0;
-    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+    bool live = static_cast<int64_t>(blockIdx.x) >= n_units || apply_phi(0u);
+    for (int64_t u = blockIdx.x; live && u < n_units; u += gridDim.x, ++it) {
       const uint32_t par = it & 1u;
       const uint32_t uu = static_cast<uint32_t>(u);
       const int32_t qt = static_cast<int32_t>(uu % static_cast<uint32_t>(g.nqt));
@@ -334,39 +360,39 @@ tc_small(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
       const int32_t h = static_cast<int32_t>(bh % static_cast<uint32_t>(g.H));
       const int32_t b = static_cast<int32_t>(bh / static_cast<uint32_t>(g.H));
 
-      // ---- phi in place over the q and k tiles (contiguous)
-      if (!small_warp_wait(full_qk, par, abortf)) break;
-      {
-        uint4* base = reinterpret_cast<uint4*>(sq);
-        for (int e = tid; e < n16; e += kWorkers) base[e] = phi8(base[e], add_eps, eps2);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(phid);
-
       // ---- P[t][s] = score * W[b(t)][b(s)], bf16, K-major SW128, 64 keys per chunk
       if (!small_warp_wait(done1, par, abortf)) break;
       tc_fence_after();
       const int32_t nq = qt * kQRows + row;
       const uint8_t* wrow =
           reinterpret_cast<const uint8_t*>(sw) + (nq < g.N ? soff[nq] / 4 : 0) * (g.M + 1) * 4;
-      for (int c = 0; c < n_chunks; ++c) {
+      // two score buffers: the tensor-memory load of chunk c + 1 is in flight
+      // while chunk c is weighted (n_chunks <= 4, so the loop unrolls fully)
+      const int mlim = g.KR / 32;
+      uint32_t r[2][32];
+      if (half < mlim) tmem_ld_x32(lane_base + half * 32, r[0]);
+#pragma unroll
+      for (int c = 0; c < kMaxKeys / 64; ++c) {
+        if (c >= n_chunks) break;
         const int m = 2 * c + half;         // 32 keys of this warpgroup in chunk c
-        if (m < g.KR / 32) {
-          uint32_t r[32];
-          tmem_ld_x32(lane_base + m * 32, r);
-          uint4 offs[4];
+        uint4 offs[4];
+        if (m < mlim) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) offs[i] = reinterpret_cast<const uint4*>(soff + m * 32)[i];
-          tmem_ld_wait();
+        }
+        tmem_ld_wait();                     // chunk c's scores (the only load in flight)
+        if (c + 1 < kMaxKeys / 64 && c + 1 < n_chunks && m + 2 < mlim)
+          tmem_ld_x32(lane_base + (m + 2) * 32, r[(c + 1) & 1]);
+        if (m < mlim) {
           const uint32_t* ow = reinterpret_cast<const uint32_t*>(offs);
+          const uint32_t* rc = r[c & 1];
           uint32_t packed[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const uint32_t o2 = ow[e >> 1];
             const float w0 = *reinterpret_cast<const float*>(wrow + (o2 & 0xFFFFu));
             const float w1 = *reinterpret_cast<const float*>(wrow + (o2 >> 16));
-            packed[e >> 1] = pack2(__uint_as_float(r[e]) * w0, __uint_as_float(r[e + 1]) * w1);
+            packed[e >> 1] = pack2(__uint_as_float(rc[e]) * w0, __uint_as_float(rc[e + 1]) * w1);
           }
           uint8_t* prow = sp + c * Cfg::P_CHUNK + row * 128;
 #pragma unroll
@@ -379,6 +405,10 @@ tc_small(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUten
         __syncwarp();
         if (lane == 0) mbar_arrive(chunk + c);
       }
+      tmem_ld_wait();                       // nothing left in flight (no-op when none was issued)
+
+      // ---- the next unit's phi, while MMA 2 of this one runs
+      if (u + gridDim.x < n_units && !apply_phi(par ^ 1u)) break;
 
       // ---- output: o_t = (P V)_t / (P 1)_t + eps), this warpgroup's half of the columns
       if (!small_warp_wait(done2, par, abortf)) break;
