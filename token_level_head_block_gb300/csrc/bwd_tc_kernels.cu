@@ -629,10 +629,16 @@ struct BkCfg {
   static constexpr size_t SMEM = CTRL_OFF + 128 + 1024;
   static constexpr int TMEM_COLS = 256;           // per head: dv (D columns), dphi(k) (D columns)
 };
-constexpr int kBkThreads = 256;
+constexpr int kBkThreads = 256;                 // warps 0-7: phi, MMA issue (thread 0), epilogue
+constexpr int kBkAll = kBkThreads + 32;          // + warp 8: stores and k, v loads
+constexpr uint32_t kBkBar = 1;                   // named barrier of warps 0-7
 
+// Warps 0-7 take every chunk through phi, the MMAs and the epilogue; warp 8
+// stores a chunk's dk, dv as soon as its epilogue is written and loads the
+// chunk two ahead into the stage once the stores have read it, so each load
+// has a whole chunk of work to land under.
 template <int D>
-__global__ void __launch_bounds__(kBkThreads, 1)
+__global__ void __launch_bounds__(kBkAll, 1)
 tc_bwd_key(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
            const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
            const __grid_constant__ CUtensorMap tm_ds, TcGeom g, int32_t G, int64_t n_items, int phi_kind,
@@ -650,7 +656,8 @@ tc_bwd_key(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
   uint64_t* bl = reinterpret_cast<uint64_t*>(smem + Cfg::CTRL_OFF);   // [2] k, v tiles landed
   uint64_t* bs = bl + 2;                                               // dS, dz of an item landed
   uint64_t* bm = bl + 3;                                               // MMAs complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bl + 4);
+  uint64_t* be = bl + 4;                                               // [2] dk, dv of the stage written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bl + 6);
   volatile uint32_t* abortf = tmem_slot + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -659,6 +666,8 @@ tc_bwd_key(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     mbar_init(bl + 1, 1);
     mbar_init(bs, 1);
     mbar_init(bm, 1);
+    mbar_init(be, 1);
+    mbar_init(be + 1, 1);
     *abortf = 0u;
     fence_mbar_init();
     prefetch_tmap(&tm_k);
@@ -672,13 +681,13 @@ tc_bwd_key(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     tmem_relinquish();
   }
   // ones extension of v (K columns 0, 1 = 1 for every token) and the dz tiles
-  for (int e = tid; e < Cfg::EXT / 16; e += kBkThreads) {
+  for (int e = tid; e < Cfg::EXT / 16; e += kBkAll) {
     const int r = e / 8, p = e % 8;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if ((p ^ swz128(r)) == 0) v.x = 0x3F803F80u;   // bf16 1.0, 1.0
     reinterpret_cast<uint4*>(ones)[e] = v;
   }
-  for (int e = tid; e < HP * Cfg::ZB / 16; e += kBkThreads)
+  for (int e = tid; e < HP * Cfg::ZB / 16; e += kBkAll)
     reinterpret_cast<uint4*>(zb)[e] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   tc_fence_before();
@@ -723,168 +732,193 @@ tc_bwd_key(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUt
     }
   };
 
-  uint32_t n_l[2] = {0, 0}, n_s = 0, n_m = 0;
-  uint32_t c_l[2] = {0, 0}, c_s = 0, c_m = 0;
-  uint32_t chunk_no = 0;   // chunks processed by this CTA (stage = chunk_no & 1)
-  if (tid == 0 && static_cast<int64_t>(blockIdx.x) < n_items) {
-    issue_ds(blockIdx.x);
-    issue_kv(0, blockIdx.x, 0);
-    n_s = n_l[0] = 1;
-  }
-  const bool add_eps = phi_kind == MHLA_PHI_RELU_EPS;
-  const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
-  const int row = 32 * (warp & 3) + lane;
-  const int wg = warp >> 2;
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-  bool ok = true;
-
-  for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-    int32_t grp, j, b;
-    item_coords(item, grp, j, b);
-    if (!__syncthreads_and(bwait(bs, c_s & 1u, abortf))) break;
-    ++c_s;
-    if (tid < HP * D) {   // dz hi, lo into K columns 0, 1 of row r of the extension
-      const int hh = tid / D, r = tid % D;
-      const float zv = grp * HP + hh < g.H ? zraw[hh * D + r] : 0.0f;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
-      *reinterpret_cast<uint32_t*>(zb + hh * Cfg::ZB + r * 128 + swz128(r) * 16) =
-          static_cast<uint32_t>(__bfloat16_as_ushort(hi)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    for (int c = 0; c < g.chunks; ++c, ++chunk_no) {
-      const int st = chunk_no & 1;
-      uint8_t* kt = stages + st * Cfg::STAGE;
-      uint8_t* vt = kt + Cfg::HT;
-      uint8_t* mask = masks + st * Cfg::MASK_BYTES;
-      const bool last = c + 1 == g.chunks;
-      const int64_t nitem = last ? item + gridDim.x : item;
-      const int nc = last ? 0 : c + 1;
-      const bool has_next = nitem < n_items;
-      if (!__syncthreads_and(bwait(bl + st, c_l[st] & 1u, abortf))) { ok = false; break; }
-      ++c_l[st];
-      // ---- phi in place on the k tiles, and the k > 0 bits
-      for (int e = tid; e < Cfg::HT / 16; e += kBkThreads) {
-        const int hh = e / (Cfg::TILE / 16), rem = e % (Cfg::TILE / 16);
-        const int t = rem / (D / 8), p = rem % (D / 8);
-        uint4* ptr = reinterpret_cast<uint4*>(kt) + e;
-        const uint4 raw = *ptr;
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t bits = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
-          bits |= (__low2float(v2) > 0.0f ? 1u : 0u) << (2 * k);
-          bits |= (__high2float(v2) > 0.0f ? 1u : 0u) << (2 * k + 1);
+  if (warp == kBkThreads / 32) {
+    // ------------------------------------------------ stores and k, v loads
+    if (lane == 0) {
+      uint32_t n_l[2] = {0, 0};
+      // the chunk sequence of this CTA: (item, c) in order, k = position
+      int64_t l_item = blockIdx.x;     // next chunk to load
+      int l_c = 0;
+      auto load_next = [&](int st) {
+        if (l_item >= n_items) return;
+        issue_kv(st, l_item, l_c);
+        ++n_l[st];
+        if (++l_c == g.chunks) { l_c = 0; l_item += gridDim.x; }
+      };
+      load_next(0);
+      load_next(1);
+      uint32_t k = 0;
+      for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+        int32_t grp, j, b;
+        item_coords(item, grp, j, b);
+        bool ok = true;
+        for (int c = 0; c < g.chunks; ++c, ++k) {
+          const int st = static_cast<int>(k & 1u);
+          if (!bwait(be + st, (k >> 1) & 1u, abortf)) { ok = false; break; }
+          uint8_t* kt = stages + st * Cfg::STAGE;
+          uint8_t* vt = kt + Cfg::HT;
+          int32_t x, y, z;
+          chunk_coords(g, j, c, b, x, y, z);
+          for (int hh = 0; hh < HP; ++hh) {
+            if (grp * HP + hh >= g.H) continue;
+            tma_store_5d_hint(&tm_dk, kt + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z, policy_evict_first());
+            tma_store_5d_hint(&tm_dv, vt + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z, policy_evict_first());
+          }
+          bulk_commit_group();
+          if (l_item < n_items) {
+            bulk_wait_group_read<0>();   // the stores have read the stage: the chunk two ahead loads into it
+            load_next(st);
+          }
         }
-        mask[(hh * Cfg::C + t) * (D / 8) + (p ^ swz<D>(t))] = static_cast<uint8_t>(bits);
-        *ptr = phi8_packed(raw, add_eps, eps2);
+        if (!ok) break;
+      }
+      bulk_wait_group0();
+      for (int st = 0; st < 2; ++st)
+        if (n_l[st]) bdrain(bl + st, (n_l[st] - 1) & 1u);
+    }
+  } else {
+    // ------------------------------------------------ warps 0-7
+    uint32_t n_s = 0, n_m = 0, c_s = 0, c_m = 0;
+    uint32_t c_l[2] = {0, 0};
+    uint32_t chunk_no = 0;   // chunks processed by this CTA (stage = chunk_no & 1)
+    if (tid == 0 && static_cast<int64_t>(blockIdx.x) < n_items) {
+      issue_ds(blockIdx.x);
+      n_s = 1;
+    }
+    const bool add_eps = phi_kind == MHLA_PHI_RELU_EPS;
+    const __nv_bfloat162 eps2 = __float2bfloat162_rn(eps);
+    const int row = 32 * (warp & 3) + lane;
+    const int wg = warp >> 2;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    bool ok = true;
+
+    for (int64_t item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      int32_t grp, j, b;
+      item_coords(item, grp, j, b);
+      if (!named_bar_and(kBkBar, kBkThreads, bwait(bs, c_s & 1u, abortf))) break;
+      ++c_s;
+      if (tid < HP * D) {   // dz hi, lo into K columns 0, 1 of row r of the extension
+        const int hh = tid / D, r = tid % D;
+        const float zv = grp * HP + hh < g.H ? zraw[hh * D + r] : 0.0f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(zv);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(zv - __bfloat162float(hi));
+        *reinterpret_cast<uint32_t*>(zb + hh * Cfg::ZB + r * 128 + swz128(r) * 16) =
+            static_cast<uint32_t>(__bfloat16_as_ushort(hi)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16);
       }
       fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
+      named_bar_sync(kBkBar, kBkThreads);
 
-      if (tid == 0) {
-        tc_fence_after();
-        // MMA D: dv = phi(k) dS;  MMA E: dphi(k) = [v | 1 1] [dS^T ; dz hi lo]
-        constexpr uint32_t idd = idesc_bf16_f32(128, D, /*a K-major*/ false, /*b MN-major*/ true);
-        constexpr uint32_t ide = idesc_bf16_f32(128, D, /*a K-major*/ false, /*b K-major*/ false);
-#pragma unroll
-        for (int hh = 0; hh < HP; ++hh) {
-          const uint32_t ka = smem_u32(kt + hh * Cfg::TILE), va = smem_u32(vt + hh * Cfg::TILE);
-          const uint32_t sb = smem_u32(dst + hh * Cfg::ST);
-          const uint32_t dvc = tmem + hh * 2 * D, dkc = dvc + D;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            mma_bf16(dvc, smem_desc(ka + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
-                     smem_desc(sb + ks * 2 * Cfg::SBO, Cfg::ST, Cfg::SBO, Cfg::LAYOUT), idd, ks > 0 ? 1u : 0u);
-            mma_bf16(dkc, smem_desc(va + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
-                     smem_desc(sb + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT), ide, ks > 0 ? 1u : 0u);
-          }
-          mma_bf16(dkc, smem_desc(smem_u32(ones), 16, 1024, 2), smem_desc(smem_u32(zb + hh * Cfg::ZB), 16, 1024, 2),
-                   ide, 1u);
-        }
-        mma_commit(bm);
-        ++n_m;
-        // the other stage: its dk, dv stores must have read it, then the next chunk loads into it
-        if (has_next) {
-          bulk_wait_group_read<0>();
-          issue_kv(st ^ 1, nitem, nc);
-          ++n_l[st ^ 1];
-        }
-      }
-      if (!__syncthreads_and(bwait(bm, c_m & 1u, abortf))) { ok = false; break; }
-      ++c_m;
-      tc_fence_after();
-      if (tid == 0 && has_next && last) {   // dS, dz consumed by this item's last MMAs
-        issue_ds(nitem);
-        ++n_s;
-      }
-
-      // ---- epilogue: dv into the v tiles, dk = dphi(k) * [k > 0] into the k tiles
-      for (int hh = wg; hh < HP; hh += 2) {
-        uint32_t a[D];
-        if constexpr (D == 64) {
-          tmem_ld_x32(lane_base + hh * 2 * D, *reinterpret_cast<uint32_t(*)[32]>(a));
-          tmem_ld_x32(lane_base + hh * 2 * D + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
-        } else {
-          tmem_ld_x32(lane_base + hh * 2 * D, *reinterpret_cast<uint32_t(*)[32]>(a));
-        }
-        tmem_ld_wait();
-        uint8_t* vrow = vt + hh * Cfg::TILE + row * Cfg::ROWB;
-#pragma unroll
-        for (int u = 0; u < D / 8; ++u)
-          *reinterpret_cast<uint4*>(vrow + ((u ^ swz<D>(row)) * 16)) =
-              make_uint4(pack_bf16(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1])),
-                         pack_bf16(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3])),
-                         pack_bf16(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5])),
-                         pack_bf16(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7])));
-        if constexpr (D == 64) {
-          tmem_ld_x32(lane_base + hh * 2 * D + D, *reinterpret_cast<uint32_t(*)[32]>(a));
-          tmem_ld_x32(lane_base + hh * 2 * D + D + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
-        } else {
-          tmem_ld_x32(lane_base + hh * 2 * D + D, *reinterpret_cast<uint32_t(*)[32]>(a));
-        }
-        tmem_ld_wait();
-        const uint8_t* mrow = mask + (hh * Cfg::C + row) * (D / 8);
-        uint8_t* krow = kt + hh * Cfg::TILE + row * Cfg::ROWB;
-#pragma unroll
-        for (int u = 0; u < D / 8; ++u) {
-          const uint32_t bits = mrow[u];
-          uint32_t ow[4];
+      for (int c = 0; c < g.chunks; ++c, ++chunk_no) {
+        const int st = chunk_no & 1;
+        uint8_t* kt = stages + st * Cfg::STAGE;
+        uint8_t* vt = kt + Cfg::HT;
+        uint8_t* mask = masks + st * Cfg::MASK_BYTES;
+        const bool last = c + 1 == g.chunks;
+        const int64_t nitem = item + gridDim.x;
+        if (!named_bar_and(kBkBar, kBkThreads, bwait(bl + st, c_l[st] & 1u, abortf))) { ok = false; break; }
+        ++c_l[st];
+        // ---- phi in place on the k tiles, and the k > 0 bits
+        for (int e = tid; e < Cfg::HT / 16; e += kBkThreads) {
+          const int hh = e / (Cfg::TILE / 16), rem = e % (Cfg::TILE / 16);
+          const int t = rem / (D / 8), p = rem % (D / 8);
+          uint4* ptr = reinterpret_cast<uint4*>(kt) + e;
+          const uint4 raw = *ptr;
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t bits = 0;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float a0 = (bits >> (2 * k)) & 1u ? __uint_as_float(a[8 * u + 2 * k]) : 0.0f;
-            const float a1 = (bits >> (2 * k + 1)) & 1u ? __uint_as_float(a[8 * u + 2 * k + 1]) : 0.0f;
-            ow[k] = pack_bf16(a0, a1);
+            const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+            bits |= (__low2float(v2) > 0.0f ? 1u : 0u) << (2 * k);
+            bits |= (__high2float(v2) > 0.0f ? 1u : 0u) << (2 * k + 1);
           }
-          *reinterpret_cast<uint4*>(krow + ((u ^ swz<D>(row)) * 16)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+          mask[(hh * Cfg::C + t) * (D / 8) + (p ^ swz<D>(t))] = static_cast<uint8_t>(bits);
+          *ptr = phi8_packed(raw, add_eps, eps2);
         }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) {
-        int32_t x, y, z;
-        chunk_coords(g, j, c, b, x, y, z);
-        for (int hh = 0; hh < HP; ++hh) {
-          if (grp * HP + hh >= g.H) continue;
-          tma_store_5d_hint(&tm_dk, kt + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z, policy_evict_first());
-          tma_store_5d_hint(&tm_dv, vt + hh * Cfg::TILE, 0, grp * HP + hh, x, y, z, policy_evict_first());
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(kBkBar, kBkThreads);
+
+        if (tid == 0) {
+          tc_fence_after();
+          // MMA D: dv = phi(k) dS;  MMA E: dphi(k) = [v | 1 1] [dS^T ; dz hi lo]
+          constexpr uint32_t idd = idesc_bf16_f32(128, D, /*a K-major*/ false, /*b MN-major*/ true);
+          constexpr uint32_t ide = idesc_bf16_f32(128, D, /*a K-major*/ false, /*b K-major*/ false);
+#pragma unroll
+          for (int hh = 0; hh < HP; ++hh) {
+            const uint32_t ka = smem_u32(kt + hh * Cfg::TILE), va = smem_u32(vt + hh * Cfg::TILE);
+            const uint32_t sb = smem_u32(dst + hh * Cfg::ST);
+            const uint32_t dvc = tmem + hh * 2 * D, dkc = dvc + D;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              mma_bf16(dvc, smem_desc(ka + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
+                       smem_desc(sb + ks * 2 * Cfg::SBO, Cfg::ST, Cfg::SBO, Cfg::LAYOUT), idd, ks > 0 ? 1u : 0u);
+              mma_bf16(dkc, smem_desc(va + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT),
+                       smem_desc(sb + ks * 32, 16, Cfg::SBO, Cfg::LAYOUT), ide, ks > 0 ? 1u : 0u);
+            }
+            mma_bf16(dkc, smem_desc(smem_u32(ones), 16, 1024, 2),
+                     smem_desc(smem_u32(zb + hh * Cfg::ZB), 16, 1024, 2), ide, 1u);
+          }
+          mma_commit(bm);
+          ++n_m;
         }
-        bulk_commit_group();
+        if (!named_bar_and(kBkBar, kBkThreads, bwait(bm, c_m & 1u, abortf))) { ok = false; break; }
+        ++c_m;
+        tc_fence_after();
+        if (tid == 0 && last && nitem < n_items) {   // dS, dz consumed by this item's last MMAs
+          issue_ds(nitem);
+          ++n_s;
+        }
+
+        // ---- epilogue: dv into the v tiles, dk = dphi(k) * [k > 0] into the k tiles
+        for (int hh = wg; hh < HP; hh += 2) {
+          uint32_t a[D];
+          if constexpr (D == 64) {
+            tmem_ld_x32(lane_base + hh * 2 * D, *reinterpret_cast<uint32_t(*)[32]>(a));
+            tmem_ld_x32(lane_base + hh * 2 * D + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+          } else {
+            tmem_ld_x32(lane_base + hh * 2 * D, *reinterpret_cast<uint32_t(*)[32]>(a));
+          }
+          tmem_ld_wait();
+          uint8_t* vrow = vt + hh * Cfg::TILE + row * Cfg::ROWB;
+#pragma unroll
+          for (int u = 0; u < D / 8; ++u)
+            *reinterpret_cast<uint4*>(vrow + ((u ^ swz<D>(row)) * 16)) =
+                make_uint4(pack_bf16(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1])),
+                           pack_bf16(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3])),
+                           pack_bf16(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5])),
+                           pack_bf16(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7])));
+          if constexpr (D == 64) {
+            tmem_ld_x32(lane_base + hh * 2 * D + D, *reinterpret_cast<uint32_t(*)[32]>(a));
+            tmem_ld_x32(lane_base + hh * 2 * D + D + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+          } else {
+            tmem_ld_x32(lane_base + hh * 2 * D + D, *reinterpret_cast<uint32_t(*)[32]>(a));
+          }
+          tmem_ld_wait();
+          const uint8_t* mrow = mask + (hh * Cfg::C + row) * (D / 8);
+          uint8_t* krow = kt + hh * Cfg::TILE + row * Cfg::ROWB;
+#pragma unroll
+          for (int u = 0; u < D / 8; ++u) {
+            const uint32_t bits = mrow[u];
+            uint32_t ow[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float a0 = (bits >> (2 * k)) & 1u ? __uint_as_float(a[8 * u + 2 * k]) : 0.0f;
+              const float a1 = (bits >> (2 * k + 1)) & 1u ? __uint_as_float(a[8 * u + 2 * k + 1]) : 0.0f;
+              ow[k] = pack_bf16(a0, a1);
+            }
+            *reinterpret_cast<uint4*>(krow + ((u ^ swz<D>(row)) * 16)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(kBkBar, kBkThreads);
+        if (tid == 0) mbar_arrive(be + st);   // warp 8 stores the stage, then reloads it
       }
     }
-  }
-
-  if (tid == 0) {
-    bulk_wait_group0();
-    for (int st = 0; st < 2; ++st)
-      if (n_l[st] > c_l[st]) bdrain(bl + st, (n_l[st] - 1) & 1u);
-    if (n_s > c_s) bdrain(bs, (n_s - 1) & 1u);
-    if (n_m > c_m) bdrain(bm, (n_m - 1) & 1u);
+    if (tid == 0) {
+      if (n_s > c_s) bdrain(bs, (n_s - 1) & 1u);
+      if (n_m > c_m) bdrain(bm, (n_m - 1) & 1u);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1195,7 +1229,7 @@ int launch_tc_bwd_d(const Problem& p, const float* W, const BwdOperands& bo, voi
       return MHLA_ERR_CUDA;
     const int grid = static_cast<int>(std::min<int64_t>(n_items, sms));
     KernelTimer timer("tc_bwd_key", stream);
-    tc_bwd_key<D><<<grid, kBkThreads, Cfg::SMEM, stream>>>(tk, tv, tdk, tdv, tds, geo, G, n_items, p.phi_kind, p.eps,
+    tc_bwd_key<D><<<grid, kBkAll, Cfg::SMEM, stream>>>(tk, tv, tdk, tdv, tds, geo, G, n_items, p.phi_kind, p.eps,
                                                            zt);
     if (cudaGetLastError() != cudaSuccess) return MHLA_ERR_CUDA;
   }
